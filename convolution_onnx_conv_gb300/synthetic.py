@@ -1,0 +1,108 @@
+"""Seeded synthetic inputs, shared by the CUDA path's tests/benchmark and the
+oracle's tests.  This module draws random numbers and rounds them to the
+storage dtype; it holds none of the convolution's arithmetic.
+
+Recipe (the model files the pages benchmark are not available; only the layer
+shapes are used):
+
+* ``uniform``: x, W ~ U[-1, 1] rounded to bf16 (round-to-nearest-even),
+  bias ~ U[-0.1, 0.1] fp32.
+* ``normal``: x ~ N(0, 1) -> bf16; W He-normal (sigma^2 = 2 / fan_in) -> bf16;
+  BN gamma ~ U[0.5, 1.5], beta ~ N(0, 0.1), mean ~ N(0, 0.1), var ~ U[0.5, 1.5].
+* ``int``: x ~ U{-128..127}, W ~ U{-127..127} (int8), bias ~ U{-2^16..2^16}
+  (int32), per-channel requant multiplier M in [2^30, 2^31) and shift sh with
+  M / 2^sh ~ 127 / (4 sigma_acc) * U[0.5, 1.5], sigma_acc = 73.9^2 sqrt(C R S),
+  so that the int8 outputs span the range without saturating everywhere.
+
+All draws come from ``torch.Generator().manual_seed(seed)`` on the CPU.  The
+logical layout of every tensor is the ONNX one (NCHW / KCRS); callers choose
+the storage layout.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import torch
+
+from .workloads import ConvSpec
+
+
+def seed_for(config: int, layer_index: int) -> int:
+    return 1000 * config + layer_index
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def _uniform(g, shape, lo, hi):
+    return torch.rand(shape, generator=g, dtype=torch.float32) * (hi - lo) + lo
+
+
+def conv_inputs(spec: ConvSpec, seed: int) -> Dict[str, Optional[torch.Tensor]]:
+    """x (bf16, NCHW), w (bf16, KCRS), bias (fp32 or None), bn = (gamma, beta, mean, var)."""
+    g = _gen(seed)
+    Cg = spec.C // spec.group
+    xs = (spec.N, spec.C, spec.H, spec.W)
+    ws = (spec.K, Cg, spec.R, spec.S)
+    if spec.values == "uniform":
+        x = _uniform(g, xs, -1.0, 1.0)
+        w = _uniform(g, ws, -1.0, 1.0)
+    else:
+        x = torch.randn(xs, generator=g, dtype=torch.float32)
+        w = torch.randn(ws, generator=g, dtype=torch.float32) * math.sqrt(2.0 / (Cg * spec.R * spec.S))
+    out = {"x": x.to(torch.bfloat16), "w": w.to(torch.bfloat16), "bias": None, "bn": None}
+    if spec.has_bias:
+        out["bias"] = _uniform(g, (spec.K,), -0.1, 0.1)
+    if spec.has_bn:
+        gamma = _uniform(g, (spec.K,), 0.5, 1.5)
+        beta = torch.randn(spec.K, generator=g) * 0.1
+        mean = torch.randn(spec.K, generator=g) * 0.1
+        var = _uniform(g, (spec.K,), 0.5, 1.5)
+        out["bn"] = (gamma, beta, mean, var)
+    return out
+
+
+def int8_inputs(spec: ConvSpec, seed: int) -> Dict[str, torch.Tensor]:
+    """x int8, w int8 (NCHW / KCRS), bias int32[K], mult int32[K], shift int32[K]."""
+    g = _gen(seed)
+    Cg = spec.C // spec.group
+    x = torch.randint(-128, 128, (spec.N, spec.C, spec.H, spec.W), generator=g, dtype=torch.int8)
+    w = torch.randint(-127, 128, (spec.K, Cg, spec.R, spec.S), generator=g, dtype=torch.int8)
+    bias = torch.randint(-(1 << 16), (1 << 16) + 1, (spec.K,), generator=g, dtype=torch.int32)
+    sigma_acc = 73.9 * 73.9 * math.sqrt(Cg * spec.R * spec.S)
+    u = _uniform(g, (spec.K,), 0.5, 1.5).double()
+    mult = torch.empty(spec.K, dtype=torch.int32)
+    shift = torch.empty(spec.K, dtype=torch.int32)
+    for k in range(spec.K):
+        scale = 127.0 / (4.0 * sigma_acc) * float(u[k])
+        e = math.floor(math.log2(scale))           # scale = f * 2^e, f in [1, 2)
+        sh = 30 - e
+        m = int(round(scale * 2.0 ** sh))
+        if m >= (1 << 31):
+            m >>= 1
+            sh -= 1
+        mult[k] = m
+        shift[k] = sh
+    return {"x": x, "w": w, "bias": bias, "mult": mult, "shift": shift}
+
+
+def sample_points(spec: ConvSpec, count: int, seed: int) -> torch.Tensor:
+    """``count`` output coordinates (n, k, oh, ow), always including the corners
+    and edges of the output (where padding matters) and the last channel."""
+    ho, wo = spec.out_hw
+    g = _gen(seed)
+    pts = torch.stack([torch.randint(0, spec.N, (count,), generator=g),
+                       torch.randint(0, spec.K, (count,), generator=g),
+                       torch.randint(0, ho, (count,), generator=g),
+                       torch.randint(0, wo, (count,), generator=g)], dim=1)
+    fixed = []
+    for n in {0, spec.N - 1}:
+        for k in {0, spec.K - 1}:
+            for oh in {0, ho - 1}:
+                for ow in {0, wo - 1}:
+                    fixed.append((n, k, oh, ow))
+    return torch.cat([torch.tensor(fixed, dtype=torch.int64), pts.to(torch.int64)], dim=0)

@@ -1,0 +1,400 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself
+(brute force written differently, library routines on tiny inputs, closed
+forms, hand-worked values, invariants of the mathematics, golden fixtures).
+No GPU is needed."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------- independent routes
+
+def im2col_conv_numpy(x, w, bias, strides, pads, dilations, group, dtype=np.float64):
+    """im2col + matrix product per group (the page's CPU-executor method in the
+    "Kyanite" README, section "CPU executor"), written independently of the oracle."""
+    N, C, H, W = x.shape
+    K, Cg, R, S = w.shape
+    sh, sw = strides
+    pt, pl, pb, pr = pads
+    dh, dw = dilations
+    xp = np.zeros((N, C, H + pt + pb, W + pl + pr), dtype=dtype)
+    xp[:, :, pt:pt + H, pl:pl + W] = x
+    Ho = (H + pt + pb - dh * (R - 1) - 1) // sh + 1
+    Wo = (W + pl + pr - dw * (S - 1) - 1) // sw + 1
+    cols = np.empty((N, C, R, S, Ho, Wo), dtype=dtype)
+    for r in range(R):
+        for s in range(S):
+            cols[:, :, r, s] = xp[:, :, r * dh: r * dh + sh * (Ho - 1) + 1: sh,
+                                  s * dw: s * dw + sw * (Wo - 1) + 1: sw]
+    Kg = K // group
+    out = np.empty((N, K, Ho, Wo), dtype=dtype)
+    for g in range(group):
+        a = cols[:, g * Cg:(g + 1) * Cg].reshape(N, Cg * R * S, Ho * Wo)
+        b = w[g * Kg:(g + 1) * Kg].reshape(Kg, Cg * R * S).astype(dtype)
+        out[:, g * Kg:(g + 1) * Kg] = np.einsum("kj,njp->nkp", b, a).reshape(N, Kg, Ho, Wo)
+    if bias is not None:
+        out += np.asarray(bias, dtype=dtype).reshape(1, K, 1, 1)
+    return out
+
+
+def torch_conv_f64(x, w, bias, strides, pads, dilations, group):
+    pt, pl, pb, pr = pads
+    xt = torch.nn.functional.pad(torch.from_numpy(np.asarray(x, np.float64)), (pl, pr, pt, pb))
+    b = None if bias is None else torch.from_numpy(np.asarray(bias, np.float64))
+    return torch.nn.functional.conv2d(xt, torch.from_numpy(np.asarray(w, np.float64)), b,
+                                      stride=strides, dilation=dilations, groups=group).numpy()
+
+
+def random_cases(count, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < count:
+        N = int(rng.integers(1, 3))
+        R, S = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        st = (int(rng.integers(1, 4)), int(rng.integers(1, 4)))
+        dl = (int(rng.integers(1, 3)), int(rng.integers(1, 3)))
+        pads = tuple(int(v) for v in rng.integers(0, 3, size=4))
+        H, W = int(rng.integers(1, 8)), int(rng.integers(1, 8))
+        kind = int(rng.integers(0, 3))
+        if kind == 0:
+            group = 1
+            C, K = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        elif kind == 1:
+            group = 2
+            C, K = 2 * int(rng.integers(1, 5)), 2 * int(rng.integers(1, 5))
+        else:
+            C = int(rng.integers(1, 9))
+            group, K = C, C * int(rng.integers(1, 3))
+        Ho = (H + pads[0] + pads[2] - dl[0] * (R - 1) - 1) // st[0] + 1
+        Wo = (W + pads[1] + pads[3] - dl[1] * (S - 1) - 1) // st[1] + 1
+        if Ho < 1 or Wo < 1:
+            continue
+        cases.append((N, C, H, W, K, R, S, st, pads, dl, group))
+    return cases
+
+
+# ------------------------------------------------------------------ brute force
+
+@pytest.mark.parametrize("case", random_cases(80, 7))
+def test_conv_matches_im2col_and_torch(case):
+    N, C, H, W, K, R, S, st, pads, dl, group = case
+    rng = np.random.default_rng(hash(case) & 0xFFFF)
+    x = rng.standard_normal((N, C, H, W))
+    w = rng.standard_normal((K, C // group, R, S))
+    bias = rng.standard_normal(K) if rng.integers(0, 2) else None
+    z = oracle.conv2d(x, w, bias, st, pads, dl, group)
+    ref1 = im2col_conv_numpy(x, w, bias, st, pads, dl, group)
+    ref2 = torch_conv_f64(x, w, bias, st, pads, dl, group)
+    assert z.shape == ref1.shape == ref2.shape
+    scale = max(1.0, float(np.abs(ref1).max()))
+    assert np.abs(z - ref1).max() <= 1e-12 * scale
+    assert np.abs(z - ref2).max() <= 1e-12 * scale
+    # the point evaluator returns the same numbers
+    pts = np.array(list(itertools.product(range(N), range(K), range(z.shape[2]),
+                                          range(z.shape[3]))), dtype=np.int64)
+    zp = oracle.conv2d_points(x, w, bias, st, pads, dl, group, pts)
+    assert np.array_equal(zp, z.reshape(-1))
+
+
+@pytest.mark.parametrize("case", random_cases(40, 11))
+def test_int8_conv_matches_integer_im2col(case):
+    N, C, H, W, K, R, S, st, pads, dl, group = case
+    rng = np.random.default_rng(hash(case) & 0xFFFF)
+    x = rng.integers(-128, 128, (N, C, H, W)).astype(np.int8)
+    w = rng.integers(-128, 128, (K, C // group, R, S)).astype(np.int8)
+    acc = oracle.conv2d_s8(x, w, st, pads, dl, group)
+    ref = im2col_conv_numpy(x.astype(np.int64), w.astype(np.int64), None, st, pads, dl, group,
+                            dtype=np.int64)
+    assert acc.dtype == np.int64 and np.array_equal(acc, ref)
+    pts = np.array(list(itertools.product(range(N), range(K), range(acc.shape[2]),
+                                          range(acc.shape[3]))), dtype=np.int64)
+    assert np.array_equal(oracle.conv2d_s8_points(x, w, st, pads, dl, group, pts),
+                          acc.reshape(-1))
+
+
+def test_rejects_bad_arguments():
+    x = np.zeros((1, 4, 5, 5))
+    with pytest.raises(ValueError):
+        oracle.conv2d(x, np.zeros((2, 3, 3, 3)))               # C/group mismatch
+    with pytest.raises(ValueError):
+        oracle.conv2d(x, np.zeros((2, 4, 7, 7)))               # window larger than input
+    with pytest.raises(ValueError):
+        oracle.conv2d_points(x, np.zeros((2, 4, 3, 3)), None, (1, 1), (0, 0, 0, 0), (1, 1), 1,
+                             np.array([[0, 2, 0, 0]]))          # k out of range
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("C,H,W,R,S,st,pads,dl", [
+    (16, 9, 9, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1)),
+    (3, 12, 12, 7, 7, (2, 2), (3, 3, 3, 3), (1, 1)),
+    (5, 10, 8, 3, 2, (2, 1), (2, 0, 1, 1), (2, 1)),
+    (64, 6, 6, 1, 1, (1, 1), (0, 0, 0, 0), (1, 1)),
+])
+def test_all_ones_counts_valid_taps(C, H, W, R, S, st, pads, dl):
+    """All-ones x and W: each output is C times the number of taps that land
+    inside the image; C*R*S in the interior."""
+    K = 3
+    z = oracle.conv2d(np.ones((1, C, H, W)), np.ones((K, C, R, S)), None, st, pads, dl, 1)
+    Ho, Wo = z.shape[2:]
+    for oh in range(Ho):
+        nr = sum(0 <= oh * st[0] - pads[0] + r * dl[0] < H for r in range(R))
+        for ow in range(Wo):
+            ns = sum(0 <= ow * st[1] - pads[1] + s * dl[1] < W for s in range(S))
+            assert np.all(z[0, :, oh, ow] == C * nr * ns)
+    if R == 3 and H >= 3:
+        assert z[0, 0, 1, 1] == C * R * S
+
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split(None, 1)
+            out.setdefault(key, []).append(vals[0] if vals else "")
+    return out
+
+
+def test_golden_allones_matmul_64():
+    g = _read_golden("allones_1x1_c64.txt")
+    N, C, H, W, K, R, S, sh, sw, pt, pl, pb, pr, dh, dw, group = map(int, g["shape"][0].split())
+    z = oracle.conv2d(np.ones((N, C, H, W)), np.ones((K, C // group, R, S)), None, (sh, sw),
+                      (pt, pl, pb, pr), (dh, dw), group)
+    assert z.size == int(g["expected_count"][0])
+    assert np.all(z == float(g["expected_all"][0]))
+
+
+def test_golden_handworked():
+    g = _read_golden("handworked_2x2.txt")
+    x = np.array([float(v) for v in g["x"][0].split()]).reshape(1, 1, 3, 3)
+    w = np.array([float(v) for v in g["w"][0].split()]).reshape(1, 1, 2, 2)
+    assert len(g["case"]) == 5
+    for case in g["case"]:
+        attrs, shape, vals = case.split("|")
+        sh, sw, pt, pl, pb, pr, dh, dw = map(int, attrs.split())
+        ho, wo = map(int, shape.split())
+        want = np.array([float(v) for v in vals.split()]).reshape(1, 1, ho, wo)
+        z = oracle.conv2d(x, w, None, (sh, sw), (pt, pl, pb, pr), (dh, dw), 1)
+        assert np.array_equal(z, want), case
+        xi = x.astype(np.int8)
+        wi = w.astype(np.int8)
+        assert np.array_equal(oracle.conv2d_s8(xi, wi, (sh, sw), (pt, pl, pb, pr), (dh, dw), 1),
+                              want.astype(np.int64))
+
+
+def test_golden_relu6():
+    g = _read_golden("relu6_clamp.txt")
+    u = np.array([float(v) for v in g["u"][0].split()])
+    assert np.array_equal(oracle.activation(u, oracle.ACT_RELU),
+                          np.array([float(v) for v in g["relu"][0].split()]))
+    assert np.array_equal(oracle.activation(u, oracle.ACT_RELU6),
+                          np.array([float(v) for v in g["relu6"][0].split()]))
+    assert np.array_equal(oracle.activation(u, oracle.ACT_NONE), u)
+    assert np.array_equal(oracle.activation(u, oracle.ACT_CLIP, -1.0, 2.0),
+                          np.clip(u, -1.0, 2.0))
+
+
+def test_1x1_conv_is_matmul():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 24, 5, 7))
+    w = rng.standard_normal((40, 24, 1, 1))
+    z = oracle.conv2d(x, w)
+    for n in range(2):
+        ref = w[:, :, 0, 0] @ x[n].reshape(24, -1)
+        assert np.allclose(z[n].reshape(40, -1), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_identity_kernel_returns_input():
+    rng = np.random.default_rng(4)
+    C = 6
+    x = rng.standard_normal((2, C, 9, 5))
+    w = np.zeros((C, C, 3, 3))
+    for c in range(C):
+        w[c, c, 1, 1] = 1.0
+    assert np.array_equal(oracle.conv2d(x, w, None, (1, 1), (1, 1, 1, 1)), x)
+
+
+def test_depthwise_is_per_channel_conv():
+    rng = np.random.default_rng(5)
+    C = 5
+    x = rng.standard_normal((2, C, 8, 8))
+    w = rng.standard_normal((C, 1, 3, 3))
+    z = oracle.conv2d(x, w, None, (2, 2), (1, 1, 1, 1), (1, 1), C)
+    for c in range(C):
+        zc = oracle.conv2d(x[:, c:c + 1], w[c:c + 1], None, (2, 2), (1, 1, 1, 1), (1, 1), 1)
+        assert np.array_equal(z[:, c:c + 1], zc)
+
+
+def test_stride_is_subsampled_unit_stride():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((1, 4, 11, 10))
+    w = rng.standard_normal((3, 4, 3, 3))
+    z1 = oracle.conv2d(x, w, None, (1, 1), (1, 1, 1, 1))
+    z2 = oracle.conv2d(x, w, None, (2, 2), (1, 1, 1, 1))
+    assert np.array_equal(z2, z1[:, :, ::2, ::2])
+
+
+def test_dilation_is_zero_dilated_kernel():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((1, 3, 12, 12))
+    w = rng.standard_normal((4, 3, 3, 3))
+    wd = np.zeros((4, 3, 5, 5))
+    wd[:, :, ::2, ::2] = w
+    assert np.allclose(oracle.conv2d(x, w, None, (1, 1), (2, 2, 2, 2), (2, 2)),
+                       oracle.conv2d(x, wd, None, (1, 1), (2, 2, 2, 2), (1, 1)),
+                       rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ BN and auto_pad
+
+def test_bn_fold_invariant():
+    """conv(s*W) + (s*bias + t) == BN(conv(W) + bias), s = gamma/sqrt(var+eps),
+    t = beta - mean*s: the fold of the "tensorforge" page (W' = scale*W,
+    bias = shift), checked in unrounded float64."""
+    rng = np.random.default_rng(8)
+    K, C = 8, 5
+    x = rng.standard_normal((2, C, 7, 7))
+    w = rng.standard_normal((K, C, 3, 3))
+    bias = rng.standard_normal(K)
+    gamma, beta = rng.uniform(0.5, 1.5, K), rng.normal(0, 0.1, K)
+    mean, var = rng.normal(0, 0.1, K), rng.uniform(0.5, 1.5, K)
+    eps = 1e-5
+    s = gamma / np.sqrt(var + eps)
+    t = beta - mean * s
+    lhs = oracle.conv2d(x, w * s[:, None, None, None], s * bias + t, (1, 1), (1, 1, 1, 1))
+    rhs = oracle.batchnorm(oracle.conv2d(x, w, bias, (1, 1), (1, 1, 1, 1)), gamma, beta, mean,
+                           var, eps)
+    assert np.abs(lhs - rhs).max() <= 1e-12 * np.abs(rhs).max()
+    # identity BN: gamma=1, beta=0, mean=0, var=1-eps
+    z = oracle.conv2d(x, w, bias, (1, 1), (1, 1, 1, 1))
+    ident = oracle.batchnorm(z, np.ones(K), np.zeros(K), np.zeros(K), np.full(K, 1 - eps), eps)
+    assert np.abs(ident - z).max() <= 1e-15 * np.abs(z).max()
+    # point form agrees with the tensor form
+    chan = np.broadcast_to(np.arange(K).reshape(1, K, 1, 1), z.shape).reshape(-1)
+    assert np.array_equal(oracle.batchnorm(z.reshape(-1), gamma, beta, mean, var, eps, chan),
+                          oracle.batchnorm(z, gamma, beta, mean, var, eps).reshape(-1))
+
+
+def test_bn_hand_value():
+    # (z - mean)/sqrt(var + eps)*gamma + beta with var + eps = 4: (5 - 1)/2*3 + 0.5 = 6.5
+    out = oracle.batchnorm(np.full((1, 1, 1, 1), 5.0), [3.0], [0.5], [1.0], [4.0 - 1e-5], 1e-5)
+    assert abs(out.item() - 6.5) < 1e-12
+
+
+@pytest.mark.parametrize("n_in,k,s,d,upper,lower", [
+    (5, 3, 2, 1, (1, 1), (1, 1)),
+    (4, 3, 2, 1, (0, 1), (1, 0)),
+    (7, 1, 2, 1, (0, 0), (0, 0)),
+    (6, 3, 1, 2, (2, 2), (2, 2)),
+    (224, 7, 2, 1, (2, 3), (3, 2)),
+])
+def test_auto_pad(n_in, k, s, d, upper, lower):
+    pu = oracle.resolve_pads(n_in, n_in, k, k, (s, s), (d, d), auto_pad="SAME_UPPER")
+    pl = oracle.resolve_pads(n_in, n_in, k, k, (s, s), (d, d), auto_pad="SAME_LOWER")
+    assert (pu[0], pu[2]) == upper and (pl[0], pl[2]) == lower
+    for p in (pu, pl):
+        assert oracle.out_hw(n_in, n_in, k, k, (s, s), p, (d, d)) == (-(-n_in // s),) * 2
+    assert oracle.resolve_pads(n_in, n_in, k, k, (s, s), (d, d), (1, 2, 3, 4), "VALID") == (0,) * 4
+    assert oracle.resolve_pads(n_in, n_in, k, k, (s, s), (d, d), (1, 2, 3, 4)) == (1, 2, 3, 4)
+
+
+def test_same_upper_matches_torch_same():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 2, 6, 9))
+    w = rng.standard_normal((3, 2, 4, 2))
+    p = oracle.resolve_pads(6, 9, 4, 2, auto_pad="SAME_UPPER")
+    ref = torch.nn.functional.conv2d(torch.from_numpy(x), torch.from_numpy(w),
+                                     padding="same").numpy()
+    assert np.allclose(oracle.conv2d(x, w, None, (1, 1), p), ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------- requant
+
+def test_requant_hand_cases():
+    K = 1
+    b = np.zeros(K, np.int32)
+    m = np.full(K, 1 << 30, np.int32)       # M / 2^31 = 0.5
+    sh = np.full(K, 31, np.int32)
+    v = np.array([3, -3, 1, -1, 2, -2, 0])
+    ch = np.zeros_like(v)
+    # 1.5 -> 2, -1.5 -> -1, 0.5 -> 1, -0.5 -> 0 (ties toward +inf)
+    assert oracle.requant_s8(v, ch, b, m, sh).tolist() == [2, -1, 1, 0, 1, -1, 0]
+    # saturation at the int8 range
+    assert oracle.requant_s8(np.array([400, -400, 255, -257]), np.zeros(4, np.int64), b, m,
+                             sh).tolist() == [127, -128, 127, -128]
+    # ReLU clamps at the output zero point; bias is added before scaling
+    zp = 5
+    assert oracle.requant_s8(np.array([-20, 0, 20]), np.zeros(3, np.int64), b, m, sh, zp,
+                             relu=True).tolist() == [5, 5, 15]
+    assert oracle.requant_s8(np.array([-20, 0, 20]), np.zeros(3, np.int64), b, m, sh, zp,
+                             relu=False).tolist() == [-5, 5, 15]
+    assert oracle.requant_s8(np.array([1]), np.zeros(1, np.int64), np.array([9], np.int32), m,
+                             sh).tolist() == [5]
+    # per-channel parameters select by channel
+    acc = np.arange(2 * 3 * 2 * 2, dtype=np.int64).reshape(2, 3, 2, 2) * 10
+    mm = np.array([1 << 30, 1 << 29, 3 << 28], np.int32)
+    ss = np.full(3, 31, np.int32)
+    out = oracle.requant_s8(acc, None, np.zeros(3, np.int32), mm, ss)
+    for k in range(3):
+        ref = oracle.requant_s8(acc[:, k], np.zeros_like(acc[:, k]), np.zeros(1, np.int32),
+                                mm[k:k + 1], ss[k:k + 1])
+        assert np.array_equal(out[:, k], ref)
+
+
+def test_requant_matches_exact_rational_rounding():
+    """Python integers: round-half-up of v*M/2^sh is floor((2vM + 2^sh) / 2^(sh+1))."""
+    rng = np.random.default_rng(10)
+    K = 64
+    mult = rng.integers(1 << 30, (1 << 31) - 1, K).astype(np.int32)
+    shift = rng.integers(20, 50, K).astype(np.int32)
+    bias = rng.integers(-(1 << 16), 1 << 16, K).astype(np.int32)
+    acc = rng.integers(-(1 << 27), 1 << 27, 5000)
+    chan = rng.integers(0, K, 5000)
+    for zp, relu in ((0, True), (-7, False), (12, True)):
+        out = oracle.requant_s8(acc, chan, bias, mult, shift, zp, relu)
+        for a, k, o in zip(acc.tolist(), chan.tolist(), out.tolist()):
+            v = a + int(bias[k])
+            M, s = int(mult[k]), int(shift[k])
+            q = (2 * v * M + (1 << s)) // (1 << (s + 1)) + zp
+            lo = max(zp, -128) if relu else -128
+            assert o == min(max(q, lo), 127)
+    with pytest.raises(ValueError):
+        oracle.requant_s8(np.array([1]), np.zeros(1, np.int64), np.zeros(1, np.int32),
+                          np.zeros(1, np.int32), np.full(1, 31, np.int32))
+
+
+# ----------------------------------------------------------- tolerance sanity
+
+def test_fp32_accumulation_meets_tolerance():
+    """A plain float32 running sum over the largest reduction of the workloads
+    (C=512, 3x3: 4608 terms) stays inside |d| <= 1e-3 + 1e-3|ref| of the float64
+    result, so the tolerance is attainable by fp32 accumulation."""
+    g = torch.Generator().manual_seed(11)
+    C, K = 512, 8
+    x = torch.randn(1, C, 7, 7, generator=g).to(torch.bfloat16).double().numpy()
+    w = (torch.randn(K, C, 3, 3, generator=g) * math.sqrt(2.0 / (C * 9))
+         ).to(torch.bfloat16).double().numpy()
+    ref = oracle.conv2d(x, w, None, (1, 1), (1, 1, 1, 1))
+    f32 = oracle.conv2d_f32acc(x, w, None, (1, 1), (1, 1, 1, 1))
+    ok, worst, _ = oracle.tolerance_ok(f32, ref)
+    assert ok and worst < 0.1, worst
+
+
+def test_tolerance_helper_flags_a_planted_error():
+    ref = np.linspace(-3, 3, 101)
+    y = ref.copy()
+    assert oracle.tolerance_ok(y, ref)[0]
+    y[17] += 2e-3 + 1e-3 * abs(ref[17])
+    ok, worst, idx = oracle.tolerance_ok(y, ref)
+    assert not ok and idx == 17 and worst > 1.0
