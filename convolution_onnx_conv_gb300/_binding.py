@@ -1,0 +1,294 @@
+"""ctypes binding of ``libconvfused.so`` (argument marshalling only).
+
+The Python names are the C names; every compute step runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from . import _build
+
+# --- enums (mirror include/conv_fused.h)
+CONVF_OK, CONVF_ERR_INVALID_ARG, CONVF_ERR_UNSUPPORTED, CONVF_ERR_OOM, CONVF_ERR_CUDA, \
+    CONVF_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+CONVF_BF16, CONVF_S8 = 0, 1
+CONVF_NCHW, CONVF_NHWC = 0, 1
+CONVF_ACT_NONE, CONVF_ACT_RELU, CONVF_ACT_RELU6, CONVF_ACT_CLIP = 0, 1, 2, 3
+CONVF_AUTO_PAD_NOTSET, CONVF_AUTO_PAD_SAME_UPPER, CONVF_AUTO_PAD_SAME_LOWER, \
+    CONVF_AUTO_PAD_VALID = 0, 1, 2, 3
+CONVF_VARIANT_AUTO, CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_DEPTHWISE, \
+    CONVF_VARIANT_INT8, CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 0, 1, 2, 3, 4, 5
+VARIANT_NAMES = {0: "auto", 1: "implicit_gemm_im2col", 2: "gemm_1x1", 3: "depthwise",
+                 4: "int8_mma", 5: "implicit_gemm_gather"}
+AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
+
+EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale_shift",
+            "conv_fused_plan", "conv_fused_pack_weights", "conv_fused_create", "conv_fused_run",
+            "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
+            "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
+            "conv_fused_watchdog_selftest"]
+
+
+class ConvDesc(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("C", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
+                ("K", ctypes.c_int), ("R", ctypes.c_int), ("S", ctypes.c_int),
+                ("stride", ctypes.c_int * 2), ("dilation", ctypes.c_int * 2),
+                ("pads", ctypes.c_int * 4), ("auto_pad", ctypes.c_int), ("group", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("x_layout", ctypes.c_int), ("y_layout", ctypes.c_int),
+                ("act", ctypes.c_int), ("clip_lo", ctypes.c_float), ("clip_hi", ctypes.c_float),
+                ("variant", ctypes.c_int)]
+
+
+def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1,
+              dtype=CONVF_BF16, act=CONVF_ACT_NONE, clip=(0.0, 6.0), auto_pad="NOTSET",
+              variant=CONVF_VARIANT_AUTO, layout=CONVF_NHWC) -> ConvDesc:
+    d = ConvDesc()
+    d.N, d.C, d.H, d.W, d.K, d.R, d.S = N, C, H, W, K, R, S
+    d.stride[:] = list(stride)
+    d.dilation[:] = list(dilation)
+    d.pads[:] = list(pads)
+    d.auto_pad = AUTO_PAD[auto_pad] if isinstance(auto_pad, str) else int(auto_pad)
+    d.group = group
+    d.dtype = dtype
+    d.x_layout = d.y_layout = layout
+    d.act = act
+    d.clip_lo, d.clip_hi = float(clip[0]), float(clip[1])
+    d.variant = variant
+    return d
+
+
+class ConvFusedError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False):
+    """Load the CUDA library (building it first only when asked)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libconvfused.so is not built ({_build.LIB}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    P = ctypes.POINTER
+    dptr = P(ConvDesc)
+    vp = ctypes.c_void_p
+    lib.conv_fused_output_shape.argtypes = [dptr, P(ctypes.c_int)]
+    lib.conv_fused_resolve_pads.argtypes = [dptr, P(ctypes.c_int)]
+    lib.conv_bn_scale_shift.argtypes = [ctypes.c_int] + [P(ctypes.c_float)] * 4 + [ctypes.c_float] + \
+        [P(ctypes.c_float)] * 2
+    lib.conv_fused_plan.argtypes = [dptr, ctypes.c_int, P(ctypes.c_int), P(ctypes.c_int), P(ctypes.c_int)]
+    lib.conv_fused_pack_weights.argtypes = [dptr, ctypes.c_int, vp, vp, ctypes.c_size_t]
+    lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
+    lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
+    lib.conv_fused_status.argtypes = [vp]
+    lib.conv_fused_clear_status.argtypes = [vp]
+    lib.conv_fused_destroy.argtypes = [vp]
+    lib.conv_fused_destroy.restype = None
+    lib.conv_fused_variant.argtypes = [vp]
+    lib.conv_fused_describe.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.conv_fused_last_error.argtypes = []
+    lib.conv_fused_last_error.restype = ctypes.c_char_p
+    lib.conv_fused_watchdog_selftest.argtypes = [vp, ctypes.c_longlong, vp]
+    for name in EXPORTED:
+        if name not in ("conv_fused_destroy", "conv_fused_last_error"):
+            getattr(lib, name).restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != CONVF_OK:
+        raise ConvFusedError(status, conv_fused_last_error())
+
+
+def _addr(a) -> Optional[int]:
+    """Host address of a numpy array / CPU tensor, device address of a CUDA tensor, or an int."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        return a.data_ptr()
+    return a.ctypes.data
+
+
+# --------------------------------------------------------------------------- C entry points
+
+def conv_fused_last_error() -> str:
+    return load_library().conv_fused_last_error().decode()
+
+
+def conv_fused_output_shape(desc: ConvDesc):
+    out = (ctypes.c_int * 4)()
+    _check(load_library().conv_fused_output_shape(ctypes.byref(desc), out))
+    return tuple(out)
+
+
+def conv_fused_resolve_pads(desc: ConvDesc):
+    out = (ctypes.c_int * 4)()
+    _check(load_library().conv_fused_resolve_pads(ctypes.byref(desc), out))
+    return tuple(out)
+
+
+def conv_bn_scale_shift(gamma, beta, mean, var, eps: float = 1e-5):
+    """Returns (scale, shift) as float32 numpy arrays."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.float32)) for a in (gamma, beta, mean, var)]
+    K = arrs[0].shape[0]
+    scale = np.empty(K, np.float32)
+    shift = np.empty(K, np.float32)
+    fp = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+    _check(load_library().conv_bn_scale_shift(K, *[fp(a) for a in arrs], float(eps), fp(scale), fp(shift)))
+    return scale, shift
+
+
+def conv_fused_plan(desc: ConvDesc, num_sms: int = 152):
+    v, bn, kt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load_library().conv_fused_plan(ctypes.byref(desc), num_sms, ctypes.byref(v), ctypes.byref(bn),
+                                          ctypes.byref(kt)))
+    return v.value, bn.value, kt.value
+
+
+def conv_fused_pack_weights(desc: ConvDesc, variant: int, W_bits, out):
+    _check(load_library().conv_fused_pack_weights(ctypes.byref(desc), variant, _addr(W_bits), _addr(out),
+                                                  out.size if hasattr(out, "size") and not callable(out.size)
+                                                  else out.numel()))
+
+
+def conv_fused_create(desc: ConvDesc, W, bias=None, bn_scale=None, bn_shift=None, requant_mult=None,
+                      requant_shift=None, out_zero_point: int = 0) -> int:
+    """Host arrays (numpy or CPU tensors, contiguous) in, handle (int) out."""
+    h = ctypes.c_void_p()
+    _check(load_library().conv_fused_create(ctypes.byref(desc), _addr(W), _addr(bias), _addr(bn_scale),
+                                            _addr(bn_shift), _addr(requant_mult), _addr(requant_shift),
+                                            int(out_zero_point), ctypes.byref(h)))
+    return h.value
+
+
+def conv_fused_run(handle: int, x, y, stream=None):
+    """x, y: device pointers (ints) or CUDA tensors; stream: cudaStream_t int, torch stream or None."""
+    s = stream
+    if s is not None and hasattr(s, "cuda_stream"):
+        s = s.cuda_stream
+    _check(load_library().conv_fused_run(handle, _addr(x), _addr(y), s))
+
+
+def conv_fused_status(handle: int) -> int:
+    return load_library().conv_fused_status(handle)
+
+
+def conv_fused_clear_status(handle: int):
+    _check(load_library().conv_fused_clear_status(handle))
+
+
+def conv_fused_destroy(handle: int):
+    load_library().conv_fused_destroy(handle)
+
+
+def conv_fused_variant(handle: int) -> int:
+    v = load_library().conv_fused_variant(handle)
+    if v < 0:
+        _check(v)
+    return v
+
+
+def conv_fused_describe(handle: int) -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(load_library().conv_fused_describe(handle, buf, 512))
+    return buf.value.decode()
+
+
+def conv_fused_watchdog_selftest(status_dev, budget_cycles: int, stream=None):
+    s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
+    _check(load_library().conv_fused_watchdog_selftest(_addr(status_dev), int(budget_cycles), s))
+
+
+# --------------------------------------------------------------------------- torch convenience
+
+class FusedConv:
+    """One prepared conv node over torch tensors.
+
+    ``w`` (bf16 KCRS or int8), ``bias`` and the BN affine are CPU tensors; they are copied
+    to the device once here.  Calling the object runs the kernel on the current torch stream
+    with ``x`` a CUDA tensor in channels-last storage (logical NCHW) and returns y (fp32 or
+    int8, channels-last).
+    """
+
+    def __init__(self, N, C, H, W, K, R, S, w, bias=None, bn_scale=None, bn_shift=None, stride=(1, 1),
+                 pads=(0, 0, 0, 0), dilation=(1, 1), group=1, act=CONVF_ACT_NONE, clip=(0.0, 6.0),
+                 auto_pad="NOTSET", variant=CONVF_VARIANT_AUTO, requant_mult=None, requant_shift=None,
+                 out_zero_point=0):
+        import torch
+        s8 = w.dtype == torch.int8
+        self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group,
+                              CONVF_S8 if s8 else CONVF_BF16, act, clip, auto_pad, variant)
+        wc = w.contiguous().cpu()
+        wbits = wc if s8 else wc.view(torch.int16)
+        keep = [wbits]
+
+        def host(t, dt):
+            if t is None:
+                return None
+            t = torch.as_tensor(t).to(dt).contiguous().cpu()
+            keep.append(t)
+            return t
+
+        self.handle = conv_fused_create(self.desc, wbits, host(bias, torch.int32 if s8 else torch.float32),
+                                        host(bn_scale, torch.float32), host(bn_shift, torch.float32),
+                                        host(requant_mult, torch.int32), host(requant_shift, torch.int32),
+                                        out_zero_point)
+        self.out_shape = conv_fused_output_shape(self.desc)
+        self.s8 = s8
+
+    @property
+    def variant(self) -> int:
+        return conv_fused_variant(self.handle)
+
+    def describe(self) -> str:
+        return conv_fused_describe(self.handle)
+
+    def new_output(self):
+        import torch
+        N, K, Ho, Wo = self.out_shape
+        return torch.empty((N, Ho, Wo, K), dtype=torch.int8 if self.s8 else torch.float32,
+                           device="cuda").permute(0, 3, 1, 2)
+
+    def __call__(self, x, y=None, stream=None):
+        import torch
+        if not x.is_cuda:
+            raise ValueError("x must be a CUDA tensor")
+        if not x.is_contiguous(memory_format=torch.channels_last) and x.numel() > 0:
+            raise ValueError("x must use channels-last storage")
+        if y is None:
+            y = self.new_output()
+        conv_fused_run(self.handle, x.data_ptr(), y.data_ptr(),
+                       stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+        return y
+
+    def status(self) -> int:
+        return conv_fused_status(self.handle)
+
+    def close(self):
+        if self.handle:
+            conv_fused_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

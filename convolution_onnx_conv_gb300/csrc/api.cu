@@ -1,0 +1,781 @@
+// C-ABI of the fused ONNX Conv library: argument validation (refuse, never guess), ONNX
+// attribute normalisation, BN fold, weight prepack, the shape-keyed variant selector, tensor
+// map encoding and kernel dispatch.  Everything per-call is prepared in create; run only
+// (re)encodes the two activation/output tensor maps when the caller's pointers change.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/conv_fused.h"
+#include "convf_internal.h"
+
+namespace convf {
+// defined once per tile width in tc_conv_inst.cu
+cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
+                                const CUtensorMap&, int, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
+                                const CUtensorMap&, int, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
+                                 const CUtensorMap&, int, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
+                                 const CUtensorMap&, int, bool, cudaStream_t);
+}  // namespace convf
+
+using namespace convf;
+
+namespace {
+
+constexpr uint32_t kMagic = 0xC0F5ED01u;
+constexpr uint32_t kDeadMagic = 0xDEADC0F5u;
+
+thread_local std::string g_last_error;
+
+convf_status fail(convf_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+convf_status ok() {
+  g_last_error.clear();
+  return CONVF_OK;
+}
+
+// ------------------------------------------------------------------ attribute normalisation
+struct Shape {
+  int N, C, H, W, K, R, S, Cg;
+  int sh, sw, dh, dw;
+  int pt, pl, pb, pr;
+  int Ho, Wo;
+  long long M;  // N*Ho*Wo
+};
+
+long long extent(long long in, long long k, long long st, long long pb, long long pe, long long d) {
+  const long long span = in + pb + pe - d * (k - 1) - 1;
+  return span < 0 ? 0 : span / st + 1;
+}
+
+convf_status resolve(const convf_desc* d, Shape* s) {
+  if (!d) return fail(CONVF_ERR_INVALID_ARG, "desc is NULL");
+  if (d->N < 0) return fail(CONVF_ERR_INVALID_ARG, "N=%d must be >= 0", d->N);
+  const int dims[6] = {d->C, d->H, d->W, d->K, d->R, d->S};
+  const char* names[6] = {"C", "H", "W", "K", "R", "S"};
+  for (int i = 0; i < 6; ++i)
+    if (dims[i] < 1) return fail(CONVF_ERR_INVALID_ARG, "%s=%d must be >= 1", names[i], dims[i]);
+  if (d->stride[0] < 1 || d->stride[1] < 1)
+    return fail(CONVF_ERR_INVALID_ARG, "strides (%d,%d) must be >= 1", d->stride[0], d->stride[1]);
+  if (d->dilation[0] < 1 || d->dilation[1] < 1)
+    return fail(CONVF_ERR_INVALID_ARG, "dilations (%d,%d) must be >= 1", d->dilation[0],
+                d->dilation[1]);
+  if (d->group < 1) return fail(CONVF_ERR_INVALID_ARG, "group=%d must be >= 1", d->group);
+  if (d->C % d->group != 0 || d->K % d->group != 0)
+    return fail(CONVF_ERR_INVALID_ARG, "group=%d must divide C=%d and K=%d", d->group, d->C, d->K);
+  s->N = d->N; s->C = d->C; s->H = d->H; s->W = d->W; s->K = d->K; s->R = d->R; s->S = d->S;
+  s->Cg = d->C / d->group;
+  s->sh = d->stride[0]; s->sw = d->stride[1]; s->dh = d->dilation[0]; s->dw = d->dilation[1];
+  switch (d->auto_pad) {
+    case CONVF_AUTO_PAD_NOTSET:
+      for (int i = 0; i < 4; ++i)
+        if (d->pads[i] < 0) return fail(CONVF_ERR_INVALID_ARG, "pads[%d]=%d must be >= 0", i, d->pads[i]);
+      s->pt = d->pads[0]; s->pl = d->pads[1]; s->pb = d->pads[2]; s->pr = d->pads[3];
+      break;
+    case CONVF_AUTO_PAD_VALID:
+      s->pt = s->pl = s->pb = s->pr = 0;
+      break;
+    case CONVF_AUTO_PAD_SAME_UPPER:
+    case CONVF_AUTO_PAD_SAME_LOWER: {
+      const int in[2] = {d->H, d->W}, k[2] = {d->R, d->S}, st[2] = {s->sh, s->sw}, dl[2] = {s->dh, s->dw};
+      int beg[2], end[2];
+      for (int a = 0; a < 2; ++a) {
+        const long long out = (in[a] + st[a] - 1) / st[a];
+        long long total = (out - 1) * st[a] + (long long)(k[a] - 1) * dl[a] + 1 - in[a];
+        if (total < 0) total = 0;
+        const long long small = total / 2;
+        beg[a] = (int)(d->auto_pad == CONVF_AUTO_PAD_SAME_UPPER ? small : total - small);
+        end[a] = (int)(total - beg[a]);
+      }
+      s->pt = beg[0]; s->pl = beg[1]; s->pb = end[0]; s->pr = end[1];
+      break;
+    }
+    default:
+      return fail(CONVF_ERR_INVALID_ARG, "auto_pad=%d is not one of NOTSET/SAME_UPPER/SAME_LOWER/VALID",
+                  d->auto_pad);
+  }
+  const long long Ho = extent(s->H, s->R, s->sh, s->pt, s->pb, s->dh);
+  const long long Wo = extent(s->W, s->S, s->sw, s->pl, s->pr, s->dw);
+  if (Ho < 1 || Wo < 1)
+    return fail(CONVF_ERR_INVALID_ARG, "the %dx%d window (dilation %d,%d) does not fit the padded %dx%d input",
+                s->R, s->S, s->dh, s->dw, s->H + s->pt + s->pb, s->W + s->pl + s->pr);
+  s->Ho = (int)Ho;
+  s->Wo = (int)Wo;
+  s->M = (long long)s->N * Ho * Wo;
+  const long long lim = 0x7FFFFFFFLL;
+  if ((long long)s->N * s->H * s->W * s->C > lim || s->M * s->K > lim ||
+      (long long)s->K * s->Cg * s->R * s->S > lim)
+    return fail(CONVF_ERR_UNSUPPORTED, "tensor sizes exceed the 2^31-element indexing limit");
+  return CONVF_OK;
+}
+
+convf_status check_misc(const convf_desc* d) {
+  if (d->dtype != CONVF_BF16 && d->dtype != CONVF_S8)
+    return fail(CONVF_ERR_INVALID_ARG, "dtype=%d is not CONVF_BF16 or CONVF_S8", d->dtype);
+  if ((d->x_layout != CONVF_NCHW && d->x_layout != CONVF_NHWC) ||
+      (d->y_layout != CONVF_NCHW && d->y_layout != CONVF_NHWC))
+    return fail(CONVF_ERR_INVALID_ARG, "layouts (%d,%d) must be CONVF_NCHW or CONVF_NHWC", d->x_layout,
+                d->y_layout);
+  if (d->x_layout != CONVF_NHWC || d->y_layout != CONVF_NHWC)
+    return fail(CONVF_ERR_UNSUPPORTED, "only channels-last (CONVF_NHWC) storage is served");
+  if (d->act < CONVF_ACT_NONE || d->act > CONVF_ACT_CLIP)
+    return fail(CONVF_ERR_INVALID_ARG, "act=%d is not a convf_act", d->act);
+  if (d->act == CONVF_ACT_CLIP && !(d->clip_lo <= d->clip_hi))
+    return fail(CONVF_ERR_INVALID_ARG, "clip bounds (%g, %g) need lo <= hi", d->clip_lo, d->clip_hi);
+  if (d->dtype == CONVF_S8 && (d->act == CONVF_ACT_RELU6 || d->act == CONVF_ACT_CLIP))
+    return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
+  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
+    return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
+  return CONVF_OK;
+}
+
+// ------------------------------------------------------------------ variant selector
+// Why a shape cannot use a variant ("" = it can).
+std::string cannot(int v, const convf_desc* d, const Shape& s) {
+  const bool bf = d->dtype == CONVF_BF16;
+  char b[256];
+  switch (v) {
+    case CONVF_VARIANT_DEPTHWISE:
+      if (!bf) return "depthwise serves bf16 only";
+      if (!(d->group == s.C && s.K == s.C)) return "depthwise needs group == C == K";
+      if (s.C % 8) return "depthwise needs C % 8 == 0 (16-byte channel vectors)";
+      return "";
+    case CONVF_VARIANT_GEMM_1X1:
+      if (!bf) return "1x1 GEMM serves bf16 only";
+      if (d->group != 1) return "1x1 GEMM needs group == 1";
+      if (s.R != 1 || s.S != 1 || s.sh != 1 || s.sw != 1 || s.pt || s.pl || s.pb || s.pr)
+        return "1x1 GEMM needs a 1x1 filter, unit strides and no padding";
+      if (s.C % 8) return "1x1 GEMM needs C % 8 == 0 (16-byte TMA row stride)";
+      if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
+      return "";
+    case CONVF_VARIANT_IMPLICIT_GEMM:
+      if (!bf) return "implicit GEMM serves bf16 only";
+      if (d->group != 1) return "implicit GEMM needs group == 1 (grouped conv other than depthwise is refused)";
+      if (s.C % 8) return "TMA im2col needs C % 8 == 0 (use the gather variant)";
+      if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
+      if (s.sh > 8 || s.sw > 8) return "TMA im2col traversal strides are limited to 8";
+      if (s.pt > 128 || s.pl > 128) return "TMA im2col box corners are limited to [-128, 127]";
+      if ((long long)(s.R - 1) * s.dh - s.pb > 128 || (long long)(s.S - 1) * s.dw - s.pr > 128 ||
+          s.pb - (long long)(s.R - 1) * s.dh > 127 || s.pr - (long long)(s.S - 1) * s.dw > 127)
+        return "TMA im2col box corners are limited to [-128, 127]";
+      if ((long long)(s.R - 1) * s.dh > 65535 || (long long)(s.S - 1) * s.dw > 65535)
+        return "filter offsets exceed 16 bits";
+      return "";
+    case CONVF_VARIANT_IMPLICIT_GEMM_GATHER:
+      if (!bf) return "implicit GEMM serves bf16 only";
+      if (d->group != 1) return "implicit GEMM needs group == 1";
+      if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
+      return "";
+    case CONVF_VARIANT_INT8:
+      if (bf) return "the int8 kernel serves CONVF_S8 only";
+      if (d->group != 1) return "the int8 kernel needs group == 1";
+      if (s.C % 64) return "the int8 kernel needs C % 64 == 0";
+      if (s.K % 16) return "the int8 kernel needs K % 16 == 0";
+      return "";
+  }
+  snprintf(b, sizeof b, "unknown variant %d", v);
+  return b;
+}
+
+convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
+  if (d->variant != CONVF_VARIANT_AUTO) {
+    std::string why = cannot(d->variant, d, s);
+    if (!why.empty()) return fail(CONVF_ERR_UNSUPPORTED, "forced variant %d refused: %s", d->variant, why.c_str());
+    *out = d->variant;
+    return CONVF_OK;
+  }
+  const int order_bf16[4] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM,
+                             CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
+  if (d->dtype == CONVF_S8) {
+    std::string why = cannot(CONVF_VARIANT_INT8, d, s);
+    if (!why.empty()) return fail(CONVF_ERR_UNSUPPORTED, "int8 conv refused: %s", why.c_str());
+    *out = CONVF_VARIANT_INT8;
+    return CONVF_OK;
+  }
+  std::string reasons;
+  for (int v : order_bf16) {
+    std::string why = cannot(v, d, s);
+    if (why.empty()) {
+      *out = v;
+      return CONVF_OK;
+    }
+    reasons += (reasons.empty() ? "" : "; ") + why;
+  }
+  return fail(CONVF_ERR_UNSUPPORTED, "no kernel serves this conv: %s", reasons.c_str());
+}
+
+// Tile width for the tcgen05 kernels: minimise waves x per-tile time, where a K16 step of a
+// 128 x bn MMA costs max(bn/2, (A + B bytes)/128) cycles (tensor rate vs shared-memory reads).
+int pick_bn(long long M, int K, int num_sms) {
+  const long long mblocks = (M + 127) / 128;
+  int best = 256;
+  double best_cost = 1e300;
+  for (int bn : {256, 128, 64, 32}) {
+    if (bn > 32 && bn / 2 >= K) continue;  // no point in a tile twice as wide as K
+    const long long tiles = mblocks * ((K + bn - 1) / bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const double step = std::max(bn / 2.0, (4096.0 + bn * 32.0) / 128.0);
+    const double cost = (double)waves * step;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// ------------------------------------------------------------------ driver entry points
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode_tiled = nullptr;
+EncodeIm2colFn g_encode_im2col = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encoders() {
+  std::call_once(g_encode_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<EncodeTiledFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(f);
+  });
+  return g_encode_tiled && g_encode_im2col;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+// ====================================================================== handle
+struct convf_handle {
+  uint32_t magic;
+  convf_desc desc;
+  Shape s;
+  int variant;
+  int device;
+  int num_sms;
+  // one device allocation carved into the arrays below
+  void* dev;
+  size_t dev_bytes;
+  uint16_t* w_bf16;
+  int8_t* w_s8;
+  float* taps;
+  float* scale;
+  float* bias;
+  int32_t* qbias;
+  int32_t* qmult;
+  int32_t* qshift;
+  int* status;
+  int32_t zp;
+  float lo, hi;
+  // tcgen05 configuration
+  int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks;
+  CUtensorMap tmB;
+  CUtensorMap tmA, tmY;
+  const void* map_x;
+  const void* map_y;
+};
+
+namespace {
+
+convf_status check_handle(const convf_handle* h) {
+  if (!h) return fail(CONVF_ERR_INVALID_ARG, "handle is NULL");
+  if (h->magic == kDeadMagic) return fail(CONVF_ERR_INVALID_ARG, "handle was destroyed");
+  if (h->magic != kMagic) return fail(CONVF_ERR_INVALID_ARG, "not a convf handle");
+  return CONVF_OK;
+}
+
+void act_bounds(const convf_desc* d, float* lo, float* hi) {
+  switch (d->act) {
+    case CONVF_ACT_RELU: *lo = 0.f; *hi = INFINITY; break;
+    case CONVF_ACT_RELU6: *lo = 0.f; *hi = 6.f; break;
+    case CONVF_ACT_CLIP: *lo = d->clip_lo; *hi = d->clip_hi; break;
+    default: *lo = -INFINITY; *hi = INFINITY; break;
+  }
+}
+
+// Prepacked weight row length (elements) for the tcgen05 variants.
+void tc_layout(int variant, const Shape& s, int* a_mode, int* cblocks, int* ktot) {
+  if (variant == CONVF_VARIANT_GEMM_1X1) {
+    *a_mode = kA2D;
+    *cblocks = (s.C + 63) / 64;
+    *ktot = *cblocks * 64;
+  } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM) {
+    *a_mode = kAIm2col;
+    *cblocks = (s.C + 63) / 64;
+    *ktot = s.R * s.S * *cblocks * 64;
+  } else {
+    *a_mode = kAGather;
+    *cblocks = 0;
+    *ktot = (int)align_up((size_t)s.R * s.S * s.C, 64);
+  }
+}
+
+// W[K][C][R][S] (bf16 bits) -> [K][ktot]: reduction index (tap, channel) with the channel
+// fastest; im2col mode pads every tap's channel run to a multiple of 64, the other modes pad
+// only the end of the row.
+void pack_bf16(const uint16_t* W, const Shape& s, int a_mode, int ktot, uint16_t* out) {
+  std::memset(out, 0, sizeof(uint16_t) * (size_t)s.K * ktot);
+  const int cpad = a_mode == kAIm2col ? (s.C + 63) / 64 * 64 : s.C;
+  for (int k = 0; k < s.K; ++k)
+    for (int c = 0; c < s.C; ++c)
+      for (int r = 0; r < s.R; ++r)
+        for (int q = 0; q < s.S; ++q)
+          out[(size_t)k * ktot + (size_t)(r * s.S + q) * cpad + c] =
+              W[(((size_t)k * s.C + c) * s.R + r) * s.S + q];
+}
+
+float bf16_to_f32(uint16_t v) {
+  uint32_t u = (uint32_t)v << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* conv_fused_last_error(void) { return g_last_error.c_str(); }
+
+convf_status conv_fused_resolve_pads(const convf_desc* desc, int pads_out[4]) {
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if (!pads_out) return fail(CONVF_ERR_INVALID_ARG, "pads_out is NULL");
+  pads_out[0] = s.pt; pads_out[1] = s.pl; pads_out[2] = s.pb; pads_out[3] = s.pr;
+  return ok();
+}
+
+convf_status conv_fused_output_shape(const convf_desc* desc, int out_nchw[4]) {
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if (!out_nchw) return fail(CONVF_ERR_INVALID_ARG, "out_nchw is NULL");
+  out_nchw[0] = s.N; out_nchw[1] = s.K; out_nchw[2] = s.Ho; out_nchw[3] = s.Wo;
+  return ok();
+}
+
+convf_status conv_bn_scale_shift(int K, const float* gamma, const float* beta, const float* mean,
+                                 const float* var, float eps, float* scale, float* shift) {
+  if (K < 1) return fail(CONVF_ERR_INVALID_ARG, "K=%d must be >= 1", K);
+  if (!gamma || !beta || !mean || !var || !scale || !shift)
+    return fail(CONVF_ERR_INVALID_ARG, "a BN array is NULL");
+  if (!(eps > 0.f)) return fail(CONVF_ERR_INVALID_ARG, "eps=%g must be > 0", eps);
+  for (int k = 0; k < K; ++k) {
+    const double v = (double)var[k] + (double)eps;
+    if (!(v > 0.0)) return fail(CONVF_ERR_INVALID_ARG, "var[%d] + eps = %g is not positive", k, v);
+    const double sc = (double)gamma[k] / std::sqrt(v);
+    scale[k] = (float)sc;
+    shift[k] = (float)((double)beta[k] - (double)mean[k] * sc);
+  }
+  return ok();
+}
+
+// Host-only view of the selector: the variant and tcgen05 tile width create would choose for
+// `desc` on a GPU with `num_sms` SMs (no CUDA call).
+convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, int* tile_n, int* ktot) {
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if ((st = check_misc(desc)) != CONVF_OK) return st;
+  int v = 0;
+  if ((st = select_variant(desc, s, &v)) != CONVF_OK) return st;
+  if (variant) *variant = v;
+  int bn = 0, kt = 0;
+  if (v == CONVF_VARIANT_GEMM_1X1 || v == CONVF_VARIANT_IMPLICIT_GEMM || v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
+    int am, cb;
+    tc_layout(v, s, &am, &cb, &kt);
+    bn = pick_bn(s.M, s.K, num_sms > 0 ? num_sms : 1);
+  } else if (v == CONVF_VARIANT_INT8) {
+    kt = s.R * s.S * s.C;
+  }
+  if (tile_n) *tile_n = bn;
+  if (ktot) *ktot = kt;
+  return ok();
+}
+
+// Host-only prepack of bf16 weights for a tcgen05 variant ([K][ktot], see pack_bf16).
+convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const uint16_t* W, uint16_t* out,
+                                     size_t out_elems) {
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if (!W || !out) return fail(CONVF_ERR_INVALID_ARG, "W/out is NULL");
+  if (variant != CONVF_VARIANT_GEMM_1X1 && variant != CONVF_VARIANT_IMPLICIT_GEMM &&
+      variant != CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
+    return fail(CONVF_ERR_INVALID_ARG, "variant %d has no bf16 GEMM packing", variant);
+  if (desc->group != 1) return fail(CONVF_ERR_UNSUPPORTED, "GEMM packing needs group == 1");
+  int am, cb, kt;
+  tc_layout(variant, s, &am, &cb, &kt);
+  if (out_elems < (size_t)s.K * kt) return fail(CONVF_ERR_INVALID_ARG, "out holds %zu < %zu elements", out_elems,
+                                                (size_t)s.K * kt);
+  pack_bf16(W, s, am, kt, out);
+  return ok();
+}
+
+convf_status conv_fused_create(const convf_desc* desc, const void* W, const void* bias,
+                               const float* bn_scale, const float* bn_shift,
+                               const int32_t* requant_mult, const int32_t* requant_shift,
+                               int32_t out_zero_point, convf_handle** out) {
+  if (!out) return fail(CONVF_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if ((st = check_misc(desc)) != CONVF_OK) return st;
+  if (!W) return fail(CONVF_ERR_INVALID_ARG, "W is NULL");
+  const bool s8 = desc->dtype == CONVF_S8;
+  if (s8) {
+    if (bn_scale || bn_shift) return fail(CONVF_ERR_INVALID_ARG, "bn_scale/bn_shift must be NULL on the int8 path");
+    if (!requant_mult || !requant_shift) return fail(CONVF_ERR_INVALID_ARG, "requant_mult/requant_shift are required on the int8 path");
+    if (out_zero_point < -128 || out_zero_point > 127)
+      return fail(CONVF_ERR_INVALID_ARG, "out_zero_point=%d is outside int8", out_zero_point);
+    for (int k = 0; k < s.K; ++k) {
+      if (requant_mult[k] <= 0) return fail(CONVF_ERR_INVALID_ARG, "requant_mult[%d]=%d must be > 0", k, requant_mult[k]);
+      if (requant_shift[k] < 1 || requant_shift[k] > 62)
+        return fail(CONVF_ERR_INVALID_ARG, "requant_shift[%d]=%d must be in 1..62", k, requant_shift[k]);
+    }
+  } else {
+    if ((bn_scale == nullptr) != (bn_shift == nullptr))
+      return fail(CONVF_ERR_INVALID_ARG, "bn_scale and bn_shift must be given together");
+    if (bn_scale)
+      for (int k = 0; k < s.K; ++k)
+        if (!std::isfinite(bn_scale[k]) || !std::isfinite(bn_shift[k]))
+          return fail(CONVF_ERR_INVALID_ARG, "bn_scale/bn_shift[%d] is not finite", k);
+  }
+  int variant = 0;
+  if ((st = select_variant(desc, s, &variant)) != CONVF_OK) return st;
+
+  // ---------------------------------------------------------------- host-side prep
+  convf_handle* h = new (std::nothrow) convf_handle();
+  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed");
+  h->desc = *desc;
+  h->s = s;
+  h->variant = variant;
+  h->zp = out_zero_point;
+  act_bounds(desc, &h->lo, &h->hi);
+
+  cudaError_t ce = cudaGetDevice(&h->device);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (ce != cudaSuccess) {
+    delete h;
+    return fail(CONVF_ERR_CUDA, "no usable CUDA device: %s", cudaGetErrorString(ce));
+  }
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  if (cc_major != 10 || cc_minor != 3) {
+    delete h;
+    return fail(CONVF_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a only", cc_major, cc_minor);
+  }
+
+  // BN fold: epilogue scale and bias' = scale*B + shift, in double, stored as float
+  const int Kpad = (int)align_up((size_t)s.K, 256);
+  std::vector<float> scale(Kpad, 0.f), biasf(Kpad, 0.f);
+  for (int k = 0; k < s.K; ++k) {
+    const double sc = bn_scale ? (double)bn_scale[k] : 1.0;
+    const double sf = bn_shift ? (double)bn_shift[k] : 0.0;
+    const double b = (!s8 && bias) ? (double)static_cast<const float*>(bias)[k] : 0.0;
+    scale[k] = (float)sc;
+    biasf[k] = (float)(sc * b + sf);
+  }
+
+  // device layout
+  size_t off = 0;
+  auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  size_t o_w = 0, o_taps = 0, o_scale = 0, o_bias = 0, o_qb = 0, o_qm = 0, o_qs = 0;
+  std::vector<uint16_t> wpack;
+  std::vector<float> taps;
+  if (variant == CONVF_VARIANT_DEPTHWISE) {
+    taps.assign((size_t)s.R * s.S * s.C, 0.f);
+    const uint16_t* Wb = static_cast<const uint16_t*>(W);
+    for (int c = 0; c < s.C; ++c)
+      for (int r = 0; r < s.R; ++r)
+        for (int q = 0; q < s.S; ++q)
+          taps[(size_t)(r * s.S + q) * s.C + c] =
+              (float)((double)scale[c] * (double)bf16_to_f32(Wb[((size_t)c * s.R + r) * s.S + q]));
+    o_taps = carve(taps.size() * sizeof(float));
+    o_bias = carve((size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_INT8) {
+    o_w = carve((size_t)s.K * s.R * s.S * s.C);
+    o_qb = carve((size_t)s.K * 4);
+    o_qm = carve((size_t)s.K * 4);
+    o_qs = carve((size_t)s.K * 4);
+  } else {
+    tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot);
+    wpack.resize((size_t)s.K * h->ktot);
+    pack_bf16(static_cast<const uint16_t*>(W), s, h->a_mode, h->ktot, wpack.data());
+    o_w = carve(wpack.size() * sizeof(uint16_t));
+    o_scale = carve((size_t)Kpad * sizeof(float));
+    o_bias = carve((size_t)Kpad * sizeof(float));
+  }
+  const size_t o_status = carve(sizeof(int));
+  h->dev_bytes = off;
+  ce = cudaMalloc(&h->dev, h->dev_bytes);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s", off, cudaGetErrorString(ce));
+  }
+  char* base = static_cast<char*>(h->dev);
+  h->status = reinterpret_cast<int*>(base + o_status);
+  std::vector<char> staging(h->dev_bytes, 0);
+  if (variant == CONVF_VARIANT_DEPTHWISE) {
+    h->taps = reinterpret_cast<float*>(base + o_taps);
+    h->bias = reinterpret_cast<float*>(base + o_bias);
+    std::memcpy(staging.data() + o_taps, taps.data(), taps.size() * sizeof(float));
+    std::memcpy(staging.data() + o_bias, biasf.data(), (size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_INT8) {
+    h->w_s8 = reinterpret_cast<int8_t*>(base + o_w);
+    h->qbias = reinterpret_cast<int32_t*>(base + o_qb);
+    h->qmult = reinterpret_cast<int32_t*>(base + o_qm);
+    h->qshift = reinterpret_cast<int32_t*>(base + o_qs);
+    // [K][C][R][S] -> [K][R][S][C]
+    const int8_t* Wi = static_cast<const int8_t*>(W);
+    int8_t* dst = reinterpret_cast<int8_t*>(staging.data() + o_w);
+    for (int k = 0; k < s.K; ++k)
+      for (int c = 0; c < s.C; ++c)
+        for (int r = 0; r < s.R; ++r)
+          for (int q = 0; q < s.S; ++q)
+            dst[(((size_t)k * s.R + r) * s.S + q) * s.C + c] = Wi[(((size_t)k * s.C + c) * s.R + r) * s.S + q];
+    int32_t* qb = reinterpret_cast<int32_t*>(staging.data() + o_qb);
+    for (int k = 0; k < s.K; ++k) qb[k] = bias ? static_cast<const int32_t*>(bias)[k] : 0;
+    std::memcpy(staging.data() + o_qm, requant_mult, (size_t)s.K * 4);
+    std::memcpy(staging.data() + o_qs, requant_shift, (size_t)s.K * 4);
+  } else {
+    h->w_bf16 = reinterpret_cast<uint16_t*>(base + o_w);
+    h->scale = reinterpret_cast<float*>(base + o_scale);
+    h->bias = reinterpret_cast<float*>(base + o_bias);
+    std::memcpy(staging.data() + o_w, wpack.data(), wpack.size() * sizeof(uint16_t));
+    std::memcpy(staging.data() + o_scale, scale.data(), (size_t)Kpad * sizeof(float));
+    std::memcpy(staging.data() + o_bias, biasf.data(), (size_t)Kpad * sizeof(float));
+  }
+  ce = cudaMemcpy(h->dev, staging.data(), h->dev_bytes, cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) {
+    cudaFree(h->dev);
+    delete h;
+    return fail(CONVF_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(ce));
+  }
+
+  if (variant == CONVF_VARIANT_GEMM_1X1 || variant == CONVF_VARIANT_IMPLICIT_GEMM ||
+      variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
+    if (!load_encoders()) {
+      cudaFree(h->dev);
+      delete h;
+      return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled/Im2col are unavailable from the driver");
+    }
+    h->bn = pick_bn(s.M, s.K, h->num_sms);
+    h->num_kb = h->ktot / 64;
+    h->n_blocks = (s.K + h->bn - 1) / h->bn;
+    const long long tiles = (s.M + 127) / 128 * h->n_blocks;
+    h->num_tiles = (int)tiles;
+    h->grid = (int)std::min<long long>(tiles, h->num_sms);
+    const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
+    const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)h->bn};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w_bf16, dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      cudaFree(h->dev);
+      delete h;
+      return fail(CONVF_ERR_CUDA, "weight tensor map encoding failed (CUresult %d)", (int)r);
+    }
+  }
+  h->magic = kMagic;
+  *out = h;
+  return ok();
+}
+
+namespace {
+convf_status encode_io_maps(convf_handle* h, const void* x, const void* y) {
+  const Shape& s = h->s;
+  CUresult r;
+  if (h->a_mode == kA2D) {
+    const cuuint64_t dims[2] = {(cuuint64_t)s.C, (cuuint64_t)s.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)s.C * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t es[2] = {1, 1};
+    r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "activation tensor map encoding failed (CUresult %d)", (int)r);
+  } else if (h->a_mode == kAIm2col) {
+    const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2, (cuuint64_t)s.H * s.W * s.C * 2};
+    const int lower[2] = {-s.pl, -s.pt};
+    const int upper[2] = {s.pr - (s.S - 1) * s.dw, s.pb - (s.R - 1) * s.dh};
+    const cuuint32_t es[4] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1};
+    r = g_encode_im2col(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, lower,
+                        upper, 64, 128, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "im2col tensor map encoding failed (CUresult %d)", (int)r);
+  } else {
+    std::memset(&h->tmA, 0, sizeof h->tmA);
+  }
+  const cuuint64_t ydims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
+  const cuuint64_t ystr[1] = {(cuuint64_t)s.K * 4};
+  const cuuint32_t ybox[2] = {32, 128};
+  const cuuint32_t es[2] = {1, 1};
+  r = g_encode_tiled(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(y), ydims, ystr, ybox, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "output tensor map encoding failed (CUresult %d)", (int)r);
+  h->map_x = x;
+  h->map_y = y;
+  return CONVF_OK;
+}
+}  // namespace
+
+convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  const Shape& s = h->s;
+  if (s.M == 0) return ok();   // empty batch: nothing to compute
+  if (!x || !y) return fail(CONVF_ERR_INVALID_ARG, "x/y is NULL");
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15))
+    return fail(CONVF_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  const size_t esz = h->variant == CONVF_VARIANT_INT8 ? 1 : 2;
+  const size_t xb = (size_t)s.N * s.H * s.W * s.C * esz;
+  const size_t yb = (size_t)s.M * s.K * (h->variant == CONVF_VARIANT_INT8 ? 1 : 4);
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
+  if (x0 < y0 + yb && y0 < x0 + xb) return fail(CONVF_ERR_INVALID_ARG, "x and y overlap");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
+    return fail(CONVF_ERR_INVALID_ARG, "the current device (%d) is not the handle's device (%d)", dev, h->device);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaSuccess;
+  switch (h->variant) {
+    case CONVF_VARIANT_DEPTHWISE: {
+      DwParams p{};
+      p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.Ho = s.Ho; p.Wo = s.Wo; p.R = s.R; p.S = s.S;
+      p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl; p.dh = s.dh; p.dw = s.dw;
+      p.x = static_cast<const uint16_t*>(x); p.taps = h->taps; p.bias = h->bias; p.y = static_cast<float*>(y);
+      p.lo = h->lo; p.hi = h->hi;
+      ce = launch_depthwise(p, h->num_sms, strm);
+      break;
+    }
+    case CONVF_VARIANT_INT8: {
+      S8Params p{};
+      p.M = (int)s.M; p.Kout = s.K; p.C = s.C; p.H = s.H; p.W = s.W; p.Ho = s.Ho; p.Wo = s.Wo; p.R = s.R; p.S = s.S;
+      p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl; p.dh = s.dh; p.dw = s.dw;
+      p.num_kb = s.R * s.S * s.C / 64;
+      p.x = static_cast<const int8_t*>(x); p.w = h->w_s8; p.bias = h->qbias; p.mult = h->qmult;
+      p.shift = h->qshift; p.y = static_cast<int8_t*>(y); p.zp = h->zp; p.relu = h->desc.act == CONVF_ACT_RELU;
+      ce = launch_s8_conv(p, strm);
+      break;
+    }
+    default: {
+      if (x != h->map_x || y != h->map_y) {
+        if ((st = encode_io_maps(h, x, y)) != CONVF_OK) return st;
+      }
+      TcConvParams p{};
+      p.M = (int)s.M; p.Kout = s.K; p.num_kb = h->num_kb; p.cblocks = h->cblocks; p.R = s.R; p.S = s.S;
+      p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
+      p.H = s.H; p.W = s.W; p.C = s.C; p.Ho = s.Ho; p.Wo = s.Wo;
+      p.n_blocks = h->n_blocks; p.num_tiles = h->num_tiles; p.a_mode = h->a_mode;
+      p.scale = h->scale; p.bias = h->bias; p.x = static_cast<const uint16_t*>(x);
+      p.lo = h->lo; p.hi = h->hi; p.status = h->status;
+      const bool gather = h->a_mode == kAGather;
+      switch (h->bn) {
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
+      }
+    }
+  }
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
+convf_status conv_fused_status(convf_handle* h) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  int v = 0;
+  cudaError_t ce = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "status read failed: %s", cudaGetErrorString(ce));
+  if (v & kStatusTimeout) return fail(CONVF_ERR_TIMEOUT, "a bounded device wait ran out in an earlier run");
+  return ok();
+}
+
+convf_status conv_fused_clear_status(convf_handle* h) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  cudaError_t ce = cudaMemset(h->status, 0, sizeof(int));
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "status clear failed: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
+void conv_fused_destroy(convf_handle* h) {
+  if (!h || h->magic != kMagic) return;
+  h->magic = kDeadMagic;
+  cudaFree(h->dev);
+  delete h;
+}
+
+int conv_fused_variant(const convf_handle* h) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  return h->variant;
+}
+
+convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
+  static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
+                                "implicit_gemm_gather"};
+  const Shape& s = h->s;
+  if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8)
+    snprintf(buf, len, "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
+  else
+    snprintf(buf, len,
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d tiles=%d grid=%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->bn, h->num_kb, h->num_tiles, h->grid,
+             h->dev_bytes);
+  return ok();
+}
+
+convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles, void* stream) {
+  if (!status_dev) return fail(CONVF_ERR_INVALID_ARG, "status_dev is NULL");
+  if (budget_cycles < 1 || budget_cycles > 20000000000LL)
+    return fail(CONVF_ERR_INVALID_ARG, "budget_cycles=%lld is outside 1..2e10", budget_cycles);
+  cudaError_t ce = launch_watchdog_selftest(status_dev, budget_cycles, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "self-test launch failed: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Internal interface between the host prep (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace convf {
+
+// Bit set in a handle's device status word when a bounded device wait ran out.
+constexpr int kStatusTimeout = 1;
+
+// ---------------------------------------------------------------- tcgen05 implicit GEMM
+// GEMM view of the conv: rows m = (n, oh, ow) (M = N*Ho*Wo), columns = output channels,
+// reduction j over (tap, channel).  A = activation rows (im2col on the fly), B = prepacked
+// weights [K][Ktot] bf16 (Ktot = num_kb * 64), D = fp32 accumulator in TMEM.
+enum AMode : int { kA2D = 0, kAIm2col = 1, kAGather = 2 };
+
+struct TcConvParams {
+  int M;            // output rows N*Ho*Wo
+  int Kout;         // output channels
+  int num_kb;       // 64-wide reduction blocks per tile
+  int cblocks;      // channel blocks per tap (im2col mode)
+  int R, S;         // filter taps
+  int dh, dw;       // dilations
+  int sh, sw;       // strides
+  int pt, pl;       // leading pads
+  int H, W, C;      // input extent (gather mode)
+  int Ho, Wo;       // output extent
+  int n_blocks;     // ceil(Kout / BN)
+  int num_tiles;    // ceil(M / 128) * n_blocks
+  int a_mode;       // AMode
+  const float* scale;     // [Kpad] per-channel epilogue scale (BN scale)
+  const float* bias;      // [Kpad] per-channel epilogue bias (scale*B + shift)
+  const uint16_t* x;      // NHWC bf16 input (gather mode)
+  float lo, hi;           // activation clamp
+  int* status;            // device status word
+};
+
+// Launches the persistent kernel with tile width bn (32, 64, 128 or 256).
+cudaError_t launch_tc_conv(int bn, const TcConvParams& p, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const CUtensorMap& tmY, int grid,
+                           cudaStream_t stream);
+int tc_conv_smem_bytes(int bn, bool gather);
+
+// ---------------------------------------------------------------- depthwise (CUDA cores)
+struct DwParams {
+  int N, C, H, W, Ho, Wo, R, S;
+  int sh, sw, pt, pl, dh, dw;
+  const uint16_t* x;      // NHWC bf16
+  const float* taps;      // [R*S][C] fp32, BN scale folded in
+  const float* bias;      // [C]
+  float* y;               // NHWC fp32
+  float lo, hi;
+};
+cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- int8 implicit GEMM
+struct S8Params {
+  int M, Kout, C, H, W, Ho, Wo, R, S;
+  int sh, sw, pt, pl, dh, dw;
+  int num_kb;             // R*S*C/64
+  const int8_t* x;        // NHWC int8
+  const int8_t* w;        // [K][R][S][C] int8
+  const int32_t* bias;    // [K]
+  const int32_t* mult;    // [K]
+  const int32_t* shift;  // [K]
+  int8_t* y;              // NHWC int8
+  int zp, relu;
+};
+cudaError_t launch_s8_conv(const S8Params& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- watchdog self-test
+cudaError_t launch_watchdog_selftest(int32_t* status, long long budget, cudaStream_t stream);
+
+}  // namespace convf

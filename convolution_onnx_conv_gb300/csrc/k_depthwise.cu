@@ -1,0 +1,161 @@
+// Depthwise convolution (group == C == K) on CUDA cores: memory-bound (about 2-3 flop per
+// byte), so no tensor cores.  NHWC bf16 in, fp32 taps with the BN scale folded in, fp32 out.
+// Each thread owns 8 channels (one 16-byte vector) x kOW consecutive outputs of one row;
+// consecutive threads take consecutive channel vectors of the same pixel, so every load and
+// store is a coalesced 128-bit access.  Inputs shared by neighbouring threads (the 3x3 halo)
+// are re-read through L1/L2, not from HBM.
+#include "convf_internal.h"
+#include "ptx.cuh"
+
+namespace convf {
+
+constexpr int kOW = 4;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float clampf(float v, float lo, float hi) { return fminf(fmaxf(v, lo), hi); }
+
+// 3x3, dilation 1, equal strides SW in {1, 2}.
+template <int SW>
+__global__ void __launch_bounds__(256) dw3x3_kernel(const DwParams p) {
+  const int C8 = p.C >> 3;
+  const int owb_n = (p.Wo + kOW - 1) / kOW;
+  const long long total = static_cast<long long>(p.N) * p.Ho * owb_n * C8;
+  constexpr int NCOL = (kOW - 1) * SW + 3;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(idx % C8);
+    long long t = idx / C8;
+    const int owb = static_cast<int>(t % owb_n);
+    t /= owb_n;
+    const int oh = static_cast<int>(t % p.Ho);
+    const int n = static_cast<int>(t / p.Ho);
+    const int c0 = c8 * 8;
+    const int ow0 = owb * kOW;
+
+    float acc[kOW][8];
+    {
+      const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.bias + c0));
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.bias + c0 + 4));
+#pragma unroll
+      for (int j = 0; j < kOW; ++j) {
+        acc[j][0] = b0.x; acc[j][1] = b0.y; acc[j][2] = b0.z; acc[j][3] = b0.w;
+        acc[j][4] = b1.x; acc[j][5] = b1.y; acc[j][6] = b1.z; acc[j][7] = b1.w;
+      }
+    }
+    const int iw_base = ow0 * SW - p.pl;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const int ih = oh * SW - p.pt + r;
+      if (ih < 0 || ih >= p.H) continue;
+      float tap[3][8];
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const float4 t0 = __ldg(reinterpret_cast<const float4*>(p.taps + (r * 3 + s) * p.C + c0));
+        const float4 t1 = __ldg(reinterpret_cast<const float4*>(p.taps + (r * 3 + s) * p.C + c0 + 4));
+        tap[s][0] = t0.x; tap[s][1] = t0.y; tap[s][2] = t0.z; tap[s][3] = t0.w;
+        tap[s][4] = t1.x; tap[s][5] = t1.y; tap[s][6] = t1.z; tap[s][7] = t1.w;
+      }
+      const uint16_t* xrow = p.x + (static_cast<size_t>(n) * p.H + ih) * p.W * p.C + c0;
+      uint4 raw[NCOL];
+#pragma unroll
+      for (int col = 0; col < NCOL; ++col) {
+        const int iw = iw_base + col;
+        raw[col] = (iw >= 0 && iw < p.W)
+                       ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(iw) * p.C))
+                       : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int col = 0; col < NCOL; ++col) {
+        float xv[8];
+        bf16x8_to_f32(raw[col], xv);
+#pragma unroll
+        for (int j = 0; j < kOW; ++j) {
+          const int s = col - j * SW;
+          if (s >= 0 && s < 3) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(xv[e], tap[s][e], acc[j][e]);
+          }
+        }
+      }
+    }
+    float* yrow = p.y + ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo) * p.C + c0;
+#pragma unroll
+    for (int j = 0; j < kOW; ++j) {
+      if (ow0 + j < p.Wo) {
+        float4* dst = reinterpret_cast<float4*>(yrow + static_cast<size_t>(ow0 + j) * p.C);
+        dst[0] = make_float4(clampf(acc[j][0], p.lo, p.hi), clampf(acc[j][1], p.lo, p.hi),
+                             clampf(acc[j][2], p.lo, p.hi), clampf(acc[j][3], p.lo, p.hi));
+        dst[1] = make_float4(clampf(acc[j][4], p.lo, p.hi), clampf(acc[j][5], p.lo, p.hi),
+                             clampf(acc[j][6], p.lo, p.hi), clampf(acc[j][7], p.lo, p.hi));
+      }
+    }
+  }
+}
+
+// Any filter size, strides and dilations: one output pixel x 8 channels per thread.
+__global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
+  const int C8 = p.C >> 3;
+  const long long total = static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(idx % C8);
+    long long t = idx / C8;
+    const int ow = static_cast<int>(t % p.Wo);
+    t /= p.Wo;
+    const int oh = static_cast<int>(t % p.Ho);
+    const int n = static_cast<int>(t / p.Ho);
+    const int c0 = c8 * 8;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = __ldg(p.bias + c0 + e);
+    for (int r = 0; r < p.R; ++r) {
+      const int ih = oh * p.sh - p.pt + r * p.dh;
+      if (ih < 0 || ih >= p.H) continue;
+      for (int s = 0; s < p.S; ++s) {
+        const int iw = ow * p.sw - p.pl + s * p.dw;
+        if (iw < 0 || iw >= p.W) continue;
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+            p.x + ((static_cast<size_t>(n) * p.H + ih) * p.W + iw) * p.C + c0));
+        float xv[8];
+        bf16x8_to_f32(raw, xv);
+        const float* tp = p.taps + (r * p.S + s) * p.C + c0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(xv[e], __ldg(tp + e), acc[e]);
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(p.y + ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo + ow) * p.C + c0);
+    dst[0] = make_float4(clampf(acc[0], p.lo, p.hi), clampf(acc[1], p.lo, p.hi),
+                         clampf(acc[2], p.lo, p.hi), clampf(acc[3], p.lo, p.hi));
+    dst[1] = make_float4(clampf(acc[4], p.lo, p.hi), clampf(acc[5], p.lo, p.hi),
+                         clampf(acc[6], p.lo, p.hi), clampf(acc[7], p.lo, p.hi));
+  }
+}
+
+cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream) {
+  const bool fast = p.R == 3 && p.S == 3 && p.dh == 1 && p.dw == 1 && p.sh == p.sw &&
+                    (p.sh == 1 || p.sh == 2);
+  const long long C8 = p.C / 8;
+  const long long work = fast ? static_cast<long long>(p.N) * p.Ho * ((p.Wo + kOW - 1) / kOW) * C8
+                              : static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
+  if (work == 0) return cudaSuccess;
+  long long blocks = (work + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8 * 4;
+  if (blocks > cap) blocks = cap;
+  if (fast && p.sh == 1)
+    dw3x3_kernel<1><<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  else if (fast)
+    dw3x3_kernel<2><<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  else
+    dw_generic_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace convf

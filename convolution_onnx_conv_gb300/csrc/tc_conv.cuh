@@ -1,0 +1,326 @@
+// Persistent tcgen05 implicit-GEMM convolution with a fused scale + bias + clamp epilogue.
+//
+// GEMM view (the "tensorforge" page does im2col + GEMM, section "Status"; here the im2col is
+// never materialised): rows m = (n, oh, ow), M = N*Ho*Wo; columns = output channels K;
+// reduction over (tap r,s; channel c) in 64-wide blocks.  One CTA per SM loops over 128 x BN
+// output tiles.  Warp roles:
+//   warp 0      TMA producer: weight tile (2D tiled load) and, except in gather mode, the
+//               activation tile (2D tiled load for 1x1/stride-1/pad-0, else an im2col load
+//               whose tap offsets select the filter position; padding is TMA zero fill)
+//   warp 1      TMEM allocation + single-thread tcgen05.mma issue into a double-buffered
+//               fp32 accumulator (2 x BN TMEM columns)
+//   warps 2-5   epilogue: tcgen05.ld -> y = clamp(scale[k]*acc + bias[k], lo, hi) -> swizzled
+//               smem staging -> TMA store (clips the ragged M and K edges)
+//   warps 6-9   (gather mode only) activation rows gathered by threads, for channel counts
+//               that TMA cannot address (C not a multiple of 8, e.g. a 3-channel stem)
+#pragma once
+#include "convf_internal.h"
+#include "ptx.cuh"
+
+namespace convf {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kATileBytes = kBM * kBK * 2;
+constexpr int kEpiCols = 32;
+constexpr int kEpiTileBytes = kBM * kEpiCols * 4;
+constexpr int kNumEpiBuf = 2;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kBTileBytes = BN * kBK * 2;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem =
+      1024 + kStages * (kATileBytes + kBTileBytes) + kNumEpiBuf * kEpiTileBytes + kBarBytes;
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
+};
+
+template <int BN, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
+    tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
+  using Cfg = TcCfg<BN>;
+  constexpr int kStages = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages * kATileBytes;
+  uint8_t* sEpi = sB + kStages * Cfg::kBTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kNumEpiBuf * kEpiTileBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // go/abort decisions broadcast by a leader thread through a named barrier; two slots used
+  // alternately so the leader never overwrites a flag another thread has yet to read
+  volatile int* epi_go = abort_flag + 1;
+  volatile int* gat_go = abort_flag + 3;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], GATHER ? 1 + 128 : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmY);
+    if (!GATHER) tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t tx = Cfg::kBTileBytes + (GATHER ? 0 : kATileBytes);
+      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        const int m0 = (tile / p.n_blocks) * kBM;
+        const int n0 = (tile % p.n_blocks) * BN;
+        int img = 0, hb = 0, wb = 0;
+        if (p.a_mode == kAIm2col) {
+          const int hw = p.Ho * p.Wo;
+          img = m0 / hw;
+          const int rem = m0 - img * hw;
+          const int oh = rem / p.Wo;
+          const int ow = rem - oh * p.Wo;
+          hb = oh * p.sh - p.pt;
+          wb = ow * p.sw - p.pl;
+        }
+        int tap = 0, cb = 0;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
+          mbar_arrive_expect_tx(&full[stage], tx);
+          if (!GATHER) {
+            uint8_t* dA = sA + stage * kATileBytes;
+            if (p.a_mode == kA2D) {
+              tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
+            } else {
+              const int r = tap / p.S;
+              const int s = tap - r * p.S;
+              tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img,
+                                 static_cast<uint16_t>(s * p.dw), static_cast<uint16_t>(r * p.dh));
+              if (++cb == p.cblocks) {
+                cb = 0;
+                ++tap;
+              }
+            }
+          }
+          tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto teardown;
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * kATileBytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * Cfg::kBTileBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;       // 0..127
+    const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;         // tile row == TMEM lane
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int ebuf = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      const int m0 = (tile / p.n_blocks) * kBM;
+      const int n0 = (tile % p.n_blocks) * BN;
+      if (et == 0) epi_go[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
+      named_barrier(1, 128);
+      if (!epi_go[it & 1]) break;
+      tc_fence_after();
+      const int left = p.Kout - n0;
+      const int nchunks = left >= BN ? BN / kEpiCols : (left + kEpiCols - 1) / kEpiCols;
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const int nc = n0 + ch * kEpiCols;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(acc * BN + ch * kEpiCols),
+                           v);
+        tmem_ld_wait();
+        if (ch == nchunks - 1) {
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
+        const float4* sc4 = reinterpret_cast<const float4*>(p.scale + nc);
+        const float4* bi4 = reinterpret_cast<const float4*>(p.bias + nc);
+        float o[32];
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 sc = __ldg(sc4 + j4);
+          const float4 bi = __ldg(bi4 + j4);
+          o[4 * j4 + 0] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 0]), sc.x, bi.x), p.lo), p.hi);
+          o[4 * j4 + 1] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 1]), sc.y, bi.y), p.lo), p.hi);
+          o[4 * j4 + 2] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 2]), sc.z, bi.z), p.lo), p.hi);
+          o[4 * j4 + 3] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 3]), sc.w, bi.w), p.lo), p.hi);
+        }
+        // the staging buffer used two chunks ago must have been read out by its TMA store
+        if (et == 0) bulk_wait_read<1>();
+        named_barrier(1, 128);
+        uint8_t* buf = sEpi + ebuf * kEpiTileBytes + row * 128;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          *reinterpret_cast<float4*>(buf + ((c16 ^ (row & 7)) << 4)) =
+              make_float4(o[4 * c16], o[4 * c16 + 1], o[4 * c16 + 2], o[4 * c16 + 3]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, 128);
+        if (et == 0) {
+          tma_store_2d(&tmY, sEpi + ebuf * kEpiTileBytes, nc, m0);
+          bulk_commit();
+        }
+        ebuf ^= 1;
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (et == 0) bulk_wait_all();
+  } else if (GATHER) {
+    // ------------------------------------------------------------------ row gatherers
+    const int gt = threadIdx.x - 192;      // tile row 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    const int hw = p.Ho * p.Wo;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      const int m = (tile / p.n_blocks) * kBM + gt;
+      const bool row_ok = m < p.M;
+      const int img = row_ok ? m / hw : 0;
+      const int rem = m - img * hw;
+      const int oh = rem / p.Wo;
+      const int ow = rem - oh * p.Wo;
+      const int ih0 = oh * p.sh - p.pt;
+      const int iw0 = ow * p.sw - p.pl;
+      const uint16_t* xn = p.x + static_cast<size_t>(img) * p.H * p.W * p.C;
+      int c = 0, s = 0, r = 0;   // decomposition of the reduction index, channel fastest
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (gt == 0) gat_go[kb & 1] = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
+        named_barrier(2, 128);
+        if (!gat_go[kb & 1]) goto teardown;
+        uint8_t* dst = sA + stage * kATileBytes + gt * 128;
+#pragma unroll 1
+        for (int c16 = 0; c16 < 8; ++c16) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            uint32_t val = 0;
+            if (row_ok && r < p.R) {
+              const int ih = ih0 + r * p.dh;
+              const int iw = iw0 + s * p.dw;
+              if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+                val = __ldg(xn + (static_cast<size_t>(ih) * p.W + iw) * p.C + c);
+            }
+            if (e & 1)
+              pk[e >> 1] |= val << 16;
+            else
+              pk[e >> 1] = val;
+            if (++c == p.C) {
+              c = 0;
+              if (++s == p.S) {
+                s = 0;
+                ++r;
+              }
+            }
+          }
+          *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+
+teardown:
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // a wait ran out: give copies and MMAs already in flight time to land before TMEM is freed
+    for (int i = 0; i < 2000; ++i) __nanosleep(100000);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <int BN, bool GATHER>
+cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const CUtensorMap& tmY, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  auto* k = tc_conv_kernel<BN, GATHER>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcCfg<BN>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k<<<grid, GATHER ? 320 : 192, TcCfg<BN>::kSmem, stream>>>(p, tmA, tmB, tmY);
+  return cudaGetLastError();
+}
+
+}  // namespace convf

@@ -1,0 +1,18 @@
+// One tile width of the tcgen05 implicit-GEMM kernel per translation unit (compiled with
+// -DCONVF_BN=32/64/128/256) so the instantiations build in parallel.
+#include "tc_conv.cuh"
+
+#ifndef CONVF_BN
+#error "compile with -DCONVF_BN=<tile width>"
+#endif
+#define CONVF_CAT2(a, b) a##b
+#define CONVF_CAT(a, b) CONVF_CAT2(a, b)
+
+namespace convf {
+cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
+                                                   const CUtensorMap& tmB, const CUtensorMap& tmY, int grid,
+                                                   bool gather, cudaStream_t stream) {
+  return gather ? launch_tc_conv_t<CONVF_BN, true>(p, tmA, tmB, tmY, grid, stream)
+                : launch_tc_conv_t<CONVF_BN, false>(p, tmA, tmB, tmY, grid, stream);
+}
+}  // namespace convf

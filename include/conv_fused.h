@@ -1,0 +1,182 @@
+/*
+ * conv_fused.h -- fused ONNX Conv (+ folded inference BatchNorm, bias, ReLU/ReLU6/Clip)
+ * on one GB300 GPU (sm_103a).  Plain C ABI: host/device pointers and sizes only.
+ *
+ * What the operation is
+ * ---------------------
+ *   ONNX Conv (public operator specification): X[N][C][H][W] (NCHW semantics),
+ *   W[K][C/group][R][S], optional bias B[K], attributes strides, pads
+ *   [h_begin, w_begin, h_end, w_end], dilations, group, auto_pad.
+ *   Followed, per output channel k, by an affine y = scale[k]*z + shift[k] -- the inference
+ *   BatchNorm folded offline into the conv ("tensorforge", section "ResNet fusion":
+ *   Conv -> BN -> Relu becomes one fused conv epilogue, W' = scale*W, bias = shift) -- and by a
+ *   clamp activation (ReLU, ReLU6 = min(max(u,0),6), Clip(lo,hi); consecutive relu/min/max fuse
+ *   into one min+max, "Kyanite" README, section "Optimizer").
+ *   The library selects one of four kernels per shape ("OxiONNX 0.1.7 Released", Technical
+ *   Deep Dive 2, "Real Conv dispatch": ImplicitGemmConv / Conv1x1 / DepthwiseConv per shape),
+ *   plus a static-int8 kernel ("onnx-vulkan-rs", feature list: static int8 convolutions on
+ *   the tensor cores) -- and refuses, at create time, any node it cannot honour, naming the
+ *   reason; there is no CPU fallback (the same page: refuse at load time, never answer wrongly).
+ *
+ * Storage layout
+ * --------------
+ *   Logical dimensions are always ONNX NCHW.  The kernels read and write channels-last storage
+ *   (NHWC: x[n][h][w][c], y[n][oh][ow][k]), i.e. a torch channels_last tensor.  CONVF_NCHW
+ *   storage is refused with CONVF_ERR_UNSUPPORTED.
+ *
+ * Numerics
+ * --------
+ *   CONVF_BF16: x and W are bf16 (raw uint16 bits), accumulation fp32, y fp32.  The BN scale
+ *   is applied to the fp32 accumulator (y = clamp(scale*acc + bias', lo, hi), bias' =
+ *   scale*B + shift), which equals conv(scale*W) + bias' without rounding scale*W to bf16.
+ *   Depthwise folds scale into fp32 taps.
+ *   CONVF_S8: x, W int8 (symmetric, zero point 0), int32 accumulation, int32 bias, then per
+ *   output channel q = (v*mult + 2^(shift-1)) >> shift (int64, arithmetic shift), v = acc +
+ *   bias, o = clamp(q + out_zero_point, relu ? max(zp,-128) : -128, 127) as int8.
+ *
+ * Ownership and errors
+ * --------------------
+ *   create copies every host array it is given (the library owns the device copies; the
+ *   caller may free its arrays on return).  run reads caller-owned device x and writes
+ *   caller-owned device y, asynchronously on the caller's stream; it allocates nothing and
+ *   never synchronises.  Every call returns a convf_status; conv_fused_last_error() gives a
+ *   thread-local message naming the offending argument.  A handle is used from one stream at a
+ *   time.  Device waits inside the kernels are bounded: a wait that runs out sets a status bit
+ *   that conv_fused_status reports as CONVF_ERR_TIMEOUT after the caller synchronises.
+ */
+#ifndef CONV_FUSED_H
+#define CONV_FUSED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CONVF_OK = 0,
+  CONVF_ERR_INVALID_ARG = -1,  /* malformed argument (named in conv_fused_last_error) */
+  CONVF_ERR_UNSUPPORTED = -2,  /* well-formed but not served by any kernel: refused, no fallback */
+  CONVF_ERR_OOM = -3,          /* device allocation failed at create */
+  CONVF_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+  CONVF_ERR_TIMEOUT = -5       /* a bounded device wait ran out during a run */
+} convf_status;
+
+typedef enum { CONVF_BF16 = 0, CONVF_S8 = 1 } convf_dtype;
+typedef enum { CONVF_NCHW = 0, CONVF_NHWC = 1 } convf_layout;
+typedef enum {
+  CONVF_ACT_NONE = 0, CONVF_ACT_RELU = 1, CONVF_ACT_RELU6 = 2, CONVF_ACT_CLIP = 3
+} convf_act;
+typedef enum {
+  CONVF_AUTO_PAD_NOTSET = 0, CONVF_AUTO_PAD_SAME_UPPER = 1, CONVF_AUTO_PAD_SAME_LOWER = 2,
+  CONVF_AUTO_PAD_VALID = 3
+} convf_auto_pad;
+
+/* Kernel variants.  CONVF_VARIANT_AUTO lets the shape-keyed selector choose; any other value
+ * forces that kernel (refused with CONVF_ERR_UNSUPPORTED if it cannot serve the shape). */
+typedef enum {
+  CONVF_VARIANT_AUTO = 0,
+  CONVF_VARIANT_IMPLICIT_GEMM = 1,   /* tcgen05 implicit GEMM, TMA im2col activation tiles */
+  CONVF_VARIANT_GEMM_1X1 = 2,        /* same kernel, activations read as a [N*H*W][C] matrix */
+  CONVF_VARIANT_DEPTHWISE = 3,       /* CUDA-core depthwise (group == C == K) */
+  CONVF_VARIANT_INT8 = 4,            /* int8 tensor-core MMA, int32 accumulate, requant */
+  CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 5  /* tcgen05 implicit GEMM, activation rows gathered by
+                                            threads (any C, e.g. the 3-channel stem) */
+} convf_variant;
+
+typedef struct {
+  int N, C, H, W;          /* x: [N][C][H][W] logical; N may be 0 (empty run)                */
+  int K, R, S;             /* W: [K][C/group][R][S]                                           */
+  int stride[2];           /* (h, w), >= 1                                                    */
+  int dilation[2];         /* (h, w), >= 1                                                    */
+  int pads[4];             /* ONNX order h_begin, w_begin, h_end, w_end; ignored unless NOTSET */
+  int auto_pad;            /* convf_auto_pad                                                  */
+  int group;               /* C % group == 0 && K % group == 0                                */
+  int dtype;               /* convf_dtype                                                     */
+  int x_layout, y_layout;  /* convf_layout; only CONVF_NHWC is served                         */
+  int act;                 /* convf_act                                                       */
+  float clip_lo, clip_hi;  /* bounds for CONVF_ACT_CLIP (lo <= hi)                            */
+  int variant;             /* convf_variant; 0 = selector                                     */
+} convf_desc;
+
+typedef struct convf_handle convf_handle;
+
+/* Output logical shape [N][K][Ho][Wo] of desc (ONNX Conv shape rule, auto_pad resolved).
+ * CONVF_ERR_INVALID_ARG if the attributes are malformed or the window does not fit. */
+convf_status conv_fused_output_shape(const convf_desc* desc, int out_nchw[4]);
+
+/* Resolved explicit pads (h_begin, w_begin, h_end, w_end) for desc's auto_pad (ONNX rule:
+ * SAME_* pads to ceil(in/stride) outputs, the odd element at the end for SAME_UPPER and at the
+ * beginning for SAME_LOWER; VALID = no padding). */
+convf_status conv_fused_resolve_pads(const convf_desc* desc, int pads_out[4]);
+
+/* BN inference affine from its parameters, computed in double and rounded to float:
+ *   scale[k] = gamma[k] / sqrt(var[k] + eps),  shift[k] = beta[k] - mean[k] * scale[k].
+ * All arrays are host float[K]; eps > 0 (ONNX default 1e-5). */
+convf_status conv_bn_scale_shift(int K, const float* gamma, const float* beta, const float* mean,
+                                 const float* var, float eps, float* scale, float* shift);
+
+/* Host-only view of the shape-keyed selector (no CUDA call): the variant create would pick
+ * for desc, the tcgen05 tile width (128 x *tile_n output tile; 0 for the other kernels) on a
+ * GPU with num_sms SMs, and the prepacked weight row length *ktot (elements).  Any output
+ * pointer may be NULL.  Refusals are the same as create's. */
+convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, int* tile_n,
+                             int* ktot);
+
+/* Host-only weight prepack for a tcgen05 variant (CONVF_VARIANT_GEMM_1X1, _IMPLICIT_GEMM or
+ * _IMPLICIT_GEMM_GATHER): W [K][C][R][S] bf16 bits -> out [K][ktot] bf16 bits, reduction index
+ * (r*S + s)*Cp + c with Cp = C rounded up to 64 for the im2col variant (each tap's channel run
+ * is zero-padded) and Cp = C otherwise; the row tail is zero.  out_elems >= K*ktot. */
+convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const uint16_t* W,
+                                     uint16_t* out, size_t out_elems);
+
+/* Build a handle: validate, resolve pads, fold BN into the epilogue, prepack W for the
+ * selected kernel and upload it once (the only host->device crossing besides the launch).
+ *   W:       host, ONNX layout [K][C/group][R][S]; uint16 bf16 bits (CONVF_BF16) or int8.
+ *   bias:    host float[K] (bf16 path) or int32[K] (s8 path), or NULL (absent = 0).
+ *   bn_scale, bn_shift: host float[K] each (the folded BN affine, see conv_bn_scale_shift),
+ *            or NULL (identity).  Must be NULL on the s8 path.
+ *   requant_mult (int32[K], > 0), requant_shift (int32[K], 1..62), out_zero_point: s8 path
+ *            only (NULL / ignored on the bf16 path).
+ *   *out receives the handle (NULL on failure; partial allocations are released). */
+convf_status conv_fused_create(const convf_desc* desc, const void* W, const void* bias,
+                               const float* bn_scale, const float* bn_shift,
+                               const int32_t* requant_mult, const int32_t* requant_shift,
+                               int32_t out_zero_point, convf_handle** out);
+
+/* Run the fused conv: x (device, NHWC, bf16 bits or int8) -> y (device, NHWC, float32 for the
+ * bf16 path, int8 for the s8 path).  Both must be 16-byte aligned and must not overlap.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  Asynchronous: no allocation,
+ * no synchronisation; launch errors are returned as CONVF_ERR_CUDA. */
+convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream);
+
+/* Device status of the handle's previous runs, read after the caller synchronised the
+ * stream: CONVF_OK, or CONVF_ERR_TIMEOUT if a bounded wait ran out (the status is sticky
+ * until conv_fused_clear_status). */
+convf_status conv_fused_status(convf_handle* h);
+convf_status conv_fused_clear_status(convf_handle* h);
+
+/* Frees the handle's device memory.  The caller must have synchronised the stream. */
+void conv_fused_destroy(convf_handle* h);
+
+/* Selected kernel variant (convf_variant) of a handle, or a negative status. */
+int conv_fused_variant(const convf_handle* h);
+
+/* One-line description (variant, tile shape, grid) into buf[len]; returns the status. */
+convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len);
+
+/* Thread-local message for the last failing call on this thread ("" if none). */
+const char* conv_fused_last_error(void);
+
+/* Failure-detection self-test of the bounded device wait used by every kernel: launches one
+ * CTA that waits on an mbarrier nobody arrives at, with a budget of `budget_cycles` SM
+ * cycles, on `stream`.  *status_dev (device int32) receives CONVF_ERR_TIMEOUT's bit pattern
+ * (1) when the wait ran out.  No other effect. */
+convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles,
+                                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CONV_FUSED_H */

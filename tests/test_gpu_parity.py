@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element
+on the same seeded inputs.  bf16/fp32 paths: |y - ref| <= 1e-3 + 1e-3 |ref|; int8: bit-exact.
+Small cases compare every output (several tiles plus a ragged tail); the full-size workloads
+compare sampled outputs, always including the corners and edges of each output plane."""
+import numpy as np
+import pytest
+import torch
+
+import convolution_onnx_conv_gb300 as cf
+from convolution_onnx_conv_gb300 import synthetic, workloads
+from convolution_onnx_conv_gb300.workloads import ConvSpec, ACT_NONE, ACT_RELU, ACT_RELU6, ACT_CLIP
+
+from parity import check_full, check_sampled, inputs_for, make_conv, oracle_full, run_gpu, to_device_nhwc
+
+pytestmark = pytest.mark.gpu
+
+V = cf
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cf.load_library(build_if_missing=True)
+
+
+def _assert(res, spec, variant=None):
+    ok, worst, idx, status, used, desc = res[:6]
+    assert status == cf.CONVF_OK, (spec.name, status, desc)
+    if variant is not None:
+        assert used == variant, (spec.name, used, desc)
+    assert ok, f"{spec.name}: worst={worst} at flat index {idx} ({desc})"
+
+
+# ------------------------------------------------------------------ the single-conv config
+
+def test_single_conv_bias_relu():
+    spec = workloads.single_conv_relu()
+    _assert(check_full(spec, synthetic.seed_for(1, 0)), spec, V.CONVF_VARIANT_IMPLICIT_GEMM)
+
+
+# ------------------------------------------------------------------ small shapes, all outputs
+
+def S(name, N, C, H, W, K, R, S_, stride=(1, 1), pads=(0, 0, 0, 0), dil=(1, 1), group=1, act=ACT_RELU,
+      bias=False, bn=True, values="normal"):
+    return ConvSpec(name, N, C, H, W, K, R, S_, stride, pads, dil, group, act, bias, bn, "bf16", values)
+
+
+SMALL = [
+    # 1x1 GEMM mode: ragged M (3 tiles), C not a multiple of 64, K not a multiple of the tile
+    (S("g1x1_c72_k96", 2, 72, 13, 13, 96, 1, 1), V.CONVF_VARIANT_GEMM_1X1),
+    (S("g1x1_c64_k256", 2, 64, 12, 12, 256, 1, 1, act=ACT_NONE), V.CONVF_VARIANT_GEMM_1X1),
+    (S("g1x1_c16_k24", 3, 16, 11, 9, 24, 1, 1, act=ACT_RELU6, bias=True), V.CONVF_VARIANT_GEMM_1X1),
+    (S("g1x1_c256_k512", 1, 256, 14, 14, 512, 1, 1), V.CONVF_VARIANT_GEMM_1X1),
+    # TMA im2col
+    (S("i2c_3x3_s1", 2, 64, 15, 15, 64, 3, 3, pads=(1, 1, 1, 1)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_3x3_s2", 2, 64, 15, 15, 128, 3, 3, (2, 2), (1, 1, 1, 1)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_3x3_c72_ragged", 1, 72, 10, 13, 40, 3, 3, pads=(1, 1, 1, 1), bias=True),
+     V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_dil2_asym", 2, 16, 12, 11, 32, 3, 3, (1, 1), (2, 1, 0, 2), (2, 2)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_5x3_s2x1", 1, 8, 17, 9, 16, 5, 3, (2, 1), (2, 1, 2, 1)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_7x7_s2_c8", 2, 8, 23, 23, 64, 7, 7, (2, 2), (3, 3, 3, 3)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_1x1_s2", 2, 64, 14, 14, 128, 1, 1, (2, 2)), V.CONVF_VARIANT_IMPLICIT_GEMM),
+    (S("i2c_3x3_c256_k256", 1, 256, 9, 9, 256, 3, 3, pads=(1, 1, 1, 1), act=ACT_NONE),
+     V.CONVF_VARIANT_IMPLICIT_GEMM),
+    # thread-gathered rows (C not a multiple of 8)
+    (S("gat_stem_c3", 2, 3, 30, 30, 64, 7, 7, (2, 2), (3, 3, 3, 3)), V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
+    (S("gat_c5_3x3", 1, 5, 19, 21, 20, 3, 3, pads=(1, 1, 1, 1), bias=True), V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
+    # depthwise
+    (S("dw_s1_c32", 2, 32, 15, 15, 32, 3, 3, pads=(1, 1, 1, 1), group=32, act=ACT_RELU6), V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s2_c40", 2, 40, 17, 16, 40, 3, 3, (2, 2), (1, 1, 1, 1), group=40, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_5x5_dil2", 1, 16, 13, 13, 16, 5, 5, (1, 1), (4, 4, 4, 4), (2, 2), group=16, act=ACT_NONE, bias=True),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_3x3_s2_asym", 1, 24, 9, 12, 24, 3, 3, (2, 2), (0, 1, 1, 0), group=24), V.CONVF_VARIANT_DEPTHWISE),
+]
+
+
+@pytest.mark.parametrize("spec,variant", SMALL, ids=[s.name for s, _ in SMALL])
+def test_small_shapes_full(spec, variant):
+    _assert(check_full(spec, 7000 + SMALL.index((spec, variant))), spec, variant)
+
+
+@pytest.mark.parametrize("variant", [V.CONVF_VARIANT_IMPLICIT_GEMM, V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER])
+def test_same_shape_through_both_activation_loaders(variant):
+    spec = S("both_3x3", 2, 64, 12, 12, 64, 3, 3, pads=(1, 1, 1, 1), bias=True)
+    _assert(check_full(spec, 7100, variant), spec, variant)
+
+
+def test_1x1_forced_through_im2col_and_gather():
+    spec = S("one_by_one", 2, 64, 10, 10, 64, 1, 1)
+    for v in (V.CONVF_VARIANT_GEMM_1X1, V.CONVF_VARIANT_IMPLICIT_GEMM, V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER):
+        _assert(check_full(spec, 7200, v), spec, v)
+
+
+@pytest.mark.parametrize("act", [ACT_NONE, ACT_RELU, ACT_RELU6, ACT_CLIP])
+def test_activations(act):
+    spec = S("acts", 1, 64, 9, 9, 64, 3, 3, pads=(1, 1, 1, 1), act=act, values="uniform", bias=True, bn=False)
+    inp = inputs_for(spec, 7300)
+    inp["clip"] = (-0.5, 0.75)
+    _assert(check_full(spec, 7300, act=act, inp=inp), spec)
+    dw = S("acts_dw", 1, 64, 9, 9, 64, 3, 3, pads=(1, 1, 1, 1), group=64, act=act, values="uniform")
+    inp = inputs_for(dw, 7301)
+    inp["clip"] = (-0.5, 0.75)
+    _assert(check_full(dw, 7301, act=act, inp=inp), dw)
+
+
+def test_empty_batch_is_a_no_op():
+    spec = S("empty", 0, 64, 8, 8, 64, 3, 3, pads=(1, 1, 1, 1))
+    inp = inputs_for(S("e1", 1, 64, 8, 8, 64, 3, 3, pads=(1, 1, 1, 1)), 1)
+    conv = make_conv(spec, inp)
+    x = torch.empty((0, 64, 8, 8), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((0, 64, 8, 8), dtype=torch.float32, device="cuda")
+    cf.conv_fused_run(conv.handle, 0, 0)
+    cf.conv_fused_run(conv.handle, x.data_ptr(), y.data_ptr())
+    torch.cuda.synchronize()
+    assert conv.status() == cf.CONVF_OK
+    conv.close()
+
+
+def test_run_refuses_bad_pointers():
+    spec = S("ptrs", 1, 64, 8, 8, 64, 3, 3, pads=(1, 1, 1, 1))
+    conv = make_conv(spec, inputs_for(spec, 2))
+    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_run(conv.handle, p + 8, p + 65536)
+    assert "aligned" in str(e.value)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_run(conv.handle, p, p + 4096)
+    assert "overlap" in str(e.value)
+    conv.close()
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_run(conv.handle or 0, p, p + 65536)
+
+
+# ------------------------------------------------------------------ int8, bit-exact
+
+INT8_SMALL = [
+    ConvSpec("s8_3x3_s1", 2, 64, 12, 12, 64, 3, 3, (1, 1), (1, 1, 1, 1), act=ACT_RELU, has_bias=True,
+             has_bn=False, dtype="s8", values="int"),
+    ConvSpec("s8_3x3_s2_k80", 2, 128, 13, 13, 80, 3, 3, (2, 2), (1, 1, 1, 1), act=ACT_RELU, has_bias=True,
+             has_bn=False, dtype="s8", values="int"),
+    ConvSpec("s8_1x1_noact", 3, 64, 9, 11, 144, 1, 1, act=ACT_NONE, has_bias=True, has_bn=False, dtype="s8",
+             values="int"),
+    ConvSpec("s8_dil2_asym", 1, 64, 11, 10, 32, 3, 3, (1, 1), (2, 0, 1, 2), (2, 2), act=ACT_RELU,
+             has_bias=True, has_bn=False, dtype="s8", values="int"),
+]
+
+
+@pytest.mark.parametrize("spec", INT8_SMALL, ids=[s.name for s in INT8_SMALL])
+def test_int8_bit_exact(spec):
+    _assert(check_full(spec, 7400 + INT8_SMALL.index(spec)), spec, V.CONVF_VARIANT_INT8)
+
+
+def test_int8_zero_point_and_saturation():
+    spec = INT8_SMALL[0]
+    inp = inputs_for(spec, 7450)
+    inp["zp"] = -5
+    inp["mult"] = inp["mult"] * 0 + (1 << 30)   # scale 2^30 / 2^sh: many saturate at both ends
+    inp["shift"] = inp["shift"] * 0 + 38
+    _assert(check_full(spec, 7450, inp=inp), spec)
+    ref = oracle_full(spec, inp)
+    assert (ref == 127).any() and (ref == -5).any()
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled)
+
+def _sampled(spec, seed):
+    res = check_sampled(spec, seed)
+    _assert(res, spec)
+    y = res[6]
+    assert torch.isfinite(y).all() if y.dtype.is_floating_point else True
+
+
+@pytest.mark.parametrize("spec", workloads.bottleneck_1x1(32), ids=lambda s: s.name)
+def test_bottleneck_1x1_b32(spec):
+    _sampled(spec, synthetic.seed_for(2, workloads.bottleneck_1x1(32).index(spec)))
+
+
+RESNET = workloads.resnet50_layers(32) + workloads.resnet50_layers(1)
+
+
+@pytest.mark.parametrize("spec", RESNET, ids=lambda s: s.name)
+def test_resnet50_layers(spec):
+    _sampled(spec, synthetic.seed_for(3, RESNET.index(spec)))
+
+
+MBV2 = workloads.mobilenetv2_layers(64) + workloads.mobilenetv2_layers(1)
+
+
+@pytest.mark.parametrize("spec", MBV2, ids=lambda s: s.name)
+def test_mobilenetv2_layers(spec):
+    _sampled(spec, synthetic.seed_for(4, MBV2.index(spec)))
+
+
+INT8 = workloads.int8_layers(64)
+
+
+@pytest.mark.parametrize("spec", INT8, ids=lambda s: s.name)
+def test_int8_layers_b64(spec):
+    _sampled(spec, synthetic.seed_for(5, INT8.index(spec)))
+
+
+# ------------------------------------------------------------------ streams, reuse, failure detection
+
+def test_non_default_stream_after_a_producer():
+    """The two-stream race class: x is produced by a kernel on a side stream, and the conv
+    runs on that same stream right after it; the result must match the oracle exactly as
+    when the input was copied synchronously."""
+    spec = S("stream", 2, 64, 20, 20, 128, 3, 3, pads=(1, 1, 1, 1), act=ACT_NONE)
+    inp = inputs_for(spec, 7500)
+    conv = make_conv(spec, inp)
+    ref = oracle_full(spec, inp)
+    s = torch.cuda.Stream()
+    src = to_device_nhwc(inp["x"])
+    with torch.cuda.stream(s):
+        x = torch.empty_like(src)
+        torch.cuda._sleep(1000000)           # keep the stream busy so a race would show
+        x.copy_(src * 1.0)
+        y = conv(x)
+    s.synchronize()
+    from parity import compare
+    ok, worst, idx = compare(y.cpu().contiguous().numpy(), ref, False)
+    assert ok, worst
+    conv.close()
+
+
+def test_back_to_back_runs_reuse_buffers():
+    spec = S("reuse", 2, 64, 14, 14, 64, 3, 3, pads=(1, 1, 1, 1))
+    inp = inputs_for(spec, 7600)
+    y1, st1, _, _ = run_gpu(spec, inp, runs=1)
+    y5, st5, _, _ = run_gpu(spec, inp, runs=5)
+    assert st1 == st5 == cf.CONVF_OK
+    assert torch.equal(y1, y5)
+
+
+def test_watchdog_gives_up_and_reports():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cf.conv_fused_watchdog_selftest(status, 2_000_000)     # ~1 ms: nobody ever arrives
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    # the context is still usable afterwards
+    assert float((torch.ones(4, device="cuda") * 2).sum()) == 8.0

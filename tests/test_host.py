@@ -1,0 +1,182 @@
+"""Host-side tests of the C-ABI library (no GPU, no kernel launch): the shared library
+loads and exports every entry point the header declares; validation and refusal codes;
+auto_pad and output shapes; the BN affine; the selector; the weight prepack layout."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import convolution_onnx_conv_gb300 as cf
+from convolution_onnx_conv_gb300 import _build, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return cf.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "conv_fused.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:convf_status|void|int|const char\*)\s+(\w+)\s*\(", src,
+                                 flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(cf.EXPORTED) == names
+
+
+def desc(**kw):
+    base = dict(N=1, C=16, H=8, W=8, K=32, R=3, S=3, stride=(1, 1), pads=(1, 1, 1, 1))
+    base.update(kw)
+    return cf.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(C=0), cf.CONVF_ERR_INVALID_ARG, "C=0"),
+    (dict(N=-1), cf.CONVF_ERR_INVALID_ARG, "N=-1"),
+    (dict(stride=(0, 1)), cf.CONVF_ERR_INVALID_ARG, "strides"),
+    (dict(dilation=(1, 0)), cf.CONVF_ERR_INVALID_ARG, "dilations"),
+    (dict(pads=(-1, 0, 0, 0)), cf.CONVF_ERR_INVALID_ARG, "pads[0]"),
+    (dict(group=3), cf.CONVF_ERR_INVALID_ARG, "group=3"),
+    (dict(R=11, pads=(0, 0, 0, 0)), cf.CONVF_ERR_INVALID_ARG, "does not fit"),
+    (dict(auto_pad=7), cf.CONVF_ERR_INVALID_ARG, "auto_pad"),
+    (dict(layout=cf.CONVF_NCHW), cf.CONVF_ERR_UNSUPPORTED, "channels-last"),
+    (dict(act=9), cf.CONVF_ERR_INVALID_ARG, "act=9"),
+    (dict(act=cf.CONVF_ACT_CLIP, clip=(2.0, 1.0)), cf.CONVF_ERR_INVALID_ARG, "clip"),
+    (dict(group=2, K=32), cf.CONVF_ERR_UNSUPPORTED, "no kernel serves"),
+    (dict(C=12, K=12, group=12), cf.CONVF_ERR_UNSUPPORTED, "C % 8"),
+    (dict(K=30), cf.CONVF_ERR_UNSUPPORTED, "K % 4"),
+    (dict(dtype=cf.CONVF_S8, C=48), cf.CONVF_ERR_UNSUPPORTED, "C % 64"),
+    (dict(dtype=cf.CONVF_S8, C=64, act=cf.CONVF_ACT_RELU6), cf.CONVF_ERR_UNSUPPORTED, "int8"),
+    (dict(variant=cf.CONVF_VARIANT_GEMM_1X1), cf.CONVF_ERR_UNSUPPORTED, "forced variant"),
+    (dict(variant=cf.CONVF_VARIANT_DEPTHWISE), cf.CONVF_ERR_UNSUPPORTED, "group == C == K"),
+    (dict(variant=11), cf.CONVF_ERR_INVALID_ARG, "variant=11"),
+    (dict(N=1 << 14, H=1 << 10, W=1 << 10), cf.CONVF_ERR_UNSUPPORTED, "2^31"),
+])
+def test_refusals_name_the_offender(kw, status, needle):
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_plan(desc(**kw))
+    assert e.value.status == status
+    assert needle in str(e.value)
+
+
+def test_create_refuses_before_touching_the_gpu():
+    d = desc()
+    w = np.zeros((32, 16, 3, 3), np.uint16)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(d, None)
+    assert e.value.status == cf.CONVF_ERR_INVALID_ARG
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(d, w, bn_scale=np.ones(32, np.float32))
+    assert "together" in str(e.value)
+    s8 = desc(dtype=cf.CONVF_S8, C=64)
+    w8 = np.zeros((32, 64, 3, 3), np.int8)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(s8, w8)
+    assert "requant" in str(e.value)
+    bad_shift = np.zeros(32, np.int32)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(s8, w8, None, None, None, np.ones(32, np.int32), bad_shift)
+    assert "requant_shift[0]" in str(e.value)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(s8, w8, None, None, None, np.ones(32, np.int32), np.ones(32, np.int32), 300)
+    assert "out_zero_point" in str(e.value)
+
+
+def test_handle_checks(lib):
+    assert lib.conv_fused_run(None, None, None, None) == cf.CONVF_ERR_INVALID_ARG
+    assert lib.conv_fused_status(None) == cf.CONVF_ERR_INVALID_ARG
+    assert lib.conv_fused_variant(None) == cf.CONVF_ERR_INVALID_ARG
+    junk = (ctypes.c_uint32 * 64)()
+    assert lib.conv_fused_run(ctypes.addressof(junk), None, None, None) == cf.CONVF_ERR_INVALID_ARG
+    assert "not a convf handle" in cf.conv_fused_last_error()
+    lib.conv_fused_destroy(None)   # no-op
+
+
+@pytest.mark.parametrize("n_in,k,s,d,mode", [(5, 3, 2, 1, "SAME_UPPER"), (4, 3, 2, 1, "SAME_UPPER"),
+                                              (4, 3, 2, 1, "SAME_LOWER"), (224, 7, 2, 1, "SAME_LOWER"),
+                                              (6, 3, 1, 2, "SAME_UPPER"), (9, 4, 3, 1, "VALID"),
+                                              (9, 4, 3, 1, "NOTSET")])
+def test_auto_pad_and_output_shape(n_in, k, s, d, mode):
+    dsc = cf.make_desc(2, 8, n_in, n_in + 1, 16, k, k, (s, s), (1, 0, 2, 1), (d, d), auto_pad=mode)
+    pads = cf.conv_fused_resolve_pads(dsc)
+    if mode.startswith("SAME"):
+        total_h = max(0, (-(-n_in // s) - 1) * s + (k - 1) * d + 1 - n_in)
+        small = total_h // 2
+        want_h = (small, total_h - small) if mode == "SAME_UPPER" else (total_h - small, small)
+        assert (pads[0], pads[2]) == want_h
+    elif mode == "VALID":
+        assert pads == (0, 0, 0, 0)
+    else:
+        assert pads == (1, 0, 2, 1)
+    N, K, Ho, Wo = cf.conv_fused_output_shape(dsc)
+    assert (N, K) == (2, 16)
+    assert Ho == (n_in + pads[0] + pads[2] - d * (k - 1) - 1) // s + 1
+    assert Wo == (n_in + 1 + pads[1] + pads[3] - d * (k - 1) - 1) // s + 1
+
+
+def test_bn_scale_shift_matches_formula():
+    rng = np.random.default_rng(0)
+    K = 37
+    g, b = rng.uniform(0.5, 1.5, K), rng.normal(0, 0.1, K)
+    m, v = rng.normal(0, 0.1, K), rng.uniform(0.5, 1.5, K)
+    g, b, m, v = (a.astype(np.float32) for a in (g, b, m, v))
+    scale, shift = cf.conv_bn_scale_shift(g, b, m, v, 1e-5)
+    s64 = g.astype(np.float64) / np.sqrt(v.astype(np.float64) + np.float64(np.float32(1e-5)))
+    t64 = b.astype(np.float64) - m.astype(np.float64) * s64
+    assert np.array_equal(scale, s64.astype(np.float32))
+    assert np.array_equal(shift, t64.astype(np.float32))
+    with pytest.raises(cf.ConvFusedError):
+        cf.conv_bn_scale_shift(g, b, m, np.full(K, -1.0, np.float32), 1e-5)
+
+
+def test_selector_on_the_workloads():
+    names = {}
+    for spec in workloads.resnet50_layers(32) + workloads.mobilenetv2_layers(64) + workloads.int8_layers(64):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         spec.dilation, spec.group, cf.CONVF_S8 if spec.dtype == "s8" else cf.CONVF_BF16)
+        v, bn, kt = cf.conv_fused_plan(d)
+        names[spec.name] = v
+        if spec.dtype == "s8":
+            assert v == cf.CONVF_VARIANT_INT8
+        elif spec.group > 1:
+            assert v == cf.CONVF_VARIANT_DEPTHWISE
+        elif spec.C == 3:
+            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER and kt == 192 and bn in (32, 64, 128, 256)
+        elif spec.R == 1 and spec.stride == (1, 1):
+            assert v == cf.CONVF_VARIANT_GEMM_1X1 and kt == -(-spec.C // 64) * 64
+        else:
+            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM and kt == spec.R * spec.S * (-(-spec.C // 64) * 64)
+    assert len(names) == 53 + 50 + 7
+
+
+@pytest.mark.parametrize("variant,C,R,S", [(cf.CONVF_VARIANT_GEMM_1X1, 72, 1, 1),
+                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM, 72, 3, 3),
+                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 3, 7, 7),
+                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 24, 3, 2)])
+def test_weight_prepack_layout(variant, C, R, S):
+    K = 20
+    pad = (R // 2, S // 2, R // 2, S // 2)
+    d = cf.make_desc(1, C, 9, 9, K, R, S, (1, 1), pad, variant=variant)
+    _, _, kt = cf.conv_fused_plan(d)
+    rng = np.random.default_rng(1)
+    W = rng.integers(1, 1 << 15, (K, C, R, S)).astype(np.uint16)
+    out = np.full((K, kt), 7, np.uint16)
+    cf.conv_fused_pack_weights(d, variant, W, out)
+    cp = -(-C // 64) * 64 if variant == cf.CONVF_VARIANT_IMPLICIT_GEMM else C
+    want = np.zeros((K, kt), np.uint16)
+    for r in range(R):
+        for s in range(S):
+            want[:, (r * S + s) * cp:(r * S + s) * cp + C] = W[:, :, r, s]
+    assert np.array_equal(out, want)
+    assert kt % 64 == 0
