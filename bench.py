@@ -1,0 +1,439 @@
+"""Benchmark of the fused ONNX Conv path on GB300.
+
+A step is one pass of the ResNet-50 (v2) conv stack at batch 32: all 53 conv layers (7x7/2
+stem, 1x1 and 3x3 bottleneck convs, strided projections) with folded BN + ReLU, bf16 inputs,
+fp32 accumulation and output, each layer on its own resident input/output buffers (about
+2.2 GB per step, far larger than L2, so every layer reads its input from HBM).  `value` is
+the whole-job TFLOP/s (2*N*K*Ho*Wo*C*R*S per layer, padded taps included).  The same run
+also times the MobileNetV2 depthwise layers at batch 64 (GB/s against HBM) and the static
+int8 ResNet 3x3 layers at batch 64 (TOP/s), and reports them beside the headline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--layers-out F]
+
+For N > 1 it runs under torchrun as independent replicas (one per GPU, weak scaling); the
+only collectives are the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused conv TFLOP/s (ResNet-50 bs32, % bf16 peak); depthwise GB/s (% HBM)"
+WORKLOAD = ("ResNet-50 v2 conv stack, 53 layers (7x7/2 stem, 1x1 and 3x3 bottlenecks, strided "
+            "projections) at batch 32, 224x224 input, bf16 x/W, fp32 accumulate and output, "
+            "folded BN + ReLU epilogue, channels-last")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs") or d.get("hbm_GBs") or d["hbm"])
+        bf16 = float(d.get("bf16_tflops") or d["bf16"])
+        sus = float(d.get("bf16_tflops_sustained") or bf16)
+        return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": sus}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        self.sel = sel
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in self.samples:
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ workloads
+def build_layers(specs, seed_base, torch, cf, synthetic, s8=False):
+    """FusedConv handles + resident device inputs/outputs for each spec (plus host copies)."""
+    out = []
+    for i, spec in enumerate(specs):
+        seed = synthetic.seed_for(seed_base, i)
+        if s8:
+            inp = synthetic.int8_inputs(spec, seed)
+            conv = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                                stride=spec.stride, pads=spec.pads, act=spec.act, requant_mult=inp["mult"],
+                                requant_shift=inp["shift"])
+        else:
+            inp = synthetic.conv_inputs(spec, seed)
+            scale, shift = cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5) \
+                if inp["bn"] is not None else (None, None)
+            conv = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                                scale, shift, stride=spec.stride, pads=spec.pads, group=spec.group,
+                                act=spec.act)
+        x_host = inp["x"].contiguous(memory_format=torch.channels_last)
+        x = x_host.cuda()
+        y = conv.new_output()
+        out.append({"spec": spec, "conv": conv, "x": x, "y": y, "x_host": x_host, "inp": inp})
+    return out
+
+
+def capture_graph(layers, torch, reps=1):
+    """One CUDA graph that launches every layer of the sequence `reps` times, in order."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for L in layers:
+                L["conv"](L["x"], L["y"])
+    return g
+
+
+def time_graph(g, steps, torch):
+    """Device time of `steps` back-to-back replays (ms), events on the replay stream."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def time_launches(layers, steps, torch):
+    """Per-launch device durations: every launch of the sequence bracketed by CUDA events on
+    its stream; the stream is held by a sleep kernel while the host enqueues a step, so the
+    launches run back to back and the events time the kernels, not the host.  Returns the
+    summed ms per layer over `steps` passes."""
+    n = len(layers)
+    per = [0.0] * n
+    for _ in range(steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda._sleep(int(4e6 + 1e5 * n))
+        for i, L in enumerate(layers):
+            ev[i][0].record()
+            L["conv"](L["x"], L["y"])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        for i in range(n):
+            per[i] += ev[i][0].elapsed_time(ev[i][1])
+    return per
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+_ORACLE_CACHE = {}
+
+
+def _oracle_layer_inputs(spec, seed, synthetic):
+    """float64 inputs of one image of the layer (the sample's points all lie in image 0)."""
+    key = (spec.name, seed)
+    if key not in _ORACLE_CACHE:
+        one = spec.with_batch(1)
+        inp = synthetic.conv_inputs(one, seed)
+        bn = tuple(t.numpy() for t in inp["bn"]) if inp["bn"] is not None else None
+        _ORACLE_CACHE[key] = (one, inp["x"].double().numpy(), inp["w"].double().numpy(), bn)
+    return _ORACLE_CACHE[key]
+
+
+def oracle_sample(specs, budget_s, seed_base, synthetic):
+    """Times the CPU oracle (conv points -> BN -> activation, float64) on a bounded random
+    sample of output points of every layer (points of the first image; the per-point work is
+    the layer's C*R*S multiply-adds, as in the full batch).  Returns
+    (flop/s, seconds, points, threads, sampled fraction)."""
+    import oracle
+    total_flops = sum(s.flops for s in specs)
+    cal = next(s for s in specs if s.C * s.R * s.S >= 576)
+    one, x64, w64, bn = _oracle_layer_inputs(cal, 999, synthetic)
+    pts = synthetic.sample_points(one, 2000, 1).numpy()
+    t0 = time.perf_counter()
+    oracle.conv2d_points(x64, w64, None, cal.stride, cal.pads, cal.dilation, cal.group, pts)
+    dt = time.perf_counter() - t0
+    rate = pts.shape[0] * 2 * cal.C * cal.R * cal.S / max(dt, 1e-6)
+    frac = min(1.0, budget_s * rate / total_flops)
+    done_flops, secs, npts = 0, 0.0, 0
+    for i, spec in enumerate(specs):
+        ho, wo = spec.out_hw
+        count = max(16, int(spec.N * spec.K * ho * wo * frac))
+        one, x64, w64, bn = _oracle_layer_inputs(spec, synthetic.seed_for(seed_base, i), synthetic)
+        pts = synthetic.sample_points(one, count, i).numpy()
+        t0 = time.perf_counter()
+        oracle.conv_bn_act_points(x64, w64, None, bn, spec.act, spec.stride, spec.pads, spec.dilation,
+                                  spec.group, pts)
+        secs += time.perf_counter() - t0
+        done_flops += pts.shape[0] * 2 * (spec.C // spec.group) * spec.R * spec.S
+        npts += pts.shape[0]
+    return done_flops / secs, secs, npts, oracle.num_threads(), frac
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle as it stands, timed on this host's cores on bounded
+    samples of the same workload, reported in the same metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from convolution_onnx_conv_gb300 import synthetic, workloads
+    import oracle
+    specs = workloads.resnet50_layers(32)
+    per_step = 1.0      # seconds of oracle work per step
+    for _ in range(args.warmup):
+        oracle_sample(specs, per_step * 0.3, 3, synthetic)
+    rates, secs, flops_total, pts_total = [], 0.0, 0.0, 0
+    for _ in range(args.steps):
+        r, s, n, threads, frac = oracle_sample(specs, per_step, 3, synthetic)
+        rates.append(r)
+        secs += s
+        flops_total += r * s
+        pts_total += n
+    value = flops_total / secs / 1e12
+    sample = (f"random output points of all 53 layers (fraction {frac:.2e} of each layer's outputs, "
+              f"{pts_total} points over {args.steps} steps, drawn from one image per layer), float64 "
+              f"seven-loop oracle + BN + ReLU")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": 32, "sampled": True},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers-out", default=None, help="write per-layer results (JSONL) here")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import torch.distributed as dist
+    import convolution_onnx_conv_gb300 as cf
+    from convolution_onnx_conv_gb300 import synthetic, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    cf.load_library(build_if_missing=True)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    peaks, peak_src = load_peaks()
+    specs = workloads.resnet50_layers(32)
+    layers = build_layers(specs, 3, torch, cf, synthetic)
+    dw_specs = workloads.depthwise_layers(64)
+    dw_layers = build_layers(dw_specs, 4, torch, cf, synthetic)
+    s8_specs = workloads.int8_layers(64)
+    s8_layers = build_layers(s8_specs, 5, torch, cf, synthetic, s8=True)
+
+    for _ in range(args.warmup):
+        for L in layers + dw_layers + s8_layers:
+            L["conv"](L["x"], L["y"])
+    torch.cuda.synchronize()
+    g_r50 = capture_graph(layers, torch)
+    g_dw = capture_graph(dw_layers, torch)
+    g_s8 = capture_graph(s8_layers, torch)
+    for g in (g_r50, g_dw, g_s8):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.1)
+    barrier()
+    torch.cuda.synchronize()
+    total_ms = time_graph(g_r50, args.steps, torch)            # the timed region: K steps
+    torch.cuda.synchronize()
+    barrier()
+    per_layer = time_launches(layers, max(3, args.steps // 5), torch)
+    lsteps = max(3, args.steps // 5)
+    dw_steps = max(3, args.steps // 2)
+    dw_total = time_graph(g_dw, dw_steps, torch)
+    dw_per = time_launches(dw_layers, lsteps, torch)
+    s8_steps = max(3, args.steps // 5)
+    s8_total = time_graph(g_s8, s8_steps, torch)
+    s8_per = time_launches(s8_layers, lsteps, torch)
+    clocks = sampler.stop()
+
+    statuses = [L["conv"].status() for L in layers + dw_layers + s8_layers]
+    if any(s != 0 for s in statuses):
+        raise SystemExit(f"device status error: {statuses}")
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    flops_step = sum(s.flops for s in specs)
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # dominant kernel: the tcgen05 implicit-GEMM conv (every ResNet layer runs it)
+    tc_ms = sum(per_layer) / lsteps
+    achieved = flops_step / (tc_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+            "kernel": "tc_conv_kernel (tcgen05 implicit GEMM, all tile widths)",
+            "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside a long step)",
+            "per_launch_flops": flops_step / len(specs), "launch_ms": tc_ms / len(specs)}
+    idx17 = [i for i, s in enumerate(specs) if s.R > 1]
+    f17 = sum(specs[i].flops for i in idx17)
+    t17 = sum(per_layer[i] for i in idx17) / lsteps
+    tf17 = f17 / (t17 * 1e-3) / 1e12
+    dw_bytes = sum(s.algorithmic_bytes for s in dw_specs)
+    dw_ms = dw_total / dw_steps
+    dw_gbs = dw_bytes / (dw_ms * 1e-3) / 1e9
+    dw_kernel_gbs = dw_bytes / (sum(dw_per) / lsteps * 1e-3) / 1e9
+    s8_ops = sum(s.flops for s in s8_specs)
+    s8_ms = s8_total / s8_steps
+    s8_tops = s8_ops / (s8_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies inside the timing
+    e2e_steps = max(2, min(5, args.steps))
+    for L in layers:
+        L["x_pin"] = L["x_host"].pin_memory()
+        L["y_pin"] = torch.empty_strided(L["y"].shape, L["y"].stride(), dtype=L["y"].dtype, pin_memory=True)
+    h2d = sum(L["x"].numel() * L["x"].element_size() for L in layers)
+    d2h = sum(L["y"].numel() * L["y"].element_size() for L in layers)
+
+    def e2e_step():
+        for L in layers:
+            L["x"].copy_(L["x_pin"], non_blocking=True)
+            L["conv"](L["x"], L["y"])
+            L["y_pin"].copy_(L["y"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_val = world * flops_step * e2e_steps / (float(te.item()) * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, secs, npts, threads, frac = oracle_sample(specs, args.cpu_budget, 3, synthetic)
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{npts} random output points over all 53 layers (fraction {frac:.2e} of the "
+                         f"outputs, drawn from one image per layer), float64 seven-loop conv + BN + ReLU, "
+                         f"{secs:.1f} s"}
+
+    if args.layers_out and rank == 0:
+        with open(args.layers_out, "w") as f:
+            for s, L, ms in zip(specs, layers, per_layer):
+                ms /= lsteps
+                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
+                                    "tflops": s.flops / (ms * 1e-3) / 1e12,
+                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9,
+                                    "ai": s.flops / s.algorithmic_bytes}) + "\n")
+            for s, L, ms in zip(dw_specs, dw_layers, dw_per):
+                ms /= lsteps
+                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
+                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9}) + "\n")
+            for s, L, ms in zip(s8_specs, s8_layers, s8_per):
+                ms /= lsteps
+                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
+                                    "tops": s.flops / (ms * 1e-3) / 1e12}) + "\n")
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 32 * world, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2: 53 distinct resident input/output buffer pairs, "
+                             f"{(h2d + d2h) / 1e9:.2f} GB per step"},
+            "pct_bf16_peak": value / peaks["bf16_tflops"],
+            "implicit_gemm_3x3_7x7": {"layers": len(idx17), "tflops": tf17, "pct_bf16_peak": tf17 / peaks["bf16_tflops"]},
+            "depthwise": {"workload": "MobileNetV2 depthwise 3x3 layers (17) at batch 64, bf16 in, fp32 out",
+                          "gb_s": dw_gbs, "pct_hbm": dw_gbs / peaks["hbm_gbs"], "ms": dw_ms,
+                          "kernel_gb_s": dw_kernel_gbs},
+            "int8": {"workload": "ResNet-50 3x3 shapes (7) at batch 64, int8 in/out, int32 acc",
+                     "tops": s8_tops, "ms": s8_ms},
+            "peaks": {**peaks, "source": peak_src},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": len(specs) * args.steps,
+            "timing": "step = one CUDA-graph replay of the 53 conv launches; per-kernel durations from "
+                      "event pairs around each launch with the stream pre-queued",
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -145,6 +145,8 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
   if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
+  if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
+    return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
   return CONVF_OK;
 }
 
@@ -225,11 +227,12 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
 
 // Tile width for the tcgen05 kernels: minimise waves x per-tile time, where a K16 step of a
 // 128 x bn MMA costs max(bn/2, (A + B bytes)/128) cycles (tensor rate vs shared-memory reads).
-int pick_bn(long long M, int K, int num_sms) {
+int pick_bn(long long M, int K, int num_sms, int max_bn) {
   const long long mblocks = (M + 127) / 128;
-  int best = 256;
+  int best = max_bn;
   double best_cost = 1e300;
   for (int bn : {256, 128, 64, 32}) {
+    if (bn > max_bn) continue;
     if (bn > 32 && bn / 2 >= K) continue;  // no point in a tile twice as wide as K
     const long long tiles = mblocks * ((K + bn - 1) / bn);
     const long long waves = (tiles + num_sms - 1) / num_sms;
@@ -241,6 +244,33 @@ int pick_bn(long long M, int K, int num_sms) {
     }
   }
   return best;
+}
+
+// Gather variant: input rows one 128-pixel tile reads, staged whole in shared memory, when
+// tiles never straddle two images, rows are 16-byte multiples and the rows fit one 32 KB
+// buffer; 0 means the gatherers read global memory directly.
+int patch_rows_for(const Shape& s) {
+  const long long hw = (long long)s.Ho * s.Wo;
+  if (hw % 128 != 0) return 0;
+  const long long row_bytes = (long long)s.W * s.C * 2;
+  if (row_bytes % 16 != 0) return 0;
+  long long q = (127 + s.Wo - 1) / s.Wo + 1;   // output rows one tile can touch
+  if (q > s.Ho) q = s.Ho;
+  const long long rows = (q - 1) * s.sh + (long long)(s.R - 1) * s.dh + 1;
+  if (rows * row_bytes > 32768) return 0;
+  return (int)rows;
+}
+
+// Gather variant with at most 8 channels and staged rows: the reduction is laid out as whole
+// taps of cpt = 4 or 8 channels (zero-padded), assembled with one vector read per tap; 0 keeps
+// the channel-by-channel layout.
+int gather_cpt(const Shape& s) {
+  if (s.C > 8) return 0;
+  const int rows = patch_rows_for(s);
+  if (rows == 0) return 0;
+  const int cpt = s.C <= 4 ? 4 : 8;
+  if ((long long)rows * s.W * cpt * 2 > 32768) return 0;
+  return cpt;
 }
 
 // ------------------------------------------------------------------ driver entry points
@@ -297,7 +327,7 @@ struct convf_handle {
   int32_t zp;
   float lo, hi;
   // tcgen05 configuration
-  int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks;
+  int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
   CUtensorMap tmB;
   CUtensorMap tmA, tmY;
   const void* map_x;
@@ -322,29 +352,31 @@ void act_bounds(const convf_desc* d, float* lo, float* hi) {
   }
 }
 
-// Prepacked weight row length (elements) for the tcgen05 variants.
-void tc_layout(int variant, const Shape& s, int* a_mode, int* cblocks, int* ktot) {
+// Prepacked weight layout for the tcgen05 variants: row length ktot (elements) and the
+// channel stride cpad of each tap's run inside a row.
+void tc_layout(int variant, const Shape& s, int* a_mode, int* cblocks, int* ktot, int* cpad) {
   if (variant == CONVF_VARIANT_GEMM_1X1) {
     *a_mode = kA2D;
     *cblocks = (s.C + 63) / 64;
     *ktot = *cblocks * 64;
+    *cpad = *ktot;
   } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM) {
     *a_mode = kAIm2col;
     *cblocks = (s.C + 63) / 64;
-    *ktot = s.R * s.S * *cblocks * 64;
+    *cpad = *cblocks * 64;
+    *ktot = s.R * s.S * *cpad;
   } else {
     *a_mode = kAGather;
     *cblocks = 0;
-    *ktot = (int)align_up((size_t)s.R * s.S * s.C, 64);
+    const int cpt = gather_cpt(s);
+    *cpad = cpt ? cpt : s.C;
+    *ktot = (int)align_up((size_t)s.R * s.S * *cpad, 64);
   }
 }
 
-// W[K][C][R][S] (bf16 bits) -> [K][ktot]: reduction index (tap, channel) with the channel
-// fastest; im2col mode pads every tap's channel run to a multiple of 64, the other modes pad
-// only the end of the row.
-void pack_bf16(const uint16_t* W, const Shape& s, int a_mode, int ktot, uint16_t* out) {
+// W[K][C][R][S] (bf16 bits) -> [K][ktot]: reduction index (r*S + s)*cpad + c, zero elsewhere.
+void pack_bf16(const uint16_t* W, const Shape& s, int cpad, int ktot, uint16_t* out) {
   std::memset(out, 0, sizeof(uint16_t) * (size_t)s.K * ktot);
-  const int cpad = a_mode == kAIm2col ? (s.C + 63) / 64 * 64 : s.C;
   for (int k = 0; k < s.K; ++k)
     for (int c = 0; c < s.C; ++c)
       for (int r = 0; r < s.R; ++r)
@@ -413,9 +445,12 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
   if (variant) *variant = v;
   int bn = 0, kt = 0;
   if (v == CONVF_VARIANT_GEMM_1X1 || v == CONVF_VARIANT_IMPLICIT_GEMM || v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
-    int am, cb;
-    tc_layout(v, s, &am, &cb, &kt);
-    bn = pick_bn(s.M, s.K, num_sms > 0 ? num_sms : 1);
+    int am, cb, cp;
+    tc_layout(v, s, &am, &cb, &kt, &cp);
+    const int max_bn = v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? 128 : 256;
+    if (desc->tile_n > max_bn)
+      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d exceeds %d for the gather variant", desc->tile_n, max_bn);
+    bn = desc->tile_n ? desc->tile_n : pick_bn(s.M, s.K, num_sms > 0 ? num_sms : 1, max_bn);
   } else if (v == CONVF_VARIANT_INT8) {
     kt = s.R * s.S * s.C;
   }
@@ -435,11 +470,11 @@ convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const 
       variant != CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
     return fail(CONVF_ERR_INVALID_ARG, "variant %d has no bf16 GEMM packing", variant);
   if (desc->group != 1) return fail(CONVF_ERR_UNSUPPORTED, "GEMM packing needs group == 1");
-  int am, cb, kt;
-  tc_layout(variant, s, &am, &cb, &kt);
+  int am, cb, kt, cp;
+  tc_layout(variant, s, &am, &cb, &kt, &cp);
   if (out_elems < (size_t)s.K * kt) return fail(CONVF_ERR_INVALID_ARG, "out holds %zu < %zu elements", out_elems,
                                                 (size_t)s.K * kt);
-  pack_bf16(W, s, am, kt, out);
+  pack_bf16(W, s, cp, kt, out);
   return ok();
 }
 
@@ -532,9 +567,10 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     o_qm = carve((size_t)s.K * 4);
     o_qs = carve((size_t)s.K * 4);
   } else {
-    tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot);
+    int cpad = 0;
+    tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot, &cpad);
     wpack.resize((size_t)s.K * h->ktot);
-    pack_bf16(static_cast<const uint16_t*>(W), s, h->a_mode, h->ktot, wpack.data());
+    pack_bf16(static_cast<const uint16_t*>(W), s, cpad, h->ktot, wpack.data());
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
@@ -594,7 +630,16 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       delete h;
       return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled/Im2col are unavailable from the driver");
     }
-    h->bn = pick_bn(s.M, s.K, h->num_sms);
+    const int max_bn = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? 128 : 256;
+    if (desc->tile_n > max_bn) {
+      cudaFree(h->dev);
+      delete h;
+      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d exceeds %d for the gather variant", desc->tile_n, max_bn);
+    }
+    h->bn = desc->tile_n ? desc->tile_n : pick_bn(s.M, s.K, h->num_sms, max_bn);
+    h->patch_rows = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? patch_rows_for(s) : 0;
+    h->cpt = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? gather_cpt(s) : 0;
+    h->row_bytes = s.W * s.C * 2;
     h->num_kb = h->ktot / 64;
     h->n_blocks = (s.K + h->bn - 1) / h->bn;
     const long long tiles = (s.M + 127) / 128 * h->n_blocks;
@@ -706,6 +751,7 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.H = s.H; p.W = s.W; p.C = s.C; p.Ho = s.Ho; p.Wo = s.Wo;
       p.n_blocks = h->n_blocks; p.num_tiles = h->num_tiles; p.a_mode = h->a_mode;
       p.scale = h->scale; p.bias = h->bias; p.x = static_cast<const uint16_t*>(x);
+      p.patch_rows = h->patch_rows; p.row_bytes = h->row_bytes; p.cpt = h->cpt;
       p.lo = h->lo; p.hi = h->hi; p.status = h->status;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
@@ -763,9 +809,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
   else
     snprintf(buf, len,
-             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d tiles=%d grid=%d weight_bytes=%zu",
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d tiles=%d grid=%d "
+             "patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->bn, h->num_kb, h->num_tiles, h->grid,
-             h->dev_bytes);
+             h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
 }
 

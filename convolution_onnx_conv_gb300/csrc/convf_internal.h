@@ -32,6 +32,9 @@ struct TcConvParams {
   const float* scale;     // [Kpad] per-channel epilogue scale (BN scale)
   const float* bias;      // [Kpad] per-channel epilogue bias (scale*B + shift)
   const uint16_t* x;      // NHWC bf16 input (gather mode)
+  int patch_rows;         // gather mode: input rows staged per tile in smem (0 = read global)
+  int row_bytes;          // W*C*2, bytes of one input row
+  int cpt;                // gather mode: channels per tap in the reduction layout (4, 8; 0 = C)
   float lo, hi;           // activation clamp
   int* status;            // device status word
 };

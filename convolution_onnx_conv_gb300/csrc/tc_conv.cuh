@@ -25,15 +25,19 @@ constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kEpiCols = 32;
 constexpr int kEpiTileBytes = kBM * kEpiCols * 4;
 constexpr int kNumEpiBuf = 2;
+constexpr int kPatchBufBytes = 32768;
 
-template <int BN>
+template <int BN, bool GATHER>
 struct TcCfg {
   static constexpr int kBTileBytes = BN * kBK * 2;
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem =
-      1024 + kStages * (kATileBytes + kBTileBytes) + kNumEpiBuf * kEpiTileBytes + kBarBytes;
+  // gather mode: two buffers for the raw input rows one tile needs (TcConvParams::patch_rows)
+  // plus one buffer holding them with channels padded to whole taps (TcConvParams::cpt)
+  static constexpr int kPatchBytes = GATHER ? 3 * kPatchBufBytes : 0;
+  static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + kNumEpiBuf * kEpiTileBytes +
+                               kPatchBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
 };
@@ -42,7 +46,7 @@ template <int BN, bool GATHER>
 __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, GATHER>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -50,12 +54,15 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATileBytes;
   uint8_t* sEpi = sB + kStages * Cfg::kBTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kNumEpiBuf * kEpiTileBytes);
+  uint8_t* sPatch = sEpi + kNumEpiBuf * kEpiTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sPatch + Cfg::kPatchBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = bars + 2 * kStages + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  uint64_t* pfull = bars + 2 * kStages + 4;    // input-row patch landed (gather mode)
+  uint64_t* pempty = bars + 2 * kStages + 6;   // input-row patch consumed (gather mode)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // go/abort decisions broadcast by a leader thread through a named barrier; two slots used
   // alternately so the leader never overwrites a flag another thread has yet to read
@@ -73,6 +80,8 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 128);
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -97,9 +106,27 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
       int stage = 0;
       uint32_t phase = 0;
       const uint32_t tx = Cfg::kBTileBytes + (GATHER ? 0 : kATileBytes);
-      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
         const int m0 = (tile / p.n_blocks) * kBM;
         const int n0 = (tile % p.n_blocks) * BN;
+        if (GATHER && p.patch_rows > 0) {
+          // bulk-copy the input rows this tile reads (whole rows of W*C bf16) into smem
+          const int pb = it & 1;
+          if (!mbar_wait(&pempty[pb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) goto teardown;
+          const int hw = p.Ho * p.Wo;
+          const int img = m0 / hw;
+          const int ih_first = ((m0 - img * hw) / p.Wo) * p.sh - p.pt;
+          int valid = 0;
+          for (int i = 0; i < p.patch_rows; ++i) valid += (ih_first + i >= 0 && ih_first + i < p.H);
+          mbar_arrive_expect_tx(&pfull[pb], static_cast<uint32_t>(valid * p.row_bytes));
+          for (int i = 0; i < p.patch_rows; ++i) {
+            const int ih = ih_first + i;
+            if (ih >= 0 && ih < p.H)
+              bulk_load(sPatch + pb * kPatchBufBytes + i * p.row_bytes,
+                        p.x + (static_cast<size_t>(img) * p.H + ih) * p.W * p.C, p.row_bytes, &pfull[pb]);
+          }
+        }
         int img = 0, hb = 0, wb = 0;
         if (p.a_mode == kAIm2col) {
           const int hw = p.Ho * p.Wo;
@@ -238,12 +265,18 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
     if (et == 0) bulk_wait_all();
   } else if (GATHER) {
     // ------------------------------------------------------------------ row gatherers
+    // Reduction index j = (r*S + s)*C + c (channel fastest).  With p.patch_rows > 0 the rows
+    // are assembled from the tile's input rows staged in shared memory by the producer;
+    // otherwise they are read from global memory directly.
     const int gt = threadIdx.x - 192;      // tile row 0..127
     int stage = 0;
     uint32_t phase = 0;
+    int gi = 0;                            // broadcast counter (selects the go slot)
     const int hw = p.Ho * p.Wo;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-      const int m = (tile / p.n_blocks) * kBM + gt;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      const int m0 = (tile / p.n_blocks) * kBM;
+      const int m = m0 + gt;
       const bool row_ok = m < p.M;
       const int img = row_ok ? m / hw : 0;
       const int rem = m - img * hw;
@@ -251,38 +284,114 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
       const int ow = rem - oh * p.Wo;
       const int ih0 = oh * p.sh - p.pt;
       const int iw0 = ow * p.sw - p.pl;
-      const uint16_t* xn = p.x + static_cast<size_t>(img) * p.H * p.W * p.C;
-      int c = 0, s = 0, r = 0;   // decomposition of the reduction index, channel fastest
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (gt == 0) gat_go[kb & 1] = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
-        named_barrier(2, 128);
-        if (!gat_go[kb & 1]) goto teardown;
-        uint8_t* dst = sA + stage * kATileBytes + gt * 128;
-#pragma unroll 1
-        for (int c16 = 0; c16 < 8; ++c16) {
-          uint32_t pk[4];
+      const bool use_patch = p.patch_rows > 0;
+      const int pb = it & 1;
+      int ih_first = 0;
+      const uint16_t* src;
+      if (use_patch) {
+        if (gt == 0) gat_go[gi & 1] = mbar_wait(&pfull[pb], (it >> 1) & 1, abort_flag, p.status) ? 1 : 0;
+        named_barrier(2, 128);             // also: every thread has finished the previous tile
+        if (!gat_go[gi & 1]) goto teardown;
+        ++gi;
+        const int img0 = m0 / hw;
+        ih_first = ((m0 - img0 * hw) / p.Wo) * p.sh - p.pt;
+        src = reinterpret_cast<const uint16_t*>(sPatch + pb * kPatchBufBytes);
+        if (p.cpt > 0) {
+          // repack the raw rows (C channels per pixel) into whole taps of cpt channels
+          const uint16_t* raw = src;
+          uint16_t* tp = reinterpret_cast<uint16_t*>(sPatch + 2 * kPatchBufBytes);
+          const int pixels = p.patch_rows * p.W;
+          for (int px = gt; px < pixels; px += 128) {
+            uint16_t v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            uint32_t val = 0;
-            if (row_ok && r < p.R) {
-              const int ih = ih0 + r * p.dh;
-              const int iw = iw0 + s * p.dw;
-              if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
-                val = __ldg(xn + (static_cast<size_t>(ih) * p.W + iw) * p.C + c);
+            for (int c2 = 0; c2 < 8; ++c2) v[c2] = c2 < p.C ? raw[px * p.C + c2] : 0;
+            if (p.cpt == 4) {
+              *reinterpret_cast<uint2*>(tp + px * 4) =
+                  make_uint2(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16));
+            } else {
+              *reinterpret_cast<uint4*>(tp + px * 8) =
+                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
             }
-            if (e & 1)
-              pk[e >> 1] |= val << 16;
-            else
-              pk[e >> 1] = val;
-            if (++c == p.C) {
-              c = 0;
+          }
+          named_barrier(2, 128);           // repack complete: the raw buffer can be refilled
+          if (gt == 0) mbar_arrive(&pempty[pb]);
+          src = tp;
+        }
+      } else {
+        src = p.x + static_cast<size_t>(img) * p.H * p.W * p.C;
+      }
+      int c = 0, s = 0, r = 0;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (gt == 0) gat_go[gi & 1] = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
+        named_barrier(2, 128);
+        if (!gat_go[gi & 1]) goto teardown;
+        ++gi;
+        uint8_t* dst = sA + stage * kATileBytes + gt * 128;
+        if (p.cpt > 0) {
+          // whole taps: reduction index j = tap*cpt + channel; one 8- or 16-byte read per tap
+#pragma unroll 1
+          for (int c16 = 0; c16 < 8; ++c16) {
+            uint4 out = make_uint4(0, 0, 0, 0);
+            const int per = p.cpt == 4 ? 2 : 1;
+            for (int t = 0; t < per; ++t) {
+              uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
+              if (row_ok && r < p.R) {
+                const int ih = ih0 + r * p.dh;
+                const int iw = iw0 + s * p.dw;
+                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
+                  const uint16_t* q = src + ((ih - ih_first) * p.W + iw) * p.cpt;
+                  if (p.cpt == 4) {
+                    lo = *reinterpret_cast<const uint2*>(q);
+                  } else {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(q);
+                    lo = make_uint2(w4.x, w4.y);
+                    hi = make_uint2(w4.z, w4.w);
+                  }
+                }
+              }
+              if (p.cpt == 4) {
+                if (t == 0) { out.x = lo.x; out.y = lo.y; } else { out.z = lo.x; out.w = lo.y; }
+              } else {
+                out = make_uint4(lo.x, lo.y, hi.x, hi.y);
+              }
               if (++s == p.S) {
                 s = 0;
                 ++r;
               }
             }
+            *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = out;
           }
-          *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        } else {
+#pragma unroll 1
+          for (int c16 = 0; c16 < 8; ++c16) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              uint32_t val = 0;
+              if (row_ok && r < p.R) {
+                const int ih = ih0 + r * p.dh;
+                const int iw = iw0 + s * p.dw;
+                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
+                  const int row = use_patch ? ih - ih_first : ih;
+                  val = use_patch ? src[(row * p.W + iw) * p.C + c]
+                                  : __ldg(src + (static_cast<size_t>(row) * p.W + iw) * p.C + c);
+                }
+              }
+              if (e & 1)
+                pk[e >> 1] |= val << 16;
+              else
+                pk[e >> 1] = val;
+              if (++c == p.C) {
+                c = 0;
+                if (++s == p.S) {
+                  s = 0;
+                  ++r;
+                }
+              }
+            }
+            *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
         fence_proxy_async_smem();
         mbar_arrive(&full[stage]);
@@ -290,6 +399,10 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
           stage = 0;
           phase ^= 1;
         }
+      }
+      if (use_patch && p.cpt == 0) {
+        named_barrier(2, 128);             // every row of this tile has been assembled
+        if (gt == 0) mbar_arrive(&pempty[pb]);
       }
     }
   }
@@ -315,11 +428,11 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
   auto* k = tc_conv_kernel<BN, GATHER>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<BN>::kSmem);
+                                         TcCfg<BN, GATHER>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, GATHER ? 320 : 192, TcCfg<BN>::kSmem, stream>>>(p, tmA, tmB, tmY);
+  k<<<grid, GATHER ? 320 : 192, TcCfg<BN, GATHER>::kSmem, stream>>>(p, tmA, tmB, tmY);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,13 @@ namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
                                                    const CUtensorMap& tmB, const CUtensorMap& tmY, int grid,
                                                    bool gather, cudaStream_t stream) {
+#if CONVF_BN == 256
+  // gather mode needs room for the input-row patch: tile widths up to 128 only
+  if (gather) return cudaErrorInvalidValue;
+  return launch_tc_conv_t<CONVF_BN, false>(p, tmA, tmB, tmY, grid, stream);
+#else
   return gather ? launch_tc_conv_t<CONVF_BN, true>(p, tmA, tmB, tmY, grid, stream)
                 : launch_tc_conv_t<CONVF_BN, false>(p, tmA, tmB, tmY, grid, stream);
+#endif
 }
 }  // namespace convf

@@ -98,6 +98,7 @@ typedef struct {
   int act;                 /* convf_act                                                       */
   float clip_lo, clip_hi;  /* bounds for CONVF_ACT_CLIP (lo <= hi)                            */
   int variant;             /* convf_variant; 0 = selector                                     */
+  int tile_n;              /* tcgen05 variants: output-channel tile width 32/64/128/256, 0 = auto */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;
@@ -127,7 +128,10 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
 /* Host-only weight prepack for a tcgen05 variant (CONVF_VARIANT_GEMM_1X1, _IMPLICIT_GEMM or
  * _IMPLICIT_GEMM_GATHER): W [K][C][R][S] bf16 bits -> out [K][ktot] bf16 bits, reduction index
  * (r*S + s)*Cp + c with Cp = C rounded up to 64 for the im2col variant (each tap's channel run
- * is zero-padded) and Cp = C otherwise; the row tail is zero.  out_elems >= K*ktot. */
+ * is zero-padded); for the gather variant Cp = 4 (C <= 4) or 8 (C <= 8) when a tile's input rows
+ * can be staged in shared memory (N*Ho*Wo tiles of 128 never straddle images, W*C*2 is a
+ * multiple of 16 and the rows fit 32 KB), else Cp = C; the row tail is zero.
+ * out_elems >= K*ktot. */
 convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const uint16_t* W,
                                      uint16_t* out, size_t out_elems);
 

@@ -66,6 +66,10 @@ SMALL = [
     # thread-gathered rows (C not a multiple of 8)
     (S("gat_stem_c3", 2, 3, 30, 30, 64, 7, 7, (2, 2), (3, 3, 3, 3)), V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
     (S("gat_c5_3x3", 1, 5, 19, 21, 20, 3, 3, pads=(1, 1, 1, 1), bias=True), V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
+    # gathered rows assembled from input rows staged in shared memory (tiles within one image)
+    (S("gat_patch_c3_7x7", 2, 3, 32, 32, 64, 7, 7, (2, 2), (3, 3, 3, 3)), V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
+    (S("gat_patch_c6_3x3", 3, 6, 16, 16, 32, 3, 3, pads=(1, 1, 1, 1), bias=True),
+     V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER),
     # depthwise
     (S("dw_s1_c32", 2, 32, 15, 15, 32, 3, 3, pads=(1, 1, 1, 1), group=32, act=ACT_RELU6), V.CONVF_VARIANT_DEPTHWISE),
     (S("dw_s2_c40", 2, 40, 17, 16, 40, 3, 3, (2, 2), (1, 1, 1, 1), group=40, act=ACT_RELU6),
@@ -85,6 +89,23 @@ def test_small_shapes_full(spec, variant):
 def test_same_shape_through_both_activation_loaders(variant):
     spec = S("both_3x3", 2, 64, 12, 12, 64, 3, 3, pads=(1, 1, 1, 1), bias=True)
     _assert(check_full(spec, 7100, variant), spec, variant)
+
+
+@pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
+def test_every_tile_width(tile_n):
+    spec = S(f"tiles{tile_n}", 2, 64, 17, 17, 200, 3, 3, pads=(1, 1, 1, 1), bias=True)
+    inp = inputs_for(spec, 7150)
+    from parity import compare
+    c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                     *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                     pads=spec.pads, act=spec.act, tile_n=tile_n)
+    assert f"tile=128x{tile_n}" in c.describe()
+    y = c(to_device_nhwc(inp["x"]))
+    torch.cuda.synchronize()
+    assert c.status() == cf.CONVF_OK
+    ok, worst, idx = compare(y.cpu().contiguous().numpy(), oracle_full(spec, inp), False)
+    c.close()
+    assert ok, (worst, idx)
 
 
 def test_1x1_forced_through_im2col_and_gather():

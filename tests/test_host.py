@@ -152,7 +152,8 @@ def test_selector_on_the_workloads():
         elif spec.group > 1:
             assert v == cf.CONVF_VARIANT_DEPTHWISE
         elif spec.C == 3:
-            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER and kt == 192 and bn in (32, 64, 128, 256)
+            # 3 channels padded to whole taps of 4: 49 taps x 4 = 196 -> 256
+            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER and kt == 256 and bn in (32, 64, 128)
         elif spec.R == 1 and spec.stride == (1, 1):
             assert v == cf.CONVF_VARIANT_GEMM_1X1 and kt == -(-spec.C // 64) * 64
         else:
@@ -160,20 +161,24 @@ def test_selector_on_the_workloads():
     assert len(names) == 53 + 50 + 7
 
 
-@pytest.mark.parametrize("variant,C,R,S", [(cf.CONVF_VARIANT_GEMM_1X1, 72, 1, 1),
-                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM, 72, 3, 3),
-                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 3, 7, 7),
-                                           (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 24, 3, 2)])
-def test_weight_prepack_layout(variant, C, R, S):
+@pytest.mark.parametrize("variant,C,R,S,HW,cp", [(cf.CONVF_VARIANT_GEMM_1X1, 72, 1, 1, 9, 128),
+                                                 (cf.CONVF_VARIANT_IMPLICIT_GEMM, 72, 3, 3, 9, 128),
+                                                 (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 3, 7, 7, 9, 3),
+                                                 (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 24, 3, 2, 9, 24),
+                                                 # 16x16 outputs: tiles stay inside one image, rows
+                                                 # staged in smem -> whole taps of 4 / 8 channels
+                                                 (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 3, 3, 3, 16, 4),
+                                                 (cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER, 6, 3, 3, 16, 8)])
+def test_weight_prepack_layout(variant, C, R, S, HW, cp):
     K = 20
     pad = (R // 2, S // 2, R // 2, S // 2)
-    d = cf.make_desc(1, C, 9, 9, K, R, S, (1, 1), pad, variant=variant)
+    d = cf.make_desc(1, C, HW, HW, K, R, S, (1, 1), pad, variant=variant)
     _, _, kt = cf.conv_fused_plan(d)
+    assert kt == -(-(R * S * cp) // 64) * 64
     rng = np.random.default_rng(1)
     W = rng.integers(1, 1 << 15, (K, C, R, S)).astype(np.uint16)
     out = np.full((K, kt), 7, np.uint16)
     cf.conv_fused_pack_weights(d, variant, W, out)
-    cp = -(-C // 64) * 64 if variant == cf.CONVF_VARIANT_IMPLICIT_GEMM else C
     want = np.zeros((K, kt), np.uint16)
     for r in range(R):
         for s in range(S):
