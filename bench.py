@@ -250,6 +250,27 @@ def reference_arm(args):
     print(json.dumps(line))
 
 
+def profile_layers(which):
+    import torch
+    import convolution_onnx_conv_gb300 as cf
+    from convolution_onnx_conv_gb300 import synthetic, workloads
+    cf.load_library(build_if_missing=True)
+    kind, idx = which.split(":")
+    idx = [int(i) for i in idx.split(",")]
+    table = {"r50": (workloads.resnet50_layers(32), 3, False), "dw": (workloads.depthwise_layers(64), 4, False),
+             "s8": (workloads.int8_layers(64), 5, True)}
+    specs, base, s8 = table[kind]
+    layers = build_layers([specs[i] for i in idx], base, torch, cf, synthetic, s8=s8)
+    for _ in range(2):
+        for L in layers:
+            L["conv"](L["x"], L["y"])
+    torch.cuda.synchronize()
+    for L in layers:
+        L["conv"](L["x"], L["y"])
+        torch.cuda.synchronize()
+        print(L["spec"].name, L["conv"].describe())
+
+
 # ------------------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -260,9 +281,14 @@ def main():
     ap.add_argument("--layers-out", default=None, help="write per-layer results (JSONL) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--profile", default=None,
+                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I' or 's8:I' runs those "
+                         "layers twice (warm-up) and then once more each, printing their kernel descriptions")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile:
+        return profile_layers(args.profile)
     args.warmup = max(args.warmup, 3)
 
     import torch

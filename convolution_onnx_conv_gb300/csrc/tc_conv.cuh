@@ -11,7 +11,7 @@
 //               fp32 accumulator (2 x BN TMEM columns)
 //   warps 2-5   epilogue: tcgen05.ld -> y = clamp(scale[k]*acc + bias[k], lo, hi) -> swizzled
 //               smem staging -> TMA store (clips the ragged M and K edges)
-//   warps 6-9   (gather mode only) activation rows gathered by threads, for channel counts
+//   warps 6-13  (gather mode only) activation rows gathered by threads, for channel counts
 //               that TMA cannot address (C not a multiple of 8, e.g. a 3-channel stem)
 #pragma once
 #include "convf_internal.h"
@@ -26,6 +26,7 @@ constexpr int kEpiCols = 32;
 constexpr int kEpiTileBytes = kBM * kEpiCols * 4;
 constexpr int kNumEpiBuf = 2;
 constexpr int kPatchBufBytes = 32768;
+constexpr int kGatherThreads = 256;
 
 template <int BN, bool GATHER>
 struct TcCfg {
@@ -43,7 +44,7 @@ struct TcCfg {
 };
 
 template <int BN, bool GATHER>
-__global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
+__global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
   using Cfg = TcCfg<BN, GATHER>;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], GATHER ? 1 + 128 : 1);
+      mbar_init(&full[s], GATHER ? 1 + kGatherThreads : 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -265,18 +266,23 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
     if (et == 0) bulk_wait_all();
   } else if (GATHER) {
     // ------------------------------------------------------------------ row gatherers
-    // Reduction index j = (r*S + s)*C + c (channel fastest).  With p.patch_rows > 0 the rows
-    // are assembled from the tile's input rows staged in shared memory by the producer;
-    // otherwise they are read from global memory directly.
-    const int gt = threadIdx.x - 192;      // tile row 0..127
+    // 256 threads, two per tile row: thread gt assembles half gh of row gr in every k-block
+    // (16-byte chunks 4*gh .. 4*gh+3 of the row's 128 bytes).  Reduction index
+    // j = (r*S + s)*Cp + c.  With p.patch_rows > 0 the rows come from the tile's input rows that
+    // the producer bulk-copied into smem (repacked into whole taps of cpt channels when
+    // cpt > 0); otherwise they are read from global memory.
+    const int gt = threadIdx.x - 192;
+    const int gr = gt & 127;
+    const int gh = gt >> 7;
     int stage = 0;
     uint32_t phase = 0;
     int gi = 0;                            // broadcast counter (selects the go slot)
     const int hw = p.Ho * p.Wo;
+    const bool use_patch = p.patch_rows > 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
       const int m0 = (tile / p.n_blocks) * kBM;
-      const int m = m0 + gt;
+      const int m = m0 + gr;
       const bool row_ok = m < p.M;
       const int img = row_ok ? m / hw : 0;
       const int rem = m - img * hw;
@@ -284,13 +290,12 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
       const int ow = rem - oh * p.Wo;
       const int ih0 = oh * p.sh - p.pt;
       const int iw0 = ow * p.sw - p.pl;
-      const bool use_patch = p.patch_rows > 0;
       const int pb = it & 1;
       int ih_first = 0;
       const uint16_t* src;
       if (use_patch) {
         if (gt == 0) gat_go[gi & 1] = mbar_wait(&pfull[pb], (it >> 1) & 1, abort_flag, p.status) ? 1 : 0;
-        named_barrier(2, 128);             // also: every thread has finished the previous tile
+        named_barrier(2, kGatherThreads);  // also: every thread has finished the previous tile
         if (!gat_go[gi & 1]) goto teardown;
         ++gi;
         const int img0 = m0 / hw;
@@ -301,70 +306,76 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
           const uint16_t* raw = src;
           uint16_t* tp = reinterpret_cast<uint16_t*>(sPatch + 2 * kPatchBufBytes);
           const int pixels = p.patch_rows * p.W;
-          for (int px = gt; px < pixels; px += 128) {
-            uint16_t v[8];
+          for (int px = gt; px < pixels; px += kGatherThreads) {
+            uint32_t v[8];
 #pragma unroll
-            for (int c2 = 0; c2 < 8; ++c2) v[c2] = c2 < p.C ? raw[px * p.C + c2] : 0;
-            if (p.cpt == 4) {
-              *reinterpret_cast<uint2*>(tp + px * 4) =
-                  make_uint2(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16));
-            } else {
+            for (int c2 = 0; c2 < 8; ++c2) v[c2] = c2 < p.C ? raw[px * p.C + c2] : 0u;
+            if (p.cpt == 4)
+              *reinterpret_cast<uint2*>(tp + px * 4) = make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+            else
               *reinterpret_cast<uint4*>(tp + px * 8) =
-                  make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
-                             v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
-            }
+                  make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
           }
-          named_barrier(2, 128);           // repack complete: the raw buffer can be refilled
+          named_barrier(2, kGatherThreads);  // repack complete: the raw buffer can be refilled
           if (gt == 0) mbar_arrive(&pempty[pb]);
           src = tp;
         }
       } else {
         src = p.x + static_cast<size_t>(img) * p.H * p.W * p.C;
       }
-      int c = 0, s = 0, r = 0;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (gt == 0) gat_go[gi & 1] = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
-        named_barrier(2, 128);
+        named_barrier(2, kGatherThreads);
         if (!gat_go[gi & 1]) goto teardown;
         ++gi;
-        uint8_t* dst = sA + stage * kATileBytes + gt * 128;
-        if (p.cpt > 0) {
-          // whole taps: reduction index j = tap*cpt + channel; one 8- or 16-byte read per tap
-#pragma unroll 1
-          for (int c16 = 0; c16 < 8; ++c16) {
-            uint4 out = make_uint4(0, 0, 0, 0);
-            const int per = p.cpt == 4 ? 2 : 1;
-            for (int t = 0; t < per; ++t) {
-              uint2 lo = make_uint2(0, 0), hi = make_uint2(0, 0);
-              if (row_ok && r < p.R) {
-                const int ih = ih0 + r * p.dh;
-                const int iw = iw0 + s * p.dw;
-                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
-                  const uint16_t* q = src + ((ih - ih_first) * p.W + iw) * p.cpt;
-                  if (p.cpt == 4) {
-                    lo = *reinterpret_cast<const uint2*>(q);
-                  } else {
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(q);
-                    lo = make_uint2(w4.x, w4.y);
-                    hi = make_uint2(w4.z, w4.w);
-                  }
-                }
-              }
-              if (p.cpt == 4) {
-                if (t == 0) { out.x = lo.x; out.y = lo.y; } else { out.z = lo.x; out.w = lo.y; }
-              } else {
-                out = make_uint4(lo.x, lo.y, hi.x, hi.y);
-              }
-              if (++s == p.S) {
-                s = 0;
-                ++r;
-              }
+        uint8_t* dst = sA + stage * kATileBytes + gr * 128;
+        if (p.cpt == 4) {
+          // 8 whole taps of 4 channels (8 bytes each) -> chunks 4*gh .. 4*gh+3
+          const int t0 = kb * 16 + gh * 8;
+          int r = t0 / p.S, s = t0 - (t0 / p.S) * p.S;
+          uint2 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[i] = make_uint2(0, 0);
+            const int ih = ih0 + r * p.dh, iw = iw0 + s * p.dw;
+            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+              v[i] = *reinterpret_cast<const uint2*>(src + ((ih - ih_first) * p.W + iw) * 4);
+            if (++s == p.S) {
+              s = 0;
+              ++r;
             }
-            *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = out;
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + (((gh * 4 + q) ^ (gr & 7)) << 4)) =
+                make_uint4(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
+        } else if (p.cpt == 8) {
+          // 4 whole taps of 8 channels (16 bytes each)
+          const int t0 = kb * 8 + gh * 4;
+          int r = t0 / p.S, s = t0 - (t0 / p.S) * p.S;
+          uint4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[i] = make_uint4(0, 0, 0, 0);
+            const int ih = ih0 + r * p.dh, iw = iw0 + s * p.dw;
+            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+              v[i] = *reinterpret_cast<const uint4*>(src + ((ih - ih_first) * p.W + iw) * 8);
+            if (++s == p.S) {
+              s = 0;
+              ++r;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dst + (((gh * 4 + q) ^ (gr & 7)) << 4)) = v[q];
         } else {
+          // channel by channel: elements j0 .. j0+31 of the row
+          const int j0 = kb * 64 + gh * 32;
+          int c = j0 % p.C;
+          const int t = j0 / p.C;
+          int s = t % p.S;
+          int r = t / p.S;
 #pragma unroll 1
-          for (int c16 = 0; c16 < 8; ++c16) {
+          for (int q = 0; q < 4; ++q) {
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -372,11 +383,9 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
               if (row_ok && r < p.R) {
                 const int ih = ih0 + r * p.dh;
                 const int iw = iw0 + s * p.dw;
-                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
-                  const int row = use_patch ? ih - ih_first : ih;
-                  val = use_patch ? src[(row * p.W + iw) * p.C + c]
-                                  : __ldg(src + (static_cast<size_t>(row) * p.W + iw) * p.C + c);
-                }
+                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+                  val = use_patch ? src[((ih - ih_first) * p.W + iw) * p.C + c]
+                                  : __ldg(src + (static_cast<size_t>(ih) * p.W + iw) * p.C + c);
               }
               if (e & 1)
                 pk[e >> 1] |= val << 16;
@@ -390,7 +399,7 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
                 }
               }
             }
-            *reinterpret_cast<uint4*>(dst + ((c16 ^ (gt & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(dst + (((gh * 4 + q) ^ (gr & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
         fence_proxy_async_smem();
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
         }
       }
       if (use_patch && p.cpt == 0) {
-        named_barrier(2, 128);             // every row of this tile has been assembled
+        named_barrier(2, kGatherThreads);  // every row of this tile has been assembled
         if (gt == 0) mbar_arrive(&pempty[pb]);
       }
     }
@@ -432,7 +441,7 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, GATHER ? 320 : 192, TcCfg<BN, GATHER>::kSmem, stream>>>(p, tmA, tmB, tmY);
+  k<<<grid, GATHER ? 192 + kGatherThreads : 192, TcCfg<BN, GATHER>::kSmem, stream>>>(p, tmA, tmB, tmY);
   return cudaGetLastError();
 }
 
