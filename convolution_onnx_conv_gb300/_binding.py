@@ -39,12 +39,12 @@ class ConvDesc(ctypes.Structure):
                 ("pads", ctypes.c_int * 4), ("auto_pad", ctypes.c_int), ("group", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("x_layout", ctypes.c_int), ("y_layout", ctypes.c_int),
                 ("act", ctypes.c_int), ("clip_lo", ctypes.c_float), ("clip_hi", ctypes.c_float),
-                ("variant", ctypes.c_int), ("tile_n", ctypes.c_int)]
+                ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
 
 def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1,
               dtype=CONVF_BF16, act=CONVF_ACT_NONE, clip=(0.0, 6.0), auto_pad="NOTSET",
-              variant=CONVF_VARIANT_AUTO, layout=CONVF_NHWC, tile_n=0) -> ConvDesc:
+              variant=CONVF_VARIANT_AUTO, layout=CONVF_NHWC, tile_n=0, cta_pair=0) -> ConvDesc:
     d = ConvDesc()
     d.N, d.C, d.H, d.W, d.K, d.R, d.S = N, C, H, W, K, R, S
     d.stride[:] = list(stride)
@@ -58,6 +58,7 @@ def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1
     d.clip_lo, d.clip_hi = float(clip[0]), float(clip[1])
     d.variant = variant
     d.tile_n = tile_n
+    d.cta_pair = cta_pair
     return d
 
 
@@ -91,7 +92,8 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_resolve_pads.argtypes = [dptr, P(ctypes.c_int)]
     lib.conv_bn_scale_shift.argtypes = [ctypes.c_int] + [P(ctypes.c_float)] * 4 + [ctypes.c_float] + \
         [P(ctypes.c_float)] * 2
-    lib.conv_fused_plan.argtypes = [dptr, ctypes.c_int, P(ctypes.c_int), P(ctypes.c_int), P(ctypes.c_int)]
+    lib.conv_fused_plan.argtypes = [dptr, ctypes.c_int, P(ctypes.c_int), P(ctypes.c_int), P(ctypes.c_int),
+                                    P(ctypes.c_int)]
     lib.conv_fused_pack_weights.argtypes = [dptr, ctypes.c_int, vp, vp, ctypes.c_size_t]
     lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
     lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
@@ -157,11 +159,12 @@ def conv_bn_scale_shift(gamma, beta, mean, var, eps: float = 1e-5):
     return scale, shift
 
 
-def conv_fused_plan(desc: ConvDesc, num_sms: int = 152):
-    v, bn, kt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+def conv_fused_plan(desc: ConvDesc, num_sms: int = 152, with_pair: bool = False):
+    """(variant, tile_n, ktot) or, with with_pair, (variant, tile_n, ktot, cta_pair)."""
+    v, bn, kt, pr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(load_library().conv_fused_plan(ctypes.byref(desc), num_sms, ctypes.byref(v), ctypes.byref(bn),
-                                          ctypes.byref(kt)))
-    return v.value, bn.value, kt.value
+                                          ctypes.byref(kt), ctypes.byref(pr)))
+    return (v.value, bn.value, kt.value, pr.value) if with_pair else (v.value, bn.value, kt.value)
 
 
 def conv_fused_pack_weights(desc: ConvDesc, variant: int, W_bits, out):
@@ -232,11 +235,12 @@ class FusedConv:
     def __init__(self, N, C, H, W, K, R, S, w, bias=None, bn_scale=None, bn_shift=None, stride=(1, 1),
                  pads=(0, 0, 0, 0), dilation=(1, 1), group=1, act=CONVF_ACT_NONE, clip=(0.0, 6.0),
                  auto_pad="NOTSET", variant=CONVF_VARIANT_AUTO, requant_mult=None, requant_shift=None,
-                 out_zero_point=0, tile_n=0):
+                 out_zero_point=0, tile_n=0, cta_pair=0):
         import torch
         s8 = w.dtype == torch.int8
         self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group,
-                              CONVF_S8 if s8 else CONVF_BF16, act, clip, auto_pad, variant, tile_n=tile_n)
+                              CONVF_S8 if s8 else CONVF_BF16, act, clip, auto_pad, variant, tile_n=tile_n,
+                              cta_pair=cta_pair)
         wc = w.contiguous().cpu()
         wbits = wc if s8 else wc.view(torch.int16)
         keep = [wbits]

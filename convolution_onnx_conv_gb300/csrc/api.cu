@@ -21,13 +21,13 @@
 namespace convf {
 // defined once per tile width in tc_conv_inst.cu
 cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                const CUtensorMap&, int, bool, cudaStream_t);
+                                const CUtensorMap&, int, bool, bool, cudaStream_t);
 cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                const CUtensorMap&, int, bool, cudaStream_t);
+                                const CUtensorMap&, int, bool, bool, cudaStream_t);
 cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, bool, cudaStream_t);
+                                 const CUtensorMap&, int, bool, bool, cudaStream_t);
 cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, bool, cudaStream_t);
+                                 const CUtensorMap&, int, bool, bool, cudaStream_t);
 }  // namespace convf
 
 using namespace convf;
@@ -147,6 +147,8 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
   if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
+  if (d->cta_pair < 0 || d->cta_pair > 2)
+    return fail(CONVF_ERR_INVALID_ARG, "cta_pair=%d is not 0 (auto), 1 (single CTA) or 2 (CTA pair)", d->cta_pair);
   return CONVF_OK;
 }
 
@@ -225,34 +227,42 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
   return fail(CONVF_ERR_UNSUPPORTED, "no kernel serves this conv: %s", reasons.c_str());
 }
 
-// Tile width for the tcgen05 kernels: minimise waves x per-tile time, where a K16 step of a
-// 128 x bn MMA costs max(bn/2, (A + B bytes)/128) cycles (tensor rate vs shared-memory reads).
-int pick_bn(long long M, int K, int num_sms, int max_bn) {
-  const long long mblocks = (M + 127) / 128;
-  int best = max_bn;
+// Tile shape for the tcgen05 kernels: minimise waves x per-tile time.  Per 64-wide reduction
+// block a single CTA spends about {670, 694, 782, 1620} SM cycles for tile widths
+// {32, 64, 128, 256} (measured on GB300 over the ResNet-50 layers: each SM ingests operands at
+// about 43 B/cycle, plus pipeline overheads); a tile also writes 128 x bn fp32 outputs at about
+// 20 B/cycle per SM.  CTA pairs (256-row tiles, half the weight tile per CTA) cut the ingested
+// bytes but measured slower on every ResNet-50 layer (longer cross-SM handshakes), so they are
+// used only when requested: pair_mode 0 = auto (single CTAs), 1 = single, 2 = pairs.
+void pick_tile(long long M, int K, int num_kb, int num_sms, int max_bn, int pair_mode, int* bn_out, bool* pair_out) {
+  const bool pair = pair_mode == 2;
+  const long long tile_m = pair ? 256 : 128;
+  const long long units = pair ? num_sms / 2 : num_sms;
+  int best_bn = max_bn;
   double best_cost = 1e300;
   for (int bn : {256, 128, 64, 32}) {
     if (bn > max_bn) continue;
-    if (bn > 32 && bn / 2 >= K) continue;  // no point in a tile twice as wide as K
-    const long long tiles = mblocks * ((K + bn - 1) / bn);
-    const long long waves = (tiles + num_sms - 1) / num_sms;
-    const double step = std::max(bn / 2.0, (4096.0 + bn * 32.0) / 128.0);
-    const double cost = (double)waves * step;
+    if (bn > 32 && bn / 2 >= K && bn != max_bn) continue;  // no point in a tile twice as wide as K
+    const long long tiles = (M + tile_m - 1) / tile_m * ((K + bn - 1) / bn);
+    const long long waves = (tiles + units - 1) / units;
+    const double kb_cycles = bn == 32 ? 670.0 : bn == 64 ? 694.0 : bn == 128 ? 782.0 : 1620.0;
+    const double cost = (double)waves * std::max(num_kb * kb_cycles, 128.0 * bn * 4.0 / 20.0);
     if (cost < best_cost * 0.999) {
       best_cost = cost;
-      best = bn;
+      best_bn = bn;
     }
   }
-  return best;
+  *bn_out = best_bn;
+  *pair_out = pair;
 }
 
 // Gather variant: input rows one 128-pixel tile reads, staged whole in shared memory, when
 // tiles never straddle two images, rows are 16-byte multiples and the rows fit one 32 KB
 // buffer; 0 means the gatherers read global memory directly.
-int patch_rows_for(const Shape& s) {
+int patch_rows_for(const Shape& s, int channels) {
   const long long hw = (long long)s.Ho * s.Wo;
   if (hw % 128 != 0) return 0;
-  const long long row_bytes = (long long)s.W * s.C * 2;
+  const long long row_bytes = (long long)s.W * channels * 2;
   if (row_bytes % 16 != 0) return 0;
   long long q = (127 + s.Wo - 1) / s.Wo + 1;   // output rows one tile can touch
   if (q > s.Ho) q = s.Ho;
@@ -266,11 +276,8 @@ int patch_rows_for(const Shape& s) {
 // the channel-by-channel layout.
 int gather_cpt(const Shape& s) {
   if (s.C > 8) return 0;
-  const int rows = patch_rows_for(s);
-  if (rows == 0) return 0;
   const int cpt = s.C <= 4 ? 4 : 8;
-  if ((long long)rows * s.W * cpt * 2 > 32768) return 0;
-  return cpt;
+  return patch_rows_for(s, cpt) > 0 ? cpt : 0;
 }
 
 // ------------------------------------------------------------------ driver entry points
@@ -323,11 +330,13 @@ struct convf_handle {
   int32_t* qbias;
   int32_t* qmult;
   int32_t* qshift;
+  uint16_t* xpad;   // gather variant with padded channels: x with cpt channels per pixel
   int* status;
   int32_t zp;
   float lo, hi;
   // tcgen05 configuration
   int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
+  bool pair;        // CTA-pair (cta_group::2) 256-row tiles
   CUtensorMap tmB;
   CUtensorMap tmA, tmY;
   const void* map_x;
@@ -435,7 +444,9 @@ convf_status conv_bn_scale_shift(int K, const float* gamma, const float* beta, c
 
 // Host-only view of the selector: the variant and tcgen05 tile width create would choose for
 // `desc` on a GPU with `num_sms` SMs (no CUDA call).
-convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, int* tile_n, int* ktot) {
+convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, int* tile_n, int* ktot,
+                             int* cta_pair) {
+  if (cta_pair) *cta_pair = 0;
   Shape s;
   convf_status st = resolve(desc, &s);
   if (st != CONVF_OK) return st;
@@ -447,10 +458,17 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
   if (v == CONVF_VARIANT_GEMM_1X1 || v == CONVF_VARIANT_IMPLICIT_GEMM || v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
     int am, cb, cp;
     tc_layout(v, s, &am, &cb, &kt, &cp);
-    const int max_bn = v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? 128 : 256;
+    const bool gather = v == CONVF_VARIANT_IMPLICIT_GEMM_GATHER;
+    const int max_bn = gather ? 128 : 256;
     if (desc->tile_n > max_bn)
       return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d exceeds %d for the gather variant", desc->tile_n, max_bn);
-    bn = desc->tile_n ? desc->tile_n : pick_bn(s.M, s.K, num_sms > 0 ? num_sms : 1, max_bn);
+    if (gather && desc->cta_pair == 2)
+      return fail(CONVF_ERR_UNSUPPORTED, "the gather variant runs on single CTAs");
+    bool pair = false;
+    pick_tile(s.M, s.K, kt / 64, num_sms > 1 ? num_sms : 2, desc->tile_n ? desc->tile_n : max_bn,
+              gather ? 1 : desc->cta_pair, &bn, &pair);
+    if (desc->tile_n) bn = desc->tile_n;
+    if (cta_pair) *cta_pair = pair ? 1 : 0;
   } else if (v == CONVF_VARIANT_INT8) {
     kt = s.R * s.S * s.C;
   }
@@ -548,7 +566,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   // device layout
   size_t off = 0;
   auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  size_t o_w = 0, o_taps = 0, o_scale = 0, o_bias = 0, o_qb = 0, o_qm = 0, o_qs = 0;
+  size_t o_w = 0, o_taps = 0, o_scale = 0, o_bias = 0, o_qb = 0, o_qm = 0, o_qs = 0, o_pad = 0;
   std::vector<uint16_t> wpack;
   std::vector<float> taps;
   if (variant == CONVF_VARIANT_DEPTHWISE) {
@@ -574,6 +592,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
+    if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER && gather_cpt(s) > 0)
+      o_pad = carve((size_t)s.N * s.H * s.W * gather_cpt(s) * sizeof(uint16_t));
   }
   const size_t o_status = carve(sizeof(int));
   h->dev_bytes = off;
@@ -610,6 +630,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     std::memcpy(staging.data() + o_qs, requant_shift, (size_t)s.K * 4);
   } else {
     h->w_bf16 = reinterpret_cast<uint16_t*>(base + o_w);
+    h->xpad = o_pad ? reinterpret_cast<uint16_t*>(base + o_pad) : nullptr;
     h->scale = reinterpret_cast<float*>(base + o_scale);
     h->bias = reinterpret_cast<float*>(base + o_bias);
     std::memcpy(staging.data() + o_w, wpack.data(), wpack.size() * sizeof(uint16_t));
@@ -630,24 +651,29 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       delete h;
       return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled/Im2col are unavailable from the driver");
     }
-    const int max_bn = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? 128 : 256;
-    if (desc->tile_n > max_bn) {
+    const bool gather = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER;
+    const int max_bn = gather ? 128 : 256;
+    if (desc->tile_n > max_bn || (gather && desc->cta_pair == 2)) {
       cudaFree(h->dev);
       delete h;
-      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d exceeds %d for the gather variant", desc->tile_n, max_bn);
+      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d / cta_pair=%d not served by the gather variant", desc->tile_n,
+                  desc->cta_pair);
     }
-    h->bn = desc->tile_n ? desc->tile_n : pick_bn(s.M, s.K, h->num_sms, max_bn);
-    h->patch_rows = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? patch_rows_for(s) : 0;
+    pick_tile(s.M, s.K, h->ktot / 64, h->num_sms, desc->tile_n ? desc->tile_n : max_bn, gather ? 1 : desc->cta_pair,
+              &h->bn, &h->pair);
+    if (desc->tile_n) h->bn = desc->tile_n;
     h->cpt = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? gather_cpt(s) : 0;
-    h->row_bytes = s.W * s.C * 2;
+    h->patch_rows = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? patch_rows_for(s, h->cpt ? h->cpt : s.C) : 0;
+    h->row_bytes = s.W * (h->cpt ? h->cpt : s.C) * 2;
     h->num_kb = h->ktot / 64;
     h->n_blocks = (s.K + h->bn - 1) / h->bn;
-    const long long tiles = (s.M + 127) / 128 * h->n_blocks;
+    const long long tile_m = h->pair ? 256 : 128;
+    const long long tiles = (s.M + tile_m - 1) / tile_m * h->n_blocks;
     h->num_tiles = (int)tiles;
-    h->grid = (int)std::min<long long>(tiles, h->num_sms);
+    h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2) : (int)std::min<long long>(tiles, h->num_sms);
     const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
     const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)h->bn};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn)};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w_bf16, dims, strides, box, es,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -752,13 +778,21 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.n_blocks = h->n_blocks; p.num_tiles = h->num_tiles; p.a_mode = h->a_mode;
       p.scale = h->scale; p.bias = h->bias; p.x = static_cast<const uint16_t*>(x);
       p.patch_rows = h->patch_rows; p.row_bytes = h->row_bytes; p.cpt = h->cpt;
+      if (h->cpt > 0) {
+        // whole taps: pad the channels into the handle's scratch copy of x first
+        ce = launch_pad_channels(static_cast<const uint16_t*>(x), h->xpad, (long long)s.N * s.H * s.W, s.C, h->cpt,
+                                 h->num_sms, strm);
+        if (ce != cudaSuccess) break;
+        p.x = h->xpad;
+        p.C = h->cpt;
+      }
       p.lo = h->lo; p.hi = h->hi; p.status = h->status;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
-        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
-        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
-        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
-        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->tmY, h->grid, gather, strm); break;
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
       }
     }
   }
@@ -809,10 +843,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
   else
     snprintf(buf, len,
-             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d tiles=%d grid=%d "
-             "patch_rows=%d tap_channels=%d weight_bytes=%zu",
-             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->bn, h->num_kb, h->num_tiles, h->grid,
-             h->patch_rows, h->cpt, h->dev_bytes);
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d kblocks=%d tiles=%d "
+             "grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
+             h->num_kb, h->num_tiles, h->grid, h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
 }
 

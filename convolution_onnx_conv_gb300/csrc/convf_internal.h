@@ -3,11 +3,40 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace convf {
 
 // Bit set in a handle's device status word when a bounded device wait ran out.
 constexpr int kStatusTimeout = 1;
+
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream finishes; every kernel here waits (griddepcontrol.wait) before its
+// first global-memory access, so stream order is kept for data.
+// `cluster` > 1 launches clusters of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- tcgen05 implicit GEMM
 // GEMM view of the conv: rows m = (n, oh, ow) (M = N*Ho*Wo), columns = output channels,
@@ -39,11 +68,11 @@ struct TcConvParams {
   int* status;            // device status word
 };
 
-// Launches the persistent kernel with tile width bn (32, 64, 128 or 256).
-cudaError_t launch_tc_conv(int bn, const TcConvParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmB, const CUtensorMap& tmY, int grid,
-                           cudaStream_t stream);
-int tc_conv_smem_bytes(int bn, bool gather);
+
+
+// NHWC bf16 with C <= 8 channels -> NHWC bf16 with cpt (4 or 8) channels, zero-padded.
+cudaError_t launch_pad_channels(const uint16_t* x, uint16_t* out, long long pixels, int C, int cpt, int num_sms,
+                                cudaStream_t stream);
 
 // ---------------------------------------------------------------- depthwise (CUDA cores)
 struct DwParams {

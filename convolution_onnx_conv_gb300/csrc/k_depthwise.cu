@@ -1,6 +1,6 @@
 // Depthwise convolution (group == C == K) on CUDA cores: memory-bound (about 2-3 flop per
 // byte), so no tensor cores.  NHWC bf16 in, fp32 taps with the BN scale folded in, fp32 out.
-// Each thread owns 8 channels (one 16-byte vector) x kOW consecutive outputs of one row;
+// Each thread owns 8 channels (one 16-byte vector) x kOW = 2 consecutive outputs of one row;
 // consecutive threads take consecutive channel vectors of the same pixel, so every load and
 // store is a coalesced 128-bit access.  Inputs shared by neighbouring threads (the 3x3 halo)
 // are re-read through L1/L2, not from HBM.
@@ -9,7 +9,7 @@
 
 namespace convf {
 
-constexpr int kOW = 4;
+constexpr int kOW = 2;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -22,23 +22,45 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 
 __device__ __forceinline__ float clampf(float v, float lo, float hi) { return fminf(fmaxf(v, lo), hi); }
 
-// 3x3, dilation 1, equal strides SW in {1, 2}.
+// 3x3, dilation 1, equal strides SW in {1, 2}.  All 3 x NCOL input vectors a thread needs are
+// loaded before any arithmetic (padding reads as zero without a branch), so every thread keeps
+// 12-15 independent 16-byte loads in flight.
 template <int SW>
-__global__ void __launch_bounds__(256) dw3x3_kernel(const DwParams p) {
+__global__ void __launch_bounds__(256, SW == 1 ? 3 : 2) dw3x3_kernel(const DwParams p) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
+  // grid.y walks output rows (n, oh); grid.x x 256 threads cover (output column block, channel
+  // vector) of one row with 32-bit index arithmetic
   const int C8 = p.C >> 3;
   const int owb_n = (p.Wo + kOW - 1) / kOW;
-  const long long total = static_cast<long long>(p.N) * p.Ho * owb_n * C8;
+  const int row_items = owb_n * C8;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= row_items) return;
+  const int c8 = j % C8;
+  const int owb = j / C8;
   constexpr int NCOL = (kOW - 1) * SW + 3;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c8 = static_cast<int>(idx % C8);
-    long long t = idx / C8;
-    const int owb = static_cast<int>(t % owb_n);
-    t /= owb_n;
-    const int oh = static_cast<int>(t % p.Ho);
-    const int n = static_cast<int>(t / p.Ho);
+  for (int nh = blockIdx.y; nh < p.N * p.Ho; nh += gridDim.y) {
+    const int oh = nh % p.Ho;
+    const int n = nh / p.Ho;
     const int c0 = c8 * 8;
     const int ow0 = owb * kOW;
+    const int iw_base = ow0 * SW - p.pl;
+    const int ih_base = oh * SW - p.pt;
+
+    uint4 raw[3][NCOL];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const int ih = ih_base + r;
+      const bool row_ok = ih >= 0 && ih < p.H;
+      const uint16_t* xrow = p.x + (static_cast<size_t>(n) * p.H + (row_ok ? ih : 0)) * p.W * p.C + c0;
+#pragma unroll
+      for (int col = 0; col < NCOL; ++col) {
+        const int iw = iw_base + col;
+        const bool ok = row_ok && iw >= 0 && iw < p.W;
+        raw[r][col] = ok ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(iw) * p.C))
+                         : make_uint4(0, 0, 0, 0);
+      }
+    }
 
     float acc[kOW][8];
     {
@@ -50,11 +72,8 @@ __global__ void __launch_bounds__(256) dw3x3_kernel(const DwParams p) {
         acc[j][4] = b1.x; acc[j][5] = b1.y; acc[j][6] = b1.z; acc[j][7] = b1.w;
       }
     }
-    const int iw_base = ow0 * SW - p.pl;
 #pragma unroll
     for (int r = 0; r < 3; ++r) {
-      const int ih = oh * SW - p.pt + r;
-      if (ih < 0 || ih >= p.H) continue;
       float tap[3][8];
 #pragma unroll
       for (int s = 0; s < 3; ++s) {
@@ -63,19 +82,10 @@ __global__ void __launch_bounds__(256) dw3x3_kernel(const DwParams p) {
         tap[s][0] = t0.x; tap[s][1] = t0.y; tap[s][2] = t0.z; tap[s][3] = t0.w;
         tap[s][4] = t1.x; tap[s][5] = t1.y; tap[s][6] = t1.z; tap[s][7] = t1.w;
       }
-      const uint16_t* xrow = p.x + (static_cast<size_t>(n) * p.H + ih) * p.W * p.C + c0;
-      uint4 raw[NCOL];
-#pragma unroll
-      for (int col = 0; col < NCOL; ++col) {
-        const int iw = iw_base + col;
-        raw[col] = (iw >= 0 && iw < p.W)
-                       ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(iw) * p.C))
-                       : make_uint4(0, 0, 0, 0);
-      }
 #pragma unroll
       for (int col = 0; col < NCOL; ++col) {
         float xv[8];
-        bf16x8_to_f32(raw[col], xv);
+        bf16x8_to_f32(raw[r][col], xv);
 #pragma unroll
         for (int j = 0; j < kOW; ++j) {
           const int s = col - j * SW;
@@ -102,6 +112,8 @@ __global__ void __launch_bounds__(256) dw3x3_kernel(const DwParams p) {
 
 // Any filter size, strides and dilations: one output pixel x 8 channels per thread.
 __global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const int C8 = p.C >> 3;
   const long long total = static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -143,19 +155,20 @@ cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream
   const bool fast = p.R == 3 && p.S == 3 && p.dh == 1 && p.dw == 1 && p.sh == p.sw &&
                     (p.sh == 1 || p.sh == 2);
   const long long C8 = p.C / 8;
-  const long long work = fast ? static_cast<long long>(p.N) * p.Ho * ((p.Wo + kOW - 1) / kOW) * C8
-                              : static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
-  if (work == 0) return cudaSuccess;
+  if (static_cast<long long>(p.N) * p.Ho * p.Wo * C8 == 0) return cudaSuccess;
+  const dim3 b(256);
+  if (fast) {
+    const long long row_items = ((p.Wo + kOW - 1) / kOW) * C8;
+    const long long rows = static_cast<long long>(p.N) * p.Ho;
+    const dim3 g(static_cast<unsigned>((row_items + 255) / 256), static_cast<unsigned>(rows < 65535 ? rows : 65535));
+    return p.sh == 1 ? launch_pdl(dw3x3_kernel<1>, g, b, 0, stream, 1, p)
+                     : launch_pdl(dw3x3_kernel<2>, g, b, 0, stream, 1, p);
+  }
+  const long long work = static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
   long long blocks = (work + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8 * 4;
+  const long long cap = static_cast<long long>(num_sms) * 3 * 16;
   if (blocks > cap) blocks = cap;
-  if (fast && p.sh == 1)
-    dw3x3_kernel<1><<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-  else if (fast)
-    dw3x3_kernel<2><<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-  else
-    dw_generic_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(dw_generic_kernel, dim3(static_cast<unsigned>(blocks)), b, 0, stream, 1, p);
 }
 
 }  // namespace convf

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256, 1) s8_conv_kernel(const S8Params p) {
   uint8_t* sA = s8_smem;
   uint8_t* sB = s8_smem + kS8Stages * kS8TileBytes;
 
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 2;   // 0..1 : 64-row slab
@@ -173,8 +175,7 @@ cudaError_t launch_s8_conv(const S8Params& p, cudaStream_t stream) {
   }
   if (p.M == 0) return cudaSuccess;
   dim3 grid((p.M + kS8BM - 1) / kS8BM, (p.Kout + kS8BN - 1) / kS8BN);
-  s8_conv_kernel<<<grid, 256, kS8Smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(s8_conv_kernel, grid, dim3(256), kS8Smem, stream, 1, p);
 }
 
 }  // namespace convf

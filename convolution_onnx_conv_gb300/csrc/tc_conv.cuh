@@ -28,26 +28,36 @@ constexpr int kNumEpiBuf = 2;
 constexpr int kPatchBufBytes = 32768;
 constexpr int kGatherThreads = 256;
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, bool PAIR>
 struct TcCfg {
-  static constexpr int kBTileBytes = BN * kBK * 2;
-  static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
+  // with a CTA pair each CTA holds half of the weight tile (BN/2 rows)
+  static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * kBK * 2;
+  static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3)
+                                        : (PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8)));
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
-  // gather mode: two buffers for the raw input rows one tile needs (TcConvParams::patch_rows)
-  // plus one buffer holding them with channels padded to whole taps (TcConvParams::cpt)
-  static constexpr int kPatchBytes = GATHER ? 3 * kPatchBufBytes : 0;
+  // gather mode: two buffers for the input rows one tile needs (TcConvParams::patch_rows)
+  static constexpr int kPatchBytes = GATHER ? 2 * kPatchBufBytes : 0;
   static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + kNumEpiBuf * kEpiTileBytes +
                                kPatchBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
 };
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
-  using Cfg = TcCfg<BN, GATHER>;
+  static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
+  using Cfg = TcCfg<BN, GATHER, PAIR>;
+  // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
+  // both CTAs' TMEM; each CTA loads its own 128 activation rows and half of the weight tile.
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
+  const bool leader = crank == 0;
+  constexpr int kTileM = PAIR ? 2 * kBM : kBM;
+  const int tstart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int mrow_off = PAIR ? static_cast<int>(crank) * kBM : 0;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], PAIR ? 256 : 128);
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 1);
     }
@@ -93,13 +103,22 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     if (!GATHER) tma_prefetch_desc(&tmA);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers and TMEM exist before any cross-CTA operation
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // setup above touched only smem/TMEM: overlap it with the previous kernel's tail
+  pdl_launch_dependents();
+  pdl_wait_prior();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -108,8 +127,8 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
       uint32_t phase = 0;
       const uint32_t tx = Cfg::kBTileBytes + (GATHER ? 0 : kATileBytes);
       int it = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-        const int m0 = (tile / p.n_blocks) * kBM;
+      for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
+        const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
         const int n0 = (tile % p.n_blocks) * BN;
         if (GATHER && p.patch_rows > 0) {
           // bulk-copy the input rows this tile reads (whole rows of W*C bf16) into smem
@@ -141,23 +160,35 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
         int tap = 0, cb = 0;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
-          mbar_arrive_expect_tx(&full[stage], tx);
+          // a pair's loads all complete on the leader's barrier, which expects both CTAs' bytes
+          if (!PAIR || leader) mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * tx : tx);
+          const uint32_t fbar = PAIR ? map_to_rank(smem_u32(&full[stage]), 0) : 0;
           if (!GATHER) {
             uint8_t* dA = sA + stage * kATileBytes;
             if (p.a_mode == kA2D) {
-              tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
+              if (PAIR)
+                tma_load_2d_pair(dA, &tmA, fbar, kb * kBK, m0);
+              else
+                tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
             } else {
               const int r = tap / p.S;
               const int s = tap - r * p.S;
-              tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img,
-                                 static_cast<uint16_t>(s * p.dw), static_cast<uint16_t>(r * p.dh));
+              if (PAIR)
+                tma_load_im2col_4d_pair(dA, &tmA, fbar, cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
+                                        static_cast<uint16_t>(r * p.dh));
+              else
+                tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img,
+                                   static_cast<uint16_t>(s * p.dw), static_cast<uint16_t>(r * p.dh));
               if (++cb == p.cblocks) {
                 cb = 0;
                 ++tap;
               }
             }
           }
-          tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
+          if (PAIR)
+            tma_load_2d_pair(sB + stage * Cfg::kBTileBytes, &tmB, fbar, kb * kBK, n0 + static_cast<int>(crank) * (BN / 2));
+          else
+            tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -167,13 +198,13 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tstart; tile < p.num_tiles; tile += tstep) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -185,15 +216,24 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
-            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            if (PAIR)
+              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            else
+              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
           }
-          tc_commit(&empty[stage]);
+          if (PAIR)
+            tc_commit_pair(&empty[stage], 3);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        tc_commit(&tfull[acc]);
+        if (PAIR)
+          tc_commit_pair(&tfull[acc], 3);
+        else
+          tc_commit(&tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -209,8 +249,8 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     uint32_t acc_phase = 0;
     int ebuf = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-      const int m0 = (tile / p.n_blocks) * kBM;
+    for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
+      const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
       const int n0 = (tile % p.n_blocks) * BN;
       if (et == 0) epi_go[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
       named_barrier(1, 128);
@@ -227,7 +267,10 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
         tmem_ld_wait();
         if (ch == nchunks - 1) {
           tc_fence_before();
-          mbar_arrive(&tempty[acc]);
+          if (PAIR && !leader)
+            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+          else
+            mbar_arrive(&tempty[acc]);
         }
         const float4* sc4 = reinterpret_cast<const float4*>(p.scale + nc);
         const float4* bi4 = reinterpret_cast<const float4*>(p.bias + nc);
@@ -269,8 +312,8 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     // 256 threads, two per tile row: thread gt assembles half gh of row gr in every k-block
     // (16-byte chunks 4*gh .. 4*gh+3 of the row's 128 bytes).  Reduction index
     // j = (r*S + s)*Cp + c.  With p.patch_rows > 0 the rows come from the tile's input rows that
-    // the producer bulk-copied into smem (repacked into whole taps of cpt channels when
-    // cpt > 0); otherwise they are read from global memory.
+    // the producer bulk-copied into smem; with cpt > 0 the input already holds whole taps of
+    // cpt channels (zero-padded by pad_channels_kernel) and each tap is one vector read.
     const int gt = threadIdx.x - 192;
     const int gr = gt & 127;
     const int gh = gt >> 7;
@@ -280,7 +323,7 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     const int hw = p.Ho * p.Wo;
     const bool use_patch = p.patch_rows > 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
       const int m0 = (tile / p.n_blocks) * kBM;
       const int m = m0 + gr;
       const bool row_ok = m < p.M;
@@ -301,25 +344,6 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
         const int img0 = m0 / hw;
         ih_first = ((m0 - img0 * hw) / p.Wo) * p.sh - p.pt;
         src = reinterpret_cast<const uint16_t*>(sPatch + pb * kPatchBufBytes);
-        if (p.cpt > 0) {
-          // repack the raw rows (C channels per pixel) into whole taps of cpt channels
-          const uint16_t* raw = src;
-          uint16_t* tp = reinterpret_cast<uint16_t*>(sPatch + 2 * kPatchBufBytes);
-          const int pixels = p.patch_rows * p.W;
-          for (int px = gt; px < pixels; px += kGatherThreads) {
-            uint32_t v[8];
-#pragma unroll
-            for (int c2 = 0; c2 < 8; ++c2) v[c2] = c2 < p.C ? raw[px * p.C + c2] : 0u;
-            if (p.cpt == 4)
-              *reinterpret_cast<uint2*>(tp + px * 4) = make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
-            else
-              *reinterpret_cast<uint4*>(tp + px * 8) =
-                  make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
-          }
-          named_barrier(2, kGatherThreads);  // repack complete: the raw buffer can be refilled
-          if (gt == 0) mbar_arrive(&pempty[pb]);
-          src = tp;
-        }
       } else {
         src = p.x + static_cast<size_t>(img) * p.H * p.W * p.C;
       }
@@ -409,7 +433,7 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
           phase ^= 1;
         }
       }
-      if (use_patch && p.cpt == 0) {
+      if (use_patch) {
         named_barrier(2, kGatherThreads);  // every row of this tile has been assembled
         if (gt == 0) mbar_arrive(&pempty[pb]);
       }
@@ -423,26 +447,34 @@ teardown:
     for (int i = 0; i < 2000; ++i) __nanosleep(100000);
   }
   __syncthreads();
+  if (PAIR) cluster_sync();   // no CTA of the pair leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, bool PAIR>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const CUtensorMap& tmY, int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<BN, GATHER>::kSmem);
+                                         TcCfg<BN, GATHER, PAIR>::kSmem);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
-  k<<<grid, GATHER ? 192 + kGatherThreads : 192, TcCfg<BN, GATHER>::kSmem, stream>>>(p, tmA, tmB, tmY);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(GATHER ? 192 + kGatherThreads : 192), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
+                    PAIR ? 2 : 1, p, tmA, tmB, tmY);
 }
 
 }  // namespace convf

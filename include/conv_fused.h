@@ -99,6 +99,8 @@ typedef struct {
   float clip_lo, clip_hi;  /* bounds for CONVF_ACT_CLIP (lo <= hi)                            */
   int variant;             /* convf_variant; 0 = selector                                     */
   int tile_n;              /* tcgen05 variants: output-channel tile width 32/64/128/256, 0 = auto */
+  int cta_pair;            /* tcgen05 variants: 0 = auto, 1 = single-CTA 128-row tiles, 2 = CTA pairs
+                              (cta_group::2, 256-row tiles, each CTA loads half the weight tile) */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;
@@ -119,11 +121,12 @@ convf_status conv_bn_scale_shift(int K, const float* gamma, const float* beta, c
                                  const float* var, float eps, float* scale, float* shift);
 
 /* Host-only view of the shape-keyed selector (no CUDA call): the variant create would pick
- * for desc, the tcgen05 tile width (128 x *tile_n output tile; 0 for the other kernels) on a
- * GPU with num_sms SMs, and the prepacked weight row length *ktot (elements).  Any output
- * pointer may be NULL.  Refusals are the same as create's. */
+ * for desc, the tcgen05 tile width *tile_n (0 for the other kernels) and whether the tiles run on
+ * CTA pairs (*cta_pair = 1: 256 x tile_n tiles; 0: 128 x tile_n) on a GPU with num_sms SMs, and
+ * the prepacked weight row length *ktot (elements).  Any output pointer may be NULL.  Refusals
+ * are the same as create's. */
 convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, int* tile_n,
-                             int* ktot);
+                             int* ktot, int* cta_pair);
 
 /* Host-only weight prepack for a tcgen05 variant (CONVF_VARIANT_GEMM_1X1, _IMPLICIT_GEMM or
  * _IMPLICIT_GEMM_GATHER): W [K][C][R][S] bf16 bits -> out [K][ktot] bf16 bits, reduction index

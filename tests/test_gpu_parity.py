@@ -91,15 +91,25 @@ def test_same_shape_through_both_activation_loaders(variant):
     _assert(check_full(spec, 7100, variant), spec, variant)
 
 
+@pytest.mark.parametrize("cta_pair", [1, 2])
 @pytest.mark.parametrize("tile_n", [32, 64, 128, 256])
-def test_every_tile_width(tile_n):
-    spec = S(f"tiles{tile_n}", 2, 64, 17, 17, 200, 3, 3, pads=(1, 1, 1, 1), bias=True)
+@pytest.mark.parametrize("shape", ["3x3", "1x1", "1x1s2"])
+def test_every_tile_width(tile_n, cta_pair, shape):
+    """Every tile width on single CTAs and on CTA pairs (256-row tiles, half the weight tile
+    per CTA); M = 578 / 300 / 98 leaves a last pair tile whose second half is partly or
+    entirely past the end; K = 200 leaves a ragged last column tile."""
+    if shape == "3x3":
+        spec = S(f"tiles{tile_n}", 2, 64, 17, 17, 200, 3, 3, pads=(1, 1, 1, 1), bias=True)
+    elif shape == "1x1":
+        spec = S(f"tiles{tile_n}_1x1", 3, 72, 10, 10, 200, 1, 1, bias=True)
+    else:
+        spec = S(f"tiles{tile_n}_1x1s2", 2, 64, 14, 14, 200, 1, 1, (2, 2), bias=True)
     inp = inputs_for(spec, 7150)
     from parity import compare
     c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
                      *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
-                     pads=spec.pads, act=spec.act, tile_n=tile_n)
-    assert f"tile=128x{tile_n}" in c.describe()
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, cta_pair=cta_pair)
+    assert f"tile={256 if cta_pair == 2 else 128}x{tile_n} cta_pair={cta_pair - 1}" in c.describe()
     y = c(to_device_nhwc(inp["x"]))
     torch.cuda.synchronize()
     assert c.status() == cf.CONVF_OK

@@ -61,6 +61,8 @@ def desc(**kw):
     (dict(variant=cf.CONVF_VARIANT_GEMM_1X1), cf.CONVF_ERR_UNSUPPORTED, "forced variant"),
     (dict(variant=cf.CONVF_VARIANT_DEPTHWISE), cf.CONVF_ERR_UNSUPPORTED, "group == C == K"),
     (dict(variant=11), cf.CONVF_ERR_INVALID_ARG, "variant=11"),
+    (dict(cta_pair=3), cf.CONVF_ERR_INVALID_ARG, "cta_pair=3"),
+    (dict(C=3, K=32, cta_pair=2), cf.CONVF_ERR_UNSUPPORTED, "single CTAs"),
     (dict(N=1 << 14, H=1 << 10, W=1 << 10), cf.CONVF_ERR_UNSUPPORTED, "2^31"),
 ])
 def test_refusals_name_the_offender(kw, status, needle):
@@ -138,6 +140,17 @@ def test_bn_scale_shift_matches_formula():
     assert np.array_equal(shift, t64.astype(np.float32))
     with pytest.raises(cf.ConvFusedError):
         cf.conv_bn_scale_shift(g, b, m, np.full(K, -1.0, np.float32), 1e-5)
+
+
+def test_tile_choice_and_overrides():
+    # 3x3 128->128 at 28x28, batch 32: 128-wide single-CTA tiles (the measured best)
+    d = cf.make_desc(32, 128, 28, 28, 128, 3, 3, (1, 1), (1, 1, 1, 1))
+    v, bn, kt, pair = cf.conv_fused_plan(d, with_pair=True)
+    assert (v, bn, kt, pair) == (cf.CONVF_VARIANT_IMPLICIT_GEMM, 128, 1152, 0)
+    d.cta_pair = 2
+    assert cf.conv_fused_plan(d, with_pair=True)[3] == 1
+    d.tile_n = 64
+    assert cf.conv_fused_plan(d, with_pair=True)[1] == 64
 
 
 def test_selector_on_the_workloads():
