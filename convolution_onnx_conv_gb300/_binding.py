@@ -29,7 +29,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_plan", "conv_fused_pack_weights", "conv_fused_create", "conv_fused_run",
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
-            "conv_fused_watchdog_selftest"]
+            "conv_fused_watchdog_selftest", "conv_fused_run_noalloc"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -106,6 +106,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_last_error.argtypes = []
     lib.conv_fused_last_error.restype = ctypes.c_char_p
     lib.conv_fused_watchdog_selftest.argtypes = [vp, ctypes.c_longlong, vp]
+    lib.conv_fused_run_noalloc.argtypes = [dptr, vp, vp, vp, vp, vp, vp, vp]
     for name in EXPORTED:
         if name not in ("conv_fused_destroy", "conv_fused_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -219,6 +220,13 @@ def conv_fused_describe(handle: int) -> str:
 def conv_fused_watchdog_selftest(status_dev, budget_cycles: int, stream=None):
     s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
     _check(load_library().conv_fused_watchdog_selftest(_addr(status_dev), int(budget_cycles), s))
+
+
+def conv_fused_run_noalloc(desc: ConvDesc, x, w_packed, scale, bias, y, status=None, stream=None):
+    """Allocation-free run: every argument a device pointer (int) or CUDA tensor."""
+    s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
+    _check(load_library().conv_fused_run_noalloc(ctypes.byref(desc), _addr(x), _addr(w_packed), _addr(scale),
+                                                 _addr(bias), _addr(y), _addr(status), s))
 
 
 # --------------------------------------------------------------------------- torch convenience

@@ -860,3 +860,142 @@ convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free run
+// Scratch for conv_fused_run_noalloc: a file-scope device array, so the entry point needs no
+// cudaMalloc.  Every GPU that loads this library reserves it until the process exits.  Host code
+// must not use its name as a device address (on the host it is only a stand-in symbol); the
+// device address is looked up with cudaGetSymbolAddress, once per device.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on first use per device).
+convf_status noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(ce));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CONVF_ERR_UNSUPPORTED, "device index %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    ce = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (ce != cudaSuccess || !p)
+      return fail(CONVF_ERR_CUDA, "cudaGetSymbolAddress(scratch) failed: %s", cudaGetErrorString(ce));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return CONVF_OK;
+}
+}  // namespace
+
+extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const void* x, const void* w_packed,
+                                               const float* scale, const float* bias, void* y, int32_t* status_dev,
+                                               void* stream) {
+  Shape s;
+  convf_status st = resolve(desc, &s);
+  if (st != CONVF_OK) return st;
+  if ((st = check_misc(desc)) != CONVF_OK) return st;
+  if (desc->dtype != CONVF_BF16 || desc->group != 1)
+    return fail(CONVF_ERR_UNSUPPORTED, "the allocation-free run serves bf16 convs with group == 1");
+  if (!cannot(CONVF_VARIANT_IMPLICIT_GEMM_GATHER, desc, s).empty())
+    return fail(CONVF_ERR_UNSUPPORTED, "allocation-free run refused: %s",
+                cannot(CONVF_VARIANT_IMPLICIT_GEMM_GATHER, desc, s).c_str());
+  const int cpt = gather_cpt(s);
+  if (cpt == 0)
+    return fail(CONVF_ERR_UNSUPPORTED,
+                "the allocation-free run serves convs with at most 8 input channels whose 128-row tiles stay "
+                "inside one image and whose input rows fit the 32 KB staging buffer");
+  if (desc->tile_n > 128 || desc->cta_pair == 2)
+    return fail(CONVF_ERR_UNSUPPORTED, "tile_n > 128 / CTA pairs are not served by the gathered-row kernel");
+  // scratch layout: [padded x][scale, padded to 256][bias, padded to 256][status word]; every
+  // size refusal comes before any pointer is looked at
+  const int Kpad = (int)align_up((size_t)s.K, 256);
+  const size_t xpad_bytes = align_up((size_t)s.N * s.H * s.W * cpt * sizeof(uint16_t), 256);
+  const size_t vec_bytes = (size_t)Kpad * sizeof(float);
+  const size_t need = xpad_bytes + 2 * vec_bytes + 256;
+  if (need > kNoAllocScratchBytes)
+    return fail(CONVF_ERR_UNSUPPORTED, "the allocation-free run needs %zu bytes of scratch; its maximum is %zu",
+                need, kNoAllocScratchBytes);
+  if (s.M == 0) return ok();
+  if (!x || !w_packed || !scale || !bias || !y) return fail(CONVF_ERR_INVALID_ARG, "x/w_packed/scale/bias/y is NULL");
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
+      (reinterpret_cast<uintptr_t>(w_packed) & 15))
+    return fail(CONVF_ERR_INVALID_ARG, "x, w_packed and y must be 16-byte aligned");
+  if (!load_encoders()) return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != CONVF_OK) return st;
+  int dev = 0, num_sms = 0;
+  cudaGetDevice(&dev);
+  cudaError_t ce = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "device query failed: %s", cudaGetErrorString(ce));
+
+  char* base = static_cast<char*>(scratch);
+  uint16_t* xpad = reinterpret_cast<uint16_t*>(base);
+  float* sc = reinterpret_cast<float*>(base + xpad_bytes);
+  float* bi = reinterpret_cast<float*>(base + xpad_bytes + vec_bytes);
+  int* status = status_dev ? reinterpret_cast<int*>(status_dev)
+                           : reinterpret_cast<int*>(base + xpad_bytes + 2 * vec_bytes);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+
+  // the epilogue reads whole 32-column chunks: copy the vectors and zero their padding
+  if ((ce = cudaMemsetAsync(sc, 0, 2 * vec_bytes, strm)) != cudaSuccess ||
+      (ce = cudaMemcpyAsync(sc, scale, (size_t)s.K * sizeof(float), cudaMemcpyDeviceToDevice, strm)) != cudaSuccess ||
+      (ce = cudaMemcpyAsync(bi, bias, (size_t)s.K * sizeof(float), cudaMemcpyDeviceToDevice, strm)) != cudaSuccess)
+    return fail(CONVF_ERR_CUDA, "scratch set-up copy failed: %s", cudaGetErrorString(ce));
+
+  int am = 0, cblocks = 0, ktot = 0, cpad = 0;
+  tc_layout(CONVF_VARIANT_IMPLICIT_GEMM_GATHER, s, &am, &cblocks, &ktot, &cpad);
+  int bn = 0;
+  bool pair = false;
+  pick_tile(s.M, s.K, ktot / 64, num_sms, desc->tile_n ? desc->tile_n : 128, 1, &bn, &pair);
+  if (desc->tile_n) bn = desc->tile_n;
+  const int n_blocks = (s.K + bn - 1) / bn;
+  const long long tiles = (s.M + 127) / 128 * n_blocks;
+  const int grid = (int)std::min<long long>(tiles, num_sms);
+
+  CUtensorMap tmA, tmB, tmY;
+  std::memset(&tmA, 0, sizeof tmA);
+  const cuuint32_t es[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)ktot, (cuuint64_t)s.K};
+    const cuuint64_t strides[1] = {(cuuint64_t)ktot * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)bn};
+    CUresult r = g_encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_packed), dims, strides,
+                                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "weight tensor map encoding failed (CUresult %d)", (int)r);
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)s.K * 4};
+    const cuuint32_t box[2] = {32, 128};
+    CUresult r = g_encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "output tensor map encoding failed (CUresult %d)", (int)r);
+  }
+
+  ce = launch_pad_channels(static_cast<const uint16_t*>(x), xpad, (long long)s.N * s.H * s.W, s.C, cpt, num_sms, strm);
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "channel pre-pass launch failed: %s", cudaGetErrorString(ce));
+  float lo, hi;
+  act_bounds(desc, &lo, &hi);
+  TcConvParams p{};
+  p.M = (int)s.M; p.Kout = s.K; p.num_kb = ktot / 64; p.cblocks = 0; p.R = s.R; p.S = s.S;
+  p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
+  p.H = s.H; p.W = s.W; p.C = cpt; p.Ho = s.Ho; p.Wo = s.Wo;
+  p.n_blocks = n_blocks; p.num_tiles = (int)tiles; p.a_mode = kAGather;
+  p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status;
+  p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
+  switch (bn) {
+    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, tmY, grid, true, false, strm); break;
+    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, tmY, grid, true, false, strm); break;
+    default: ce = launch_tc_conv_bn128(p, tmA, tmB, tmY, grid, true, false, strm); break;
+  }
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
+  return ok();
+}

@@ -183,6 +183,32 @@ const char* conv_fused_last_error(void);
 convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles,
                                           void* stream);
 
+/* Allocation-free run (this entry point has no counterpart in the method's sources; it serves
+ * callers that cannot allocate device memory — e.g. code that runs while a CUDA graph is being
+ * captured, inside a fixed device-memory budget that a host framework owns, or on a real-time
+ * path where an allocation's latency or failure is not acceptable).  It runs the gathered-row
+ * tcgen05 conv (convs with at most 8 input channels, such as an RGB stem, whose 128-row output
+ * tiles stay inside one image) without a handle and without any allocation: the caller passes
+ * every buffer, and the only scratch (the input with channels padded to whole taps, the padded
+ * epilogue vectors and a status word) lives in a 16 MiB device array that the library reserves
+ * on every GPU that loads it, until the process exits.
+ *   desc:      as for create (NHWC storage; tile_n <= 128; cta_pair 0 or 1).
+ *   x, y:      device, NHWC bf16 in / fp32 out, 16-byte aligned.
+ *   w_packed:  device, the weights prepacked for CONVF_VARIANT_IMPLICIT_GEMM_GATHER exactly as
+ *              conv_fused_pack_weights writes them ([K][ktot] bf16 bits), 16-byte aligned.
+ *   scale, bias: device float[K], the folded epilogue y = clamp(scale*acc + bias, lo, hi)
+ *              (bias = bn_scale*B + bn_shift).
+ *   status_dev: optional device int32 that receives the timeout bit (1) if a bounded wait ran
+ *              out (NULL: not reported).
+ * Sizes needing more scratch than 16 MiB are refused with CONVF_ERR_UNSUPPORTED.  The first call
+ * on a device looks up the scratch array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the one scratch array: calls whose
+ * work overlaps on the GPU (other streams, or without ordering between them) race on it.
+ * Asynchronous on `stream`; it never calls cudaMalloc, cudaFree or an allocating routine. */
+convf_status conv_fused_run_noalloc(const convf_desc* desc, const void* x, const void* w_packed,
+                                    const float* scale, const float* bias, void* y,
+                                    int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
