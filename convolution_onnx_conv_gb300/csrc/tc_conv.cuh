@@ -4,14 +4,16 @@
 // never materialised): rows m = (n, oh, ow), M = N*Ho*Wo; columns = output channels K;
 // reduction over (tap r,s; channel c) in 64-wide blocks.  One CTA per SM loops over 128 x BN
 // output tiles.  Warp roles:
-//   warp 0      TMA producer: weight tile (2D tiled load) and, except in gather mode, the
-//               activation tile (2D tiled load for 1x1/stride-1/pad-0, else an im2col load
-//               whose tap offsets select the filter position; padding is TMA zero fill)
+//   warp 0      activation producer: TMA activation tile (2D tiled load for 1x1/stride-1/pad-0,
+//               else an im2col load whose tap offsets select the filter position; padding is
+//               TMA zero fill); in gather mode the per-tile bulk copies of input rows
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue into a double-buffered
 //               fp32 accumulator (2 x BN TMEM columns)
-//   warps 2-5   epilogue: tcgen05.ld -> y = clamp(scale[k]*acc + bias[k], lo, hi) -> swizzled
-//               smem staging -> TMA store (clips the ragged M and K edges)
-//   warps 6-13  (gather mode only) activation rows gathered by threads, for channel counts
+//   warp 2      weight producer: TMA weight tile (2D tiled load)
+//   warps 3-10  epilogue, two warpgroups on alternate 32-column chunks (warps 3-6 only in
+//               gather mode): tcgen05.ld -> y = clamp(scale[k]*acc + bias[k], lo, hi) ->
+//               swizzled smem staging -> TMA store (clips the ragged M and K edges)
+//   warps 7-14  (gather mode only) activation rows gathered by threads, for channel counts
 //               that TMA cannot address (C not a multiple of 8, e.g. a 3-channel stem)
 #pragma once
 #include "convf_internal.h"
@@ -32,20 +34,26 @@ template <int BN, bool GATHER, bool PAIR>
 struct TcCfg {
   // with a CTA pair each CTA holds half of the weight tile (BN/2 rows)
   static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * kBK * 2;
+  // two epilogue warpgroups (alternate 32-column chunks) except in gather mode, whose extra
+  // warps take the register and smem room
+  static constexpr int kEpiGroups = GATHER ? 1 : 2;
+  static constexpr int kThreads = 96 + 128 * kEpiGroups + (GATHER ? kGatherThreads : 0);
+  // operand ingest per SM does not grow with pipeline depth, so stages give way to the epilogue
   static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3)
-                                        : (PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8)));
+                                        : (PAIR ? (BN == 256 ? 5 : (BN == 128 ? 6 : 8))
+                                                : (BN == 256 ? 3 : (BN == 128 ? 5 : (BN == 64 ? 6 : 8))));
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
   // gather mode: two buffers for the input rows one tile needs (TcConvParams::patch_rows)
   static constexpr int kPatchBytes = GATHER ? 2 * kPatchBufBytes : 0;
-  static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + kNumEpiBuf * kEpiTileBytes +
+  static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + kEpiGroups * kNumEpiBuf * kEpiTileBytes +
                                kPatchBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
 };
 
 template <int BN, bool GATHER, bool PAIR>
-__global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
+__global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
@@ -65,7 +73,7 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATileBytes;
   uint8_t* sEpi = sB + kStages * Cfg::kBTileBytes;
-  uint8_t* sPatch = sEpi + kNumEpiBuf * kEpiTileBytes;
+  uint8_t* sPatch = sEpi + Cfg::kEpiGroups * kNumEpiBuf * kEpiTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPatch + Cfg::kPatchBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -77,20 +85,21 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // go/abort decisions broadcast by a leader thread through a named barrier; two slots used
   // alternately so the leader never overwrites a flag another thread has yet to read
-  volatile int* epi_go = abort_flag + 1;
-  volatile int* gat_go = abort_flag + 3;
+  volatile int* epi_go = abort_flag + 1;   // two slots per epilogue group
+  volatile int* gat_go = abort_flag + 5;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], GATHER ? 1 + kGatherThreads : 1);
+      // weight producer + (activation producer | one arrival per gather warp)
+      mbar_init(&full[s], GATHER ? 1 + kGatherThreads / 32 : 2);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], PAIR ? 256 : 128);
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4 * Cfg::kEpiGroups);   // one arrival per epilogue warp
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 1);
     }
@@ -98,10 +107,10 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmY);
     if (!GATHER) tma_prefetch_desc(&tmA);
   }
+  if (warp == 2 && lane == 0) tma_prefetch_desc(&tmB);
   if (warp == 1) {
     if (PAIR) {
       tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
@@ -121,31 +130,35 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
   pdl_wait_prior();
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ activation producer
+    // (TMA activation tiles; in gather mode the per-tile input-row bulk copies instead).  A TMA
+    // operation holds its issuing warp for a few hundred cycles, so activations and weights are
+    // issued from two different warps.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      const uint32_t tx = Cfg::kBTileBytes + (GATHER ? 0 : kATileBytes);
       int it = 0;
       for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
         const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
-        const int n0 = (tile % p.n_blocks) * BN;
-        if (GATHER && p.patch_rows > 0) {
-          // bulk-copy the input rows this tile reads (whole rows of W*C bf16) into smem
-          const int pb = it & 1;
-          if (!mbar_wait(&pempty[pb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) goto teardown;
-          const int hw = p.Ho * p.Wo;
-          const int img = m0 / hw;
-          const int ih_first = ((m0 - img * hw) / p.Wo) * p.sh - p.pt;
-          int valid = 0;
-          for (int i = 0; i < p.patch_rows; ++i) valid += (ih_first + i >= 0 && ih_first + i < p.H);
-          mbar_arrive_expect_tx(&pfull[pb], static_cast<uint32_t>(valid * p.row_bytes));
-          for (int i = 0; i < p.patch_rows; ++i) {
-            const int ih = ih_first + i;
-            if (ih >= 0 && ih < p.H)
-              bulk_load(sPatch + pb * kPatchBufBytes + i * p.row_bytes,
-                        p.x + (static_cast<size_t>(img) * p.H + ih) * p.W * p.C, p.row_bytes, &pfull[pb]);
+        if (GATHER) {
+          if (p.patch_rows > 0) {
+            // bulk-copy the input rows this tile reads (whole rows of W*C bf16) into smem
+            const int pb = it & 1;
+            if (!mbar_wait(&pempty[pb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) goto teardown;
+            const int hw = p.Ho * p.Wo;
+            const int img = m0 / hw;
+            const int ih_first = ((m0 - img * hw) / p.Wo) * p.sh - p.pt;
+            int valid = 0;
+            for (int i = 0; i < p.patch_rows; ++i) valid += (ih_first + i >= 0 && ih_first + i < p.H);
+            mbar_arrive_expect_tx(&pfull[pb], static_cast<uint32_t>(valid * p.row_bytes));
+            for (int i = 0; i < p.patch_rows; ++i) {
+              const int ih = ih_first + i;
+              if (ih >= 0 && ih < p.H)
+                bulk_load(sPatch + pb * kPatchBufBytes + i * p.row_bytes,
+                          p.x + (static_cast<size_t>(img) * p.H + ih) * p.W * p.C, p.row_bytes, &pfull[pb]);
+            }
           }
+          continue;
         }
         int img = 0, hb = 0, wb = 0;
         if (p.a_mode == kAIm2col) {
@@ -161,32 +174,49 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
           // a pair's loads all complete on the leader's barrier, which expects both CTAs' bytes
-          if (!PAIR || leader) mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * tx : tx);
+          if (!PAIR || leader) mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * kATileBytes : kATileBytes);
           const uint32_t fbar = PAIR ? map_to_rank(smem_u32(&full[stage]), 0) : 0;
-          if (!GATHER) {
-            uint8_t* dA = sA + stage * kATileBytes;
-            if (p.a_mode == kA2D) {
-              if (PAIR)
-                tma_load_2d_pair(dA, &tmA, fbar, kb * kBK, m0);
-              else
-                tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
-            } else {
-              const int r = tap / p.S;
-              const int s = tap - r * p.S;
-              if (PAIR)
-                tma_load_im2col_4d_pair(dA, &tmA, fbar, cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
-                                        static_cast<uint16_t>(r * p.dh));
-              else
-                tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img,
-                                   static_cast<uint16_t>(s * p.dw), static_cast<uint16_t>(r * p.dh));
-              if (++cb == p.cblocks) {
-                cb = 0;
-                ++tap;
-              }
+          uint8_t* dA = sA + stage * kATileBytes;
+          if (p.a_mode == kA2D) {
+            if (PAIR)
+              tma_load_2d_pair(dA, &tmA, fbar, kb * kBK, m0);
+            else
+              tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
+          } else {
+            const int r = tap / p.S;
+            const int s = tap - r * p.S;
+            if (PAIR)
+              tma_load_im2col_4d_pair(dA, &tmA, fbar, cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
+                                      static_cast<uint16_t>(r * p.dh));
+            else
+              tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
+                                 static_cast<uint16_t>(r * p.dh));
+            if (++cb == p.cblocks) {
+              cb = 0;
+              ++tap;
             }
           }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ weight producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = tstart; tile < p.num_tiles; tile += tstep) {
+        const int n0 = (tile % p.n_blocks) * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
+          if (!PAIR || leader)
+            mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * Cfg::kBTileBytes : Cfg::kBTileBytes);
           if (PAIR)
-            tma_load_2d_pair(sB + stage * Cfg::kBTileBytes, &tmB, fbar, kb * kBK, n0 + static_cast<int>(crank) * (BN / 2));
+            tma_load_2d_pair(sB + stage * Cfg::kBTileBytes, &tmB, map_to_rank(smem_u32(&full[stage]), 0), kb * kBK,
+                             n0 + static_cast<int>(crank) * (BN / 2));
           else
             tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
           if (++stage == kStages) {
@@ -240,11 +270,19 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
         }
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 3 + 4 * Cfg::kEpiGroups) {
     // ------------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;       // 0..127
+    // kEpiGroups warpgroups; group eg takes the 32-column chunks eg, eg + kEpiGroups, ... of
+    // every tile, with its own staging buffers and named barrier.
+    constexpr int G = Cfg::kEpiGroups;
+    const int et = threadIdx.x - 96;
+    const int eg = et >> 7;                // epilogue group
+    const int el = et & 127;               // index within the group (0 = leader)
+    const int bar_id = 1 + 2 * eg;         // named barriers 1 and 3 (2 belongs to the gatherers)
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;         // tile row == TMEM lane
+    uint8_t* epi = sEpi + eg * kNumEpiBuf * kEpiTileBytes;
+    volatile int* go = epi_go + 2 * eg;
     int acc = 0;
     uint32_t acc_phase = 0;
     int ebuf = 0;
@@ -252,25 +290,32 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
       const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
       const int n0 = (tile % p.n_blocks) * BN;
-      if (et == 0) epi_go[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
-      named_barrier(1, 128);
-      if (!epi_go[it & 1]) break;
+      if (el == 0) go[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
+      named_barrier(bar_id, 128);
+      if (!go[it & 1]) break;
       tc_fence_after();
       const int left = p.Kout - n0;
       const int nchunks = left >= BN ? BN / kEpiCols : (left + kEpiCols - 1) / kEpiCols;
-      for (int ch = 0; ch < nchunks; ++ch) {
+      bool released = false;
+      for (int ch = eg; ch < nchunks; ch += G) {
         const int nc = n0 + ch * kEpiCols;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * BN + ch * kEpiCols),
                            v);
         tmem_ld_wait();
-        if (ch == nchunks - 1) {
+        if (ch + G >= nchunks) {
+          // the warp's last TMEM read of the tile: release the accumulator buffer (one arrival
+          // per warp; tcgen05.ld is warp-collective, so the whole warp is here)
           tc_fence_before();
-          if (PAIR && !leader)
-            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
-          else
-            mbar_arrive(&tempty[acc]);
+          __syncwarp();
+          if (lane == 0) {
+            if (PAIR && !leader)
+              mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+            else
+              mbar_arrive(&tempty[acc]);
+          }
+          released = true;
         }
         const float4* sc4 = reinterpret_cast<const float4*>(p.scale + nc);
         const float4* bi4 = reinterpret_cast<const float4*>(p.bias + nc);
@@ -285,28 +330,39 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
           o[4 * j4 + 3] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 3]), sc.w, bi.w), p.lo), p.hi);
         }
         // the staging buffer used two chunks ago must have been read out by its TMA store
-        if (et == 0) bulk_wait_read<1>();
-        named_barrier(1, 128);
-        uint8_t* buf = sEpi + ebuf * kEpiTileBytes + row * 128;
+        if (el == 0) bulk_wait_read<1>();
+        named_barrier(bar_id, 128);
+        uint8_t* buf = epi + ebuf * kEpiTileBytes + row * 128;
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
           *reinterpret_cast<float4*>(buf + ((c16 ^ (row & 7)) << 4)) =
               make_float4(o[4 * c16], o[4 * c16 + 1], o[4 * c16 + 2], o[4 * c16 + 3]);
         }
         fence_proxy_async_smem();
-        named_barrier(1, 128);
-        if (et == 0) {
-          tma_store_2d(&tmY, sEpi + ebuf * kEpiTileBytes, nc, m0);
+        named_barrier(bar_id, 128);
+        if (el == 0) {
+          tma_store_2d(&tmY, epi + ebuf * kEpiTileBytes, nc, m0);
           bulk_commit();
         }
         ebuf ^= 1;
+      }
+      if (!released) {
+        // no chunk of this tile fell to this group: nothing read, release at once
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && !leader)
+            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+          else
+            mbar_arrive(&tempty[acc]);
+        }
       }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
     }
-    if (et == 0) bulk_wait_all();
+    if (el == 0) bulk_wait_all();
   } else if (GATHER) {
     // ------------------------------------------------------------------ row gatherers
     // 256 threads, two per tile row: thread gt assembles half gh of row gr in every k-block
@@ -314,7 +370,7 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
     // j = (r*S + s)*Cp + c.  With p.patch_rows > 0 the rows come from the tile's input rows that
     // the producer bulk-copied into smem; with cpt > 0 the input already holds whole taps of
     // cpt channels (zero-padded by pad_channels_kernel) and each tap is one vector read.
-    const int gt = threadIdx.x - 192;
+    const int gt = threadIdx.x - 96 - 128 * Cfg::kEpiGroups;
     const int gr = gt & 127;
     const int gh = gt >> 7;
     int stage = 0;
@@ -427,7 +483,8 @@ __global__ void __launch_bounds__(GATHER ? 192 + kGatherThreads : 192, 1)
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&full[stage]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);   // one arrival per gather warp
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
@@ -473,7 +530,7 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
     }
     configured = true;
   }
-  return launch_pdl(k, dim3(grid), dim3(GATHER ? 192 + kGatherThreads : 192), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
+  return launch_pdl(k, dim3(grid), dim3(TcCfg<BN, GATHER, PAIR>::kThreads), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
                     PAIR ? 2 : 1, p, tmA, tmB, tmY);
 }
 
