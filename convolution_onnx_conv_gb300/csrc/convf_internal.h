@@ -83,6 +83,7 @@ struct DwParams {
   const float* bias;      // [C]
   float* y;               // NHWC fp32
   float lo, hi;
+  int th;                 // output rows walked per thread (set by the launcher)
 };
 cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream);
 
