@@ -29,7 +29,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_plan", "conv_fused_pack_weights", "conv_fused_create", "conv_fused_run",
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
-            "conv_fused_watchdog_selftest", "conv_fused_run_noalloc"]
+            "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -107,6 +107,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_last_error.restype = ctypes.c_char_p
     lib.conv_fused_watchdog_selftest.argtypes = [vp, ctypes.c_longlong, vp]
     lib.conv_fused_run_noalloc.argtypes = [dptr, vp, vp, vp, vp, vp, vp, vp]
+    lib.conv_fused_measure_int8_mma_rate.argtypes = [vp, P(ctypes.c_double)]
     for name in EXPORTED:
         if name not in ("conv_fused_destroy", "conv_fused_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -220,6 +221,14 @@ def conv_fused_describe(handle: int) -> str:
 def conv_fused_watchdog_selftest(status_dev, budget_cycles: int, stream=None):
     s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
     _check(load_library().conv_fused_watchdog_selftest(_addr(status_dev), int(budget_cycles), s))
+
+
+def conv_fused_measure_int8_mma_rate(stream=None) -> float:
+    """TOP/s of back-to-back int8 mma.sync on this GPU (register operands)."""
+    s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
+    out = ctypes.c_double()
+    _check(load_library().conv_fused_measure_int8_mma_rate(s, ctypes.byref(out)))
+    return out.value
 
 
 def conv_fused_run_noalloc(desc: ConvDesc, x, w_packed, scale, bias, y, status=None, stream=None):

@@ -850,6 +850,16 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   return ok();
 }
 
+convf_status conv_fused_measure_int8_mma_rate(void* stream, double* tops) {
+  if (!tops) return fail(CONVF_ERR_INVALID_ARG, "tops is NULL");
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce == cudaSuccess) ce = measure_s8_mma_rate(sms, static_cast<cudaStream_t>(stream), tops);
+  if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "int8 MMA rate measurement failed: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
 convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles, void* stream) {
   if (!status_dev) return fail(CONVF_ERR_INVALID_ARG, "status_dev is NULL");
   if (budget_cycles < 1 || budget_cycles > 20000000000LL)

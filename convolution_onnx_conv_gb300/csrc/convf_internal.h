@@ -101,6 +101,7 @@ struct S8Params {
   int zp, relu;
 };
 cudaError_t launch_s8_conv(const S8Params& p, cudaStream_t stream);
+cudaError_t measure_s8_mma_rate(int num_sms, cudaStream_t stream, double* tops);
 
 // ---------------------------------------------------------------- watchdog self-test
 cudaError_t launch_watchdog_selftest(int32_t* status, long long budget, cudaStream_t stream);

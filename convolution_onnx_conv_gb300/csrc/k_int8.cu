@@ -166,6 +166,52 @@ __global__ void __launch_bounds__(256, 1) s8_conv_kernel(const S8Params p) {
   }
 }
 
+// Rate of the int8 warp-level MMA on this GPU: every warp issues back-to-back m16n8k32 MMAs on
+// register operands into 8 independent accumulators (no memory traffic), the roofline
+// denominator of the int8 path.
+__global__ void __launch_bounds__(256) s8_mma_rate_kernel(int iters, int* sink) {
+  int acc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0;
+  const uint32_t t = threadIdx.x;
+  const uint32_t a[4] = {t * 0x01010101u, t * 0x02030405u, t ^ 0x7F7F7F7Fu, t + 0x11111111u};
+  const uint32_t b0 = t * 0x03050709u, b1 = t ^ 0x55AA55AAu;
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mma_s8_16832(acc[j], a, b0, b1);
+  }
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sum += acc[j][e];
+  if (sum == 0x7FFFFFFF) sink[0] = sum;   // keeps the MMAs live
+}
+
+cudaError_t measure_s8_mma_rate(int num_sms, cudaStream_t stream, double* tops) {
+  int* sink = nullptr;
+  cudaError_t e = cudaSuccess;
+  const int iters = 4096, blocks = num_sms * 4;
+  cudaEvent_t e0, e1;
+  if ((e = cudaEventCreate(&e0)) != cudaSuccess) return e;
+  if ((e = cudaEventCreate(&e1)) != cudaSuccess) return e;
+  s8_mma_rate_kernel<<<blocks, 256, 0, stream>>>(64, sink);   // warm-up
+  cudaEventRecord(e0, stream);
+  s8_mma_rate_kernel<<<blocks, 256, 0, stream>>>(iters, sink);
+  cudaEventRecord(e1, stream);
+  e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return e;
+  const double ops = 2.0 * 16 * 8 * 32 * 8.0 * iters * (blocks * 8.0);
+  *tops = ops / (ms * 1e-3) / 1e12;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_s8_conv(const S8Params& p, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {

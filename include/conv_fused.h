@@ -183,6 +183,11 @@ const char* conv_fused_last_error(void);
 convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles,
                                           void* stream);
 
+/* Measurement helper (the int8 path's roofline denominator): times back-to-back
+ * mma.sync.m16n8k32 int8 MMAs on register operands over every SM of the current device and
+ * returns the rate in TOP/s (2 ops per multiply-add).  Synchronises `stream`. */
+convf_status conv_fused_measure_int8_mma_rate(void* stream, double* tops);
+
 /* Allocation-free run (this entry point has no counterpart in the method's sources; it serves
  * callers that cannot allocate device memory — e.g. code that runs while a CUDA graph is being
  * captured, inside a fixed device-memory budget that a host framework owns, or on a real-time

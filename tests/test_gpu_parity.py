@@ -266,6 +266,11 @@ def test_back_to_back_runs_reuse_buffers():
     assert torch.equal(y1, y5)
 
 
+def test_int8_mma_rate_measurement():
+    tops = cf.conv_fused_measure_int8_mma_rate()
+    assert 1.0 < tops < 20000.0
+
+
 def test_watchdog_gives_up_and_reports():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     cf.conv_fused_watchdog_selftest(status, 2_000_000)     # ~1 ms: nobody ever arrives
