@@ -729,6 +729,26 @@ convf_status encode_io_maps(convf_handle* h, const void* x, const void* y) {
 }
 }  // namespace
 
+namespace {
+// depthwise 3x3: 4-D tiled map over x {C, W, H, N}, box = one tile's input window x 32 channels
+convf_status encode_dw_map(convf_handle* h, const void* x) {
+  const Shape& s = h->s;
+  if (!load_encoders()) return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  int bw = 0, bh = 0, bn = 0;
+  dw_tile_box(s.sh, s.Wo, &bw, &bh, &bn);
+  const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2, (cuuint64_t)s.H * s.W * s.C * 2};
+  const cuuint32_t box[4] = {32, (cuuint32_t)bw, (cuuint32_t)bh, (cuuint32_t)bn};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box,
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "depthwise tensor map encoding failed (CUresult %d)", (int)r);
+  h->map_x = x;
+  return CONVF_OK;
+}
+}  // namespace
+
 convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream) {
   convf_status st = check_handle(h);
   if (st != CONVF_OK) return st;
@@ -753,8 +773,11 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.Ho = s.Ho; p.Wo = s.Wo; p.R = s.R; p.S = s.S;
       p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl; p.dh = s.dh; p.dw = s.dw;
       p.x = static_cast<const uint16_t*>(x); p.taps = h->taps; p.bias = h->bias; p.y = static_cast<float*>(y);
-      p.lo = h->lo; p.hi = h->hi;
-      ce = launch_depthwise(p, h->num_sms, strm);
+      p.lo = h->lo; p.hi = h->hi; p.status = h->status;
+      if (dw_uses_tma(p) && x != h->map_x) {
+        if ((st = encode_dw_map(h, x)) != CONVF_OK) return st;
+      }
+      ce = launch_depthwise(p, &h->tmA, h->num_sms, strm);
       break;
     }
     case CONVF_VARIANT_INT8: {

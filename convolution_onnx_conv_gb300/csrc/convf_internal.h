@@ -74,6 +74,23 @@ struct TcConvParams {
 cudaError_t launch_pad_channels(const uint16_t* x, uint16_t* out, long long pixels, int C, int cpt, int num_sms,
                                 cudaStream_t stream);
 
+// Division by a run-time invariant d >= 1 as a multiply-high, add and shift (the round-up
+// method of Granlund and Montgomery, "Division by invariant integers using multiplication",
+// 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, the quotient of any
+// n < 2^31 is (umulhi(n, m) + n) >> l, and the sum cannot overflow 32 bits.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{d, 0, 0};
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+  return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) { return (__umulhi(n, f.m) + n) >> f.l; }
+#endif
+
 // ---------------------------------------------------------------- depthwise (CUDA cores)
 struct DwParams {
   int N, C, H, W, Ho, Wo, R, S;
@@ -83,9 +100,14 @@ struct DwParams {
   const float* bias;      // [C]
   float* y;               // NHWC fp32
   float lo, hi;
-  int th;                 // output rows walked per thread (set by the launcher)
+  int* status;            // device status word (watchdog bit)
+  FastDiv f_slabs, f_owbs, f_ohbs;   // tile-index decoding (set by the launcher)
 };
-cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream);
+// tmX: 4-D tiled map {C, W, H, N} of x with box {32, box_w, box_h, box_n} from dw_tile_box();
+// used by the 3x3 dilation-1 strides-{1,2} kernel, ignored by the general one.
+bool dw_uses_tma(const DwParams& p);
+void dw_tile_box(int stride, int Wo, int* box_w, int* box_h, int* box_n);
+cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- int8 implicit GEMM
 struct S8Params {

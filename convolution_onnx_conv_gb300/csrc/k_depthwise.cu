@@ -1,15 +1,19 @@
 // Depthwise convolution (group == C == K) on CUDA cores: memory-bound (about 2-3 flop per
 // byte), so no tensor cores.  NHWC bf16 in, fp32 taps with the BN scale folded in, fp32 out.
-// Each thread owns 8 channels (one 16-byte vector) x kOW = 2 consecutive outputs of a column
-// strip; consecutive threads take consecutive channel vectors of the same pixel, so every load
-// and store is a coalesced 128-bit access.  Inputs shared by neighbouring columns are re-read
-// through L1/L2, not from HBM; inputs shared by neighbouring rows stay in registers.
+//
+// 3x3, dilation 1, strides {1, 2}: a persistent kernel over tiles of 7 output rows x 16 output
+// columns x 32 channels.  One thread per CTA streams each tile's input window (with its halo)
+// into a ring of shared-memory stages with a single 4-D TMA load, so the loads of the next
+// tiles are in flight while the current one is computed and no register holds a byte in flight;
+// padding is the TMA's zero fill.  Each thread owns 4 channels of one output column and walks
+// the window's input rows once, scattering every converted row into the (up to three) output
+// rows it feeds, then stores each output row as one 16-byte vector as soon as it is complete.
 #include "convf_internal.h"
 #include "ptx.cuh"
 
-namespace convf {
+#include <mutex>
 
-constexpr int kOW = 2;
+namespace convf {
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -22,121 +26,205 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 
 __device__ __forceinline__ float clampf(float v, float lo, float hi) { return fminf(fmaxf(v, lo), hi); }
 
-// 3x3, dilation 1, equal strides SW in {1, 2}.  Each thread owns 8 channels x kOW outputs of a
-// column and walks down p.th output rows, keeping the 3 input rows it needs in registers: per
-// new output row it loads only the SW new input rows (NCOL 16-byte vectors each), all issued
-// before the arithmetic.  Padding reads as zero without a branch.  The strip height p.th is
-// chosen by the host so that enough threads run to keep the memory system busy.
+// Two fp32 lanes in one 64-bit register pair, for the packed fp32 FMA of sm_100-class SMs
+// (two independent round-to-nearest fused multiply-adds per instruction).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack_f32x2(uint32_t lo_bits, uint32_t hi_bits) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+  return r;
+}
+__device__ __forceinline__ f32x2 pack_f32x2(float lo, float hi) {
+  return pack_f32x2(__float_as_uint(lo), __float_as_uint(hi));
+}
+__device__ __forceinline__ void unpack_f32x2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// a 32-bit word holding two bf16 values (channel e in the low half) -> fp32 pair (e, e+1)
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
+
+// Column lanes per image in a tile: 16, or 8 when the output is at most 8 columns wide, in
+// which case one tile holds two images (the 16 lanes stay busy on 7-wide layers).
+__host__ __device__ __forceinline__ int dw_tile_cols(int Wo) { return Wo <= 8 ? 8 : 16; }
+
 template <int SW>
-__global__ void __launch_bounds__(256, 2) dw3x3_kernel(const DwParams p) {
+struct DwTile {
+  static constexpr int kTH = 7;                          // output rows per tile
+  static constexpr int kLanes = 16;                      // output columns per tile (all images)
+  static constexpr int kCS = 32;                         // channels per tile (64-byte TMA rows)
+  static constexpr int kThreads = kLanes * kCS / 4;      // 4 channels per thread: 128
+  static constexpr int kInH = (kTH - 1) * SW + 3;        // input window rows: 9 or 15
+  __host__ __device__ static constexpr int in_w(int cols) { return (cols - 1) * SW + 3; }
+  __host__ __device__ static constexpr int bytes(int cols) { return (kLanes / cols) * kInH * in_w(cols) * kCS * 2; }
+  static constexpr int kMaxBytes = bytes(16) > bytes(8) ? bytes(16) : bytes(8);
+  static constexpr int kStageBytes = (kMaxBytes + 127) / 128 * 128;
+  static constexpr int kStages = SW == 1 ? 3 : 2;
+  static constexpr int kSlots = SW == 1 ? 3 : 2;         // output rows accumulated at once
+  static constexpr int kSmem = kStages * kStageBytes + 128 + 2 * 8 * kStages;
+};
+
+template <int SW, int TCOLS>
+__global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                         const DwParams p) {
+  using T = DwTile<SW>;
+  extern __shared__ uint8_t dw_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dw_smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kStages * T::kStageBytes);
+  uint64_t* empty = full + T::kStages;
+  __shared__ int abort_flag;
+  volatile int* abort_v = &abort_flag;
+
+  const int tid = threadIdx.x;
+  const int cq = tid & 7;                  // 4-channel group within the tile's 32 channels
+  const int lane = tid >> 3;               // output column lane of the tile
+  constexpr int tcols = TCOLS;
+  constexpr int nb = T::kLanes / tcols;    // images per tile
+  constexpr int in_w = T::in_w(tcols);
+  constexpr uint32_t tile_bytes = T::bytes(tcols);
+  const int img = lane / tcols;            // this lane's image within the tile
+  const int col = lane - img * tcols;      // and its output column within the column block
+  if (tid == 0) {
+#pragma unroll
+    for (int st = 0; st < T::kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], T::kThreads / 32);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    abort_flag = 0;
+  }
+  __syncthreads();
   pdl_launch_dependents();
   pdl_wait_prior();
-  // grid.y walks (image, strip of kTH output rows); grid.x x 256 threads cover (output column
-  // block, channel vector) of a row, with 32-bit index arithmetic
-  const int C8 = p.C >> 3;
-  const int owb_n = (p.Wo + kOW - 1) / kOW;
-  const int row_items = owb_n * C8;
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= row_items) return;
-  const int c8 = j % C8;
-  const int owb = j / C8;
-  const int c0 = c8 * 8;
-  const int ow0 = owb * kOW;
-  const int iw_base = ow0 * SW - p.pl;
-  constexpr int NCOL = (kOW - 1) * SW + 3;
-  const int strips = (p.Ho + p.th - 1) / p.th;
 
-  float bias[8];
-  {
-    const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.bias + c0));
-    const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.bias + c0 + 4));
-    bias[0] = b0.x; bias[1] = b0.y; bias[2] = b0.z; bias[3] = b0.w;
-    bias[4] = b1.x; bias[5] = b1.y; bias[6] = b1.z; bias[7] = b1.w;
+  const int slabs = p.f_slabs.d;
+  const int owbs = p.f_owbs.d;
+  const int ohbs = p.f_ohbs.d;
+  const int units = (p.N + nb - 1) / nb * ohbs * owbs * slabs;
+  const int G = gridDim.x;
+  int issued = 0, waited = 0;   // tiles whose loads this thread issued / saw land (thread 0's count)
+
+  // tile u -> (slab fastest, then column block, row block, image group)
+  auto decode = [&](uint32_t u, int& slab, int& owb, int& ohb, int& ng) {
+    const uint32_t t = fast_div(u, p.f_slabs);
+    slab = static_cast<int>(u - t * p.f_slabs.d);
+    const uint32_t t2 = fast_div(t, p.f_owbs);
+    owb = static_cast<int>(t - t2 * p.f_owbs.d);
+    ng = static_cast<int>(fast_div(t2, p.f_ohbs));
+    ohb = static_cast<int>(t2 - ng * p.f_ohbs.d);
+  };
+  // load this CTA's j-th tile (tile index u) into stage j % kStages, once every warp has
+  // released that stage's previous tile (j - kStages)
+  auto issue = [&](int j, int u) {
+    const int stage = j % T::kStages;
+    if (j >= T::kStages && !mbar_wait(&empty[stage], ((j / T::kStages) - 1) & 1, abort_v, p.status)) return;
+    int slab, owb, ohb, ng;
+    decode(u, slab, owb, ohb, ng);
+    mbar_arrive_expect_tx(&full[stage], tile_bytes);
+    tma_load_4d(smem + stage * T::kStageBytes, &tmX, &full[stage], slab * T::kCS, owb * tcols * SW - p.pl,
+                ohb * T::kTH * SW - p.pt, ng * nb);
+    ++issued;
+  };
+  if (tid == 0) {
+#pragma unroll
+    for (int j = 0; j < T::kStages - 1; ++j)
+      if (static_cast<int>(blockIdx.x) + j * G < units) issue(j, blockIdx.x + j * G);
   }
 
-  for (int ns = blockIdx.y; ns < p.N * strips; ns += gridDim.y) {
-    const int n = ns / strips;
-    const int oh_begin = (ns - n * strips) * p.th;
-    const int oh_end = min(oh_begin + p.th, p.Ho);
-    const uint16_t* ximg = p.x + static_cast<size_t>(n) * p.H * p.W * p.C + c0;
-    auto load_row = [&](int ih, uint4 (&dst)[NCOL]) {
-      const bool row_ok = ih >= 0 && ih < p.H;
-      const uint16_t* xrow = ximg + static_cast<size_t>(row_ok ? ih : 0) * p.W * p.C;
+  f32x2 tap[9][2], bias[2];    // channel pairs (c, c+1), (c+2, c+3)
+  int cur_slab = -1;
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += G, ++k) {
+    if (*abort_v) break;
+    const int stage = k % T::kStages;
+    if (tid == 0 && u + (T::kStages - 1) * G < units) issue(k + T::kStages - 1, u + (T::kStages - 1) * G);
+    if (!mbar_wait(&full[stage], (k / T::kStages) & 1, abort_v, p.status)) break;
+    waited = k + 1;
+    int slab, owb, ohb, n;
+    decode(u, slab, owb, ohb, n);
+    n = n * nb + img;
+    const int c = slab * T::kCS + cq * 4;
+    const bool c_ok = c < p.C;
+    if (slab != cur_slab) {
+      cur_slab = slab;
 #pragma unroll
-      for (int col = 0; col < NCOL; ++col) {
-        const int iw = iw_base + col;
-        dst[col] = (row_ok && iw >= 0 && iw < p.W)
-                       ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(iw) * p.C))
-                       : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 9; ++j) {
+        const float4 v = c_ok ? __ldg(reinterpret_cast<const float4*>(p.taps + j * p.C + c)) : make_float4(0, 0, 0, 0);
+        tap[j][0] = pack_f32x2(v.x, v.y);
+        tap[j][1] = pack_f32x2(v.z, v.w);
       }
-    };
-    // window rows: win[0..2] = input rows oh*SW - pt + 0..2
-    uint4 win[3][NCOL];
-    const int ih0 = oh_begin * SW - p.pt;
-    if (SW == 1) {
-      load_row(ih0, win[0]);
-      load_row(ih0 + 1, win[1]);
-    } else {
-      load_row(ih0, win[0]);
+      const float4 b = c_ok ? __ldg(reinterpret_cast<const float4*>(p.bias + c)) : make_float4(0, 0, 0, 0);
+      bias[0] = pack_f32x2(b.x, b.y);
+      bias[1] = pack_f32x2(b.z, b.w);
     }
-    for (int oh = oh_begin; oh < oh_end; ++oh) {
-      const int ihb = oh * SW - p.pt;
-      if (SW == 1) {
-        load_row(ihb + 2, win[2]);
-      } else {
-        load_row(ihb + 1, win[1]);
-        load_row(ihb + 2, win[2]);
+    const int ow = owb * tcols + col;
+    const bool col_ok = c_ok && ow < p.Wo && n < p.N;
+    const int oh0 = ohb * T::kTH;
+    float* ybase = p.y + ((static_cast<size_t>(n) * p.Ho + oh0) * p.Wo + ow) * p.C + c;
+    const size_t yrow = static_cast<size_t>(p.Wo) * p.C;
+    // this thread's 4 channels of window column col*SW of its image, as 8-byte words; the
+    // window is [image][row][column][32 channels], one pixel = 8 words
+    const uint2* win = reinterpret_cast<const uint2*>(smem + stage * T::kStageBytes) +
+                       (img * T::kInH * in_w + col * SW) * 8 + cq;
+
+    f32x2 acc[T::kSlots][2];
+#pragma unroll
+    for (int q = 0; q < T::kSlots; ++q) {
+      acc[q][0] = bias[0];
+      acc[q][1] = bias[1];
+    }
+#pragma unroll
+    for (int i = 0; i < T::kInH; ++i) {
+      f32x2 xv[3][2];
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const uint2 v = win[(i * in_w + s) * 8];
+        xv[s][0] = bf16x2_to_f32x2(v.x);
+        xv[s][1] = bf16x2_to_f32x2(v.y);
       }
-      float acc[kOW][8];
-#pragma unroll
-      for (int jj = 0; jj < kOW; ++jj)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[jj][e] = bias[e];
+      // input row i feeds output row o through filter row r = i - o*SW
 #pragma unroll
       for (int r = 0; r < 3; ++r) {
-        float tap[3][8];
+        if (i - r < 0 || (i - r) % SW != 0) continue;
+        const int o = (i - r) / SW;
+        if (o >= T::kTH) continue;
 #pragma unroll
-        for (int s = 0; s < 3; ++s) {
-          const float4 t0 = __ldg(reinterpret_cast<const float4*>(p.taps + (r * 3 + s) * p.C + c0));
-          const float4 t1 = __ldg(reinterpret_cast<const float4*>(p.taps + (r * 3 + s) * p.C + c0 + 4));
-          tap[s][0] = t0.x; tap[s][1] = t0.y; tap[s][2] = t0.z; tap[s][3] = t0.w;
-          tap[s][4] = t1.x; tap[s][5] = t1.y; tap[s][6] = t1.z; tap[s][7] = t1.w;
-        }
+        for (int s = 0; s < 3; ++s)
 #pragma unroll
-        for (int col = 0; col < NCOL; ++col) {
-          float xv[8];
-          bf16x8_to_f32(win[r][col], xv);
-#pragma unroll
-          for (int jj = 0; jj < kOW; ++jj) {
-            const int s = col - jj * SW;
-            if (s >= 0 && s < 3) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[jj][e] = fmaf(xv[e], tap[s][e], acc[jj][e]);
-            }
-          }
-        }
+          for (int e = 0; e < 2; ++e)
+            acc[o % T::kSlots][e] = fma_f32x2(xv[s][e], tap[r * 3 + s][e], acc[o % T::kSlots][e]);
       }
-      float* yrow = p.y + ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo) * p.C + c0;
-#pragma unroll
-      for (int jj = 0; jj < kOW; ++jj) {
-        if (ow0 + jj < p.Wo) {
-          float4* dst = reinterpret_cast<float4*>(yrow + static_cast<size_t>(ow0 + jj) * p.C);
-          dst[0] = make_float4(clampf(acc[jj][0], p.lo, p.hi), clampf(acc[jj][1], p.lo, p.hi),
-                               clampf(acc[jj][2], p.lo, p.hi), clampf(acc[jj][3], p.lo, p.hi));
-          dst[1] = make_float4(clampf(acc[jj][4], p.lo, p.hi), clampf(acc[jj][5], p.lo, p.hi),
-                               clampf(acc[jj][6], p.lo, p.hi), clampf(acc[jj][7], p.lo, p.hi));
+      // output row o is complete after input row o*SW + 2
+      if (i >= 2 && (i - 2) % SW == 0) {
+        const int o = (i - 2) / SW;
+        f32x2 (&a)[2] = acc[o % T::kSlots];
+        if (col_ok && oh0 + o < p.Ho) {
+          float v0, v1, v2, v3;
+          unpack_f32x2(a[0], v0, v1);
+          unpack_f32x2(a[1], v2, v3);
+          // streaming store: the output is not re-read here, keep L2 for the input windows
+          __stcs(reinterpret_cast<float4*>(ybase + o * yrow),
+                 make_float4(clampf(v0, p.lo, p.hi), clampf(v1, p.lo, p.hi), clampf(v2, p.lo, p.hi),
+                             clampf(v3, p.lo, p.hi)));
         }
+        a[0] = bias[0];
+        a[1] = bias[1];
       }
-      // slide the window down by SW input rows
-#pragma unroll
-      for (int col = 0; col < NCOL; ++col) {
-        if (SW == 1) {
-          win[0][col] = win[1][col];
-          win[1][col] = win[2][col];
-        } else {
-          win[0][col] = win[2][col];
-        }
-      }
+    }
+    // this warp is done with the stage
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(&empty[stage]);
+  }
+  // on a timeout, let the loads still in flight land (bounded) before the CTA's smem goes away
+  if (tid == 0 && *abort_v) {
+    for (int j = waited; j < issued; ++j) {
+      int quiet = 0;
+      mbar_wait(&full[j % T::kStages], (j / T::kStages) & 1, &quiet, nullptr, 20000000LL);
     }
   }
 }
@@ -182,29 +270,62 @@ __global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
   }
 }
 
-cudaError_t launch_depthwise(const DwParams& p, int num_sms, cudaStream_t stream) {
-  const bool fast = p.R == 3 && p.S == 3 && p.dh == 1 && p.dw == 1 && p.sh == p.sw &&
-                    (p.sh == 1 || p.sh == 2);
+bool dw_uses_tma(const DwParams& p) {
+  return p.R == 3 && p.S == 3 && p.dh == 1 && p.dw == 1 && p.sh == p.sw && (p.sh == 1 || p.sh == 2);
+}
+
+void dw_tile_box(int stride, int Wo, int* box_w, int* box_h, int* box_n) {
+  const int cols = dw_tile_cols(Wo);
+  *box_w = stride == 1 ? DwTile<1>::in_w(cols) : DwTile<2>::in_w(cols);
+  *box_h = stride == 1 ? DwTile<1>::kInH : DwTile<2>::kInH;
+  *box_n = DwTile<1>::kLanes / cols;
+}
+
+namespace {
+template <int SW, int TCOLS>
+cudaError_t launch_dw_tma(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream) {
+  using T = DwTile<SW>;
+  static std::once_flag once;
+  static cudaError_t set_err = cudaSuccess;
+  static int occ = 0;
+  std::call_once(once, [] {
+    set_err = cudaFuncSetAttribute(dw3x3_tma_kernel<SW, TCOLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   T::kSmem);
+    if (set_err == cudaSuccess)
+      set_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dw3x3_tma_kernel<SW, TCOLS>, T::kThreads,
+                                                              T::kSmem);
+    if (set_err == cudaSuccess && occ < 1) set_err = cudaErrorInvalidConfiguration;
+  });
+  if (set_err != cudaSuccess) return set_err;
+  const long long slabs = (p.C + T::kCS - 1) / T::kCS;
+  constexpr int cols = TCOLS;
+  constexpr int nb = T::kLanes / cols;
+  const long long units = static_cast<long long>((p.N + nb - 1) / nb) * ((p.Ho + T::kTH - 1) / T::kTH) *
+                          ((p.Wo + cols - 1) / cols) * slabs;
+  if (units >= (1LL << 31)) return cudaErrorInvalidValue;
+  DwParams q = p;
+  q.f_slabs = make_fastdiv(static_cast<uint32_t>(slabs));
+  q.f_owbs = make_fastdiv(static_cast<uint32_t>((p.Wo + cols - 1) / cols));
+  q.f_ohbs = make_fastdiv(static_cast<uint32_t>((p.Ho + T::kTH - 1) / T::kTH));
+  long long grid = std::min<long long>(units, static_cast<long long>(num_sms) * occ);
+  // a multiple of the channel-slab count keeps every CTA on one slab (taps loaded once)
+  if (grid < units && grid >= slabs) grid -= grid % slabs;
+  return launch_pdl(dw3x3_tma_kernel<SW, TCOLS>, dim3(static_cast<unsigned>(grid)), dim3(T::kThreads), T::kSmem, stream, 1,
+                    *tmX, q);
+}
+}  // namespace
+
+cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream) {
   const long long C8 = p.C / 8;
   if (static_cast<long long>(p.N) * p.Ho * p.Wo * C8 == 0) return cudaSuccess;
-  const dim3 b(256);
-  if (fast) {
-    const long long row_items = ((p.Wo + kOW - 1) / kOW) * C8;
-    // tallest strip (fewest redundant row loads) that still leaves >= 1024 threads per SM
-    DwParams q = p;
-    q.th = 1;
-    for (int th : {8, 4, 2}) {
-      const long long threads = static_cast<long long>(p.N) * ((p.Ho + th - 1) / th) * row_items;
-      if (threads >= static_cast<long long>(num_sms) * 1024) {
-        q.th = th;
-        break;
-      }
-    }
-    const long long strips = static_cast<long long>(p.N) * ((p.Ho + q.th - 1) / q.th);
-    const dim3 g(static_cast<unsigned>((row_items + 255) / 256), static_cast<unsigned>(strips < 65535 ? strips : 65535));
-    return p.sh == 1 ? launch_pdl(dw3x3_kernel<1>, g, b, 0, stream, 1, q)
-                     : launch_pdl(dw3x3_kernel<2>, g, b, 0, stream, 1, q);
+  if (dw_uses_tma(p)) {
+    if (!tmX) return cudaErrorInvalidValue;
+    const bool narrow = dw_tile_cols(p.Wo) == 8;
+    if (p.sh == 1)
+      return narrow ? launch_dw_tma<1, 8>(p, tmX, num_sms, stream) : launch_dw_tma<1, 16>(p, tmX, num_sms, stream);
+    return narrow ? launch_dw_tma<2, 8>(p, tmX, num_sms, stream) : launch_dw_tma<2, 16>(p, tmX, num_sms, stream);
   }
+  const dim3 b(256);
   const long long work = static_cast<long long>(p.N) * p.Ho * p.Wo * C8;
   long long blocks = (work + 255) / 256;
   const long long cap = static_cast<long long>(num_sms) * 3 * 16;

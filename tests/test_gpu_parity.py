@@ -77,12 +77,37 @@ SMALL = [
     (S("dw_5x5_dil2", 1, 16, 13, 13, 16, 5, 5, (1, 1), (4, 4, 4, 4), (2, 2), group=16, act=ACT_NONE, bias=True),
      V.CONVF_VARIANT_DEPTHWISE),
     (S("dw_3x3_s2_asym", 1, 24, 9, 12, 24, 3, 3, (2, 2), (0, 1, 1, 0), group=24), V.CONVF_VARIANT_DEPTHWISE),
+    # 3x3 tiles of 7 rows x 16 columns x 32 channels: windows wider than the image and than C,
+    # a half-empty last channel slab, ragged row and column blocks, pads larger than the halo
+    (S("dw_s1_c8_tiny", 3, 8, 5, 6, 8, 3, 3, pads=(1, 1, 1, 1), group=8, act=ACT_NONE, bias=True),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s1_c144_ragged", 2, 144, 15, 37, 144, 3, 3, pads=(1, 1, 1, 1), group=144, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s1_pad3_asym", 1, 64, 8, 9, 64, 3, 3, pads=(3, 2, 0, 3), group=64), V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s2_c96_odd", 2, 96, 23, 31, 96, 3, 3, (2, 2), (1, 1, 1, 1), group=96, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s2_pad0", 1, 32, 16, 16, 32, 3, 3, (2, 2), group=32), V.CONVF_VARIANT_DEPTHWISE),
+    # outputs at most 8 columns wide: two images per tile, the last image group half past N
+    (S("dw_s1_narrow_odd_n", 5, 96, 7, 7, 96, 3, 3, pads=(1, 1, 1, 1), group=96, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s2_narrow_odd_n", 3, 64, 13, 15, 64, 3, 3, (2, 2), (1, 1, 1, 1), group=64, bias=True),
+     V.CONVF_VARIANT_DEPTHWISE),
 ]
 
 
 @pytest.mark.parametrize("spec,variant", SMALL, ids=[s.name for s, _ in SMALL])
 def test_small_shapes_full(spec, variant):
     _assert(check_full(spec, 7000 + SMALL.index((spec, variant))), spec, variant)
+
+
+@pytest.mark.parametrize("spec", [
+    S("dw_s1_many_tiles", 16, 192, 56, 56, 192, 3, 3, pads=(1, 1, 1, 1), group=192, act=ACT_RELU6),
+    S("dw_s2_many_tiles", 32, 192, 57, 57, 192, 3, 3, (2, 2), (1, 1, 1, 1), group=192, act=ACT_RELU6),
+], ids=lambda s: s.name)
+def test_depthwise_every_output_with_several_tiles_per_cta(spec):
+    """More tiles than resident CTAs, so every CTA cycles its shared-memory stages more than once
+    (the stride-2 case about four times); every output is compared."""
+    _assert(check_full(spec, 7200, V.CONVF_VARIANT_DEPTHWISE), spec, V.CONVF_VARIANT_DEPTHWISE)
 
 
 @pytest.mark.parametrize("variant", [V.CONVF_VARIANT_IMPLICIT_GEMM, V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER])

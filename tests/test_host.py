@@ -198,3 +198,27 @@ def test_weight_prepack_layout(variant, C, R, S, HW, cp):
             want[:, (r * S + s) * cp:(r * S + s) * cp + C] = W[:, :, r, s]
     assert np.array_equal(out, want)
     assert kt % 64 == 0
+
+
+def test_fast_division_by_invariant_integers():
+    """The depthwise kernel decodes tile indices with the round-up multiply-high method of
+    Granlund and Montgomery: l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, and
+    q = (umulhi(n, m) + n) >> l for n < 2^31.  Checked against n // d at the edges of the range
+    and on random pairs, with the 32-bit wrap of the device arithmetic made explicit."""
+    import random
+    rng = random.Random(5)
+    ds = [1, 2, 3, 5, 7, 12, 30, 64, 1000, 2**16 + 1, 2**30, 2**31 - 1] + [rng.randrange(1, 2**31) for _ in range(200)]
+    ns = [0, 1, 2**31 - 1, 2**31 - 2] + [rng.randrange(0, 2**31) for _ in range(200)]
+    for d in ds:
+        l = 0
+        while (1 << l) < d:
+            l += 1
+        m = ((1 << 32) * ((1 << l) - d)) // d + 1
+        assert 0 < m < 2**32 or (d == 1 and m == 1)
+        for n in ns + [d - 1, d, d + 1, 2 * d - 1, (2**31 - 1) // d * d]:
+            if not 0 <= n < 2**31:
+                continue
+            hi = (n * m) >> 32
+            s = (hi + n) & 0xFFFFFFFF
+            assert s == hi + n            # no 32-bit overflow for n < 2^31
+            assert s >> l == n // d, (n, d)
