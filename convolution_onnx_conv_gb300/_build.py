@@ -19,7 +19,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
-UNITS = [("api.cu", []), ("k_depthwise.cu", []), ("k_int8.cu", []), ("k_watchdog.cu", []), ("k_pad.cu", [])] + [
+UNITS = [("api.cu", []), ("k_depthwise.cu", []), ("k_int8.cu", []), ("k_watchdog.cu", []), ("k_pad.cu", []),
+         ("tc_window.cu", [])] + [
     ("tc_conv_inst.cu", [f"-DCONVF_BN={bn}"]) for bn in (32, 64, 128, 256)]
 
 

@@ -53,6 +53,8 @@ convf_status ok() {
   return CONVF_OK;
 }
 
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
 // ------------------------------------------------------------------ attribute normalisation
 struct Shape {
   int N, C, H, W, K, R, S, Cg;
@@ -143,13 +145,77 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "clip bounds (%g, %g) need lo <= hi", d->clip_lo, d->clip_hi);
   if (d->dtype == CONVF_S8 && (d->act == CONVF_ACT_RELU6 || d->act == CONVF_ACT_CLIP))
     return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
-  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
+  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
   if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
   if (d->cta_pair < 0 || d->cta_pair > 2)
     return fail(CONVF_ERR_INVALID_ARG, "cta_pair=%d is not 0 (auto), 1 (single CTA) or 2 (CTA pair)", d->cta_pair);
   return CONVF_OK;
+}
+
+// ------------------------------------------------------------------ window-mode geometry
+// Padded input rows of Wp pixels x cpt channels with pl zero columns in front; windows of E
+// elements (one filter row of one output pixel, zero-padded to 16/32/64); weights [R][bnp][E].
+struct WinGeom {
+  bool rows;        // row mode: windows exactly 16 bytes apart (sw * cpt == 8)
+  int nchunk;       // row mode: 128-byte chunks of one filter row's input segment
+  int cpt, E, Wp, bnp, stages, ow_blocks;
+  long long tiles;
+  uint32_t a_stage, b_bytes, b_region, tmem_cols;
+  size_t smem;
+};
+
+std::string win_geom(const Shape& s, WinGeom* g) {
+  if (s.C > 8) return "window mode needs C <= 8";
+  if (s.dh != 1 || s.dw != 1) return "window mode needs dilation 1";
+  g->cpt = s.C <= 4 ? 4 : 8;
+  if ((s.sw * g->cpt * 2) % 16) return "window mode needs sw*cpt*2 to be a multiple of 16 bytes (stride_w even for C <= 4)";
+  if (s.S * g->cpt > 64) return "window mode needs S*cpt <= 64";
+  g->E = s.S * g->cpt <= 16 ? 16 : (s.S * g->cpt <= 32 ? 32 : 64);
+  if (s.R * g->E > 256) return "window mode needs R*E <= 256 (one 64 KB activation stage)";
+  if (s.K > 256) return "window mode needs K <= 256";
+  g->bnp = (int)align_up((size_t)s.K, 32);
+  g->rows = s.sw * g->cpt == 8;
+  const long long need = std::max<long long>((long long)s.pl + s.W, (long long)(s.Wo - 1) * s.sw + g->E / g->cpt);
+  // row mode reads whole 128-byte chunks of a row
+  g->Wp = (int)align_up((size_t)need, (size_t)(g->rows ? 64 / g->cpt : 16 / (2 * g->cpt)));
+  g->nchunk = (int)((127 * 8 + g->E + 63) / 64);
+  if ((long long)s.N * s.H * g->Wp * g->cpt > 0x7FFFFFFFLL) return "window mode's padded input exceeds 2^31 elements";
+  g->ow_blocks = (s.Wo + 127) / 128;
+  g->tiles = (long long)s.N * s.Ho * g->ow_blocks;
+  if (g->tiles > 0x7FFFFFFFLL) return "window mode tile count exceeds 2^31";
+  g->a_stage = (uint32_t)(g->rows ? s.R * g->nchunk * 128 : s.R * 128 * g->E * 2);
+  g->b_bytes = (uint32_t)(s.R * g->bnp * g->E * 2);
+  g->b_region = (uint32_t)align_up(g->b_bytes, 1024);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * g->bnp)) cols *= 2;
+  g->tmem_cols = cols;
+  const size_t budget = 232448;
+  const size_t fixed = kWinFixedSmem + g->b_region;
+  const size_t a_stride = align_up(g->a_stage, 1024);   // stages start on 1 KB boundaries
+  if (fixed + 2 * a_stride > budget) return "window mode's stages and weights exceed shared memory";
+  g->stages = (int)std::min<size_t>(4, (budget - fixed) / a_stride);
+  g->smem = fixed + (size_t)g->stages * a_stride;
+  return "";
+}
+
+// W[K][C][R][S] (bf16 bits) -> per filter row r a bnp x E operand, window element
+// e = s*cpt + c, zero elsewhere: row-major [R][bnp][E] (the TMA swizzles it on load), or in row
+// mode the no-swizzle core-matrix order: 8 channels x 8 elements per 128 bytes, K-adjacent
+// core matrices 128 B apart, 8-channel groups E*16 B apart.
+void pack_window(const uint16_t* W, const Shape& s, const WinGeom& g, uint16_t* out) {
+  std::memset(out, 0, sizeof(uint16_t) * (size_t)s.R * g.bnp * g.E);
+  for (int r = 0; r < s.R; ++r)
+    for (int k = 0; k < s.K; ++k)
+      for (int q = 0; q < s.S; ++q)
+        for (int c = 0; c < s.C; ++c) {
+          const int e = q * g.cpt + c;
+          const size_t at = g.rows ? (size_t)r * g.bnp * g.E + (size_t)(k / 8) * g.E * 8 + (size_t)(e / 8) * 64 +
+                                         (k % 8) * 8 + (e % 8)
+                                   : ((size_t)r * g.bnp + k) * g.E + e;
+          out[at] = W[(((size_t)k * s.C + c) * s.R + r) * s.S + q];
+        }
 }
 
 // ------------------------------------------------------------------ variant selector
@@ -184,6 +250,13 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       if ((long long)(s.R - 1) * s.dh > 65535 || (long long)(s.S - 1) * s.dw > 65535)
         return "filter offsets exceed 16 bits";
       return "";
+    case CONVF_VARIANT_IMPLICIT_GEMM_WINDOW: {
+      if (!bf) return "implicit GEMM serves bf16 only";
+      if (d->group != 1) return "implicit GEMM needs group == 1";
+      if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
+      WinGeom g;
+      return win_geom(s, &g);
+    }
     case CONVF_VARIANT_IMPLICIT_GEMM_GATHER:
       if (!bf) return "implicit GEMM serves bf16 only";
       if (d->group != 1) return "implicit GEMM needs group == 1";
@@ -207,8 +280,8 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
     *out = d->variant;
     return CONVF_OK;
   }
-  const int order_bf16[4] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM,
-                             CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
+  const int order_bf16[5] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM,
+                             CONVF_VARIANT_IMPLICIT_GEMM_WINDOW, CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
   if (d->dtype == CONVF_S8) {
     std::string why = cannot(CONVF_VARIANT_INT8, d, s);
     if (!why.empty()) return fail(CONVF_ERR_UNSUPPORTED, "int8 conv refused: %s", why.c_str());
@@ -218,6 +291,9 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
   std::string reasons;
   for (int v : order_bf16) {
     std::string why = cannot(v, d, s);
+    // a tile is one output row segment of 128 pixels: narrower outputs leave most rows idle
+    if (why.empty() && v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW && s.Wo < 32)
+      why = "window mode is chosen automatically only for outputs at least 32 pixels wide";
     if (why.empty()) {
       *out = v;
       return CONVF_OK;
@@ -307,8 +383,6 @@ bool load_encoders() {
   return g_encode_tiled && g_encode_im2col;
 }
 
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
 }  // namespace
 
 // ====================================================================== handle
@@ -337,6 +411,7 @@ struct convf_handle {
   // tcgen05 configuration
   int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
   bool pair;        // CTA-pair (cta_group::2) 256-row tiles
+  WinGeom wg;       // window variant geometry
   CUtensorMap tmB;
   CUtensorMap tmA, tmY;
   const void* map_x;
@@ -469,6 +544,11 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
               gather ? 1 : desc->cta_pair, &bn, &pair);
     if (desc->tile_n) bn = desc->tile_n;
     if (cta_pair) *cta_pair = pair ? 1 : 0;
+  } else if (v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
+    WinGeom g;
+    win_geom(s, &g);
+    bn = g.bnp;
+    kt = s.R * g.E;
   } else if (v == CONVF_VARIANT_INT8) {
     kt = s.R * s.S * s.C;
   }
@@ -579,6 +659,15 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
               (float)((double)scale[c] * (double)bf16_to_f32(Wb[((size_t)c * s.R + r) * s.S + q]));
     o_taps = carve(taps.size() * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
+    win_geom(s, &h->wg);
+    wpack.resize((size_t)s.R * h->wg.bnp * h->wg.E);
+    pack_window(static_cast<const uint16_t*>(W), s, h->wg, wpack.data());
+    h->ktot = s.R * h->wg.E;
+    o_w = carve(wpack.size() * sizeof(uint16_t));
+    o_scale = carve((size_t)Kpad * sizeof(float));
+    o_bias = carve((size_t)Kpad * sizeof(float));
+    o_pad = carve((size_t)s.N * s.H * h->wg.Wp * h->wg.cpt * sizeof(uint16_t));
   } else if (variant == CONVF_VARIANT_INT8) {
     o_w = carve((size_t)s.K * s.R * s.S * s.C);
     o_qb = carve((size_t)s.K * 4);
@@ -644,6 +733,52 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     return fail(CONVF_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(ce));
   }
 
+  if (variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
+    const WinGeom& g = h->wg;
+    h->bn = g.bnp;
+    h->num_tiles = (int)g.tiles;
+    h->grid = (int)std::min<long long>(g.tiles, h->num_sms);
+    h->cpt = g.cpt;
+    CUresult r = CUDA_SUCCESS;
+    if (!load_encoders()) r = CUDA_ERROR_NOT_SUPPORTED;
+    const CUtensorMapSwizzle sw = g.E == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                            : (g.E == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r == CUDA_SUCCESS && h->xpad && g.rows) {
+      // row mode: {64-element chunks, chunks per row, rows, images}, box = nchunk chunks x R rows
+      const size_t rowb = (size_t)g.Wp * g.cpt * 2;
+      const cuuint64_t dims[4] = {64, (cuuint64_t)(rowb / 128), (cuuint64_t)s.H, (cuuint64_t)s.N};
+      const cuuint64_t strides[3] = {128, (cuuint64_t)rowb, (cuuint64_t)s.H * rowb};
+      const cuuint32_t box[4] = {64, (cuuint32_t)g.nchunk, (cuuint32_t)s.R, 1};
+      const cuuint32_t es[4] = {1, 1, 1, 1};
+      r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, h->xpad, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (r == CUDA_SUCCESS && h->xpad) {
+      // overlapping windows: consecutive windows start sw*cpt elements apart, each E long
+      const size_t px = (size_t)g.cpt * 2;
+      const cuuint64_t dims[4] = {(cuuint64_t)g.E, (cuuint64_t)s.Wo, (cuuint64_t)s.H, (cuuint64_t)s.N};
+      const cuuint64_t strides[3] = {(cuuint64_t)(s.sw * px), (cuuint64_t)(g.Wp * px), (cuuint64_t)s.H * g.Wp * px};
+      const cuuint32_t box[4] = {(cuuint32_t)g.E, 128, (cuuint32_t)s.R, 1};
+      const cuuint32_t es[4] = {1, 1, 1, 1};
+      r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, h->xpad, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r == CUDA_SUCCESS && !g.rows) {
+      const cuuint64_t dims[3] = {(cuuint64_t)g.E, (cuuint64_t)g.bnp, (cuuint64_t)s.R};
+      const cuuint64_t strides[2] = {(cuuint64_t)g.E * 2, (cuuint64_t)g.bnp * g.E * 2};
+      const cuuint32_t box[3] = {(cuuint32_t)g.E, (cuuint32_t)g.bnp, (cuuint32_t)s.R};
+      const cuuint32_t es[3] = {1, 1, 1};
+      r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->w_bf16, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) {
+      cudaFree(h->dev);
+      delete h;
+      return fail(CONVF_ERR_CUDA, "window-mode tensor map encoding failed (CUresult %d)", (int)r);
+    }
+  }
   if (variant == CONVF_VARIANT_GEMM_1X1 || variant == CONVF_VARIANT_IMPLICIT_GEMM ||
       variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
     if (!load_encoders()) {
@@ -780,6 +915,21 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       ce = launch_depthwise(p, &h->tmA, h->num_sms, strm);
       break;
     }
+    case CONVF_VARIANT_IMPLICIT_GEMM_WINDOW: {
+      const WinGeom& g = h->wg;
+      ce = launch_window_pad(static_cast<const uint16_t*>(x), h->xpad, s.N, s.H, s.W, s.C, g.cpt, g.Wp, s.pl,
+                             h->num_sms, strm);
+      if (ce != cudaSuccess) break;
+      WinParams p{};
+      p.N = s.N; p.H = s.H; p.Ho = s.Ho; p.Wo = s.Wo; p.Kout = s.K; p.sh = s.sh; p.pt = s.pt; p.R = s.R;
+      p.bnp = g.bnp; p.ow_blocks = g.ow_blocks; p.num_tiles = h->num_tiles; p.stages = g.stages;
+      p.a_stage_bytes = g.a_stage; p.b_bytes = g.b_bytes; p.b_region = g.b_region; p.tmem_cols = g.tmem_cols;
+      p.chunk0_per_block = 128 * s.sw * g.cpt / 64; p.nchunk = g.nchunk; p.w = h->w_bf16;
+      p.scale = h->scale; p.bias = h->bias; p.y = static_cast<float*>(y);
+      p.lo = h->lo; p.hi = h->hi; p.status = h->status;
+      ce = launch_tc_window(p, h->tmA, h->tmB, g.E, g.rows, h->grid, g.smem, strm);
+      break;
+    }
     case CONVF_VARIANT_INT8: {
       S8Params p{};
       p.M = (int)s.M; p.Kout = s.K; p.C = s.C; p.H = s.H; p.W = s.W; p.Ho = s.Ho; p.Wo = s.Wo; p.R = s.R; p.S = s.S;
@@ -859,9 +1009,16 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (st != CONVF_OK) return st;
   if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
   static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
-                                "implicit_gemm_gather"};
+                                "implicit_gemm_gather", "implicit_gemm_window"};
   const Shape& s = h->s;
-  if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8)
+  if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
+    snprintf(buf, len,
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d window=%d row_mode=%d tap_channels=%d "
+             "padded_row=%d stages=%d tiles=%d grid=%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->wg.bnp, h->wg.E, h->wg.rows ? 1 : 0,
+             h->wg.cpt, h->wg.Wp,
+             h->wg.stages, h->num_tiles, h->grid, h->dev_bytes);
+  else if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8)
     snprintf(buf, len, "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
   else

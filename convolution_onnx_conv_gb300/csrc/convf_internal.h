@@ -70,6 +70,41 @@ struct TcConvParams {
 
 
 
+// ---------------------------------------------------------------- window-mode implicit GEMM
+// Small-C convolutions (C <= 8) whose filter row, for one output pixel, is one contiguous run
+// of E bf16 in a channel- and column-padded copy of the input ([N][H][Wp][cpt], the first pl
+// columns zero): tile = 128 output pixels of one output row; one 4-D TMA load brings the
+// R x 128 overlapping windows of a tile, the weights stay resident in shared memory.
+struct WinParams {
+  int N, H, Ho, Wo, Kout;
+  int sh, pt;             // row stride and top pad (the column offset is in the padded layout)
+  int R;                  // filter rows (rows of the A box)
+  int bnp;                // output channels rounded up to 32 (MMA N, B rows)
+  int ow_blocks, num_tiles;
+  int stages;             // A stages in shared memory
+  uint32_t a_stage_bytes, b_bytes, b_region;
+  uint32_t tmem_cols;
+  int chunk0_per_block;   // row mode: 128-byte chunks between consecutive 128-window tiles
+  int nchunk;             // row mode: 128-byte chunks of one filter row's input segment
+  const uint16_t* w;      // row mode: weights in the no-swizzle core-matrix order (bulk copy)
+  const float* scale;     // [>= bnp]
+  const float* bias;      // [>= bnp]
+  float* y;               // NHWC fp32 output
+  float lo, hi;
+  int* status;
+};
+// E = elements per window row (16, 32 or 64); rows = row mode (windows 16 bytes apart: the A
+// operand is the plain input row segment, windows overlap through the MMA descriptor)
+cudaError_t launch_tc_window(const WinParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int E, bool rows,
+                             int grid, size_t smem, cudaStream_t stream);
+// shared memory: [1 KB alignment][A stages][B, b_region bytes][epilogue: 8 warps x 4 KB]
+// [scale, bias: 256 floats each][barriers and flags]
+constexpr size_t kWinFixedSmem = 1024 + 8 * 4096 + 2 * 256 * 4 + 256;
+// x [N][H][W][C] -> out [N][H][Wp][cpt] with out column j = x column j - shift (zero outside
+// the image and in the channels past C)
+cudaError_t launch_window_pad(const uint16_t* x, uint16_t* out, int N, int H, int W, int C, int cpt, int Wp,
+                              int shift, int num_sms, cudaStream_t stream);
+
 // NHWC bf16 with C <= 8 channels -> NHWC bf16 with cpt (4 or 8) channels, zero-padded.
 cudaError_t launch_pad_channels(const uint16_t* x, uint16_t* out, long long pixels, int C, int cpt, int num_sms,
                                 cudaStream_t stream);

@@ -81,8 +81,17 @@ typedef enum {
   CONVF_VARIANT_GEMM_1X1 = 2,        /* same kernel, activations read as a [N*H*W][C] matrix */
   CONVF_VARIANT_DEPTHWISE = 3,       /* CUDA-core depthwise (group == C == K) */
   CONVF_VARIANT_INT8 = 4,            /* int8 tensor-core MMA, int32 accumulate, requant */
-  CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 5  /* tcgen05 implicit GEMM, activation rows gathered by
+  CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 5, /* tcgen05 implicit GEMM, activation rows gathered by
                                             threads (any C, e.g. the 3-channel stem) */
+  CONVF_VARIANT_IMPLICIT_GEMM_WINDOW = 6  /* tcgen05 implicit GEMM for C <= 8: a pre-pass pads the
+                                            channels to 4 or 8 and the columns by the left pad,
+                                            after which one filter row of one output pixel is a
+                                            contiguous run and one TMA load (overlapping
+                                            windows) brings a tile's whole activation operand;
+                                            weights resident in shared memory.  Needs dilation
+                                            1, sw*cpt*2 a multiple of 16 bytes, S*cpt <= 64,
+                                            R*round_up(S*cpt,16) <= 256, K <= 256.  The selector
+                                            takes it for outputs at least 32 pixels wide. */
 } convf_variant;
 
 typedef struct {

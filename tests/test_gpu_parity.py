@@ -100,6 +100,24 @@ def test_small_shapes_full(spec, variant):
     _assert(check_full(spec, 7000 + SMALL.index((spec, variant))), spec, variant)
 
 
+WINDOW = [
+    # one filter row of one output pixel is a contiguous window of E = 16 / 32 / 64 elements
+    S("win_stem_c3_7x7_s2", 2, 3, 40, 40, 64, 7, 7, (2, 2), (3, 3, 3, 3)),
+    S("win_stem_c3_two_col_blocks", 1, 3, 300, 300, 64, 7, 7, (2, 2), (3, 3, 3, 3), bias=True),
+    S("win_c3_3x3_s2_relu6", 2, 3, 64, 64, 32, 3, 3, (2, 2), (1, 1, 1, 1), act=ACT_RELU6),
+    S("win_c8_3x3_s1_k40", 2, 8, 40, 40, 40, 3, 3, (1, 1), (1, 1, 1, 1), bias=True),
+    S("win_c5_3x7_s2_asym", 2, 5, 33, 45, 24, 3, 7, (2, 2), (1, 3, 0, 2), act=ACT_NONE),
+    S("win_c4_5x5_s4_k192", 1, 4, 64, 64, 192, 5, 5, (4, 4), (2, 2, 2, 2)),
+    S("win_c1_3x3_s2_nopad", 3, 1, 21, 50, 16, 3, 3, (2, 2)),
+]
+
+
+@pytest.mark.parametrize("spec", WINDOW, ids=lambda s: s.name)
+def test_window_variant_full(spec):
+    _assert(check_full(spec, 7400 + WINDOW.index(spec), V.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW), spec,
+            V.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
+
+
 @pytest.mark.parametrize("spec", [
     S("dw_s1_many_tiles", 16, 192, 56, 56, 192, 3, 3, pads=(1, 1, 1, 1), group=192, act=ACT_RELU6),
     S("dw_s2_many_tiles", 32, 192, 57, 57, 192, 3, 3, (2, 2), (1, 1, 1, 1), group=192, act=ACT_RELU6),

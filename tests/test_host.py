@@ -165,8 +165,11 @@ def test_selector_on_the_workloads():
         elif spec.group > 1:
             assert v == cf.CONVF_VARIANT_DEPTHWISE
         elif spec.C == 3:
-            # 3 channels padded to whole taps of 4: 49 taps x 4 = 196 -> 256
-            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER and kt == 256 and bn in (32, 64, 128)
+            # 3 channels padded to 4; one filter row of one output pixel is a run of S*4
+            # elements, padded to a 16/32/64-element window: 7 rows x 32 for the 7x7 stem
+            E = 16 if spec.S * 4 <= 16 else 32 if spec.S * 4 <= 32 else 64
+            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW and kt == spec.R * E
+            assert bn == -(-spec.K // 32) * 32
         elif spec.R == 1 and spec.stride == (1, 1):
             assert v == cf.CONVF_VARIANT_GEMM_1X1 and kt == -(-spec.C // 64) * 64
         else:
@@ -222,3 +225,34 @@ def test_fast_division_by_invariant_integers():
             s = (hi + n) & 0xFFFFFFFF
             assert s == hi + n            # no 32-bit overflow for n < 2^31
             assert s >> l == n // d, (n, d)
+
+
+@pytest.mark.parametrize("C,R,S,stride,dil,K,W,ok_or_reason", [
+    (3, 7, 7, (2, 2), (1, 1), 64, 224, None),                  # the ResNet stem: windows of 32
+    (3, 3, 3, (2, 2), (1, 1), 32, 224, None),                  # the MobileNet stem: windows of 16
+    (8, 3, 3, (1, 1), (1, 1), 64, 64, None),                   # 8 channels: any stride
+    (6, 3, 7, (2, 2), (1, 1), 64, 64, None),                   # 7 taps x 8 = 56 -> windows of 64
+    (3, 3, 3, (1, 1), (1, 1), 32, 64, "multiple of 16 bytes"),  # 4 channels need an even stride
+    (3, 3, 3, (2, 2), (2, 2), 32, 64, "dilation 1"),
+    (3, 11, 11, (4, 4), (1, 1), 64, 224, "R*E <= 256"),        # 11 x 64 windows
+    (3, 3, 3, (2, 2), (1, 1), 288, 64, "K <= 256"),
+    (16, 3, 3, (2, 2), (1, 1), 32, 64, "C <= 8"),
+])
+def test_window_variant_rules(C, R, S, stride, dil, K, W, ok_or_reason):
+    pad = (R // 2, S // 2, R // 2, S // 2)
+    d = cf.make_desc(2, C, W, W, K, R, S, stride, pad, dil, variant=cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
+    if ok_or_reason is None:
+        v, bn, kt = cf.conv_fused_plan(d)
+        E = 16 if S * (4 if C <= 4 else 8) <= 16 else 32 if S * (4 if C <= 4 else 8) <= 32 else 64
+        assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW and kt == R * E and bn == -(-K // 32) * 32
+    else:
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_plan(d)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and ok_or_reason in str(e.value)
+
+
+def test_window_variant_is_automatic_only_for_wide_outputs():
+    narrow = cf.make_desc(2, 3, 30, 30, 64, 7, 7, (2, 2), (3, 3, 3, 3))     # 15 output columns
+    wide = cf.make_desc(2, 3, 64, 64, 64, 7, 7, (2, 2), (3, 3, 3, 3))       # 32 output columns
+    assert cf.conv_fused_plan(narrow)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER
+    assert cf.conv_fused_plan(wide)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW
