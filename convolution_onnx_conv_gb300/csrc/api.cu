@@ -20,14 +20,10 @@
 
 namespace convf {
 // defined once per tile width in tc_conv_inst.cu
-cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&,
-                                 const CUtensorMap&, int, bool, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
 }  // namespace convf
 
 using namespace convf;
@@ -413,9 +409,8 @@ struct convf_handle {
   bool pair;        // CTA-pair (cta_group::2) 256-row tiles
   WinGeom wg;       // window variant geometry
   CUtensorMap tmB;
-  CUtensorMap tmA, tmY;
+  CUtensorMap tmA;
   const void* map_x;
-  const void* map_y;
 };
 
 namespace {
@@ -825,7 +820,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
 }
 
 namespace {
-convf_status encode_io_maps(convf_handle* h, const void* x, const void* y) {
+convf_status encode_a_map(convf_handle* h, const void* x) {
   const Shape& s = h->s;
   CUresult r;
   if (h->a_mode == kA2D) {
@@ -850,16 +845,7 @@ convf_status encode_io_maps(convf_handle* h, const void* x, const void* y) {
   } else {
     std::memset(&h->tmA, 0, sizeof h->tmA);
   }
-  const cuuint64_t ydims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
-  const cuuint64_t ystr[1] = {(cuuint64_t)s.K * 4};
-  const cuuint32_t ybox[2] = {32, 128};
-  const cuuint32_t es[2] = {1, 1};
-  r = g_encode_tiled(&h->tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(y), ydims, ystr, ybox, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "output tensor map encoding failed (CUresult %d)", (int)r);
   h->map_x = x;
-  h->map_y = y;
   return CONVF_OK;
 }
 }  // namespace
@@ -941,8 +927,8 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       break;
     }
     default: {
-      if (x != h->map_x || y != h->map_y) {
-        if ((st = encode_io_maps(h, x, y)) != CONVF_OK) return st;
+      if (x != h->map_x) {
+        if ((st = encode_a_map(h, x)) != CONVF_OK) return st;
       }
       TcConvParams p{};
       p.M = (int)s.M; p.Kout = s.K; p.num_kb = h->num_kb; p.cblocks = h->cblocks; p.R = s.R; p.S = s.S;
@@ -959,13 +945,13 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
         p.x = h->xpad;
         p.C = h->cpt;
       }
-      p.lo = h->lo; p.hi = h->hi; p.status = h->status;
+      p.lo = h->lo; p.hi = h->hi; p.status = h->status; p.y = static_cast<float*>(y);
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
-        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
-        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
-        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
-        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->tmY, h->grid, gather, h->pair, strm); break;
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
       }
     }
   }
@@ -1148,7 +1134,7 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   const long long tiles = (s.M + 127) / 128 * n_blocks;
   const int grid = (int)std::min<long long>(tiles, num_sms);
 
-  CUtensorMap tmA, tmB, tmY;
+  CUtensorMap tmA, tmB;
   std::memset(&tmA, 0, sizeof tmA);
   const cuuint32_t es[2] = {1, 1};
   {
@@ -1160,15 +1146,6 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "weight tensor map encoding failed (CUresult %d)", (int)r);
   }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)s.K * 4};
-    const cuuint32_t box[2] = {32, 128};
-    CUresult r = g_encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, es,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "output tensor map encoding failed (CUresult %d)", (int)r);
-  }
 
   ce = launch_pad_channels(static_cast<const uint16_t*>(x), xpad, (long long)s.N * s.H * s.W, s.C, cpt, num_sms, strm);
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "channel pre-pass launch failed: %s", cudaGetErrorString(ce));
@@ -1179,12 +1156,12 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
   p.H = s.H; p.W = s.W; p.C = cpt; p.Ho = s.Ho; p.Wo = s.Wo;
   p.n_blocks = n_blocks; p.num_tiles = (int)tiles; p.a_mode = kAGather;
-  p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status;
+  p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status; p.y = static_cast<float*>(y);
   p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
   switch (bn) {
-    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, tmY, grid, true, false, strm); break;
-    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, tmY, grid, true, false, strm); break;
-    default: ce = launch_tc_conv_bn128(p, tmA, tmB, tmY, grid, true, false, strm); break;
+    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, strm); break;
+    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, strm); break;
+    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, strm); break;
   }
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();

@@ -65,6 +65,7 @@ struct TcConvParams {
   int row_bytes;          // W*C*2, bytes of one input row
   int cpt;                // gather mode: channels per tap in the reduction layout (4, 8; 0 = C)
   float lo, hi;           // activation clamp
+  float* y;               // NHWC fp32 output [M][Kout]
   int* status;            // device status word
 };
 

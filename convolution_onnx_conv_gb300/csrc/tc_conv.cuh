@@ -25,8 +25,7 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kEpiCols = 32;
-constexpr int kEpiTileBytes = kBM * kEpiCols * 4;
-constexpr int kNumEpiBuf = 2;
+constexpr int kEpiWarpBytes = 32 * kEpiCols * 4;   // one epilogue warp's 32 x 32 fp32 transpose
 constexpr int kPatchBufBytes = 32768;
 constexpr int kGatherThreads = 256;
 
@@ -41,12 +40,12 @@ struct TcCfg {
   // operand ingest per SM does not grow with pipeline depth, so stages give way to the epilogue
   static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3)
                                         : (PAIR ? (BN == 256 ? 5 : (BN == 128 ? 6 : 8))
-                                                : (BN == 256 ? 3 : (BN == 128 ? 5 : (BN == 64 ? 6 : 8))));
+                                                : (BN == 256 ? 4 : (BN == 128 ? 6 : 8)));
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
   // gather mode: two buffers for the input rows one tile needs (TcConvParams::patch_rows)
   static constexpr int kPatchBytes = GATHER ? 2 * kPatchBufBytes : 0;
-  static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + kEpiGroups * kNumEpiBuf * kEpiTileBytes +
+  static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + 4 * kEpiGroups * kEpiWarpBytes +
                                kPatchBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
@@ -55,7 +54,7 @@ struct TcCfg {
 template <int BN, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY) {
+                   const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
   // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
@@ -73,7 +72,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATileBytes;
   uint8_t* sEpi = sB + kStages * Cfg::kBTileBytes;
-  uint8_t* sPatch = sEpi + Cfg::kEpiGroups * kNumEpiBuf * kEpiTileBytes;
+  uint8_t* sPatch = sEpi + 4 * Cfg::kEpiGroups * kEpiWarpBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPatch + Cfg::kPatchBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -99,7 +98,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4 * Cfg::kEpiGroups);   // one arrival per epilogue warp
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4);   // one arrival per warp of the draining group
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 1);
     }
@@ -107,7 +106,6 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmY);
     if (!GATHER) tma_prefetch_desc(&tmA);
   }
   if (warp == 2 && lane == 0) tma_prefetch_desc(&tmB);
@@ -272,41 +270,38 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
   } else if (warp < 3 + 4 * Cfg::kEpiGroups) {
     // ------------------------------------------------------------------ epilogue
-    // kEpiGroups warpgroups; group eg takes the 32-column chunks eg, eg + kEpiGroups, ... of
-    // every tile, with its own staging buffers and named barrier.
+    // kEpiGroups warpgroups take alternate tiles (with two groups, group g drains accumulator
+    // buffer g).  Each warp owns TMEM lanes 32q..32q+31 = 32 tile rows and works alone:
+    // tcgen05.ld of two 32-column chunks at a time (the buffer is released after the last
+    // read) -> its own 4 KB of smem (thread = row) -> read back as thread = (row, 4 channels),
+    // scale/bias/clamp, 16-byte stores that cover four whole 128-byte row segments.
     constexpr int G = Cfg::kEpiGroups;
-    const int et = threadIdx.x - 96;
-    const int eg = et >> 7;                // epilogue group
-    const int el = et & 127;               // index within the group (0 = leader)
-    const int bar_id = 1 + 2 * eg;         // named barriers 1 and 3 (2 belongs to the gatherers)
+    const int eg = (warp - 3) >> 2;        // epilogue group
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;         // tile row == TMEM lane
-    uint8_t* epi = sEpi + eg * kNumEpiBuf * kEpiTileBytes;
-    volatile int* go = epi_go + 2 * eg;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int ebuf = 0;
+    float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kEpiWarpBytes);
+    const int sub = lane >> 3;             // row within each group of four in the store phase
+    const int c4 = lane & 7;               // 4-channel column group
     int it = 0;
-    for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
-      const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
-      const int n0 = (tile % p.n_blocks) * BN;
-      if (el == 0) go[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status) ? 1 : 0;
-      named_barrier(bar_id, 128);
-      if (!go[it & 1]) break;
+    for (int tile = tstart + eg * tstep; tile < p.num_tiles; tile += G * tstep, it += G) {
+      const int acc = (it + eg) & 1;                 // accumulator buffer of this CTA's tile it+eg
+      const uint32_t acc_phase = ((it + eg) >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
+      const int m0 = (tile / p.n_blocks) * kTileM + mrow_off + q * 32;   // this warp's first row
+      const int n0 = (tile % p.n_blocks) * BN;
       const int left = p.Kout - n0;
       const int nchunks = left >= BN ? BN / kEpiCols : (left + kEpiCols - 1) / kEpiCols;
-      bool released = false;
-      for (int ch = eg; ch < nchunks; ch += G) {
-        const int nc = n0 + ch * kEpiCols;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(acc * BN + ch * kEpiCols),
-                           v);
+      float* yw = p.y + static_cast<size_t>(m0) * p.Kout + n0;
+      for (int ch = 0; ch < nchunks; ch += 2) {
+        const bool two = ch + 1 < nchunks;
+        uint32_t v[2][32];
+        const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                              static_cast<uint32_t>(acc * BN + ch * kEpiCols);
+        tmem_ld_32x32b_x32(tcol, v[0]);
+        if (two) tmem_ld_32x32b_x32(tcol + kEpiCols, v[1]);
         tmem_ld_wait();
-        if (ch + G >= nchunks) {
-          // the warp's last TMEM read of the tile: release the accumulator buffer (one arrival
-          // per warp; tcgen05.ld is warp-collective, so the whole warp is here)
+        if (ch + 2 >= nchunks) {
+          // the warp's last TMEM read of the tile (tcgen05.ld is warp-collective)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -315,54 +310,36 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             else
               mbar_arrive(&tempty[acc]);
           }
-          released = true;
         }
-        const float4* sc4 = reinterpret_cast<const float4*>(p.scale + nc);
-        const float4* bi4 = reinterpret_cast<const float4*>(p.bias + nc);
-        float o[32];
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 sc = __ldg(sc4 + j4);
-          const float4 bi = __ldg(bi4 + j4);
-          o[4 * j4 + 0] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 0]), sc.x, bi.x), p.lo), p.hi);
-          o[4 * j4 + 1] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 1]), sc.y, bi.y), p.lo), p.hi);
-          o[4 * j4 + 2] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 2]), sc.z, bi.z), p.lo), p.hi);
-          o[4 * j4 + 3] = fminf(fmaxf(fmaf(__uint_as_float(v[4 * j4 + 3]), sc.w, bi.w), p.lo), p.hi);
-        }
-        // the staging buffer used two chunks ago must have been read out by its TMA store
-        if (el == 0) bulk_wait_read<1>();
-        named_barrier(bar_id, 128);
-        uint8_t* buf = epi + ebuf * kEpiTileBytes + row * 128;
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int nc = (ch + h) * kEpiCols;
+          // row `lane` -> smem, 16-byte chunks XOR-swizzled by row: both phases conflict-free
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          *reinterpret_cast<float4*>(buf + ((c16 ^ (row & 7)) << 4)) =
-              make_float4(o[4 * c16], o[4 * c16 + 1], o[4 * c16 + 2], o[4 * c16 + 3]);
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(wst + lane * 32 + ((c ^ (lane & 7)) << 2)) =
+                make_float4(__uint_as_float(v[h][4 * c]), __uint_as_float(v[h][4 * c + 1]),
+                            __uint_as_float(v[h][4 * c + 2]), __uint_as_float(v[h][4 * c + 3]));
+          __syncwarp();
+          const bool col_ok = nc + 4 * c4 < left;
+          const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
+          const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + sub;
+            const float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+            if (col_ok && m0 + r < p.M)
+              *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
+                  make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
+          }
+          __syncwarp();
         }
-        fence_proxy_async_smem();
-        named_barrier(bar_id, 128);
-        if (el == 0) {
-          tma_store_2d(&tmY, epi + ebuf * kEpiTileBytes, nc, m0);
-          bulk_commit();
-        }
-        ebuf ^= 1;
-      }
-      if (!released) {
-        // no chunk of this tile fell to this group: nothing read, release at once
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (PAIR && !leader)
-            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
-          else
-            mbar_arrive(&tempty[acc]);
-        }
-      }
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
       }
     }
-    if (el == 0) bulk_wait_all();
   } else if (GATHER) {
     // ------------------------------------------------------------------ row gatherers
     // 256 threads, two per tile row: thread gt assembles half gh of row gr in every k-block
@@ -517,7 +494,7 @@ teardown:
 
 template <int BN, bool GATHER, bool PAIR>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const CUtensorMap& tmY, int grid, cudaStream_t stream) {
+                             int grid, cudaStream_t stream) {
   static bool configured = false;
   auto* k = tc_conv_kernel<BN, GATHER, PAIR>;
   if (!configured) {
@@ -531,7 +508,7 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
     configured = true;
   }
   return launch_pdl(k, dim3(grid), dim3(TcCfg<BN, GATHER, PAIR>::kThreads), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
-                    PAIR ? 2 : 1, p, tmA, tmB, tmY);
+                    PAIR ? 2 : 1, p, tmA, tmB);
 }
 
 }  // namespace convf

@@ -10,19 +10,19 @@
 
 namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
-                                                   const CUtensorMap& tmB, const CUtensorMap& tmY, int grid,
+                                                   const CUtensorMap& tmB, int grid,
                                                    bool gather, bool pair, cudaStream_t stream) {
   if (pair) {
     if (gather) return cudaErrorInvalidValue;
-    return launch_tc_conv_t<CONVF_BN, false, true>(p, tmA, tmB, tmY, grid, stream);
+    return launch_tc_conv_t<CONVF_BN, false, true>(p, tmA, tmB, grid, stream);
   }
 #if CONVF_BN == 256
   // gather mode needs room for the input-row patch: tile widths up to 128 only
   if (gather) return cudaErrorInvalidValue;
-  return launch_tc_conv_t<CONVF_BN, false, false>(p, tmA, tmB, tmY, grid, stream);
+  return launch_tc_conv_t<CONVF_BN, false, false>(p, tmA, tmB, grid, stream);
 #else
-  return gather ? launch_tc_conv_t<CONVF_BN, true, false>(p, tmA, tmB, tmY, grid, stream)
-                : launch_tc_conv_t<CONVF_BN, false, false>(p, tmA, tmB, tmY, grid, stream);
+  return gather ? launch_tc_conv_t<CONVF_BN, true, false>(p, tmA, tmB, grid, stream)
+                : launch_tc_conv_t<CONVF_BN, false, false>(p, tmA, tmB, grid, stream);
 #endif
 }
 }  // namespace convf
