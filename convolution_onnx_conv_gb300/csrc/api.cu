@@ -147,6 +147,8 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
   if (d->cta_pair < 0 || d->cta_pair > 2)
     return fail(CONVF_ERR_INVALID_ARG, "cta_pair=%d is not 0 (auto), 1 (single CTA) or 2 (CTA pair)", d->cta_pair);
+  if (d->stream_k < 0 || d->stream_k > 2)
+    return fail(CONVF_ERR_INVALID_ARG, "stream_k=%d is not 0 (auto), 1 (off) or 2 (on)", d->stream_k);
   return CONVF_OK;
 }
 
@@ -299,18 +301,26 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
   return fail(CONVF_ERR_UNSUPPORTED, "no kernel serves this conv: %s", reasons.c_str());
 }
 
-// Tile shape for the tcgen05 kernels: minimise waves x per-tile time.  Per 64-wide reduction
-// block a single CTA spends about {670, 694, 782, 1620} SM cycles for tile widths
+// Tile shape for the tcgen05 kernels: minimise the time of the busiest CTA.  Per 64-wide
+// reduction block a single CTA spends about {670, 694, 782, 1620} SM cycles for tile widths
 // {32, 64, 128, 256} (measured on GB300 over the ResNet-50 layers: each SM ingests operands at
 // about 43 B/cycle, plus pipeline overheads); a tile also writes 128 x bn fp32 outputs at about
-// 20 B/cycle per SM.  CTA pairs (256-row tiles, half the weight tile per CTA) cut the ingested
-// bytes but measured slower on every ResNet-50 layer (longer cross-SM handshakes), so they are
-// used only when requested: pair_mode 0 = auto (single CTAs), 1 = single, 2 = pairs.
-void pick_tile(long long M, int K, int num_kb, int num_sms, int max_bn, int pair_mode, int* bn_out, bool* pair_out) {
+// 20 B/cycle per SM; the busiest CTA runs ceil(tiles / CTAs) tiles.
+// CTA pairs (256-row tiles, half the weight tile per CTA) cut the ingested bytes but measured
+// slower on every ResNet-50 layer (longer cross-SM handshakes), so they are used only when
+// requested: pair_mode 0 = auto (single CTAs), 1 = single, 2 = pairs.  Stream-K likewise
+// measured slower on the ResNet-50 layers it would pick (the partial write-back and read-back
+// run at the epilogue's store rate, about 13 B/cycle per SM, and sit on the critical path), so
+// auto keeps whole tiles: sk_mode 0 = auto (off), 1 = off, 2 = on (single CTAs only; ignored
+// with pairs or when sk_ok is false).
+void pick_tile(long long M, int K, int num_kb, int num_sms, int max_bn, int pair_mode, int sk_mode, bool sk_ok,
+               int* bn_out, bool* pair_out, bool* sk_out) {
   const bool pair = pair_mode == 2;
   const long long tile_m = pair ? 256 : 128;
   const long long units = pair ? num_sms / 2 : num_sms;
+  const bool sk_allowed = sk_ok && !pair && sk_mode != 1;
   int best_bn = max_bn;
+  bool best_sk = false;
   double best_cost = 1e300;
   for (int bn : {256, 128, 64, 32}) {
     if (bn > max_bn) continue;
@@ -318,14 +328,19 @@ void pick_tile(long long M, int K, int num_kb, int num_sms, int max_bn, int pair
     const long long tiles = (M + tile_m - 1) / tile_m * ((K + bn - 1) / bn);
     const long long waves = (tiles + units - 1) / units;
     const double kb_cycles = bn == 32 ? 670.0 : bn == 64 ? 694.0 : bn == 128 ? 782.0 : 1620.0;
-    const double cost = (double)waves * std::max(num_kb * kb_cycles, 128.0 * bn * 4.0 / 20.0);
+    const double per_tile = std::max(num_kb * kb_cycles, 128.0 * bn * 4.0 / 20.0);
+    double cost = (double)waves * per_tile;
+    bool sk = false;
+    if (sk_allowed && sk_mode == 2 && num_kb >= 2) sk = true;
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best_bn = bn;
+      best_sk = sk;
     }
   }
   *bn_out = best_bn;
   *pair_out = pair;
+  *sk_out = best_sk;
 }
 
 // Gather variant: input rows one 128-pixel tile reads, staged whole in shared memory, when
@@ -407,6 +422,9 @@ struct convf_handle {
   // tcgen05 configuration
   int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
   bool pair;        // CTA-pair (cta_group::2) 256-row tiles
+  bool sk;          // stream-K work split
+  float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
+  int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
   WinGeom wg;       // window variant geometry
   CUtensorMap tmB;
   CUtensorMap tmA;
@@ -534,9 +552,9 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
       return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d exceeds %d for the gather variant", desc->tile_n, max_bn);
     if (gather && desc->cta_pair == 2)
       return fail(CONVF_ERR_UNSUPPORTED, "the gather variant runs on single CTAs");
-    bool pair = false;
+    bool pair = false, sk = false;
     pick_tile(s.M, s.K, kt / 64, num_sms > 1 ? num_sms : 2, desc->tile_n ? desc->tile_n : max_bn,
-              gather ? 1 : desc->cta_pair, &bn, &pair);
+              gather ? 1 : desc->cta_pair, desc->stream_k, !gather, &bn, &pair, &sk);
     if (desc->tile_n) bn = desc->tile_n;
     if (cta_pair) *cta_pair = pair ? 1 : 0;
   } else if (v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
@@ -641,7 +659,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   // device layout
   size_t off = 0;
   auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  size_t o_w = 0, o_taps = 0, o_scale = 0, o_bias = 0, o_qb = 0, o_qm = 0, o_qs = 0, o_pad = 0;
+  size_t o_w = 0, o_taps = 0, o_scale = 0, o_bias = 0, o_qb = 0, o_qm = 0, o_qs = 0, o_pad = 0, o_skws = 0,
+         o_skflags = 0;
   std::vector<uint16_t> wpack;
   std::vector<float> taps;
   if (variant == CONVF_VARIANT_DEPTHWISE) {
@@ -676,6 +695,20 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
+    const bool gather = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER;
+    const int max_bn = gather ? 128 : 256;
+    if (desc->tile_n > max_bn || (gather && desc->cta_pair == 2)) {
+      delete h;
+      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d / cta_pair=%d not served by the gather variant", desc->tile_n,
+                  desc->cta_pair);
+    }
+    pick_tile(s.M, s.K, h->ktot / 64, h->num_sms, desc->tile_n ? desc->tile_n : max_bn, gather ? 1 : desc->cta_pair,
+              desc->stream_k, !gather, &h->bn, &h->pair, &h->sk);
+    if (desc->tile_n) h->bn = desc->tile_n;
+    if (h->sk) {
+      o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
+      o_skflags = carve((size_t)h->num_sms * sizeof(int));
+    }
     if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER && gather_cpt(s) > 0)
       o_pad = carve((size_t)s.N * s.H * s.W * gather_cpt(s) * sizeof(uint16_t));
   }
@@ -715,6 +748,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   } else {
     h->w_bf16 = reinterpret_cast<uint16_t*>(base + o_w);
     h->xpad = o_pad ? reinterpret_cast<uint16_t*>(base + o_pad) : nullptr;
+    h->sk_ws = o_skws ? reinterpret_cast<float*>(base + o_skws) : nullptr;
+    h->sk_flags = o_skflags ? reinterpret_cast<int*>(base + o_skflags) : nullptr;   // zeroed by the upload
     h->scale = reinterpret_cast<float*>(base + o_scale);
     h->bias = reinterpret_cast<float*>(base + o_bias);
     std::memcpy(staging.data() + o_w, wpack.data(), wpack.size() * sizeof(uint16_t));
@@ -781,17 +816,6 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       delete h;
       return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled/Im2col are unavailable from the driver");
     }
-    const bool gather = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER;
-    const int max_bn = gather ? 128 : 256;
-    if (desc->tile_n > max_bn || (gather && desc->cta_pair == 2)) {
-      cudaFree(h->dev);
-      delete h;
-      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d / cta_pair=%d not served by the gather variant", desc->tile_n,
-                  desc->cta_pair);
-    }
-    pick_tile(s.M, s.K, h->ktot / 64, h->num_sms, desc->tile_n ? desc->tile_n : max_bn, gather ? 1 : desc->cta_pair,
-              &h->bn, &h->pair);
-    if (desc->tile_n) h->bn = desc->tile_n;
     h->cpt = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? gather_cpt(s) : 0;
     h->patch_rows = variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER ? patch_rows_for(s, h->cpt ? h->cpt : s.C) : 0;
     h->row_bytes = s.W * (h->cpt ? h->cpt : s.C) * 2;
@@ -800,7 +824,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     const long long tile_m = h->pair ? 256 : 128;
     const long long tiles = (s.M + tile_m - 1) / tile_m * h->n_blocks;
     h->num_tiles = (int)tiles;
-    h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2) : (int)std::min<long long>(tiles, h->num_sms);
+    h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2)
+                      : (int)std::min<long long>(h->sk ? tiles * h->num_kb : tiles, h->num_sms);
     const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
     const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn)};
@@ -946,6 +971,7 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
         p.C = h->cpt;
       }
       p.lo = h->lo; p.hi = h->hi; p.status = h->status; p.y = static_cast<float*>(y);
+      p.sk = h->sk ? 1 : 0; p.sk_ws = h->sk_ws; p.sk_flags = h->sk_flags;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
         case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
@@ -1009,10 +1035,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
   else
     snprintf(buf, len,
-             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d kblocks=%d tiles=%d "
-             "grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
+             "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
-             h->num_kb, h->num_tiles, h->grid, h->patch_rows, h->cpt, h->dev_bytes);
+             h->sk ? 1 : 0, h->num_kb, h->num_tiles, h->grid, h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
 }
 
@@ -1128,7 +1154,8 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   tc_layout(CONVF_VARIANT_IMPLICIT_GEMM_GATHER, s, &am, &cblocks, &ktot, &cpad);
   int bn = 0;
   bool pair = false;
-  pick_tile(s.M, s.K, ktot / 64, num_sms, desc->tile_n ? desc->tile_n : 128, 1, &bn, &pair);
+  bool sk = false;
+  pick_tile(s.M, s.K, ktot / 64, num_sms, desc->tile_n ? desc->tile_n : 128, 1, 1, false, &bn, &pair, &sk);
   if (desc->tile_n) bn = desc->tile_n;
   const int n_blocks = (s.K + bn - 1) / bn;
   const long long tiles = (s.M + 127) / 128 * n_blocks;

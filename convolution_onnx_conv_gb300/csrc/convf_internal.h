@@ -67,6 +67,13 @@ struct TcConvParams {
   float lo, hi;           // activation clamp
   float* y;               // NHWC fp32 output [M][Kout]
   int* status;            // device status word
+  // stream-K: every CTA takes an equal share of the num_tiles x num_kb iterations; a tile split
+  // across CTAs is finished by the CTA holding its k-block 0, which adds the others' fp32
+  // partials (one workspace slot of 128 x BN floats and one flag per CTA, flags zero between
+  // launches)
+  int sk;                 // 0 = whole tiles per CTA
+  float* sk_ws;
+  int* sk_flags;
 };
 
 

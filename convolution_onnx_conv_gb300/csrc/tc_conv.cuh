@@ -51,6 +51,40 @@ struct TcCfg {
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
 };
 
+// Work of one CTA as a sequence of segments (tile, k-blocks [ka, kend)): whole tiles tstart,
+// tstart + tstep, ... or, with stream-K, this CTA's contiguous share [it0, it1) of the
+// num_tiles x num_kb iterations cut at tile boundaries.  Every role walks the same sequence.
+struct SegSched {
+  int num_kb, num_tiles, tstep, tile;
+  bool sk;
+  long long it, it1;
+  __device__ SegSched(const TcConvParams& p, int tstart, int tstep_)
+      : num_kb(p.num_kb), num_tiles(p.num_tiles), tstep(tstep_), tile(tstart), sk(p.sk != 0), it(0), it1(0) {
+    if (sk) {
+      const long long total = static_cast<long long>(p.num_tiles) * p.num_kb;
+      it = total * blockIdx.x / gridDim.x;
+      it1 = total * (blockIdx.x + 1) / gridDim.x;
+    }
+  }
+  __device__ bool next(int& t, int& ka, int& kend) {
+    if (!sk) {
+      if (tile >= num_tiles) return false;
+      t = tile;
+      ka = 0;
+      kend = num_kb;
+      tile += tstep;
+      return true;
+    }
+    if (it >= it1) return false;
+    t = static_cast<int>(it / num_kb);
+    const long long base = static_cast<long long>(t) * num_kb;
+    ka = static_cast<int>(it - base);
+    kend = static_cast<int>(min(base + num_kb, it1) - base);
+    it = base + kend;
+    return true;
+  }
+};
+
 template <int BN, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
@@ -82,9 +116,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   uint64_t* pempty = bars + 2 * kStages + 6;   // input-row patch consumed (gather mode)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // go/abort decisions broadcast by a leader thread through a named barrier; two slots used
-  // alternately so the leader never overwrites a flag another thread has yet to read
-  volatile int* epi_go = abort_flag + 1;   // two slots per epilogue group
+  // gather mode: go/abort decisions broadcast by a leader thread through a named barrier; two
+  // slots used alternately so the leader never overwrites a flag another thread has yet to read
   volatile int* gat_go = abort_flag + 5;
 
   const int warp = threadIdx.x >> 5;
@@ -136,7 +169,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int tile = tstart; tile < p.num_tiles; tile += tstep, ++it) {
+      SegSched sched(p, tstart, tstep);
+      int tile, ka, kend;
+      for (; sched.next(tile, ka, kend); ++it) {
         const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
         if (GATHER) {
           if (p.patch_rows > 0) {
@@ -168,8 +203,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           hb = oh * p.sh - p.pt;
           wb = ow * p.sw - p.pl;
         }
-        int tap = 0, cb = 0;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        int tap = p.cblocks ? ka / p.cblocks : 0, cb = p.cblocks ? ka - (ka / p.cblocks) * p.cblocks : 0;
+        for (int kb = ka; kb < kend; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
           // a pair's loads all complete on the leader's barrier, which expects both CTAs' bytes
           if (!PAIR || leader) mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * kATileBytes : kATileBytes);
@@ -206,9 +241,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = tstart; tile < p.num_tiles; tile += tstep) {
+      SegSched sched(p, tstart, tstep);
+      int tile, ka, kend;
+      while (sched.next(tile, ka, kend)) {
         const int n0 = (tile % p.n_blocks) * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = ka; kb < kend; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
           if (!PAIR || leader)
             mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * Cfg::kBTileBytes : Cfg::kBTileBytes);
@@ -232,11 +269,13 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = tstart; tile < p.num_tiles; tile += tstep) {
+      SegSched sched(p, tstart, tstep);
+      int tile, ka, kend;
+      while (sched.next(tile, ka, kend)) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = ka; kb < kend; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto teardown;
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * kATileBytes));
@@ -245,9 +284,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
             if (PAIR)
-              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb != ka) || k != 0);
             else
-              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb != ka) || k != 0);
           }
           if (PAIR)
             tc_commit_pair(&empty[stage], 3);
@@ -275,32 +314,71 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     // tcgen05.ld of two 32-column chunks at a time (the buffer is released after the last
     // read) -> its own 4 KB of smem (thread = row) -> read back as thread = (row, 4 channels),
     // scale/bias/clamp, 16-byte stores that cover four whole 128-byte row segments.
+    // With stream-K a segment that covers only part of a tile's reduction is a contributor
+    // (k-block 0 not in it, always its CTA's first segment: the raw fp32 partial goes to this
+    // CTA's workspace slot with plain stores, then the CTA's flag is raised) or the tile's
+    // owner (k-block 0 in it, its CTA's last segment: waits for the contributors' flags, adds
+    // their partials -- eight loads in flight per contributor and chunk -- applies the
+    // epilogue and lowers the flags for the next launch).
     constexpr int G = Cfg::kEpiGroups;
     const int eg = (warp - 3) >> 2;        // epilogue group
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    const bool glead = warp == 3 + 4 * eg && lane == 0;   // group leader thread
     float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kEpiWarpBytes);
     const int sub = lane >> 3;             // row within each group of four in the store phase
     const int c4 = lane & 7;               // 4-channel column group
-    int it = 0;
-    for (int tile = tstart + eg * tstep; tile < p.num_tiles; tile += G * tstep, it += G) {
-      const int acc = (it + eg) & 1;                 // accumulator buffer of this CTA's tile it+eg
-      const uint32_t acc_phase = ((it + eg) >> 1) & 1;
+    const long long total_it = static_cast<long long>(p.num_tiles) * p.num_kb;
+    SegSched sched(p, tstart, tstep);
+    int tile, ka, kend;
+    for (int seg = 0; sched.next(tile, ka, kend); ++seg) {
+      if (seg % G != eg) continue;
+      const int acc = seg & 1;                         // accumulator buffer of segment seg
+      const uint32_t acc_phase = (seg >> 1) & 1;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int m0 = (tile / p.n_blocks) * kTileM + mrow_off + q * 32;   // this warp's first row
+      const int mode = ka > 0 ? 2 : (kend < p.num_kb ? 1 : 0);   // 0 whole, 1 owner, 2 contributor
+      int d0 = 0, d1 = 0;                              // owner: contributing CTAs [d0, d1)
+      if (mode == 1) {
+        // contributors: the CTAs after this one whose share starts inside the tile
+        const long long tend = static_cast<long long>(tile + 1) * p.num_kb;
+        d0 = blockIdx.x + 1;
+        d1 = d0;
+        while (d1 < static_cast<int>(gridDim.x) && total_it * d1 / gridDim.x < tend) ++d1;
+        if (glead) {
+          for (int d = d0; d < d1; ++d) {
+            const long long t0 = clock64();
+            while (ld_acquire_gpu(p.sk_flags + d) == 0) {
+              if (*abort_flag) break;
+              if (clock64() - t0 > kWatchdogCycles) {
+                *abort_flag = 1;
+                atomicOr(p.status, kStatusTimeout);
+                break;
+              }
+            }
+          }
+        }
+        named_barrier(1 + 2 * eg, 128);
+      }
+      const int mt = (tile / p.n_blocks) * kTileM + mrow_off + q * 32;   // this warp's first row
       const int n0 = (tile % p.n_blocks) * BN;
       const int left = p.Kout - n0;
       const int nchunks = left >= BN ? BN / kEpiCols : (left + kEpiCols - 1) / kEpiCols;
-      float* yw = p.y + static_cast<size_t>(m0) * p.Kout + n0;
-      for (int ch = 0; ch < nchunks; ch += 2) {
-        const bool two = ch + 1 < nchunks;
-        uint32_t v[2][32];
+      float* yw = p.y + static_cast<size_t>(mt) * p.Kout + n0;
+      // workspace: one [128][BN] fp32 slot per CTA; this warp's rows of slot d start at ws(d)
+      const size_t slot = static_cast<size_t>(kBM) * BN;
+      float* wsw = p.sk_ws + slot * blockIdx.x + static_cast<size_t>(q * 32) * BN;
+      // two 32-column chunks per TMEM read round (one in gather mode, whose 480 threads have
+      // fewer registers each), so the buffer is released as early as possible
+      constexpr int kRead = GATHER ? 1 : 2;
+      for (int ch = 0; ch < nchunks; ch += kRead) {
+        const bool two = kRead == 2 && ch + 1 < nchunks;
+        uint32_t v[kRead][32];
         const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * BN + ch * kEpiCols);
         tmem_ld_32x32b_x32(tcol, v[0]);
-        if (two) tmem_ld_32x32b_x32(tcol + kEpiCols, v[1]);
+        if (two) tmem_ld_32x32b_x32(tcol + kEpiCols, v[kRead - 1]);
         tmem_ld_wait();
-        if (ch + 2 >= nchunks) {
+        if (ch + kRead >= nchunks) {
           // the warp's last TMEM read of the tile (tcgen05.ld is warp-collective)
           tc_fence_before();
           __syncwarp();
@@ -312,7 +390,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kRead; ++h) {
           if (h == 1 && !two) break;
           const int nc = (ch + h) * kEpiCols;
           // row `lane` -> smem, 16-byte chunks XOR-swizzled by row: both phases conflict-free
@@ -325,19 +403,59 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           const bool col_ok = nc + 4 * c4 < left;
           const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
           const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+          float4 part[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) part[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int d = d0; d < d1; ++d) {
+            // one contributor's partial for these rows: all eight loads in flight at once
+            const float* wd = p.sk_ws + slot * d + static_cast<size_t>(q * 32) * BN + nc + 4 * c4;
+            float4 b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + sub;
+              b[i] = (col_ok && mt + r < p.M) ? __ldcg(reinterpret_cast<const float4*>(wd + static_cast<size_t>(r) * BN))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              part[i].x += b[i].x;
+              part[i].y += b[i].y;
+              part[i].z += b[i].z;
+              part[i].w += b[i].w;
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + sub;
-            const float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
-            if (col_ok && m0 + r < p.M)
-              *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
-                  make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
+            float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+            if (!col_ok || mt + r >= p.M) continue;
+            if (mode == 2) {
+              __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a);
+              continue;
+            }
+            a.x += part[i].x;
+            a.y += part[i].y;
+            a.z += part[i].z;
+            a.w += part[i].w;
+            *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
+                make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
           }
           __syncwarp();
         }
+      }
+      if (mode == 2) {
+        // partial published: every thread's stores are visible before the flag
+        __threadfence();
+        named_barrier(1 + 2 * eg, 128);
+        if (glead) st_release_gpu(p.sk_flags + blockIdx.x, 1);
+      } else if (mode == 1) {
+        // every partial has been read: lower the contributors' flags for the next launch
+        named_barrier(1 + 2 * eg, 128);
+        if (glead)
+          for (int d = d0; d < d1; ++d) p.sk_flags[d] = 0;
       }
     }
   } else if (GATHER) {

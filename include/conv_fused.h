@@ -110,6 +110,11 @@ typedef struct {
   int tile_n;              /* tcgen05 variants: output-channel tile width 32/64/128/256, 0 = auto */
   int cta_pair;            /* tcgen05 variants: 0 = auto, 1 = single-CTA 128-row tiles, 2 = CTA pairs
                               (cta_group::2, 256-row tiles, each CTA loads half the weight tile) */
+  int stream_k;            /* TMA implicit-GEMM variants on single CTAs: 0 = auto, 1 = off (whole
+                              tiles per CTA), 2 = on (each CTA takes an equal share of the tile x
+                              reduction-block iterations; a split tile is finished by the CTA holding
+                              its first reduction block, which adds the others' fp32 partials from a
+                              handle-owned workspace).  Ignored where it does not apply. */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;

@@ -161,6 +161,58 @@ def test_every_tile_width(tile_n, cta_pair, shape):
     assert ok, (worst, idx)
 
 
+SK_CASES = [
+    # 8 tiles x 36 reduction blocks over 152 CTAs: every tile split across about 19 CTAs
+    S("sk_3x3_c256_many_splits", 2, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1), bias=True),
+    # M = 300 (ragged last row tile), 8 blocks per tile
+    S("sk_1x1_c512_ragged_m", 1, 512, 15, 20, 64, 1, 1),
+    # 100 tiles x 2 blocks over 152 CTAs: CTAs hold a tile's tail and the next tile's head
+    S("sk_1x1_tails_and_heads", 4, 128, 56, 57, 64, 1, 1, act=ACT_RELU6),
+    # strided im2col, K = 200 (ragged last column tile)
+    S("sk_3x3_s2_k200", 2, 128, 15, 15, 200, 3, 3, (2, 2), (1, 1, 1, 1)),
+]
+
+
+@pytest.mark.parametrize("tile_n", [0, 32, 128, 256])
+@pytest.mark.parametrize("spec", SK_CASES, ids=lambda s: s.name)
+def test_stream_k_every_output(spec, tile_n):
+    """Stream-K forced on: split tiles are finished by the CTA holding their first reduction
+    block from the other CTAs' fp32 partials.  Three runs on one handle: the flags that gate the
+    partials must be back at zero for the next launch."""
+    inp = inputs_for(spec, 7600 + SK_CASES.index(spec))
+    from parity import compare
+    c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                     *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, stream_k=2)
+    assert "stream_k=1" in c.describe(), c.describe()
+    x = to_device_nhwc(inp["x"])
+    ref = oracle_full(spec, inp)
+    for _ in range(3):
+        y = c(x)
+        torch.cuda.synchronize()
+        assert c.status() == cf.CONVF_OK
+        ok, worst, idx = compare(y.cpu().contiguous().numpy(), ref, False)
+        assert ok, (spec.name, worst, idx, c.describe())
+    c.close()
+
+
+def test_stream_k_off_matches_on():
+    spec = SK_CASES[0]
+    inp = inputs_for(spec, 7650)
+    outs = []
+    for sk in (1, 2):
+        c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                         *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                         pads=spec.pads, act=spec.act, stream_k=sk)
+        assert f"stream_k={sk - 1}" in c.describe()
+        outs.append(c(to_device_nhwc(inp["x"])).cpu())
+        c.close()
+    # the same partial products summed in a different order: equal within the parity tolerance
+    from parity import compare
+    ok, worst, idx = compare(outs[1].contiguous().numpy(), outs[0].contiguous().numpy().astype(np.float64), False)
+    assert ok, (worst, idx)
+
+
 def test_1x1_forced_through_im2col_and_gather():
     spec = S("one_by_one", 2, 64, 10, 10, 64, 1, 1)
     for v in (V.CONVF_VARIANT_GEMM_1X1, V.CONVF_VARIANT_IMPLICIT_GEMM, V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER):

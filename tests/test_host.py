@@ -256,3 +256,18 @@ def test_window_variant_is_automatic_only_for_wide_outputs():
     wide = cf.make_desc(2, 3, 64, 64, 64, 7, 7, (2, 2), (3, 3, 3, 3))       # 32 output columns
     assert cf.conv_fused_plan(narrow)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER
     assert cf.conv_fused_plan(wide)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW
+
+
+def test_stream_k_mode_is_validated():
+    """stream_k takes 0 (auto: whole tiles), 1 (off) or 2 (on); anything else is refused."""
+    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_16_s1b1_3x3@b32"]
+    for sk in (0, 1, 2):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         stream_k=sk)
+        assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM
+    for sk in (-1, 3):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         stream_k=sk)
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_plan(d)
+        assert e.value.status == cf.CONVF_ERR_INVALID_ARG
