@@ -54,20 +54,20 @@ struct TcCfg {
 // Work of one CTA as a sequence of segments (tile, k-blocks [ka, kend)): whole tiles tstart,
 // tstart + tstep, ... or, with stream-K, this CTA's contiguous share [it0, it1) of the
 // num_tiles x num_kb iterations cut at tile boundaries.  Every role walks the same sequence.
+template <bool SK>
 struct SegSched {
   int num_kb, num_tiles, tstep, tile;
-  bool sk;
   long long it, it1;
   __device__ SegSched(const TcConvParams& p, int tstart, int tstep_)
-      : num_kb(p.num_kb), num_tiles(p.num_tiles), tstep(tstep_), tile(tstart), sk(p.sk != 0), it(0), it1(0) {
-    if (sk) {
+      : num_kb(p.num_kb), num_tiles(p.num_tiles), tstep(tstep_), tile(tstart), it(0), it1(0) {
+    if (SK) {
       const long long total = static_cast<long long>(p.num_tiles) * p.num_kb;
       it = total * blockIdx.x / gridDim.x;
       it1 = total * (blockIdx.x + 1) / gridDim.x;
     }
   }
   __device__ bool next(int& t, int& ka, int& kend) {
-    if (!sk) {
+    if (!SK) {
       if (tile >= num_tiles) return false;
       t = tile;
       ka = 0;
@@ -85,11 +85,12 @@ struct SegSched {
   }
 };
 
-template <int BN, bool GATHER, bool PAIR>
+template <int BN, bool GATHER, bool PAIR, bool SK>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
+  static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
   // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
   // both CTAs' TMEM; each CTA loads its own 128 activation rows and half of the weight tile.
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      SegSched sched(p, tstart, tstep);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       for (; sched.next(tile, ka, kend); ++it) {
         const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      SegSched sched(p, tstart, tstep);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
         const int n0 = (tile % p.n_blocks) * BN;
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      SegSched sched(p, tstart, tstep);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     const int sub = lane >> 3;             // row within each group of four in the store phase
     const int c4 = lane & 7;               // 4-channel column group
     const long long total_it = static_cast<long long>(p.num_tiles) * p.num_kb;
-    SegSched sched(p, tstart, tstep);
+    SegSched<SK> sched(p, tstart, tstep);
     int tile, ka, kend;
     for (int seg = 0; sched.next(tile, ka, kend); ++seg) {
       if (seg % G != eg) continue;
@@ -336,9 +337,10 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       const uint32_t acc_phase = (seg >> 1) & 1;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int mode = ka > 0 ? 2 : (kend < p.num_kb ? 1 : 0);   // 0 whole, 1 owner, 2 contributor
+      // 0 whole tile, 1 owner, 2 contributor (always 0 without stream-K)
+      const int mode = !SK ? 0 : (ka > 0 ? 2 : (kend < p.num_kb ? 1 : 0));
       int d0 = 0, d1 = 0;                              // owner: contributing CTAs [d0, d1)
-      if (mode == 1) {
+      if (SK && mode == 1) {
         // contributors: the CTAs after this one whose share starts inside the tile
         const long long tend = static_cast<long long>(tile + 1) * p.num_kb;
         d0 = blockIdx.x + 1;
@@ -406,7 +408,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           float4 part[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) part[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int d = d0; d < d1; ++d) {
+          if (SK)
+            for (int d = d0; d < d1; ++d) {
             // one contributor's partial for these rows: all eight loads in flight at once
             const float* wd = p.sk_ws + slot * d + static_cast<size_t>(q * 32) * BN + nc + 4 * c4;
             float4 b[8];
@@ -429,14 +432,16 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             const int r = 4 * i + sub;
             float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
             if (!col_ok || mt + r >= p.M) continue;
-            if (mode == 2) {
-              __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a);
-              continue;
+            if (SK) {
+              if (mode == 2) {
+                __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a);
+                continue;
+              }
+              a.x += part[i].x;
+              a.y += part[i].y;
+              a.z += part[i].z;
+              a.w += part[i].w;
             }
-            a.x += part[i].x;
-            a.y += part[i].y;
-            a.z += part[i].z;
-            a.w += part[i].w;
             *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
                 make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
                             fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
@@ -446,12 +451,12 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           __syncwarp();
         }
       }
-      if (mode == 2) {
+      if (SK && mode == 2) {
         // partial published: every thread's stores are visible before the flag
         __threadfence();
         named_barrier(1 + 2 * eg, 128);
         if (glead) st_release_gpu(p.sk_flags + blockIdx.x, 1);
-      } else if (mode == 1) {
+      } else if (SK && mode == 1) {
         // every partial has been read: lower the contributors' flags for the next launch
         named_barrier(1 + 2 * eg, 128);
         if (glead)
@@ -610,11 +615,11 @@ teardown:
   }
 }
 
-template <int BN, bool GATHER, bool PAIR>
+template <int BN, bool GATHER, bool PAIR, bool SK = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER, PAIR>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcCfg<BN, GATHER, PAIR>::kSmem);

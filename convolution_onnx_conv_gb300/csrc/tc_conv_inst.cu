@@ -12,6 +12,11 @@ namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
                                                    const CUtensorMap& tmB, int grid,
                                                    bool gather, bool pair, cudaStream_t stream) {
+  if (p.sk) {
+    // stream-K: single CTAs with TMA activation loads only
+    if (gather || pair) return cudaErrorInvalidValue;
+    return launch_tc_conv_t<CONVF_BN, false, false, true>(p, tmA, tmB, grid, stream);
+  }
   if (pair) {
     if (gather) return cudaErrorInvalidValue;
     return launch_tc_conv_t<CONVF_BN, false, true>(p, tmA, tmB, grid, stream);
