@@ -141,7 +141,7 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "clip bounds (%g, %g) need lo <= hi", d->clip_lo, d->clip_hi);
   if (d->dtype == CONVF_S8 && (d->act == CONVF_ACT_RELU6 || d->act == CONVF_ACT_CLIP))
     return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
-  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
+  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
   if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
@@ -216,6 +216,60 @@ void pack_window(const uint16_t* W, const Shape& s, const WinGeom& g, uint16_t* 
         }
 }
 
+// ------------------------------------------------------------------ halo-tile geometry
+struct HaloGeom {
+  int Wp, TR, tiles_per_img, cblocks, bn, tpo, b_stages;
+  uint32_t patch_bytes;
+  double valid;     // fraction of the 128 MMA rows of a tile that are real outputs
+};
+
+// Tile width for the halo kernel: per 64-channel block a CTA ingests one patch plus R*S weight
+// tiles (about 60 B/cycle per SM), issues R*S/tpo weight loads (about 600 cycles each on one
+// warp; tpo = the most taps per load within 48 KB) and runs R*S*4 MMAs (48 / 64 / 128 cycles
+// each for N = 64 / 128 / 256); minimise waves x the slowest of the three.
+std::string halo_geom(const Shape& s, int num_sms, int forced_bn, HaloGeom* g) {
+  if (s.sh != 1 || s.sw != 1) return "halo tiles need stride 1";
+  if (s.dh != 1 || s.dw != 1) return "halo tiles need dilation 1";
+  if (s.R * s.S < 2) return "halo tiles need a filter with more than one tap";
+  if (s.R * s.S > 64) return "halo tiles need R*S <= 64";
+  if (s.C % 8) return "halo tiles need C % 8 == 0 (16-byte TMA row stride)";
+  g->Wp = s.W + s.pl + s.pr;
+  if (g->Wp > 128) return "halo tiles need W + pl + pr <= 128";
+  g->TR = std::min(128 / g->Wp, s.Ho);
+  g->tiles_per_img = (s.Ho + g->TR - 1) / g->TR;
+  g->cblocks = (s.C + 63) / 64;
+  g->patch_bytes = (uint32_t)((g->TR + s.R - 1) * g->Wp * 128);
+  if (g->TR + s.R - 1 > 256) return "halo tiles: patch taller than a TMA box";
+  g->valid = (double)g->TR * s.Wo / 128.0;
+  double best = 1e300;
+  g->bn = 0;
+  for (int bn : {64, 128, 256}) {
+    if (forced_bn && bn != forced_bn) continue;
+    if (!forced_bn && bn > 64 && bn / 2 >= s.K) continue;
+    int tpo = 1;
+    for (int t = 1; t <= s.R * s.S; ++t)
+      if ((s.R * s.S) % t == 0 && (size_t)t * bn * 128 <= 49152) tpo = t;
+    const size_t stage = (size_t)tpo * bn * 128;
+    const size_t fixed = tc_halo_fixed_smem(s.R, s.S, g->Wp, g->patch_bytes);
+    if (fixed + 2 * stage > 232448) continue;
+    const int stages = (int)std::min<size_t>(8, (232448 - fixed) / stage);
+    const double ingest = g->cblocks * (g->patch_bytes + (double)s.R * s.S * bn * 128.0) / 60.0;
+    const double issue = g->cblocks * (double)(s.R * s.S / tpo) * 600.0;
+    const double mma = (double)g->cblocks * s.R * s.S * 4 * (bn == 64 ? 48.0 : bn == 128 ? 64.0 : 128.0);
+    const long long tiles = (long long)s.N * g->tiles_per_img * ((s.K + bn - 1) / bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const double cost = (double)waves * std::max(std::max(ingest, issue), mma);
+    if (cost < best * 0.999) {
+      best = cost;
+      g->bn = bn;
+      g->tpo = tpo;
+      g->b_stages = stages;
+    }
+  }
+  if (!g->bn) return "halo tiles: the patch and weight stages exceed shared memory";
+  return "";
+}
+
 // ------------------------------------------------------------------ variant selector
 // Why a shape cannot use a variant ("" = it can).
 std::string cannot(int v, const convf_desc* d, const Shape& s) {
@@ -248,6 +302,14 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       if ((long long)(s.R - 1) * s.dh > 65535 || (long long)(s.S - 1) * s.dw > 65535)
         return "filter offsets exceed 16 bits";
       return "";
+    case CONVF_VARIANT_IMPLICIT_GEMM_HALO: {
+      if (!bf) return "implicit GEMM serves bf16 only";
+      if (d->group != 1) return "implicit GEMM needs group == 1";
+      if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte output row stride)";
+      if (d->tile_n == 32) return "halo tiles come 64, 128 or 256 channels wide";
+      HaloGeom g;
+      return halo_geom(s, 148, d->tile_n, &g);
+    }
     case CONVF_VARIANT_IMPLICIT_GEMM_WINDOW: {
       if (!bf) return "implicit GEMM serves bf16 only";
       if (d->group != 1) return "implicit GEMM needs group == 1";
@@ -278,8 +340,9 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
     *out = d->variant;
     return CONVF_OK;
   }
-  const int order_bf16[5] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM,
-                             CONVF_VARIANT_IMPLICIT_GEMM_WINDOW, CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
+  const int order_bf16[6] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM_HALO,
+                             CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW,
+                             CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
   if (d->dtype == CONVF_S8) {
     std::string why = cannot(CONVF_VARIANT_INT8, d, s);
     if (!why.empty()) return fail(CONVF_ERR_UNSUPPORTED, "int8 conv refused: %s", why.c_str());
@@ -292,6 +355,12 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
     // a tile is one output row segment of 128 pixels: narrower outputs leave most rows idle
     if (why.empty() && v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW && s.Wo < 32)
       why = "window mode is chosen automatically only for outputs at least 32 pixels wide";
+    if (why.empty() && v == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
+      HaloGeom g;
+      halo_geom(s, 148, d->tile_n, &g);
+      if (g.valid < 0.6) why = "halo tiles are chosen automatically only when 60% of a tile's rows are outputs";
+      if (d->cta_pair == 2 || d->stream_k == 2) why = "halo tiles run on single CTAs without stream-K";
+    }
     if (why.empty()) {
       *out = v;
       return CONVF_OK;
@@ -426,6 +495,7 @@ struct convf_handle {
   float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
   int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
   WinGeom wg;       // window variant geometry
+  HaloGeom hg;      // halo variant geometry
   CUtensorMap tmB;
   CUtensorMap tmA;
   const void* map_x;
@@ -457,7 +527,7 @@ void tc_layout(int variant, const Shape& s, int* a_mode, int* cblocks, int* ktot
     *cblocks = (s.C + 63) / 64;
     *ktot = *cblocks * 64;
     *cpad = *ktot;
-  } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM) {
+  } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM || variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
     *a_mode = kAIm2col;
     *cblocks = (s.C + 63) / 64;
     *cpad = *cblocks * 64;
@@ -557,6 +627,12 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
               gather ? 1 : desc->cta_pair, desc->stream_k, !gather, &bn, &pair, &sk);
     if (desc->tile_n) bn = desc->tile_n;
     if (cta_pair) *cta_pair = pair ? 1 : 0;
+  } else if (v == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
+    HaloGeom g;
+    halo_geom(s, num_sms > 1 ? num_sms : 2, desc->tile_n, &g);
+    int am, cb, cp;
+    tc_layout(v, s, &am, &cb, &kt, &cp);
+    bn = g.bn;
   } else if (v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
     WinGeom g;
     win_geom(s, &g);
@@ -578,7 +654,7 @@ convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const 
   if (st != CONVF_OK) return st;
   if (!W || !out) return fail(CONVF_ERR_INVALID_ARG, "W/out is NULL");
   if (variant != CONVF_VARIANT_GEMM_1X1 && variant != CONVF_VARIANT_IMPLICIT_GEMM &&
-      variant != CONVF_VARIANT_IMPLICIT_GEMM_GATHER)
+      variant != CONVF_VARIANT_IMPLICIT_GEMM_GATHER && variant != CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     return fail(CONVF_ERR_INVALID_ARG, "variant %d has no bf16 GEMM packing", variant);
   if (desc->group != 1) return fail(CONVF_ERR_UNSUPPORTED, "GEMM packing needs group == 1");
   int am, cb, kt, cp;
@@ -682,6 +758,15 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
     o_pad = carve((size_t)s.N * s.H * h->wg.Wp * h->wg.cpt * sizeof(uint16_t));
+  } else if (variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
+    halo_geom(s, h->num_sms, desc->tile_n, &h->hg);
+    int cpad = 0;
+    tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot, &cpad);
+    wpack.resize((size_t)s.K * h->ktot);
+    pack_bf16(static_cast<const uint16_t*>(W), s, cpad, h->ktot, wpack.data());
+    o_w = carve(wpack.size() * sizeof(uint16_t));
+    o_scale = carve((size_t)Kpad * sizeof(float));
+    o_bias = carve((size_t)Kpad * sizeof(float));
   } else if (variant == CONVF_VARIANT_INT8) {
     o_w = carve((size_t)s.K * s.R * s.S * s.C);
     o_qb = carve((size_t)s.K * 4);
@@ -763,6 +848,32 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     return fail(CONVF_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(ce));
   }
 
+  if (variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
+    const HaloGeom& g = h->hg;
+    h->bn = g.bn;
+    h->num_kb = h->ktot / 64;
+    h->n_blocks = (s.K + g.bn - 1) / g.bn;
+    h->num_tiles = (int)((long long)s.N * g.tiles_per_img * h->n_blocks);
+    h->grid = (int)std::min<long long>(h->num_tiles, h->num_sms);
+    CUresult r = load_encoders() ? CUDA_SUCCESS : CUDA_ERROR_NOT_SUPPORTED;
+    if (r == CUDA_SUCCESS) {
+      // {channels of one tap, output channel, tap}: a box brings tpo consecutive taps, each a
+      // BN x 64 K-major tile
+      const int cpad = g.cblocks * 64;
+      const cuuint64_t dims[3] = {(cuuint64_t)cpad, (cuuint64_t)s.K, (cuuint64_t)(s.R * s.S)};
+      const cuuint64_t strides[2] = {(cuuint64_t)h->ktot * 2, (cuuint64_t)cpad * 2};
+      const cuuint32_t box[3] = {64, (cuuint32_t)g.bn, (cuuint32_t)g.tpo};
+      const cuuint32_t es[3] = {1, 1, 1};
+      r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->w_bf16, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) {
+      cudaFree(h->dev);
+      delete h;
+      return fail(CONVF_ERR_CUDA, "halo weight tensor map encoding failed (CUresult %d)", (int)r);
+    }
+  }
   if (variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW) {
     const WinGeom& g = h->wg;
     h->bn = g.bnp;
@@ -926,6 +1037,31 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       ce = launch_depthwise(p, &h->tmA, h->num_sms, strm);
       break;
     }
+    case CONVF_VARIANT_IMPLICIT_GEMM_HALO: {
+      const HaloGeom& g = h->hg;
+      if (x != h->map_x) {
+        // {C, W, H, N}, box = 64 channels x the padded row width x (TR + R - 1) rows of one image
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2,
+                                       (cuuint64_t)s.H * s.W * s.C * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)g.Wp, (cuuint32_t)(g.TR + s.R - 1), 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        CUresult r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "halo activation tensor map encoding failed (CUresult %d)", (int)r);
+        h->map_x = x;
+      }
+      HaloParams p{};
+      p.Ho = s.Ho; p.Wo = s.Wo; p.Wp = g.Wp; p.TR = g.TR; p.R = s.R; p.S = s.S; p.pt = s.pt; p.pl = s.pl;
+      p.cblocks = g.cblocks; p.cpad = g.cblocks * 64; p.Kout = s.K; p.n_blocks = h->n_blocks;
+      p.tiles_per_img = g.tiles_per_img; p.num_tiles = h->num_tiles; p.patch_bytes = g.patch_bytes;
+      p.tpo = g.tpo; p.b_stages = g.b_stages;
+      p.scale = h->scale; p.bias = h->bias; p.y = static_cast<float*>(y); p.lo = h->lo; p.hi = h->hi;
+      p.status = h->status;
+      ce = launch_tc_halo(p, h->tmA, h->tmB, g.bn, h->grid, strm);
+      break;
+    }
     case CONVF_VARIANT_IMPLICIT_GEMM_WINDOW: {
       const WinGeom& g = h->wg;
       ce = launch_window_pad(static_cast<const uint16_t*>(x), h->xpad, s.N, s.H, s.W, s.C, g.cpt, g.Wp, s.pl,
@@ -1021,9 +1157,15 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (st != CONVF_OK) return st;
   if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
   static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
-                                "implicit_gemm_gather", "implicit_gemm_window"};
+                                "implicit_gemm_gather", "implicit_gemm_window", "implicit_gemm_halo"};
   const Shape& s = h->s;
-  if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
+  if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    snprintf(buf, len,
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d padded_row=%d tile_rows=%d "
+             "taps_per_load=%d weight_stages=%d kblocks=%d tiles=%d grid=%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->hg.bn, h->hg.Wp, h->hg.TR, h->hg.tpo,
+             h->hg.b_stages, h->num_kb, h->num_tiles, h->grid, h->dev_bytes);
+  else if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d window=%d row_mode=%d tap_channels=%d "
              "padded_row=%d stages=%d tiles=%d grid=%d weight_bytes=%zu",

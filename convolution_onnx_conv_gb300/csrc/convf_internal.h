@@ -78,6 +78,35 @@ struct TcConvParams {
 
 
 
+// ---------------------------------------------------------------- halo-tile implicit GEMM
+// Stride-1, dilation-1 convolutions: the output is indexed in rows of Wp = W + pl + pr
+// positions (Wp - Wo of them junk), so that every filter tap (r, s) reads the zero-padded
+// input at a fixed offset r*Wp + s from the output position.  A tile is TR output rows of one
+// image (TR*Wp <= 128 MMA rows); its activation operand for one 64-channel block is ONE TMA box
+// of TR + R - 1 padded input rows, loaded once and read by all R*S taps through shifted
+// shared-memory descriptors.  Weights stream per (tap, channel block) as in the im2col kernel.
+struct HaloParams {
+  int Ho, Wo, Wp, TR, R, S, pt, pl;
+  int cblocks;            // 64-channel blocks
+  int cpad;               // channels per tap in the packed weights (cblocks * 64)
+  int Kout, n_blocks, tiles_per_img, num_tiles;
+  uint32_t patch_bytes;   // one activation box
+  int tpo;                // taps per weight load (divides R*S)
+  int b_stages;           // weight stages (2..8) of tpo * BN x 64 bf16
+  const float* scale;     // [Kpad]
+  const float* bias;      // [Kpad]
+  float* y;               // NHWC fp32 [N*Ho*Wo][Kout]
+  float lo, hi;
+  int* status;
+};
+// BN in {64, 128, 256}; tmA: 4-D tiled {C, W, H, N} box {64, Wp, TR + R - 1, 1} (128 B swizzle),
+// tmB: 3-D view {cpad, K, R*S taps} of the packed weights [K][R*S*cpad], box {64, BN, tpo}
+// (128 B swizzle)
+cudaError_t launch_tc_halo(const HaloParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int bn, int grid,
+                           cudaStream_t stream);
+// dynamic shared memory of the halo kernel besides its weight stages (total <= 232448)
+size_t tc_halo_fixed_smem(int R, int S, int Wp, uint32_t patch_bytes);
+
 // ---------------------------------------------------------------- window-mode implicit GEMM
 // Small-C convolutions (C <= 8) whose filter row, for one output pixel, is one contiguous run
 // of E bf16 in a channel- and column-padded copy of the input ([N][H][Wp][cpt], the first pl

@@ -266,6 +266,10 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+      // descriptors built once; stages move them by whole 16-byte units (the issuing thread's
+      // per-MMA work is what bounds short MMAs)
+      const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(sA));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(sB));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -279,15 +283,16 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         for (int kb = ka; kb < kend; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto teardown;
           tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * kATileBytes));
-          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * Cfg::kBTileBytes));
+          const uint64_t adesc = adesc0 + ((stage * kATileBytes) >> 4);
+          const uint64_t bdesc = bdesc0 + ((stage * Cfg::kBTileBytes) >> 4);
+          const uint32_t first = kb != ka;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
             if (PAIR)
-              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb != ka) || k != 0);
+              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
             else
-              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb != ka) || k != 0);
+              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
           }
           if (PAIR)
             tc_commit_pair(&empty[stage], 3);

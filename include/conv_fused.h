@@ -83,7 +83,7 @@ typedef enum {
   CONVF_VARIANT_INT8 = 4,            /* int8 tensor-core MMA, int32 accumulate, requant */
   CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 5, /* tcgen05 implicit GEMM, activation rows gathered by
                                             threads (any C, e.g. the 3-channel stem) */
-  CONVF_VARIANT_IMPLICIT_GEMM_WINDOW = 6  /* tcgen05 implicit GEMM for C <= 8: a pre-pass pads the
+  CONVF_VARIANT_IMPLICIT_GEMM_WINDOW = 6, /* tcgen05 implicit GEMM for C <= 8: a pre-pass pads the
                                             channels to 4 or 8 and the columns by the left pad,
                                             after which one filter row of one output pixel is a
                                             contiguous run and one TMA load (overlapping
@@ -92,6 +92,14 @@ typedef enum {
                                             1, sw*cpt*2 a multiple of 16 bytes, S*cpt <= 64,
                                             R*round_up(S*cpt,16) <= 256, K <= 256.  The selector
                                             takes it for outputs at least 32 pixels wide. */
+  CONVF_VARIANT_IMPLICIT_GEMM_HALO = 7    /* tcgen05 implicit GEMM for stride-1, dilation-1
+                                            filters: output rows padded to the input width
+                                            Wp = W + pl + pr <= 128, tiles of floor(128/Wp)
+                                            output rows; per 64-channel block one TMA box of
+                                            padded input rows serves every filter tap through
+                                            shifted shared-memory descriptors (im2col reloads
+                                            it once per tap).  The selector takes it when at
+                                            least 60% of a tile's 128 rows are real outputs. */
 } convf_variant;
 
 typedef struct {

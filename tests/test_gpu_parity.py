@@ -36,7 +36,7 @@ def _assert(res, spec, variant=None):
 
 def test_single_conv_bias_relu():
     spec = workloads.single_conv_relu()
-    _assert(check_full(spec, synthetic.seed_for(1, 0)), spec, V.CONVF_VARIANT_IMPLICIT_GEMM)
+    _assert(check_full(spec, synthetic.seed_for(1, 0)), spec, V.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
 
 
 # ------------------------------------------------------------------ small shapes, all outputs
@@ -97,7 +97,7 @@ SMALL = [
 
 @pytest.mark.parametrize("spec,variant", SMALL, ids=[s.name for s, _ in SMALL])
 def test_small_shapes_full(spec, variant):
-    _assert(check_full(spec, 7000 + SMALL.index((spec, variant))), spec, variant)
+    _assert(check_full(spec, 7000 + SMALL.index((spec, variant)), variant), spec, variant)
 
 
 WINDOW = [
@@ -151,8 +151,45 @@ def test_every_tile_width(tile_n, cta_pair, shape):
     from parity import compare
     c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
                      *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
-                     pads=spec.pads, act=spec.act, tile_n=tile_n, cta_pair=cta_pair)
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, cta_pair=cta_pair,
+                     variant=V.CONVF_VARIANT_GEMM_1X1 if shape == "1x1" else V.CONVF_VARIANT_IMPLICIT_GEMM)
     assert f"tile={256 if cta_pair == 2 else 128}x{tile_n} cta_pair={cta_pair - 1}" in c.describe()
+    y = c(to_device_nhwc(inp["x"]))
+    torch.cuda.synchronize()
+    assert c.status() == cf.CONVF_OK
+    ok, worst, idx = compare(y.cpu().contiguous().numpy(), oracle_full(spec, inp), False)
+    c.close()
+    assert ok, (worst, idx)
+
+
+HALO = [
+    # rows of W + pl + pr positions; one padded-input box per 64-channel block serves every tap
+    S("halo_3x3_w56", 2, 64, 8, 56, 64, 3, 3, pads=(1, 1, 1, 1)),
+    S("halo_3x3_c128_w28_k200", 2, 128, 28, 28, 200, 3, 3, pads=(1, 1, 1, 1), bias=True),
+    S("halo_3x3_c256_w14", 3, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1), act=ACT_RELU6),
+    S("halo_5x3_asym_pads", 2, 64, 12, 30, 64, 5, 3, pads=(2, 0, 1, 3), bias=True),
+    S("halo_c8_3x3", 2, 8, 17, 20, 32, 3, 3, pads=(1, 1, 1, 1), act=ACT_NONE),
+    S("halo_c72_ragged_blocks_k40", 2, 72, 9, 13, 40, 3, 3, pads=(1, 1, 1, 1), bias=True),
+    S("halo_short_images", 4, 64, 5, 10, 64, 3, 3, pads=(1, 1, 1, 1)),
+    S("halo_nopad_2x2", 2, 64, 9, 11, 64, 2, 2),
+]
+
+
+@pytest.mark.parametrize("spec", HALO, ids=lambda s: s.name)
+def test_halo_variant_full(spec):
+    _assert(check_full(spec, 7700 + HALO.index(spec), V.CONVF_VARIANT_IMPLICIT_GEMM_HALO), spec,
+            V.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_halo_every_tile_width(tile_n):
+    spec = S(f"halo_tiles{tile_n}", 2, 128, 14, 14, 200, 3, 3, pads=(1, 1, 1, 1), bias=True)
+    inp = inputs_for(spec, 7750)
+    from parity import compare
+    c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                     *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, variant=V.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    assert f"tile=128x{tile_n}" in c.describe(), c.describe()
     y = c(to_device_nhwc(inp["x"]))
     torch.cuda.synchronize()
     assert c.status() == cf.CONVF_OK
@@ -183,7 +220,8 @@ def test_stream_k_every_output(spec, tile_n):
     from parity import compare
     c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
                      *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
-                     pads=spec.pads, act=spec.act, tile_n=tile_n, stream_k=2)
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, stream_k=2,
+                     variant=V.CONVF_VARIANT_GEMM_1X1 if spec.R == 1 else V.CONVF_VARIANT_IMPLICIT_GEMM)
     assert "stream_k=1" in c.describe(), c.describe()
     x = to_device_nhwc(inp["x"])
     ref = oracle_full(spec, inp)
@@ -203,7 +241,7 @@ def test_stream_k_off_matches_on():
     for sk in (1, 2):
         c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
                          *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
-                         pads=spec.pads, act=spec.act, stream_k=sk)
+                         pads=spec.pads, act=spec.act, stream_k=sk, variant=V.CONVF_VARIANT_IMPLICIT_GEMM)
         assert f"stream_k={sk - 1}" in c.describe()
         outs.append(c(to_device_nhwc(inp["x"])).cpu())
         c.close()

@@ -143,8 +143,9 @@ def test_bn_scale_shift_matches_formula():
 
 
 def test_tile_choice_and_overrides():
-    # 3x3 128->128 at 28x28, batch 32: 128-wide single-CTA tiles (the measured best)
-    d = cf.make_desc(32, 128, 28, 28, 128, 3, 3, (1, 1), (1, 1, 1, 1))
+    # 3x3 128->128 at 28x28, batch 32, through TMA im2col: 128-wide single-CTA tiles (the
+    # measured best)
+    d = cf.make_desc(32, 128, 28, 28, 128, 3, 3, (1, 1), (1, 1, 1, 1), variant=cf.CONVF_VARIANT_IMPLICIT_GEMM)
     v, bn, kt, pair = cf.conv_fused_plan(d, with_pair=True)
     assert (v, bn, kt, pair) == (cf.CONVF_VARIANT_IMPLICIT_GEMM, 128, 1152, 0)
     d.cta_pair = 2
@@ -172,7 +173,12 @@ def test_selector_on_the_workloads():
             assert bn == -(-spec.K // 32) * 32
         elif spec.R == 1 and spec.stride == (1, 1):
             assert v == cf.CONVF_VARIANT_GEMM_1X1 and kt == -(-spec.C // 64) * 64
+        elif spec.stride == (1, 1) and spec.W >= 14:
+            # stride-1 3x3 with rows of W + 2 <= 128: at least 60% of each tile's rows are outputs
+            assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO and kt == spec.R * spec.S * (-(-spec.C // 64) * 64)
+            assert bn in (64, 128, 256)
         else:
+            # strided, or 7x7 images (7 rows of 9: 38% of a tile would be outputs)
             assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM and kt == spec.R * spec.S * (-(-spec.C // 64) * 64)
     assert len(names) == 53 + 50 + 7
 
@@ -260,7 +266,7 @@ def test_window_variant_is_automatic_only_for_wide_outputs():
 
 def test_stream_k_mode_is_validated():
     """stream_k takes 0 (auto: whole tiles), 1 (off) or 2 (on); anything else is refused."""
-    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_16_s1b1_3x3@b32"]
+    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_12_s1b0_3x3@b32"]   # strided: im2col
     for sk in (0, 1, 2):
         d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
                          stream_k=sk)
@@ -271,3 +277,24 @@ def test_stream_k_mode_is_validated():
         with pytest.raises(cf.ConvFusedError) as e:
             cf.conv_fused_plan(d)
         assert e.value.status == cf.CONVF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("W,pads,R,S,ok", [
+    (56, (1, 1, 1, 1), 3, 3, None),          # rows of 58: 2 output rows per tile
+    (14, (1, 1, 1, 1), 3, 3, None),          # rows of 16: 8 output rows per tile
+    (30, (2, 0, 1, 3), 5, 3, None),          # asymmetric pads: rows of 33
+    (127, (1, 1, 1, 1), 3, 3, "W + pl + pr <= 128"),
+    (20, (1, 1, 1, 1), 1, 1, "more than one tap"),
+])
+def test_halo_variant_rules(W, pads, R, S, ok):
+    d = cf.make_desc(2, 64, 12, W, 64, R, S, (1, 1), pads, variant=cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    if ok is None:
+        v, bn, kt = cf.conv_fused_plan(d)
+        assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO and kt == R * S * 64 and bn == 64
+    else:
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_plan(d)
+        assert ok in str(e.value)
+    strided = cf.make_desc(2, 64, 12, 20, 64, 3, 3, (2, 2), (1, 1, 1, 1), variant=cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    with pytest.raises(cf.ConvFusedError):
+        cf.conv_fused_plan(strided)
