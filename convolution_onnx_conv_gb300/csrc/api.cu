@@ -219,6 +219,7 @@ void pack_window(const uint16_t* W, const Shape& s, const WinGeom& g, uint16_t* 
 // ------------------------------------------------------------------ halo-tile geometry
 struct HaloGeom {
   int Wp, TR, tiles_per_img, cblocks, bn, tpo, b_stages;
+  bool resident;    // the whole weight set (one output-channel block) stays in the stages
   uint32_t patch_bytes;
   double valid;     // fraction of the 128 MMA rows of a tile that are real outputs
 };
@@ -253,8 +254,9 @@ std::string halo_geom(const Shape& s, int num_sms, int forced_bn, HaloGeom* g) {
     const size_t fixed = tc_halo_fixed_smem(s.R, s.S, g->Wp, g->patch_bytes);
     if (fixed + 2 * stage > 232448) continue;
     const int stages = (int)std::min<size_t>(8, (232448 - fixed) / stage);
-    const double ingest = g->cblocks * (g->patch_bytes + (double)s.R * s.S * bn * 128.0) / 60.0;
-    const double issue = g->cblocks * (double)(s.R * s.S / tpo) * 600.0;
+    const bool res = (s.K + bn - 1) / bn == 1 && g->cblocks * (s.R * s.S / tpo) <= stages;
+    const double ingest = g->cblocks * (g->patch_bytes + (res ? 0.0 : (double)s.R * s.S * bn * 128.0)) / 20.0;
+    const double issue = res ? 0.0 : g->cblocks * (double)(s.R * s.S / tpo) * 600.0;
     const double mma = (double)g->cblocks * s.R * s.S * 4 * (bn == 64 ? 48.0 : bn == 128 ? 64.0 : 128.0);
     const long long tiles = (long long)s.N * g->tiles_per_img * ((s.K + bn - 1) / bn);
     const long long waves = (tiles + num_sms - 1) / num_sms;
@@ -267,6 +269,7 @@ std::string halo_geom(const Shape& s, int num_sms, int forced_bn, HaloGeom* g) {
     }
   }
   if (!g->bn) return "halo tiles: the patch and weight stages exceed shared memory";
+  g->resident = (s.K + g->bn - 1) / g->bn == 1 && g->cblocks * (s.R * s.S / g->tpo) <= g->b_stages;
   return "";
 }
 
@@ -359,6 +362,9 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
       HaloGeom g;
       halo_geom(s, 148, d->tile_n, &g);
       if (g.valid < 0.6) why = "halo tiles are chosen automatically only when 60% of a tile's rows are outputs";
+      // measured: without resident weights the per-tile weight stream makes halo tiles no faster
+      // than TMA im2col
+      else if (!g.resident) why = "halo tiles are chosen automatically only when the weights stay resident";
       if (d->cta_pair == 2 || d->stream_k == 2) why = "halo tiles run on single CTAs without stream-K";
     }
     if (why.empty()) {
@@ -1056,7 +1062,7 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.Ho = s.Ho; p.Wo = s.Wo; p.Wp = g.Wp; p.TR = g.TR; p.R = s.R; p.S = s.S; p.pt = s.pt; p.pl = s.pl;
       p.cblocks = g.cblocks; p.cpad = g.cblocks * 64; p.Kout = s.K; p.n_blocks = h->n_blocks;
       p.tiles_per_img = g.tiles_per_img; p.num_tiles = h->num_tiles; p.patch_bytes = g.patch_bytes;
-      p.tpo = g.tpo; p.b_stages = g.b_stages;
+      p.tpo = g.tpo; p.b_stages = g.b_stages; p.resident = g.resident ? 1 : 0;
       p.scale = h->scale; p.bias = h->bias; p.y = static_cast<float*>(y); p.lo = h->lo; p.hi = h->hi;
       p.status = h->status;
       ce = launch_tc_halo(p, h->tmA, h->tmB, g.bn, h->grid, strm);
@@ -1162,9 +1168,9 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d padded_row=%d tile_rows=%d "
-             "taps_per_load=%d weight_stages=%d kblocks=%d tiles=%d grid=%d weight_bytes=%zu",
+             "taps_per_load=%d weight_stages=%d resident=%d kblocks=%d tiles=%d grid=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->hg.bn, h->hg.Wp, h->hg.TR, h->hg.tpo,
-             h->hg.b_stages, h->num_kb, h->num_tiles, h->grid, h->dev_bytes);
+             h->hg.b_stages, h->hg.resident ? 1 : 0, h->num_kb, h->num_tiles, h->grid, h->dev_bytes);
   else if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW)
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d window=%d row_mode=%d tap_channels=%d "

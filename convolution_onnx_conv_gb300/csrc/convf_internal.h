@@ -93,6 +93,7 @@ struct HaloParams {
   uint32_t patch_bytes;   // one activation box
   int tpo;                // taps per weight load (divides R*S)
   int b_stages;           // weight stages (2..8) of tpo * BN x 64 bf16
+  int resident;           // 1: one output-channel block whose weights fit the stages: loaded once
   const float* scale;     // [Kpad]
   const float* bias;      // [Kpad]
   float* y;               // NHWC fp32 [N*Ho*Wo][Kout]

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       if (seg % G != eg) continue;
       const int acc = seg & 1;                         // accumulator buffer of segment seg
       const uint32_t acc_phase = (seg >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       // 0 whole tile, 1 owner, 2 contributor (always 0 without stream-K)
       const int mode = !SK ? 0 : (ka > 0 ? 2 : (kend < p.num_kb ? 1 : 0));

@@ -146,11 +146,20 @@ __global__ void __launch_bounds__(kHThreads, 1)
             }
           }
           for (int gi = 0; gi < ngroups; ++gi, ++bi) {
+            const int g = gi + rot_g < ngroups ? gi + rot_g : gi + rot_g - ngroups;
+            if (p.resident) {
+              // the whole weight set stays in stage cb * ngroups + g: load it with the first tile
+              if (tile == static_cast<int>(blockIdx.x) && (bi & 1) == me) {
+                const int st = cb * ngroups + g;
+                mbar_arrive_expect_tx(&bfull[st], bstage);
+                tma_load_3d(sB + st * bstage, &tmB, &bfull[st], cb * kHBK, n0, g * p.tpo);
+              }
+              continue;
+            }
             if ((bi & 1) == me) {
-              const int t0 = (gi + rot_g < ngroups ? gi + rot_g : gi + rot_g - ngroups) * p.tpo;
               if (!mbar_wait(&bempty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
               mbar_arrive_expect_tx(&bfull[stage], bstage);
-              tma_load_3d(sB + stage * bstage, &tmB, &bfull[stage], cb * kHBK, n0, t0);
+              tma_load_3d(sB + stage * bstage, &tmB, &bfull[stage], cb * kHBK, n0, g * p.tpo);
             }
             if (++stage == kStages) {
               stage = 0;
@@ -180,11 +189,15 @@ __global__ void __launch_bounds__(kHThreads, 1)
           // descriptors are built once; taps and stages move them by whole 16-byte units (the
           // issuing thread's per-MMA work is what bounds short MMAs)
           const uint64_t apatch = adesc0 + ((slot * pstride) >> 4);
+          const int cb = cbi + rot_c < p.cblocks ? cbi + rot_c : cbi + rot_c - p.cblocks;
           for (int gi = 0; gi < ngroups; ++gi) {
-            const int t0 = (gi + rot_g < ngroups ? gi + rot_g : gi + rot_g - ngroups) * p.tpo;
-            if (!mbar_wait(&bfull[stage], phase, abort_flag, p.status)) goto teardown;
+            const int g = gi + rot_g < ngroups ? gi + rot_g : gi + rot_g - ngroups;
+            const int t0 = g * p.tpo;
+            // resident weights: stage cb * ngroups + g, landed once (phase 0) and never released
+            const int bs = p.resident ? cb * ngroups + g : stage;
+            if (!mbar_wait(&bfull[bs], p.resident ? 0u : phase, abort_flag, p.status)) goto teardown;
             tc_fence_after();
-            const uint64_t bst = bdesc0 + ((stage * bstage) >> 4);
+            const uint64_t bst = bdesc0 + ((bs * bstage) >> 4);
             for (int j = 0; j < p.tpo; ++j) {
               // tap t0 + j: the patch read r*Wp + s rows further on; its weights are tile j
               const uint64_t adesc = apatch + toff[t0 + j];
@@ -193,10 +206,12 @@ __global__ void __launch_bounds__(kHThreads, 1)
 #pragma unroll
               for (int k = 1; k < kHBK / 16; ++k) tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, 1u);
             }
-            tc_commit(&bempty[stage]);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
+            if (!p.resident) {
+              tc_commit(&bempty[stage]);
+              if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
           }
           tc_commit(&aempty[slot]);
@@ -219,7 +234,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
     const int c4 = lane & 7;
     int n_it = 0;
     for (int tile = blockIdx.x + eg * gridDim.x; tile < p.num_tiles; tile += 2 * gridDim.x, ++n_it) {
-      if (!mbar_wait(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
+      if (!mbar_wait_warp(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int n0 = (tile % p.n_blocks) * BN;
       const int rt = tile / p.n_blocks;

@@ -36,7 +36,7 @@ def _assert(res, spec, variant=None):
 
 def test_single_conv_bias_relu():
     spec = workloads.single_conv_relu()
-    _assert(check_full(spec, synthetic.seed_for(1, 0)), spec, V.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    _assert(check_full(spec, synthetic.seed_for(1, 0)), spec)
 
 
 # ------------------------------------------------------------------ small shapes, all outputs

@@ -173,12 +173,14 @@ def test_selector_on_the_workloads():
             assert bn == -(-spec.K // 32) * 32
         elif spec.R == 1 and spec.stride == (1, 1):
             assert v == cf.CONVF_VARIANT_GEMM_1X1 and kt == -(-spec.C // 64) * 64
-        elif spec.stride == (1, 1) and spec.W >= 14:
-            # stride-1 3x3 with rows of W + 2 <= 128: at least 60% of each tile's rows are outputs
+        elif spec.stride == (1, 1) and spec.W == 56:
+            # stride-1 3x3 on rows of 58 (2 output rows per tile) whose 64 x 576 weights stay
+            # resident in shared memory
             assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO and kt == spec.R * spec.S * (-(-spec.C // 64) * 64)
-            assert bn in (64, 128, 256)
+            assert bn == 64
         else:
-            # strided, or 7x7 images (7 rows of 9: 38% of a tile would be outputs)
+            # strided; weights too large to stay resident; or 7x7 images (7 rows of 9: 38% of a
+            # tile would be outputs)
             assert v == cf.CONVF_VARIANT_IMPLICIT_GEMM and kt == spec.R * spec.S * (-(-spec.C // 64) * 64)
     assert len(names) == 53 + 50 + 7
 
