@@ -334,13 +334,14 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     const int sub = lane >> 3;             // row within each group of four in the store phase
     const int c4 = lane & 7;               // 4-channel column group
     const long long total_it = static_cast<long long>(p.num_tiles) * p.num_kb;
-    SegSched<SK> sched(p, tstart, tstep);
+    // whole tiles: group eg visits only its own tiles; stream-K: every segment, keeping its own
+    SegSched<SK> sched(p, tstart + (SK ? 0 : eg * tstep), SK ? tstep : G * tstep);
     int tile, ka, kend;
-    for (int seg = 0; sched.next(tile, ka, kend); ++seg) {
-      if (seg % G != eg) continue;
+    for (int seg = SK ? 0 : eg; sched.next(tile, ka, kend); seg += SK ? 1 : G) {
+      if (SK && seg % G != eg) continue;
       const int acc = seg & 1;                         // accumulator buffer of segment seg
       const uint32_t acc_phase = (seg >> 1) & 1;
-      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       // 0 whole tile, 1 owner, 2 contributor (always 0 without stream-K)
       const int mode = !SK ? 0 : (ka > 0 ? 2 : (kend < p.num_kb ? 1 : 0));

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
     const int c4 = lane & 7;
     int n_it = 0;
     for (int tile = blockIdx.x + eg * gridDim.x; tile < p.num_tiles; tile += 2 * gridDim.x, ++n_it) {
-      if (!mbar_wait_warp(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
+      if (!mbar_wait(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int n0 = (tile % p.n_blocks) * BN;
       const int rt = tile / p.n_blocks;

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kWinThreads, 1)
     const int nchunks = p.bnp / kWinEpiCols;
     int n_it = 0;
     for (int tile = blockIdx.x + eg * tstep; tile < p.num_tiles; tile += 2 * tstep, ++n_it) {
-      if (!mbar_wait_warp(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
+      if (!mbar_wait(&tfull[eg], n_it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int owb = tile % p.ow_blocks;
       const int orow = tile / p.ow_blocks;   // n * Ho + oh
