@@ -149,6 +149,8 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "cta_pair=%d is not 0 (auto), 1 (single CTA) or 2 (CTA pair)", d->cta_pair);
   if (d->stream_k < 0 || d->stream_k > 2)
     return fail(CONVF_ERR_INVALID_ARG, "stream_k=%d is not 0 (auto), 1 (off) or 2 (on)", d->stream_k);
+  if (d->kblocks_per_step < 0 || d->kblocks_per_step > 4)
+    return fail(CONVF_ERR_INVALID_ARG, "kblocks_per_step=%d is not 0 (auto) or 1..4", d->kblocks_per_step);
   return CONVF_OK;
 }
 
@@ -388,6 +390,15 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
 // run at the epilogue's store rate, about 13 B/cycle per SM, and sit on the critical path), so
 // auto keeps whole tiles: sk_mode 0 = auto (off), 1 = off, 2 = on (single CTAs only; ignored
 // with pairs or when sk_ok is false).
+// k-blocks per pipeline step of the TMA implicit-GEMM kernel: the first of 4, 2, 3 that divides
+// the stage count and the tile's k-blocks and still leaves two steps in flight (measured on the
+// ResNet-50 layers: 4 beats 2 on 128 x 64 tiles, 2 matches or beats 3 on 128 x 128 tiles).
+int auto_kblocks_per_step(int stages, int num_kb) {
+  for (int k : {4, 2, 3})
+    if (stages % k == 0 && num_kb % k == 0 && stages / k >= 2) return k;
+  return 1;
+}
+
 void pick_tile(long long M, int K, int num_kb, int num_sms, int max_bn, int pair_mode, int sk_mode, bool sk_ok,
                int* bn_out, bool* pair_out, bool* sk_out) {
   const bool pair = pair_mode == 2;
@@ -498,6 +509,8 @@ struct convf_handle {
   int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
   bool pair;        // CTA-pair (cta_group::2) 256-row tiles
   bool sk;          // stream-K work split
+  int kpb;          // k-blocks per pipeline step (TcConvParams::kpb)
+  bool a3d;         // 1x1 activation map is 3-D {64, M, C/64} (one box per step)
   float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
   int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
   WinGeom wg;       // window variant geometry
@@ -796,6 +809,23 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     pick_tile(s.M, s.K, h->ktot / 64, h->num_sms, desc->tile_n ? desc->tile_n : max_bn, gather ? 1 : desc->cta_pair,
               desc->stream_k, !gather, &h->bn, &h->pair, &h->sk);
     if (desc->tile_n) h->bn = desc->tile_n;
+    h->kpb = 1;
+    if (!gather && !h->pair && !h->sk) {
+      const int st = tc_conv_stages(h->bn, false, false);
+      const int nkb = h->ktot / 64;
+      if (desc->kblocks_per_step) {
+        if (st % desc->kblocks_per_step || nkb % desc->kblocks_per_step) {
+          delete h;
+          return fail(CONVF_ERR_UNSUPPORTED,
+                      "kblocks_per_step=%d must divide both the %d reduction blocks and the %d pipeline stages of "
+                      "%d-wide tiles", desc->kblocks_per_step, nkb, st, h->bn);
+        }
+        h->kpb = desc->kblocks_per_step;
+      } else {
+        h->kpb = auto_kblocks_per_step(st, nkb);
+      }
+    }
+    h->a3d = h->a_mode == kA2D && !gather && !h->pair && h->kpb > 1 && s.C % 64 == 0;
     if (h->sk) {
       o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
       o_skflags = carve((size_t)h->num_sms * sizeof(int));
@@ -943,13 +973,26 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     h->num_tiles = (int)tiles;
     h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2)
                       : (int)std::min<long long>(h->sk ? tiles * h->num_kb : tiles, h->num_sms);
-    const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
-    const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn)};
-    const cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w_bf16, dims, strides, box, es,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER || h->pair || h->kpb == 1) {
+      const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
+      const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
+      const cuuint32_t box[2] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn)};
+      const cuuint32_t es[2] = {1, 1};
+      r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w_bf16, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      // {64 elements of a k-block, output channel, k-block}: one box = kpb consecutive bn x 64
+      // K-major tiles
+      const cuuint64_t dims[3] = {64, (cuuint64_t)s.K, (cuuint64_t)(h->ktot / 64)};
+      const cuuint64_t strides[2] = {(cuuint64_t)h->ktot * 2, 128};
+      const cuuint32_t box[3] = {64, (cuuint32_t)h->bn, (cuuint32_t)h->kpb};
+      const cuuint32_t es[3] = {1, 1, 1};
+      r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->w_bf16, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
       cudaFree(h->dev);
       delete h;
@@ -965,7 +1008,17 @@ namespace {
 convf_status encode_a_map(convf_handle* h, const void* x) {
   const Shape& s = h->s;
   CUresult r;
-  if (h->a_mode == kA2D) {
+  if (h->a_mode == kA2D && h->a3d) {
+    // {64 channels of a k-block, output row, k-block}: one box = kpb consecutive 128 x 64 tiles
+    const cuuint64_t dims[3] = {64, (cuuint64_t)s.M, (cuuint64_t)(s.C / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)s.C * 2, 128};
+    const cuuint32_t box[3] = {64, 128, (cuuint32_t)h->kpb};
+    const cuuint32_t es[3] = {1, 1, 1};
+    r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "activation tensor map encoding failed (CUresult %d)", (int)r);
+  } else if (h->a_mode == kA2D) {
     const cuuint64_t dims[2] = {(cuuint64_t)s.C, (cuuint64_t)s.M};
     const cuuint64_t strides[1] = {(cuuint64_t)s.C * 2};
     const cuuint32_t box[2] = {64, 128};
@@ -1114,6 +1167,7 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       }
       p.lo = h->lo; p.hi = h->hi; p.status = h->status; p.y = static_cast<float*>(y);
       p.sk = h->sk ? 1 : 0; p.sk_ws = h->sk_ws; p.sk_flags = h->sk_flags;
+      p.kpb = h->kpb; p.a3d = h->a3d ? 1 : 0;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
         case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
@@ -1184,9 +1238,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
-             "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
+             "kblocks_per_step=%d act_box_per_step=%d tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
-             h->sk ? 1 : 0, h->num_kb, h->num_tiles, h->grid, h->patch_rows, h->cpt, h->dev_bytes);
+             h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0, h->num_tiles, h->grid, h->patch_rows, h->cpt,
+             h->dev_bytes);
   return ok();
 }
 
@@ -1331,6 +1386,7 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
   p.H = s.H; p.W = s.W; p.C = cpt; p.Ho = s.Ho; p.Wo = s.Wo;
   p.n_blocks = n_blocks; p.num_tiles = (int)tiles; p.a_mode = kAGather;
+  p.kpb = 1; p.a3d = 0;
   p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status; p.y = static_cast<float*>(y);
   p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
   switch (bn) {

@@ -74,7 +74,20 @@ struct TcConvParams {
   int sk;                 // 0 = whole tiles per CTA
   float* sk_ws;
   int* sk_flags;
+  // k-blocks per pipeline step (1, 2, 3 or 4; divides num_kb and the stage count): one weight
+  // TMA box of kpb consecutive 64-wide blocks, and one activation box when a3d (2-D mode, C a
+  // multiple of 64: the map is {64, M, C/64}); otherwise kpb activation loads shared by the two
+  // producer warps.  Single CTAs without stream-K only; 1 elsewhere.
+  int kpb;
+  int a3d;
 };
+
+// Pipeline stages (64-wide k-blocks held in shared memory) of the TMA implicit-GEMM kernel per
+// tile width: operand ingest per SM does not grow with depth, so stages give way to the epilogue.
+constexpr int tc_conv_stages(int bn, bool gather, bool pair) {
+  return gather ? (bn <= 64 ? 4 : 3)
+                : (pair ? (bn == 256 ? 5 : (bn == 128 ? 6 : 8)) : (bn == 256 ? 4 : (bn == 128 ? 6 : 8)));
+}
 
 
 

@@ -4,15 +4,17 @@
 // never materialised): rows m = (n, oh, ow), M = N*Ho*Wo; columns = output channels K;
 // reduction over (tap r,s; channel c) in 64-wide blocks.  One CTA per SM loops over 128 x BN
 // output tiles.  Warp roles:
-//   warp 0      activation producer: TMA activation tile (2D tiled load for 1x1/stride-1/pad-0,
-//               else an im2col load whose tap offsets select the filter position; padding is
-//               TMA zero fill); in gather mode the per-tile bulk copies of input rows
+//   warp 0      activation producer: TMA activation tiles (2D/3D tiled loads for
+//               1x1/stride-1/pad-0, else im2col loads whose tap offsets select the filter
+//               position; padding is TMA zero fill); in gather mode the per-tile bulk copies of
+//               input rows
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue into a double-buffered
 //               fp32 accumulator (2 x BN TMEM columns)
-//   warp 2      weight producer: TMA weight tile (2D tiled load)
-//   warps 3-10  epilogue, two warpgroups on alternate 32-column chunks (warps 3-6 only in
-//               gather mode): tcgen05.ld -> y = clamp(scale[k]*acc + bias[k], lo, hi) ->
-//               swizzled smem staging -> TMA store (clips the ragged M and K edges)
+//   warp 2      weight producer: TMA weight boxes of one or several k-blocks (plus half of the
+//               im2col activation loads when a pipeline step holds several k-blocks)
+//   warps 3-10  epilogue, two warpgroups on alternate tiles (warps 3-6 only in gather mode):
+//               tcgen05.ld -> per-warp smem transpose -> y = clamp(scale[k]*acc + bias[k],
+//               lo, hi) -> 16-byte global stores (the ragged M and K edges masked)
 //   warps 7-14  (gather mode only) activation rows gathered by threads, for channel counts
 //               that TMA cannot address (C not a multiple of 8, e.g. a 3-channel stem)
 #pragma once
@@ -37,10 +39,7 @@ struct TcCfg {
   // warps take the register and smem room
   static constexpr int kEpiGroups = GATHER ? 1 : 2;
   static constexpr int kThreads = 96 + 128 * kEpiGroups + (GATHER ? kGatherThreads : 0);
-  // operand ingest per SM does not grow with pipeline depth, so stages give way to the epilogue
-  static constexpr int kStages = GATHER ? (BN <= 64 ? 4 : 3)
-                                        : (PAIR ? (BN == 256 ? 5 : (BN == 128 ? 6 : 8))
-                                                : (BN == 256 ? 4 : (BN == 128 ? 6 : 8)));
+  static constexpr int kStages = tc_conv_stages(BN, GATHER, PAIR);
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
   // gather mode: two buffers for the input rows one tile needs (TcConvParams::patch_rows)
@@ -161,11 +160,74 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   pdl_launch_dependents();
   pdl_wait_prior();
 
+  // One pipeline step moves kpb k-blocks (TcConvParams::kpb) through kpb consecutive stage
+  // slots under the first slot's barriers.  A TMA operation holds its issuing warp for several
+  // hundred cycles and an SM takes a new one only every few hundred cycles, so the bytes per
+  // operation and the number of issuing warps set the operand ingest rate: the weights of a
+  // step are one box, and the activations one box (3-D map) or kpb loads split between the two
+  // producer warps (even k-blocks on warp 0, odd ones on warp 2).
+  const int kpb = (GATHER || PAIR || SK) ? 1 : p.kpb;
+  const bool a3d = !GATHER && !PAIR && p.a3d;
+  const bool a_odd = !GATHER && !a3d && kpb > 1;
+  const uint32_t a_bytes0 = static_cast<uint32_t>((a3d ? kpb : (kpb + 1) / 2) * kATileBytes);
+  const uint32_t b_bytes2 = static_cast<uint32_t>(kpb * Cfg::kBTileBytes + (a_odd ? kpb / 2 : 0) * kATileBytes);
+  // first output pixel's input window origin (im2col mode)
+  auto tile_origin = [&](int m0, int& img, int& hb, int& wb) {
+    if (p.a_mode == kAIm2col) {
+      const int hw = p.Ho * p.Wo;
+      img = m0 / hw;
+      const int rem = m0 - img * hw;
+      const int oh = rem / p.Wo;
+      const int ow = rem - oh * p.Wo;
+      hb = oh * p.sh - p.pt;
+      wb = ow * p.sw - p.pl;
+    }
+  };
+  // filter tap (r, s) and channel block cb of a k-block (im2col mode): computed once per tile,
+  // then stepped one k-block at a time (the issuing thread's scalar work delays its next copy)
+  struct KPos {
+    int r, s, cb;
+  };
+  auto kpos_at = [&](int kb) {
+    KPos q{0, 0, 0};
+    if (p.a_mode == kAIm2col) {
+      const int tap = kb / p.cblocks;
+      q.cb = kb - tap * p.cblocks;
+      q.r = tap / p.S;
+      q.s = tap - q.r * p.S;
+    }
+    return q;
+  };
+  auto kpos_next = [&](KPos& q) {
+    if (++q.cb == p.cblocks) {
+      q.cb = 0;
+      if (++q.s == p.S) {
+        q.s = 0;
+        ++q.r;
+      }
+    }
+  };
+  // activation tile of k-block kb at position q: a 2-D tile, or the im2col column of its filter
+  // tap and channel block (padding is TMA zero fill)
+  auto load_a = [&](int kb, const KPos& q, uint8_t* dA, uint64_t* bar, int m0, int img, int hb, int wb) {
+    if (p.a_mode == kA2D) {
+      if (PAIR)
+        tma_load_2d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), kb * kBK, m0);
+      else
+        tma_load_2d(dA, &tmA, bar, kb * kBK, m0);
+    } else {
+      if (PAIR)
+        tma_load_im2col_4d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), q.cb * kBK, wb, hb, img,
+                                static_cast<uint16_t>(q.s * p.dw), static_cast<uint16_t>(q.r * p.dh));
+      else
+        tma_load_im2col_4d(dA, &tmA, bar, q.cb * kBK, wb, hb, img, static_cast<uint16_t>(q.s * p.dw),
+                           static_cast<uint16_t>(q.r * p.dh));
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------------ activation producer
-    // (TMA activation tiles; in gather mode the per-tile input-row bulk copies instead).  A TMA
-    // operation holds its issuing warp for a few hundred cycles, so activations and weights are
-    // issued from two different warps.
+    // (TMA activation tiles; in gather mode the per-tile input-row bulk copies instead)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -195,42 +257,23 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           continue;
         }
         int img = 0, hb = 0, wb = 0;
-        if (p.a_mode == kAIm2col) {
-          const int hw = p.Ho * p.Wo;
-          img = m0 / hw;
-          const int rem = m0 - img * hw;
-          const int oh = rem / p.Wo;
-          const int ow = rem - oh * p.Wo;
-          hb = oh * p.sh - p.pt;
-          wb = ow * p.sw - p.pl;
-        }
-        int tap = p.cblocks ? ka / p.cblocks : 0, cb = p.cblocks ? ka - (ka / p.cblocks) * p.cblocks : 0;
-        for (int kb = ka; kb < kend; ++kb) {
+        tile_origin(m0, img, hb, wb);
+        KPos q = kpos_at(ka);
+        for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
           // a pair's loads all complete on the leader's barrier, which expects both CTAs' bytes
-          if (!PAIR || leader) mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * kATileBytes : kATileBytes);
-          const uint32_t fbar = PAIR ? map_to_rank(smem_u32(&full[stage]), 0) : 0;
-          uint8_t* dA = sA + stage * kATileBytes;
-          if (p.a_mode == kA2D) {
-            if (PAIR)
-              tma_load_2d_pair(dA, &tmA, fbar, kb * kBK, m0);
-            else
-              tma_load_2d(dA, &tmA, &full[stage], kb * kBK, m0);
+          if (!PAIR || leader)
+            mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * kATileBytes : a_bytes0);
+          if (a3d) {
+            tma_load_3d(sA + stage * kATileBytes, &tmA, &full[stage], 0, m0, kb);
           } else {
-            const int r = tap / p.S;
-            const int s = tap - r * p.S;
-            if (PAIR)
-              tma_load_im2col_4d_pair(dA, &tmA, fbar, cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
-                                      static_cast<uint16_t>(r * p.dh));
-            else
-              tma_load_im2col_4d(dA, &tmA, &full[stage], cb * kBK, wb, hb, img, static_cast<uint16_t>(s * p.dw),
-                                 static_cast<uint16_t>(r * p.dh));
-            if (++cb == p.cblocks) {
-              cb = 0;
-              ++tap;
+            for (int j = 0; j < kpb; ++j) {
+              if (!(j & 1)) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+              kpos_next(q);
             }
           }
-          if (++stage == kStages) {
+          stage += kpb;
+          if (stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -239,6 +282,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ weight producer
+    // (plus the odd-numbered activation loads of a step when the activation is not one box)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -246,16 +290,29 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
         const int n0 = (tile % p.n_blocks) * BN;
-        for (int kb = ka; kb < kend; ++kb) {
+        const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
+        int img = 0, hb = 0, wb = 0;
+        if (a_odd) tile_origin(m0, img, hb, wb);
+        KPos q = kpos_at(a_odd ? ka : 0);
+        for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
           if (!PAIR || leader)
-            mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * Cfg::kBTileBytes : Cfg::kBTileBytes);
+            mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * Cfg::kBTileBytes : b_bytes2);
           if (PAIR)
             tma_load_2d_pair(sB + stage * Cfg::kBTileBytes, &tmB, map_to_rank(smem_u32(&full[stage]), 0), kb * kBK,
                              n0 + static_cast<int>(crank) * (BN / 2));
-          else
+          else if (kpb == 1)
             tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
-          if (++stage == kStages) {
+          else
+            tma_load_3d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], 0, n0, kb);
+          if (a_odd) {
+            for (int j = 0; j < kpb; ++j) {
+              if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+              kpos_next(q);
+            }
+          }
+          stage += kpb;
+          if (stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -280,25 +337,32 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = ka; kb < kend; ++kb) {
+        // one k-block per iteration: wait at the first slot of a step, release the step's
+        // slots after its last k-block
+        // one wait and one release per step; the k-blocks of a step issue back to back (a
+        // per-k-block branch on the step position measured 30% slower on 128 x 64 tiles)
+        for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto teardown;
           tc_fence_after();
-          const uint64_t adesc = adesc0 + ((stage * kATileBytes) >> 4);
-          const uint64_t bdesc = bdesc0 + ((stage * Cfg::kBTileBytes) >> 4);
-          const uint32_t first = kb != ka;
+          for (int j = 0; j < kpb; ++j) {
+            const uint64_t adesc = adesc0 + (((stage + j) * kATileBytes) >> 4);
+            const uint64_t bdesc = bdesc0 + (((stage + j) * Cfg::kBTileBytes) >> 4);
+            const uint32_t first = kb + j != ka;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
-            if (PAIR)
-              tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
-            else
-              tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
+            for (int k = 0; k < kBK / 16; ++k) {
+              // advance 16 bf16 (32 B) along K inside the 128 B swizzle atom
+              if (PAIR)
+                tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
+              else
+                tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
+            }
           }
           if (PAIR)
             tc_commit_pair(&empty[stage], 3);
           else
             tc_commit(&empty[stage]);
-          if (++stage == kStages) {
+          stage += kpb;
+          if (stage == kStages) {
             stage = 0;
             phase ^= 1;
           }

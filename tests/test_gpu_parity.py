@@ -251,6 +251,54 @@ def test_stream_k_off_matches_on():
     assert ok, (worst, idx)
 
 
+KPB_CASES = [
+    # (spec, tile width, k-blocks per pipeline step to run)
+    (S("kpb_1x1_c256_ragged_m", 1, 256, 15, 20, 64, 1, 1), 64, [1, 2, 4]),
+    (S("kpb_1x1_c192_three", 2, 192, 9, 9, 136, 1, 1, act=ACT_RELU), 128, [1, 3]),
+    # C % 64 != 0: no 3-D activation box, the step's loads split between the producer warps
+    (S("kpb_1x1_c96_split_loads", 2, 96, 11, 13, 64, 1, 1), 64, [2]),
+    # 400 tiles over at most 152 CTAs: the stage ring wraps across tiles
+    (S("kpb_1x1_many_tiles_per_cta", 4, 128, 56, 57, 256, 1, 1, act=ACT_RELU6), 64, [1, 2]),
+    (S("kpb_3x3_c64_s2", 2, 64, 15, 15, 96, 3, 3, (2, 2), (1, 1, 1, 1)), 128, [1, 3]),
+    (S("kpb_3x3_c128_k200", 2, 128, 12, 12, 200, 3, 3, pads=(1, 1, 1, 1), bias=True), 128, [2, 3]),
+    (S("kpb_3x3_c256_four", 1, 256, 10, 10, 64, 3, 3, pads=(1, 1, 1, 1)), 64, [2, 4]),
+    (S("kpb_3x3_c128_tile256", 1, 128, 10, 10, 256, 3, 3, pads=(1, 1, 1, 1)), 256, [1, 2]),
+]
+
+
+@pytest.mark.parametrize("case", KPB_CASES, ids=lambda c: c[0].name)
+def test_kblocks_per_step_every_output(case):
+    """Several k-blocks per pipeline step: one weight box (and one activation box for 1x1 with
+    C % 64 == 0) per step, or activation loads shared by the two producer warps."""
+    spec, tile_n, kpbs = case
+    inp = inputs_for(spec, 7700 + KPB_CASES.index(case))
+    from parity import compare
+    ref = oracle_full(spec, inp)
+    x = to_device_nhwc(inp["x"])
+    for kpb in kpbs:
+        c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                         *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                         pads=spec.pads, act=spec.act, tile_n=tile_n, kblocks_per_step=kpb,
+                         variant=V.CONVF_VARIANT_GEMM_1X1 if spec.R == 1 else V.CONVF_VARIANT_IMPLICIT_GEMM)
+        assert f"kblocks_per_step={kpb} " in c.describe(), c.describe()
+        y = c(x)
+        torch.cuda.synchronize()
+        assert c.status() == cf.CONVF_OK
+        ok, worst, idx = compare(y.cpu().contiguous().numpy(), ref, False)
+        assert ok, (spec.name, kpb, worst, idx, c.describe())
+        c.close()
+
+
+def test_kblocks_per_step_must_divide_blocks_and_stages():
+    spec = S("kpb_refused", 1, 192, 8, 8, 64, 1, 1)
+    inp = inputs_for(spec, 7790)
+    for tile_n, kpb in ((64, 3), (128, 4), (64, 2)):   # 8 stages vs 3; 6 stages vs 4; 3 blocks vs 2
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], tile_n=tile_n,
+                         kblocks_per_step=kpb, variant=V.CONVF_VARIANT_GEMM_1X1)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "must divide" in str(e.value)
+
+
 def test_1x1_forced_through_im2col_and_gather():
     spec = S("one_by_one", 2, 64, 10, 10, 64, 1, 1)
     for v in (V.CONVF_VARIANT_GEMM_1X1, V.CONVF_VARIANT_IMPLICIT_GEMM, V.CONVF_VARIANT_IMPLICIT_GEMM_GATHER):

@@ -266,6 +266,21 @@ def test_window_variant_is_automatic_only_for_wide_outputs():
     assert cf.conv_fused_plan(wide)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM_WINDOW
 
 
+def test_kblocks_per_step_is_validated():
+    """kblocks_per_step takes 0 (auto) or 1..4; anything else is refused before any device work."""
+    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_28_s2b1_1x1a@b32"]
+    for k in (0, 1, 2, 4):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         kblocks_per_step=k)
+        assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_GEMM_1X1
+    for k in (-1, 5, 8):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         kblocks_per_step=k)
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_plan(d)
+        assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "kblocks_per_step" in str(e.value)
+
+
 def test_stream_k_mode_is_validated():
     """stream_k takes 0 (auto: whole tiles), 1 (off) or 2 (on); anything else is refused."""
     spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_12_s1b0_3x3@b32"]   # strided: im2col
