@@ -80,6 +80,10 @@ struct TcConvParams {
   // producer warps.  Single CTAs without stream-K only; 1 elsewhere.
   int kpb;
   int a3d;
+  // both epilogue warpgroups drain every tile (one column half each) instead of alternate tiles:
+  // faster when a CTA has few tiles (its last tile's epilogue is the kernel's tail), slower
+  // with many (twice the per-tile epilogue steps); 64+ column tiles without stream-K only
+  int split_epi;
 };
 
 // Pipeline stages (64-wide k-blocks held in shared memory) of the TMA implicit-GEMM kernel per

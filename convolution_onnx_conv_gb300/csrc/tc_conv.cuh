@@ -12,7 +12,8 @@
 //               fp32 accumulator (2 x BN TMEM columns)
 //   warp 2      weight producer: TMA weight boxes of one or several k-blocks (plus half of the
 //               im2col activation loads when a pipeline step holds several k-blocks)
-//   warps 3-10  epilogue, two warpgroups on alternate tiles (warps 3-6 only in gather mode):
+//   warps 3-10  epilogue, two warpgroups on the two column halves of every tile (alternate
+//               tiles for 32-wide tiles and stream-K; warps 3-6 only in gather mode):
 //               tcgen05.ld -> per-warp smem transpose -> y = clamp(scale[k]*acc + bias[k],
 //               lo, hi) -> 16-byte global stores (the ragged M and K edges masked)
 //   warps 7-14  (gather mode only) activation rows gathered by threads, for channel counts
@@ -38,6 +39,8 @@ struct TcCfg {
   // two epilogue warpgroups (alternate 32-column chunks) except in gather mode, whose extra
   // warps take the register and smem room
   static constexpr int kEpiGroups = GATHER ? 1 : 2;
+  // tiles of 64+ columns: both groups can drain every tile, one column half each
+  static constexpr bool kSplitEpiOk = kEpiGroups == 2 && BN >= 64;
   static constexpr int kThreads = 96 + 128 * kEpiGroups + (GATHER ? kGatherThreads : 0);
   static constexpr int kStages = tc_conv_stages(BN, GATHER, PAIR);
   static constexpr int kTmemCols = 2 * BN;
@@ -91,6 +94,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
+  // TcConvParams::split_epi on whole tiles of 64+ columns: both epilogue groups drain every
+  // tile, one column half each (a tile's epilogue takes half as long, which shortens the last
+  // tile of every CTA); otherwise (many tiles per CTA, stream-K segments, 32-column tiles,
+  // gather mode) the groups take alternate tiles
+  const bool split_epi = Cfg::kSplitEpiOk && !SK && p.split_epi;
   // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
   // both CTAs' TMEM; each CTA loads its own 128 activation rows and half of the weight tile.
   const uint32_t crank = PAIR ? cluster_ctarank() : 0;
@@ -131,7 +139,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4);   // one arrival per warp of the draining group
+      // one arrival per warp that drains the buffer (both groups when they split the columns)
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4 * (split_epi ? 2 : 1));
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 1);
     }
@@ -379,8 +388,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
   } else if (warp < 3 + 4 * Cfg::kEpiGroups) {
     // ------------------------------------------------------------------ epilogue
-    // kEpiGroups warpgroups take alternate tiles (with two groups, group g drains accumulator
-    // buffer g).  Each warp owns TMEM lanes 32q..32q+31 = 32 tile rows and works alone:
+    // Two warpgroups split every tile's columns (split_epi), or take alternate tiles.  Each
+    // warp owns TMEM lanes 32q..32q+31 = 32 tile rows and works alone:
     // tcgen05.ld of two 32-column chunks at a time (the buffer is released after the last
     // read) -> its own 4 KB of smem (thread = row) -> read back as thread = (row, 4 channels),
     // scale/bias/clamp, 16-byte stores that cover four whole 128-byte row segments.
@@ -398,10 +407,12 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     const int sub = lane >> 3;             // row within each group of four in the store phase
     const int c4 = lane & 7;               // 4-channel column group
     const long long total_it = static_cast<long long>(p.num_tiles) * p.num_kb;
-    // whole tiles: group eg visits only its own tiles; stream-K: every segment, keeping its own
-    SegSched<SK> sched(p, tstart + (SK ? 0 : eg * tstep), SK ? tstep : G * tstep);
+    // alternate whole tiles: group eg visits only its own tiles; split columns: every tile;
+    // stream-K: every segment, keeping its own
+    const bool kAll = SK || split_epi;
+    SegSched<SK> sched(p, tstart + (kAll ? 0 : eg * tstep), kAll ? tstep : G * tstep);
     int tile, ka, kend;
-    for (int seg = SK ? 0 : eg; sched.next(tile, ka, kend); seg += SK ? 1 : G) {
+    for (int seg = kAll ? 0 : eg; sched.next(tile, ka, kend); seg += kAll ? 1 : G) {
       if (SK && seg % G != eg) continue;
       const int acc = seg & 1;                         // accumulator buffer of segment seg
       const uint32_t acc_phase = (seg >> 1) & 1;
@@ -442,15 +453,26 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       // two 32-column chunks per TMEM read round (one in gather mode, whose 480 threads have
       // fewer registers each), so the buffer is released as early as possible
       constexpr int kRead = GATHER ? 1 : 2;
-      for (int ch = 0; ch < nchunks; ch += kRead) {
-        const bool two = kRead == 2 && ch + 1 < nchunks;
+      // this group's chunks [cbeg, cend): all of them, or one half when the groups split columns
+      const int chalf = (nchunks + 1) >> 1;
+      const int cbeg = split_epi ? (eg == 0 ? 0 : chalf) : 0;
+      const int cend = split_epi ? (eg == 0 ? chalf : nchunks) : nchunks;
+      if (cbeg >= cend && lane == 0) {
+        // nothing of this tile to drain (ragged last column block): release at once
+        if (PAIR && !leader)
+          mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+        else
+          mbar_arrive(&tempty[acc]);
+      }
+      for (int ch = cbeg; ch < cend; ch += kRead) {
+        const bool two = kRead == 2 && ch + 1 < cend;
         uint32_t v[kRead][32];
         const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(acc * BN + ch * kEpiCols);
         tmem_ld_32x32b_x32(tcol, v[0]);
         if (two) tmem_ld_32x32b_x32(tcol + kEpiCols, v[kRead - 1]);
         tmem_ld_wait();
-        if (ch + kRead >= nchunks) {
+        if (ch + kRead >= cend) {
           // the warp's last TMEM read of the tile (tcgen05.ld is warp-collective)
           tc_fence_before();
           __syncwarp();
@@ -465,6 +487,10 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         for (int h = 0; h < kRead; ++h) {
           if (h == 1 && !two) break;
           const int nc = (ch + h) * kEpiCols;
+          const bool col_ok = nc + 4 * c4 < left;
+          // this thread's 4 channels (loaded before the transpose so their latency overlaps it)
+          const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
+          const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
           // row `lane` -> smem, 16-byte chunks XOR-swizzled by row: both phases conflict-free
 #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -472,9 +498,14 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 make_float4(__uint_as_float(v[h][4 * c]), __uint_as_float(v[h][4 * c + 1]),
                             __uint_as_float(v[h][4 * c + 2]), __uint_as_float(v[h][4 * c + 3]));
           __syncwarp();
-          const bool col_ok = nc + 4 * c4 < left;
-          const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
-          const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+          // all eight of this thread's (row, 4 channels) read back first: the shared-memory loads
+          // issue back to back instead of one load latency per row
+          float4 a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + sub;
+            a[i] = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+          }
           float4 part[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) part[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -500,23 +531,22 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + sub;
-            float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
             if (!col_ok || mt + r >= p.M) continue;
             if (SK) {
               if (mode == 2) {
-                __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a);
+                __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a[i]);
                 continue;
               }
-              a.x += part[i].x;
-              a.y += part[i].y;
-              a.z += part[i].z;
-              a.w += part[i].w;
+              a[i].x += part[i].x;
+              a[i].y += part[i].y;
+              a[i].z += part[i].z;
+              a[i].w += part[i].w;
             }
             *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
-                make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
+                make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
           }
           __syncwarp();
         }
