@@ -260,27 +260,33 @@ __global__ void __launch_bounds__(kHThreads, 1)
         for (int h = 0; h < 2; ++h) {
           if (h == 1 && !two) break;
           const int nc = (ch + h) * kHEpiCols;
+          const bool col_ok = nc + 4 * c4 < left;
+          // this thread's 4 channels, fetched before the transpose so their latency overlaps it
+          const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
+          const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<float4*>(wst + lane * 32 + ((c ^ (lane & 7)) << 2)) =
                 make_float4(__uint_as_float(v[h][4 * c]), __uint_as_float(v[h][4 * c + 1]),
                             __uint_as_float(v[h][4 * c + 2]), __uint_as_float(v[h][4 * c + 3]));
           __syncwarp();
-          const bool col_ok = nc + 4 * c4 < left;
-          const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
-          const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+          // all eight rows read back first, so the shared-memory loads issue back to back
+          float4 a[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + sub;
-            const int tr = q * 32 + r;
-            const float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+            a[i] = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int tr = q * 32 + 4 * i + sub;
             const int off = rm_off[tr];
             if (!col_ok || off < 0 || oh0 + rm_dr[tr] >= p.Ho) continue;
             *reinterpret_cast<float4*>(ybase + static_cast<size_t>(off) * p.Kout + nc + 4 * c4) =
-                make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
+                make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
+                            fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
           }
           __syncwarp();
         }

@@ -231,16 +231,26 @@ __global__ void __launch_bounds__(kWinThreads, 1)
           const bool col_ok = nc + 4 * c4 < p.Kout;
           const float4 sc = *reinterpret_cast<const float4*>(sScale + nc + 4 * c4);
           const float4 bi = *reinterpret_cast<const float4*>(sBias + nc + 4 * c4);
+          // rows read back four at a time ahead of their math, so the shared-memory loads issue
+          // back to back (four, not eight: this kernel has fewer registers to spare)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 4 * i + sub;
-            const float4 a = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
-            if (col_ok && ow0 + r < p.Wo)
-              *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
-                  make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.y, sc.y, bi.y), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.z, sc.z, bi.z), p.lo), p.hi),
-                              fminf(fmaxf(fmaf(a.w, sc.w, bi.w), p.lo), p.hi));
+          for (int i0 = 0; i0 < 8; i0 += 4) {
+            float4 a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 4 * (i0 + i) + sub;
+              a[i] = *reinterpret_cast<const float4*>(wst + r * 32 + ((c4 ^ (r & 7)) << 2));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 4 * (i0 + i) + sub;
+              if (col_ok && ow0 + r < p.Wo)
+                *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
+                    make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
+                                fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
+                                fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
+                                fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
+            }
           }
           __syncwarp();
         }
