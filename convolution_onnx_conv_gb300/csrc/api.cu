@@ -20,10 +20,14 @@
 
 namespace convf {
 // defined once per tile width in tc_conv_inst.cu
-cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
-cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, cudaStream_t);
+cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+                               cudaStream_t);
+cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+                               cudaStream_t);
+cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+                               cudaStream_t);
+cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+                               cudaStream_t);
 }  // namespace convf
 
 using namespace convf;
@@ -151,6 +155,9 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "stream_k=%d is not 0 (auto), 1 (off) or 2 (on)", d->stream_k);
   if (d->kblocks_per_step < 0 || d->kblocks_per_step > 4)
     return fail(CONVF_ERR_INVALID_ARG, "kblocks_per_step=%d is not 0 (auto) or 1..4", d->kblocks_per_step);
+  if (d->cluster_multicast < 0 || d->cluster_multicast > 2)
+    return fail(CONVF_ERR_INVALID_ARG, "cluster_multicast=%d is not 0 (auto), 1 (off) or 2 (on)",
+                d->cluster_multicast);
   return CONVF_OK;
 }
 
@@ -393,6 +400,13 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
 // k-blocks per pipeline step of the TMA implicit-GEMM kernel: the first of 4, 2, 3 that divides
 // the stage count and the tile's k-blocks and still leaves two steps in flight (measured on the
 // ResNet-50 layers: 4 beats 2 on 128 x 64 tiles, 2 matches or beats 3 on 128 x 128 tiles).
+// Multicast clusters for the TMA implicit-GEMM kernel, chosen automatically: not yet (off
+// unless requested).
+bool auto_cluster_multicast(const Shape& s, int bn, int num_kb, int n_blocks, int num_sms) {
+  (void)s; (void)bn; (void)num_kb; (void)n_blocks; (void)num_sms;
+  return false;
+}
+
 int auto_kblocks_per_step(int stages, int num_kb) {
   for (int k : {4, 2, 3})
     if (stages % k == 0 && num_kb % k == 0 && stages / k >= 2) return k;
@@ -511,6 +525,7 @@ struct convf_handle {
   bool sk;          // stream-K work split
   int kpb;          // k-blocks per pipeline step (TcConvParams::kpb)
   bool a3d;         // 1x1 activation map is 3-D {64, M, C/64} (one box per step)
+  bool mc;          // clusters of two CTAs on neighbouring channel blocks share activation tiles
   float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
   int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
   WinGeom wg;       // window variant geometry
@@ -810,8 +825,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
               desc->stream_k, !gather, &h->bn, &h->pair, &h->sk);
     if (desc->tile_n) h->bn = desc->tile_n;
     h->kpb = 1;
-    if (!gather && !h->pair && !h->sk) {
-      const int st = tc_conv_stages(h->bn, false, false);
+    if (!gather && !h->sk) {
+      const int st = tc_conv_stages(h->bn, false, h->pair);
       const int nkb = h->ktot / 64;
       if (desc->kblocks_per_step) {
         if (st % desc->kblocks_per_step || nkb % desc->kblocks_per_step) {
@@ -825,7 +840,23 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
         h->kpb = auto_kblocks_per_step(st, nkb);
       }
     }
-    h->a3d = h->a_mode == kA2D && !gather && !h->pair && h->kpb > 1 && s.C % 64 == 0;
+    h->a3d = h->a_mode == kA2D && !gather && h->kpb > 1 && s.C % 64 == 0;
+    {
+      const int nb = (s.K + h->bn - 1) / h->bn;
+      const bool mc_ok = !gather && !h->pair && !h->sk && nb % 2 == 0;
+      h->mc = false;
+      if (desc->cluster_multicast == 2) {
+        if (!mc_ok) {
+          delete h;
+          return fail(CONVF_ERR_UNSUPPORTED,
+                      "cluster_multicast needs single-CTA whole tiles with TMA activation loads and an even "
+                      "number of %d-wide output-channel blocks (%d here)", h->bn, nb);
+        }
+        h->mc = true;
+      } else if (desc->cluster_multicast == 0) {
+        h->mc = mc_ok && auto_cluster_multicast(s, h->bn, h->ktot / 64, nb, h->num_sms);
+      }
+    }
     if (h->sk) {
       o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
       o_skflags = carve((size_t)h->num_sms * sizeof(int));
@@ -972,9 +1003,10 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     const long long tiles = (s.M + tile_m - 1) / tile_m * h->n_blocks;
     h->num_tiles = (int)tiles;
     h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2)
+              : h->mc ? 2 * (int)std::min<long long>(tiles / 2, h->num_sms / 2)
                       : (int)std::min<long long>(h->sk ? tiles * h->num_kb : tiles, h->num_sms);
     CUresult r;
-    if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER || h->pair || h->kpb == 1) {
+    if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER || h->kpb == 1) {
       const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};
       const cuuint64_t strides[1] = {(cuuint64_t)h->ktot * 2};
       const cuuint32_t box[2] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn)};
@@ -987,7 +1019,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       // K-major tiles
       const cuuint64_t dims[3] = {64, (cuuint64_t)s.K, (cuuint64_t)(h->ktot / 64)};
       const cuuint64_t strides[2] = {(cuuint64_t)h->ktot * 2, 128};
-      const cuuint32_t box[3] = {64, (cuuint32_t)h->bn, (cuuint32_t)h->kpb};
+      const cuuint32_t box[3] = {64, (cuuint32_t)(h->pair ? h->bn / 2 : h->bn), (cuuint32_t)h->kpb};
       const cuuint32_t es[3] = {1, 1, 1};
       r = g_encode_tiled(&h->tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, h->w_bf16, dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1173,10 +1205,10 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.split_epi = h->num_tiles <= 8LL * h->grid ? 1 : 0;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
-        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
       }
     }
   }
@@ -1241,10 +1273,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
-             "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d tiles=%d grid=%d patch_rows=%d "
-             "tap_channels=%d weight_bytes=%zu",
+             "kblocks_per_step=%d act_box_per_step=%d cluster_multicast=%d split_epilogue=%d tiles=%d grid=%d "
+             "patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
-             h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0,
+             h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0, h->mc ? 1 : 0,
              (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0, h->num_tiles,
              h->grid, h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
@@ -1395,9 +1427,9 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status; p.y = static_cast<float*>(y);
   p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
   switch (bn) {
-    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, strm); break;
-    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, strm); break;
-    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, strm); break;
+    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, false, strm); break;
+    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, false, strm); break;
+    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, false, strm); break;
   }
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();

@@ -11,7 +11,12 @@
 namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
                                                    const CUtensorMap& tmB, int grid,
-                                                   bool gather, bool pair, cudaStream_t stream) {
+                                                   bool gather, bool pair, bool mc, cudaStream_t stream) {
+  if (mc) {
+    // multicast clusters: single-CTA MMAs, whole tiles, TMA activation loads only
+    if (gather || pair || p.sk) return cudaErrorInvalidValue;
+    return launch_tc_conv_t<CONVF_BN, false, false, false, true>(p, tmA, tmB, grid, stream);
+  }
   if (p.sk) {
     // stream-K: single CTAs with TMA activation loads only
     if (gather || pair) return cudaErrorInvalidValue;

@@ -123,12 +123,17 @@ typedef struct {
                               reduction-block iterations; a split tile is finished by the CTA holding
                               its first reduction block, which adds the others' fp32 partials from a
                               handle-owned workspace).  Ignored where it does not apply. */
-  int kblocks_per_step;    /* TMA implicit-GEMM variants on single CTAs without stream-K: 64-wide
+  int kblocks_per_step;    /* TMA implicit-GEMM variants without stream-K (single CTAs or pairs): 64-wide
                               reduction blocks per pipeline step, 0 = auto, else 1..4 (must divide
                               both the block count and the tile width's stage count).  A step's
                               weights are one TMA box, and so are its activations in the 1x1 mode
                               when C % 64 == 0; more bytes per TMA operation raise the operand
                               ingest rate.  Ignored where it does not apply. */
+  int cluster_multicast;   /* TMA implicit-GEMM variants on single CTAs without stream-K: 0 = auto,
+                              1 = off, 2 = on (refused with CONVF_ERR_UNSUPPORTED unless the
+                              output channels form an even number of tile_n blocks): clusters of two
+                              CTAs compute the same rows for two neighbouring channel blocks, and
+                              each activation tile is loaded once and multicast into both CTAs. */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;

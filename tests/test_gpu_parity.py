@@ -289,6 +289,39 @@ def test_kblocks_per_step_every_output(case):
         c.close()
 
 
+PAIR_KPB_CASES = [
+    # CTA pairs (256-row tiles, half the weight tile per CTA) with several k-blocks per step
+    (S("pkpb_1x1_c256_ragged_m", 1, 256, 15, 21, 200, 1, 1), 64, [2, 4]),
+    (S("pkpb_1x1_c256_tile256", 2, 256, 9, 9, 256, 1, 1, act=ACT_RELU), 256, [2]),
+    (S("pkpb_1x1_c96_split_loads", 2, 96, 11, 13, 128, 1, 1), 128, [2]),
+    (S("pkpb_3x3_c128", 2, 128, 12, 12, 256, 3, 3, pads=(1, 1, 1, 1), bias=True), 256, [2, 3]),
+    (S("pkpb_3x3_s2_c128", 2, 128, 15, 15, 128, 3, 3, (2, 2), (1, 1, 1, 1)), 128, [3]),
+    (S("pkpb_1x1_many_tiles_per_cta", 4, 128, 56, 57, 256, 1, 1, act=ACT_RELU6), 128, [2]),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_KPB_CASES, ids=lambda c: c[0].name)
+def test_cta_pair_kblocks_per_step_every_output(case):
+    spec, tile_n, kpbs = case
+    inp = inputs_for(spec, 7760 + PAIR_KPB_CASES.index(case))
+    from parity import compare
+    ref = oracle_full(spec, inp)
+    x = to_device_nhwc(inp["x"])
+    for kpb in kpbs:
+        c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                         *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                         pads=spec.pads, act=spec.act, tile_n=tile_n, cta_pair=2, kblocks_per_step=kpb,
+                         variant=V.CONVF_VARIANT_GEMM_1X1 if spec.R == 1 else V.CONVF_VARIANT_IMPLICIT_GEMM)
+        d = c.describe()
+        assert f"kblocks_per_step={kpb} " in d and "cta_pair=1" in d, d
+        y = c(x)
+        torch.cuda.synchronize()
+        assert c.status() == cf.CONVF_OK
+        ok, worst, idx = compare(y.cpu().contiguous().numpy(), ref, False)
+        assert ok, (spec.name, kpb, worst, idx, d)
+        c.close()
+
+
 def test_kblocks_per_step_must_divide_blocks_and_stages():
     spec = S("kpb_refused", 1, 192, 8, 8, 64, 1, 1)
     inp = inputs_for(spec, 7790)
@@ -297,6 +330,50 @@ def test_kblocks_per_step_must_divide_blocks_and_stages():
             cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], tile_n=tile_n,
                          kblocks_per_step=kpb, variant=V.CONVF_VARIANT_GEMM_1X1)
         assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "must divide" in str(e.value)
+
+
+MC_CASES = [
+    # (spec, tile width, k-blocks per step): two neighbouring channel blocks per cluster
+    (S("mc_3x3_c256_k256", 2, 256, 12, 12, 256, 3, 3, pads=(1, 1, 1, 1), bias=True), 64, 4),
+    (S("mc_3x3_s2_k200_ragged", 2, 128, 15, 15, 200, 3, 3, (2, 2), (1, 1, 1, 1)), 64, 2),
+    (S("mc_3x3_c64_one_block_per_step", 1, 64, 9, 11, 256, 3, 3, pads=(1, 1, 1, 1)), 128, 1),
+    (S("mc_1x1_c256_act_box", 1, 256, 15, 20, 256, 1, 1, act=ACT_RELU), 128, 2),
+    (S("mc_1x1_c96_split_loads", 2, 96, 11, 13, 128, 1, 1), 64, 2),
+    # 400 tile pairs over 76 clusters: the stage ring wraps across tiles in both CTAs
+    (S("mc_1x1_many_pairs", 4, 128, 56, 57, 256, 1, 1, act=ACT_RELU6), 64, 2),
+]
+
+
+@pytest.mark.parametrize("case", MC_CASES, ids=lambda c: c[0].name)
+def test_cluster_multicast_every_output(case):
+    """Clusters of two CTAs on neighbouring channel blocks: each activation tile is loaded by one
+    CTA and multicast into both; a stage is refilled only after both CTAs' MMAs released it."""
+    spec, tile_n, kpb = case
+    inp = inputs_for(spec, 7800 + MC_CASES.index(case))
+    from parity import compare
+    ref = oracle_full(spec, inp)
+    c = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                     *cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5), stride=spec.stride,
+                     pads=spec.pads, act=spec.act, tile_n=tile_n, kblocks_per_step=kpb, cluster_multicast=2,
+                     variant=V.CONVF_VARIANT_GEMM_1X1 if spec.R == 1 else V.CONVF_VARIANT_IMPLICIT_GEMM)
+    assert "cluster_multicast=1 " in c.describe(), c.describe()
+    x = to_device_nhwc(inp["x"])
+    for _ in range(2):
+        y = c(x)
+        torch.cuda.synchronize()
+        assert c.status() == cf.CONVF_OK
+        ok, worst, idx = compare(y.cpu().contiguous().numpy(), ref, False)
+        assert ok, (spec.name, worst, idx, c.describe())
+    c.close()
+
+
+def test_cluster_multicast_needs_an_even_number_of_channel_blocks():
+    spec = S("mc_refused", 1, 64, 8, 8, 192, 3, 3, pads=(1, 1, 1, 1))   # 3 blocks of 64
+    inp = inputs_for(spec, 7890)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], pads=spec.pads, tile_n=64,
+                     cluster_multicast=2, variant=V.CONVF_VARIANT_IMPLICIT_GEMM)
+    assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "even number" in str(e.value)
 
 
 def test_1x1_forced_through_im2col_and_gather():

@@ -281,6 +281,20 @@ def test_kblocks_per_step_is_validated():
         assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "kblocks_per_step" in str(e.value)
 
 
+def test_cluster_multicast_mode_is_validated():
+    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_44_s3b0_3x3@b32"]
+    for m in (0, 1, 2):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         cluster_multicast=m)
+        assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM
+    for m in (-1, 3):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         cluster_multicast=m)
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_plan(d)
+        assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "cluster_multicast" in str(e.value)
+
+
 def test_stream_k_mode_is_validated():
     """stream_k takes 0 (auto: whole tiles), 1 (off) or 2 (on); anything else is refused."""
     spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_12_s1b0_3x3@b32"]   # strided: im2col
