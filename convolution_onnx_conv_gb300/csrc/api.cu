@@ -825,7 +825,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
               desc->stream_k, !gather, &h->bn, &h->pair, &h->sk);
     if (desc->tile_n) h->bn = desc->tile_n;
     h->kpb = 1;
-    if (!gather && !h->sk) {
+    if (!gather) {
       const int st = tc_conv_stages(h->bn, false, h->pair);
       const int nkb = h->ktot / 64;
       if (desc->kblocks_per_step) {
@@ -1004,7 +1004,9 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     h->num_tiles = (int)tiles;
     h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2)
               : h->mc ? 2 * (int)std::min<long long>(tiles / 2, h->num_sms / 2)
-                      : (int)std::min<long long>(h->sk ? tiles * h->num_kb : tiles, h->num_sms);
+                      // stream-K: every CTA needs at least one pipeline step of its own (a CTA
+                      // with an empty share would be waited for as a contributor)
+                      : (int)std::min<long long>(h->sk ? tiles * (h->num_kb / h->kpb) : tiles, h->num_sms);
     CUresult r;
     if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER || h->kpb == 1) {
       const cuuint64_t dims[2] = {(cuuint64_t)h->ktot, (cuuint64_t)s.K};

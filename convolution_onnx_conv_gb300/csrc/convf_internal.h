@@ -77,7 +77,7 @@ struct TcConvParams {
   // k-blocks per pipeline step (1, 2, 3 or 4; divides num_kb and the stage count): one weight
   // TMA box of kpb consecutive 64-wide blocks, and one activation box when a3d (2-D mode, C a
   // multiple of 64: the map is {64, M, C/64}); otherwise kpb activation loads shared by the two
-  // producer warps.  Without stream-K or gathered rows only; 1 elsewhere.
+  // producer warps.  1 in gather mode.
   int kpb;
   int a3d;
   // both epilogue warpgroups drain every tile (one column half each) instead of alternate tiles:

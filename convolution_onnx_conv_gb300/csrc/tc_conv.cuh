@@ -58,15 +58,17 @@ struct TcCfg {
 // num_tiles x num_kb iterations cut at tile boundaries.  Every role walks the same sequence.
 // With multicast clusters (mc_rank >= 0) the sequence runs over tile pairs (an M block and two
 // neighbouring output-channel blocks) and each CTA of the pair takes its own channel block.
+// Stream-K shares are counted in pipeline steps (kpb k-blocks), so segments start and end on
+// step boundaries.
 template <bool SK>
 struct SegSched {
-  int num_kb, num_tiles, tstep, tile, mc_rank, nb;
+  int num_kb, num_tiles, tstep, tile, mc_rank, nb, kpb, spt;
   long long it, it1;
   __device__ SegSched(const TcConvParams& p, int tstart, int tstep_, int mc_rank_ = -1)
       : num_kb(p.num_kb), num_tiles(mc_rank_ >= 0 ? p.num_tiles / 2 : p.num_tiles), tstep(tstep_), tile(tstart),
-        mc_rank(mc_rank_), nb(p.n_blocks), it(0), it1(0) {
+        mc_rank(mc_rank_), nb(p.n_blocks), kpb(p.kpb), spt(p.num_kb / p.kpb), it(0), it1(0) {
     if (SK) {
-      const long long total = static_cast<long long>(p.num_tiles) * p.num_kb;
+      const long long total = static_cast<long long>(p.num_tiles) * spt;
       it = total * blockIdx.x / gridDim.x;
       it1 = total * (blockIdx.x + 1) / gridDim.x;
     }
@@ -85,11 +87,13 @@ struct SegSched {
       return true;
     }
     if (it >= it1) return false;
-    t = static_cast<int>(it / num_kb);
-    const long long base = static_cast<long long>(t) * num_kb;
-    ka = static_cast<int>(it - base);
-    kend = static_cast<int>(min(base + num_kb, it1) - base);
-    it = base + kend;
+    t = static_cast<int>(it / spt);
+    const long long base = static_cast<long long>(t) * spt;
+    const int s0 = static_cast<int>(it - base);
+    const int s1 = static_cast<int>(min(base + spt, it1) - base);
+    ka = s0 * kpb;
+    kend = s1 * kpb;
+    it = base + s1;
     return true;
   }
 };
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   // operation and the number of issuing warps set the operand ingest rate: the weights of a
   // step are one box, and the activations one box (3-D map) or kpb loads split between the two
   // producer warps (even k-blocks on warp 0, odd ones on warp 2).
-  const int kpb = (GATHER || SK) ? 1 : p.kpb;
+  const int kpb = GATHER ? 1 : p.kpb;
   const bool a3d = !GATHER && p.a3d;
   // MC: warp 0 issues this CTA's half of the activation loads and expects all of them
   const bool a_odd = !GATHER && !MC && !a3d && kpb > 1;
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kEpiWarpBytes);
     const int sub = lane >> 3;             // row within each group of four in the store phase
     const int c4 = lane & 7;               // 4-channel column group
-    const long long total_it = static_cast<long long>(p.num_tiles) * p.num_kb;
+    const long long total_it = static_cast<long long>(p.num_tiles) * (p.num_kb / p.kpb);   // in steps
     // alternate whole tiles: group eg visits only its own tiles; split columns: every tile;
     // stream-K: every segment, keeping its own
     const bool kAll = SK || split_epi;
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       int d0 = 0, d1 = 0;                              // owner: contributing CTAs [d0, d1)
       if (SK && mode == 1) {
         // contributors: the CTAs after this one whose share starts inside the tile
-        const long long tend = static_cast<long long>(tile + 1) * p.num_kb;
+        const long long tend = static_cast<long long>(tile + 1) * (p.num_kb / p.kpb);
         d0 = blockIdx.x + 1;
         d1 = d0;
         while (d1 < static_cast<int>(gridDim.x) && total_it * d1 / gridDim.x < tend) ++d1;

@@ -123,7 +123,7 @@ typedef struct {
                               reduction-block iterations; a split tile is finished by the CTA holding
                               its first reduction block, which adds the others' fp32 partials from a
                               handle-owned workspace).  Ignored where it does not apply. */
-  int kblocks_per_step;    /* TMA implicit-GEMM variants without stream-K (single CTAs or pairs): 64-wide
+  int kblocks_per_step;    /* TMA implicit-GEMM variants (single CTAs, pairs, stream-K): 64-wide
                               reduction blocks per pipeline step, 0 = auto, else 1..4 (must divide
                               both the block count and the tile width's stage count).  A step's
                               weights are one TMA box, and so are its activations in the 1x1 mode
