@@ -16,6 +16,7 @@ only collectives are the timing barrier and the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -32,6 +33,25 @@ WORKLOAD = ("ResNet-50 v2 conv stack, 53 layers (7x7/2 stem, 1x1 and 3x3 bottlen
             "projections) at batch 32, 224x224 input, bf16 x/W, fp32 accumulate and output, "
             "folded BN + ReLU epilogue, channels-last")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of tc_conv_kernel per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean
+# over the 49 tc_conv launches of one ResNet-50 pass; ncu flushes the caches before each kernel,
+# so the output still in L2 when a kernel ends is not counted as written), captured with
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+#       --clock-control none -k regex:tc_conv -s 98 -c 49 python bench.py --profile r50:0,...,52
+# It describes the kernel sources it was taken on (their SHA-256 prefix) and is reported as
+# null for any other sources.
+TC_TRAFFIC = {"bytes_per_launch": 15.71e6, "read_per_launch": 12.60e6, "write_per_launch": 3.11e6,
+              "sources_sha256_16": "866189d719d9ed35"}
+TC_SOURCES = ("tc_conv.cuh", "tc_conv_inst.cu", "ptx.cuh", "convf_internal.h", "api.cu")
+
+
+def tc_traffic():
+    h = hashlib.sha256()
+    for f in TC_SOURCES:
+        with open(os.path.join(ROOT, "convolution_onnx_conv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return TC_TRAFFIC["bytes_per_launch"] if h.hexdigest()[:16] == TC_TRAFFIC["sources_sha256_16"] else None
 
 
 def load_peaks():
@@ -358,14 +378,19 @@ def main():
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
     ms_per_step = total_ms / args.steps
 
-    # dominant kernel: the tcgen05 implicit-GEMM conv (every ResNet layer runs it)
-    tc_ms = sum(per_layer) / lsteps
-    achieved = flops_step / (tc_ms * 1e-3) / 1e12
+    # dominant kernel: the tcgen05 implicit-GEMM conv (49 of the 53 layers: every 1x1 and every
+    # strided or 7x7 layer; the halo and window kernels take the other four)
+    tc_idx = [i for i, L in enumerate(layers)
+              if L["conv"].describe().split()[0] in ("variant=gemm_1x1", "variant=implicit_gemm_im2col")]
+    tc_ms = sum(per_layer[i] for i in tc_idx) / lsteps
+    tc_flops = sum(specs[i].flops for i in tc_idx)
+    achieved = tc_flops / (tc_ms * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
-            "kernel": "tc_conv_kernel (tcgen05 implicit GEMM, all tile widths)",
+            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": tc_traffic(),
+            "kernel": f"tc_conv_kernel (tcgen05 implicit GEMM, all tile widths; {len(tc_idx)} layers)",
             "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside a long step)",
-            "per_launch_flops": flops_step / len(specs), "launch_ms": tc_ms / len(specs)}
+            "per_launch_flops": tc_flops / len(tc_idx), "launch_ms": tc_ms / len(tc_idx),
+            "per_launch_algorithmic_bytes": sum(specs[i].algorithmic_bytes for i in tc_idx) / len(tc_idx)}
     idx17 = [i for i, s in enumerate(specs) if s.R > 1]
     f17 = sum(specs[i].flops for i in idx17)
     t17 = sum(per_layer[i] for i in idx17) / lsteps
