@@ -400,13 +400,6 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
 // k-blocks per pipeline step of the TMA implicit-GEMM kernel: the first of 4, 2, 3 that divides
 // the stage count and the tile's k-blocks and still leaves two steps in flight (measured on the
 // ResNet-50 layers: 4 beats 2 on 128 x 64 tiles, 2 matches or beats 3 on 128 x 128 tiles).
-// Multicast clusters for the TMA implicit-GEMM kernel, chosen automatically: not yet (off
-// unless requested).
-bool auto_cluster_multicast(const Shape& s, int bn, int num_kb, int n_blocks, int num_sms) {
-  (void)s; (void)bn; (void)num_kb; (void)n_blocks; (void)num_sms;
-  return false;
-}
-
 int auto_kblocks_per_step(int stages, int num_kb) {
   for (int k : {4, 2, 3})
     if (stages % k == 0 && num_kb % k == 0 && stages / k >= 2) return k;
@@ -853,9 +846,9 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
                       "number of %d-wide output-channel blocks (%d here)", h->bn, nb);
         }
         h->mc = true;
-      } else if (desc->cluster_multicast == 0) {
-        h->mc = mc_ok && auto_cluster_multicast(s, h->bn, h->ktot / 64, nb, h->num_sms);
       }
+      // automatic choice: off (measured 3-8% slower than single CTAs on every ResNet-50 layer
+      // tried: halving the activation loads does not help once the MMA issue is the bound)
     }
     if (h->sk) {
       o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
