@@ -17,6 +17,13 @@ Every function is the plain definition of one stage, kept separate on purpose:
     the conv weights offline ("tensorforge", section "ResNet fusion":
     W' = scale * W, bias = shift); here it stays a separate stage so that the
     library's fold is checked, not assumed.
+``residual_add``
+    The skip connection of a residual block, r added element-wise to the conv +
+    BN result before the activation, as in the single fused conv, residual,
+    bias and ReLU operation the "Kyanite" README lists (section "Cuda
+    Executor").  Where it sits relative to BN is not stated there; here it
+    follows the folded BN affine (the bottleneck's shortcut joins after the
+    block's last BN), a reading.
 ``activation``
     ReLU = max(u, 0); ReLU6 = min(max(u, 0), 6), the two clamps of the
     residual + batchnorm + relu6 example kernel in the "Kyanite" README
@@ -207,6 +214,11 @@ def batchnorm(z, gamma, beta, mean, var, eps=1e-5, chan=None):
             + b.reshape(shp))
 
 
+def residual_add(u, r):
+    """u + r element-wise, in float64 (the residual stage; see the module docstring)."""
+    return np.asarray(u, dtype=np.float64) + np.asarray(r, dtype=np.float64)
+
+
 def activation(u, act=ACT_NONE, lo=0.0, hi=6.0):
     """none: u;  ReLU: max(u, 0);  ReLU6: min(max(u, 0), 6);  Clip: min(max(u, lo), hi)."""
     u = np.asarray(u, dtype=np.float64)
@@ -281,21 +293,27 @@ def requant_s8(acc, chan, bias, mult, shift, zero_point=0, relu=False):
 # ------------------------------------------------------------- whole pipeline
 
 def conv_bn_act(x, w, bias=None, bn=None, act=ACT_NONE, lo=0.0, hi=6.0, strides=(1, 1),
-                pads=(0, 0, 0, 0), dilations=(1, 1), group=1, eps=1e-5):
-    """Conv, then BN (if ``bn`` = (gamma, beta, mean, var)), then activation."""
+                pads=(0, 0, 0, 0), dilations=(1, 1), group=1, eps=1e-5, residual=None):
+    """Conv, then BN (if ``bn`` = (gamma, beta, mean, var)), then the residual (if given, NCHW of
+    the output's shape), then activation."""
     z = conv2d(x, w, bias, strides, pads, dilations, group)
     if bn is not None:
         z = batchnorm(z, *bn, eps=eps)
+    if residual is not None:
+        z = residual_add(z, residual)
     return activation(z, act, lo, hi)
 
 
 def conv_bn_act_points(x, w, bias, bn, act, strides, pads, dilations, group, pts, lo=0.0,
-                       hi=6.0, eps=1e-5):
-    """The same three stages evaluated at selected (n, k, oh, ow) points only."""
+                       hi=6.0, eps=1e-5, residual=None):
+    """The same stages evaluated at selected (n, k, oh, ow) points only (``residual``: NCHW)."""
     pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
     z = conv2d_points(x, w, bias, strides, pads, dilations, group, pts)
     if bn is not None:
         z = batchnorm(z, *bn, eps=eps, chan=pts[:, 1])
+    if residual is not None:
+        r = np.asarray(residual)
+        z = residual_add(z, r[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]])
     return activation(z, act, lo, hi)
 
 

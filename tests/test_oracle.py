@@ -398,3 +398,58 @@ def test_tolerance_helper_flags_a_planted_error():
     y[17] += 2e-3 + 1e-3 * abs(ref[17])
     ok, worst, idx = oracle.tolerance_ok(y, ref)
     assert not ok and idx == 17 and worst > 1.0
+
+
+# ----------------------------------------------------------- residual stage
+
+def test_residual_with_identity_kernel_is_shifted_input():
+    """Closed form: an identity 3x3 kernel (pad 1) returns x, so with a residual r and ReLU the
+    whole pipeline must give max(x + r, 0) exactly."""
+    rng = np.random.default_rng(40)
+    C = 5
+    x = rng.standard_normal((2, C, 7, 6))
+    r = rng.standard_normal((2, C, 7, 6))
+    w = np.zeros((C, C, 3, 3))
+    for c in range(C):
+        w[c, c, 1, 1] = 1.0
+    y = oracle.conv_bn_act(x, w, None, None, oracle.ACT_RELU, pads=(1, 1, 1, 1), residual=r)
+    assert np.array_equal(y, np.maximum(x + r, 0.0))
+
+
+def test_residual_joins_after_bn_and_before_the_clamp():
+    """A residual equal to minus the BN output leaves a zero pre-activation: every activation
+    then gives 0 (Clip gives its lower bound), whatever the conv and BN values."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((1, 4, 6, 6))
+    w = rng.standard_normal((3, 4, 3, 3))
+    bn = (rng.uniform(0.5, 1.5, 3), rng.normal(0, 0.1, 3), rng.normal(0, 0.1, 3), rng.uniform(0.5, 1.5, 3))
+    u = oracle.batchnorm(oracle.conv2d(x, w, None, (1, 1), (1, 1, 1, 1)), *bn)
+    for act in (oracle.ACT_NONE, oracle.ACT_RELU, oracle.ACT_RELU6):
+        y = oracle.conv_bn_act(x, w, None, bn, act, pads=(1, 1, 1, 1), residual=-u)
+        assert np.max(np.abs(y)) < 1e-12
+    y = oracle.conv_bn_act(x, w, None, bn, oracle.ACT_CLIP, 0.25, 2.0, pads=(1, 1, 1, 1), residual=-u)
+    assert np.allclose(y, 0.25, atol=1e-12)
+
+
+def test_residual_pipeline_matches_torch_on_tiny_cases():
+    """Library route: torch conv2d (float64) + batch_norm (inference) + residual + ReLU6."""
+    rng = np.random.default_rng(42)
+    for trial in range(6):
+        N, C, K, H, W = 2, int(rng.integers(1, 6)), int(rng.integers(1, 6)), 6, 5
+        x = rng.standard_normal((N, C, H, W))
+        w = rng.standard_normal((K, C, 3, 3))
+        b = rng.standard_normal(K)
+        bn = (rng.uniform(0.5, 1.5, K), rng.normal(0, 0.1, K), rng.normal(0, 0.1, K), rng.uniform(0.5, 1.5, K))
+        stride = (1 + trial % 2, 1)
+        z = torch.nn.functional.conv2d(torch.from_numpy(x), torch.from_numpy(w), torch.from_numpy(b), stride, 1)
+        z = torch.nn.functional.batch_norm(z, torch.from_numpy(bn[2]), torch.from_numpy(bn[3]),
+                                           torch.from_numpy(bn[0]), torch.from_numpy(bn[1]), False, 0.0, 1e-5)
+        r = rng.standard_normal(tuple(z.shape))
+        ref = torch.clamp(z + torch.from_numpy(r), 0.0, 6.0).numpy()
+        y = oracle.conv_bn_act(x, w, b, bn, oracle.ACT_RELU6, strides=stride, pads=(1, 1, 1, 1), residual=r)
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+        pts = np.array([[n, k, i, j] for n in range(N) for k in range(K) for i in range(z.shape[2])
+                        for j in range(z.shape[3])][::7], dtype=np.int64)
+        yp = oracle.conv_bn_act_points(x, w, b, bn, oracle.ACT_RELU6, stride, (1, 1, 1, 1), (1, 1), 1, pts,
+                                       residual=r)
+        assert np.allclose(yp, ref[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]], rtol=1e-12, atol=1e-12)
