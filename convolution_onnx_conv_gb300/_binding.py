@@ -15,6 +15,7 @@ from . import _build
 CONVF_OK, CONVF_ERR_INVALID_ARG, CONVF_ERR_UNSUPPORTED, CONVF_ERR_OOM, CONVF_ERR_CUDA, \
     CONVF_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 CONVF_BF16, CONVF_S8 = 0, 1
+CONVF_OUT_F32, CONVF_OUT_BF16 = 0, 1
 CONVF_NCHW, CONVF_NHWC = 0, 1
 CONVF_ACT_NONE, CONVF_ACT_RELU, CONVF_ACT_RELU6, CONVF_ACT_CLIP = 0, 1, 2, 3
 CONVF_AUTO_PAD_NOTSET, CONVF_AUTO_PAD_SAME_UPPER, CONVF_AUTO_PAD_SAME_LOWER, \
@@ -30,7 +31,8 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_plan", "conv_fused_pack_weights", "conv_fused_create", "conv_fused_run",
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
-            "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate"]
+            "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
+            "conv_fused_run_residual"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -42,13 +44,13 @@ class ConvDesc(ctypes.Structure):
                 ("act", ctypes.c_int), ("clip_lo", ctypes.c_float), ("clip_hi", ctypes.c_float),
                 ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("kblocks_per_step", ctypes.c_int),
-                ("cluster_multicast", ctypes.c_int)]
+                ("cluster_multicast", ctypes.c_int), ("out_dtype", ctypes.c_int), ("residual", ctypes.c_int)]
 
 
 def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1,
               dtype=CONVF_BF16, act=CONVF_ACT_NONE, clip=(0.0, 6.0), auto_pad="NOTSET",
               variant=CONVF_VARIANT_AUTO, layout=CONVF_NHWC, tile_n=0, cta_pair=0, stream_k=0,
-              kblocks_per_step=0, cluster_multicast=0) -> ConvDesc:
+              kblocks_per_step=0, cluster_multicast=0, out_dtype=CONVF_OUT_F32, residual=0) -> ConvDesc:
     d = ConvDesc()
     d.N, d.C, d.H, d.W, d.K, d.R, d.S = N, C, H, W, K, R, S
     d.stride[:] = list(stride)
@@ -66,6 +68,8 @@ def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1
     d.stream_k = stream_k
     d.kblocks_per_step = kblocks_per_step
     d.cluster_multicast = cluster_multicast
+    d.out_dtype = out_dtype
+    d.residual = residual
     return d
 
 
@@ -104,6 +108,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_pack_weights.argtypes = [dptr, ctypes.c_int, vp, vp, ctypes.c_size_t]
     lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
     lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
+    lib.conv_fused_run_residual.argtypes = [vp, vp, vp, vp, vp]
     lib.conv_fused_status.argtypes = [vp]
     lib.conv_fused_clear_status.argtypes = [vp]
     lib.conv_fused_destroy.argtypes = [vp]
@@ -200,6 +205,14 @@ def conv_fused_run(handle: int, x, y, stream=None):
     _check(load_library().conv_fused_run(handle, _addr(x), _addr(y), s))
 
 
+def conv_fused_run_residual(handle: int, x, r, y, stream=None):
+    """conv_fused_run for residual handles: y = act(scale * conv(x) + bias' + r)."""
+    s = stream
+    if s is not None and hasattr(s, "cuda_stream"):
+        s = s.cuda_stream
+    _check(load_library().conv_fused_run_residual(handle, _addr(x), _addr(r), _addr(y), s))
+
+
 def conv_fused_status(handle: int) -> int:
     return load_library().conv_fused_status(handle)
 
@@ -259,13 +272,17 @@ class FusedConv:
     def __init__(self, N, C, H, W, K, R, S, w, bias=None, bn_scale=None, bn_shift=None, stride=(1, 1),
                  pads=(0, 0, 0, 0), dilation=(1, 1), group=1, act=CONVF_ACT_NONE, clip=(0.0, 6.0),
                  auto_pad="NOTSET", variant=CONVF_VARIANT_AUTO, requant_mult=None, requant_shift=None,
-                 out_zero_point=0, tile_n=0, cta_pair=0, stream_k=0, kblocks_per_step=0, cluster_multicast=0):
+                 out_zero_point=0, tile_n=0, cta_pair=0, stream_k=0, kblocks_per_step=0, cluster_multicast=0,
+                 out_bf16=False, residual=False):
         import torch
         s8 = w.dtype == torch.int8
         self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group,
                               CONVF_S8 if s8 else CONVF_BF16, act, clip, auto_pad, variant, tile_n=tile_n,
                               cta_pair=cta_pair, stream_k=stream_k, kblocks_per_step=kblocks_per_step,
-                              cluster_multicast=cluster_multicast)
+                              cluster_multicast=cluster_multicast,
+                              out_dtype=CONVF_OUT_BF16 if out_bf16 else CONVF_OUT_F32, residual=int(bool(residual)))
+        self.out_bf16 = bool(out_bf16)
+        self.residual = bool(residual)
         wc = w.contiguous().cpu()
         wbits = wc if s8 else wc.view(torch.int16)
         keep = [wbits]
@@ -294,10 +311,12 @@ class FusedConv:
     def new_output(self):
         import torch
         N, K, Ho, Wo = self.out_shape
-        return torch.empty((N, Ho, Wo, K), dtype=torch.int8 if self.s8 else torch.float32,
-                           device="cuda").permute(0, 3, 1, 2)
+        dt = torch.int8 if self.s8 else (torch.bfloat16 if self.out_bf16 else torch.float32)
+        return torch.empty((N, Ho, Wo, K), dtype=dt, device="cuda").permute(0, 3, 1, 2)
 
-    def __call__(self, x, y=None, stream=None):
+    def __call__(self, x, y=None, stream=None, r=None):
+        """Runs on the current torch stream; ``r`` is the residual (y's shape, dtype and
+        channels-last storage) for handles made with ``residual=True``."""
         import torch
         if not x.is_cuda:
             raise ValueError("x must be a CUDA tensor")
@@ -305,8 +324,13 @@ class FusedConv:
             raise ValueError("x must use channels-last storage")
         if y is None:
             y = self.new_output()
-        conv_fused_run(self.handle, x.data_ptr(), y.data_ptr(),
-                       stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+        s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+        if self.residual:
+            if r is None:
+                raise ValueError("this conv adds a residual: pass r")
+            conv_fused_run_residual(self.handle, x.data_ptr(), r.data_ptr(), y.data_ptr(), s)
+        else:
+            conv_fused_run(self.handle, x.data_ptr(), y.data_ptr(), s)
         return y
 
     def status(self) -> int:

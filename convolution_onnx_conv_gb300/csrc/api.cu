@@ -158,6 +158,10 @@ convf_status check_misc(const convf_desc* d) {
   if (d->cluster_multicast < 0 || d->cluster_multicast > 2)
     return fail(CONVF_ERR_INVALID_ARG, "cluster_multicast=%d is not 0 (auto), 1 (off) or 2 (on)",
                 d->cluster_multicast);
+  if (d->out_dtype != CONVF_OUT_F32 && d->out_dtype != CONVF_OUT_BF16)
+    return fail(CONVF_ERR_INVALID_ARG, "out_dtype=%d is not CONVF_OUT_F32 (0) or CONVF_OUT_BF16 (1)", d->out_dtype);
+  if (d->residual != 0 && d->residual != 1)
+    return fail(CONVF_ERR_INVALID_ARG, "residual=%d is not 0 or 1", d->residual);
   return CONVF_OK;
 }
 
@@ -287,6 +291,9 @@ std::string halo_geom(const Shape& s, int num_sms, int forced_bn, HaloGeom* g) {
 std::string cannot(int v, const convf_desc* d, const Shape& s) {
   const bool bf = d->dtype == CONVF_BF16;
   char b[256];
+  if ((d->out_dtype != CONVF_OUT_F32 || d->residual) && v != CONVF_VARIANT_GEMM_1X1 &&
+      v != CONVF_VARIANT_IMPLICIT_GEMM)
+    return "bf16 output and the residual input are served by the TMA implicit-GEMM and 1x1 kernels only";
   switch (v) {
     case CONVF_VARIANT_DEPTHWISE:
       if (!bf) return "depthwise serves bf16 only";
@@ -515,6 +522,8 @@ struct convf_handle {
   // tcgen05 configuration
   int bn, a_mode, num_kb, cblocks, ktot, grid, num_tiles, n_blocks, patch_rows, row_bytes, cpt;
   bool pair;        // CTA-pair (cta_group::2) 256-row tiles
+  bool out_bf16;    // y (and the residual) are bf16
+  bool has_res;     // runs add a residual tensor (conv_fused_run_residual)
   bool sk;          // stream-K work split
   int kpb;          // k-blocks per pipeline step (TcConvParams::kpb)
   bool a3d;         // 1x1 activation map is 3-D {64, M, C/64} (one box per step)
@@ -729,6 +738,8 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   convf_handle* h = new (std::nothrow) convf_handle();
   if (!h) return fail(CONVF_ERR_OOM, "host allocation failed");
   h->desc = *desc;
+  h->out_bf16 = desc->out_dtype == CONVF_OUT_BF16;
+  h->has_res = desc->residual != 0;
   h->s = s;
   h->variant = variant;
   h->zp = out_zero_point;
@@ -1092,19 +1103,27 @@ convf_status encode_dw_map(convf_handle* h, const void* x) {
 }
 }  // namespace
 
-convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream) {
-  convf_status st = check_handle(h);
-  if (st != CONVF_OK) return st;
+namespace {
+convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, void* stream) {
   const Shape& s = h->s;
+  convf_status st = CONVF_OK;
   if (s.M == 0) return ok();   // empty batch: nothing to compute
   if (!x || !y) return fail(CONVF_ERR_INVALID_ARG, "x/y is NULL");
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15))
     return fail(CONVF_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
   const size_t esz = h->variant == CONVF_VARIANT_INT8 ? 1 : 2;
   const size_t xb = (size_t)s.N * s.H * s.W * s.C * esz;
-  const size_t yb = (size_t)s.M * s.K * (h->variant == CONVF_VARIANT_INT8 ? 1 : 4);
+  const size_t yb = (size_t)s.M * s.K * (h->variant == CONVF_VARIANT_INT8 ? 1 : (h->out_bf16 ? 2 : 4));
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
   if (x0 < y0 + yb && y0 < x0 + xb) return fail(CONVF_ERR_INVALID_ARG, "x and y overlap");
+  if (h->has_res) {
+    if (!res) return fail(CONVF_ERR_INVALID_ARG, "the residual r is NULL");
+    const uintptr_t r0 = reinterpret_cast<uintptr_t>(res);
+    if (r0 & 15) return fail(CONVF_ERR_INVALID_ARG, "the residual r must be 16-byte aligned");
+    if (r0 != y0 && r0 < y0 + yb && y0 < r0 + yb)
+      return fail(CONVF_ERR_INVALID_ARG, "the residual r overlaps y without being y");
+    if (r0 < x0 + xb && x0 < r0 + yb) return fail(CONVF_ERR_INVALID_ARG, "the residual r overlaps x");
+  }
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
     return fail(CONVF_ERR_INVALID_ARG, "the current device (%d) is not the handle's device (%d)", dev, h->device);
@@ -1195,6 +1214,7 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
       p.lo = h->lo; p.hi = h->hi; p.status = h->status; p.y = static_cast<float*>(y);
       p.sk = h->sk ? 1 : 0; p.sk_ws = h->sk_ws; p.sk_flags = h->sk_flags;
       p.kpb = h->kpb; p.a3d = h->a3d ? 1 : 0;
+      p.res = h->has_res ? res : nullptr; p.out_bf16 = h->out_bf16 ? 1 : 0;
       // split epilogue columns when CTAs hold at most 8 tiles (measured on the ResNet-50 1x1
       // layers: 5 tiles per CTA gain, 10 and 20 lose)
       p.split_epi = h->num_tiles <= 8LL * h->grid ? 1 : 0;
@@ -1209,6 +1229,21 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
   }
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();
+}
+}  // namespace
+
+convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  if (h->has_res) return fail(CONVF_ERR_INVALID_ARG, "this handle adds a residual: call conv_fused_run_residual");
+  return run_impl(h, x, nullptr, y, stream);
+}
+
+convf_status conv_fused_run_residual(convf_handle* h, const void* x, const void* r, void* y, void* stream) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  if (!h->has_res) return fail(CONVF_ERR_INVALID_ARG, "this handle was created without a residual (residual = 0)");
+  return run_impl(h, x, r, y, stream);
 }
 
 convf_status conv_fused_status(convf_handle* h) {
@@ -1268,11 +1303,12 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
-             "kblocks_per_step=%d act_box_per_step=%d cluster_multicast=%d split_epilogue=%d tiles=%d grid=%d "
-             "patch_rows=%d tap_channels=%d weight_bytes=%zu",
+             "kblocks_per_step=%d act_box_per_step=%d cluster_multicast=%d split_epilogue=%d out=%s residual=%d "
+             "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
              h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0, h->mc ? 1 : 0,
-             (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0, h->num_tiles,
+             (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0,
+             h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->num_tiles,
              h->grid, h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
 }

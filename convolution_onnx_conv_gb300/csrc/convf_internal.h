@@ -65,7 +65,9 @@ struct TcConvParams {
   int row_bytes;          // W*C*2, bytes of one input row
   int cpt;                // gather mode: channels per tap in the reduction layout (4, 8; 0 = C)
   float lo, hi;           // activation clamp
-  float* y;               // NHWC fp32 output [M][Kout]
+  float* y;               // NHWC output [M][Kout]: fp32, or bf16 bits when out_bf16
+  const void* res;        // residual [M][Kout] of y's element type added before the clamp, or null
+  int out_bf16;           // y (and res) hold bf16 (round to nearest even) instead of fp32
   int* status;            // device status word
   // stream-K: every CTA takes an equal share of the num_tiles x num_kb iterations; a tile split
   // across CTAs is finished by the CTA holding its k-block 0, which adds the others' fp32

@@ -19,6 +19,8 @@
 //   warps 7-14  (gather mode only) activation rows gathered by threads, for channel counts
 //               that TMA cannot address (C not a multiple of 8, e.g. a 3-channel stem)
 #pragma once
+#include <cuda_bf16.h>
+
 #include "convf_internal.h"
 #include "ptx.cuh"
 
@@ -98,13 +100,17 @@ struct SegSched {
   }
 };
 
-template <int BN, bool GATHER, bool PAIR, bool SK, bool MC>
+// EXT: the epilogue adds a residual and/or stores bf16 (TcConvParams::res, out_bf16); its own
+// instantiation, so the plain fp32 epilogue keeps its code (a shared one cost 1.3% of the
+// ResNet-50 step).
+template <int BN, bool GATHER, bool PAIR, bool SK, bool MC, bool EXT>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   static_assert(!(MC && (GATHER || PAIR || SK)), "multicast clusters run whole tiles with TMA activation loads");
+  static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
   // TcConvParams::split_epi on whole tiles of 64+ columns: both epilogue groups drain every
   // tile, one column half each (a tile's epilogue takes half as long, which shortens the last
@@ -453,6 +459,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     const bool glead = warp == 3 + 4 * eg && lane == 0;   // group leader thread
     float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kEpiWarpBytes);
     const int sub = lane >> 3;             // row within each group of four in the store phase
+    constexpr bool plain_out = !EXT;   // fp32 y, no residual
     const int c4 = lane & 7;               // 4-channel column group
     const long long total_it = static_cast<long long>(p.num_tiles) * (p.num_kb / p.kpb);   // in steps
     // alternate whole tiles: group eg visits only its own tiles; split columns: every tile;
@@ -576,6 +583,48 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               part[i].w += b[i].w;
             }
           }
+          if (!plain_out && !(SK && mode == 2)) {
+            // residual and/or bf16 output: v = scale*acc + bias' (+ r), clamp, store as fp32 or
+            // as four round-to-nearest-even bf16 (8 bytes)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + sub;
+              if (!col_ok || mt + r >= p.M) continue;
+              if (SK) {
+                a[i].x += part[i].x;
+                a[i].y += part[i].y;
+                a[i].z += part[i].z;
+                a[i].w += part[i].w;
+              }
+              const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;   // element index
+              float4 v = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
+                                     fmaf(a[i].w, sc.w, bi.w));
+              if (p.res) {
+                float4 rv;
+                if (p.out_bf16) {
+                  const uint2 rb = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
+                  rv = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
+                                   __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
+                } else {
+                  rv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
+                }
+                v.x += rv.x;
+                v.y += rv.y;
+                v.z += rv.z;
+                v.w += rv.w;
+              }
+              v = make_float4(fminf(fmaxf(v.x, p.lo), p.hi), fminf(fmaxf(v.y, p.lo), p.hi),
+                              fminf(fmaxf(v.z, p.lo), p.hi), fminf(fmaxf(v.w, p.lo), p.hi));
+              if (p.out_bf16) {
+                const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x, v.y);
+                const __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z, v.w);
+                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.y) + e) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&lo2), *reinterpret_cast<const uint32_t*>(&hi2));
+              } else {
+                *reinterpret_cast<float4*>(p.y + e) = v;
+              }
+            }
+          } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + sub;
@@ -595,6 +644,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                             fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
                             fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
                             fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
+          }
           }
           __syncwarp();
         }
@@ -763,11 +813,11 @@ teardown:
   }
 }
 
-template <int BN, bool GATHER, bool PAIR, bool SK = false, bool MC = false>
+template <int BN, bool GATHER, bool PAIR, bool SK = false, bool MC = false, bool EXT = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, MC>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, MC, EXT>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcCfg<BN, GATHER, PAIR>::kSmem);

@@ -64,6 +64,8 @@ typedef enum {
 } convf_status;
 
 typedef enum { CONVF_BF16 = 0, CONVF_S8 = 1 } convf_dtype;
+/* element type of y (and of the residual) on the bf16 path */
+typedef enum { CONVF_OUT_F32 = 0, CONVF_OUT_BF16 = 1 } convf_out_dtype;
 typedef enum { CONVF_NCHW = 0, CONVF_NHWC = 1 } convf_layout;
 typedef enum {
   CONVF_ACT_NONE = 0, CONVF_ACT_RELU = 1, CONVF_ACT_RELU6 = 2, CONVF_ACT_CLIP = 3
@@ -134,6 +136,16 @@ typedef struct {
                               output channels form an even number of tile_n blocks): clusters of two
                               CTAs compute the same rows for two neighbouring channel blocks, and
                               each activation tile is loaded once and multicast into both CTAs. */
+  int out_dtype;           /* convf_out_dtype of y on the bf16 path: CONVF_OUT_F32 (default) or
+                              CONVF_OUT_BF16 (the fp32 result rounded to nearest-even bf16) */
+  int residual;            /* 1: y = act(scale * conv + bias' + r) for a residual tensor r of
+                              y's shape, layout and element type, passed to
+                              conv_fused_run_residual (the skip connection of a bottleneck block,
+                              added after the folded BN and before the activation, as in the
+                              single fused conv, residual, bias and ReLU operation the "Kyanite"
+                              README lists in section "Cuda Executor").  0: no residual.
+                              Both options are served by the TMA implicit-GEMM and 1x1 kernels
+                              only (C % 8 == 0, group 1); other shapes are refused. */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;
@@ -185,11 +197,18 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
                                const int32_t* requant_mult, const int32_t* requant_shift,
                                int32_t out_zero_point, convf_handle** out);
 
-/* Run the fused conv: x (device, NHWC, bf16 bits or int8) -> y (device, NHWC, float32 for the
- * bf16 path, int8 for the s8 path).  Both must be 16-byte aligned and must not overlap.
+/* Run the fused conv: x (device, NHWC, bf16 bits or int8) -> y (device, NHWC, float32 -- or bf16
+ * bits with out_dtype = CONVF_OUT_BF16 -- for the bf16 path, int8 for the s8 path).  Both must be 16-byte aligned and must not overlap.
  * `stream` is a cudaStream_t (NULL = legacy default stream).  Asynchronous: no allocation,
  * no synchronisation; launch errors are returned as CONVF_ERR_CUDA. */
 convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream);
+
+/* conv_fused_run for a handle created with residual = 1: y = act(scale * conv(x) + bias' + r).
+ * r (device, NHWC, the element type of y, y's shape) must be 16-byte aligned; it may be y itself
+ * (each element is read before it is written, by the same thread) but must not overlap y
+ * otherwise, nor x.  conv_fused_run refuses residual handles and this call refuses the others
+ * (CONVF_ERR_INVALID_ARG). */
+convf_status conv_fused_run_residual(convf_handle* h, const void* x, const void* r, void* y, void* stream);
 
 /* Device status of the handle's previous runs, read after the caller synchronised the
  * stream: CONVF_OK, or CONVF_ERR_TIMEOUT if a bounded wait ran out (the status is sticky

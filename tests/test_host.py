@@ -295,6 +295,35 @@ def test_cluster_multicast_mode_is_validated():
         assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "cluster_multicast" in str(e.value)
 
 
+def test_bf16_output_and_residual_are_validated_and_routed():
+    """out_dtype and residual take 0/1; with either, only the TMA implicit-GEMM and 1x1 kernels
+    serve the conv: the 56x56 3x3 layer moves off the halo tiles, the RGB stem and depthwise and
+    int8 convs are refused."""
+    layers = {s.name: s for s in workloads.resnet50_layers(32)}
+
+    def plan(spec, **kw):
+        return cf.conv_fused_plan(cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S,
+                                               spec.stride, spec.pads, group=spec.group, **kw))[0]
+
+    halo = layers["r50_02_s0b0_3x3@b32"]
+    assert plan(halo) == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO
+    assert plan(halo, out_dtype=cf.CONVF_OUT_BF16) == cf.CONVF_VARIANT_IMPLICIT_GEMM
+    assert plan(halo, residual=1) == cf.CONVF_VARIANT_IMPLICIT_GEMM
+    assert plan(layers["r50_03_s0b0_1x1b@b32"], residual=1, out_dtype=1) == cf.CONVF_VARIANT_GEMM_1X1
+    for kw in ({"out_dtype": 1}, {"residual": 1}):
+        with pytest.raises(cf.ConvFusedError) as e:
+            plan(layers["r50_00_stem7x7@b32"], **kw)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "1x1 kernels only" in str(e.value)
+        dw = next(iter(workloads.depthwise_layers(64)))
+        with pytest.raises(cf.ConvFusedError) as e:
+            plan(dw, **kw)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED
+    for kw in ({"out_dtype": 2}, {"out_dtype": -1}, {"residual": 2}):
+        with pytest.raises(cf.ConvFusedError) as e:
+            plan(halo, **kw)
+        assert e.value.status == cf.CONVF_ERR_INVALID_ARG
+
+
 def test_stream_k_mode_is_validated():
     """stream_k takes 0 (auto: whole tiles), 1 (off) or 2 (on); anything else is refused."""
     spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_12_s1b0_3x3@b32"]   # strided: im2col
