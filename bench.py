@@ -151,13 +151,40 @@ def build_layers(specs, seed_base, torch, cf, synthetic, s8=False):
     return out
 
 
+def build_ext_layers(specs, layers, torch, cf):
+    """The ResNet-50 step with bf16 outputs (a bf16 network's activations) and the bottleneck
+    shortcut added in each block's last 1x1 conv (a bf16 residual of y's shape): the extended
+    epilogue.  A layer it cannot serve (the 3-channel stem) keeps its fp32 handle."""
+    out = []
+    for i, (spec, L) in enumerate(zip(specs, layers)):
+        inp = L["inp"]
+        scale, shift = cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5) \
+            if inp["bn"] is not None else (None, None)
+        res = "1x1b" in spec.name
+        try:
+            conv = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                                scale, shift, stride=spec.stride, pads=spec.pads, group=spec.group,
+                                act=spec.act, out_bf16=True, residual=res)
+        except cf.ConvFusedError:
+            out.append(L)
+            continue
+        y = conv.new_output()
+        r = None
+        if res:
+            g = torch.Generator().manual_seed(9000 + i)
+            r = torch.randn(tuple(y.shape), generator=g).to(torch.bfloat16).contiguous(
+                memory_format=torch.channels_last).cuda()
+        out.append({"spec": spec, "conv": conv, "x": L["x"], "y": y, "r": r})
+    return out
+
+
 def capture_graph(layers, torch, reps=1):
     """One CUDA graph that launches every layer of the sequence `reps` times, in order."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for _ in range(reps):
             for L in layers:
-                L["conv"](L["x"], L["y"])
+                L["conv"](L["x"], L["y"], r=L.get("r"))
     return g
 
 
@@ -404,6 +431,22 @@ def main():
     s8_tops = s8_ops / (s8_ms * 1e-3) / 1e12
     s8_peak = cf.conv_fused_measure_int8_mma_rate()
 
+    # the same step with bf16 outputs and the bottleneck shortcuts (extended epilogue)
+    ext_layers = build_ext_layers(specs, layers, torch, cf)
+    for _ in range(args.warmup):
+        for L in ext_layers:
+            L["conv"](L["x"], L["y"], r=L.get("r"))
+    g_ext = capture_graph(ext_layers, torch)
+    for _ in range(args.warmup):
+        g_ext.replay()
+    torch.cuda.synchronize()
+    ext_steps = max(3, args.steps // 2)
+    ext_ms = time_graph(g_ext, ext_steps, torch) / ext_steps
+    ext_bf16 = sum(1 for L in ext_layers if getattr(L["conv"], "out_bf16", False))
+    ext_res = sum(1 for L in ext_layers if L.get("r") is not None)
+    if any(L["conv"].status() != 0 for L in ext_layers):
+        raise SystemExit("device status error in the bf16-output / residual step")
+
     # end to end through the public API with host buffers (pinned), copies inside the timing
     e2e_steps = max(2, min(5, args.steps))
     for L in layers:
@@ -478,6 +521,10 @@ def main():
                      "pct_of_measured_int8_mma": s8_tops / s8_peak,
                      "peak_source": "measured live: back-to-back mma.sync.m16n8k32 s8 on register operands "
                                     "(sm_103a has no tcgen05 int8 kind)"},
+            "bf16_out_residual": {"workload": "the same 53 layers with bf16 outputs (fp32 stem) and a bf16 "
+                                              "residual added in each bottleneck's last 1x1 conv",
+                                  "ms_per_step": ext_ms, "tflops": flops_step / (ext_ms * 1e-3) / 1e12,
+                                  "bf16_layers": ext_bf16, "residual_layers": ext_res},
             "peaks": {**peaks, "source": peak_src},
             "roofline": roof,
             "cpu_baseline": cpu,

@@ -546,6 +546,25 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           // this thread's 4 channels (loaded before the transpose so their latency overlaps it)
           const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
           const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+          // EXT: the residual of this thread's eight (row, 4 channels), all eight loads in flight
+          // before the transpose (one memory latency per chunk, not one per row)
+          float4 rv[EXT ? 8 : 1];
+          if (EXT) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const int r = 4 * i + sub;
+              if (p.res == nullptr || (SK && mode == 2) || !col_ok || mt + r >= p.M) continue;
+              const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;
+              if (p.out_bf16) {
+                const uint2 rb = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
+                rv[i] = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
+                                    __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
+              } else {
+                rv[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
+              }
+            }
+          }
           // row `lane` -> smem, 16-byte chunks XOR-swizzled by row: both phases conflict-free
 #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -599,19 +618,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;   // element index
               float4 v = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
                                      fmaf(a[i].w, sc.w, bi.w));
-              if (p.res) {
-                float4 rv;
-                if (p.out_bf16) {
-                  const uint2 rb = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
-                  rv = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
-                                   __uint_as_float(rb.y << 16), __uint_as_float(rb.y & 0xffff0000u));
-                } else {
-                  rv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
-                }
-                v.x += rv.x;
-                v.y += rv.y;
-                v.z += rv.z;
-                v.w += rv.w;
+              if (EXT) {   // zero where there is no residual
+                v.x += rv[EXT ? i : 0].x;
+                v.y += rv[EXT ? i : 0].y;
+                v.z += rv[EXT ? i : 0].z;
+                v.w += rv[EXT ? i : 0].w;
               }
               v = make_float4(fminf(fmaxf(v.x, p.lo), p.hi), fminf(fmaxf(v.y, p.lo), p.hi),
                               fminf(fmaxf(v.z, p.lo), p.hi), fminf(fmaxf(v.w, p.lo), p.hi));
