@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # It describes the kernel sources it was taken on (their SHA-256 prefix) and is reported as
 # null for any other sources.
 TC_TRAFFIC = {"bytes_per_launch": 15.70e6, "read_per_launch": 12.60e6, "write_per_launch": 3.10e6,
-              "sources_sha256_16": "d546d094843c49ad"}
+              "sources_sha256_16": "8b8efce5b0b03746"}
 TC_SOURCES = ("tc_conv.cuh", "tc_conv_inst.cu", "ptx.cuh", "convf_internal.h", "api.cu")
 
 

@@ -547,9 +547,31 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
           const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
           // EXT: the residual of this thread's eight (row, 4 channels), all eight loads in flight
-          // before the transpose (one memory latency per chunk, not one per row)
+          // before the transpose (one memory latency per chunk, not one per row).  bf16 output with
+          // K % 8 == 0 (w16) maps threads to (row, 8 channels) instead, so that every load and
+          // store moves 16 bytes; its residual bits sit in rv[0..3].
+          const bool w16 = EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0;
+          const int sub8 = lane >> 2;   // w16: row within each group of eight
+          const int c8 = lane & 3;      // w16: 8-channel column group
           float4 rv[EXT ? 8 : 1];
-          if (EXT) {
+          if (EXT && w16) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const int r = 8 * i + sub8;
+              const int col = nc + 8 * c8;
+              if (p.res == nullptr || col >= left || mt + r >= p.M) continue;
+              const uint16_t* rp = static_cast<const uint16_t*>(p.res) + static_cast<size_t>(mt + r) * p.Kout + n0 + col;
+              if (col + 8 <= left) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(rp));
+                rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
+                                    __uint_as_float(q.w));
+              } else {   // the last 4 channels of the row (K % 8 == 0 leaves none; kept for safety)
+                const uint2 q = __ldg(reinterpret_cast<const uint2*>(rp));
+                rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), 0.f, 0.f);
+              }
+            }
+          } else if (EXT) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -572,6 +594,48 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 make_float4(__uint_as_float(v[h][4 * c]), __uint_as_float(v[h][4 * c + 1]),
                             __uint_as_float(v[h][4 * c + 2]), __uint_as_float(v[h][4 * c + 3]));
           __syncwarp();
+          if (EXT && w16) {
+            // bf16 output, thread = (row 8i + sub8, channels 8*c8 .. +7): two 16-byte smem reads,
+            // one 16-byte residual load (prefetched) and one 16-byte store per row
+            const int col = nc + 8 * c8;
+            const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col));
+            const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col + 4));
+            const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col));
+            const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col + 4));
+            float4 x0[4], x1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * i + sub8;
+              x0[i] = *reinterpret_cast<const float4*>(wst + r * 32 + (((2 * c8) ^ (r & 7)) << 2));
+              x1[i] = *reinterpret_cast<const float4*>(wst + r * 32 + (((2 * c8 + 1) ^ (r & 7)) << 2));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * i + sub8;
+              if (col >= left || mt + r >= p.M) continue;
+              float o[8] = {fmaf(x0[i].x, s0.x, b0.x), fmaf(x0[i].y, s0.y, b0.y), fmaf(x0[i].z, s0.z, b0.z),
+                            fmaf(x0[i].w, s0.w, b0.w), fmaf(x1[i].x, s1.x, b1.x), fmaf(x1[i].y, s1.y, b1.y),
+                            fmaf(x1[i].z, s1.z, b1.z), fmaf(x1[i].w, s1.w, b1.w)};
+              const uint32_t rb[4] = {__float_as_uint(rv[i].x), __float_as_uint(rv[i].y), __float_as_uint(rv[i].z),
+                                      __float_as_uint(rv[i].w)};
+              uint32_t pk[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                // residual (zero bits when there is none) added before the clamp, then RNE to bf16
+                const float lo = fminf(fmaxf(o[2 * j] + __uint_as_float(rb[j] << 16), p.lo), p.hi);
+                const float hi = fminf(fmaxf(o[2 * j + 1] + __uint_as_float(rb[j] & 0xffff0000u), p.lo), p.hi);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              uint16_t* yp = reinterpret_cast<uint16_t*>(p.y) + static_cast<size_t>(mt + r) * p.Kout + n0 + col;
+              if (col + 8 <= left)
+                *reinterpret_cast<uint4*>(yp) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              else
+                *reinterpret_cast<uint2*>(yp) = make_uint2(pk[0], pk[1]);
+            }
+            __syncwarp();
+            continue;
+          }
           // all eight of this thread's (row, 4 channels) read back first: the shared-memory loads
           // issue back to back instead of one load latency per row
           float4 a[8];

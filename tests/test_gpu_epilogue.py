@@ -83,6 +83,8 @@ CASES = [
     (S("res_1x1_c256_f32", 2, 256, 14, 15, 128, 1, 1), False, True, {}),
     (S("bf16out_3x3_c64", 2, 64, 12, 12, 96, 3, 3, pads=(1, 1, 1, 1), act=ACT_RELU6, bias=True), True, False, {}),
     (S("res_bf16_3x3_s2_k200", 2, 128, 15, 15, 200, 3, 3, (2, 2), (1, 1, 1, 1)), True, True, {}),
+    # K % 8 == 4: bf16 rows are not 16-byte aligned, the 4-channel (8-byte) store path serves them
+    (S("res_bf16_k100_8byte_rows", 2, 64, 9, 10, 100, 1, 1), True, True, {}),
     # more than 8 tiles per CTA: the epilogue groups take alternate tiles
     (S("res_bf16_1x1_many_tiles", 4, 128, 56, 57, 256, 1, 1), True, True, {"tile_n": 64}),
     (S("res_f32_stream_k", 2, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1)), False, True, {"stream_k": 2}),
