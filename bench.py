@@ -39,19 +39,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # so the output still in L2 when a kernel ends is not counted as written), captured with
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
 #       --clock-control none -k regex:tc_conv -s 98 -c 49 python bench.py --profile r50:0,...,52
-# It describes the kernel sources it was taken on (their SHA-256 prefix) and is reported as
-# null for any other sources.
+# It describes the kernel sources it was taken on (SHA-256 prefix of their code with comments
+# and blank space removed) and is reported as null for any other sources.
 TC_TRAFFIC = {"bytes_per_launch": 15.70e6, "read_per_launch": 12.60e6, "write_per_launch": 3.10e6,
-              "sources_sha256_16": "8b8efce5b0b03746"}
+              "sources_sha256_16": "c76090f5f2e979eb"}
 TC_SOURCES = ("tc_conv.cuh", "tc_conv_inst.cu", "ptx.cuh", "convf_internal.h", "api.cu")
 
 
-def tc_traffic():
+def sources_digest():
+    """SHA-256 prefix of the conv kernel's sources, comments and blank space removed."""
+    import re
     h = hashlib.sha256()
     for f in TC_SOURCES:
-        with open(os.path.join(ROOT, "convolution_onnx_conv_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return TC_TRAFFIC["bytes_per_launch"] if h.hexdigest()[:16] == TC_TRAFFIC["sources_sha256_16"] else None
+        with open(os.path.join(ROOT, "convolution_onnx_conv_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def tc_traffic():
+    return TC_TRAFFIC["bytes_per_launch"] if sources_digest() == TC_TRAFFIC["sources_sha256_16"] else None
 
 
 def load_peaks():

@@ -38,8 +38,8 @@ template <int BN, bool GATHER, bool PAIR>
 struct TcCfg {
   // with a CTA pair each CTA holds half of the weight tile (BN/2 rows)
   static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * kBK * 2;
-  // two epilogue warpgroups (alternate 32-column chunks) except in gather mode, whose extra
-  // warps take the register and smem room
+  // two epilogue warpgroups (alternate tiles, or the two column halves of every tile) except
+  // in gather mode, whose extra warps take the register and smem room
   static constexpr int kEpiGroups = GATHER ? 1 : 2;
   // tiles of 64+ columns: both groups can drain every tile, one column half each
   static constexpr bool kSplitEpiOk = kEpiGroups == 2 && BN >= 64;
@@ -57,11 +57,10 @@ struct TcCfg {
 
 // Work of one CTA as a sequence of segments (tile, k-blocks [ka, kend)): whole tiles tstart,
 // tstart + tstep, ... or, with stream-K, this CTA's contiguous share [it0, it1) of the
-// num_tiles x num_kb iterations cut at tile boundaries.  Every role walks the same sequence.
-// With multicast clusters (mc_rank >= 0) the sequence runs over tile pairs (an M block and two
-// neighbouring output-channel blocks) and each CTA of the pair takes its own channel block.
-// Stream-K shares are counted in pipeline steps (kpb k-blocks), so segments start and end on
-// step boundaries.
+// num_tiles x (num_kb / kpb) pipeline steps, cut at tile boundaries (so segments start and end on
+// step boundaries).  Every role walks the same sequence.  With multicast clusters
+// (mc_rank >= 0) the sequence runs over tile pairs (an M block and two neighbouring
+// output-channel blocks) and each CTA of the pair takes its own channel block.
 template <bool SK>
 struct SegSched {
   int num_kb, num_tiles, tstep, tile, mc_rank, nb, kpb, spt;
