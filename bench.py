@@ -496,22 +496,28 @@ def main():
         with open(args.layers_out, "w") as f:
             for s, L, ms in zip(specs, layers, per_layer):
                 ms /= lsteps
-                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
-                                    "tflops": s.flops / (ms * 1e-3) / 1e12,
-                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9,
-                                    "ai": s.flops / s.algorithmic_bytes}) + "\n")
+                ai = s.flops / s.algorithmic_bytes
+                # attainable: the tensor peak or the HBM bandwidth times the layer's intensity
+                att = min(peaks["bf16_tflops_sustained"], ai * peaks["hbm_gbs"] / 1e3)
+                tf = s.flops / (ms * 1e-3) / 1e12
+                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "tflops": tf,
+                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9, "ai": ai,
+                                    "attainable_tflops": att, "pct_attainable": tf / att}) + "\n")
             for s, L, ms in zip(dw_specs, dw_layers, dw_per):
                 ms /= lsteps
-                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
-                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9}) + "\n")
+                gbs = s.algorithmic_bytes / (ms * 1e-3) / 1e9
+                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "gbs": gbs,
+                                    "pct_hbm": gbs / peaks["hbm_gbs"]}) + "\n")
             for s, L, ms in zip(s8_specs, s8_layers, s8_per):
                 ms /= lsteps
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
                                     "tops": s.flops / (ms * 1e-3) / 1e12}) + "\n")
 
-    # one kernel per conv, plus the channel-padding pre-pass of gathered-row convs with few channels
-    launches_per_step = sum(1 + ("tap_channels=0" not in L["conv"].describe() and
-                                 "implicit_gemm_gather" in L["conv"].describe()) for L in layers)
+    # one kernel per conv, plus the channel-padding pre-pass of gathered-row convs with few
+    # channels and the channel/column pre-pass of the window variant
+    launches_per_step = sum(1 + (("tap_channels=0" not in L["conv"].describe() and
+                                  "implicit_gemm_gather" in L["conv"].describe()) or
+                                 "implicit_gemm_window" in L["conv"].describe()) for L in layers)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
