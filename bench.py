@@ -63,6 +63,24 @@ def tc_traffic():
     return TC_TRAFFIC["bytes_per_launch"] if sources_digest() == TC_TRAFFIC["sources_sha256_16"] else None
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (each replica's measured time), so the job is timed by its
+    slowest replica; x itself on one rank."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_step, steps, ms):
+    """Replicas (weak scaling): every rank runs the whole step on its own GPU, so the job does
+    world x the work of one step per step in `ms` milliseconds."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -406,12 +424,9 @@ def main():
     if any(s != 0 for s in statuses):
         raise SystemExit(f"device status error: {statuses}")
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     flops_step = sum(s.flops for s in specs)
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
     # dominant kernel: the tcgen05 implicit-GEMM conv (49 of the 53 layers: every 1x1 and every
@@ -479,10 +494,7 @@ def main():
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_val = world * flops_step * e2e_steps / (float(te.item()) * 1e-3) / 1e12
+    e2e_val = whole_job_tflops(world, flops_step, e2e_steps, max_over_ranks(e0.elapsed_time(e1), world, "cuda"))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
