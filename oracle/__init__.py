@@ -28,6 +28,18 @@ Every function is the plain definition of one stage, kept separate on purpose:
     ReLU = max(u, 0); ReLU6 = min(max(u, 0), 6), the two clamps of the
     residual + batchnorm + relu6 example kernel in the "Kyanite" README
     (section "Cuda Executor"); Clip(lo, hi) generally.
+``qlinear_conv_acc`` / ``qlinear_requant``
+    ONNX QLinearConv (public operator specification): uint8 or int8 x and w
+    with zero points (w's per output channel), integer sums of the corrected
+    operands ``sum (x - x_zp)(w - w_zp[k]) + B[k]`` (the quantized input pads
+    with its zero point, so padded taps add nothing), then
+    ``y = saturate(round_half_even(acc * x_scale * w_scale[k] / y_scale) + y_zp)``.
+    The scale product is taken in float64 on the float32 scales (a reading: the
+    specification fixes no precision for it).  The oracle subtracts the zero
+    points before multiplying; the expanded form of the same sums is the
+    zero-point correction identity the "onnx-vulkan-rs" page gives, in its notes
+    on the quantized kernels, for blocks of four products (the tests check one
+    against the other).
 ``conv2d_s8`` / ``requant_s8``
     The static-int8 path ("onnx-vulkan-rs", feature list: static int8
     convolutions on the tensor cores; ConvInteger via im2col): exact integer
@@ -70,6 +82,9 @@ def _lib():
         lib.oracle_requant_s8.argtypes = [i64p, i64p, ctypes.c_int64, i32p, i32p, i32p,
                                           ctypes.c_int32, ctypes.c_int, i8p]
         lib.oracle_conv2d_f32acc.argtypes = [fp, fp, fp] + ints + [fp]
+        i16p = ctypes.POINTER(ctypes.c_int16)
+        lib.oracle_conv2d_i16.argtypes = [i16p, i16p] + ints + [i64p]
+        lib.oracle_conv2d_i16.restype = ctypes.c_int
         lib.oracle_out_extent.argtypes = [ctypes.c_long] * 6
         lib.oracle_out_extent.restype = ctypes.c_long
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -288,6 +303,56 @@ def requant_s8(acc, chan, bias, mult, shift, zero_point=0, relu=False):
     if rc != 0:
         raise ValueError("oracle_requant_s8 rejected its arguments")
     return out.reshape(shape)
+
+
+# ------------------------------------------------------------ QLinearConv path
+
+def _per_channel(v, K, dtype):
+    v = np.asarray(v, dtype=dtype).reshape(-1)
+    if v.size == 1:
+        return np.full(K, v[0], dtype=dtype)
+    if v.size != K:
+        raise ValueError(f"per-channel parameter has {v.size} entries for {K} output channels")
+    return v
+
+
+def qlinear_conv_acc(x, x_zero_point, w, w_zero_point, bias=None, strides=(1, 1), pads=(0, 0, 0, 0),
+                     dilations=(1, 1), group=1):
+    """Integer sums sum (x - x_zp)(w - w_zp[k]) (+ B[k]) of ONNX QLinearConv, int64 [N][K][Ho][Wo].
+
+    x, w: uint8 or int8 arrays (NCHW, KCRS); x_zero_point a scalar; w_zero_point a scalar or one
+    per output channel; bias int32[K] or None.
+    """
+    x = np.asarray(x)
+    w = np.asarray(w)
+    for a in (x, w):
+        if a.dtype not in (np.uint8, np.int8):
+            raise ValueError("QLinearConv operands are uint8 or int8")
+    K = w.shape[0]
+    xd = np.ascontiguousarray(x.astype(np.int16) - np.int16(int(x_zero_point)))
+    wz = _per_channel(w_zero_point, K, np.int16)
+    wd = np.ascontiguousarray(w.astype(np.int16) - wz.reshape((K,) + (1,) * (w.ndim - 1)))
+    dims = _dims(xd.shape, wd.shape, strides, pads, dilations, group)
+    Ho, Wo = out_hw(dims[2], dims[3], dims[5], dims[6], strides, pads, dilations)
+    acc = np.empty((dims[0], dims[4], Ho, Wo), dtype=np.int64)
+    rc = _lib().oracle_conv2d_i16(_ptr(xd, ctypes.c_int16), _ptr(wd, ctypes.c_int16), *dims,
+                                  _ptr(acc, ctypes.c_int64))
+    if rc != 0:
+        raise ValueError("oracle_conv2d_i16 rejected its arguments")
+    if bias is not None:
+        acc += np.asarray(bias, dtype=np.int64).reshape(1, K, 1, 1)
+    return acc
+
+
+def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uint8):
+    """y = saturate(round_half_even(acc * x_scale * w_scale[k] / y_scale) + y_zp) for NCHW acc."""
+    acc = np.asarray(acc, dtype=np.int64)
+    K = acc.shape[1]
+    ws = _per_channel(w_scale, K, np.float32).astype(np.float64)
+    m = np.float64(np.float32(x_scale)) * ws / np.float64(np.float32(y_scale))
+    v = np.rint(acc.astype(np.float64) * m.reshape(1, K, 1, 1)) + int(y_zero_point)
+    info = np.iinfo(y_dtype)
+    return np.clip(v, info.min, info.max).astype(y_dtype)
 
 
 # ------------------------------------------------------------- whole pipeline

@@ -163,6 +163,55 @@ static int64_t oracle_conv_point_s8(const int8_t *x, const int8_t *w,
     return acc;
 }
 
+/* Zero-point-corrected operands (x - x_zero_point, w - w_zero_point[k], int16): the padding of a
+ * quantized input holds its zero point, so a padded tap contributes (zp - zp) * w = 0 and is
+ * skipped exactly like the zero padding above. */
+static int64_t oracle_conv_point_i16(const int16_t *x, const int16_t *w,
+                                     int C, int H, int W, int K, int R, int S,
+                                     int sh, int sw, int pt, int pl, int dh, int dw, int group,
+                                     long n, long k, long oh, long ow)
+{
+    const long Cg = C / group;
+    const long Kg = K / group;
+    const long g = k / Kg;
+    int64_t acc = 0;
+    for (long c = 0; c < Cg; ++c) {
+        const long ci = g * Cg + c;
+        for (long r = 0; r < R; ++r) {
+            const long ih = oh * sh - pt + r * dh;
+            if (ih < 0 || ih >= H) continue;
+            for (long s = 0; s < S; ++s) {
+                const long iw = ow * sw - pl + s * dw;
+                if (iw < 0 || iw >= W) continue;
+                acc += (int64_t)x[((n * C + ci) * H + ih) * W + iw] *
+                       (int64_t)w[((k * Cg + c) * R + r) * S + s];
+            }
+        }
+    }
+    return acc;
+}
+
+/* Exact integer conv of zero-point-corrected operands: acc[N][K][Ho][Wo] (int64, no bias). */
+int oracle_conv2d_i16(const int16_t *x, const int16_t *w,
+                      int N, int C, int H, int W, int K, int R, int S,
+                      int sh, int sw, int pt, int pl, int pb, int pr,
+                      int dh, int dw, int group, int64_t *acc)
+{
+    long Ho, Wo;
+    if (!oracle_check(N, C, H, W, K, R, S, sh, sw, pt, pl, pb, pr, dh, dw, group, &Ho, &Wo))
+        return ORACLE_BAD_ARGS;
+    long n, k;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (n = 0; n < N; ++n)
+        for (k = 0; k < K; ++k)
+            for (long oh = 0; oh < Ho; ++oh)
+                for (long ow = 0; ow < Wo; ++ow)
+                    acc[((n * K + k) * Ho + oh) * Wo + ow] =
+                        oracle_conv_point_i16(x, w, C, H, W, K, R, S, sh, sw, pt, pl, dh, dw,
+                                              group, n, k, oh, ow);
+    return ORACLE_OK;
+}
+
 /* Exact integer conv: acc[N][K][Ho][Wo] = sum x * w (int64, no bias). */
 int oracle_conv2d_s8(const int8_t *x, const int8_t *w,
                      int N, int C, int H, int W, int K, int R, int S,

@@ -453,3 +453,82 @@ def test_residual_pipeline_matches_torch_on_tiny_cases():
         yp = oracle.conv_bn_act_points(x, w, b, bn, oracle.ACT_RELU6, stride, (1, 1, 1, 1), (1, 1), 1, pts,
                                        residual=r)
         assert np.allclose(yp, ref[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------- QLinearConv (zero points)
+
+def _windows(xp, R, S, sh, sw, Ho, Wo):
+    """im2col of an already padded NCHW input: [N][C][R][S][Ho][Wo]."""
+    N, C = xp.shape[:2]
+    out = np.empty((N, C, R, S, Ho, Wo), dtype=xp.dtype)
+    for r in range(R):
+        for s in range(S):
+            out[:, :, r, s] = xp[:, :, r: r + sh * (Ho - 1) + 1: sh, s: s + sw * (Wo - 1) + 1: sw]
+    return out
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_qlinear_sums_match_the_zero_point_identity(case):
+    """The page's expansion sum (a - az)(b - bz) = sum ab - az sum b - bz sum a + n az bz, taken over
+    every tap of the zero-point-padded input (n = C*R*S), against the oracle's direct sums."""
+    rng = np.random.default_rng(50 + case)
+    N, C, K, H, W = 2, int(rng.integers(1, 5)), int(rng.integers(1, 5)), 6, 7
+    R = S = 3
+    st = (1 + case % 2, 1 + (case // 2) % 2)
+    pads = (1, 1, 1, 1) if case % 3 else (0, 1, 2, 0)
+    xu = case % 2 == 0                                 # uint8 or int8 activations
+    x = (rng.integers(0, 256, (N, C, H, W)).astype(np.uint8) if xu
+         else rng.integers(-128, 128, (N, C, H, W)).astype(np.int8))
+    w = rng.integers(-127, 128, (K, C, R, S)).astype(np.int8)
+    zx = int(rng.integers(0, 256)) if xu else int(rng.integers(-128, 128))
+    zw = rng.integers(-20, 21, K)
+    bias = rng.integers(-5000, 5000, K).astype(np.int32)
+    acc = oracle.qlinear_conv_acc(x, zx, w, zw, bias, st, pads)
+    pt, pl, pb, pr = pads
+    xp = np.full((N, C, H + pt + pb, W + pl + pr), zx, dtype=np.int64)
+    xp[:, :, pt:pt + H, pl:pl + W] = x
+    Ho, Wo = acc.shape[2:]
+    cols = _windows(xp, R, S, st[0], st[1], Ho, Wo).reshape(N, C * R * S, Ho, Wo)
+    wf = w.reshape(K, -1).astype(np.int64)
+    n = C * R * S
+    sum_ab = np.einsum("kj,njhw->nkhw", wf, cols)
+    sum_a = cols.sum(axis=1)[:, None]                 # over the input taps, per output position
+    sum_b = wf.sum(axis=1)[None, :, None, None]
+    zwk = zw.reshape(1, K, 1, 1)
+    ident = sum_ab - zx * sum_b - zwk * sum_a + n * zx * zwk + bias.reshape(1, K, 1, 1)
+    assert np.array_equal(acc, ident)
+
+
+def test_qlinear_without_zero_points_is_the_int8_sum():
+    rng = np.random.default_rng(60)
+    x = rng.integers(-128, 128, (2, 5, 7, 6)).astype(np.int8)
+    w = rng.integers(-127, 128, (4, 5, 3, 3)).astype(np.int8)
+    acc = oracle.qlinear_conv_acc(x, 0, w, 0, None, (2, 1), (1, 0, 1, 2))
+    assert np.array_equal(acc, oracle.conv2d_s8(x, w, (2, 1), (1, 0, 1, 2)))
+
+
+def test_qlinear_input_at_its_zero_point_leaves_the_bias():
+    """x == x_zp everywhere: every corrected product is 0, so y = saturate(rint(B*m) + y_zp)."""
+    rng = np.random.default_rng(61)
+    zx = 117
+    x = np.full((1, 3, 5, 5), zx, dtype=np.uint8)
+    w = rng.integers(-127, 128, (6, 3, 3, 3)).astype(np.int8)
+    bias = np.array([-400, -3, 0, 7, 250, 90000], dtype=np.int32)
+    acc = oracle.qlinear_conv_acc(x, zx, w, rng.integers(-3, 4, 6), bias, (1, 1), (1, 1, 1, 1))
+    assert np.array_equal(acc, np.broadcast_to(bias.reshape(1, 6, 1, 1), acc.shape))
+    y = oracle.qlinear_requant(acc, 0.25, 0.5, 1.0, 100)          # m = 1/8, y_zp = 100
+    # -400/8 = -50 -> 50; -3/8 -> -0 -> 100; 0 -> 100; 7/8 -> 1 -> 101; 250/8 = 31.25 -> 131;
+    # 90000/8 = 11250 -> saturates at 255
+    assert y[0, :, 0, 0].tolist() == [50, 100, 100, 101, 131, 255]
+
+
+def test_qlinear_requant_rounds_half_to_even_and_saturates():
+    acc = np.array([1, 3, 5, -1, -3, 7, 1000, -1000], dtype=np.int64).reshape(1, 8, 1, 1)
+    y = oracle.qlinear_requant(acc, 0.5, 1.0, 1.0, 0, np.int8)     # m = 0.5
+    assert y.reshape(-1).tolist() == [0, 2, 2, 0, -2, 4, 127, -128]
+    y = oracle.qlinear_requant(acc, 0.5, 1.0, 1.0, 3, np.uint8)
+    assert y.reshape(-1).tolist() == [3, 5, 5, 3, 1, 7, 255, 0]
+    # per-channel weight scales: channel k scales by k + 1
+    acc = np.full((1, 3, 1, 1), 10, dtype=np.int64)
+    y = oracle.qlinear_requant(acc, 0.5, np.array([1.0, 2.0, 3.0], np.float32), 2.0, 0, np.int8)
+    assert y.reshape(-1).tolist() == [2, 5, 8]                      # 2.5 -> 2, 5, 7.5 -> 8
