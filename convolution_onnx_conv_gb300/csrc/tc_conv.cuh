@@ -58,16 +58,14 @@ struct TcCfg {
 // Work of one CTA as a sequence of segments (tile, k-blocks [ka, kend)): whole tiles tstart,
 // tstart + tstep, ... or, with stream-K, this CTA's contiguous share [it0, it1) of the
 // num_tiles x (num_kb / kpb) pipeline steps, cut at tile boundaries (so segments start and end on
-// step boundaries).  Every role walks the same sequence.  With multicast clusters
-// (mc_rank >= 0) the sequence runs over tile pairs (an M block and two neighbouring
-// output-channel blocks) and each CTA of the pair takes its own channel block.
+// step boundaries).  Every role walks the same sequence.
 template <bool SK>
 struct SegSched {
-  int num_kb, num_tiles, tstep, tile, mc_rank, nb, kpb, spt;
+  int num_kb, num_tiles, tstep, tile, kpb, spt;
   long long it, it1;
-  __device__ SegSched(const TcConvParams& p, int tstart, int tstep_, int mc_rank_ = -1)
-      : num_kb(p.num_kb), num_tiles(mc_rank_ >= 0 ? p.num_tiles / 2 : p.num_tiles), tstep(tstep_), tile(tstart),
-        mc_rank(mc_rank_), nb(p.n_blocks), kpb(p.kpb), spt(p.num_kb / p.kpb), it(0), it1(0) {
+  __device__ SegSched(const TcConvParams& p, int tstart, int tstep_)
+      : num_kb(p.num_kb), num_tiles(p.num_tiles), tstep(tstep_), tile(tstart), kpb(p.kpb), spt(p.num_kb / p.kpb),
+        it(0), it1(0) {
     if (SK) {
       const long long total = static_cast<long long>(p.num_tiles) * spt;
       it = total * blockIdx.x / gridDim.x;
@@ -78,10 +76,6 @@ struct SegSched {
     if (!SK) {
       if (tile >= num_tiles) return false;
       t = tile;
-      if (mc_rank >= 0) {
-        const int hp = nb >> 1;
-        t = (tile / hp) * nb + 2 * (tile % hp) + mc_rank;
-      }
       ka = 0;
       kend = num_kb;
       tile += tstep;
@@ -102,13 +96,12 @@ struct SegSched {
 // EXT: the epilogue adds a residual and/or stores bf16 (TcConvParams::res, out_bf16); its own
 // instantiation, so the plain fp32 epilogue keeps its code (a shared one cost 1.3% of the
 // ResNet-50 step).
-template <int BN, bool GATHER, bool PAIR, bool SK, bool MC, bool EXT>
+template <int BN, bool GATHER, bool PAIR, bool SK, bool EXT>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
-  static_assert(!(MC && (GATHER || PAIR || SK)), "multicast clusters run whole tiles with TMA activation loads");
   static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
   // TcConvParams::split_epi on whole tiles of 64+ columns: both epilogue groups drain every
@@ -118,16 +111,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   const bool split_epi = Cfg::kSplitEpiOk && !SK && p.split_epi;
   // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
   // both CTAs' TMEM; each CTA loads its own 128 activation rows and half of the weight tile.
-  // Multicast cluster of 2 (MC): the two CTAs compute the same 128 rows for two neighbouring
-  // output-channel blocks; each activation tile is loaded once, by one of them, and multicast
-  // into both CTAs' shared memory (half the activation TMA operations and L2 reads per CTA).
-  // Every CTA issues its own MMAs; a stage is reused only after both CTAs' MMAs released it.
-  const uint32_t crank = (PAIR || MC) ? cluster_ctarank() : 0;
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
   const bool leader = !PAIR || crank == 0;
-  const int mc_rank = MC ? static_cast<int>(crank) : -1;
   constexpr int kTileM = PAIR ? 2 * kBM : kBM;
-  const int tstart = (PAIR || MC) ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int tstep = (PAIR || MC) ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int tstart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int mrow_off = PAIR ? static_cast<int>(crank) * kBM : 0;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -157,7 +145,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       // weight producer + (activation producer | one arrival per gather warp)
       mbar_init(&full[s], GATHER ? 1 + kGatherThreads / 32 : 2);
-      mbar_init(&empty[s], MC ? 2 : 1);   // MC: both CTAs' MMAs release a stage
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -184,7 +172,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR || MC) cluster_sync();   // the peer's barriers and TMEM exist before any cross-CTA operation
+  if (PAIR) cluster_sync();   // the peer's barriers and TMEM exist before any cross-CTA operation
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // setup above touched only smem/TMEM: overlap it with the previous kernel's tail
@@ -199,9 +187,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   // producer warps (even k-blocks on warp 0, odd ones on warp 2).
   const int kpb = GATHER ? 1 : p.kpb;
   const bool a3d = !GATHER && p.a3d;
-  // MC: warp 0 issues this CTA's half of the activation loads and expects all of them
-  const bool a_odd = !GATHER && !MC && !a3d && kpb > 1;
-  const uint32_t a_bytes0 = static_cast<uint32_t>((a3d || MC ? kpb : (kpb + 1) / 2) * kATileBytes);
+  const bool a_odd = !GATHER && !a3d && kpb > 1;
+  const uint32_t a_bytes0 = static_cast<uint32_t>((a3d ? kpb : (kpb + 1) / 2) * kATileBytes);
   const uint32_t b_bytes2 = static_cast<uint32_t>(kpb * Cfg::kBTileBytes + (a_odd ? kpb / 2 : 0) * kATileBytes);
   // first output pixel's input window origin (im2col mode)
   auto tile_origin = [&](int m0, int& img, int& hb, int& wb) {
@@ -257,15 +244,6 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     }
   };
 
-  // the same tile multicast into both CTAs of an MC cluster
-  auto load_a_mc = [&](int kb, const KPos& q, uint8_t* dA, uint64_t* bar, int m0, int img, int hb, int wb) {
-    if (p.a_mode == kA2D)
-      tma_load_2d_mc(dA, &tmA, bar, kb * kBK, m0, 3);
-    else
-      tma_load_im2col_4d_mc(dA, &tmA, bar, q.cb * kBK, wb, hb, img, static_cast<uint16_t>(q.s * p.dw),
-                            static_cast<uint16_t>(q.r * p.dh), 3);
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------------ activation producer
     // (TMA activation tiles; in gather mode the per-tile input-row bulk copies instead)
@@ -273,7 +251,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      SegSched<SK> sched(p, tstart, tstep, mc_rank);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       for (; sched.next(tile, ka, kend); ++it) {
         const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
@@ -305,20 +283,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           // a pair's loads all complete on the leader's barrier, which expects both CTAs' bytes
           if (!PAIR || leader)
             mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * a_bytes0 : a_bytes0);
-          if (MC) {
-            // this CTA's half: whole steps (one box each) or single k-blocks, by parity; the
-            // peer issues the other half into both CTAs
-            if (a3d) {
-              if (((kb / kpb) & 1) == static_cast<int>(crank))
-                tma_load_3d_mc(sA + stage * kATileBytes, &tmA, &full[stage], 0, m0, kb, 3);
-            } else {
-              for (int j = 0; j < kpb; ++j) {
-                if (((kb + j) & 1) == static_cast<int>(crank))
-                  load_a_mc(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
-                kpos_next(q);
-              }
-            }
-          } else if (a3d) {
+          if (a3d) {
             if (PAIR)
               tma_load_3d_pair(sA + stage * kATileBytes, &tmA, map_to_rank(smem_u32(&full[stage]), 0), 0, m0, kb);
             else
@@ -343,7 +308,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      SegSched<SK> sched(p, tstart, tstep, mc_rank);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
         const int n0 = (tile % p.n_blocks) * BN;
@@ -391,7 +356,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      SegSched<SK> sched(p, tstart, tstep, mc_rank);
+      SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
@@ -419,8 +384,6 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           }
           if (PAIR)
             tc_commit_pair(&empty[stage], 3);
-          else if (MC)
-            tc_commit_mc(&empty[stage], 3);
           else
             tc_commit(&empty[stage]);
           stage += kpb;
@@ -464,7 +427,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     // alternate whole tiles: group eg visits only its own tiles; split columns: every tile;
     // stream-K: every segment, keeping its own
     const bool kAll = SK || split_epi;
-    SegSched<SK> sched(p, tstart + (kAll ? 0 : eg * tstep), kAll ? tstep : G * tstep, mc_rank);
+    SegSched<SK> sched(p, tstart + (kAll ? 0 : eg * tstep), kAll ? tstep : G * tstep);
     int tile, ka, kend;
     for (int seg = kAll ? 0 : eg; sched.next(tile, ka, kend); seg += kAll ? 1 : G) {
       if (SK && seg % G != eg) continue;
@@ -876,7 +839,7 @@ teardown:
     for (int i = 0; i < 2000; ++i) __nanosleep(100000);
   }
   __syncthreads();
-  if (PAIR || MC) cluster_sync();   // no CTA of the pair leaves while the other may still signal it
+  if (PAIR) cluster_sync();   // no CTA of the pair leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -887,11 +850,11 @@ teardown:
   }
 }
 
-template <int BN, bool GATHER, bool PAIR, bool SK = false, bool MC = false, bool EXT = false>
+template <int BN, bool GATHER, bool PAIR, bool SK = false, bool EXT = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, MC, EXT>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXT>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcCfg<BN, GATHER, PAIR>::kSmem);
@@ -903,7 +866,7 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
     configured = true;
   }
   return launch_pdl(k, dim3(grid), dim3(TcCfg<BN, GATHER, PAIR>::kThreads), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
-                    (PAIR || MC) ? 2 : 1, p, tmA, tmB);
+                    PAIR ? 2 : 1, p, tmA, tmB);
 }
 
 }  // namespace convf

@@ -11,18 +11,12 @@
 namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
                                                    const CUtensorMap& tmB, int grid,
-                                                   bool gather, bool pair, bool mc, cudaStream_t stream) {
+                                                   bool gather, bool pair, cudaStream_t stream) {
   if (p.res != nullptr || p.out_bf16) {
     // residual and/or bf16 output: the extended-epilogue instantiations
     if (gather) return cudaErrorInvalidValue;
-    if (mc) return launch_tc_conv_t<CONVF_BN, false, false, false, true, true>(p, tmA, tmB, grid, stream);
-    if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, false, true>(p, tmA, tmB, grid, stream);
-    if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, false, true>(p, tmA, tmB, grid, stream);
-    return launch_tc_conv_t<CONVF_BN, false, false, false, false, true>(p, tmA, tmB, grid, stream);
-  }
-  if (mc) {
-    // multicast clusters: single-CTA MMAs, whole tiles, TMA activation loads only
-    if (gather || pair || p.sk) return cudaErrorInvalidValue;
+    if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, true>(p, tmA, tmB, grid, stream);
+    if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, true>(p, tmA, tmB, grid, stream);
     return launch_tc_conv_t<CONVF_BN, false, false, false, true>(p, tmA, tmB, grid, stream);
   }
   if (p.sk) {

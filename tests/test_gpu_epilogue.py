@@ -89,8 +89,7 @@ CASES = [
     (S("res_bf16_1x1_many_tiles", 4, 128, 56, 57, 256, 1, 1), True, True, {"tile_n": 64}),
     (S("res_f32_stream_k", 2, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1)), False, True, {"stream_k": 2}),
     (S("res_bf16_cta_pair", 2, 128, 12, 12, 128, 3, 3, pads=(1, 1, 1, 1)), True, True, {"cta_pair": 2}),
-    (S("bf16out_multicast", 2, 128, 12, 12, 256, 3, 3, pads=(1, 1, 1, 1)), True, False,
-     {"cluster_multicast": 2, "tile_n": 128}),
+    (S("bf16out_tile128_k256", 2, 128, 12, 12, 256, 3, 3, pads=(1, 1, 1, 1)), True, False, {"tile_n": 128}),
 ]
 
 

@@ -281,20 +281,6 @@ def test_kblocks_per_step_is_validated():
         assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "kblocks_per_step" in str(e.value)
 
 
-def test_cluster_multicast_mode_is_validated():
-    spec = {s.name: s for s in workloads.resnet50_layers(32)}["r50_44_s3b0_3x3@b32"]
-    for m in (0, 1, 2):
-        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
-                         cluster_multicast=m)
-        assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_IMPLICIT_GEMM
-    for m in (-1, 3):
-        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
-                         cluster_multicast=m)
-        with pytest.raises(cf.ConvFusedError) as e:
-            cf.conv_fused_plan(d)
-        assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "cluster_multicast" in str(e.value)
-
-
 def test_bf16_output_and_residual_are_validated_and_routed():
     """out_dtype and residual take 0/1; with either, only the TMA implicit-GEMM and 1x1 kernels
     serve the conv: the 56x56 3x3 layer moves off the halo tiles, the RGB stem and depthwise and
