@@ -44,13 +44,13 @@ class ConvDesc(ctypes.Structure):
                 ("act", ctypes.c_int), ("clip_lo", ctypes.c_float), ("clip_hi", ctypes.c_float),
                 ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("kblocks_per_step", ctypes.c_int),
-                ("cluster_multicast", ctypes.c_int), ("out_dtype", ctypes.c_int), ("residual", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("residual", ctypes.c_int)]
 
 
 def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1,
               dtype=CONVF_BF16, act=CONVF_ACT_NONE, clip=(0.0, 6.0), auto_pad="NOTSET",
               variant=CONVF_VARIANT_AUTO, layout=CONVF_NHWC, tile_n=0, cta_pair=0, stream_k=0,
-              kblocks_per_step=0, cluster_multicast=0, out_dtype=CONVF_OUT_F32, residual=0) -> ConvDesc:
+              kblocks_per_step=0, out_dtype=CONVF_OUT_F32, residual=0) -> ConvDesc:
     d = ConvDesc()
     d.N, d.C, d.H, d.W, d.K, d.R, d.S = N, C, H, W, K, R, S
     d.stride[:] = list(stride)
@@ -67,7 +67,6 @@ def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1
     d.cta_pair = cta_pair
     d.stream_k = stream_k
     d.kblocks_per_step = kblocks_per_step
-    d.cluster_multicast = cluster_multicast
     d.out_dtype = out_dtype
     d.residual = residual
     return d
@@ -272,14 +271,13 @@ class FusedConv:
     def __init__(self, N, C, H, W, K, R, S, w, bias=None, bn_scale=None, bn_shift=None, stride=(1, 1),
                  pads=(0, 0, 0, 0), dilation=(1, 1), group=1, act=CONVF_ACT_NONE, clip=(0.0, 6.0),
                  auto_pad="NOTSET", variant=CONVF_VARIANT_AUTO, requant_mult=None, requant_shift=None,
-                 out_zero_point=0, tile_n=0, cta_pair=0, stream_k=0, kblocks_per_step=0, cluster_multicast=0,
+                 out_zero_point=0, tile_n=0, cta_pair=0, stream_k=0, kblocks_per_step=0,
                  out_bf16=False, residual=False):
         import torch
         s8 = w.dtype == torch.int8
         self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group,
                               CONVF_S8 if s8 else CONVF_BF16, act, clip, auto_pad, variant, tile_n=tile_n,
                               cta_pair=cta_pair, stream_k=stream_k, kblocks_per_step=kblocks_per_step,
-                              cluster_multicast=cluster_multicast,
                               out_dtype=CONVF_OUT_BF16 if out_bf16 else CONVF_OUT_F32, residual=int(bool(residual)))
         self.out_bf16 = bool(out_bf16)
         self.residual = bool(residual)

@@ -20,13 +20,13 @@
 
 namespace convf {
 // defined once per tile width in tc_conv_inst.cu
-cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool, bool,
+cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
                                cudaStream_t);
 }  // namespace convf
 
@@ -155,9 +155,6 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "stream_k=%d is not 0 (auto), 1 (off) or 2 (on)", d->stream_k);
   if (d->kblocks_per_step < 0 || d->kblocks_per_step > 4)
     return fail(CONVF_ERR_INVALID_ARG, "kblocks_per_step=%d is not 0 (auto) or 1..4", d->kblocks_per_step);
-  if (d->cluster_multicast < 0 || d->cluster_multicast > 2)
-    return fail(CONVF_ERR_INVALID_ARG, "cluster_multicast=%d is not 0 (auto), 1 (off) or 2 (on)",
-                d->cluster_multicast);
   if (d->out_dtype != CONVF_OUT_F32 && d->out_dtype != CONVF_OUT_BF16)
     return fail(CONVF_ERR_INVALID_ARG, "out_dtype=%d is not CONVF_OUT_F32 (0) or CONVF_OUT_BF16 (1)", d->out_dtype);
   if (d->residual != 0 && d->residual != 1)
@@ -527,7 +524,6 @@ struct convf_handle {
   bool sk;          // stream-K work split
   int kpb;          // k-blocks per pipeline step (TcConvParams::kpb)
   bool a3d;         // 1x1 activation map is 3-D {64, M, C/64} (one box per step)
-  bool mc;          // clusters of two CTAs on neighbouring channel blocks share activation tiles
   float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
   int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
   WinGeom wg;       // window variant geometry
@@ -845,22 +841,6 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       }
     }
     h->a3d = h->a_mode == kA2D && !gather && h->kpb > 1 && s.C % 64 == 0;
-    {
-      const int nb = (s.K + h->bn - 1) / h->bn;
-      const bool mc_ok = !gather && !h->pair && !h->sk && nb % 2 == 0;
-      h->mc = false;
-      if (desc->cluster_multicast == 2) {
-        if (!mc_ok) {
-          delete h;
-          return fail(CONVF_ERR_UNSUPPORTED,
-                      "cluster_multicast needs single-CTA whole tiles with TMA activation loads and an even "
-                      "number of %d-wide output-channel blocks (%d here)", h->bn, nb);
-        }
-        h->mc = true;
-      }
-      // automatic choice: off (measured 3-8% slower than single CTAs on every ResNet-50 layer
-      // tried: halving the activation loads does not help once the MMA issue is the bound)
-    }
     if (h->sk) {
       o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
       o_skflags = carve((size_t)h->num_sms * sizeof(int));
@@ -1007,7 +987,6 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     const long long tiles = (s.M + tile_m - 1) / tile_m * h->n_blocks;
     h->num_tiles = (int)tiles;
     h->grid = h->pair ? 2 * (int)std::min<long long>(tiles, h->num_sms / 2)
-              : h->mc ? 2 * (int)std::min<long long>(tiles / 2, h->num_sms / 2)
                       // stream-K: every CTA needs at least one pipeline step of its own (a CTA
                       // with an empty share would be waited for as a contributor)
                       : (int)std::min<long long>(h->sk ? tiles * (h->num_kb / h->kpb) : tiles, h->num_sms);
@@ -1220,10 +1199,10 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.split_epi = h->num_tiles <= 8LL * h->grid ? 1 : 0;
       const bool gather = h->a_mode == kAGather;
       switch (h->bn) {
-        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
-        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
-        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
-        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, h->mc, strm); break;
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
       }
     }
   }
@@ -1303,10 +1282,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
-             "kblocks_per_step=%d act_box_per_step=%d cluster_multicast=%d split_epilogue=%d out=%s residual=%d "
+             "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d out=%s residual=%d "
              "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
-             h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0, h->mc ? 1 : 0,
+             h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0,
              (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0,
              h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->num_tiles,
              h->grid, h->patch_rows, h->cpt, h->dev_bytes);
@@ -1385,6 +1364,14 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
                 "inside one image and whose input rows fit the 32 KB staging buffer");
   if (desc->tile_n > 128 || desc->cta_pair == 2)
     return fail(CONVF_ERR_UNSUPPORTED, "tile_n > 128 / CTA pairs are not served by the gathered-row kernel");
+  if (desc->stream_k == 2)
+    return fail(CONVF_ERR_UNSUPPORTED, "stream_k = 2 (on) is not served by the allocation-free run: it has no "
+                                       "workspace for partial tiles");
+  if (desc->kblocks_per_step > 1)
+    return fail(CONVF_ERR_UNSUPPORTED, "kblocks_per_step = %d is not served by the gathered-row kernel (one "
+                                       "reduction block per step)", desc->kblocks_per_step);
+  if (desc->out_dtype != CONVF_OUT_F32 || desc->residual)
+    return fail(CONVF_ERR_UNSUPPORTED, "the allocation-free run writes fp32 outputs without a residual");
   // scratch layout: [padded x][scale, padded to 256][bias, padded to 256][status word]; every
   // size refusal comes before any pointer is looked at
   const int Kpad = (int)align_up((size_t)s.K, 256);
@@ -1415,8 +1402,9 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
                            : reinterpret_cast<int*>(base + xpad_bytes + 2 * vec_bytes);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
 
-  // the epilogue reads whole 32-column chunks: copy the vectors and zero their padding
-  if ((ce = cudaMemsetAsync(sc, 0, 2 * vec_bytes, strm)) != cudaSuccess ||
+  // the epilogue reads whole 32-column chunks: copy the vectors and zero their padding; the
+  // internal status word (used when status_dev is NULL) starts every call at zero
+  if ((ce = cudaMemsetAsync(sc, 0, 2 * vec_bytes + 256, strm)) != cudaSuccess ||
       (ce = cudaMemcpyAsync(sc, scale, (size_t)s.K * sizeof(float), cudaMemcpyDeviceToDevice, strm)) != cudaSuccess ||
       (ce = cudaMemcpyAsync(bi, bias, (size_t)s.K * sizeof(float), cudaMemcpyDeviceToDevice, strm)) != cudaSuccess)
     return fail(CONVF_ERR_CUDA, "scratch set-up copy failed: %s", cudaGetErrorString(ce));
@@ -1458,9 +1446,9 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status; p.y = static_cast<float*>(y);
   p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
   switch (bn) {
-    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, false, strm); break;
-    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, false, strm); break;
-    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, false, strm); break;
+    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, strm); break;
+    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, strm); break;
+    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, strm); break;
   }
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();

@@ -131,11 +131,6 @@ typedef struct {
                               weights are one TMA box, and so are its activations in the 1x1 mode
                               when C % 64 == 0; more bytes per TMA operation raise the operand
                               ingest rate.  Ignored where it does not apply. */
-  int cluster_multicast;   /* TMA implicit-GEMM variants on single CTAs without stream-K: 0 = auto,
-                              1 = off, 2 = on (refused with CONVF_ERR_UNSUPPORTED unless the
-                              output channels form an even number of tile_n blocks): clusters of two
-                              CTAs compute the same rows for two neighbouring channel blocks, and
-                              each activation tile is loaded once and multicast into both CTAs. */
   int out_dtype;           /* convf_out_dtype of y on the bf16 path: CONVF_OUT_F32 (default) or
                               CONVF_OUT_BF16 (the fp32 result rounded to nearest-even bf16) */
   int residual;            /* 1: y = act(scale * conv + bias' + r) for a residual tensor r of
@@ -256,7 +251,10 @@ convf_status conv_fused_measure_int8_mma_rate(void* stream, double* tops);
  *   scale, bias: device float[K], the folded epilogue y = clamp(scale*acc + bias, lo, hi)
  *              (bias = bn_scale*B + bn_shift).
  *   status_dev: optional device int32 that receives the timeout bit (1) if a bounded wait ran
- *              out (NULL: not reported).
+ *              out.  With NULL a timeout is not reported to the caller at all (the bit lands in
+ *              a word inside the scratch array, which every call clears first and nobody reads).
+ *   desc options the gathered-row kernel cannot honour are refused (CONVF_ERR_UNSUPPORTED):
+ *   tile_n > 128, cta_pair = 2, stream_k = 2, kblocks_per_step > 1, bf16 output, residual.
  * Sizes needing more scratch than 16 MiB are refused with CONVF_ERR_UNSUPPORTED.  The first call
  * on a device looks up the scratch array's device address (cudaGetSymbolAddress); make that
  * first call before any stream capture.  All calls share the one scratch array: calls whose

@@ -15,7 +15,8 @@ import convolution_onnx_conv_gb300 as cf
 from convolution_onnx_conv_gb300 import synthetic
 from convolution_onnx_conv_gb300.workloads import ConvSpec, ACT_RELU
 
-from parity import ATOL, RTOL, make_conv, to_device_nhwc
+import oracle
+from parity import ATOL, RTOL, make_conv, oracle_full, to_device_nhwc
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +28,13 @@ def _lib():
     cf.load_library(build_if_missing=True)
 
 
-def _stem_case(N=2):
-    spec = ConvSpec("noalloc_stem", N, 3, 32, 32, 64, 7, 7, (2, 2), (3, 3, 3, 3), act=ACT_RELU, has_bias=True,
-                    has_bn=True)
-    return spec, synthetic.conv_inputs(spec, 9100)
+CASES = [
+    # an RGB stem (3 channels padded to taps of 4) and an 8-channel 3x3 conv (taps of 8)
+    ConvSpec("noalloc_stem", 2, 3, 32, 32, 64, 7, 7, (2, 2), (3, 3, 3, 3), act=ACT_RELU, has_bias=True,
+             has_bn=True),
+    ConvSpec("noalloc_c8_3x3", 2, 8, 16, 16, 40, 3, 3, (1, 1), (1, 1, 1, 1), act=ACT_RELU, has_bias=True,
+             has_bn=True),
+]
 
 
 def _desc(spec):
@@ -38,14 +42,17 @@ def _desc(spec):
                         spec.dilation, spec.group, act=spec.act)
 
 
-def test_noalloc_matches_the_handle_path_on_two_calls():
-    spec, inp = _stem_case()
+@pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
+def test_noalloc_matches_the_handle_path_on_two_calls(spec):
+    inp = synthetic.conv_inputs(spec, 9100 + CASES.index(spec))
     conv = make_conv(spec, inp)
     assert conv.variant == cf.CONVF_VARIANT_IMPLICIT_GEMM_GATHER
     x = to_device_nhwc(inp["x"])
     y_ref = conv(x)
     torch.cuda.synchronize()
     conv.close()
+    ref_handle = y_ref.cpu().contiguous().numpy().astype(np.float64)
+    ref_oracle = oracle_full(spec, inp)
 
     # the caller's buffers: prepacked weights and the folded epilogue vectors, on the device
     desc = _desc(spec)
@@ -67,8 +74,11 @@ def test_noalloc_matches_the_handle_path_on_two_calls():
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         got = y.cpu().contiguous().numpy().astype(np.float64)
-        ref = y_ref.cpu().contiguous().numpy().astype(np.float64)
-        assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+        # against the handle path (the same kernel's other entry point) ...
+        assert np.all(np.abs(got - ref_handle) <= ATOL + RTOL * np.abs(ref_handle))
+        # ... and against the CPU oracle (NCHW logical view of the channels-last result)
+        ok, worst, idx = oracle.tolerance_ok(got, ref_oracle, ATOL, RTOL)
+        assert ok, (spec.name, worst, idx)
 
 
 def test_noalloc_refuses_what_it_cannot_serve():
@@ -81,7 +91,15 @@ def test_noalloc_refuses_what_it_cannot_serve():
     with pytest.raises(cf.ConvFusedError) as e:
         cf.conv_fused_run_noalloc(_desc(wide), 0, 0, 0, 0, 0)
     assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "at most 8 input channels" in str(e.value)
-    spec, _ = _stem_case()
+    spec = CASES[0]
     with pytest.raises(cf.ConvFusedError) as e:
         cf.conv_fused_run_noalloc(_desc(spec), 0, 0, 0, 0, 0)
     assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "NULL" in str(e.value)
+    # options the gathered-row kernel cannot honour are refused by name, not ignored
+    for kw, word in (({"stream_k": 2}, "stream_k"), ({"kblocks_per_step": 2}, "kblocks_per_step"),
+                     ({"out_dtype": cf.CONVF_OUT_BF16}, "bf16 output")):
+        d = cf.make_desc(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, spec.stride, spec.pads,
+                         spec.dilation, spec.group, act=spec.act, **kw)
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_run_noalloc(d, 0, 0, 0, 0, 0)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and word in str(e.value)
