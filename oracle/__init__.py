@@ -34,8 +34,12 @@ Every function is the plain definition of one stage, kept separate on purpose:
     operands ``sum (x - x_zp)(w - w_zp[k]) + B[k]`` (the quantized input pads
     with its zero point, so padded taps add nothing), then
     ``y = saturate(round_half_even(acc * x_scale * w_scale[k] / y_scale) + y_zp)``.
-    The scale product is taken in float64 on the float32 scales (a reading: the
-    specification fixes no precision for it).  The oracle subtracts the zero
+    The specification fixes no precision for this product; it is taken in the
+    GPU kernel's precision (a reading): one per-channel multiplier
+    ``m[k] = float32(x_scale * w_scale[k] / y_scale)`` (the quotient formed in
+    float64 on the float32 scales, rounded once), then
+    ``round_half_even(float32(acc) * m[k])`` with both the int->float conversion
+    and the product rounded to nearest-even float32.  The oracle subtracts the zero
     points before multiplying; the expanded form of the same sums is the
     zero-point correction identity the "onnx-vulkan-rs" page gives, in its notes
     on the quantized kernels, for blocks of four products (the tests check one
@@ -329,6 +333,9 @@ def qlinear_conv_acc(x, x_zero_point, w, w_zero_point, bias=None, strides=(1, 1)
         if a.dtype not in (np.uint8, np.int8):
             raise ValueError("QLinearConv operands are uint8 or int8")
     K = w.shape[0]
+    # each zero point has its tensor's element type (ONNX QLinearConv type constraints)
+    _check_range(x_zero_point, x.dtype, "x_zero_point")
+    _check_range(w_zero_point, w.dtype, "w_zero_point")
     xd = np.ascontiguousarray(x.astype(np.int16) - np.int16(int(x_zero_point)))
     wz = _per_channel(w_zero_point, K, np.int16)
     wd = np.ascontiguousarray(w.astype(np.int16) - wz.reshape((K,) + (1,) * (w.ndim - 1)))
@@ -344,13 +351,31 @@ def qlinear_conv_acc(x, x_zero_point, w, w_zero_point, bias=None, strides=(1, 1)
     return acc
 
 
+def _check_range(v, dtype, name):
+    info = np.iinfo(dtype)
+    a = np.asarray(v, dtype=np.int64).reshape(-1)
+    if a.size and (a.min() < info.min or a.max() > info.max):
+        raise ValueError(f"{name} must lie in {np.dtype(dtype).name}'s range [{info.min}, {info.max}]")
+
+
+def qlinear_multiplier(x_scale, w_scale, y_scale, K):
+    """Per-channel requantisation multiplier float32(x_scale * w_scale[k] / y_scale), the quotient
+    formed in float64 on the float32 scales and rounded once to float32."""
+    ws = _per_channel(w_scale, K, np.float32).astype(np.float64)
+    return (np.float64(np.float32(x_scale)) * ws / np.float64(np.float32(y_scale))).astype(np.float32)
+
+
 def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uint8):
-    """y = saturate(round_half_even(acc * x_scale * w_scale[k] / y_scale) + y_zp) for NCHW acc."""
+    """y = saturate(round_half_even(float32(acc) * m[k]) + y_zp) for NCHW acc (module docstring:
+    float32 steps, each rounded to nearest even).  y's type is y_zero_point's type."""
+    if np.dtype(y_dtype) not in (np.dtype(np.uint8), np.dtype(np.int8)):
+        raise ValueError("QLinearConv's y is uint8 or int8")
+    _check_range(y_zero_point, y_dtype, "y_zero_point")
     acc = np.asarray(acc, dtype=np.int64)
     K = acc.shape[1]
-    ws = _per_channel(w_scale, K, np.float32).astype(np.float64)
-    m = np.float64(np.float32(x_scale)) * ws / np.float64(np.float32(y_scale))
-    v = np.rint(acc.astype(np.float64) * m.reshape(1, K, 1, 1)) + int(y_zero_point)
+    m = qlinear_multiplier(x_scale, w_scale, y_scale, K)
+    p = acc.astype(np.float32) * m.reshape(1, K, 1, 1)          # float32 * float32 -> float32
+    v = np.rint(p).astype(np.int64) + int(y_zero_point)
     info = np.iinfo(y_dtype)
     return np.clip(v, info.min, info.max).astype(y_dtype)
 

@@ -532,3 +532,43 @@ def test_qlinear_requant_rounds_half_to_even_and_saturates():
     acc = np.full((1, 3, 1, 1), 10, dtype=np.int64)
     y = oracle.qlinear_requant(acc, 0.5, np.array([1.0, 2.0, 3.0], np.float32), 2.0, 0, np.int8)
     assert y.reshape(-1).tolist() == [2, 5, 8]                      # 2.5 -> 2, 5, 7.5 -> 8
+
+
+def test_qlinear_refuses_zero_points_outside_their_types():
+    """ONNX QLinearConv: x_zero_point has x's type, w_zero_point w's type, y's type is
+    y_zero_point's type; a zero point outside that type's range is refused, not wrapped."""
+    x = np.zeros((1, 2, 4, 4), np.int8)
+    w = np.zeros((3, 2, 3, 3), np.int8)
+    with pytest.raises(ValueError, match="x_zero_point"):
+        oracle.qlinear_conv_acc(x, 200, w, 0)
+    with pytest.raises(ValueError, match="w_zero_point"):
+        oracle.qlinear_conv_acc(x, 0, w, np.array([0, 130, 0]))
+    with pytest.raises(ValueError, match="w_zero_point"):
+        oracle.qlinear_conv_acc(x, 0, w.astype(np.uint8), -1)
+    acc = np.zeros((1, 3, 2, 2), np.int64)
+    with pytest.raises(ValueError, match="y_zero_point"):
+        oracle.qlinear_requant(acc, 1.0, 1.0, 1.0, -3, np.uint8)
+    with pytest.raises(ValueError, match="y_zero_point"):
+        oracle.qlinear_requant(acc, 1.0, 1.0, 1.0, 128, np.int8)
+    with pytest.raises(ValueError, match="uint8 or int8"):
+        oracle.qlinear_requant(acc, 1.0, 1.0, 1.0, 0, np.int16)
+
+
+def test_qlinear_requant_takes_float32_steps():
+    """The multiplier is one float32 rounding of the float64 quotient, and the product is a
+    float32 product: sums above 2^24 first round to float32 (ties to even), so neighbouring
+    integers can land on the same code; a float64 product would separate them."""
+    m = oracle.qlinear_multiplier(0.1, np.array([0.3], np.float32), 0.7, 1)
+    ref = np.float32(np.float64(np.float32(0.1)) * np.float64(np.float32(0.3)) / np.float64(np.float32(0.7)))
+    assert m.dtype == np.float32 and m[0] == ref
+    # acc = 7*2^22 - 1 is a float32 tie that rounds to 7*2^22 (even), so with m = 2^-23 the float32
+    # product is exactly 3.5 -> 4 (half to even); the float64 product 3.5 - 2^-23 would give 3
+    acc = np.array([7 * (1 << 22) - 1, 7 * (1 << 22) + 1], dtype=np.int64).reshape(1, 2, 1, 1)
+    y = oracle.qlinear_requant(acc, 1.0, np.array([2.0 ** -23, 2.0 ** -23], np.float32), 1.0, 0, np.int8)
+    assert y.reshape(-1).tolist() == [4, 4]
+    y = oracle.qlinear_requant(acc, 1.0, np.array([2.0 ** -2, 2.0 ** -2], np.float32), 1.0, 0, np.int8)
+    assert y.reshape(-1).tolist() == [127, 127]         # saturation
+    # 5 * 0.1f: float32(0.1) * 5 = 0.50000000745 in float64 but exactly 0.5 in float32 -> 0 (even)
+    acc = np.array([5], dtype=np.int64).reshape(1, 1, 1, 1)
+    y = oracle.qlinear_requant(acc, 0.1, np.array([1.0], np.float32), 1.0, 0, np.int8)
+    assert y.reshape(-1).tolist() == [0]
