@@ -246,6 +246,72 @@ def time_launches(layers, steps, torch):
     return per
 
 
+def scale_to(per, steps, total_ms):
+    """Per-launch event durations (summed over `steps` passes) rescaled so that one pass adds up
+    to `total_ms` (the graph-timed step): the events serialise launches and add a little each."""
+    per = [p / steps for p in per]
+    tot = sum(per)
+    return [p * total_ms / tot for p in per] if tot > 0 else per
+
+
+def attainable_ms(spec, peaks):
+    """Roofline time of one layer: FLOPs at the bf16 burst peak or algorithmic bytes at HBM."""
+    return max(spec.flops / (peaks["bf16_tflops"] * 1e12), spec.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
+
+
+def layer_bound(spec, peaks):
+    t = spec.flops / (peaks["bf16_tflops"] * 1e12)
+    b = spec.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    return "tensor" if t >= b else "hbm"
+
+
+def other_configs(args, torch, cf, synthetic, workloads, peaks):
+    """The other workloads, each one CUDA-graph replay per pass: the single conv (batch 1), the
+    whole MobileNetV2 conv stack at batch 64 (with its 1x1 expand/project layers alone as well)
+    and the batch-1 latency of the ResNet-50 and MobileNetV2 stacks."""
+    out = {}
+    steps = max(5, args.steps // 2)
+
+    def timed(specs, base, reps=1):
+        Ls = build_layers(specs, base, torch, cf, synthetic)
+        for _ in range(args.warmup):
+            for L in Ls:
+                L["conv"](L["x"], L["y"])
+        g = capture_graph(Ls, torch)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ms = time_graph(g, steps, torch) / steps
+        if any(L["conv"].status() != 0 for L in Ls):
+            raise SystemExit("device status error in " + specs[0].name)
+        return ms, Ls
+
+    one = workloads.single_conv_relu()
+    ms, _ = timed([one], 1)
+    out["single_conv"] = {"workload": "Conv 3x3 + bias + ReLU, N=1, C=16, 32x32, K=32 (fp32 out)",
+                          "us": ms * 1e3, "tflops": one.flops / (ms * 1e-3) / 1e12}
+    mv = workloads.mobilenetv2_layers(64)
+    ms, Ls = timed(mv, 4)
+    pw = [s for s in mv if s.R == 1]
+    ms_pw, _ = timed(pw, 6)
+    pw_bytes = sum(s.algorithmic_bytes for s in pw)
+    out["mobilenetv2_b64"] = {
+        "workload": "MobileNetV2 conv stack (17 blocks: 1x1 expand + ReLU6, depthwise 3x3 + ReLU6, 1x1 "
+                    "project) at batch 64, bf16 in, fp32 out",
+        "ms_per_step": ms, "tflops": sum(s.flops for s in mv) / (ms * 1e-3) / 1e12,
+        "gb_s": sum(s.algorithmic_bytes for s in mv) / (ms * 1e-3) / 1e9,
+        "expand_project_1x1": {"layers": len(pw), "ms": ms_pw, "gb_s": pw_bytes / (ms_pw * 1e-3) / 1e9,
+                               "pct_hbm": pw_bytes / (ms_pw * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               "tflops": sum(s.flops for s in pw) / (ms_pw * 1e-3) / 1e12}}
+    r1 = workloads.resnet50_layers(1)
+    ms_r1, _ = timed(r1, 7)
+    m1 = workloads.mobilenetv2_layers(1)
+    ms_m1, _ = timed(m1, 8)
+    out["latency_b1"] = {"note": "batch 1, one CUDA-graph replay of the whole conv stack (working set in L2)",
+                         "resnet50_us": ms_r1 * 1e3, "mobilenetv2_us": ms_m1 * 1e3}
+    return out
+
+
 # ------------------------------------------------------------------------------ CPU oracle
 _ORACLE_CACHE = {}
 
@@ -402,6 +468,17 @@ def main():
             g.replay()
     torch.cuda.synchronize()
 
+    # dominant kernel: the tcgen05 implicit-GEMM conv (every 1x1 and every strided 3x3 layer; the
+    # halo and window kernels take the other four).  Its time per step is a graph replay of only
+    # its own layers, in step order, on their own resident buffers: a subset of the step, so it
+    # cannot exceed the step's time.
+    tc_idx = [i for i, L in enumerate(layers)
+              if L["conv"].describe().split()[0] in ("variant=gemm_1x1", "variant=implicit_gemm_im2col")]
+    g_tc = capture_graph([layers[i] for i in tc_idx], torch)
+    for _ in range(args.warmup):
+        g_tc.replay()
+    torch.cuda.synchronize()
+
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.1)
@@ -410,8 +487,10 @@ def main():
     total_ms = time_graph(g_r50, args.steps, torch)            # the timed region: K steps
     torch.cuda.synchronize()
     barrier()
-    per_layer = time_launches(layers, max(3, args.steps // 5), torch)
+    tc_steps = max(3, args.steps // 2)
+    tc_ms = time_graph(g_tc, tc_steps, torch) / tc_steps
     lsteps = max(3, args.steps // 5)
+    per_layer = time_launches(layers, lsteps, torch)
     dw_steps = max(3, args.steps // 2)
     dw_total = time_graph(g_dw, dw_steps, torch)
     dw_per = time_launches(dw_layers, lsteps, torch)
@@ -429,31 +508,42 @@ def main():
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
-    # dominant kernel: the tcgen05 implicit-GEMM conv (49 of the 53 layers: every 1x1 and every
-    # strided or 7x7 layer; the halo and window kernels take the other four)
-    tc_idx = [i for i, L in enumerate(layers)
-              if L["conv"].describe().split()[0] in ("variant=gemm_1x1", "variant=implicit_gemm_im2col")]
-    tc_ms = sum(per_layer[i] for i in tc_idx) / lsteps
+    # per-layer times: event pairs around each launch (serialised, no dependent-launch overlap)
+    # rescaled so that they add up to the graph-timed step
+    per_layer = scale_to(per_layer, lsteps, ms_per_step)
+    dw_per = scale_to(dw_per, lsteps, dw_total / dw_steps)
+    s8_per = scale_to(s8_per, lsteps, s8_total / s8_steps)
+
     tc_flops = sum(specs[i].flops for i in tc_idx)
     achieved = tc_flops / (tc_ms * 1e-3) / 1e12
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": tc_traffic(),
-            "kernel": f"tc_conv_kernel (tcgen05 implicit GEMM, all tile widths; {len(tc_idx)} layers)",
-            "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside a long step)",
+    # attainable time of each layer: its FLOPs at the tensor peak or its algorithmic bytes at the
+    # HBM bandwidth, whichever is longer (the bound of that layer)
+    att_ms = [attainable_ms(specs[i], peaks) for i in tc_idx]
+    n_tensor = sum(1 for i in tc_idx if layer_bound(specs[i], peaks) == "tensor")
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": tc_traffic(),
+            "kernel": f"tc_conv_kernel (tcgen05 implicit GEMM, all tile widths; {len(tc_idx)} layers per step)",
+            "peak_source": f"{peak_src} bf16 dense, burst (the kernel's layers timed alone as one graph replay)",
+            "kernel_ms_per_step": tc_ms, "launches_per_step": len(tc_idx),
             "per_launch_flops": tc_flops / len(tc_idx), "launch_ms": tc_ms / len(tc_idx),
-            "per_launch_algorithmic_bytes": sum(specs[i].algorithmic_bytes for i in tc_idx) / len(tc_idx)}
+            "per_launch_algorithmic_bytes": sum(specs[i].algorithmic_bytes for i in tc_idx) / len(tc_idx),
+            "layer_bounds": {"tensor": n_tensor, "hbm": len(tc_idx) - n_tensor},
+            "attainable_frac": sum(att_ms) / tc_ms,
+            "attainable_note": "sum over the kernel's layers of max(FLOPs / bf16 burst peak, algorithmic "
+                               "bytes / HBM peak), divided by the measured time of the same layers"}
     idx17 = [i for i, s in enumerate(specs) if s.R > 1]
     f17 = sum(specs[i].flops for i in idx17)
-    t17 = sum(per_layer[i] for i in idx17) / lsteps
+    t17 = sum(per_layer[i] for i in idx17)
     tf17 = f17 / (t17 * 1e-3) / 1e12
     dw_bytes = sum(s.algorithmic_bytes for s in dw_specs)
     dw_ms = dw_total / dw_steps
     dw_gbs = dw_bytes / (dw_ms * 1e-3) / 1e9
-    dw_kernel_gbs = dw_bytes / (sum(dw_per) / lsteps * 1e-3) / 1e9
     s8_ops = sum(s.flops for s in s8_specs)
     s8_ms = s8_total / s8_steps
     s8_tops = s8_ops / (s8_ms * 1e-3) / 1e12
     s8_peak = cf.conv_fused_measure_int8_mma_rate()
+
+    extra = other_configs(args, torch, cf, synthetic, workloads, peaks)
 
     # the same step with bf16 outputs and the bottleneck shortcuts (extended epilogue)
     ext_layers = build_ext_layers(specs, layers, torch, cf)
@@ -471,19 +561,39 @@ def main():
     if any(L["conv"].status() != 0 for L in ext_layers):
         raise SystemExit("device status error in the bf16-output / residual step")
 
-    # end to end through the public API with host buffers (pinned), copies inside the timing
+    # end to end through the public API with host buffers (pinned), copies inside the timing: each
+    # layer's input goes up on a copy stream, the conv runs on the compute stream once its input
+    # has landed, and its output comes back on a second copy stream, so copies of one layer
+    # overlap the kernels and copies of the others
     e2e_steps = max(2, min(5, args.steps))
     for L in layers:
         L["x_pin"] = L["x_host"].pin_memory()
         L["y_pin"] = torch.empty_strided(L["y"].shape, L["y"].stride(), dtype=L["y"].dtype, pin_memory=True)
     h2d = sum(L["x"].numel() * L["x"].element_size() for L in layers)
     d2h = sum(L["y"].numel() * L["y"].element_size() for L in layers)
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_step():
+        start = torch.cuda.Event()
+        start.record(s_comp)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
         for L in layers:
-            L["x"].copy_(L["x_pin"], non_blocking=True)
+            with torch.cuda.stream(s_in):
+                L["x"].copy_(L["x_pin"], non_blocking=True)
+                L["ev_in"] = torch.cuda.Event()
+                L["ev_in"].record(s_in)
+            s_comp.wait_event(L["ev_in"])
             L["conv"](L["x"], L["y"])
-            L["y_pin"].copy_(L["y"], non_blocking=True)
+            ev_run = torch.cuda.Event()
+            ev_run.record(s_comp)
+            s_out.wait_event(ev_run)
+            with torch.cuda.stream(s_out):
+                L["y_pin"].copy_(L["y"], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        s_comp.wait_event(done)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -507,21 +617,18 @@ def main():
     if args.layers_out and rank == 0:
         with open(args.layers_out, "w") as f:
             for s, L, ms in zip(specs, layers, per_layer):
-                ms /= lsteps
                 ai = s.flops / s.algorithmic_bytes
                 # attainable: the tensor peak or the HBM bandwidth times the layer's intensity
-                att = min(peaks["bf16_tflops_sustained"], ai * peaks["hbm_gbs"] / 1e3)
+                att = min(peaks["bf16_tflops"], ai * peaks["hbm_gbs"] / 1e3)
                 tf = s.flops / (ms * 1e-3) / 1e12
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "tflops": tf,
                                     "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9, "ai": ai,
                                     "attainable_tflops": att, "pct_attainable": tf / att}) + "\n")
             for s, L, ms in zip(dw_specs, dw_layers, dw_per):
-                ms /= lsteps
                 gbs = s.algorithmic_bytes / (ms * 1e-3) / 1e9
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "gbs": gbs,
                                     "pct_hbm": gbs / peaks["hbm_gbs"]}) + "\n")
             for s, L, ms in zip(s8_specs, s8_layers, s8_per):
-                ms /= lsteps
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
                                     "tops": s.flops / (ms * 1e-3) / 1e12}) + "\n")
 
@@ -541,8 +648,7 @@ def main():
             "pct_bf16_peak": value / peaks["bf16_tflops"],
             "implicit_gemm_3x3_7x7": {"layers": len(idx17), "tflops": tf17, "pct_bf16_peak": tf17 / peaks["bf16_tflops"]},
             "depthwise": {"workload": "MobileNetV2 depthwise 3x3 layers (17) at batch 64, bf16 in, fp32 out",
-                          "gb_s": dw_gbs, "pct_hbm": dw_gbs / peaks["hbm_gbs"], "ms": dw_ms,
-                          "kernel_gb_s": dw_kernel_gbs},
+                          "gb_s": dw_gbs, "pct_hbm": dw_gbs / peaks["hbm_gbs"], "ms": dw_ms},
             "int8": {"workload": "ResNet-50 3x3 shapes (7) at batch 64, int8 in/out, int32 acc",
                      "tops": s8_tops, "ms": s8_ms, "mma_sync_s8_peak_tops": s8_peak,
                      "pct_of_measured_int8_mma": s8_tops / s8_peak,
@@ -552,14 +658,17 @@ def main():
                                               "residual added in each bottleneck's last 1x1 conv",
                                   "ms_per_step": ext_ms, "tflops": flops_step / (ext_ms * 1e-3) / 1e12,
                                   "bf16_layers": ext_bf16, "residual_layers": ext_res},
+            **extra,
             "peaks": {**peaks, "source": peak_src},
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps, "copies": "pinned host buffers; H2D and D2H on two copy streams "
+                                                   "overlapping the kernels on the compute stream"},
             "gpu_launches": launches_per_step * args.steps,
-            "timing": "step = one CUDA-graph replay of the 53 conv launches; per-kernel durations from "
-                      "event pairs around each launch with the stream pre-queued",
+            "timing": "step = one CUDA-graph replay of the 53 conv launches; the dominant kernel = one graph "
+                      "replay of its own layers; per-layer times (layer log) from event pairs around each "
+                      "launch, rescaled to add up to the step",
             "clocks": clocks,
         }
         print(json.dumps(line))
