@@ -14,7 +14,7 @@ from . import _build
 # --- enums (mirror include/conv_fused.h)
 CONVF_OK, CONVF_ERR_INVALID_ARG, CONVF_ERR_UNSUPPORTED, CONVF_ERR_OOM, CONVF_ERR_CUDA, \
     CONVF_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-CONVF_BF16, CONVF_S8 = 0, 1
+CONVF_BF16, CONVF_S8, CONVF_Q8 = 0, 1, 2
 CONVF_OUT_F32, CONVF_OUT_BF16 = 0, 1
 CONVF_NCHW, CONVF_NHWC = 0, 1
 CONVF_ACT_NONE, CONVF_ACT_RELU, CONVF_ACT_RELU6, CONVF_ACT_CLIP = 0, 1, 2, 3
@@ -22,9 +22,10 @@ CONVF_AUTO_PAD_NOTSET, CONVF_AUTO_PAD_SAME_UPPER, CONVF_AUTO_PAD_SAME_LOWER, \
     CONVF_AUTO_PAD_VALID = 0, 1, 2, 3
 CONVF_VARIANT_AUTO, CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_DEPTHWISE, \
     CONVF_VARIANT_INT8, CONVF_VARIANT_IMPLICIT_GEMM_GATHER, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW, \
-    CONVF_VARIANT_IMPLICIT_GEMM_HALO = 0, 1, 2, 3, 4, 5, 6, 7
+    CONVF_VARIANT_IMPLICIT_GEMM_HALO, CONVF_VARIANT_INT8_TC = 0, 1, 2, 3, 4, 5, 6, 7, 8
 VARIANT_NAMES = {0: "auto", 1: "implicit_gemm_im2col", 2: "gemm_1x1", 3: "depthwise",
-                 4: "int8_mma", 5: "implicit_gemm_gather", 6: "implicit_gemm_window", 7: "implicit_gemm_halo"}
+                 4: "int8_mma", 5: "implicit_gemm_gather", 6: "implicit_gemm_window", 7: "implicit_gemm_halo",
+                 8: "int8_tcgen05_exact"}
 AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
 
 EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale_shift",
@@ -32,7 +33,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
-            "conv_fused_run_residual"]
+            "conv_fused_run_residual", "conv_fused_create_qlinear"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -45,6 +46,14 @@ class ConvDesc(ctypes.Structure):
                 ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("kblocks_per_step", ctypes.c_int),
                 ("out_dtype", ctypes.c_int), ("residual", ctypes.c_int)]
+
+
+class QParams(ctypes.Structure):
+    """convf_qparams: ONNX QLinearConv scales and zero points (host arrays for w's)."""
+    _fields_ = [("x_signed", ctypes.c_int), ("w_signed", ctypes.c_int), ("y_signed", ctypes.c_int),
+                ("x_zero_point", ctypes.c_int32), ("w_zero_point", ctypes.c_void_p), ("x_scale", ctypes.c_float),
+                ("w_scale", ctypes.c_void_p), ("y_scale", ctypes.c_float), ("y_zero_point", ctypes.c_int32),
+                ("relu", ctypes.c_int)]
 
 
 def make_desc(N, C, H, W, K, R, S, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1,
@@ -106,6 +115,7 @@ def load_library(build_if_missing: bool = False):
                                     P(ctypes.c_int)]
     lib.conv_fused_pack_weights.argtypes = [dptr, ctypes.c_int, vp, vp, ctypes.c_size_t]
     lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
+    lib.conv_fused_create_qlinear.argtypes = [dptr, vp, vp, P(QParams), P(vp)]
     lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
     lib.conv_fused_run_residual.argtypes = [vp, vp, vp, vp, vp]
     lib.conv_fused_status.argtypes = [vp]
@@ -193,6 +203,15 @@ def conv_fused_create(desc: ConvDesc, W, bias=None, bn_scale=None, bn_shift=None
     _check(load_library().conv_fused_create(ctypes.byref(desc), _addr(W), _addr(bias), _addr(bn_scale),
                                             _addr(bn_shift), _addr(requant_mult), _addr(requant_shift),
                                             int(out_zero_point), ctypes.byref(h)))
+    return h.value
+
+
+def conv_fused_create_qlinear(desc: ConvDesc, W, bias, q: QParams) -> int:
+    """QLinearConv handle: desc.dtype == CONVF_Q8, W host int8/uint8 [K][C/group][R][S], bias host
+    int32[K] or None, q the scales and zero points (its w arrays host pointers)."""
+    h = ctypes.c_void_p()
+    _check(load_library().conv_fused_create_qlinear(ctypes.byref(desc), _addr(W), _addr(bias), ctypes.byref(q),
+                                                    ctypes.byref(h)))
     return h.value
 
 
@@ -344,3 +363,41 @@ class FusedConv:
             self.close()
         except Exception:
             pass
+
+
+class QLinearConv(FusedConv):
+    """ONNX QLinearConv over torch tensors: ``w`` int8 or uint8 (KCRS, CPU), ``bias`` int32[K] or
+    None, per-channel ``w_scale`` / ``w_zero_point`` (or scalars).  Calling it with an 8-bit
+    channels-last CUDA tensor x returns the 8-bit y (uint8 or int8 per ``y_signed``)."""
+
+    def __init__(self, N, C, H, W, K, R, S, w, bias=None, x_scale=1.0, x_zero_point=0, w_scale=1.0,
+                 w_zero_point=0, y_scale=1.0, y_zero_point=0, x_signed=False, y_signed=False, relu=False,
+                 stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1), group=1, auto_pad="NOTSET",
+                 variant=CONVF_VARIANT_AUTO, tile_n=0, kblocks_per_step=0):
+        import numpy as np
+        import torch
+        self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group, CONVF_Q8, CONVF_ACT_NONE,
+                              (0.0, 6.0), auto_pad, variant, tile_n=tile_n, kblocks_per_step=kblocks_per_step)
+        self.out_bf16 = False
+        self.residual = False
+        self.s8 = True
+        self.y_signed = bool(y_signed)
+        wc = w.contiguous().cpu()
+        ws = np.ascontiguousarray(np.broadcast_to(np.asarray(w_scale, dtype=np.float32).reshape(-1), (K,)))
+        wz = np.ascontiguousarray(np.broadcast_to(np.asarray(w_zero_point, dtype=np.int32).reshape(-1), (K,)))
+        b = None if bias is None else torch.as_tensor(bias).to(torch.int32).contiguous().cpu()
+        self._keep = [wc, ws, wz, b]
+        q = QParams()
+        q.x_signed, q.w_signed, q.y_signed = int(bool(x_signed)), int(wc.dtype == torch.int8), int(bool(y_signed))
+        q.x_zero_point, q.y_zero_point = int(x_zero_point), int(y_zero_point)
+        q.x_scale, q.y_scale = float(x_scale), float(y_scale)
+        q.w_zero_point, q.w_scale = wz.ctypes.data, ws.ctypes.data
+        q.relu = int(bool(relu))
+        self.handle = conv_fused_create_qlinear(self.desc, wc, b, q)
+        self.out_shape = conv_fused_output_shape(self.desc)
+
+    def new_output(self):
+        import torch
+        N, K, Ho, Wo = self.out_shape
+        dt = torch.int8 if self.y_signed else torch.uint8
+        return torch.empty((N, Ho, Wo, K), dtype=dt, device="cuda").permute(0, 3, 1, 2)

@@ -131,8 +131,8 @@ convf_status resolve(const convf_desc* d, Shape* s) {
 }
 
 convf_status check_misc(const convf_desc* d) {
-  if (d->dtype != CONVF_BF16 && d->dtype != CONVF_S8)
-    return fail(CONVF_ERR_INVALID_ARG, "dtype=%d is not CONVF_BF16 or CONVF_S8", d->dtype);
+  if (d->dtype != CONVF_BF16 && d->dtype != CONVF_S8 && d->dtype != CONVF_Q8)
+    return fail(CONVF_ERR_INVALID_ARG, "dtype=%d is not CONVF_BF16, CONVF_S8 or CONVF_Q8", d->dtype);
   if ((d->x_layout != CONVF_NCHW && d->x_layout != CONVF_NHWC) ||
       (d->y_layout != CONVF_NCHW && d->y_layout != CONVF_NHWC))
     return fail(CONVF_ERR_INVALID_ARG, "layouts (%d,%d) must be CONVF_NCHW or CONVF_NHWC", d->x_layout,
@@ -145,7 +145,7 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "clip bounds (%g, %g) need lo <= hi", d->clip_lo, d->clip_hi);
   if (d->dtype == CONVF_S8 && (d->act == CONVF_ACT_RELU6 || d->act == CONVF_ACT_CLIP))
     return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
-  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_INT8_TC)
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
   if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
@@ -284,6 +284,11 @@ std::string halo_geom(const Shape& s, int num_sms, int forced_bn, HaloGeom* g) {
 }
 
 // ------------------------------------------------------------------ variant selector
+// A 1x1 filter with unit strides and no padding: the activation operand is a plain matrix.
+bool pure_1x1(const Shape& s) {
+  return s.R == 1 && s.S == 1 && s.sh == 1 && s.sw == 1 && !s.pt && !s.pl && !s.pb && !s.pr;
+}
+
 // Why a shape cannot use a variant ("" = it can).
 std::string cannot(int v, const convf_desc* d, const Shape& s) {
   const bool bf = d->dtype == CONVF_BF16;
@@ -339,10 +344,24 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
       return "";
     case CONVF_VARIANT_INT8:
-      if (bf) return "the int8 kernel serves CONVF_S8 only";
+      if (d->dtype != CONVF_S8) return "the mma.sync int8 kernel serves CONVF_S8 only";
       if (d->group != 1) return "the int8 kernel needs group == 1";
       if (s.C % 64) return "the int8 kernel needs C % 64 == 0";
       if (s.K % 16) return "the int8 kernel needs K % 16 == 0";
+      return "";
+    case CONVF_VARIANT_INT8_TC:
+      if (bf) return "the exact-integer tcgen05 kernel serves CONVF_S8 and CONVF_Q8 only";
+      if (d->group != 1) return "the exact-integer tcgen05 kernel needs group == 1";
+      if (s.C % 8) return "the exact-integer tcgen05 kernel needs C % 8 == 0 (16-byte rows of its bf16 staging copy)";
+      if (s.K % 16) return "the exact-integer tcgen05 kernel needs K % 16 == 0 (16-byte 8-bit output groups)";
+      if (pure_1x1(s)) return "";
+      if (s.sh > 8 || s.sw > 8) return "TMA im2col traversal strides are limited to 8";
+      if (s.pt > 128 || s.pl > 128) return "TMA im2col box corners are limited to [-128, 127]";
+      if ((long long)(s.R - 1) * s.dh - s.pb > 128 || (long long)(s.S - 1) * s.dw - s.pr > 128 ||
+          s.pb - (long long)(s.R - 1) * s.dh > 127 || s.pr - (long long)(s.S - 1) * s.dw > 127)
+        return "TMA im2col box corners are limited to [-128, 127]";
+      if ((long long)(s.R - 1) * s.dh > 65535 || (long long)(s.S - 1) * s.dw > 65535)
+        return "filter offsets exceed 16 bits";
       return "";
   }
   snprintf(b, sizeof b, "unknown variant %d", v);
@@ -359,9 +378,17 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
   const int order_bf16[6] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM_HALO,
                              CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW,
                              CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
-  if (d->dtype == CONVF_S8) {
-    std::string why = cannot(CONVF_VARIANT_INT8, d, s);
-    if (!why.empty()) return fail(CONVF_ERR_UNSUPPORTED, "int8 conv refused: %s", why.c_str());
+  if (d->dtype == CONVF_S8 || d->dtype == CONVF_Q8) {
+    // exact integers on tcgen05 first; static int8 falls back to the warp-level MMA kernel
+    std::string why = cannot(CONVF_VARIANT_INT8_TC, d, s);
+    if (why.empty()) {
+      *out = CONVF_VARIANT_INT8_TC;
+      return CONVF_OK;
+    }
+    if (d->dtype == CONVF_Q8) return fail(CONVF_ERR_UNSUPPORTED, "QLinearConv refused: %s", why.c_str());
+    std::string why2 = cannot(CONVF_VARIANT_INT8, d, s);
+    if (!why2.empty())
+      return fail(CONVF_ERR_UNSUPPORTED, "int8 conv refused: %s; %s", why.c_str(), why2.c_str());
     *out = CONVF_VARIANT_INT8;
     return CONVF_OK;
   }
@@ -526,6 +553,13 @@ struct convf_handle {
   bool a3d;         // 1x1 activation map is 3-D {64, M, C/64} (one box per step)
   float* sk_ws;     // stream-K: one 128 x bn fp32 partial per CTA
   int* sk_flags;    // stream-K: one flag per CTA (zero between launches)
+  // exact-integer tcgen05 variant (8-bit convs)
+  uint16_t* xq;     // bf16 staging copy of x - x_zero_point, written by the pre-pass each run
+  int x_signed, x_zp, iq_chunk_kb, iq_mode, q_lo, q_hi;
+  int32_t* q_bias;
+  int32_t* q_mult;
+  int32_t* q_shift;
+  float* q_scale;
   WinGeom wg;       // window variant geometry
   HaloGeom hg;      // halo variant geometry
   CUtensorMap tmB;
@@ -672,6 +706,13 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
     kt = s.R * g.E;
   } else if (v == CONVF_VARIANT_INT8) {
     kt = s.R * s.S * s.C;
+  } else if (v == CONVF_VARIANT_INT8_TC) {
+    int am, cb, cp;
+    tc_layout(pure_1x1(s) ? CONVF_VARIANT_GEMM_1X1 : CONVF_VARIANT_IMPLICIT_GEMM, s, &am, &cb, &kt, &cp);
+    bool pair = false, sk = false;
+    pick_tile(s.M, s.K, kt / 64, num_sms > 1 ? num_sms : 2, 128, 1, 1, false, &bn, &pair, &sk);
+    if (bn < 64) bn = 64;
+    if (desc->tile_n == 64 || desc->tile_n == 128) bn = desc->tile_n;
   }
   if (tile_n) *tile_n = bn;
   if (ktot) *ktot = kt;
@@ -697,10 +738,15 @@ convf_status conv_fused_pack_weights(const convf_desc* desc, int variant, const 
   return ok();
 }
 
-convf_status conv_fused_create(const convf_desc* desc, const void* W, const void* bias,
-                               const float* bn_scale, const float* bn_shift,
-                               const int32_t* requant_mult, const int32_t* requant_shift,
-                               int32_t out_zero_point, convf_handle** out) {
+namespace {
+convf_status encode_a_map(convf_handle* h, const void* x);   // below, with the run path
+
+int q8_lo(int is_signed) { return is_signed ? -128 : 0; }
+int q8_hi(int is_signed) { return is_signed ? 127 : 255; }
+
+convf_status create_impl(const convf_desc* desc, const void* W, const void* bias, const float* bn_scale,
+                         const float* bn_shift, const int32_t* requant_mult, const int32_t* requant_shift,
+                         int32_t out_zero_point, const convf_qparams* qp, convf_handle** out) {
   if (!out) return fail(CONVF_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   Shape s;
@@ -709,6 +755,29 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   if ((st = check_misc(desc)) != CONVF_OK) return st;
   if (!W) return fail(CONVF_ERR_INVALID_ARG, "W is NULL");
   const bool s8 = desc->dtype == CONVF_S8;
+  const bool q8 = desc->dtype == CONVF_Q8;
+  if (q8 != (qp != nullptr))
+    return fail(CONVF_ERR_INVALID_ARG, q8 ? "CONVF_Q8 handles are made by conv_fused_create_qlinear"
+                                          : "conv_fused_create_qlinear needs desc->dtype == CONVF_Q8");
+  if (q8) {
+    if (!qp->w_zero_point || !qp->w_scale) return fail(CONVF_ERR_INVALID_ARG, "w_zero_point/w_scale is NULL");
+    for (int v : {qp->x_signed, qp->w_signed, qp->y_signed, qp->relu})
+      if (v != 0 && v != 1) return fail(CONVF_ERR_INVALID_ARG, "x_signed/w_signed/y_signed/relu must be 0 or 1");
+    if (qp->x_zero_point < q8_lo(qp->x_signed) || qp->x_zero_point > q8_hi(qp->x_signed))
+      return fail(CONVF_ERR_INVALID_ARG, "x_zero_point=%d is outside x's type", qp->x_zero_point);
+    if (qp->y_zero_point < q8_lo(qp->y_signed) || qp->y_zero_point > q8_hi(qp->y_signed))
+      return fail(CONVF_ERR_INVALID_ARG, "y_zero_point=%d is outside y's type", qp->y_zero_point);
+    if (!(std::isfinite(qp->x_scale) && qp->x_scale > 0.f) || !(std::isfinite(qp->y_scale) && qp->y_scale > 0.f))
+      return fail(CONVF_ERR_INVALID_ARG, "x_scale and y_scale must be finite and > 0");
+    for (int k = 0; k < s.K; ++k) {
+      if (qp->w_zero_point[k] < q8_lo(qp->w_signed) || qp->w_zero_point[k] > q8_hi(qp->w_signed))
+        return fail(CONVF_ERR_INVALID_ARG, "w_zero_point[%d]=%d is outside w's type", k, qp->w_zero_point[k]);
+      if (!(std::isfinite(qp->w_scale[k]) && qp->w_scale[k] > 0.f))
+        return fail(CONVF_ERR_INVALID_ARG, "w_scale[%d] must be finite and > 0", k);
+    }
+    if (bn_scale || bn_shift || requant_mult || requant_shift)
+      return fail(CONVF_ERR_INVALID_ARG, "BN and fixed-point requant arrays do not apply to QLinearConv");
+  }
   if (s8) {
     if (bn_scale || bn_shift) return fail(CONVF_ERR_INVALID_ARG, "bn_scale/bn_shift must be NULL on the int8 path");
     if (!requant_mult || !requant_shift) return fail(CONVF_ERR_INVALID_ARG, "requant_mult/requant_shift are required on the int8 path");
@@ -761,7 +830,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   for (int k = 0; k < s.K; ++k) {
     const double sc = bn_scale ? (double)bn_scale[k] : 1.0;
     const double sf = bn_shift ? (double)bn_shift[k] : 0.0;
-    const double b = (!s8 && bias) ? (double)static_cast<const float*>(bias)[k] : 0.0;
+    const double b = (!s8 && !q8 && bias) ? (double)static_cast<const float*>(bias)[k] : 0.0;
     scale[k] = (float)sc;
     biasf[k] = (float)(sc * b + sf);
   }
@@ -801,6 +870,72 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_INT8_TC) {
+    // 8-bit operands as exact bf16 integers: w - w_zero_point[k] (|v| <= 255), prepacked like the
+    // bf16 implicit GEMM (1x1 matrix rows or per-tap 64-channel runs)
+    const bool wsig = q8 ? qp->w_signed != 0 : true;
+    h->x_signed = q8 ? qp->x_signed : 1;
+    h->x_zp = q8 ? qp->x_zero_point : 0;
+    int cpad = 0;
+    tc_layout(pure_1x1(s) ? CONVF_VARIANT_GEMM_1X1 : CONVF_VARIANT_IMPLICIT_GEMM, s, &h->a_mode, &h->cblocks,
+              &h->ktot, &cpad);
+    const size_t wn = (size_t)s.K * s.C * s.R * s.S;
+    std::vector<uint16_t> wb(wn);
+    const uint8_t* Wq = static_cast<const uint8_t*>(W);
+    int maxb = 0;
+    for (size_t i = 0; i < wn; ++i) {
+      const int k = (int)(i / ((size_t)s.C * s.R * s.S));
+      const int w = (wsig ? (int)(int8_t)Wq[i] : (int)Wq[i]) - (q8 ? qp->w_zero_point[k] : 0);
+      maxb = std::max(maxb, std::abs(w));
+      const float f = (float)w;   // |w| <= 255: exact in bf16, so the top half of the float is it
+      uint32_t u;
+      std::memcpy(&u, &f, 4);
+      wb[i] = (uint16_t)(u >> 16);
+    }
+    wpack.resize((size_t)s.K * h->ktot);
+    pack_bf16(wb.data(), s, cpad, h->ktot, wpack.data());
+    // chunk of reduction blocks whose |partial sums| stay <= 2^24 (exact in the fp32 accumulator)
+    const int lo = q8_lo(h->x_signed), hi = q8_hi(h->x_signed);
+    const long long maxa = std::max(std::abs(lo - h->x_zp), std::abs(hi - h->x_zp));
+    const int nkb = h->ktot / 64;
+    long long bound = maxb == 0 || maxa == 0 ? nkb : (1LL << 24) / (maxa * maxb * 64);
+    bool pair = false, sk = false;
+    pick_tile(s.M, s.K, nkb, h->num_sms, 128, 1, 1, false, &h->bn, &pair, &sk);
+    if (h->bn < 64) h->bn = 64;
+    if (desc->tile_n == 64 || desc->tile_n == 128) h->bn = desc->tile_n;
+    else if (desc->tile_n) {
+      delete h;
+      return fail(CONVF_ERR_UNSUPPORTED, "tile_n=%d: the exact-integer kernel comes 64 or 128 wide", desc->tile_n);
+    }
+    const int stg = tc_conv_stages(h->bn, false, false);
+    if (desc->kblocks_per_step) {
+      if (stg % desc->kblocks_per_step || nkb % desc->kblocks_per_step) {
+        delete h;
+        return fail(CONVF_ERR_UNSUPPORTED,
+                    "kblocks_per_step=%d must divide both the %d reduction blocks and the %d pipeline stages of "
+                    "%d-wide tiles", desc->kblocks_per_step, nkb, stg, h->bn);
+      }
+      h->kpb = desc->kblocks_per_step;
+    } else {
+      h->kpb = auto_kblocks_per_step(stg, nkb);
+    }
+    if (bound < h->kpb) {
+      delete h;
+      return fail(CONVF_ERR_UNSUPPORTED, "the exact-integer chunk (%lld blocks) is shorter than a pipeline step", bound);
+    }
+    h->iq_chunk_kb = (int)std::min<long long>(nkb, bound / h->kpb * h->kpb);
+    h->a3d = h->a_mode == kA2D && h->kpb > 1 && s.C % 64 == 0;
+    h->iq_mode = q8 ? 1 : 0;
+    h->zp = q8 ? qp->y_zero_point : out_zero_point;
+    const bool ysig = q8 ? qp->y_signed != 0 : true;
+    const bool relu = q8 ? qp->relu != 0 : desc->act == CONVF_ACT_RELU;
+    h->q_lo = relu ? std::max(h->zp, q8_lo(ysig)) : q8_lo(ysig);
+    h->q_hi = q8_hi(ysig);
+    o_w = carve(wpack.size() * sizeof(uint16_t));
+    o_qb = carve((size_t)Kpad * 4);
+    o_qm = carve((size_t)Kpad * 4);
+    o_qs = carve((size_t)Kpad * 4);
+    o_pad = carve((size_t)s.N * s.H * s.W * s.C * sizeof(uint16_t));
   } else if (variant == CONVF_VARIANT_INT8) {
     o_w = carve((size_t)s.K * s.R * s.S * s.C);
     o_qb = carve((size_t)s.K * 4);
@@ -864,6 +999,25 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     h->bias = reinterpret_cast<float*>(base + o_bias);
     std::memcpy(staging.data() + o_taps, taps.data(), taps.size() * sizeof(float));
     std::memcpy(staging.data() + o_bias, biasf.data(), (size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_INT8_TC) {
+    h->w_bf16 = reinterpret_cast<uint16_t*>(base + o_w);
+    h->q_bias = reinterpret_cast<int32_t*>(base + o_qb);
+    h->q_mult = reinterpret_cast<int32_t*>(base + o_qm);
+    h->q_shift = reinterpret_cast<int32_t*>(base + o_qs);
+    h->q_scale = reinterpret_cast<float*>(base + o_qm);   // mode 1 keeps its float multipliers here
+    h->xq = reinterpret_cast<uint16_t*>(base + o_pad);
+    std::memcpy(staging.data() + o_w, wpack.data(), wpack.size() * sizeof(uint16_t));
+    int32_t* qb = reinterpret_cast<int32_t*>(staging.data() + o_qb);
+    for (int k = 0; k < s.K; ++k) qb[k] = bias ? static_cast<const int32_t*>(bias)[k] : 0;
+    if (q8) {
+      // m[k] = float32(x_scale * w_scale[k] / y_scale), the quotient formed in double
+      float* qm = reinterpret_cast<float*>(staging.data() + o_qm);
+      for (int k = 0; k < s.K; ++k)
+        qm[k] = (float)((double)qp->x_scale * (double)qp->w_scale[k] / (double)qp->y_scale);
+    } else {
+      std::memcpy(staging.data() + o_qm, requant_mult, (size_t)s.K * 4);
+      std::memcpy(staging.data() + o_qs, requant_shift, (size_t)s.K * 4);
+    }
   } else if (variant == CONVF_VARIANT_INT8) {
     h->w_s8 = reinterpret_cast<int8_t*>(base + o_w);
     h->qbias = reinterpret_cast<int32_t*>(base + o_qb);
@@ -972,7 +1126,7 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
     }
   }
   if (variant == CONVF_VARIANT_GEMM_1X1 || variant == CONVF_VARIANT_IMPLICIT_GEMM ||
-      variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER) {
+      variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER || variant == CONVF_VARIANT_INT8_TC) {
     if (!load_encoders()) {
       cudaFree(h->dev);
       delete h;
@@ -1015,10 +1169,36 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
       delete h;
       return fail(CONVF_ERR_CUDA, "weight tensor map encoding failed (CUresult %d)", (int)r);
     }
+    if (variant == CONVF_VARIANT_INT8_TC) {
+      // the activation operand is the handle's bf16 staging copy: its map is encoded once
+      convf_status ms = encode_a_map(h, h->xq);
+      if (ms != CONVF_OK) {
+        cudaFree(h->dev);
+        delete h;
+        return ms;
+      }
+    }
   }
   h->magic = kMagic;
   *out = h;
   return ok();
+}
+}  // namespace
+
+convf_status conv_fused_create(const convf_desc* desc, const void* W, const void* bias,
+                               const float* bn_scale, const float* bn_shift,
+                               const int32_t* requant_mult, const int32_t* requant_shift,
+                               int32_t out_zero_point, convf_handle** out) {
+  return create_impl(desc, W, bias, bn_scale, bn_shift, requant_mult, requant_shift, out_zero_point, nullptr, out);
+}
+
+convf_status conv_fused_create_qlinear(const convf_desc* desc, const void* W, const int32_t* bias,
+                                       const convf_qparams* q, convf_handle** out) {
+  if (!q) {
+    if (out) *out = nullptr;
+    return fail(CONVF_ERR_INVALID_ARG, "q is NULL");
+  }
+  return create_impl(desc, W, bias, nullptr, nullptr, nullptr, nullptr, 0, q, out);
 }
 
 namespace {
@@ -1090,9 +1270,10 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
   if (!x || !y) return fail(CONVF_ERR_INVALID_ARG, "x/y is NULL");
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(y) & 15))
     return fail(CONVF_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
-  const size_t esz = h->variant == CONVF_VARIANT_INT8 ? 1 : 2;
+  const bool q8bit = h->variant == CONVF_VARIANT_INT8 || h->variant == CONVF_VARIANT_INT8_TC;
+  const size_t esz = q8bit ? 1 : 2;
   const size_t xb = (size_t)s.N * s.H * s.W * s.C * esz;
-  const size_t yb = (size_t)s.M * s.K * (h->variant == CONVF_VARIANT_INT8 ? 1 : (h->out_bf16 ? 2 : 4));
+  const size_t yb = (size_t)s.M * s.K * (q8bit ? 1 : (h->out_bf16 ? 2 : 4));
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
   if (x0 < y0 + yb && y0 < x0 + xb) return fail(CONVF_ERR_INVALID_ARG, "x and y overlap");
   if (h->has_res) {
@@ -1161,6 +1342,27 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       ce = launch_tc_window(p, h->tmA, h->tmB, g.E, g.rows, h->grid, g.smem, strm);
       break;
     }
+    case CONVF_VARIANT_INT8_TC: {
+      // x - x_zero_point as exact bf16 into the handle's staging copy, then the tcgen05 GEMM in
+      // its integer-exact mode (the staging copy's tensor map was encoded at create)
+      ce = launch_q8_to_bf16(static_cast<const uint8_t*>(x), h->xq, (long long)s.N * s.H * s.W * s.C, h->x_signed,
+                             h->x_zp, h->num_sms, strm);
+      if (ce != cudaSuccess) break;
+      TcConvParams p{};
+      p.M = (int)s.M; p.Kout = s.K; p.num_kb = h->num_kb; p.cblocks = h->cblocks; p.R = s.R; p.S = s.S;
+      p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
+      p.H = s.H; p.W = s.W; p.C = s.C; p.Ho = s.Ho; p.Wo = s.Wo;
+      p.n_blocks = h->n_blocks; p.num_tiles = h->num_tiles; p.a_mode = h->a_mode;
+      p.x = h->xq; p.status = h->status; p.kpb = h->kpb; p.a3d = h->a3d ? 1 : 0; p.split_epi = 1;
+      p.iq_chunk_kb = h->iq_chunk_kb; p.iq_mode = h->iq_mode;
+      p.q_bias = h->q_bias; p.q_mult = h->q_mult; p.q_shift = h->q_shift; p.q_scale = h->q_scale;
+      p.q_zp = h->zp; p.q_lo = h->q_lo; p.q_hi = h->q_hi; p.y8 = static_cast<uint8_t*>(y);
+      if (h->bn == 64)
+        ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, false, false, strm);
+      else
+        ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, false, false, strm);
+      break;
+    }
     case CONVF_VARIANT_INT8: {
       S8Params p{};
       p.M = (int)s.M; p.Kout = s.K; p.C = s.C; p.H = s.H; p.W = s.W; p.Ho = s.Ho; p.Wo = s.Wo; p.R = s.R; p.S = s.S;
@@ -1175,7 +1377,7 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       if (x != h->map_x) {
         if ((st = encode_a_map(h, x)) != CONVF_OK) return st;
       }
-      TcConvParams p{};
+      TcConvParams p{};   // (the integer-exact 8-bit path has its own case above)
       p.M = (int)s.M; p.Kout = s.K; p.num_kb = h->num_kb; p.cblocks = h->cblocks; p.R = s.R; p.S = s.S;
       p.dh = s.dh; p.dw = s.dw; p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl;
       p.H = s.H; p.W = s.W; p.C = s.C; p.Ho = s.Ho; p.Wo = s.Wo;
@@ -1261,7 +1463,8 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (st != CONVF_OK) return st;
   if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
   static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
-                                "implicit_gemm_gather", "implicit_gemm_window", "implicit_gemm_halo"};
+                                "implicit_gemm_gather", "implicit_gemm_window", "implicit_gemm_halo",
+                                "int8_tcgen05_exact"};
   const Shape& s = h->s;
   if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     snprintf(buf, len,
@@ -1276,6 +1479,12 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->wg.bnp, h->wg.E, h->wg.rows ? 1 : 0,
              h->wg.cpt, h->wg.Wp,
              h->wg.stages, h->num_tiles, h->grid, h->dev_bytes);
+  else if (h->variant == CONVF_VARIANT_INT8_TC)
+    snprintf(buf, len,
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d kblocks_per_step=%d "
+             "act_box_per_step=%d exact_chunk_kblocks=%d requant=%s tiles=%d grid=%d weight_bytes=%zu",
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->bn, h->num_kb, h->kpb, h->a3d ? 1 : 0,
+             h->iq_chunk_kb, h->iq_mode ? "float32" : "fixed_point", h->num_tiles, h->grid, h->dev_bytes);
   else if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8)
     snprintf(buf, len, "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);

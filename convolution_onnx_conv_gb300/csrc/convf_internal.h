@@ -86,6 +86,20 @@ struct TcConvParams {
   // faster when a CTA has few tiles (its last tile's epilogue is the kernel's tail), slower
   // with many (twice the per-tile epilogue steps); 64+ column tiles without stream-K only
   int split_epi;
+  // ---- integer-exact mode (the IQ instantiation): the operands are integers held exactly in
+  // bf16 (8-bit values minus their zero points), so every product is an integer of at most 16
+  // bits; the fp32 accumulator restarts every iq_chunk_kb reduction blocks, a count chosen so
+  // that no partial sum exceeds 2^24 in magnitude (every partial sum is then an exactly
+  // represented integer), and the epilogue converts each chunk to int32 and adds the chunks.
+  int iq_chunk_kb;        // reduction blocks per exact chunk (a multiple of kpb)
+  int iq_mode;            // requantisation: 0 fixed point (static int8), 1 float32 (QLinearConv)
+  const int32_t* q_bias;  // [Kpad] int32 bias added to the exact sum
+  const int32_t* q_mult;  // [Kpad] mode 0: multiplier M (> 0)
+  const int32_t* q_shift; // [Kpad] mode 0: shift sh (1..62): q = (v*M + 2^(sh-1)) >> sh
+  const float* q_scale;   // [Kpad] mode 1: float32 multiplier m: q = rint(float(v) * m)
+  int q_zp;               // output zero point, added after the rounding
+  int q_lo, q_hi;         // output clamp (the 8-bit type's range, the zero point below for ReLU)
+  uint8_t* y8;            // NHWC 8-bit output [M][Kout] (int8 or uint8 bits)
 };
 
 // Pipeline stages (64-wide k-blocks held in shared memory) of the TMA implicit-GEMM kernel per
@@ -96,6 +110,11 @@ constexpr int tc_conv_stages(int bn, bool gather, bool pair) {
 }
 
 
+
+// 8-bit NHWC (int8 when is_signed, else uint8) -> bf16 bits of (x - zp), exact (|x - zp| <= 255);
+// n elements, n % 8 == 0, both pointers 16-byte aligned.
+cudaError_t launch_q8_to_bf16(const uint8_t* x, uint16_t* out, long long n, int is_signed, int zp, int num_sms,
+                              cudaStream_t stream);
 
 // ---------------------------------------------------------------- halo-tile implicit GEMM
 // Stride-1, dilation-1 convolutions: the output is indexed in rows of Wp = W + pl + pr

@@ -2,6 +2,8 @@
 // NHWC bf16 with cpt channels (4 or 8), the extra channels zero, so that each filter tap of a
 // pixel is one aligned 8- or 16-byte vector.  One thread per pixel; reads and writes are
 // consecutive across the warp.
+#include <cuda_bf16.h>
+
 #include "convf_internal.h"
 #include "ptx.cuh"
 
@@ -32,6 +34,60 @@ cudaError_t launch_pad_channels(const uint16_t* x, uint16_t* out, long long pixe
   if (blocks > cap) blocks = cap;
   return launch_pdl(pad_channels_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, x, out, pixels,
                     C, cpt);
+}
+
+// 8-bit activations for the integer-exact tcgen05 path: each byte b (int8 or uint8) becomes the
+// bf16 bits of b - zp, an integer of magnitude at most 255 and therefore exact in bf16 (8
+// significant bits).  Zero-filled padding taps then stand for the zero point, as ONNX's
+// quantized convolutions pad.  16 bytes in, 32 bytes out per thread and step.
+__device__ __forceinline__ uint32_t q8pair_to_bf16x2(uint32_t b0, uint32_t b1, int is_signed, int zp) {
+  const int v0 = (is_signed ? static_cast<int>(static_cast<int8_t>(b0)) : static_cast<int>(b0)) - zp;
+  const int v1 = (is_signed ? static_cast<int>(static_cast<int8_t>(b1)) : static_cast<int>(b1)) - zp;
+  const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(v0), static_cast<float>(v1));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(256) q8_to_bf16_kernel(const uint8_t* __restrict__ x, uint16_t* __restrict__ out,
+                                                         long long n, int is_signed, int zp) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
+  const long long groups = n >> 3;   // 8 elements per group (n % 8 == 0)
+  for (long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 2; g < groups;
+       g += static_cast<long long>(gridDim.x) * blockDim.x * 2) {
+    if (g + 1 < groups) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + g * 8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = q8pair_to_bf16x2(w[i] & 0xff, (w[i] >> 8) & 0xff, is_signed, zp);
+        o[2 * i + 1] = q8pair_to_bf16x2((w[i] >> 16) & 0xff, w[i] >> 24, is_signed, zp);
+      }
+      *reinterpret_cast<uint4*>(out + g * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(out + g * 8 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + g * 8));
+      const uint32_t w[2] = {v.x, v.y};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        o[2 * i] = q8pair_to_bf16x2(w[i] & 0xff, (w[i] >> 8) & 0xff, is_signed, zp);
+        o[2 * i + 1] = q8pair_to_bf16x2((w[i] >> 16) & 0xff, w[i] >> 24, is_signed, zp);
+      }
+      *reinterpret_cast<uint4*>(out + g * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+cudaError_t launch_q8_to_bf16(const uint8_t* x, uint16_t* out, long long n, int is_signed, int zp, int num_sms,
+                              cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const long long pairs = (n / 8 + 1) / 2;
+  long long blocks = (pairs + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(q8_to_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, x, out, n,
+                    is_signed, zp);
 }
 
 }  // namespace convf

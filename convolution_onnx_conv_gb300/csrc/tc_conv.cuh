@@ -96,19 +96,26 @@ struct SegSched {
 // EXT: the epilogue adds a residual and/or stores bf16 (TcConvParams::res, out_bf16); its own
 // instantiation, so the plain fp32 epilogue keeps its code (a shared one cost 1.3% of the
 // ResNet-50 step).
-template <int BN, bool GATHER, bool PAIR, bool SK, bool EXT>
+// IQ: integer-exact mode for 8-bit convolutions (TcConvParams::iq_*): the accumulator restarts
+// every iq_chunk_kb reduction blocks into alternating TMEM buffers; both epilogue warpgroups
+// drain every chunk (one column half each), add it to int32 sums held in registers and, after a
+// tile's last chunk, requantise and store 8-bit outputs.
+template <int BN, bool GATHER, bool PAIR, bool SK, bool EXT, bool IQ = false>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
+  static_assert(!(IQ && (GATHER || PAIR || SK || EXT)), "the integer-exact mode runs whole tiles on single CTAs");
+  static_assert(!IQ || BN == 64 || BN == 128, "the integer-exact epilogue holds 32 or 64 int32 sums per thread");
   using Cfg = TcCfg<BN, GATHER, PAIR>;
   // TcConvParams::split_epi on whole tiles of 64+ columns: both epilogue groups drain every
   // tile, one column half each (a tile's epilogue takes half as long, which shortens the last
   // tile of every CTA); otherwise (many tiles per CTA, stream-K segments, 32-column tiles,
   // gather mode) the groups take alternate tiles
-  const bool split_epi = Cfg::kSplitEpiOk && !SK && p.split_epi;
+  // (the integer-exact mode always splits: both groups then wait on every chunk in order)
+  const bool split_epi = Cfg::kSplitEpiOk && !SK && (IQ || p.split_epi);
   // CTA pair (cluster of 2): the leader (rank 0) issues M = 256 MMAs over both CTAs' smem into
   // both CTAs' TMEM; each CTA loads its own 128 activation rows and half of the weight tile.
   const uint32_t crank = PAIR ? cluster_ctarank() : 0;
@@ -161,12 +168,14 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     if (!GATHER) tma_prefetch_desc(&tmA);
   }
   if (warp == 2 && lane == 0) tma_prefetch_desc(&tmB);
+  // the integer-exact mode keeps its running int32 sums in a third BN-column region
+  constexpr uint32_t kTmemAlloc = IQ ? 512u : static_cast<uint32_t>(Cfg::kTmemCols);
   if (warp == 1) {
     if (PAIR) {
-      tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+      tmem_alloc_pair(tmem_slot, kTmemAlloc);
       tmem_relinquish_pair();
     } else {
-      tmem_alloc(tmem_slot, Cfg::kTmemCols);
+      tmem_alloc(tmem_slot, kTmemAlloc);
       tmem_relinquish();
     }
   }
@@ -359,6 +368,40 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       SegSched<SK> sched(p, tstart, tstep);
       int tile, ka, kend;
       while (sched.next(tile, ka, kend)) {
+        if (IQ) {
+          // exact chunks: the accumulator restarts every iq_chunk_kb blocks, each chunk into the
+          // next TMEM buffer (the epilogue adds the chunks in int32)
+          for (int c0 = ka; c0 < kend; c0 += p.iq_chunk_kb) {
+            if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            const int c1 = min(c0 + p.iq_chunk_kb, kend);
+            for (int kb = c0; kb < c1; kb += kpb) {
+              if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) goto teardown;
+              tc_fence_after();
+              for (int j = 0; j < kpb; ++j) {
+                const uint64_t adesc = adesc0 + (((stage + j) * kATileBytes) >> 4);
+                const uint64_t bdesc = bdesc0 + (((stage + j) * Cfg::kBTileBytes) >> 4);
+                const uint32_t first = kb + j != c0;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k == 0 ? first : 1u);
+              }
+              tc_commit(&empty[stage]);
+              stage += kpb;
+              if (stage == kStages) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            tc_commit(&tfull[acc]);
+            if (++acc == 2) {
+              acc = 0;
+              acc_phase ^= 1;
+            }
+          }
+          continue;
+        }
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) goto teardown;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -418,6 +461,94 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     constexpr int G = Cfg::kEpiGroups;
     const int eg = (warp - 3) >> 2;        // epilogue group
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    if constexpr (IQ) {
+      // ---- integer-exact epilogue: thread = tile row 32q + lane, columns [eg*BN/2, (eg+1)*BN/2).
+      // The running int32 sums live in TMEM columns [2*BN, 3*BN) (this warp's lanes), so a thread
+      // only ever holds 16 columns in registers.
+      constexpr int HC = BN / 2;           // this group's columns of a tile
+      const int nch = (p.num_kb + p.iq_chunk_kb - 1) / p.iq_chunk_kb;
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t sums = lane_base + static_cast<uint32_t>(2 * BN + eg * HC);
+      SegSched<false> sched(p, tstart, tstep);
+      int tile, ka, kend;
+      int chunk = 0;                       // chunks drained by this CTA so far (buffer, phase)
+      while (sched.next(tile, ka, kend)) {
+        const int row = (tile / p.n_blocks) * kBM + q * 32 + lane;
+        const int n0 = (tile % p.n_blocks) * BN;
+        const int c0 = n0 + eg * HC;       // this group's first output channel
+        const bool has_cols = c0 < p.Kout;
+        for (int c = 0; c < nch; ++c, ++chunk) {
+          const int acc = chunk & 1;
+          if (!mbar_wait(&tfull[acc], (chunk >> 1) & 1, abort_flag, p.status)) goto teardown;
+          tc_fence_after();
+          if (has_cols) {
+            const uint32_t buf = lane_base + static_cast<uint32_t>(acc * BN + eg * HC);
+#pragma unroll 1
+            for (int h = 0; h < HC / 16; ++h) {
+              uint32_t v[16], t[16];
+              tmem_ld_32x32b_x16(buf + 16 * h, v);
+              if (c > 0) tmem_ld_32x32b_x16(sums + 16 * h, t);
+              tmem_ld_wait();
+              // every chunk sum is an integer of magnitude <= 2^24: the conversion is exact
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                t[i] = static_cast<uint32_t>((c > 0 ? static_cast<int>(t[i]) : 0) + __float2int_rn(__uint_as_float(v[i])));
+              tmem_st_32x32b_x16(sums + 16 * h, t);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);   // the chunk buffer is free for the MMA again
+        }
+        if (!has_cols) continue;
+        uint8_t* yrow = p.y8 + static_cast<size_t>(row) * p.Kout;
+#pragma unroll 1
+        for (int g = 0; g < HC / 16; ++g) {
+          const int col = c0 + 16 * g;
+          uint32_t t[16];
+          tmem_ld_32x32b_x16(sums + 16 * g, t);   // warp-collective: before any per-thread exit
+          tmem_ld_wait();
+          if (col >= p.Kout || row >= p.M) continue;   // Kout % 16 == 0: whole 16-channel groups
+          uint32_t packed[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int4 bv = __ldg(reinterpret_cast<const int4*>(p.q_bias + col + 4 * h));
+            const int bb[4] = {bv.x, bv.y, bv.z, bv.w};
+            int qv[4];
+            if (p.iq_mode == 0) {
+              const int4 mv = __ldg(reinterpret_cast<const int4*>(p.q_mult + col + 4 * h));
+              const int4 sv = __ldg(reinterpret_cast<const int4*>(p.q_shift + col + 4 * h));
+              const int mm[4] = {mv.x, mv.y, mv.z, mv.w};
+              const int ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // q = (v*M + 2^(sh-1)) >> sh in 64 bits (arithmetic shift: rounds half up)
+                const long long v = static_cast<long long>(static_cast<int>(t[4 * h + e])) + bb[e];
+                const long long r = (v * mm[e] + (1LL << (ss[e] - 1))) >> ss[e];
+                const long long o = r + p.q_zp;
+                qv[e] = static_cast<int>(o < p.q_lo ? p.q_lo : (o > p.q_hi ? p.q_hi : o));
+              }
+            } else {
+              const float4 fv = __ldg(reinterpret_cast<const float4*>(p.q_scale + col + 4 * h));
+              const float ff[4] = {fv.x, fv.y, fv.z, fv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // float32 steps, each rounded to nearest even: float(v) * m, then to an integer
+                const long long v = static_cast<long long>(static_cast<int>(t[4 * h + e])) + bb[e];
+                const float pr = __fmul_rn(__ll2float_rn(v), ff[e]);
+                const long long o = static_cast<long long>(__float2int_rn(fminf(fmaxf(pr, -1.0e9f), 1.0e9f))) + p.q_zp;
+                qv[e] = static_cast<int>(o < p.q_lo ? p.q_lo : (o > p.q_hi ? p.q_hi : o));
+              }
+            }
+            packed[h] = (static_cast<uint32_t>(qv[0]) & 0xffu) | ((static_cast<uint32_t>(qv[1]) & 0xffu) << 8) |
+                        ((static_cast<uint32_t>(qv[2]) & 0xffu) << 16) | ((static_cast<uint32_t>(qv[3]) & 0xffu) << 24);
+          }
+          *reinterpret_cast<uint4*>(yrow + col) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+      }
+      goto teardown;
+    }
     const bool glead = warp == 3 + 4 * eg && lane == 0;   // group leader thread
     float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kEpiWarpBytes);
     const int sub = lane >> 3;             // row within each group of four in the store phase
@@ -844,17 +975,17 @@ teardown:
     __syncwarp();
     tc_fence_after();
     if (PAIR)
-      tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+      tmem_dealloc_pair(tmem_base, kTmemAlloc);
     else
-      tmem_dealloc(tmem_base, Cfg::kTmemCols);
+      tmem_dealloc(tmem_base, kTmemAlloc);
   }
 }
 
-template <int BN, bool GATHER, bool PAIR, bool SK = false, bool EXT = false>
+template <int BN, bool GATHER, bool PAIR, bool SK = false, bool EXT = false, bool IQ = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXT>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXT, IQ>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcCfg<BN, GATHER, PAIR>::kSmem);

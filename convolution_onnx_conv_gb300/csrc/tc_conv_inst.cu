@@ -12,6 +12,15 @@ namespace convf {
 cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const CUtensorMap& tmA,
                                                    const CUtensorMap& tmB, int grid,
                                                    bool gather, bool pair, cudaStream_t stream) {
+  if (p.y8 != nullptr) {
+    // integer-exact 8-bit convolution: single CTAs, whole tiles, 64- or 128-wide tiles
+    if (gather || pair || p.sk) return cudaErrorInvalidValue;
+#if CONVF_BN == 64 || CONVF_BN == 128
+    return launch_tc_conv_t<CONVF_BN, false, false, false, false, true>(p, tmA, tmB, grid, stream);
+#else
+    return cudaErrorInvalidValue;
+#endif
+  }
   if (p.res != nullptr || p.out_bf16) {
     // residual and/or bf16 output: the extended-epilogue instantiations
     if (gather) return cudaErrorInvalidValue;

@@ -90,6 +90,39 @@ def int8_inputs(spec: ConvSpec, seed: int) -> Dict[str, torch.Tensor]:
     return {"x": x, "w": w, "bias": bias, "mult": mult, "shift": shift}
 
 
+def qlinear_inputs(spec: ConvSpec, seed: int, x_signed: bool = False, w_signed: bool = True,
+                   y_signed: bool = False) -> Dict[str, object]:
+    """ONNX QLinearConv operands: x (uint8 U{0..255} or int8 U{-128..127}) with a zero point near
+    the middle of its range, w (int8 U{-127..127} or uint8 U{0..255}) with small per-channel zero
+    points, int32 bias U{-2^15..2^15}, x_scale ~ U[0.01, 0.03], w_scale[k] ~ U[0.002, 0.006], and
+    y_scale / y_zero_point chosen so that the outputs span the 8-bit range (y_scale = 4 sigma of
+    the real-valued sums / 127)."""
+    g = _gen(seed)
+    Cg = spec.C // spec.group
+    xs = (spec.N, spec.C, spec.H, spec.W)
+    ws = (spec.K, Cg, spec.R, spec.S)
+    if x_signed:
+        x = torch.randint(-128, 128, xs, generator=g, dtype=torch.int8)
+        x_zp = int(torch.randint(-30, 31, (1,), generator=g))
+    else:
+        x = torch.randint(0, 256, xs, generator=g, dtype=torch.int32).to(torch.uint8)
+        x_zp = int(torch.randint(98, 159, (1,), generator=g))
+    if w_signed:
+        w = torch.randint(-127, 128, ws, generator=g, dtype=torch.int8)
+        w_zp = torch.randint(-10, 11, (spec.K,), generator=g, dtype=torch.int32)
+    else:
+        w = torch.randint(0, 256, ws, generator=g, dtype=torch.int32).to(torch.uint8)
+        w_zp = torch.randint(118, 139, (spec.K,), generator=g, dtype=torch.int32)
+    bias = torch.randint(-(1 << 15), (1 << 15) + 1, (spec.K,), generator=g, dtype=torch.int32)
+    x_scale = float(_uniform(g, (1,), 0.01, 0.03))
+    w_scale = _uniform(g, (spec.K,), 0.002, 0.006)
+    sigma = 74.0 * 74.0 * math.sqrt(Cg * spec.R * spec.S) * x_scale * float(w_scale.mean())
+    y_scale = float(4.0 * sigma / 127.0)
+    y_zp = int(torch.randint(-20, 21, (1,), generator=g)) if y_signed else int(torch.randint(100, 157, (1,), generator=g))
+    return {"x": x, "x_zp": x_zp, "w": w, "w_zp": w_zp, "bias": bias, "x_scale": x_scale, "w_scale": w_scale,
+            "y_scale": y_scale, "y_zp": y_zp, "x_signed": x_signed, "y_signed": y_signed}
+
+
 def sample_points(spec: ConvSpec, count: int, seed: int) -> torch.Tensor:
     """``count`` output coordinates (n, k, oh, ow), always including the corners
     and edges of the output (where padding matters) and the last channel."""

@@ -63,7 +63,9 @@ typedef enum {
   CONVF_ERR_TIMEOUT = -5       /* a bounded device wait ran out during a run */
 } convf_status;
 
-typedef enum { CONVF_BF16 = 0, CONVF_S8 = 1 } convf_dtype;
+/* CONVF_Q8: ONNX QLinearConv -- 8-bit x, W and y with scales and zero points
+ * (conv_fused_create_qlinear); the element types are given by its convf_qparams. */
+typedef enum { CONVF_BF16 = 0, CONVF_S8 = 1, CONVF_Q8 = 2 } convf_dtype;
 /* element type of y (and of the residual) on the bf16 path */
 typedef enum { CONVF_OUT_F32 = 0, CONVF_OUT_BF16 = 1 } convf_out_dtype;
 typedef enum { CONVF_NCHW = 0, CONVF_NHWC = 1 } convf_layout;
@@ -82,7 +84,9 @@ typedef enum {
   CONVF_VARIANT_IMPLICIT_GEMM = 1,   /* tcgen05 implicit GEMM, TMA im2col activation tiles */
   CONVF_VARIANT_GEMM_1X1 = 2,        /* same kernel, activations read as a [N*H*W][C] matrix */
   CONVF_VARIANT_DEPTHWISE = 3,       /* CUDA-core depthwise (group == C == K) */
-  CONVF_VARIANT_INT8 = 4,            /* int8 tensor-core MMA, int32 accumulate, requant */
+  CONVF_VARIANT_INT8 = 4,            /* int8 warp-level MMA (mma.sync), int32 accumulate, requant;
+                                        C % 64 == 0, K % 16 == 0.  Chosen only when the
+                                        exact-integer tcgen05 variant cannot serve the shape */
   CONVF_VARIANT_IMPLICIT_GEMM_GATHER = 5, /* tcgen05 implicit GEMM, activation rows gathered by
                                             threads (any C, e.g. the 3-channel stem) */
   CONVF_VARIANT_IMPLICIT_GEMM_WINDOW = 6, /* tcgen05 implicit GEMM for C <= 8: a pre-pass pads the
@@ -94,7 +98,7 @@ typedef enum {
                                             1, sw*cpt*2 a multiple of 16 bytes, S*cpt <= 64,
                                             R*round_up(S*cpt,16) <= 256, K <= 256.  The selector
                                             takes it for outputs at least 32 pixels wide. */
-  CONVF_VARIANT_IMPLICIT_GEMM_HALO = 7    /* tcgen05 implicit GEMM for stride-1, dilation-1
+  CONVF_VARIANT_IMPLICIT_GEMM_HALO = 7,   /* tcgen05 implicit GEMM for stride-1, dilation-1
                                             filters: output rows padded to the input width
                                             Wp = W + pl + pr <= 128, tiles of floor(128/Wp)
                                             output rows; per 64-channel block one TMA box of
@@ -102,6 +106,14 @@ typedef enum {
                                             shifted shared-memory descriptors (im2col reloads
                                             it once per tap).  The selector takes it when at
                                             least 60% of a tile's 128 rows are real outputs. */
+  CONVF_VARIANT_INT8_TC = 8          /* 8-bit convs (CONVF_S8, CONVF_Q8) on tcgen05: a pre-pass writes
+                                        x - x_zero_point as bf16 (exact: |v| <= 255) into a handle
+                                        workspace, the weights are prepacked as bf16 w - w_zero_point,
+                                        and the tcgen05 implicit GEMM restarts its fp32 accumulator
+                                        every chunk of reduction blocks small enough that no partial
+                                        sum exceeds 2^24 (so every partial sum is an exact integer);
+                                        the epilogue adds the chunks in int32 and requantises.
+                                        Bit-exact.  C % 8 == 0, K % 16 == 0, group 1. */
 } convf_variant;
 
 typedef struct {
@@ -144,6 +156,24 @@ typedef struct {
 } convf_desc;
 
 typedef struct convf_handle convf_handle;
+
+/* Quantisation parameters of ONNX QLinearConv (public operator specification): real x =
+ * (x - x_zero_point) * x_scale, real w[k] = (w[k] - w_zero_point[k]) * w_scale[k], y =
+ * saturate(round(conv_real / y_scale) + y_zero_point), bias int32 in units of x_scale *
+ * w_scale[k].  Each zero point has its tensor's element type.  The rounding step is taken in
+ * float32 (the specification fixes no precision): m[k] = float32(x_scale * w_scale[k] / y_scale)
+ * formed in double, then y = saturate(round_half_even(float32(acc + bias[k]) * m[k]) + y_zp),
+ * where acc = sum (x - x_zp)(w - w_zp[k]) is exact and the padded input stands for x_zp. */
+typedef struct {
+  int x_signed, w_signed, y_signed;  /* element types: 1 = int8, 0 = uint8                   */
+  int32_t x_zero_point;              /* in x's range                                          */
+  const int32_t* w_zero_point;       /* host [K], each in w's range (per output channel)     */
+  float x_scale;                     /* > 0, finite                                           */
+  const float* w_scale;              /* host [K], > 0, finite                                 */
+  float y_scale;                     /* > 0, finite                                           */
+  int32_t y_zero_point;              /* in y's range                                          */
+  int relu;                          /* 1: clamp below at y_zero_point (a fused Relu)         */
+} convf_qparams;
 
 /* Output logical shape [N][K][Ho][Wo] of desc (ONNX Conv shape rule, auto_pad resolved).
  * CONVF_ERR_INVALID_ARG if the attributes are malformed or the window does not fit. */
@@ -192,8 +222,18 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
                                const int32_t* requant_mult, const int32_t* requant_shift,
                                int32_t out_zero_point, convf_handle** out);
 
-/* Run the fused conv: x (device, NHWC, bf16 bits or int8) -> y (device, NHWC, float32 -- or bf16
- * bits with out_dtype = CONVF_OUT_BF16 -- for the bf16 path, int8 for the s8 path).  Both must be 16-byte aligned and must not overlap.
+/* ONNX QLinearConv ("onnx-vulkan-rs", notes on the quantized kernels: zero-point corrected integer
+ * sums, a +-1 LSB contract against other runtimes): desc->dtype must be CONVF_Q8 (act and the
+ * performance knobs other than tile_n are ignored; use q->relu).
+ *   W:    host [K][C/group][R][S], int8 or uint8 per q->w_signed.
+ *   bias: host int32[K] or NULL.
+ *   q:    the scales and zero points above (copied).
+ * Served by CONVF_VARIANT_INT8_TC only.  run then takes 8-bit x and writes 8-bit y. */
+convf_status conv_fused_create_qlinear(const convf_desc* desc, const void* W, const int32_t* bias,
+                                       const convf_qparams* q, convf_handle** out);
+
+/* Run the fused conv: x (device, NHWC, bf16 bits or 8-bit) -> y (device, NHWC, float32 -- or bf16
+ * bits with out_dtype = CONVF_OUT_BF16 -- for the bf16 path, 8-bit for the s8 and q8 paths).  Both must be 16-byte aligned and must not overlap.
  * `stream` is a cudaStream_t (NULL = legacy default stream).  Asynchronous: no allocation,
  * no synchronisation; launch errors are returned as CONVF_ERR_CUDA. */
 convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* stream);

@@ -365,9 +365,11 @@ def qlinear_multiplier(x_scale, w_scale, y_scale, K):
     return (np.float64(np.float32(x_scale)) * ws / np.float64(np.float32(y_scale))).astype(np.float32)
 
 
-def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uint8):
+def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uint8, relu=False):
     """y = saturate(round_half_even(float32(acc) * m[k]) + y_zp) for NCHW acc (module docstring:
-    float32 steps, each rounded to nearest even).  y's type is y_zero_point's type."""
+    float32 steps, each rounded to nearest even).  y's type is y_zero_point's type.  ``relu``: a
+    Relu fused after the conv, which in the quantized domain keeps the codes whose real value
+    (y - y_zp) * y_scale is >= 0, i.e. raises every code below y_zp to y_zp."""
     if np.dtype(y_dtype) not in (np.dtype(np.uint8), np.dtype(np.int8)):
         raise ValueError("QLinearConv's y is uint8 or int8")
     _check_range(y_zero_point, y_dtype, "y_zero_point")
@@ -377,7 +379,10 @@ def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uin
     p = acc.astype(np.float32) * m.reshape(1, K, 1, 1)          # float32 * float32 -> float32
     v = np.rint(p).astype(np.int64) + int(y_zero_point)
     info = np.iinfo(y_dtype)
-    return np.clip(v, info.min, info.max).astype(y_dtype)
+    y = np.clip(v, info.min, info.max)
+    if relu:
+        y = np.maximum(y, int(y_zero_point))
+    return y.astype(y_dtype)
 
 
 # ------------------------------------------------------------- whole pipeline

@@ -105,3 +105,34 @@ def check_sampled(spec: ConvSpec, seed: int, count: int = 2000, variant=cf.CONVF
     got = y.numpy()[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
     ok, worst, idx = compare(got, ref, spec.dtype == "s8")
     return ok, worst, idx, status, used, desc, y
+
+
+# ------------------------------------------------------------------ QLinearConv
+
+def make_qconv(spec: ConvSpec, inp, relu=False, variant=cf.CONVF_VARIANT_AUTO, **kw):
+    return cf.QLinearConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                          x_scale=inp["x_scale"], x_zero_point=inp["x_zp"], w_scale=inp["w_scale"].numpy(),
+                          w_zero_point=inp["w_zp"].numpy(), y_scale=inp["y_scale"], y_zero_point=inp["y_zp"],
+                          x_signed=inp["x_signed"], y_signed=inp["y_signed"], relu=relu, stride=spec.stride,
+                          pads=spec.pads, dilation=spec.dilation, group=spec.group, variant=variant, **kw)
+
+
+def oracle_qlinear(spec: ConvSpec, inp, relu=False):
+    acc = oracle.qlinear_conv_acc(inp["x"].numpy(), inp["x_zp"], inp["w"].numpy(), inp["w_zp"].numpy(),
+                                  inp["bias"].numpy(), spec.stride, spec.pads, spec.dilation, spec.group)
+    return oracle.qlinear_requant(acc, inp["x_scale"], inp["w_scale"].numpy(), inp["y_scale"], inp["y_zp"],
+                                  np.int8 if inp["y_signed"] else np.uint8, relu=relu)
+
+
+def check_qlinear(spec: ConvSpec, inp, relu=False, **kw):
+    """(mismatch count, flat index of the first mismatch, status, describe) over every output."""
+    conv = make_qconv(spec, inp, relu, **kw)
+    x = to_device_nhwc(inp["x"])
+    y = conv(x)
+    torch.cuda.synchronize()
+    status, desc = conv.status(), conv.describe()
+    conv.close()
+    got = y.cpu().contiguous().numpy()
+    ref = oracle_qlinear(spec, inp, relu)
+    bad = np.flatnonzero(got.reshape(-1) != ref.reshape(-1))
+    return int(bad.size), int(bad[0]) if bad.size else -1, status, desc

@@ -397,7 +397,7 @@ INT8_SMALL = [
 
 @pytest.mark.parametrize("spec", INT8_SMALL, ids=[s.name for s in INT8_SMALL])
 def test_int8_bit_exact(spec):
-    _assert(check_full(spec, 7400 + INT8_SMALL.index(spec)), spec, V.CONVF_VARIANT_INT8)
+    _assert(check_full(spec, 7400 + INT8_SMALL.index(spec)), spec, V.CONVF_VARIANT_INT8_TC)
 
 
 def test_int8_zero_point_and_saturation():

@@ -56,7 +56,7 @@ def desc(**kw):
     (dict(group=2, K=32), cf.CONVF_ERR_UNSUPPORTED, "no kernel serves"),
     (dict(C=12, K=12, group=12), cf.CONVF_ERR_UNSUPPORTED, "C % 8"),
     (dict(K=30), cf.CONVF_ERR_UNSUPPORTED, "K % 4"),
-    (dict(dtype=cf.CONVF_S8, C=48), cf.CONVF_ERR_UNSUPPORTED, "C % 64"),
+    (dict(dtype=cf.CONVF_S8, C=12), cf.CONVF_ERR_UNSUPPORTED, "C % 64"),
     (dict(dtype=cf.CONVF_S8, C=64, act=cf.CONVF_ACT_RELU6), cf.CONVF_ERR_UNSUPPORTED, "int8"),
     (dict(variant=cf.CONVF_VARIANT_GEMM_1X1), cf.CONVF_ERR_UNSUPPORTED, "forced variant"),
     (dict(variant=cf.CONVF_VARIANT_DEPTHWISE), cf.CONVF_ERR_UNSUPPORTED, "group == C == K"),
@@ -162,7 +162,8 @@ def test_selector_on_the_workloads():
         v, bn, kt = cf.conv_fused_plan(d)
         names[spec.name] = v
         if spec.dtype == "s8":
-            assert v == cf.CONVF_VARIANT_INT8
+            # the exact-integer tcgen05 kernel: 3x3 with 64-channel runs per tap, 128- or 64-wide tiles
+            assert v == cf.CONVF_VARIANT_INT8_TC and kt == 9 * spec.C and bn in (64, 128)
         elif spec.group > 1:
             assert v == cf.CONVF_VARIANT_DEPTHWISE
         elif spec.C == 3:
@@ -344,3 +345,67 @@ def test_halo_variant_rules(W, pads, R, S, ok):
     strided = cf.make_desc(2, 64, 12, 20, 64, 3, 3, (2, 2), (1, 1, 1, 1), variant=cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     with pytest.raises(cf.ConvFusedError):
         cf.conv_fused_plan(strided)
+
+
+def _qdesc(C=64, K=64, R=3, pads=(1, 1, 1, 1), **kw):
+    return cf.make_desc(2, C, 8, 8, K, R, R, (1, 1), pads, dtype=cf.CONVF_Q8, **kw)
+
+
+def _qparams(K, xz=128, wz=0, x_signed=0, w_signed=1, y_signed=0, yz=120, xs=0.02, ws=0.004, ys=0.5):
+    q = cf.QParams()
+    q.x_signed, q.w_signed, q.y_signed = x_signed, w_signed, y_signed
+    q.x_zero_point, q.y_zero_point = xz, yz
+    q.x_scale, q.y_scale = xs, ys
+    wzs = np.full(K, wz, np.int32)
+    wss = np.full(K, ws, np.float32)
+    q.w_zero_point, q.w_scale = wzs.ctypes.data, wss.ctypes.data
+    q.relu = 0
+    return q, (wzs, wss)
+
+
+def test_qlinear_create_refuses_before_any_cuda_call():
+    """Every QLinearConv refusal (zero points outside their types, bad scales, shapes the
+    exact-integer kernel cannot serve, the wrong entry point) happens on the host."""
+    w = np.zeros((64, 64, 3, 3), np.int8)
+    cases = [
+        (dict(xz=300), "x_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(xz=-1), "x_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(x_signed=1, xz=128), "x_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(yz=-3), "y_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(y_signed=1, yz=200), "y_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(wz=130), "w_zero_point", cf.CONVF_ERR_INVALID_ARG),
+        (dict(xs=0.0), "x_scale", cf.CONVF_ERR_INVALID_ARG),
+        (dict(ws=-1.0), "w_scale", cf.CONVF_ERR_INVALID_ARG),
+    ]
+    for kw, word, status in cases:
+        q, keep = _qparams(64, **kw)
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_create_qlinear(_qdesc(), w, None, q)
+        assert e.value.status == status and word in str(e.value), (kw, str(e.value))
+    q, keep = _qparams(64)
+    for desc, word in ((_qdesc(C=12, K=64), "C % 8"), (_qdesc(K=40), "K % 16"),
+                       (cf.make_desc(2, 64, 8, 8, 64, 3, 3, (1, 1), (1, 1, 1, 1), group=2, dtype=cf.CONVF_Q8),
+                        "group")):
+        with pytest.raises(cf.ConvFusedError) as e:
+            cf.conv_fused_create_qlinear(desc, np.zeros((desc.K, desc.C // desc.group, 3, 3), np.int8), None, q)
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and word in str(e.value), str(e.value)
+    # the plain create refuses CONVF_Q8 and the QLinearConv create refuses other dtypes
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(_qdesc(), w)
+    assert "conv_fused_create_qlinear" in str(e.value)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create_qlinear(cf.make_desc(2, 64, 8, 8, 64, 3, 3, (1, 1), (1, 1, 1, 1), dtype=cf.CONVF_S8),
+                                     w, None, q)
+    assert "CONVF_Q8" in str(e.value)
+
+
+def test_int8_selector_prefers_the_exact_tcgen05_kernel():
+    d = cf.make_desc(64, 128, 28, 28, 128, 3, 3, (1, 1), (1, 1, 1, 1), dtype=cf.CONVF_S8)
+    assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_INT8_TC
+    d.variant = cf.CONVF_VARIANT_INT8
+    assert cf.conv_fused_plan(d)[0] == cf.CONVF_VARIANT_INT8
+    # K % 16 != 0: neither kernel serves it
+    d = cf.make_desc(2, 64, 8, 8, 40, 3, 3, (1, 1), (1, 1, 1, 1), dtype=cf.CONVF_S8)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_plan(d)
+    assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "K % 16" in str(e.value)

@@ -572,3 +572,17 @@ def test_qlinear_requant_takes_float32_steps():
     acc = np.array([5], dtype=np.int64).reshape(1, 1, 1, 1)
     y = oracle.qlinear_requant(acc, 0.1, np.array([1.0], np.float32), 1.0, 0, np.int8)
     assert y.reshape(-1).tolist() == [0]
+
+
+def test_qlinear_relu_keeps_the_codes_of_non_negative_real_values():
+    """A fused Relu in the quantized domain: dequantized, the result is max(dequantized y, 0)."""
+    rng = np.random.default_rng(62)
+    acc = rng.integers(-40000, 40000, (2, 4, 3, 3)).astype(np.int64)
+    for y_dtype, zp in ((np.uint8, 120), (np.int8, -7)):
+        y = oracle.qlinear_requant(acc, 0.02, np.array([0.004, 0.003, 0.005, 0.002], np.float32), 0.3, zp, y_dtype)
+        yr = oracle.qlinear_requant(acc, 0.02, np.array([0.004, 0.003, 0.005, 0.002], np.float32), 0.3, zp, y_dtype,
+                                    relu=True)
+        real = (y.astype(np.int64) - zp) * 0.3
+        real_r = (yr.astype(np.int64) - zp) * 0.3
+        assert np.array_equal(real_r, np.maximum(real, 0.0))
+        assert (yr < zp).sum() == 0 and (y < zp).any()
