@@ -186,6 +186,28 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   // setup above touched only smem/TMEM: overlap it with the previous kernel's tail
   pdl_launch_dependents();
+  // The weights are not written by the previous kernel: the weight producer issues the weight
+  // boxes of its first pipeline steps (one pass over the free stages) before waiting for it, so
+  // only the activations are on the critical path when it completes.  Those stages get the
+  // weight bytes as expected transactions without an arrival; the producer arrives on them
+  // after the wait (with its share of the activation bytes), so no phase can complete early.
+  int pre_steps = 0;
+  if (!PAIR && warp == 2 && lane == 0) {
+    SegSched<SK> sched(p, tstart, tstep);
+    int tile, ka, kend;
+    if (sched.next(tile, ka, kend)) {
+      const int n0 = (tile % p.n_blocks) * BN;
+      const int kpb0 = GATHER ? 1 : p.kpb;
+      for (int kb = ka; kb < kend && (pre_steps + 1) * kpb0 <= kStages; kb += kpb0, ++pre_steps) {
+        const int stage = pre_steps * kpb0;
+        mbar_expect_tx(&full[stage], static_cast<uint32_t>(kpb0 * Cfg::kBTileBytes));
+        if (kpb0 == 1)
+          tma_load_2d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], kb * kBK, n0);
+        else
+          tma_load_3d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], 0, n0, kb);
+      }
+    }
+  }
   pdl_wait_prior();
 
   // One pipeline step moves kpb k-blocks (TcConvParams::kpb) through kpb consecutive stage
@@ -327,6 +349,23 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         KPos q = kpos_at(a_odd ? ka : 0);
         for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
+          if (pre_steps > 0) {
+            // weights already issued before the dependent-launch wait: arrive with the rest
+            --pre_steps;
+            mbar_arrive_expect_tx(&full[stage], b_bytes2 - static_cast<uint32_t>(kpb * Cfg::kBTileBytes));
+            if (a_odd) {
+              for (int j = 0; j < kpb; ++j) {
+                if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+                kpos_next(q);
+              }
+            }
+            stage += kpb;
+            if (stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if (!PAIR || leader)
             mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * b_bytes2 : b_bytes2);
           if (PAIR && kpb == 1)
