@@ -22,10 +22,10 @@ CONVF_AUTO_PAD_NOTSET, CONVF_AUTO_PAD_SAME_UPPER, CONVF_AUTO_PAD_SAME_LOWER, \
     CONVF_AUTO_PAD_VALID = 0, 1, 2, 3
 CONVF_VARIANT_AUTO, CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_DEPTHWISE, \
     CONVF_VARIANT_INT8, CONVF_VARIANT_IMPLICIT_GEMM_GATHER, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW, \
-    CONVF_VARIANT_IMPLICIT_GEMM_HALO, CONVF_VARIANT_INT8_TC = 0, 1, 2, 3, 4, 5, 6, 7, 8
+    CONVF_VARIANT_IMPLICIT_GEMM_HALO, CONVF_VARIANT_INT8_TC, CONVF_VARIANT_GROUPED_DIRECT = 0, 1, 2, 3, 4, 5, 6, 7, 8, 9
 VARIANT_NAMES = {0: "auto", 1: "implicit_gemm_im2col", 2: "gemm_1x1", 3: "depthwise",
                  4: "int8_mma", 5: "implicit_gemm_gather", 6: "implicit_gemm_window", 7: "implicit_gemm_halo",
-                 8: "int8_tcgen05_exact"}
+                 8: "int8_tcgen05_exact", 9: "grouped_direct"}
 AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
 
 EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale_shift",

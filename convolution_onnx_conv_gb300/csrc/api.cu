@@ -145,7 +145,7 @@ convf_status check_misc(const convf_desc* d) {
     return fail(CONVF_ERR_INVALID_ARG, "clip bounds (%g, %g) need lo <= hi", d->clip_lo, d->clip_hi);
   if (d->dtype == CONVF_S8 && (d->act == CONVF_ACT_RELU6 || d->act == CONVF_ACT_CLIP))
     return fail(CONVF_ERR_UNSUPPORTED, "the int8 path serves act NONE or RELU only");
-  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_INT8_TC)
+  if (d->variant < CONVF_VARIANT_AUTO || d->variant > CONVF_VARIANT_GROUPED_DIRECT)
     return fail(CONVF_ERR_INVALID_ARG, "variant=%d is not a convf_variant", d->variant);
   if (d->tile_n != 0 && d->tile_n != 32 && d->tile_n != 64 && d->tile_n != 128 && d->tile_n != 256)
     return fail(CONVF_ERR_INVALID_ARG, "tile_n=%d is not 0, 32, 64, 128 or 256", d->tile_n);
@@ -289,13 +289,56 @@ bool pure_1x1(const Shape& s) {
   return s.R == 1 && s.S == 1 && s.sh == 1 && s.sw == 1 && !s.pt && !s.pl && !s.pb && !s.pr;
 }
 
+// Grouped convolution on the tcgen05 kernels: an output-channel tile of bn channels must cover
+// whole groups (bn % Kg == 0) or lie inside one (Kg % bn == 0); its reduction then runs over one
+// window of input channels -- the groups' channels, cw = max(bn / Kg, 1) * Cg wide, padded to
+// 64 -- starting at (n0 / Kg) * Cg, which must be a multiple of 8 channels (16-byte TMA
+// coordinates).  The packed weights are block diagonal over that window (zero outside each
+// output channel's own group), so the MMA does cwpad / Cg times the grouped conv's work: shapes
+// where that exceeds 16 are left to the direct kernel.  The tile width minimises waves x
+// per-tile cost, as pick_tile does for dense convs.
+struct GroupTile {
+  int bn, cwpad;
+};
+
+std::string grouped_tile(const Shape& s, int group, int num_sms, int forced_bn, GroupTile* g) {
+  const int Kg = s.K / group, Cg = s.Cg;
+  double best = 1e300;
+  g->bn = 0;
+  for (int bn : {32, 64, 128, 256}) {
+    if (forced_bn && bn != forced_bn) continue;
+    if (bn % Kg != 0 && Kg % bn != 0) continue;
+    const int nb = (s.K + bn - 1) / bn;
+    bool aligned = true;
+    for (int j = 0; j < nb && aligned; ++j) aligned = ((long long)j * bn / Kg) * Cg % 8 == 0;
+    if (!aligned) continue;
+    const int cw = (bn % Kg == 0 ? bn / Kg : 1) * Cg;
+    const int cwpad = (int)align_up((size_t)cw, 64);
+    if (cwpad > 16 * Cg) continue;
+    const long long tiles = (s.M + 127) / 128 * nb;
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const double kb = bn == 32 ? 670.0 : bn == 64 ? 694.0 : bn == 128 ? 782.0 : 1620.0;
+    const double cost = (double)waves * std::max((double)s.R * s.S * (cwpad / 64) * kb, 128.0 * bn * 4.0 / 20.0);
+    if (cost < best * 0.999) {
+      best = cost;
+      g->bn = bn;
+      g->cwpad = cwpad;
+    }
+  }
+  if (!g->bn)
+    return "grouped convs on the tensor cores need tiles that cover whole groups or lie inside one, 8-channel "
+           "aligned group windows and at most 16x block-diagonal padding";
+  return "";
+}
+
 // Why a shape cannot use a variant ("" = it can).
 std::string cannot(int v, const convf_desc* d, const Shape& s) {
   const bool bf = d->dtype == CONVF_BF16;
   char b[256];
   if ((d->out_dtype != CONVF_OUT_F32 || d->residual) && v != CONVF_VARIANT_GEMM_1X1 &&
-      v != CONVF_VARIANT_IMPLICIT_GEMM)
-    return "bf16 output and the residual input are served by the TMA implicit-GEMM and 1x1 kernels only";
+      v != CONVF_VARIANT_IMPLICIT_GEMM && v != CONVF_VARIANT_GROUPED_DIRECT)
+    return "bf16 output and the residual input are served by the TMA implicit-GEMM, 1x1 and direct grouped kernels "
+           "only";
   switch (v) {
     case CONVF_VARIANT_DEPTHWISE:
       if (!bf) return "depthwise serves bf16 only";
@@ -304,7 +347,12 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       return "";
     case CONVF_VARIANT_GEMM_1X1:
       if (!bf) return "1x1 GEMM serves bf16 only";
-      if (d->group != 1) return "1x1 GEMM needs group == 1";
+      if (d->group != 1) {
+        if (d->cta_pair == 2 || d->stream_k == 2) return "grouped convs run on single CTAs without stream-K";
+        GroupTile g;
+        const std::string why = grouped_tile(s, d->group, 148, d->tile_n, &g);
+        if (!why.empty()) return why;
+      }
       if (s.R != 1 || s.S != 1 || s.sh != 1 || s.sw != 1 || s.pt || s.pl || s.pb || s.pr)
         return "1x1 GEMM needs a 1x1 filter, unit strides and no padding";
       if (s.C % 8) return "1x1 GEMM needs C % 8 == 0 (16-byte TMA row stride)";
@@ -312,7 +360,12 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       return "";
     case CONVF_VARIANT_IMPLICIT_GEMM:
       if (!bf) return "implicit GEMM serves bf16 only";
-      if (d->group != 1) return "implicit GEMM needs group == 1 (grouped conv other than depthwise is refused)";
+      if (d->group != 1) {
+        if (d->cta_pair == 2 || d->stream_k == 2) return "grouped convs run on single CTAs without stream-K";
+        GroupTile g;
+        const std::string why = grouped_tile(s, d->group, 148, d->tile_n, &g);
+        if (!why.empty()) return why;
+      }
       if (s.C % 8) return "TMA im2col needs C % 8 == 0 (use the gather variant)";
       if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
       if (s.sh > 8 || s.sw > 8) return "TMA im2col traversal strides are limited to 8";
@@ -342,6 +395,9 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
       if (!bf) return "implicit GEMM serves bf16 only";
       if (d->group != 1) return "implicit GEMM needs group == 1";
       if (s.K % 4) return "the tcgen05 kernels need K % 4 == 0 (16-byte TMA output row stride)";
+      return "";
+    case CONVF_VARIANT_GROUPED_DIRECT:
+      if (!bf) return "the direct grouped kernel serves bf16 only";
       return "";
     case CONVF_VARIANT_INT8:
       if (d->dtype != CONVF_S8) return "the mma.sync int8 kernel serves CONVF_S8 only";
@@ -375,9 +431,10 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
     *out = d->variant;
     return CONVF_OK;
   }
-  const int order_bf16[6] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM_HALO,
+  // (the direct grouped kernel last: it takes only what no tensor-core kernel can)
+  const int order_bf16[7] = {CONVF_VARIANT_DEPTHWISE, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_IMPLICIT_GEMM_HALO,
                              CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW,
-                             CONVF_VARIANT_IMPLICIT_GEMM_GATHER};
+                             CONVF_VARIANT_IMPLICIT_GEMM_GATHER, CONVF_VARIANT_GROUPED_DIRECT};
   if (d->dtype == CONVF_S8 || d->dtype == CONVF_Q8) {
     // exact integers on tcgen05 first; static int8 falls back to the warp-level MMA kernel
     std::string why = cannot(CONVF_VARIANT_INT8_TC, d, s);
@@ -398,6 +455,10 @@ convf_status select_variant(const convf_desc* d, const Shape& s, int* out) {
     // a tile is one output row segment of 128 pixels: narrower outputs leave most rows idle
     if (why.empty() && v == CONVF_VARIANT_IMPLICIT_GEMM_WINDOW && s.Wo < 32)
       why = "window mode is chosen automatically only for outputs at least 32 pixels wide";
+    // the direct kernel is a fallback for grouped convs only: a dense conv the tensor-core kernels
+    // refuse (e.g. a bf16-output stem) is refused rather than moved to CUDA cores
+    if (why.empty() && v == CONVF_VARIANT_GROUPED_DIRECT && d->group == 1)
+      why = "the direct grouped kernel is chosen automatically only for grouped convs";
     if (why.empty() && v == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
       HaloGeom g;
       halo_geom(s, 148, d->tile_n, &g);
@@ -618,6 +679,22 @@ void pack_bf16(const uint16_t* W, const Shape& s, int cpad, int ktot, uint16_t* 
               W[(((size_t)k * s.C + c) * s.R + r) * s.S + q];
 }
 
+// Grouped: W[K][Cg][R][S] -> [K][ktot], row k = output channel of group k / Kg in the tile of bn
+// channels whose window starts at input channel cb0 = (n0 / Kg) * Cg: element (r*S + s)*cpad + c
+// holds W[k][cb0 + c - (k / Kg) * Cg][r][s] when that channel is in k's group, else zero.
+void pack_bf16_grouped(const uint16_t* W, const Shape& s, int group, int bn, int cpad, int ktot, uint16_t* out) {
+  std::memset(out, 0, sizeof(uint16_t) * (size_t)s.K * ktot);
+  const int Kg = s.K / group, Cg = s.Cg;
+  for (int k = 0; k < s.K; ++k) {
+    const int cb0 = ((k / bn) * bn / Kg) * Cg;
+    const int off = (k / Kg) * Cg - cb0;   // position of k's group inside the window
+    for (int c = 0; c < Cg; ++c)
+      for (int r = 0; r < s.R; ++r)
+        for (int q = 0; q < s.S; ++q)
+          out[(size_t)k * ktot + (size_t)(r * s.S + q) * cpad + off + c] = W[(((size_t)k * Cg + c) * s.R + r) * s.S + q];
+  }
+}
+
 float bf16_to_f32(uint16_t v) {
   uint32_t u = (uint32_t)v << 16;
   float f;
@@ -692,6 +769,13 @@ convf_status conv_fused_plan(const convf_desc* desc, int num_sms, int* variant, 
     pick_tile(s.M, s.K, kt / 64, num_sms > 1 ? num_sms : 2, desc->tile_n ? desc->tile_n : max_bn,
               gather ? 1 : desc->cta_pair, desc->stream_k, !gather, &bn, &pair, &sk);
     if (desc->tile_n) bn = desc->tile_n;
+    if (desc->group > 1) {
+      GroupTile g;
+      grouped_tile(s, desc->group, num_sms > 1 ? num_sms : 2, desc->tile_n, &g);
+      bn = g.bn;
+      kt = v == CONVF_VARIANT_GEMM_1X1 ? g.cwpad : s.R * s.S * g.cwpad;
+      pair = false;
+    }
     if (cta_pair) *cta_pair = pair ? 1 : 0;
   } else if (v == CONVF_VARIANT_IMPLICIT_GEMM_HALO) {
     HaloGeom g;
@@ -870,6 +954,18 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
+  } else if (variant == CONVF_VARIANT_GROUPED_DIRECT) {
+    // [R*S][Cg][K] fp32 with the BN scale folded in (consecutive threads = consecutive k)
+    taps.assign((size_t)s.R * s.S * s.Cg * s.K, 0.f);
+    const uint16_t* Wb = static_cast<const uint16_t*>(W);
+    for (int k = 0; k < s.K; ++k)
+      for (int c = 0; c < s.Cg; ++c)
+        for (int r = 0; r < s.R; ++r)
+          for (int q = 0; q < s.S; ++q)
+            taps[((size_t)(r * s.S + q) * s.Cg + c) * s.K + k] =
+                (float)((double)scale[k] * (double)bf16_to_f32(Wb[(((size_t)k * s.Cg + c) * s.R + r) * s.S + q]));
+    o_taps = carve(taps.size() * sizeof(float));
+    o_bias = carve((size_t)Kpad * sizeof(float));
   } else if (variant == CONVF_VARIANT_INT8_TC) {
     // 8-bit operands as exact bf16 integers: w - w_zero_point[k] (|v| <= 255), prepacked like the
     // bf16 implicit GEMM (1x1 matrix rows or per-tap 64-channel runs)
@@ -943,9 +1039,21 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
     o_qs = carve((size_t)s.K * 4);
   } else {
     int cpad = 0;
-    tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot, &cpad);
-    wpack.resize((size_t)s.K * h->ktot);
-    pack_bf16(static_cast<const uint16_t*>(W), s, cpad, h->ktot, wpack.data());
+    GroupTile gt{0, 0};
+    if (desc->group > 1) {
+      // grouped: the tile width fixes the channel window; block-diagonal weights over it
+      grouped_tile(s, desc->group, h->num_sms, desc->tile_n, &gt);
+      h->a_mode = variant == CONVF_VARIANT_GEMM_1X1 ? kA2D : kAIm2col;
+      h->cblocks = gt.cwpad / 64;
+      cpad = gt.cwpad;
+      h->ktot = variant == CONVF_VARIANT_GEMM_1X1 ? gt.cwpad : s.R * s.S * gt.cwpad;
+      wpack.resize((size_t)s.K * h->ktot);
+      pack_bf16_grouped(static_cast<const uint16_t*>(W), s, desc->group, gt.bn, cpad, h->ktot, wpack.data());
+    } else {
+      tc_layout(variant, s, &h->a_mode, &h->cblocks, &h->ktot, &cpad);
+      wpack.resize((size_t)s.K * h->ktot);
+      pack_bf16(static_cast<const uint16_t*>(W), s, cpad, h->ktot, wpack.data());
+    }
     o_w = carve(wpack.size() * sizeof(uint16_t));
     o_scale = carve((size_t)Kpad * sizeof(float));
     o_bias = carve((size_t)Kpad * sizeof(float));
@@ -959,6 +1067,10 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
     pick_tile(s.M, s.K, h->ktot / 64, h->num_sms, desc->tile_n ? desc->tile_n : max_bn, gather ? 1 : desc->cta_pair,
               desc->stream_k, !gather, &h->bn, &h->pair, &h->sk);
     if (desc->tile_n) h->bn = desc->tile_n;
+    if (desc->group > 1) {
+      h->bn = gt.bn;
+      h->pair = h->sk = false;
+    }
     h->kpb = 1;
     if (!gather) {
       const int st = tc_conv_stages(h->bn, false, h->pair);
@@ -975,7 +1087,7 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
         h->kpb = auto_kblocks_per_step(st, nkb);
       }
     }
-    h->a3d = h->a_mode == kA2D && !gather && h->kpb > 1 && s.C % 64 == 0;
+    h->a3d = h->a_mode == kA2D && !gather && h->kpb > 1 && s.C % 64 == 0 && desc->group == 1;
     if (h->sk) {
       o_skws = carve((size_t)h->num_sms * 128 * h->bn * sizeof(float));
       o_skflags = carve((size_t)h->num_sms * sizeof(int));
@@ -994,7 +1106,7 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
   char* base = static_cast<char*>(h->dev);
   h->status = reinterpret_cast<int*>(base + o_status);
   std::vector<char> staging(h->dev_bytes, 0);
-  if (variant == CONVF_VARIANT_DEPTHWISE) {
+  if (variant == CONVF_VARIANT_DEPTHWISE || variant == CONVF_VARIANT_GROUPED_DIRECT) {
     h->taps = reinterpret_cast<float*>(base + o_taps);
     h->bias = reinterpret_cast<float*>(base + o_bias);
     std::memcpy(staging.data() + o_taps, taps.data(), taps.size() * sizeof(float));
@@ -1342,6 +1454,16 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       ce = launch_tc_window(p, h->tmA, h->tmB, g.E, g.rows, h->grid, g.smem, strm);
       break;
     }
+    case CONVF_VARIANT_GROUPED_DIRECT: {
+      GdParams p{};
+      p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.K = s.K; p.R = s.R; p.S = s.S; p.Ho = s.Ho; p.Wo = s.Wo;
+      p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl; p.dh = s.dh; p.dw = s.dw;
+      p.Cg = s.Cg; p.Kg = s.K / h->desc.group;
+      p.x = static_cast<const uint16_t*>(x); p.w = h->taps; p.bias = h->bias; p.y = y;
+      p.res = h->has_res ? res : nullptr; p.out_bf16 = h->out_bf16 ? 1 : 0; p.lo = h->lo; p.hi = h->hi;
+      ce = launch_grouped_direct(p, h->num_sms, strm);
+      break;
+    }
     case CONVF_VARIANT_INT8_TC: {
       // x - x_zero_point as exact bf16 into the handle's staging copy, then the tcgen05 GEMM in
       // its integer-exact mode (the staging copy's tensor map was encoded at create)
@@ -1395,6 +1517,10 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.lo = h->lo; p.hi = h->hi; p.status = h->status; p.y = static_cast<float*>(y);
       p.sk = h->sk ? 1 : 0; p.sk_ws = h->sk_ws; p.sk_flags = h->sk_flags;
       p.kpb = h->kpb; p.a3d = h->a3d ? 1 : 0;
+      if (h->desc.group > 1) {
+        p.grp_kg = s.K / h->desc.group;
+        p.grp_cg = s.Cg;
+      }
       p.res = h->has_res ? res : nullptr; p.out_bf16 = h->out_bf16 ? 1 : 0;
       // split epilogue columns when CTAs hold at most 8 tiles (measured on the ResNet-50 1x1
       // layers: 5 tiles per CTA gain, 10 and 20 lose)
@@ -1464,7 +1590,7 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
   static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
                                 "implicit_gemm_gather", "implicit_gemm_window", "implicit_gemm_halo",
-                                "int8_tcgen05_exact"};
+                                "int8_tcgen05_exact", "grouped_direct"};
   const Shape& s = h->s;
   if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     snprintf(buf, len,
@@ -1485,15 +1611,18 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              "act_box_per_step=%d exact_chunk_kblocks=%d requant=%s tiles=%d grid=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->bn, h->num_kb, h->kpb, h->a3d ? 1 : 0,
              h->iq_chunk_kb, h->iq_mode ? "float32" : "fixed_point", h->num_tiles, h->grid, h->dev_bytes);
-  else if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8)
-    snprintf(buf, len, "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d weight_bytes=%zu",
-             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->dev_bytes);
+  else if (h->variant == CONVF_VARIANT_DEPTHWISE || h->variant == CONVF_VARIANT_INT8 ||
+           h->variant == CONVF_VARIANT_GROUPED_DIRECT)
+    snprintf(buf, len, "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d group=%d out=%s residual=%d "
+             "weight_bytes=%zu", names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->desc.group,
+             h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->dev_bytes);
   else
     snprintf(buf, len,
-             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d group=%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
              "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d out=%s residual=%d "
              "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
-             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->pair ? 256 : 128, h->bn, h->pair ? 1 : 0,
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->desc.group, h->pair ? 256 : 128, h->bn,
+             h->pair ? 1 : 0,
              h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0,
              (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0,
              h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->num_tiles,

@@ -91,6 +91,10 @@ struct TcConvParams {
   // bits; the fp32 accumulator restarts every iq_chunk_kb reduction blocks, a count chosen so
   // that no partial sum exceeds 2^24 in magnitude (every partial sum is then an exactly
   // represented integer), and the epilogue converts each chunk to int32 and adds the chunks.
+  // grouped convolution (1 < group): Kg output and Cg input channels per group; a tile of BN
+  // output channels covers whole groups (BN % Kg == 0) or lies inside one (Kg % BN == 0), and
+  // its activation loads read the channel window starting at (n0 / Kg) * Cg.  0 = dense.
+  int grp_kg, grp_cg;
   int iq_chunk_kb;        // reduction blocks per exact chunk (a multiple of kpb)
   int iq_mode;            // requantisation: 0 fixed point (static int8), 1 float32 (QLinearConv)
   const int32_t* q_bias;  // [Kpad] int32 bias added to the exact sum
@@ -219,6 +223,24 @@ struct DwParams {
 bool dw_uses_tma(const DwParams& p);
 void dw_tile_box(int stride, int Wo, int* box_w, int* box_h, int* box_n);
 cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- grouped conv, direct (CUDA cores)
+// Any group count and filter: one thread per (output pixel, output channel), the reduction over
+// its group's Cg input channels and the R x S taps in fp32.  The shapes the tensor-core kernels
+// cannot take (group windows they cannot align, channel counts TMA cannot address).
+struct GdParams {
+  int N, C, H, W, K, R, S, Ho, Wo;
+  int sh, sw, pt, pl, dh, dw;
+  int Cg, Kg;
+  const uint16_t* x;      // NHWC bf16
+  const float* w;         // [R*S][Cg][K] fp32, BN scale folded in
+  const float* bias;      // [K]
+  void* y;                // NHWC fp32, or bf16 bits when out_bf16
+  const void* res;        // residual of y's type and shape, or null
+  int out_bf16;
+  float lo, hi;
+};
+cudaError_t launch_grouped_direct(const GdParams& p, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- int8 implicit GEMM
 struct S8Params {

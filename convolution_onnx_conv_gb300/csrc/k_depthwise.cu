@@ -8,6 +8,8 @@
 // padding is the TMA's zero fill.  Each thread owns 4 channels of one output column and walks
 // the window's input rows once, scattering every converted row into the (up to three) output
 // rows it feeds, then stores each output row as one 16-byte vector as soon as it is complete.
+#include <cuda_bf16.h>
+
 #include "convf_internal.h"
 #include "ptx.cuh"
 
@@ -268,6 +270,58 @@ __global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
     dst[1] = make_float4(clampf(acc[4], p.lo, p.hi), clampf(acc[5], p.lo, p.hi),
                          clampf(acc[6], p.lo, p.hi), clampf(acc[7], p.lo, p.hi));
   }
+}
+
+// Grouped convolution, direct: consecutive threads take consecutive output channels of one
+// pixel, so the weight reads ([tap][c][k]) and the output stores are coalesced and threads of one
+// group read the same input values (broadcast).
+__global__ void __launch_bounds__(256) grouped_direct_kernel(const GdParams p) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
+  const long long total = static_cast<long long>(p.N) * p.Ho * p.Wo * p.K;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(idx % p.K);
+    long long t = idx / p.K;
+    const int ow = static_cast<int>(t % p.Wo);
+    t /= p.Wo;
+    const int oh = static_cast<int>(t % p.Ho);
+    const int n = static_cast<int>(t / p.Ho);
+    const int cb = (k / p.Kg) * p.Cg;
+    float acc = __ldg(p.bias + k);
+    for (int r = 0; r < p.R; ++r) {
+      const int ih = oh * p.sh - p.pt + r * p.dh;
+      if (ih < 0 || ih >= p.H) continue;
+      for (int s = 0; s < p.S; ++s) {
+        const int iw = ow * p.sw - p.pl + s * p.dw;
+        if (iw < 0 || iw >= p.W) continue;
+        const uint16_t* xp = p.x + ((static_cast<size_t>(n) * p.H + ih) * p.W + iw) * p.C + cb;
+        const float* wp = p.w + static_cast<size_t>(r * p.S + s) * p.Cg * p.K + k;
+        for (int c = 0; c < p.Cg; ++c)
+          acc = fmaf(__uint_as_float(static_cast<uint32_t>(__ldg(xp + c)) << 16), __ldg(wp + static_cast<size_t>(c) * p.K),
+                     acc);
+      }
+    }
+    if (p.res != nullptr)
+      acc += p.out_bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p.res)[idx]) << 16)
+                        : static_cast<const float*>(p.res)[idx];
+    const float v = clampf(acc, p.lo, p.hi);
+    if (p.out_bf16) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      static_cast<uint16_t*>(p.y)[idx] = *reinterpret_cast<const uint16_t*>(&b);
+    } else {
+      static_cast<float*>(p.y)[idx] = v;
+    }
+  }
+}
+
+cudaError_t launch_grouped_direct(const GdParams& p, int num_sms, cudaStream_t stream) {
+  const long long total = static_cast<long long>(p.N) * p.Ho * p.Wo * p.K;
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(grouped_direct_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, p);
 }
 
 bool dw_uses_tma(const DwParams& p) {

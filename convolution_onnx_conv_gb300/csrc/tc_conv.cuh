@@ -259,20 +259,27 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   };
   // activation tile of k-block kb at position q: a 2-D tile, or the im2col column of its filter
   // tap and channel block (padding is TMA zero fill)
-  auto load_a = [&](int kb, const KPos& q, uint8_t* dA, uint64_t* bar, int m0, int img, int hb, int wb) {
+  // (cbase: first input channel of the tile's channel window -- nonzero only for grouped convs,
+  // whose output-channel tiles read the input channels of their own groups)
+  auto load_a = [&](int kb, const KPos& q, uint8_t* dA, uint64_t* bar, int m0, int img, int hb, int wb, int cbase) {
     if (p.a_mode == kA2D) {
       if (PAIR)
-        tma_load_2d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), kb * kBK, m0);
+        tma_load_2d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), cbase + kb * kBK, m0);
       else
-        tma_load_2d(dA, &tmA, bar, kb * kBK, m0);
+        tma_load_2d(dA, &tmA, bar, cbase + kb * kBK, m0);
     } else {
       if (PAIR)
-        tma_load_im2col_4d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), q.cb * kBK, wb, hb, img,
+        tma_load_im2col_4d_pair(dA, &tmA, map_to_rank(smem_u32(bar), 0), cbase + q.cb * kBK, wb, hb, img,
                                 static_cast<uint16_t>(q.s * p.dw), static_cast<uint16_t>(q.r * p.dh));
       else
-        tma_load_im2col_4d(dA, &tmA, bar, q.cb * kBK, wb, hb, img, static_cast<uint16_t>(q.s * p.dw),
+        tma_load_im2col_4d(dA, &tmA, bar, cbase + q.cb * kBK, wb, hb, img, static_cast<uint16_t>(q.s * p.dw),
                            static_cast<uint16_t>(q.r * p.dh));
     }
+  };
+  // grouped convs (TcConvParams::grp_kg > 0): a tile of output channels n0.. covers whole groups
+  // or lies inside one, and its channel window starts at group n0 / Kg's first input channel
+  auto tile_cbase = [&](int tile) {
+    return p.grp_kg > 0 ? ((tile % p.n_blocks) * BN / p.grp_kg) * p.grp_cg : 0;
   };
 
   if (warp == 0) {
@@ -308,6 +315,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         }
         int img = 0, hb = 0, wb = 0;
         tile_origin(m0, img, hb, wb);
+        const int cbase = tile_cbase(tile);
         KPos q = kpos_at(ka);
         for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               tma_load_3d(sA + stage * kATileBytes, &tmA, &full[stage], 0, m0, kb);
           } else {
             for (int j = 0; j < kpb; ++j) {
-              if (!(j & 1)) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+              if (!(j & 1)) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb, cbase);
               kpos_next(q);
             }
           }
@@ -346,6 +354,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
         int img = 0, hb = 0, wb = 0;
         if (a_odd) tile_origin(m0, img, hb, wb);
+        const int cbase = tile_cbase(tile);
         KPos q = kpos_at(a_odd ? ka : 0);
         for (int kb = ka; kb < kend; kb += kpb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) goto teardown;
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             mbar_arrive_expect_tx(&full[stage], b_bytes2 - static_cast<uint32_t>(kpb * Cfg::kBTileBytes));
             if (a_odd) {
               for (int j = 0; j < kpb; ++j) {
-                if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+                if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb, cbase);
                 kpos_next(q);
               }
             }
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             tma_load_3d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], 0, n0, kb);
           if (a_odd) {
             for (int j = 0; j < kpb; ++j) {
-              if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb);
+              if (j & 1) load_a(kb + j, q, sA + (stage + j) * kATileBytes, &full[stage], m0, img, hb, wb, cbase);
               kpos_next(q);
             }
           }

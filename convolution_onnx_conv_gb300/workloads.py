@@ -146,6 +146,18 @@ def depthwise_layers(n: int = 64) -> List[ConvSpec]:
     return [l for l in mobilenetv2_layers(n) if l.group > 1]
 
 
+RESNEXT_GROUPED = [  # (width, H_in, stride): the grouped 3x3 of each ResNeXt-50 32x4d stage
+    (128, 56, 1), (256, 56, 2), (512, 28, 2), (1024, 14, 2),
+]
+
+
+def resnext50_grouped_layers(n: int = 32) -> List[ConvSpec]:
+    """The grouped 3x3 convs of ResNeXt-50 (32x4d): 32 groups of 4, 8, 16 and 32 channels, the
+    first block of stages 2-4 strided on the 3x3, folded BN + ReLU."""
+    return [ConvSpec(f"rx50_3x3_g32_c{c}_{h}_s{s}@b{n}", n, c, h, h, c, 3, 3, (s, s), (1, 1, 1, 1), group=32)
+            for c, h, s in RESNEXT_GROUPED]
+
+
 INT8_SHAPES = [  # (C = K, H_in, stride): the seven distinct ResNet-50 3x3 shapes
     (64, 56, 1), (128, 56, 2), (128, 28, 1), (256, 28, 2), (256, 14, 1), (512, 14, 2),
     (512, 7, 1),

@@ -106,7 +106,7 @@ typedef enum {
                                             shifted shared-memory descriptors (im2col reloads
                                             it once per tap).  The selector takes it when at
                                             least 60% of a tile's 128 rows are real outputs. */
-  CONVF_VARIANT_INT8_TC = 8          /* 8-bit convs (CONVF_S8, CONVF_Q8) on tcgen05: a pre-pass writes
+  CONVF_VARIANT_INT8_TC = 8,         /* 8-bit convs (CONVF_S8, CONVF_Q8) on tcgen05: a pre-pass writes
                                         x - x_zero_point as bf16 (exact: |v| <= 255) into a handle
                                         workspace, the weights are prepacked as bf16 w - w_zero_point,
                                         and the tcgen05 implicit GEMM restarts its fp32 accumulator
@@ -114,6 +114,13 @@ typedef enum {
                                         sum exceeds 2^24 (so every partial sum is an exact integer);
                                         the epilogue adds the chunks in int32 and requantises.
                                         Bit-exact.  C % 8 == 0, K % 16 == 0, group 1. */
+  CONVF_VARIANT_GROUPED_DIRECT = 9   /* CUDA-core direct conv for any group count and filter (one
+                                        thread per output pixel and channel, fp32); chosen for the
+                                        grouped convs the tensor-core kernels cannot take.  (Those
+                                        take groups on CONVF_VARIANT_IMPLICIT_GEMM / _GEMM_1X1 when
+                                        an output-channel tile covers whole groups or lies inside
+                                        one: block-diagonal weights over the tile's input-channel
+                                        window, at most 16x the grouped work.) */
 } convf_variant;
 
 typedef struct {
@@ -152,7 +159,7 @@ typedef struct {
                               single fused conv, residual, bias and ReLU operation the "Kyanite"
                               README lists in section "Cuda Executor").  0: no residual.
                               Both options are served by the TMA implicit-GEMM and 1x1 kernels
-                              only (C % 8 == 0, group 1); other shapes are refused. */
+                              (C % 8 == 0) and the direct grouped kernel; other kernels refuse them. */
 } convf_desc;
 
 typedef struct convf_handle convf_handle;

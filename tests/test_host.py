@@ -53,9 +53,10 @@ def desc(**kw):
     (dict(layout=cf.CONVF_NCHW), cf.CONVF_ERR_UNSUPPORTED, "channels-last"),
     (dict(act=9), cf.CONVF_ERR_INVALID_ARG, "act=9"),
     (dict(act=cf.CONVF_ACT_CLIP, clip=(2.0, 1.0)), cf.CONVF_ERR_INVALID_ARG, "clip"),
-    (dict(group=2, K=32), cf.CONVF_ERR_UNSUPPORTED, "no kernel serves"),
-    (dict(C=12, K=12, group=12), cf.CONVF_ERR_UNSUPPORTED, "C % 8"),
-    (dict(K=30), cf.CONVF_ERR_UNSUPPORTED, "K % 4"),
+    (dict(group=2, K=32, cta_pair=2, variant=cf.CONVF_VARIANT_IMPLICIT_GEMM), cf.CONVF_ERR_UNSUPPORTED,
+     "single CTAs"),
+    (dict(C=12, K=12, group=12, variant=cf.CONVF_VARIANT_DEPTHWISE), cf.CONVF_ERR_UNSUPPORTED, "C % 8"),
+    (dict(K=30, variant=cf.CONVF_VARIANT_IMPLICIT_GEMM), cf.CONVF_ERR_UNSUPPORTED, "K % 4"),
     (dict(dtype=cf.CONVF_S8, C=12), cf.CONVF_ERR_UNSUPPORTED, "C % 64"),
     (dict(dtype=cf.CONVF_S8, C=64, act=cf.CONVF_ACT_RELU6), cf.CONVF_ERR_UNSUPPORTED, "int8"),
     (dict(variant=cf.CONVF_VARIANT_GEMM_1X1), cf.CONVF_ERR_UNSUPPORTED, "forced variant"),
@@ -283,9 +284,9 @@ def test_kblocks_per_step_is_validated():
 
 
 def test_bf16_output_and_residual_are_validated_and_routed():
-    """out_dtype and residual take 0/1; with either, only the TMA implicit-GEMM and 1x1 kernels
-    serve the conv: the 56x56 3x3 layer moves off the halo tiles, the RGB stem and depthwise and
-    int8 convs are refused."""
+    """out_dtype and residual take 0/1; with either, the dense convs are served by the TMA
+    implicit-GEMM and 1x1 kernels only: the 56x56 3x3 layer moves off the halo tiles and the RGB
+    stem is refused."""
     layers = {s.name: s for s in workloads.resnet50_layers(32)}
 
     def plan(spec, **kw):
@@ -300,11 +301,7 @@ def test_bf16_output_and_residual_are_validated_and_routed():
     for kw in ({"out_dtype": 1}, {"residual": 1}):
         with pytest.raises(cf.ConvFusedError) as e:
             plan(layers["r50_00_stem7x7@b32"], **kw)
-        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "1x1 kernels only" in str(e.value)
-        dw = next(iter(workloads.depthwise_layers(64)))
-        with pytest.raises(cf.ConvFusedError) as e:
-            plan(dw, **kw)
-        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED
+        assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "kernels only" in str(e.value)
     for kw in ({"out_dtype": 2}, {"out_dtype": -1}, {"residual": 2}):
         with pytest.raises(cf.ConvFusedError) as e:
             plan(halo, **kw)
@@ -409,3 +406,31 @@ def test_int8_selector_prefers_the_exact_tcgen05_kernel():
     with pytest.raises(cf.ConvFusedError) as e:
         cf.conv_fused_plan(d)
     assert e.value.status == cf.CONVF_ERR_UNSUPPORTED and "K % 16" in str(e.value)
+
+
+@pytest.mark.parametrize("C,K,group,R,variant,tile,ktot", [
+    # ResNeXt-style 32 groups of 4: 32-wide tiles cover 8 groups, a 32-channel window padded to 64
+    (128, 128, 32, 3, cf.CONVF_VARIANT_IMPLICIT_GEMM, 32, 9 * 64),
+    # 2 groups of 128 -> 128: tiles inside one group, a 128-channel window
+    (256, 256, 2, 3, cf.CONVF_VARIANT_IMPLICIT_GEMM, None, 9 * 128),
+    # grouped 1x1 (ShuffleNet-like): 8 groups of 32 -> 32
+    (256, 256, 8, 1, cf.CONVF_VARIANT_GEMM_1X1, None, None),
+    # channel multiplier 2 on 64 channels (Cg = 1): 64x block-diagonal padding -> direct kernel
+    (64, 128, 64, 3, cf.CONVF_VARIANT_GROUPED_DIRECT, 0, None),
+    # 3 groups of 8 -> 4: one 32-wide tile holds all three, a 24-channel window padded to 64
+    (24, 12, 3, 3, cf.CONVF_VARIANT_IMPLICIT_GEMM, 32, 9 * 64),
+    # 8 groups of 3 -> 3: no power-of-two tile covers whole groups or fits in one -> direct
+    (24, 24, 8, 3, cf.CONVF_VARIANT_GROUPED_DIRECT, 0, None),
+])
+def test_grouped_selection(C, K, group, R, variant, tile, ktot):
+    d = cf.make_desc(8, C, 14, 14, K, R, R, (1, 1), (R // 2,) * 4, group=group)
+    v, bn, kt = cf.conv_fused_plan(d)
+    assert v == variant, (v, bn, kt)
+    if tile is not None:
+        assert bn == tile, bn
+    if ktot is not None:
+        assert kt == ktot, kt
+    if variant != cf.CONVF_VARIANT_GROUPED_DIRECT:
+        Kg, Cg = K // group, C // group
+        assert bn % Kg == 0 or Kg % bn == 0
+        assert all(((j * bn) // Kg) * Cg % 8 == 0 for j in range(-(-K // bn)))
