@@ -24,6 +24,14 @@ Every function is the plain definition of one stage, kept separate on purpose:
     Executor").  Where it sits relative to BN is not stated there; here it
     follows the folded BN affine (the bottleneck's shortcut joins after the
     block's last BN), a reading.
+``round_bf16`` / ``preactivation``
+    The pre-activation of a ResNet-v2 block ("tensorforge", section "ResNet
+    fusion": the remaining BN -> ReLU pairs): per input channel
+    u = act(x * scale + shift) (a BatchNorm folded to its affine, then the
+    activation), applied to the conv's input before its zero padding.  The
+    conv consumes u as its operand, so u is stored in the operand type:
+    rounded to bf16 to nearest-even (a reading; the affine is evaluated in
+    float32 first, as the storage of x, scale and shift is float32/bf16).
 ``activation``
     ReLU = max(u, 0); ReLU6 = min(max(u, 0), 6), the two clamps of the
     residual + batchnorm + relu6 example kernel in the "Kyanite" README
@@ -238,6 +246,30 @@ def residual_add(u, r):
     return np.asarray(u, dtype=np.float64) + np.asarray(r, dtype=np.float64)
 
 
+def round_bf16(a):
+    """float32 values -> the nearest bf16 values (ties to even), returned as float64.
+
+    A bf16 value is the top 16 bits of a float32: add half of the dropped 16-bit part's range
+    (0x7FFF, plus 1 when the kept part is odd, so that ties go to the even neighbour) and drop
+    those bits.  Finite inputs only."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    if not np.all(np.isfinite(f)):
+        raise ValueError("round_bf16 takes finite values")
+    bits = f.view(np.uint32).astype(np.uint64)
+    r = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def preactivation(x, scale, shift, act=ACT_RELU, lo=0.0, hi=6.0):
+    """u = round_bf16(act(float32(x * scale[c] + shift[c]))) for NCHW x (channel axis 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    shp = (1, -1) + (1,) * (x.ndim - 2)
+    s = np.asarray(scale, dtype=np.float64).reshape(shp)
+    t = np.asarray(shift, dtype=np.float64).reshape(shp)
+    u = (x * s + t).astype(np.float32).astype(np.float64)
+    return round_bf16(activation(u, act, lo, hi))
+
+
 def activation(u, act=ACT_NONE, lo=0.0, hi=6.0):
     """none: u;  ReLU: max(u, 0);  ReLU6: min(max(u, 0), 6);  Clip: min(max(u, lo), hi)."""
     u = np.asarray(u, dtype=np.float64)
@@ -388,9 +420,12 @@ def qlinear_requant(acc, x_scale, w_scale, y_scale, y_zero_point, y_dtype=np.uin
 # ------------------------------------------------------------- whole pipeline
 
 def conv_bn_act(x, w, bias=None, bn=None, act=ACT_NONE, lo=0.0, hi=6.0, strides=(1, 1),
-                pads=(0, 0, 0, 0), dilations=(1, 1), group=1, eps=1e-5, residual=None):
-    """Conv, then BN (if ``bn`` = (gamma, beta, mean, var)), then the residual (if given, NCHW of
+                pads=(0, 0, 0, 0), dilations=(1, 1), group=1, eps=1e-5, residual=None, pre=None):
+    """Optional pre-activation of the input (``pre`` = (scale, shift, act): ``preactivation``),
+    conv, then BN (if ``bn`` = (gamma, beta, mean, var)), then the residual (if given, NCHW of
     the output's shape), then activation."""
+    if pre is not None:
+        x = preactivation(x, *pre)
     z = conv2d(x, w, bias, strides, pads, dilations, group)
     if bn is not None:
         z = batchnorm(z, *bn, eps=eps)

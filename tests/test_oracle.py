@@ -586,3 +586,50 @@ def test_qlinear_relu_keeps_the_codes_of_non_negative_real_values():
         real_r = (yr.astype(np.int64) - zp) * 0.3
         assert np.array_equal(real_r, np.maximum(real, 0.0))
         assert (yr < zp).sum() == 0 and (y < zp).any()
+
+
+# ----------------------------------------------------------- pre-activation prologue
+
+def test_round_bf16_matches_the_library_conversion_and_ties_go_to_even():
+    """Against torch's float32 -> bfloat16 conversion (a library routine, round to nearest even),
+    on random values over many binades and on exact ties."""
+    rng = np.random.default_rng(70)
+    a = (rng.standard_normal(200000) * np.exp2(rng.integers(-30, 30, 200000))).astype(np.float32)
+    ref = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(a), ref)
+    # ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> 1 (even); 1 + 3*2^-8 -> 1 + 2^-6 (even)
+    t = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 2 + 2.0 ** -7], np.float32)
+    assert oracle.round_bf16(t).tolist() == [1.0, 1 + 2.0 ** -6, -1.0, 2.0]
+
+
+def test_preactivation_closed_forms():
+    rng = np.random.default_rng(71)
+    x = oracle.round_bf16(rng.standard_normal((2, 5, 4, 3)))
+    one, zero = np.ones(5), np.zeros(5)
+    # identity affine, no activation: x itself (already bf16)
+    assert np.array_equal(oracle.preactivation(x, one, zero, oracle.ACT_NONE), x)
+    # ReLU zeroes exactly the negative inputs
+    u = oracle.preactivation(x, one, zero, oracle.ACT_RELU)
+    assert np.array_equal(u, np.maximum(x, 0.0))
+    # a per-channel affine: channel c scaled by 2^c (exact in bf16), shifted by 0
+    s = np.exp2(np.arange(5.0))
+    u = oracle.preactivation(x, s, zero, oracle.ACT_NONE)
+    assert np.array_equal(u, x * s.reshape(1, 5, 1, 1))
+
+
+def test_preactivation_pads_after_the_activation():
+    """The conv's zero padding is applied to u: with shift = 1 and ReLU every real input maps to
+    max(x + 1, 0) but padded taps still contribute 0.  Checked against torch on the padded u."""
+    rng = np.random.default_rng(72)
+    x = oracle.round_bf16(rng.standard_normal((1, 3, 5, 5)))
+    w = rng.standard_normal((4, 3, 3, 3))
+    pre = (np.ones(3), np.ones(3), oracle.ACT_RELU)
+    y = oracle.conv_bn_act(x, w, pads=(1, 1, 1, 1), pre=pre)
+    u = oracle.round_bf16(np.maximum(x + 1.0, 0.0))
+    ref = torch.nn.functional.conv2d(torch.from_numpy(u), torch.from_numpy(w), padding=1).numpy()
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # padding x with zeros first and activating after would add relu(0 + 1) = 1 on the border
+    xp = np.pad(x, ((0, 0), (0, 0), (1, 1), (1, 1)))
+    wrong = torch.nn.functional.conv2d(torch.from_numpy(oracle.round_bf16(np.maximum(xp + 1.0, 0.0))),
+                                       torch.from_numpy(w)).numpy()
+    assert not np.allclose(y[..., 0, 0], wrong[..., 0, 0])
