@@ -33,7 +33,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
-            "conv_fused_run_residual", "conv_fused_create_qlinear"]
+            "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -116,6 +116,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_pack_weights.argtypes = [dptr, ctypes.c_int, vp, vp, ctypes.c_size_t]
     lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
     lib.conv_fused_create_qlinear.argtypes = [dptr, vp, vp, P(QParams), P(vp)]
+    lib.conv_fused_create_preact.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int, P(vp)]
     lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
     lib.conv_fused_run_residual.argtypes = [vp, vp, vp, vp, vp]
     lib.conv_fused_status.argtypes = [vp]
@@ -206,6 +207,16 @@ def conv_fused_create(desc: ConvDesc, W, bias=None, bn_scale=None, bn_shift=None
     return h.value
 
 
+def conv_fused_create_preact(desc: ConvDesc, W, bias=None, bn_scale=None, bn_shift=None, pre_scale=None,
+                             pre_shift=None, pre_act: int = CONVF_ACT_RELU) -> int:
+    """Handle with a pre-activation prologue: the conv reads clamp(pre_scale*x + pre_shift)."""
+    h = ctypes.c_void_p()
+    _check(load_library().conv_fused_create_preact(ctypes.byref(desc), _addr(W), _addr(bias), _addr(bn_scale),
+                                                   _addr(bn_shift), _addr(pre_scale), _addr(pre_shift),
+                                                   int(pre_act), ctypes.byref(h)))
+    return h.value
+
+
 def conv_fused_create_qlinear(desc: ConvDesc, W, bias, q: QParams) -> int:
     """QLinearConv handle: desc.dtype == CONVF_Q8, W host int8/uint8 [K][C/group][R][S], bias host
     int32[K] or None, q the scales and zero points (its w arrays host pointers)."""
@@ -291,7 +302,7 @@ class FusedConv:
                  pads=(0, 0, 0, 0), dilation=(1, 1), group=1, act=CONVF_ACT_NONE, clip=(0.0, 6.0),
                  auto_pad="NOTSET", variant=CONVF_VARIANT_AUTO, requant_mult=None, requant_shift=None,
                  out_zero_point=0, tile_n=0, cta_pair=0, stream_k=0, kblocks_per_step=0,
-                 out_bf16=False, residual=False):
+                 out_bf16=False, residual=False, pre_scale=None, pre_shift=None, pre_act=None):
         import torch
         s8 = w.dtype == torch.int8
         self.desc = make_desc(N, C, H, W, K, R, S, stride, pads, dilation, group,
@@ -311,10 +322,17 @@ class FusedConv:
             keep.append(t)
             return t
 
-        self.handle = conv_fused_create(self.desc, wbits, host(bias, torch.int32 if s8 else torch.float32),
-                                        host(bn_scale, torch.float32), host(bn_shift, torch.float32),
-                                        host(requant_mult, torch.int32), host(requant_shift, torch.int32),
-                                        out_zero_point)
+        if pre_act is not None:
+            # pre-activation prologue (bf16 convs): the conv reads clamp(pre_scale*x + pre_shift)
+            self.handle = conv_fused_create_preact(self.desc, wbits, host(bias, torch.float32),
+                                                   host(bn_scale, torch.float32), host(bn_shift, torch.float32),
+                                                   host(pre_scale, torch.float32), host(pre_shift, torch.float32),
+                                                   pre_act)
+        else:
+            self.handle = conv_fused_create(self.desc, wbits, host(bias, torch.int32 if s8 else torch.float32),
+                                            host(bn_scale, torch.float32), host(bn_shift, torch.float32),
+                                            host(requant_mult, torch.int32), host(requant_shift, torch.int32),
+                                            out_zero_point)
         self.out_shape = conv_fused_output_shape(self.desc)
         self.s8 = s8
 

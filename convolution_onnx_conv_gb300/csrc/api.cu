@@ -621,6 +621,12 @@ struct convf_handle {
   int32_t* q_mult;
   int32_t* q_shift;
   float* q_scale;
+  // pre-activation prologue: a bf16 copy u = clamp(pre_scale*x + pre_shift) read instead of x
+  bool preact;
+  uint16_t* xs;
+  float* pre_scale;
+  float* pre_shift;
+  float pre_lo, pre_hi;
   WinGeom wg;       // window variant geometry
   HaloGeom hg;      // halo variant geometry
   CUtensorMap tmB;
@@ -830,7 +836,8 @@ int q8_hi(int is_signed) { return is_signed ? 127 : 255; }
 
 convf_status create_impl(const convf_desc* desc, const void* W, const void* bias, const float* bn_scale,
                          const float* bn_shift, const int32_t* requant_mult, const int32_t* requant_shift,
-                         int32_t out_zero_point, const convf_qparams* qp, convf_handle** out) {
+                         int32_t out_zero_point, const convf_qparams* qp, convf_handle** out,
+                         const float* pre_scale = nullptr, const float* pre_shift = nullptr, int pre_act = -1) {
   if (!out) return fail(CONVF_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   Shape s;
@@ -879,6 +886,16 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
       for (int k = 0; k < s.K; ++k)
         if (!std::isfinite(bn_scale[k]) || !std::isfinite(bn_shift[k]))
           return fail(CONVF_ERR_INVALID_ARG, "bn_scale/bn_shift[%d] is not finite", k);
+  }
+  const bool preact = pre_act >= 0;
+  if (preact) {
+    if (desc->dtype != CONVF_BF16) return fail(CONVF_ERR_UNSUPPORTED, "the pre-activation prologue serves bf16 convs only");
+    if (!pre_scale || !pre_shift) return fail(CONVF_ERR_INVALID_ARG, "pre_scale/pre_shift is NULL");
+    if (pre_act != CONVF_ACT_NONE && pre_act != CONVF_ACT_RELU && pre_act != CONVF_ACT_RELU6)
+      return fail(CONVF_ERR_INVALID_ARG, "pre_act=%d is not CONVF_ACT_NONE, _RELU or _RELU6", pre_act);
+    for (int c = 0; c < s.C; ++c)
+      if (!std::isfinite(pre_scale[c]) || !std::isfinite(pre_shift[c]))
+        return fail(CONVF_ERR_INVALID_ARG, "pre_scale/pre_shift[%d] is not finite", c);
   }
   int variant = 0;
   if ((st = select_variant(desc, s, &variant)) != CONVF_OK) return st;
@@ -1095,6 +1112,16 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
     if (variant == CONVF_VARIANT_IMPLICIT_GEMM_GATHER && gather_cpt(s) > 0)
       o_pad = carve((size_t)s.N * s.H * s.W * gather_cpt(s) * sizeof(uint16_t));
   }
+  size_t o_xs = 0, o_pre = 0;
+  const size_t Cpad = align_up((size_t)s.C, 64);
+  if (preact) {
+    h->preact = true;
+    o_xs = carve((size_t)s.N * s.H * s.W * s.C * sizeof(uint16_t));
+    o_pre = carve(2 * Cpad * sizeof(float));
+    convf_desc a{};
+    a.act = pre_act;
+    act_bounds(&a, &h->pre_lo, &h->pre_hi);
+  }
   const size_t o_status = carve(sizeof(int));
   h->dev_bytes = off;
   ce = cudaMalloc(&h->dev, h->dev_bytes);
@@ -1157,6 +1184,13 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
     std::memcpy(staging.data() + o_w, wpack.data(), wpack.size() * sizeof(uint16_t));
     std::memcpy(staging.data() + o_scale, scale.data(), (size_t)Kpad * sizeof(float));
     std::memcpy(staging.data() + o_bias, biasf.data(), (size_t)Kpad * sizeof(float));
+  }
+  if (preact) {
+    h->xs = reinterpret_cast<uint16_t*>(base + o_xs);
+    h->pre_scale = reinterpret_cast<float*>(base + o_pre);
+    h->pre_shift = h->pre_scale + Cpad;
+    std::memcpy(staging.data() + o_pre, pre_scale, (size_t)s.C * sizeof(float));
+    std::memcpy(staging.data() + o_pre + Cpad * sizeof(float), pre_shift, (size_t)s.C * sizeof(float));
   }
   ce = cudaMemcpy(h->dev, staging.data(), h->dev_bytes, cudaMemcpyHostToDevice);
   if (ce != cudaSuccess) {
@@ -1304,6 +1338,17 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
   return create_impl(desc, W, bias, bn_scale, bn_shift, requant_mult, requant_shift, out_zero_point, nullptr, out);
 }
 
+convf_status conv_fused_create_preact(const convf_desc* desc, const void* W, const void* bias,
+                                      const float* bn_scale, const float* bn_shift, const float* pre_scale,
+                                      const float* pre_shift, int pre_act, convf_handle** out) {
+  if (pre_act < 0) {
+    if (out) *out = nullptr;
+    return fail(CONVF_ERR_INVALID_ARG, "pre_act=%d is not CONVF_ACT_NONE, _RELU or _RELU6", pre_act);
+  }
+  return create_impl(desc, W, bias, bn_scale, bn_shift, nullptr, nullptr, 0, nullptr, out, pre_scale, pre_shift,
+                     pre_act);
+}
+
 convf_status conv_fused_create_qlinear(const convf_desc* desc, const void* W, const int32_t* bias,
                                        const convf_qparams* q, convf_handle** out) {
   if (!q) {
@@ -1401,6 +1446,13 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
     return fail(CONVF_ERR_INVALID_ARG, "the current device (%d) is not the handle's device (%d)", dev, h->device);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   cudaError_t ce = cudaSuccess;
+  if (h->preact) {
+    // the prologue's bf16 copy is what every variant reads (its tensor maps cache that pointer)
+    ce = launch_preact_bf16(static_cast<const uint16_t*>(x), h->xs, (long long)s.N * s.H * s.W * s.C, s.C,
+                            h->pre_scale, h->pre_shift, h->pre_lo, h->pre_hi, h->num_sms, strm);
+    if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "pre-activation launch failed: %s", cudaGetErrorString(ce));
+    x = h->xs;
+  }
   switch (h->variant) {
     case CONVF_VARIANT_DEPTHWISE: {
       DwParams p{};
@@ -1618,10 +1670,11 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->dev_bytes);
   else
     snprintf(buf, len,
-             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d group=%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
+             "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d group=%d preact=%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
              "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d out=%s residual=%d "
              "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
-             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->desc.group, h->pair ? 256 : 128, h->bn,
+             names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->desc.group, h->preact ? 1 : 0,
+             h->pair ? 256 : 128, h->bn,
              h->pair ? 1 : 0,
              h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0,
              (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0,

@@ -120,6 +120,11 @@ constexpr int tc_conv_stages(int bn, bool gather, bool pair) {
 cudaError_t launch_q8_to_bf16(const uint8_t* x, uint16_t* out, long long n, int is_signed, int zp, int num_sms,
                               cudaStream_t stream);
 
+// Pre-activation prologue: bf16 NHWC x -> bf16 bits of clamp(scale[c]*x + shift[c], lo, hi)
+// (n elements, C channels; 16-byte aligned pointers).
+cudaError_t launch_preact_bf16(const uint16_t* x, uint16_t* out, long long n, int C, const float* scale,
+                               const float* shift, float lo, float hi, int num_sms, cudaStream_t stream);
+
 // ---------------------------------------------------------------- halo-tile implicit GEMM
 // Stride-1, dilation-1 convolutions: the output is indexed in rows of Wp = W + pl + pr
 // positions (Wp - Wo of them junk), so that every filter tap (r, s) reads the zero-padded

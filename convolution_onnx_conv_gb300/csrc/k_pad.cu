@@ -79,6 +79,53 @@ __global__ void __launch_bounds__(256) q8_to_bf16_kernel(const uint8_t* __restri
   }
 }
 
+// Pre-activation prologue: u = clamp(scale[c] * x + shift[c], lo, hi) per channel, rounded to
+// bf16 (nearest even), into the handle's staging copy that the conv kernels then read; the
+// conv's zero padding is therefore applied to u.  8 channels (16 bytes) per thread when
+// C % 8 == 0, else one element per thread.
+__global__ void __launch_bounds__(256) preact_bf16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
+                                                          long long n, int C, const float* __restrict__ scale,
+                                                          const float* __restrict__ shift, float lo, float hi) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if ((C & 7) == 0) {
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n / 8; g += stride) {
+      const int c0 = static_cast<int>((g * 8) % C);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + g * 8));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = fminf(fmaxf(fmaf(__uint_as_float(w[i] << 16), __ldg(scale + c0 + 2 * i), __ldg(shift + c0 + 2 * i)), lo), hi);
+        const float b = fminf(fmaxf(fmaf(__uint_as_float(w[i] & 0xffff0000u), __ldg(scale + c0 + 2 * i + 1),
+                                         __ldg(shift + c0 + 2 * i + 1)), lo), hi);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(out + g * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+      const int c = static_cast<int>(i % C);
+      const float a = fminf(fmaxf(fmaf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16), __ldg(scale + c), __ldg(shift + c)), lo), hi);
+      const __nv_bfloat16 h = __float2bfloat16_rn(a);
+      out[i] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+  }
+}
+
+cudaError_t launch_preact_bf16(const uint16_t* x, uint16_t* out, long long n, int C, const float* scale,
+                               const float* shift, float lo, float hi, int num_sms, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const long long work = (C & 7) == 0 ? n / 8 : n;
+  long long blocks = (work + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(preact_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, x, out, n, C,
+                    scale, shift, lo, hi);
+}
+
 cudaError_t launch_q8_to_bf16(const uint8_t* x, uint16_t* out, long long n, int is_signed, int zp, int num_sms,
                               cudaStream_t stream) {
   if (n == 0) return cudaSuccess;

@@ -239,6 +239,19 @@ convf_status conv_fused_create(const convf_desc* desc, const void* W, const void
 convf_status conv_fused_create_qlinear(const convf_desc* desc, const void* W, const int32_t* bias,
                                        const convf_qparams* q, convf_handle** out);
 
+/* conv_fused_create with a pre-activation prologue (the BN -> ReLU that a ResNet-v2 block
+ * applies to its input before the first conv; "tensorforge", section "ResNet fusion"): the conv
+ * reads u = clamp(pre_scale[c] * x + pre_shift[c]) per input channel c, the clamp of pre_act
+ * (CONVF_ACT_NONE, _RELU or _RELU6), with the conv's zero padding applied to u, not to x.  u is
+ * the conv's operand and is rounded to bf16 (nearest even).  It runs as a pre-pass into a
+ * handle-owned bf16 copy of the input (one extra read and write of x per run) that every
+ * kernel variant then reads.
+ *   pre_scale, pre_shift: host float[C] (e.g. conv_bn_scale_shift of the input's BN), finite.
+ * bf16 convs only (CONVF_ERR_UNSUPPORTED otherwise); the other arguments as for create. */
+convf_status conv_fused_create_preact(const convf_desc* desc, const void* W, const void* bias,
+                                      const float* bn_scale, const float* bn_shift, const float* pre_scale,
+                                      const float* pre_shift, int pre_act, convf_handle** out);
+
 /* Run the fused conv: x (device, NHWC, bf16 bits or 8-bit) -> y (device, NHWC, float32 -- or bf16
  * bits with out_dtype = CONVF_OUT_BF16 -- for the bf16 path, 8-bit for the s8 and q8 paths).  Both must be 16-byte aligned and must not overlap.
  * `stream` is a cudaStream_t (NULL = legacy default stream).  Asynchronous: no allocation,
