@@ -32,6 +32,10 @@ Every function is the plain definition of one stage, kept separate on purpose:
     conv consumes u as its operand, so u is stored in the operand type:
     rounded to bf16 to nearest-even (a reading; the affine is evaluated in
     float32 first, as the storage of x, scale and shift is float32/bf16).
+``inverted_residual``
+    A MobileNetV2 block composed from the stages above: expand 1x1 + BN + ReLU6,
+    depthwise 3x3 + BN + ReLU6, project 1x1 + BN, and the skip connection for
+    stride-1 blocks with equal channel counts (checked against torch).
 ``activation``
     ReLU = max(u, 0); ReLU6 = min(max(u, 0), 6), the two clamps of the
     residual + batchnorm + relu6 example kernel in the "Kyanite" README
@@ -445,6 +449,25 @@ def conv_bn_act_points(x, w, bias, bn, act, strides, pads, dilations, group, pts
         r = np.asarray(residual)
         z = residual_add(z, r[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]])
     return activation(z, act, lo, hi)
+
+
+def inverted_residual(x, w_expand, bn_expand, w_dw, bn_dw, w_project, bn_project, stride=1, residual=False,
+                      eps=1e-5):
+    """MobileNetV2 inverted-residual block, stage by stage in float64: 1x1 expand -> BN -> ReLU6
+    (skipped when ``w_expand`` is None: the t = 1 block), depthwise 3x3 (pad 1, ``stride``) ->
+    BN -> ReLU6, 1x1 project -> BN (linear bottleneck, no activation), then + x when
+    ``residual`` (stride 1 and equal in/out channels).  Each ``bn_*`` is (gamma, beta, mean,
+    var).  The fused block of the "tensorforge" page's "ResNet fusion" direction (BN -> ReLU
+    pairs folded into one kernel), applied to the whole block."""
+    h = np.asarray(x, dtype=np.float64)
+    if w_expand is not None:
+        h = conv_bn_act(h, w_expand, None, bn_expand, ACT_RELU6, eps=eps)
+    ch = h.shape[1]
+    h = conv_bn_act(h, w_dw, None, bn_dw, ACT_RELU6, strides=(stride, stride), pads=(1, 1, 1, 1), group=ch, eps=eps)
+    y = conv_bn_act(h, w_project, None, bn_project, ACT_NONE, eps=eps)
+    if residual:
+        y = residual_add(y, x)
+    return y
 
 
 def tolerance_ok(y, ref, atol=1e-3, rtol=1e-3):

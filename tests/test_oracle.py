@@ -633,3 +633,36 @@ def test_preactivation_pads_after_the_activation():
     wrong = torch.nn.functional.conv2d(torch.from_numpy(oracle.round_bf16(np.maximum(xp + 1.0, 0.0))),
                                        torch.from_numpy(w)).numpy()
     assert not np.allclose(y[..., 0, 0], wrong[..., 0, 0])
+
+
+# ----------------------------------------------------------- MobileNetV2 inverted residual
+
+@pytest.mark.parametrize("cin,ch,cout,stride,res,expand", [(8, 48, 8, 1, True, True), (8, 48, 12, 2, False, True),
+                                                           (16, 16, 8, 1, False, False)])
+def test_inverted_residual_matches_torch(cin, ch, cout, stride, res, expand):
+    """The block against torch's conv2d / batch_norm / hardtanh(0, 6) on CPU in float64."""
+    rng = np.random.default_rng(80 + cin + ch + stride)
+    x = rng.standard_normal((2, cin, 9, 9))
+    we = rng.standard_normal((ch, cin, 1, 1)) if expand else None
+    wd = rng.standard_normal((ch, 1, 3, 3))
+    wp = rng.standard_normal((cout, ch, 1, 1))
+
+    def bn(k):
+        return (rng.uniform(0.5, 1.5, k), rng.normal(0, 0.1, k), rng.normal(0, 0.1, k), rng.uniform(0.5, 1.5, k))
+
+    be, bd, bp = bn(ch), bn(ch), bn(cout)
+    y = oracle.inverted_residual(x, we, be, wd, bd, wp, bp, stride, res)
+    F = torch.nn.functional
+    T = torch.from_numpy
+
+    def tbn(z, p):
+        return F.batch_norm(z, T(p[2]), T(p[3]), T(p[0]), T(p[1]), False, 0.0, 1e-5)
+
+    h = T(x)
+    if expand:
+        h = F.hardtanh(tbn(F.conv2d(h, T(we)), be), 0.0, 6.0)
+    h = F.hardtanh(tbn(F.conv2d(h, T(wd), stride=stride, padding=1, groups=ch), bd), 0.0, 6.0)
+    ref = tbn(F.conv2d(h, T(wp)), bp)
+    if res:
+        ref = ref + T(x)
+    assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
