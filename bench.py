@@ -303,6 +303,37 @@ def other_configs(args, torch, cf, synthetic, workloads, peaks):
         "expand_project_1x1": {"layers": len(pw), "ms": ms_pw, "gb_s": pw_bytes / (ms_pw * 1e-3) / 1e9,
                                "pct_hbm": pw_bytes / (ms_pw * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                "tflops": sum(s.flops for s in pw) / (ms_pw * 1e-3) / 1e12}}
+    # the same stack as 17 fused inverted-residual blocks (one kernel per block: the expanded
+    # tensor never goes to HBM); GB/s against each block's own algorithmic bytes (input, output,
+    # weights)
+    blocks = workloads.mobilenetv2_blocks(64)
+    BL = []
+    for i, (name, N, cin, h, ch, cout, st, ex, res) in enumerate(blocks):
+        inp = synthetic.block_inputs(N, cin, h, ch, cout, ex, synthetic.seed_for(11, i))
+        aff = lambda bn: cf.conv_bn_scale_shift(*[t.numpy() for t in bn], 1e-5)
+        blk = cf.InvertedResidualBlock(N, cin, h, h, ch, cout, st, inp["we"], aff(inp["bn_e"]) if ex else None,
+                                       inp["wd"], aff(inp["bn_d"]), inp["wp"], aff(inp["bn_p"]), residual=res)
+        x = inp["x"].contiguous(memory_format=torch.channels_last).cuda()
+        BL.append({"conv": blk, "x": x, "y": blk.new_output()})
+    for _ in range(args.warmup):
+        for L in BL:
+            L["conv"](L["x"], L["y"])
+    gb = capture_graph(BL, torch)
+    for _ in range(args.warmup):
+        gb.replay()
+    torch.cuda.synchronize()
+    ms_b = time_graph(gb, steps, torch) / steps
+    if any(L["conv"].status() != 0 for L in BL):
+        raise SystemExit("device status error in the fused MobileNetV2 blocks")
+    blk_bytes = 0
+    for (name, N, cin, h, ch, cout, st, ex, res) in blocks:
+        ho = (h + 2 - 3) // st + 1
+        blk_bytes += N * cin * h * h * 2 + N * cout * ho * ho * 4 + 2 * (ch * cin * ex + ch * 9 + cout * ch)
+    out["mobilenetv2_b64"]["fused_blocks"] = {
+        "workload": "the same 17 blocks, each one fused kernel (expand + depthwise + project + skip)",
+        "ms_per_step": ms_b, "tflops": sum(s.flops for s in mv) / (ms_b * 1e-3) / 1e12,
+        "gb_s": blk_bytes / (ms_b * 1e-3) / 1e9, "pct_hbm": blk_bytes / (ms_b * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "speedup_vs_per_layer": ms / ms_b}
     r1 = workloads.resnet50_layers(1)
     ms_r1, _ = timed(r1, 7)
     m1 = workloads.mobilenetv2_layers(1)

@@ -22,10 +22,11 @@ CONVF_AUTO_PAD_NOTSET, CONVF_AUTO_PAD_SAME_UPPER, CONVF_AUTO_PAD_SAME_LOWER, \
     CONVF_AUTO_PAD_VALID = 0, 1, 2, 3
 CONVF_VARIANT_AUTO, CONVF_VARIANT_IMPLICIT_GEMM, CONVF_VARIANT_GEMM_1X1, CONVF_VARIANT_DEPTHWISE, \
     CONVF_VARIANT_INT8, CONVF_VARIANT_IMPLICIT_GEMM_GATHER, CONVF_VARIANT_IMPLICIT_GEMM_WINDOW, \
-    CONVF_VARIANT_IMPLICIT_GEMM_HALO, CONVF_VARIANT_INT8_TC, CONVF_VARIANT_GROUPED_DIRECT = 0, 1, 2, 3, 4, 5, 6, 7, 8, 9
+    CONVF_VARIANT_IMPLICIT_GEMM_HALO, CONVF_VARIANT_INT8_TC, CONVF_VARIANT_GROUPED_DIRECT, \
+    CONVF_VARIANT_MBV2_BLOCK = 0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 VARIANT_NAMES = {0: "auto", 1: "implicit_gemm_im2col", 2: "gemm_1x1", 3: "depthwise",
                  4: "int8_mma", 5: "implicit_gemm_gather", 6: "implicit_gemm_window", 7: "implicit_gemm_halo",
-                 8: "int8_tcgen05_exact", 9: "grouped_direct"}
+                 8: "int8_tcgen05_exact", 9: "grouped_direct", 10: "mbv2_block"}
 AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
 
 EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale_shift",
@@ -33,7 +34,8 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_status", "conv_fused_clear_status", "conv_fused_destroy",
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
-            "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact"]
+            "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact",
+            "conv_fused_create_mbv2_block"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -46,6 +48,13 @@ class ConvDesc(ctypes.Structure):
                 ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("kblocks_per_step", ctypes.c_int),
                 ("out_dtype", ctypes.c_int), ("residual", ctypes.c_int)]
+
+
+class BlockDesc(ctypes.Structure):
+    """convf_block_desc: one MobileNetV2 inverted-residual block."""
+    _fields_ = [("N", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int), ("Cin", ctypes.c_int),
+                ("Ch", ctypes.c_int), ("Cout", ctypes.c_int), ("stride", ctypes.c_int), ("expand", ctypes.c_int),
+                ("residual", ctypes.c_int)]
 
 
 class QParams(ctypes.Structure):
@@ -117,6 +126,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_create.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int32, P(vp)]
     lib.conv_fused_create_qlinear.argtypes = [dptr, vp, vp, P(QParams), P(vp)]
     lib.conv_fused_create_preact.argtypes = [dptr, vp, vp, vp, vp, vp, vp, ctypes.c_int, P(vp)]
+    lib.conv_fused_create_mbv2_block.argtypes = [P(BlockDesc)] + [vp] * 9 + [P(vp)]
     lib.conv_fused_run.argtypes = [vp, vp, vp, vp]
     lib.conv_fused_run_residual.argtypes = [vp, vp, vp, vp, vp]
     lib.conv_fused_status.argtypes = [vp]
@@ -214,6 +224,17 @@ def conv_fused_create_preact(desc: ConvDesc, W, bias=None, bn_scale=None, bn_shi
     _check(load_library().conv_fused_create_preact(ctypes.byref(desc), _addr(W), _addr(bias), _addr(bn_scale),
                                                    _addr(bn_shift), _addr(pre_scale), _addr(pre_shift),
                                                    int(pre_act), ctypes.byref(h)))
+    return h.value
+
+
+def conv_fused_create_mbv2_block(d: BlockDesc, w_expand, e_scale, e_shift, w_dw, d_scale, d_shift, w_project,
+                                 p_scale, p_shift) -> int:
+    """Fused MobileNetV2 block handle (host arrays: bf16 bits for weights, float32 affines)."""
+    h = ctypes.c_void_p()
+    _check(load_library().conv_fused_create_mbv2_block(ctypes.byref(d), _addr(w_expand), _addr(e_scale),
+                                                       _addr(e_shift), _addr(w_dw), _addr(d_scale), _addr(d_shift),
+                                                       _addr(w_project), _addr(p_scale), _addr(p_shift),
+                                                       ctypes.byref(h)))
     return h.value
 
 
@@ -419,3 +440,38 @@ class QLinearConv(FusedConv):
         N, K, Ho, Wo = self.out_shape
         dt = torch.int8 if self.y_signed else torch.uint8
         return torch.empty((N, Ho, Wo, K), dtype=dt, device="cuda").permute(0, 3, 1, 2)
+
+
+class InvertedResidualBlock(FusedConv):
+    """A MobileNetV2 block as one fused kernel over torch tensors: ``w_expand`` (bf16 [Ch][Cin][1][1]
+    or None), ``w_dw`` (bf16 [Ch][1][3][3]), ``w_project`` (bf16 [Cout][Ch][1][1]) and each stage's
+    folded BN affine (scale, shift) as float arrays.  Calling it with x (bf16, channels-last) returns
+    y (fp32, channels-last)."""
+
+    def __init__(self, N, Cin, H, W, Ch, Cout, stride, w_expand, e_affine, w_dw, d_affine, w_project, p_affine,
+                 residual=False):
+        import numpy as np
+        import torch
+        d = BlockDesc()
+        d.N, d.H, d.W, d.Cin, d.Ch, d.Cout, d.stride = N, H, W, Cin, Ch, Cout, stride
+        d.expand = int(w_expand is not None)
+        d.residual = int(bool(residual))
+        self.block = d
+
+        def bits(t):
+            return None if t is None else t.contiguous().cpu().view(torch.int16)
+
+        def f32(a):
+            return None if a is None else np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+        es, et = (f32(e_affine[0]), f32(e_affine[1])) if e_affine is not None else (None, None)
+        keep = [bits(w_expand), es, et, bits(w_dw), f32(d_affine[0]), f32(d_affine[1]), bits(w_project),
+                f32(p_affine[0]), f32(p_affine[1])]
+        self._keep = keep
+        self.handle = conv_fused_create_mbv2_block(d, *keep)
+        Ho = (H + 2 - 3) // stride + 1
+        Wo = (W + 2 - 3) // stride + 1
+        self.out_shape = (N, Cout, Ho, Wo)
+        self.s8 = False
+        self.out_bf16 = False
+        self.residual = False

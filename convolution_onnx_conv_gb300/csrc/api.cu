@@ -627,6 +627,8 @@ struct convf_handle {
   float* pre_scale;
   float* pre_shift;
   float pre_lo, pre_hi;
+  MbParams mb;      // fused MobileNetV2 block: geometry and device arrays
+  CUtensorMap tmWe, tmWp;
   WinGeom wg;       // window variant geometry
   HaloGeom hg;      // halo variant geometry
   CUtensorMap tmB;
@@ -1331,6 +1333,216 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
 }
 }  // namespace
 
+namespace {
+// Tile geometry of the fused MobileNetV2 block: TW = min(Wo, 16 for stride 1, 8 for stride 2)
+// output columns; among the row counts TH <= 8 whose input halo fits two 128-row MMA blocks
+// (IH*IW <= 256), whose expand/project accumulators fit TMEM and whose buffers fit shared
+// memory, the tallest that still gives every SM a tile, else the one with the most tiles.
+std::string mb_geom(const convf_block_desc* d, int num_sms, MbParams* g) {
+  std::memset(g, 0, sizeof *g);
+  g->N = d->N; g->H = d->H; g->W = d->W; g->Cin = d->Cin; g->Ch = d->Ch; g->Cout = d->Cout; g->st = d->stride;
+  g->Ho = (d->H + 2 - 3) / d->stride + 1;
+  g->Wo = (d->W + 2 - 3) / d->stride + 1;
+  g->Ch_pad = (int)align_up((size_t)d->Ch, 64);
+  g->cin_kb = (d->Cin + 63) / 64;
+  g->nch = g->Ch_pad / 64;
+  g->Np = (int)align_up((size_t)d->Cout, 16);
+  g->nsplit = 1;
+  if (g->Np > 256) {
+    g->Np = (int)align_up((size_t)d->Cout, 32);
+    g->nsplit = 2;
+  }
+  if (g->Np > 512) return "fused block: Cout exceeds the project accumulator";
+  g->expand = d->expand;
+  g->residual = d->residual;
+  g->h1_stride = 68;
+  g->TW = std::min(g->Wo, d->stride == 1 ? 16 : 8);
+  int best = -1;
+  long long best_tiles = -1;
+  for (int th = std::min(g->Ho, 8); th >= 1; --th) {
+    const int IH = (th - 1) * d->stride + 3, IW = (g->TW - 1) * d->stride + 3;
+    const int P = IH * IW;
+    if (P > 256 || th * g->TW > 128) continue;
+    const int rb = P > 128 ? 2 : 1;
+    if (2 * rb * 64 + g->Np > 512) continue;
+    const uint32_t xkb = rb * 16384u;
+    const uint32_t sx = g->cin_kb * xkb;
+    const uint32_t we = g->expand ? g->cin_kb * 8192u : 0u;
+    const uint32_t wp = (uint32_t)align_up((size_t)g->Np * 128, 1024);
+    const uint32_t h1 = (uint32_t)align_up((size_t)P * 68 * 4, 1024);
+    const size_t total = 1024 + sx + 2 * we + 2 * wp + h1 + 32768 + 256;
+    if (total > 232448) continue;
+    const long long tiles = (long long)d->N * ((g->Ho + th - 1) / th) * ((g->Wo + g->TW - 1) / g->TW);
+    // rows go down from the tallest: stop at the first that gives every SM a tile, else keep
+    // the one with the most tiles
+    if (best < 0 || tiles > best_tiles) {
+      best = th;
+      best_tiles = tiles;
+    }
+    if (tiles >= num_sms) break;
+  }
+  if (best < 0) return "fused block: no tile of its output fits the shared memory and TMEM budgets";
+  g->TH = best;
+  g->IH = (best - 1) * d->stride + 3;
+  g->IW = (g->TW - 1) * d->stride + 3;
+  g->P = g->IH * g->IW;
+  g->rb = g->P > 128 ? 2 : 1;
+  g->tiles_h = (g->Ho + best - 1) / best;
+  g->tiles_w = (g->Wo + g->TW - 1) / g->TW;
+  g->num_tiles = (int)best_tiles;
+  g->x_kb_bytes = g->rb * 16384u;
+  g->we_buf = g->expand ? g->cin_kb * 8192u : 0u;
+  g->wp_buf = (uint32_t)align_up((size_t)g->Np * 128, 1024);
+  g->x_bytes = g->cin_kb * (uint32_t)g->P * 128u;
+  g->we_bytes = g->cin_kb * 8192u;
+  g->wp_bytes = (uint32_t)g->Np * 128u;
+  g->off_x = 0;
+  g->off_we = g->cin_kb * g->x_kb_bytes;
+  g->off_wp = g->off_we + 2 * g->we_buf;
+  g->off_h1 = g->off_wp + 2 * g->wp_buf;
+  g->off_a = g->off_h1 + (uint32_t)align_up((size_t)g->P * 68 * 4, 1024);
+  g->off_bar = g->off_a + 32768;
+  return "";
+}
+
+uint16_t f32_to_bf16_bits(float f) {   // round to nearest even (finite values)
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+}  // namespace
+
+convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint16_t* w_expand, const float* e_scale,
+                                          const float* e_shift, const uint16_t* w_dw, const float* d_scale,
+                                          const float* d_shift, const uint16_t* w_project, const float* p_scale,
+                                          const float* p_shift, convf_handle** out) {
+  if (!out) return fail(CONVF_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!d) return fail(CONVF_ERR_INVALID_ARG, "d is NULL");
+  if (d->N < 0 || d->H < 1 || d->W < 1 || d->Cin < 1 || d->Ch < 1 || d->Cout < 1)
+    return fail(CONVF_ERR_INVALID_ARG, "block extents (N=%d H=%d W=%d Cin=%d Ch=%d Cout=%d) must be positive", d->N,
+                d->H, d->W, d->Cin, d->Ch, d->Cout);
+  if (d->stride != 1 && d->stride != 2) return fail(CONVF_ERR_INVALID_ARG, "stride=%d is not 1 or 2", d->stride);
+  if (d->expand != 0 && d->expand != 1) return fail(CONVF_ERR_INVALID_ARG, "expand=%d is not 0 or 1", d->expand);
+  if (d->residual != 0 && d->residual != 1) return fail(CONVF_ERR_INVALID_ARG, "residual=%d is not 0 or 1", d->residual);
+  if (!d->expand && d->Ch != d->Cin) return fail(CONVF_ERR_INVALID_ARG, "without an expand conv Ch (%d) must equal Cin (%d)",
+                                                 d->Ch, d->Cin);
+  if (d->residual && (d->stride != 1 || d->Cin != d->Cout))
+    return fail(CONVF_ERR_INVALID_ARG, "the skip connection needs stride 1 and Cin == Cout");
+  if (!w_dw || !d_scale || !d_shift || !w_project || !p_scale || !p_shift ||
+      (d->expand && (!w_expand || !e_scale || !e_shift)))
+    return fail(CONVF_ERR_INVALID_ARG, "a weight or affine array is NULL");
+  if (d->Cin % 8) return fail(CONVF_ERR_UNSUPPORTED, "fused block: Cin %% 8 == 0 (16-byte TMA rows)");
+  if (d->Cin > 192) return fail(CONVF_ERR_UNSUPPORTED, "fused block: Cin <= 192 (three 64-channel blocks of halo)");
+  if (d->Cout % 4) return fail(CONVF_ERR_UNSUPPORTED, "fused block: Cout %% 4 == 0 (16-byte output stores)");
+  if ((long long)d->N * d->H * d->W * d->Cin > 0x7FFFFFFFLL || (long long)d->N * d->H * d->W * d->Cout > 0x7FFFFFFFLL)
+    return fail(CONVF_ERR_UNSUPPORTED, "tensor sizes exceed the 2^31-element indexing limit");
+  convf_handle* h = new (std::nothrow) convf_handle();
+  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed");
+  cudaError_t ce = cudaGetDevice(&h->device);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (ce != cudaSuccess) {
+    delete h;
+    return fail(CONVF_ERR_CUDA, "no usable CUDA device: %s", cudaGetErrorString(ce));
+  }
+  MbParams& g = h->mb;
+  std::string why = mb_geom(d, h->num_sms, &g);
+  if (!why.empty()) {
+    delete h;
+    return fail(CONVF_ERR_UNSUPPORTED, "%s", why.c_str());
+  }
+  h->variant = CONVF_VARIANT_MBV2_BLOCK;
+  Shape& s = h->s;
+  s.N = d->N; s.C = d->Cin; s.H = d->H; s.W = d->W; s.K = d->Cout; s.R = s.S = 3; s.Cg = 1;
+  s.sh = s.sw = d->stride; s.dh = s.dw = 1; s.pt = s.pl = s.pb = s.pr = 1;
+  s.Ho = g.Ho; s.Wo = g.Wo; s.M = (long long)d->N * g.Ho * g.Wo;
+  std::memset(&h->desc, 0, sizeof h->desc);
+  h->desc.group = 1;
+  // device arrays: We [Ch_pad][Cin_pad] bf16, Wp [Np][Ch_pad] bf16, se/be/bd [Ch_pad], wd [9][Ch_pad],
+  // sp/bp [Np] (zero padding everywhere)
+  const int cin_pad = g.cin_kb * 64;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  const size_t o_we = carve((size_t)g.Ch_pad * cin_pad * 2), o_wp = carve((size_t)g.Np * g.Ch_pad * 2);
+  const size_t o_se = carve((size_t)g.Ch_pad * 4), o_be = carve((size_t)g.Ch_pad * 4);
+  const size_t o_wd = carve((size_t)9 * g.Ch_pad * 4), o_bd = carve((size_t)g.Ch_pad * 4);
+  const size_t o_sp = carve((size_t)g.Np * 4), o_bp = carve((size_t)g.Np * 4);
+  const size_t o_status = carve(sizeof(int));
+  h->dev_bytes = off;
+  std::vector<char> st(off, 0);
+  uint16_t* we = reinterpret_cast<uint16_t*>(st.data() + o_we);
+  uint16_t* wp = reinterpret_cast<uint16_t*>(st.data() + o_wp);
+  float* se = reinterpret_cast<float*>(st.data() + o_se);
+  float* be = reinterpret_cast<float*>(st.data() + o_be);
+  float* wd = reinterpret_cast<float*>(st.data() + o_wd);
+  float* bd = reinterpret_cast<float*>(st.data() + o_bd);
+  float* sp = reinterpret_cast<float*>(st.data() + o_sp);
+  float* bp = reinterpret_cast<float*>(st.data() + o_bp);
+  for (int c = 0; c < d->Ch; ++c) {
+    if (d->expand) {
+      for (int i = 0; i < d->Cin; ++i) we[(size_t)c * cin_pad + i] = w_expand[(size_t)c * d->Cin + i];
+      se[c] = e_scale[c];
+      be[c] = e_shift[c];
+    }
+    for (int t = 0; t < 9; ++t)
+      wd[(size_t)t * g.Ch_pad + c] = (float)((double)d_scale[c] * (double)bf16_to_f32(w_dw[(size_t)c * 9 + t]));
+    bd[c] = d_shift[c];
+  }
+  for (int k = 0; k < d->Cout; ++k) {
+    for (int c = 0; c < d->Ch; ++c) wp[(size_t)k * g.Ch_pad + c] = w_project[(size_t)k * d->Ch + c];
+    sp[k] = p_scale[k];
+    bp[k] = p_shift[k];
+  }
+  for (size_t i = 0; i < (size_t)g.Ch_pad; ++i)
+    if (!std::isfinite(se[i]) || !std::isfinite(be[i]) || !std::isfinite(bd[i])) {
+      delete h;
+      return fail(CONVF_ERR_INVALID_ARG, "an expand or depthwise affine value is not finite");
+    }
+  ce = cudaMalloc(&h->dev, h->dev_bytes);
+  if (ce != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s", h->dev_bytes, cudaGetErrorString(ce));
+  }
+  ce = cudaMemcpy(h->dev, st.data(), h->dev_bytes, cudaMemcpyHostToDevice);
+  char* base = static_cast<char*>(h->dev);
+  g.se = reinterpret_cast<float*>(base + o_se); g.be = reinterpret_cast<float*>(base + o_be);
+  g.wd = reinterpret_cast<float*>(base + o_wd); g.bd = reinterpret_cast<float*>(base + o_bd);
+  g.sp = reinterpret_cast<float*>(base + o_sp); g.bp = reinterpret_cast<float*>(base + o_bp);
+  h->status = reinterpret_cast<int*>(base + o_status);
+  g.status = h->status;
+  CUresult r = ce == cudaSuccess && load_encoders() ? CUDA_SUCCESS : CUDA_ERROR_NOT_SUPPORTED;
+  if (r == CUDA_SUCCESS) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cin_pad, (cuuint64_t)g.Ch_pad};
+    const cuuint64_t strides[1] = {(cuuint64_t)cin_pad * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t es[2] = {1, 1};
+    r = g_encode_tiled(&h->tmWe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base + o_we, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r == CUDA_SUCCESS) {
+    const cuuint64_t dims[2] = {(cuuint64_t)g.Ch_pad, (cuuint64_t)g.Np};
+    const cuuint64_t strides[1] = {(cuuint64_t)g.Ch_pad * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(g.Np / g.nsplit)};
+    const cuuint32_t es[2] = {1, 1};
+    r = g_encode_tiled(&h->tmWp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base + o_wp, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) {
+    cudaFree(h->dev);
+    delete h;
+    return fail(ce != cudaSuccess ? CONVF_ERR_CUDA : CONVF_ERR_CUDA, "fused block set-up failed (%s, CUresult %d)",
+                cudaGetErrorString(ce), (int)r);
+  }
+  h->grid = (int)std::min<long long>(g.num_tiles, h->num_sms);
+  h->num_tiles = g.num_tiles;
+  h->magic = kMagic;
+  *out = h;
+  return ok();
+}
+
 convf_status conv_fused_create(const convf_desc* desc, const void* W, const void* bias,
                                const float* bn_scale, const float* bn_shift,
                                const int32_t* requant_mult, const int32_t* requant_shift,
@@ -1506,6 +1718,25 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       ce = launch_tc_window(p, h->tmA, h->tmB, g.E, g.rows, h->grid, g.smem, strm);
       break;
     }
+    case CONVF_VARIANT_MBV2_BLOCK: {
+      MbParams p = h->mb;
+      if (x != h->map_x) {
+        // {C, W, H, N}, box = 64 channels x the tile's input halo (IW x IH pixels) of one image
+        const cuuint64_t dims[4] = {(cuuint64_t)s.C, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)s.C * 2, (cuuint64_t)s.W * s.C * 2,
+                                       (cuuint64_t)s.H * s.W * s.C * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)p.IW, (cuuint32_t)p.IH, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        CUresult r = g_encode_tiled(&h->tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "fused block input tensor map failed (CUresult %d)", (int)r);
+        h->map_x = x;
+      }
+      p.y = static_cast<float*>(y);
+      ce = launch_mbv2_block(p, h->tmA, h->tmWe, h->tmWp, h->grid, strm);
+      break;
+    }
     case CONVF_VARIANT_GROUPED_DIRECT: {
       GdParams p{};
       p.N = s.N; p.C = s.C; p.H = s.H; p.W = s.W; p.K = s.K; p.R = s.R; p.S = s.S; p.Ho = s.Ho; p.Wo = s.Wo;
@@ -1642,7 +1873,7 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   if (!buf || len == 0) return fail(CONVF_ERR_INVALID_ARG, "buf is NULL or empty");
   static const char* names[] = {"auto", "implicit_gemm_im2col", "gemm_1x1", "depthwise", "int8_mma",
                                 "implicit_gemm_gather", "implicit_gemm_window", "implicit_gemm_halo",
-                                "int8_tcgen05_exact", "grouped_direct"};
+                                "int8_tcgen05_exact", "grouped_direct", "mbv2_block"};
   const Shape& s = h->s;
   if (h->variant == CONVF_VARIANT_IMPLICIT_GEMM_HALO)
     snprintf(buf, len,
@@ -1657,6 +1888,13 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->wg.bnp, h->wg.E, h->wg.rows ? 1 : 0,
              h->wg.cpt, h->wg.Wp,
              h->wg.stages, h->num_tiles, h->grid, h->dev_bytes);
+  else if (h->variant == CONVF_VARIANT_MBV2_BLOCK)
+    snprintf(buf, len,
+             "variant=%s N=%d Cin=%d Ch=%d Cout=%d HxW=%dx%d stride=%d expand=%d residual=%d tile=%dx%d halo=%dx%d "
+             "halo_row_blocks=%d hidden_chunks=%d project_n=%d tiles=%d grid=%d smem=%zu weight_bytes=%zu",
+             names[h->variant], h->mb.N, h->mb.Cin, h->mb.Ch, h->mb.Cout, h->mb.H, h->mb.W, h->mb.st, h->mb.expand,
+             h->mb.residual, h->mb.TH, h->mb.TW, h->mb.IH, h->mb.IW, h->mb.rb, h->mb.nch, h->mb.Np, h->num_tiles,
+             h->grid, mbv2_block_smem(h->mb), h->dev_bytes);
   else if (h->variant == CONVF_VARIANT_INT8_TC)
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d tile=128x%d kblocks=%d kblocks_per_step=%d "

@@ -247,6 +247,36 @@ struct GdParams {
 };
 cudaError_t launch_grouped_direct(const GdParams& p, int num_sms, cudaStream_t stream);
 
+// ---------------------------------------------------------------- fused MobileNetV2 block
+// expand 1x1 (+BN, ReLU6) -> depthwise 3x3 (+BN, ReLU6) -> project 1x1 (+BN, + x) in one kernel;
+// tiles of TH x TW outputs of one image, the IH x IW input halo (P pixels, rb blocks of 128
+// MMA rows) staged by TMA, hidden channels in chunks of 64 (k_mbblock.cu)
+struct MbParams {
+  int N, H, W, Cin, Ch, Ch_pad, Cout, Ho, Wo, st;
+  int TH, TW, IH, IW, P, rb;
+  int tiles_h, tiles_w, num_tiles;
+  int cin_kb, nch, Np, nsplit;   // input 64-channel blocks, hidden chunks, project N (Cout to 16), N halves
+  int expand, residual;          // expand == 0: the t = 1 block (hidden = input)
+  int h1_stride;                 // floats per hidden row in shared memory (64 + 4: conflict-free)
+  uint32_t x_kb_bytes;           // shared-memory bytes per input channel block (rb * 16 KB)
+  uint32_t we_buf, wp_buf;       // bytes per expand / project weight buffer (two of each)
+  uint32_t x_bytes, we_bytes, wp_bytes;   // TMA transaction bytes
+  uint32_t off_x, off_we, off_wp, off_h1, off_a, off_bar;   // shared-memory layout (1 KB aligned)
+  const float* se;               // [Ch_pad] expand BN scale
+  const float* be;               // [Ch_pad] expand BN shift
+  const float* wd;               // [9][Ch_pad] depthwise taps, BN scale folded
+  const float* bd;               // [Ch_pad] depthwise BN shift
+  const float* sp;               // [Np] project BN scale
+  const float* bp;               // [Np] project BN shift
+  float* y;                      // NHWC fp32 [N][Ho][Wo][Cout]
+  int* status;
+};
+// tmX: 4-D {Cin, W, H, N} box {64, IW, IH, 1}; tmWe: 2-D {Cin_pad, Ch_pad} box {64, 64};
+// tmWp: 2-D {Ch_pad, Np} box {64, Np / nsplit}; all 128-byte swizzled, zero fill
+cudaError_t launch_mbv2_block(const MbParams& p, const CUtensorMap& tmX, const CUtensorMap& tmWe,
+                              const CUtensorMap& tmWp, int grid, cudaStream_t stream);
+size_t mbv2_block_smem(const MbParams& p);
+
 // ---------------------------------------------------------------- int8 implicit GEMM
 struct S8Params {
   int M, Kout, C, H, W, Ho, Wo, R, S;

@@ -123,6 +123,24 @@ def qlinear_inputs(spec: ConvSpec, seed: int, x_signed: bool = False, w_signed: 
             "y_scale": y_scale, "y_zp": y_zp, "x_signed": x_signed, "y_signed": y_signed}
 
 
+def block_inputs(N: int, Cin: int, H: int, Ch: int, Cout: int, expand: bool, seed: int) -> Dict[str, object]:
+    """A MobileNetV2 block's tensors: x ~ N(0,1) -> bf16, He-normal bf16 weights per conv
+    (fan-in Cin, 9 and Ch), and per stage BN = (gamma ~ U[0.5,1.5], beta ~ N(0,0.1),
+    mean ~ N(0,0.1), var ~ U[0.5,1.5])."""
+    g = _gen(seed)
+
+    def bn(k):
+        return (_uniform(g, (k,), 0.5, 1.5), torch.randn(k, generator=g) * 0.1, torch.randn(k, generator=g) * 0.1,
+                _uniform(g, (k,), 0.5, 1.5))
+
+    x = torch.randn((N, Cin, H, H), generator=g).to(torch.bfloat16)
+    we = (torch.randn((Ch, Cin, 1, 1), generator=g) * math.sqrt(2.0 / Cin)).to(torch.bfloat16) if expand else None
+    wd = (torch.randn((Ch, 1, 3, 3), generator=g) * math.sqrt(2.0 / 9)).to(torch.bfloat16)
+    wp = (torch.randn((Cout, Ch, 1, 1), generator=g) * math.sqrt(2.0 / Ch)).to(torch.bfloat16)
+    return {"x": x, "we": we, "bn_e": bn(Ch) if expand else None, "wd": wd, "bn_d": bn(Ch), "wp": wp,
+            "bn_p": bn(Cout)}
+
+
 def sample_points(spec: ConvSpec, count: int, seed: int) -> torch.Tensor:
     """``count`` output coordinates (n, k, oh, ow), always including the corners
     and edges of the output (where padding matters) and the last channel."""

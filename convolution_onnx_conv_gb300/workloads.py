@@ -142,6 +142,13 @@ def mobilenetv2_layers(n: int = 64) -> List[ConvSpec]:
     return L
 
 
+def mobilenetv2_blocks(n: int = 64):
+    """The 17 blocks as (name, N, Cin, H, Ch, Cout, stride, expand, residual): the skip connection
+    where the block keeps its stride at 1 and its channel count (the public architecture)."""
+    return [(f"mv2_block{i:02d}@b{n}", n, cin, h, hid, cout, s, hid != cin, s == 1 and cin == cout)
+            for i, (cin, hid, cout, h, s) in enumerate(MOBILENETV2_BLOCKS)]
+
+
 def depthwise_layers(n: int = 64) -> List[ConvSpec]:
     return [l for l in mobilenetv2_layers(n) if l.group > 1]
 

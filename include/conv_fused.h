@@ -114,13 +114,16 @@ typedef enum {
                                         sum exceeds 2^24 (so every partial sum is an exact integer);
                                         the epilogue adds the chunks in int32 and requantises.
                                         Bit-exact.  C % 8 == 0, K % 16 == 0, group 1. */
-  CONVF_VARIANT_GROUPED_DIRECT = 9   /* CUDA-core direct conv for any group count and filter (one
+  CONVF_VARIANT_GROUPED_DIRECT = 9,  /* CUDA-core direct conv for any group count and filter (one
                                         thread per output pixel and channel, fp32); chosen for the
                                         grouped convs the tensor-core kernels cannot take.  (Those
                                         take groups on CONVF_VARIANT_IMPLICIT_GEMM / _GEMM_1X1 when
                                         an output-channel tile covers whole groups or lies inside
                                         one: block-diagonal weights over the tile's input-channel
                                         window, at most 16x the grouped work.) */
+  CONVF_VARIANT_MBV2_BLOCK = 10      /* a whole MobileNetV2 inverted-residual block in one kernel
+                                        (conv_fused_create_mbv2_block); never selected for a single
+                                        conv */
 } convf_variant;
 
 typedef struct {
@@ -251,6 +254,33 @@ convf_status conv_fused_create_qlinear(const convf_desc* desc, const void* W, co
 convf_status conv_fused_create_preact(const convf_desc* desc, const void* W, const void* bias,
                                       const float* bn_scale, const float* bn_shift, const float* pre_scale,
                                       const float* pre_shift, int pre_act, convf_handle** out);
+
+/* A MobileNetV2 inverted-residual block as one fused kernel (the expanded "hidden" tensor stays
+ * on chip; "tensorforge", section "ResNet fusion", taken to the whole block):
+ *   h1 = ReLU6(e_scale * conv1x1(x, w_expand) + e_shift)      (absent when expand == 0: h1 = x)
+ *   h2 = ReLU6(d_scale * dwconv3x3(h1, w_dw, stride, pad 1) + d_shift)
+ *   y  = p_scale * conv1x1(h2, w_project) + p_shift  (+ x when residual)
+ * per channel, the *_scale / *_shift being each stage's folded BN (conv_bn_scale_shift).  The
+ * hidden values are kept in fp32 and the project GEMM reads h2 as two bf16 halves (hi + lo), so
+ * the result meets the same bound as a single conv.  Run with conv_fused_run(h, x, y, stream):
+ * x NHWC bf16 [N][H][W][Cin], y NHWC fp32 [N][Ho][Wo][Cout]. */
+typedef struct {
+  int N, H, W;         /* block input extent                                                  */
+  int Cin, Ch, Cout;   /* input, hidden (expanded) and output channels; Cin % 8 == 0, Cin <= 192 */
+  int stride;          /* depthwise stride: 1 or 2                                            */
+  int expand;          /* 1: a 1x1 expand Cin -> Ch precedes the depthwise; 0: none (Ch == Cin) */
+  int residual;        /* 1: y += x (stride 1 and Cin == Cout only)                           */
+} convf_block_desc;
+
+/* w_expand: host bf16 bits [Ch][Cin] (NULL when expand == 0); w_dw: [Ch][3][3]; w_project:
+ * [Cout][Ch]; the six affine arrays host float ([Ch] or [Cout]; e_* NULL when expand == 0).
+ * Refused (CONVF_ERR_UNSUPPORTED, named) when the tile geometry or the 512 TMEM columns cannot
+ * hold the block. */
+convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint16_t* w_expand,
+                                          const float* e_scale, const float* e_shift, const uint16_t* w_dw,
+                                          const float* d_scale, const float* d_shift,
+                                          const uint16_t* w_project, const float* p_scale,
+                                          const float* p_shift, convf_handle** out);
 
 /* Run the fused conv: x (device, NHWC, bf16 bits or 8-bit) -> y (device, NHWC, float32 -- or bf16
  * bits with out_dtype = CONVF_OUT_BF16 -- for the bf16 path, 8-bit for the s8 and q8 paths).  Both must be 16-byte aligned and must not overlap.
