@@ -1370,7 +1370,7 @@ std::string mb_geom(const convf_block_desc* d, int num_sms, MbParams* g) {
     const uint32_t we = g->expand ? g->cin_kb * 8192u : 0u;
     const uint32_t wp = (uint32_t)align_up((size_t)g->Np * 128, 1024);
     const uint32_t h1 = (uint32_t)align_up((size_t)P * 68 * 4, 1024);
-    const size_t total = 1024 + sx + 2 * we + 2 * wp + h1 + 32768 + 256;
+    const size_t total = 1024 + sx + 2 * we + 2 * wp + h1 + 32768 + 2 * 3072 + 256;   // one halo buffer
     if (total > 232448) continue;
     const long long tiles = (long long)d->N * ((g->Ho + th - 1) / th) * ((g->Wo + g->TW - 1) / g->TW);
     // rows go down from the tallest: stop at the first that gives every SM a tile, else keep
@@ -1391,17 +1391,25 @@ std::string mb_geom(const convf_block_desc* d, int num_sms, MbParams* g) {
   g->tiles_w = (g->Wo + g->TW - 1) / g->TW;
   g->num_tiles = (int)best_tiles;
   g->x_kb_bytes = g->rb * 16384u;
+  g->x_buf_bytes = g->cin_kb * g->x_kb_bytes;
   g->we_buf = g->expand ? g->cin_kb * 8192u : 0u;
   g->wp_buf = (uint32_t)align_up((size_t)g->Np * 128, 1024);
   g->x_bytes = g->cin_kb * (uint32_t)g->P * 128u;
   g->we_bytes = g->cin_kb * 8192u;
   g->wp_bytes = (uint32_t)g->Np * 128u;
+  // a second halo buffer when it fits: the next tile's halo then loads behind this tile's chunks
+  {
+    const size_t one = 1024 + (size_t)g->x_buf_bytes + 2 * (size_t)g->we_buf + 2 * (size_t)g->wp_buf +
+                       align_up((size_t)g->P * 68 * 4, 1024) + 32768 + 2 * 3072 + 256;
+    g->nxb = one + g->x_buf_bytes <= 232448 ? 2 : 1;
+  }
   g->off_x = 0;
-  g->off_we = g->cin_kb * g->x_kb_bytes;
+  g->off_we = g->nxb * g->x_buf_bytes;
   g->off_wp = g->off_we + 2 * g->we_buf;
   g->off_h1 = g->off_wp + 2 * g->wp_buf;
   g->off_a = g->off_h1 + (uint32_t)align_up((size_t)g->P * 68 * 4, 1024);
-  g->off_bar = g->off_a + 32768;
+  g->off_vec = g->off_a + 32768;
+  g->off_bar = g->off_vec + 2 * 3072;
   return "";
 }
 
@@ -1467,6 +1475,7 @@ convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint1
   const size_t o_se = carve((size_t)g.Ch_pad * 4), o_be = carve((size_t)g.Ch_pad * 4);
   const size_t o_wd = carve((size_t)9 * g.Ch_pad * 4), o_bd = carve((size_t)g.Ch_pad * 4);
   const size_t o_sp = carve((size_t)g.Np * 4), o_bp = carve((size_t)g.Np * 4);
+  const size_t o_vec = carve((size_t)g.nch * 12 * 64 * 4);
   const size_t o_status = carve(sizeof(int));
   h->dev_bytes = off;
   std::vector<char> st(off, 0);
@@ -1493,6 +1502,17 @@ convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint1
     sp[k] = p_scale[k];
     bp[k] = p_shift[k];
   }
+  // per chunk j: [12][64] = expand scale, expand shift, the nine depthwise taps, depthwise shift
+  float* vec = reinterpret_cast<float*>(st.data() + o_vec);
+  for (int j = 0; j < g.nch; ++j)
+    for (int c = 0; c < 64; ++c) {
+      const int ch = j * 64 + c;
+      float* v = vec + (size_t)j * 12 * 64 + c;
+      v[0] = se[ch];
+      v[64] = be[ch];
+      for (int t = 0; t < 9; ++t) v[(2 + t) * 64] = wd[(size_t)t * g.Ch_pad + ch];
+      v[11 * 64] = bd[ch];
+    }
   for (size_t i = 0; i < (size_t)g.Ch_pad; ++i)
     if (!std::isfinite(se[i]) || !std::isfinite(be[i]) || !std::isfinite(bd[i])) {
       delete h;
@@ -1509,6 +1529,7 @@ convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint1
   g.se = reinterpret_cast<float*>(base + o_se); g.be = reinterpret_cast<float*>(base + o_be);
   g.wd = reinterpret_cast<float*>(base + o_wd); g.bd = reinterpret_cast<float*>(base + o_bd);
   g.sp = reinterpret_cast<float*>(base + o_sp); g.bp = reinterpret_cast<float*>(base + o_bp);
+  g.vec = reinterpret_cast<float*>(base + o_vec);
   h->status = reinterpret_cast<int*>(base + o_status);
   g.status = h->status;
   CUresult r = ce == cudaSuccess && load_encoders() ? CUDA_SUCCESS : CUDA_ERROR_NOT_SUPPORTED;
@@ -1891,9 +1912,10 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else if (h->variant == CONVF_VARIANT_MBV2_BLOCK)
     snprintf(buf, len,
              "variant=%s N=%d Cin=%d Ch=%d Cout=%d HxW=%dx%d stride=%d expand=%d residual=%d tile=%dx%d halo=%dx%d "
-             "halo_row_blocks=%d hidden_chunks=%d project_n=%d tiles=%d grid=%d smem=%zu weight_bytes=%zu",
+             "halo_row_blocks=%d halo_buffers=%d hidden_chunks=%d project_n=%d tiles=%d grid=%d smem=%zu weight_bytes=%zu",
              names[h->variant], h->mb.N, h->mb.Cin, h->mb.Ch, h->mb.Cout, h->mb.H, h->mb.W, h->mb.st, h->mb.expand,
-             h->mb.residual, h->mb.TH, h->mb.TW, h->mb.IH, h->mb.IW, h->mb.rb, h->mb.nch, h->mb.Np, h->num_tiles,
+             h->mb.residual, h->mb.TH, h->mb.TW, h->mb.IH, h->mb.IW, h->mb.rb, h->mb.nxb, h->mb.nch, h->mb.Np,
+             h->num_tiles,
              h->grid, mbv2_block_smem(h->mb), h->dev_bytes);
   else if (h->variant == CONVF_VARIANT_INT8_TC)
     snprintf(buf, len,

@@ -259,9 +259,12 @@ struct MbParams {
   int expand, residual;          // expand == 0: the t = 1 block (hidden = input)
   int h1_stride;                 // floats per hidden row in shared memory (64 + 4: conflict-free)
   uint32_t x_kb_bytes;           // shared-memory bytes per input channel block (rb * 16 KB)
+  uint32_t x_buf_bytes;          // one halo buffer (cin_kb * x_kb_bytes)
+  int nxb;                       // halo buffers: 2 (the next tile's halo loads behind this one) or 1
   uint32_t we_buf, wp_buf;       // bytes per expand / project weight buffer (two of each)
   uint32_t x_bytes, we_bytes, wp_bytes;   // TMA transaction bytes
-  uint32_t off_x, off_we, off_wp, off_h1, off_a, off_bar;   // shared-memory layout (1 KB aligned)
+  uint32_t off_x, off_we, off_wp, off_h1, off_a, off_vec, off_bar;   // shared-memory layout (1 KB aligned)
+  const float* vec;              // [nch][12][64]: per chunk expand scale, shift, 9 taps, dw shift
   const float* se;               // [Ch_pad] expand BN scale
   const float* be;               // [Ch_pad] expand BN shift
   const float* wd;               // [9][Ch_pad] depthwise taps, BN scale folded

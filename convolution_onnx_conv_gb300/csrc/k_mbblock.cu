@@ -34,6 +34,26 @@ constexpr int kMbTHMax = 8;       // output rows per tile, at most
 
 __device__ __forceinline__ float relu6(float v) { return fminf(fmaxf(v, 0.f), 6.f); }
 
+// two fp32 lanes in one 64-bit register pair for the packed fp32 FMA (two fused multiply-adds,
+// each rounded to nearest, per instruction)
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(f32x2 v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// per hidden chunk, the per-channel vectors in one contiguous 3 KB block (one bulk copy):
+// rows of 64 floats: expand BN scale, expand BN shift, the nine depthwise taps, depthwise shift
+constexpr int kVecRows = 12;
+constexpr uint32_t kVecBytes = kVecRows * 64 * 4;
+
 template <int ST>
 __global__ void __launch_bounds__(kMbThreads, 1)
     mbv2_block_kernel(const MbParams p, const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWe,
@@ -46,22 +66,25 @@ __global__ void __launch_bounds__(kMbThreads, 1)
   float* sH1 = reinterpret_cast<float*>(smem + p.off_h1);
   uint8_t* sAhi = smem + p.off_a;
   uint8_t* sAlo = sAhi + 16384;
+  float* sVec = reinterpret_cast<float*>(smem + p.off_vec);   // [2][kVecRows][64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
-  uint64_t* bx = bars;          // input halo landed (per tile)
-  uint64_t* bwe = bars + 1;     // [2] expand weights landed (per buffer use)
-  uint64_t* bwp = bars + 3;     // [2] project weights landed
-  uint64_t* bexp = bars + 5;    // [2] expand MMAs of a chunk complete
-  uint64_t* bdw = bars + 7;     // depthwise of a chunk written (8 worker warps)
-  uint64_t* bprj = bars + 8;    // project MMAs of a chunk complete
-  uint64_t* btile = bars + 9;   // project epilogue of a tile done (8 worker warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* bx = bars;          // [2] input halo landed (per halo buffer use)
+  uint64_t* bwe = bars + 2;     // [2] expand weights landed (per buffer use)
+  uint64_t* bwp = bars + 4;     // [2] project weights landed
+  uint64_t* bexp = bars + 6;    // [2] expand MMAs of a chunk complete
+  uint64_t* bdw = bars + 8;     // depthwise of a chunk written (8 worker warps)
+  uint64_t* bprj = bars + 9;    // project MMAs of a chunk complete
+  uint64_t* btile = bars + 10;  // project epilogue of a tile done (8 worker warps)
+  uint64_t* bvec = bars + 11;   // [2] per-channel vectors of a chunk landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bx, 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&bx[b], 1);
+      mbar_init(&bvec[b], 1);
       mbar_init(&bwe[b], 1);
       mbar_init(&bwp[b], 1);
       mbar_init(&bexp[b], 1);
@@ -110,18 +133,35 @@ __global__ void __launch_bounds__(kMbThreads, 1)
       const uint64_t dAlo = sdesc_kmajor_sw128(smem_u32(sAlo));
       int gc = 0;   // chunks issued so far (all tiles): weight buffer gc % 2, phases
       int ti = 0;   // tiles done by this CTA
-      auto load_weights = [&](int g, int j) {
+      // expand weights of chunk j into buffer g % 2; project weights likewise
+      auto load_we = [&](int g, int j) {
         const int b = g & 1;
-        if (p.expand) {
-          mbar_arrive_expect_tx(&bwe[b], p.we_bytes);
-          for (int kb = 0; kb < p.cin_kb; ++kb)
-            tma_load_2d(sWe + b * p.we_buf + kb * 8192, &tmWe, &bwe[b], kb * 64, j * 64);
-        }
+        mbar_arrive_expect_tx(&bwe[b], p.we_bytes);
+        for (int kb = 0; kb < p.cin_kb; ++kb)
+          tma_load_2d(sWe + b * p.we_buf + kb * 8192, &tmWe, &bwe[b], kb * 64, j * 64);
+      };
+      auto load_vec = [&](int g, int j) {
+        const int b = g & 1;
+        mbar_arrive_expect_tx(&bvec[b], kVecBytes);
+        bulk_load(sVec + b * kVecRows * 64, p.vec + static_cast<size_t>(j) * kVecRows * 64, kVecBytes, &bvec[b]);
+      };
+      auto load_wp = [&](int g, int j) {
+        const int b = g & 1;
         mbar_arrive_expect_tx(&bwp[b], p.wp_bytes);
         for (int h = 0; h < p.nsplit; ++h)
           tma_load_2d(sWp + b * p.wp_buf + h * nh * 128, &tmWp, &bwp[b], j * 64, h * nh);
       };
-      auto expand = [&](int g) -> bool {
+      // the input halo of tile number t (this CTA's t-th) into halo buffer t % nxb
+      auto load_x = [&](int t) {
+        int n, oy0, ox0;
+        tile_pos(blockIdx.x + t * gridDim.x, n, oy0, ox0);
+        const int xb = t % p.nxb;
+        mbar_arrive_expect_tx(&bx[xb], p.x_bytes);
+        for (int kb = 0; kb < p.cin_kb; ++kb)
+          tma_load_4d(sX + xb * p.x_buf_bytes + kb * p.x_kb_bytes, &tmX, &bx[xb], kb * 64, ox0 * ST - 1,
+                      oy0 * ST - 1, n);
+      };
+      auto expand = [&](int g, int xb) -> bool {
         const int b = g & 1;
         if (!mbar_wait(&bwe[b], (g >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
@@ -130,32 +170,51 @@ __global__ void __launch_bounds__(kMbThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc_mma_bf16(tmem + b * de_stride + rbk * 64,
-                          dX + ((kb * p.x_kb_bytes + rbk * 16384) >> 4) + 2 * k,
+                          dX + ((xb * p.x_buf_bytes + kb * p.x_kb_bytes + rbk * 16384) >> 4) + 2 * k,
                           dWe + ((b * p.we_buf + kb * 8192) >> 4) + 2 * k, idesc_e, (kb | k) != 0);
         tc_commit(&bexp[b]);
         return true;
       };
-      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++ti) {
-        int n, oy0, ox0;
-        tile_pos(tile, n, oy0, ox0);
-        // the previous tile's project epilogue has read the halo (skip connection) and the
-        // project accumulator
-        if (ti > 0 && !mbar_wait(btile, (ti - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(bx, p.x_bytes);
-        for (int kb = 0; kb < p.cin_kb; ++kb)
-          tma_load_4d(sX + kb * p.x_kb_bytes, &tmX, bx, kb * 64, ox0 * ST - 1, oy0 * ST - 1, n);
+      const int ntiles = blockIdx.x < static_cast<unsigned>(p.num_tiles)
+                             ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+      if (ntiles > 0) load_x(0);
+      bool okk = true;
+      for (ti = 0; ti < ntiles && okk; ++ti) {
+        const int xb = ti % p.nxb;
         const int g0 = gc;
-        for (int j = 0; j < p.nch && j < 2; ++j) load_weights(g0 + j, j);
+        if (ti > 0) {
+          // every MMA of the previous tile is complete: its weight buffers are free
+          if (!mbar_wait(bprj, (g0 - 1) & 1, abort_flag, p.status)) break;
+          if (p.nxb == 1) {
+            // one halo buffer: the previous tile's project epilogue must be done with it first
+            if (!mbar_wait(btile, (ti - 1) & 1, abort_flag, p.status)) break;
+            load_x(ti);
+          }
+        }
+        for (int j = 0; j < p.nch && j < 2; ++j) {
+          if (p.expand) load_we(g0 + j, j);
+          load_wp(g0 + j, j);
+          load_vec(g0 + j, j);   // (the workers of chunk g0 + j - 2 are done with the buffer)
+        }
         if (p.expand) {
-          if (!mbar_wait(bx, ti & 1, abort_flag, p.status)) break;
-          bool okk = true;
-          for (int j = 0; j < p.nch && j < 2 && okk; ++j) okk = expand(g0 + j);
+          if (!mbar_wait(&bx[xb], (ti / p.nxb) & 1, abort_flag, p.status)) break;
+          for (int j = 0; j < p.nch && j < 2 && okk; ++j) okk = expand(g0 + j, xb);
           if (!okk) break;
         }
-        bool okk = true;
+        // the project accumulator (and, with two halo buffers, the other halo buffer) is free once
+        // the previous tile's project epilogue is done; then the next tile's halo loads behind
+        // this one's chunks
+        if (ti > 0 && p.nxb == 2 && !mbar_wait(btile, (ti - 1) & 1, abort_flag, p.status)) break;
+        if (p.nxb == 2 && ti + 1 < ntiles) load_x(ti + 1);
         for (int j = 0; j < p.nch && okk; ++j) {
           const int g = g0 + j;
           const int b = g & 1;
+          // expand weights of chunk j + 2 as soon as expand j has released their buffer
+          if (p.expand && j + 2 < p.nch) {
+            if (!mbar_wait(&bexp[b], (g >> 1) & 1, abort_flag, p.status)) { okk = false; break; }
+            load_we(g + 2, j + 2);
+          }
           // project chunk j once its depthwise output is in shared memory
           if (!mbar_wait(bdw, g & 1, abort_flag, p.status) || !mbar_wait(&bwp[b], (g >> 1) & 1, abort_flag, p.status)) {
             okk = false;
@@ -170,18 +229,16 @@ __global__ void __launch_bounds__(kMbThreads, 1)
               tc_mma_bf16(tmem + dp_col + h * nh, dAlo + 2 * k, bd, idesc_p, 1u);
             }
           tc_commit(bprj);
+          // the workers are done with chunk j's vectors (its depthwise is written)
+          if (j + 2 < p.nch) load_vec(g + 2, j + 2);
           if (j + 2 < p.nch) {
-            // buffer b is free once project j (and, before it in issue order, expand j) completed
-            if (!mbar_wait(bprj, g & 1, abort_flag, p.status)) {
-              okk = false;
-              break;
-            }
-            load_weights(g + 2, j + 2);
-            if (p.expand && !expand(g + 2)) okk = false;
+            // project weights of chunk j + 2 once project j has released their buffer
+            if (!mbar_wait(bprj, g & 1, abort_flag, p.status)) { okk = false; break; }
+            load_wp(g + 2, j + 2);
+            if (p.expand && !expand(g + 2, xb)) okk = false;
           }
         }
         gc += p.nch;
-        if (!okk) break;
       }
     }
     __syncwarp();
@@ -201,13 +258,14 @@ __global__ void __launch_bounds__(kMbThreads, 1)
       for (int j = 0; j < p.nch; ++j) {
         const int g = gc + j;
         const int b = g & 1;
-        const int hc0 = j * 64;               // first hidden channel of the chunk
         if (p.expand) {
           if (!mbar_wait(&bexp[b], (g >> 1) & 1, abort_flag, p.status)) { okk = false; break; }
           tc_fence_after();
         } else if (j == 0) {
-          if (!mbar_wait(bx, ti & 1, abort_flag, p.status)) { okk = false; break; }
+          if (!mbar_wait(&bx[ti % p.nxb], (ti / p.nxb) & 1, abort_flag, p.status)) { okk = false; break; }
         }
+        if (!mbar_wait(&bvec[b], (g >> 1) & 1, abort_flag, p.status)) { okk = false; break; }
+        const float* vec = sVec + b * kVecRows * 64;
         named_barrier(1, kMbWorkers);         // the previous chunk's depthwise is done with sH1
         // ---- hidden epilogue: pixel rows of the halo -> fp32 rows of sH1
         {
@@ -228,8 +286,8 @@ __global__ void __launch_bounds__(kMbThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
                   const int c = c_beg + cc + e;
-                  const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.se + hc0 + c));
-                  const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.be + hc0 + c));
+                  const float4 s4 = *reinterpret_cast<const float4*>(vec + c);
+                  const float4 b4 = *reinterpret_cast<const float4*>(vec + 64 + c);
                   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
                   if (valid)
                     o = make_float4(relu6(fmaf(__uint_as_float(v[e]), s4.x, b4.x)),
@@ -243,15 +301,16 @@ __global__ void __launch_bounds__(kMbThreads, 1)
           } else if (pix < p.P) {
             // no expand (t = 1): the hidden tensor is the input itself, bf16 in the halo's
             // 128-byte-swizzled rows (k-block j)
-            const uint8_t* xrow = sX + j * p.x_kb_bytes + (pix >> 3) * 1024 + (pix & 7) * 128;
+            const uint8_t* xrow = sX + (ti % p.nxb) * p.x_buf_bytes + j * p.x_kb_bytes + (pix >> 3) * 1024 + (pix & 7) * 128;
             for (int c = c_beg; c < c_beg + c_cnt; c += 8) {
-              const uint4 w = *reinterpret_cast<const uint4*>(xrow + ((((c >> 3) ^ (pix & 7))) << 4));
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                hrow[c + 2 * e] = valid ? __uint_as_float(ww[e] << 16) : 0.f;
-                hrow[c + 2 * e + 1] = valid ? __uint_as_float(ww[e] & 0xffff0000u) : 0.f;
-              }
+              uint4 w = *reinterpret_cast<const uint4*>(xrow + ((((c >> 3) ^ (pix & 7))) << 4));
+              if (!valid) w = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<float4*>(hrow + c) = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                                                  __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+              *reinterpret_cast<float4*>(hrow + c + 4) = make_float4(__uint_as_float(w.z << 16),
+                                                                      __uint_as_float(w.z & 0xffff0000u),
+                                                                      __uint_as_float(w.w << 16),
+                                                                      __uint_as_float(w.w & 0xffff0000u));
             }
           }
         }
@@ -261,34 +320,48 @@ __global__ void __launch_bounds__(kMbThreads, 1)
         if (g > 0 && !mbar_wait(bprj, (g - 1) & 1, abort_flag, p.status)) { okk = false; break; }
         // ---- depthwise 3x3 (stride ST, pad 1) + BN + ReLU6 -> bf16 hi/lo A operands
         if (dox < p.TW) {
-          float4 tp[9];
+          f32x2 tp[9][2];
 #pragma unroll
-          for (int t = 0; t < 9; ++t) tp[t] = __ldg(reinterpret_cast<const float4*>(p.wd + t * p.Ch_pad + hc0 + 4 * cg));
-          const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bd + hc0 + 4 * cg));
-          float4 acc[kMbTHMax];
+          for (int t = 0; t < 9; ++t) {
+            const float4 w4 = *reinterpret_cast<const float4*>(vec + (2 + t) * 64 + 4 * cg);
+            tp[t][0] = pk2(w4.x, w4.y);
+            tp[t][1] = pk2(w4.z, w4.w);
+          }
+          const float4 bb = *reinterpret_cast<const float4*>(vec + 11 * 64 + 4 * cg);
+          f32x2 acc2[kMbTHMax][2];
 #pragma unroll
-          for (int o = 0; o < kMbTHMax; ++o) acc[o] = bb;
+          for (int o = 0; o < kMbTHMax; ++o) {
+            acc2[o][0] = pk2(bb.x, bb.y);
+            acc2[o][1] = pk2(bb.z, bb.w);
+          }
           constexpr int kIHMax = (kMbTHMax - 1) * ST + 3;
 #pragma unroll
           for (int iy = 0; iy < kIHMax; ++iy) {
             if (iy >= p.IH) continue;          // (predicates, not breaks: the loops stay unrolled)
-            float4 v[3];
+            f32x2 v[3][2];
 #pragma unroll
-            for (int s = 0; s < 3; ++s)
-              v[s] = *reinterpret_cast<const float4*>(sH1 + static_cast<size_t>(iy * p.IW + dox * ST + s) * p.h1_stride +
-                                                      4 * cg);
+            for (int s = 0; s < 3; ++s) {
+              const float4 f = *reinterpret_cast<const float4*>(sH1 + static_cast<size_t>(iy * p.IW + dox * ST + s) * p.h1_stride +
+                                                               4 * cg);
+              v[s][0] = pk2(f.x, f.y);
+              v[s][1] = pk2(f.z, f.w);
+            }
 #pragma unroll
             for (int o = 0; o < kMbTHMax; ++o) {
               const int r = iy - o * ST;
               if (r < 0 || r > 2) continue;
 #pragma unroll
               for (int s = 0; s < 3; ++s) {
-                acc[o].x = fmaf(v[s].x, tp[r * 3 + s].x, acc[o].x);
-                acc[o].y = fmaf(v[s].y, tp[r * 3 + s].y, acc[o].y);
-                acc[o].z = fmaf(v[s].z, tp[r * 3 + s].z, acc[o].z);
-                acc[o].w = fmaf(v[s].w, tp[r * 3 + s].w, acc[o].w);
+                acc2[o][0] = fma2(v[s][0], tp[r * 3 + s][0], acc2[o][0]);
+                acc2[o][1] = fma2(v[s][1], tp[r * 3 + s][1], acc2[o][1]);
               }
             }
+          }
+          float4 acc[kMbTHMax];
+#pragma unroll
+          for (int o = 0; o < kMbTHMax; ++o) {
+            upk2(acc2[o][0], acc[o].x, acc[o].y);
+            upk2(acc2[o][1], acc[o].z, acc[o].w);
           }
 #pragma unroll
           for (int o = 0; o < kMbTHMax; ++o) {
@@ -340,7 +413,8 @@ __global__ void __launch_bounds__(kMbThreads, 1)
             float4 o = make_float4(fmaf(__uint_as_float(v[e]), s4.x, b4.x), fmaf(__uint_as_float(v[e + 1]), s4.y, b4.y),
                                    fmaf(__uint_as_float(v[e + 2]), s4.z, b4.z), fmaf(__uint_as_float(v[e + 3]), s4.w, b4.w));
             if (p.residual) {
-              const uint8_t* xr = sX + (k >> 6) * p.x_kb_bytes + (hp >> 3) * 1024 + (hp & 7) * 128;
+              const uint8_t* xr = sX + (ti % p.nxb) * p.x_buf_bytes + (k >> 6) * p.x_kb_bytes + (hp >> 3) * 1024 +
+                                  (hp & 7) * 128;
               const uint2 w = *reinterpret_cast<const uint2*>(xr + (((((k & 63) >> 3) ^ (hp & 7))) << 4) + (k & 4) * 2);
               o.x += __uint_as_float(w.x << 16);
               o.y += __uint_as_float(w.x & 0xffff0000u);
