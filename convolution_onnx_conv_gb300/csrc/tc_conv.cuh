@@ -93,19 +93,21 @@ struct SegSched {
   }
 };
 
-// EXT: the epilogue adds a residual and/or stores bf16 (TcConvParams::res, out_bf16); its own
-// instantiation, so the plain fp32 epilogue keeps its code (a shared one cost 1.3% of the
-// ResNet-50 step).
+// EXTM: 0 the plain fp32 epilogue; 1 a residual (fp32 or bf16 y); 2 bf16 y without a residual.
+// Each its own instantiation: a shared epilogue cost the fp32 one 1.3% of the ResNet-50 step, and
+// the residual's prefetched rows (32 registers) made the bf16-only epilogue spill.
 // IQ: integer-exact mode for 8-bit convolutions (TcConvParams::iq_*): the accumulator restarts
 // every iq_chunk_kb reduction blocks into alternating TMEM buffers; both epilogue warpgroups
 // drain every chunk (one column half each), add it to int32 sums held in registers and, after a
 // tile's last chunk, requantise and store 8-bit outputs.
-template <int BN, bool GATHER, bool PAIR, bool SK, bool EXT, bool IQ = false>
+template <int BN, bool GATHER, bool PAIR, bool SK, int EXTM, bool IQ = false>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
+  constexpr bool EXT = EXTM != 0;   // residual and/or bf16 output
+  constexpr bool RES = EXTM == 1;   // a residual may be added
   static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
   static_assert(!(IQ && (GATHER || PAIR || SK || EXT)), "the integer-exact mode runs whole tiles on single CTAs");
   static_assert(!IQ || BN == 64 || BN == 128, "the integer-exact epilogue holds 32 or 64 int32 sums per thread");
@@ -694,8 +696,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           const bool w16 = EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0;
           const int sub8 = lane >> 2;   // w16: row within each group of eight
           const int c8 = lane & 3;      // w16: 8-channel column group
-          float4 rv[EXT ? 8 : 1];
-          if (EXT && w16) {
+          float4 rv[RES ? 8 : 1];
+          if (RES && w16) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -712,7 +714,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), 0.f, 0.f);
               }
             }
-          } else if (EXT) {
+          } else if (RES) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -757,14 +759,18 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               float o[8] = {fmaf(x0[i].x, s0.x, b0.x), fmaf(x0[i].y, s0.y, b0.y), fmaf(x0[i].z, s0.z, b0.z),
                             fmaf(x0[i].w, s0.w, b0.w), fmaf(x1[i].x, s1.x, b1.x), fmaf(x1[i].y, s1.y, b1.y),
                             fmaf(x1[i].z, s1.z, b1.z), fmaf(x1[i].w, s1.w, b1.w)};
-              const uint32_t rb[4] = {__float_as_uint(rv[i].x), __float_as_uint(rv[i].y), __float_as_uint(rv[i].z),
-                                      __float_as_uint(rv[i].w)};
               uint32_t pk[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 // residual (zero bits when there is none) added before the clamp, then RNE to bf16
-                const float lo = fminf(fmaxf(o[2 * j] + __uint_as_float(rb[j] << 16), p.lo), p.hi);
-                const float hi = fminf(fmaxf(o[2 * j + 1] + __uint_as_float(rb[j] & 0xffff0000u), p.lo), p.hi);
+                float a0 = o[2 * j], a1 = o[2 * j + 1];
+                if constexpr (RES) {
+                  const uint32_t rb = __float_as_uint(j == 0 ? rv[i].x : j == 1 ? rv[i].y : j == 2 ? rv[i].z : rv[i].w);
+                  a0 += __uint_as_float(rb << 16);
+                  a1 += __uint_as_float(rb & 0xffff0000u);
+                }
+                const float lo = fminf(fmaxf(a0, p.lo), p.hi);
+                const float hi = fminf(fmaxf(a1, p.lo), p.hi);
                 const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
                 pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
               }
@@ -823,11 +829,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;   // element index
               float4 v = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
                                      fmaf(a[i].w, sc.w, bi.w));
-              if (EXT) {   // zero where there is no residual
-                v.x += rv[EXT ? i : 0].x;
-                v.y += rv[EXT ? i : 0].y;
-                v.z += rv[EXT ? i : 0].z;
-                v.w += rv[EXT ? i : 0].w;
+              if (RES) {   // zero where there is no residual
+                v.x += rv[RES ? i : 0].x;
+                v.y += rv[RES ? i : 0].y;
+                v.z += rv[RES ? i : 0].z;
+                v.w += rv[RES ? i : 0].w;
               }
               v = make_float4(fminf(fmaxf(v.x, p.lo), p.hi), fminf(fmaxf(v.y, p.lo), p.hi),
                               fminf(fmaxf(v.z, p.lo), p.hi), fminf(fmaxf(v.w, p.lo), p.hi));
@@ -1029,11 +1035,11 @@ teardown:
   }
 }
 
-template <int BN, bool GATHER, bool PAIR, bool SK = false, bool EXT = false, bool IQ = false>
+template <int BN, bool GATHER, bool PAIR, bool SK = false, int EXTM = 0, bool IQ = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              int grid, cudaStream_t stream) {
   static bool configured = false;
-  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXT, IQ>;
+  auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXTM, IQ>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcCfg<BN, GATHER, PAIR>::kSmem);

@@ -16,7 +16,7 @@ cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const 
     // integer-exact 8-bit convolution: single CTAs, whole tiles, 64- or 128-wide tiles
     if (gather || pair || p.sk) return cudaErrorInvalidValue;
 #if CONVF_BN == 64 || CONVF_BN == 128
-    return launch_tc_conv_t<CONVF_BN, false, false, false, false, true>(p, tmA, tmB, grid, stream);
+    return launch_tc_conv_t<CONVF_BN, false, false, false, 0, true>(p, tmA, tmB, grid, stream);
 #else
     return cudaErrorInvalidValue;
 #endif
@@ -24,9 +24,15 @@ cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const 
   if (p.res != nullptr || p.out_bf16) {
     // residual and/or bf16 output: the extended-epilogue instantiations
     if (gather) return cudaErrorInvalidValue;
-    if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, true>(p, tmA, tmB, grid, stream);
-    if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, true>(p, tmA, tmB, grid, stream);
-    return launch_tc_conv_t<CONVF_BN, false, false, false, true>(p, tmA, tmB, grid, stream);
+    if (p.res != nullptr) {
+      if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, 1>(p, tmA, tmB, grid, stream);
+      if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, 1>(p, tmA, tmB, grid, stream);
+      return launch_tc_conv_t<CONVF_BN, false, false, false, 1>(p, tmA, tmB, grid, stream);
+    }
+    // bf16 output without a residual
+    if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, 2>(p, tmA, tmB, grid, stream);
+    if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, 2>(p, tmA, tmB, grid, stream);
+    return launch_tc_conv_t<CONVF_BN, false, false, false, 2>(p, tmA, tmB, grid, stream);
   }
   if (p.sk) {
     // stream-K: single CTAs with TMA activation loads only
