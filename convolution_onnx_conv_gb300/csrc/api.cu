@@ -336,9 +336,10 @@ std::string cannot(int v, const convf_desc* d, const Shape& s) {
   const bool bf = d->dtype == CONVF_BF16;
   char b[256];
   if ((d->out_dtype != CONVF_OUT_F32 || d->residual) && v != CONVF_VARIANT_GEMM_1X1 &&
-      v != CONVF_VARIANT_IMPLICIT_GEMM && v != CONVF_VARIANT_GROUPED_DIRECT)
-    return "bf16 output and the residual input are served by the TMA implicit-GEMM, 1x1 and direct grouped kernels "
-           "only";
+      v != CONVF_VARIANT_IMPLICIT_GEMM && v != CONVF_VARIANT_GROUPED_DIRECT && v != CONVF_VARIANT_DEPTHWISE &&
+      v != CONVF_VARIANT_IMPLICIT_GEMM_HALO)
+    return "bf16 output and the residual input are served by the TMA implicit-GEMM, 1x1, halo, depthwise and direct "
+           "grouped kernels only";
   switch (v) {
     case CONVF_VARIANT_DEPTHWISE:
       if (!bf) return "depthwise serves bf16 only";
@@ -1693,6 +1694,7 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.sh = s.sh; p.sw = s.sw; p.pt = s.pt; p.pl = s.pl; p.dh = s.dh; p.dw = s.dw;
       p.x = static_cast<const uint16_t*>(x); p.taps = h->taps; p.bias = h->bias; p.y = static_cast<float*>(y);
       p.lo = h->lo; p.hi = h->hi; p.status = h->status;
+      p.out_bf16 = h->out_bf16 ? 1 : 0; p.res = h->has_res ? res : nullptr;
       if (dw_uses_tma(p) && x != h->map_x) {
         if ((st = encode_dw_map(h, x)) != CONVF_OK) return st;
       }
@@ -1721,6 +1723,7 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.tpo = g.tpo; p.b_stages = g.b_stages; p.resident = g.resident ? 1 : 0;
       p.scale = h->scale; p.bias = h->bias; p.y = static_cast<float*>(y); p.lo = h->lo; p.hi = h->hi;
       p.status = h->status;
+      p.out_bf16 = h->out_bf16 ? 1 : 0; p.res = h->has_res ? res : nullptr;
       ce = launch_tc_halo(p, h->tmA, h->tmB, g.bn, h->grid, strm);
       break;
     }

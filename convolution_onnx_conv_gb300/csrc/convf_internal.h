@@ -143,9 +143,11 @@ struct HaloParams {
   int resident;           // 1: one output-channel block whose weights fit the stages: loaded once
   const float* scale;     // [Kpad]
   const float* bias;      // [Kpad]
-  float* y;               // NHWC fp32 [N*Ho*Wo][Kout]
+  float* y;               // NHWC fp32 [N*Ho*Wo][Kout], or bf16 bits when out_bf16
   float lo, hi;
   int* status;
+  int out_bf16;           // y (and res) hold bf16, rounded to nearest even
+  const void* res;        // residual of y's type and shape added before the clamp, or null
 };
 // BN in {64, 128, 256}; tmA: 4-D tiled {C, W, H, N} box {64, Wp, TR + R - 1, 1} (128 B swizzle),
 // tmB: 3-D view {cpad, K, R*S taps} of the packed weights [K][R*S*cpad], box {64, BN, tpo}
@@ -218,10 +220,12 @@ struct DwParams {
   const uint16_t* x;      // NHWC bf16
   const float* taps;      // [R*S][C] fp32, BN scale folded in
   const float* bias;      // [C]
-  float* y;               // NHWC fp32
+  float* y;               // NHWC fp32, or bf16 bits when out_bf16
   float lo, hi;
   int* status;            // device status word (watchdog bit)
   FastDiv f_slabs, f_owbs, f_ohbs;   // tile-index decoding (set by the launcher)
+  int out_bf16;           // y (and res) hold bf16, rounded to nearest even
+  const void* res;        // residual of y's type and shape added before the clamp, or null
 };
 // tmX: 4-D tiled map {C, W, H, N} of x with box {32, box_w, box_h, box_n} from dw_tile_box();
 // used by the 3x3 dilation-1 strides-{1,2} kernel, ignored by the general one.

@@ -70,7 +70,9 @@ struct DwTile {
   static constexpr int kSmem = kStages * kStageBytes + 128 + 2 * 8 * kStages;
 };
 
-template <int SW, int TCOLS>
+// EXT: bf16 output and/or a residual (DwParams::out_bf16, res), its own instantiation so the
+// fp32 store path keeps its code
+template <int SW, int TCOLS, bool EXT>
 __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                          const DwParams p) {
   using T = DwTile<SW>;
@@ -209,10 +211,41 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
           float v0, v1, v2, v3;
           unpack_f32x2(a[0], v0, v1);
           unpack_f32x2(a[1], v2, v3);
-          // streaming store: the output is not re-read here, keep L2 for the input windows
-          __stcs(reinterpret_cast<float4*>(ybase + o * yrow),
-                 make_float4(clampf(v0, p.lo, p.hi), clampf(v1, p.lo, p.hi), clampf(v2, p.lo, p.hi),
-                             clampf(v3, p.lo, p.hi)));
+          if (!EXT) {
+            // streaming store: the output is not re-read here, keep L2 for the input windows
+            __stcs(reinterpret_cast<float4*>(ybase + o * yrow),
+                   make_float4(clampf(v0, p.lo, p.hi), clampf(v1, p.lo, p.hi), clampf(v2, p.lo, p.hi),
+                               clampf(v3, p.lo, p.hi)));
+          } else {
+            // the element offset of this thread's 4 channels in y (and in the residual)
+            const size_t e = static_cast<size_t>(ybase - p.y) + static_cast<size_t>(o) * yrow;
+            if (p.res != nullptr) {
+              if (p.out_bf16) {
+                const uint2 r = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
+                v0 += __uint_as_float(r.x << 16);
+                v1 += __uint_as_float(r.x & 0xFFFF0000u);
+                v2 += __uint_as_float(r.y << 16);
+                v3 += __uint_as_float(r.y & 0xFFFF0000u);
+              } else {
+                const float4 r = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
+                v0 += r.x;
+                v1 += r.y;
+                v2 += r.z;
+                v3 += r.w;
+              }
+            }
+            v0 = clampf(v0, p.lo, p.hi);
+            v1 = clampf(v1, p.lo, p.hi);
+            v2 = clampf(v2, p.lo, p.hi);
+            v3 = clampf(v3, p.lo, p.hi);
+            if (p.out_bf16) {
+              const __nv_bfloat162 b0 = __floats2bfloat162_rn(v0, v1), b1 = __floats2bfloat162_rn(v2, v3);
+              __stcs(reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.y) + e),
+                     make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1)));
+            } else {
+              __stcs(reinterpret_cast<float4*>(p.y + e), make_float4(v0, v1, v2, v3));
+            }
+          }
         }
         a[0] = bias[0];
         a[1] = bias[1];
@@ -264,11 +297,34 @@ __global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(xv[e], __ldg(tp + e), acc[e]);
       }
     }
-    float4* dst = reinterpret_cast<float4*>(p.y + ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo + ow) * p.C + c0);
-    dst[0] = make_float4(clampf(acc[0], p.lo, p.hi), clampf(acc[1], p.lo, p.hi),
-                         clampf(acc[2], p.lo, p.hi), clampf(acc[3], p.lo, p.hi));
-    dst[1] = make_float4(clampf(acc[4], p.lo, p.hi), clampf(acc[5], p.lo, p.hi),
-                         clampf(acc[6], p.lo, p.hi), clampf(acc[7], p.lo, p.hi));
+    const size_t e = ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo + ow) * p.C + c0;
+    if (p.res != nullptr) {
+      if (p.out_bf16) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.res) + e));
+        float rf[8];
+        bf16x8_to_f32(r, rf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += rf[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += __ldg(static_cast<const float*>(p.res) + e + i);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = clampf(acc[i], p.lo, p.hi);
+    if (p.out_bf16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.y) + e) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(p.y + e);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
   }
 }
 
@@ -336,17 +392,17 @@ void dw_tile_box(int stride, int Wo, int* box_w, int* box_h, int* box_n) {
 }
 
 namespace {
-template <int SW, int TCOLS>
+template <int SW, int TCOLS, bool EXT>
 cudaError_t launch_dw_tma(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream) {
   using T = DwTile<SW>;
   static std::once_flag once;
   static cudaError_t set_err = cudaSuccess;
   static int occ = 0;
   std::call_once(once, [] {
-    set_err = cudaFuncSetAttribute(dw3x3_tma_kernel<SW, TCOLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    set_err = cudaFuncSetAttribute(dw3x3_tma_kernel<SW, TCOLS, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    T::kSmem);
     if (set_err == cudaSuccess)
-      set_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dw3x3_tma_kernel<SW, TCOLS>, T::kThreads,
+      set_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dw3x3_tma_kernel<SW, TCOLS, EXT>, T::kThreads,
                                                               T::kSmem);
     if (set_err == cudaSuccess && occ < 1) set_err = cudaErrorInvalidConfiguration;
   });
@@ -364,7 +420,7 @@ cudaError_t launch_dw_tma(const DwParams& p, const CUtensorMap* tmX, int num_sms
   long long grid = std::min<long long>(units, static_cast<long long>(num_sms) * occ);
   // a multiple of the channel-slab count keeps every CTA on one slab (taps loaded once)
   if (grid < units && grid >= slabs) grid -= grid % slabs;
-  return launch_pdl(dw3x3_tma_kernel<SW, TCOLS>, dim3(static_cast<unsigned>(grid)), dim3(T::kThreads), T::kSmem, stream, 1,
+  return launch_pdl(dw3x3_tma_kernel<SW, TCOLS, EXT>, dim3(static_cast<unsigned>(grid)), dim3(T::kThreads), T::kSmem, stream, 1,
                     *tmX, q);
 }
 }  // namespace
@@ -375,9 +431,18 @@ cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_
   if (dw_uses_tma(p)) {
     if (!tmX) return cudaErrorInvalidValue;
     const bool narrow = dw_tile_cols(p.Wo) == 8;
+    if (p.out_bf16 || p.res != nullptr) {
+      if (p.sh == 1)
+        return narrow ? launch_dw_tma<1, 8, true>(p, tmX, num_sms, stream)
+                      : launch_dw_tma<1, 16, true>(p, tmX, num_sms, stream);
+      return narrow ? launch_dw_tma<2, 8, true>(p, tmX, num_sms, stream)
+                    : launch_dw_tma<2, 16, true>(p, tmX, num_sms, stream);
+    }
     if (p.sh == 1)
-      return narrow ? launch_dw_tma<1, 8>(p, tmX, num_sms, stream) : launch_dw_tma<1, 16>(p, tmX, num_sms, stream);
-    return narrow ? launch_dw_tma<2, 8>(p, tmX, num_sms, stream) : launch_dw_tma<2, 16>(p, tmX, num_sms, stream);
+      return narrow ? launch_dw_tma<1, 8, false>(p, tmX, num_sms, stream)
+                    : launch_dw_tma<1, 16, false>(p, tmX, num_sms, stream);
+    return narrow ? launch_dw_tma<2, 8, false>(p, tmX, num_sms, stream)
+                  : launch_dw_tma<2, 16, false>(p, tmX, num_sms, stream);
   }
   const dim3 b(256);
   const long long work = static_cast<long long>(p.N) * p.Ho * p.Wo * C8;

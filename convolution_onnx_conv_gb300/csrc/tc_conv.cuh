@@ -93,7 +93,9 @@ struct SegSched {
   }
 };
 
-// EXTM: 0 the plain fp32 epilogue; 1 a residual (fp32 or bf16 y); 2 bf16 y without a residual.
+// EXTM: 0 the plain fp32 epilogue; 1 a residual (fp32 or bf16 y); 2 bf16 y without a residual;
+// 3 a residual with bf16 y and K % 8 == 0 (the 16-byte mapping known at compile time, four
+// prefetched residual vectors instead of eight).
 // Each its own instantiation: a shared epilogue cost the fp32 one 1.3% of the ResNet-50 step, and
 // the residual's prefetched rows (32 registers) made the bf16-only epilogue spill.
 // IQ: integer-exact mode for 8-bit convolutions (TcConvParams::iq_*): the accumulator restarts
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   constexpr bool EXT = EXTM != 0;   // residual and/or bf16 output
-  constexpr bool RES = EXTM == 1;   // a residual may be added
+  constexpr bool RES = EXTM == 1 || EXTM == 3;   // a residual may be added
   static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
   static_assert(!(IQ && (GATHER || PAIR || SK || EXT)), "the integer-exact mode runs whole tiles on single CTAs");
   static_assert(!IQ || BN == 64 || BN == 128, "the integer-exact epilogue holds 32 or 64 int32 sums per thread");
@@ -693,10 +695,10 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           // before the transpose (one memory latency per chunk, not one per row).  bf16 output with
           // K % 8 == 0 (w16) maps threads to (row, 8 channels) instead, so that every load and
           // store moves 16 bytes; its residual bits sit in rv[0..3].
-          const bool w16 = EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0;
+          const bool w16 = EXTM == 3 || (EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0);
           const int sub8 = lane >> 2;   // w16: row within each group of eight
           const int c8 = lane & 3;      // w16: 8-channel column group
-          float4 rv[RES ? 8 : 1];
+          float4 rv[EXTM == 3 ? 4 : (RES ? 8 : 1)];
           if (RES && w16) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -714,9 +716,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), 0.f, 0.f);
               }
             }
-          } else if (RES) {
+          } else if (RES && EXTM != 3) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < (EXTM == 3 ? 0 : 8); ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
               const int r = 4 * i + sub;
               if (p.res == nullptr || (SK && mode == 2) || !col_ok || mt + r >= p.M) continue;
@@ -829,11 +831,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;   // element index
               float4 v = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
                                      fmaf(a[i].w, sc.w, bi.w));
-              if (RES) {   // zero where there is no residual
-                v.x += rv[RES ? i : 0].x;
-                v.y += rv[RES ? i : 0].y;
-                v.z += rv[RES ? i : 0].z;
-                v.w += rv[RES ? i : 0].w;
+              if (RES && EXTM != 3) {   // zero where there is no residual
+                v.x += rv[EXTM == 1 ? i : 0].x;
+                v.y += rv[EXTM == 1 ? i : 0].y;
+                v.z += rv[EXTM == 1 ? i : 0].z;
+                v.w += rv[EXTM == 1 ? i : 0].w;
               }
               v = make_float4(fminf(fmaxf(v.x, p.lo), p.hi), fminf(fmaxf(v.y, p.lo), p.hi),
                               fminf(fmaxf(v.z, p.lo), p.hi), fminf(fmaxf(v.w, p.lo), p.hi));

@@ -24,6 +24,11 @@ cudaError_t CONVF_CAT(launch_tc_conv_bn, CONVF_BN)(const TcConvParams& p, const 
   if (p.res != nullptr || p.out_bf16) {
     // residual and/or bf16 output: the extended-epilogue instantiations
     if (gather) return cudaErrorInvalidValue;
+    if (p.res != nullptr && p.out_bf16 && (p.Kout & 7) == 0 && !p.sk) {
+      // residual with bf16 output on 16-byte rows
+      if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, 3>(p, tmA, tmB, grid, stream);
+      return launch_tc_conv_t<CONVF_BN, false, false, false, 3>(p, tmA, tmB, grid, stream);
+    }
     if (p.res != nullptr) {
       if (p.sk) return launch_tc_conv_t<CONVF_BN, false, false, true, 1>(p, tmA, tmB, grid, stream);
       if (pair) return launch_tc_conv_t<CONVF_BN, false, true, false, 1>(p, tmA, tmB, grid, stream);

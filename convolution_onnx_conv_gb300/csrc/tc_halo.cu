@@ -15,6 +15,8 @@
 // its issuing warp for a few hundred cycles whatever its size, so one weight load brings tpo
 // consecutive taps (a 3-D box {64 channels, BN rows, tpo taps}: each tap lands as its own
 // K-major 128-byte-swizzled BN x 64 operand).
+#include <cuda_bf16.h>
+
 #include "convf_internal.h"
 #include "ptx.cuh"
 
@@ -47,7 +49,8 @@ size_t tc_halo_fixed_smem(int R, int S, int Wp, uint32_t patch_bytes) {
          kHMaxTaps * 4 + 512;
 }
 
-template <int BN>
+// EXT: bf16 output and/or a residual (HaloParams::out_bf16, res) in its own instantiation
+template <int BN, bool EXT>
 __global__ void __launch_bounds__(kHThreads, 1)
     tc_halo_kernel(const HaloParams p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    uint32_t pstride) {
@@ -282,11 +285,42 @@ __global__ void __launch_bounds__(kHThreads, 1)
             const int tr = q * 32 + 4 * i + sub;
             const int off = rm_off[tr];
             if (!col_ok || off < 0 || oh0 + rm_dr[tr] >= p.Ho) continue;
-            *reinterpret_cast<float4*>(ybase + static_cast<size_t>(off) * p.Kout + nc + 4 * c4) =
-                make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
-                            fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
+            if (!EXT) {
+              *reinterpret_cast<float4*>(ybase + static_cast<size_t>(off) * p.Kout + nc + 4 * c4) =
+                  make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a[i].z, sc.z, bi.z), p.lo), p.hi),
+                              fminf(fmaxf(fmaf(a[i].w, sc.w, bi.w), p.lo), p.hi));
+              continue;
+            }
+            // residual (added after the folded BN, before the clamp) and/or bf16 output
+            const size_t e = static_cast<size_t>(ybase - p.y) + static_cast<size_t>(off) * p.Kout + nc + 4 * c4;
+            float4 o = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
+                                   fmaf(a[i].w, sc.w, bi.w));
+            if (p.res != nullptr) {
+              if (p.out_bf16) {
+                const uint2 r = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
+                o.x += __uint_as_float(r.x << 16);
+                o.y += __uint_as_float(r.x & 0xffff0000u);
+                o.z += __uint_as_float(r.y << 16);
+                o.w += __uint_as_float(r.y & 0xffff0000u);
+              } else {
+                const float4 r = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
+                o.x += r.x;
+                o.y += r.y;
+                o.z += r.z;
+                o.w += r.w;
+              }
+            }
+            o = make_float4(fminf(fmaxf(o.x, p.lo), p.hi), fminf(fmaxf(o.y, p.lo), p.hi),
+                            fminf(fmaxf(o.z, p.lo), p.hi), fminf(fmaxf(o.w, p.lo), p.hi));
+            if (p.out_bf16) {
+              const __nv_bfloat162 b0 = __floats2bfloat162_rn(o.x, o.y), b1 = __floats2bfloat162_rn(o.z, o.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.y) + e) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+            } else {
+              *reinterpret_cast<float4*>(p.y + e) = o;
+            }
           }
           __syncwarp();
         }
@@ -309,26 +343,29 @@ teardown:
 }
 
 namespace {
-template <int BN>
+template <int BN, bool EXT>
 cudaError_t launch_bn(const HaloParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                       cudaStream_t stream) {
   const uint32_t ps = patch_stride(p.R, p.S, p.Wp, p.patch_bytes);
   const size_t smem = tc_halo_fixed_smem(p.R, p.S, p.Wp, p.patch_bytes) +
                       static_cast<size_t>(p.b_stages) * p.tpo * HaloCfg<BN>::kBBytes;
   if (smem > 232448 || p.b_stages < 2 || p.b_stages > 8) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_halo_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc_halo_kernel<BN, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(tc_halo_kernel<BN>, dim3(grid), dim3(kHThreads), smem, stream, 1, p, tmA, tmB, ps);
+  return launch_pdl(tc_halo_kernel<BN, EXT>, dim3(grid), dim3(kHThreads), smem, stream, 1, p, tmA, tmB, ps);
 }
 }  // namespace
 
 cudaError_t launch_tc_halo(const HaloParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int bn, int grid,
                            cudaStream_t stream) {
+  const bool ext = p.out_bf16 || p.res != nullptr;
   switch (bn) {
-    case 64: return launch_bn<64>(p, tmA, tmB, grid, stream);
-    case 128: return launch_bn<128>(p, tmA, tmB, grid, stream);
-    case 256: return launch_bn<256>(p, tmA, tmB, grid, stream);
+    case 64: return ext ? launch_bn<64, true>(p, tmA, tmB, grid, stream) : launch_bn<64, false>(p, tmA, tmB, grid, stream);
+    case 128:
+      return ext ? launch_bn<128, true>(p, tmA, tmB, grid, stream) : launch_bn<128, false>(p, tmA, tmB, grid, stream);
+    case 256:
+      return ext ? launch_bn<256, true>(p, tmA, tmB, grid, stream) : launch_bn<256, false>(p, tmA, tmB, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

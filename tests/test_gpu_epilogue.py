@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import convolution_onnx_conv_gb300 as cf
-from convolution_onnx_conv_gb300.workloads import ConvSpec, ACT_RELU, ACT_RELU6
+from convolution_onnx_conv_gb300.workloads import ConvSpec, ACT_NONE, ACT_RELU, ACT_RELU6
 
 from parity import ATOL, RTOL, compare, inputs_for, to_device_nhwc
 
@@ -153,3 +153,49 @@ def test_run_entry_points_match_the_handle():
     assert e.value.status == cf.CONVF_ERR_INVALID_ARG and "overlaps y" in str(e.value)
     plain.close()
     res.close()
+
+
+def E(name, N, C, H, W, K, R, S_, stride=(1, 1), pads=(0, 0, 0, 0), dil=(1, 1), group=1, act=ACT_RELU, bias=False):
+    return ConvSpec(name, N, C, H, W, K, R, S_, stride, pads, dil, group, act, bias, True, "bf16", "normal")
+
+
+EXT_KERNELS = [
+    # (spec, forced variant): the halo tiles (stride-1 3x3: the 56x56 ResNet layers), the TMA
+    # depthwise (3x3, strides 1 and 2, two images per tile) and the direct depthwise (5x5 dilated)
+    (E("halo_w56", 2, 64, 8, 56, 64, 3, 3, pads=(1, 1, 1, 1)), V.CONVF_VARIANT_IMPLICIT_GEMM_HALO),
+    (E("halo_c128_k200", 2, 128, 14, 14, 200, 3, 3, pads=(1, 1, 1, 1), bias=True), V.CONVF_VARIANT_IMPLICIT_GEMM_HALO),
+    (E("dw_s1_c96", 2, 96, 15, 17, 96, 3, 3, pads=(1, 1, 1, 1), group=96, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (E("dw_s2_c64", 2, 64, 17, 16, 64, 3, 3, (2, 2), (1, 1, 1, 1), group=64, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (E("dw_narrow_c96", 5, 96, 7, 7, 96, 3, 3, pads=(1, 1, 1, 1), group=96), V.CONVF_VARIANT_DEPTHWISE),
+    (E("dw_5x5_dil2_c32", 2, 32, 13, 13, 32, 5, 5, (1, 1), (4, 4, 4, 4), (2, 2), group=32, act=ACT_NONE),
+     V.CONVF_VARIANT_DEPTHWISE),
+]
+
+
+@pytest.mark.parametrize("mode", [(True, False), (False, True), (True, True)], ids=["bf16", "res", "bf16_res"])
+@pytest.mark.parametrize("case", EXT_KERNELS, ids=lambda c: c[0].name)
+def test_halo_and_depthwise_extended_epilogue(case, mode):
+    spec, variant = case
+    out_bf16, residual = mode
+    seed = 8300 + EXT_KERNELS.index(case)
+    inp = inputs_for(spec, seed)
+    scale, shift = cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5)
+    conv = cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"], scale, shift,
+                        stride=spec.stride, pads=spec.pads, dilation=spec.dilation, group=spec.group, act=spec.act,
+                        variant=variant, out_bf16=out_bf16, residual=residual)
+    assert conv.variant == variant, conv.describe()
+    r = residual_for(conv, seed + 1, out_bf16) if residual else None
+    ref = oracle_ref(spec, inp, r)
+    x = to_device_nhwc(inp["x"])
+    for in_place in ((False, True) if residual else (False,)):
+        rd = to_device_nhwc(r) if residual else None
+        y = rd if in_place else None        # in place: y starts as the residual
+        y = conv(x, y, r=rd)
+        torch.cuda.synchronize()
+        assert conv.status() == cf.CONVF_OK
+        assert y.dtype == (torch.bfloat16 if out_bf16 else torch.float32)
+        ok, worst, idx = check(y, ref, out_bf16)
+        assert ok, (spec.name, mode, in_place, worst, idx)
+    conv.close()

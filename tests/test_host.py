@@ -284,9 +284,9 @@ def test_kblocks_per_step_is_validated():
 
 
 def test_bf16_output_and_residual_are_validated_and_routed():
-    """out_dtype and residual take 0/1; with either, the dense convs are served by the TMA
-    implicit-GEMM and 1x1 kernels only: the 56x56 3x3 layer moves off the halo tiles and the RGB
-    stem is refused."""
+    """out_dtype and residual take 0/1; with either, the TMA implicit-GEMM, 1x1, halo, depthwise
+    and direct grouped kernels serve the conv and the RGB stem (window / gathered rows) is
+    refused."""
     layers = {s.name: s for s in workloads.resnet50_layers(32)}
 
     def plan(spec, **kw):
@@ -295,8 +295,11 @@ def test_bf16_output_and_residual_are_validated_and_routed():
 
     halo = layers["r50_02_s0b0_3x3@b32"]
     assert plan(halo) == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO
-    assert plan(halo, out_dtype=cf.CONVF_OUT_BF16) == cf.CONVF_VARIANT_IMPLICIT_GEMM
-    assert plan(halo, residual=1) == cf.CONVF_VARIANT_IMPLICIT_GEMM
+    # the halo tiles and depthwise keep their layers with bf16 output and the residual
+    assert plan(halo, out_dtype=cf.CONVF_OUT_BF16) == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO
+    assert plan(halo, residual=1) == cf.CONVF_VARIANT_IMPLICIT_GEMM_HALO
+    dw = next(iter(workloads.depthwise_layers(64)))
+    assert plan(dw, out_dtype=1, residual=1) == cf.CONVF_VARIANT_DEPTHWISE
     assert plan(layers["r50_03_s0b0_1x1b@b32"], residual=1, out_dtype=1) == cf.CONVF_VARIANT_GEMM_1X1
     for kw in ({"out_dtype": 1}, {"residual": 1}):
         with pytest.raises(cf.ConvFusedError) as e:
