@@ -458,10 +458,36 @@ def profile_layers(which):
     cf.load_library(build_if_missing=True)
     kind, idx = which.split(":")
     idx = [int(i) for i in idx.split(",")]
-    table = {"r50": (workloads.resnet50_layers(32), 3, False), "dw": (workloads.depthwise_layers(64), 4, False),
-             "s8": (workloads.int8_layers(64), 5, True)}
-    specs, base, s8 = table[kind]
-    layers = build_layers([specs[i] for i in idx], base, torch, cf, synthetic, s8=s8)
+    if kind == "mb":
+        # fused MobileNetV2 blocks at batch 64
+        blocks = workloads.mobilenetv2_blocks(64)
+        layers = []
+        for i in idx:
+            name, N, cin, h, ch, cout, st, ex, res = blocks[i]
+            inp = synthetic.block_inputs(N, cin, h, ch, cout, ex, synthetic.seed_for(11, i))
+            aff = lambda bn: cf.conv_bn_scale_shift(*[t.numpy() for t in bn], 1e-5)
+            blk = cf.InvertedResidualBlock(N, cin, h, h, ch, cout, st, inp["we"], aff(inp["bn_e"]) if ex else None,
+                                           inp["wd"], aff(inp["bn_d"]), inp["wp"], aff(inp["bn_p"]), residual=res)
+            x = inp["x"].contiguous(memory_format=torch.channels_last).cuda()
+            layers.append({"spec": type("B", (), {"name": name})(), "conv": blk, "x": x, "y": blk.new_output()})
+    elif kind == "q8":
+        # QLinearConv on the ResNet-50 3x3 shapes at batch 64
+        specs = workloads.int8_layers(64)
+        layers = []
+        for i in idx:
+            spec = specs[i]
+            inp = synthetic.qlinear_inputs(spec, synthetic.seed_for(9, i), False, True, False)
+            conv = cf.QLinearConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"],
+                                  x_scale=inp["x_scale"], x_zero_point=inp["x_zp"], w_scale=inp["w_scale"].numpy(),
+                                  w_zero_point=inp["w_zp"].numpy(), y_scale=inp["y_scale"],
+                                  y_zero_point=inp["y_zp"], relu=True, stride=spec.stride, pads=spec.pads)
+            x = inp["x"].contiguous(memory_format=torch.channels_last).cuda()
+            layers.append({"spec": spec, "conv": conv, "x": x, "y": conv.new_output()})
+    else:
+        table = {"r50": (workloads.resnet50_layers(32), 3, False), "dw": (workloads.depthwise_layers(64), 4, False),
+                 "s8": (workloads.int8_layers(64), 5, True)}
+        specs, base, s8 = table[kind]
+        layers = build_layers([specs[i] for i in idx], base, torch, cf, synthetic, s8=s8)
     for _ in range(2):
         for L in layers:
             L["conv"](L["x"], L["y"])
@@ -483,8 +509,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile", default=None,
-                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I' or 's8:I' runs those "
-                         "layers twice (warm-up) and then once more each, printing their kernel descriptions")
+                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I', 's8:I', 'q8:I' (QLinearConv) "
+                         "or 'mb:I' (fused MobileNetV2 block) runs those layers twice (warm-up) and then once "
+                         "more each, printing their kernel descriptions")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
