@@ -35,7 +35,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
             "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact",
-            "conv_fused_create_mbv2_block"]
+            "conv_fused_create_mbv2_block", "conv_fused_debug_fail_alloc", "conv_fused_debug_live_handles"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -140,6 +140,8 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_watchdog_selftest.argtypes = [vp, ctypes.c_longlong, vp]
     lib.conv_fused_run_noalloc.argtypes = [dptr, vp, vp, vp, vp, vp, vp, vp]
     lib.conv_fused_measure_int8_mma_rate.argtypes = [vp, P(ctypes.c_double)]
+    lib.conv_fused_debug_fail_alloc.argtypes = [ctypes.c_int]
+    lib.conv_fused_debug_live_handles.argtypes = []
     for name in EXPORTED:
         if name not in ("conv_fused_destroy", "conv_fused_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -291,6 +293,16 @@ def conv_fused_describe(handle: int) -> str:
 def conv_fused_watchdog_selftest(status_dev, budget_cycles: int, stream=None):
     s = stream.cuda_stream if stream is not None and hasattr(stream, "cuda_stream") else stream
     _check(load_library().conv_fused_watchdog_selftest(_addr(status_dev), int(budget_cycles), s))
+
+
+def conv_fused_debug_fail_alloc(n: int):
+    """Test hook: the n-th allocation the create calls make from now on fails (0 disarms)."""
+    _check(load_library().conv_fused_debug_fail_alloc(int(n)))
+
+
+def conv_fused_debug_live_handles() -> int:
+    """Number of handles created and not yet destroyed."""
+    return int(load_library().conv_fused_debug_live_handles())
 
 
 def conv_fused_measure_int8_mma_rate(stream=None) -> float:

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -38,6 +39,26 @@ constexpr uint32_t kMagic = 0xC0F5ED01u;
 constexpr uint32_t kDeadMagic = 0xDEADC0F5u;
 
 thread_local std::string g_last_error;
+
+// Allocation-failure injection (conv_fused_debug_fail_alloc): the countdown reaching zero makes
+// that allocation fail.  Live handles are counted by a member of the handle (below).
+std::atomic<int> g_fail_countdown{0};
+std::atomic<int> g_live_handles{0};
+
+bool injected_alloc_failure() {
+  int n = g_fail_countdown.load();
+  while (n > 0) {
+    if (g_fail_countdown.compare_exchange_weak(n, n - 1)) return n == 1;
+  }
+  return false;
+}
+
+struct LiveHandleCount {
+  LiveHandleCount() { g_live_handles.fetch_add(1); }
+  LiveHandleCount(const LiveHandleCount&) { g_live_handles.fetch_add(1); }
+  LiveHandleCount& operator=(const LiveHandleCount&) = default;
+  ~LiveHandleCount() { g_live_handles.fetch_sub(1); }
+};
 
 convf_status fail(convf_status st, const char* fmt, ...) {
   char buf[512];
@@ -584,6 +605,7 @@ bool load_encoders() {
 
 // ====================================================================== handle
 struct convf_handle {
+  LiveHandleCount live;   // counts the handles in existence (conv_fused_debug_live_handles)
   uint32_t magic;
   convf_desc desc;
   Shape s;
@@ -904,8 +926,9 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
   if ((st = select_variant(desc, s, &variant)) != CONVF_OK) return st;
 
   // ---------------------------------------------------------------- host-side prep
-  convf_handle* h = new (std::nothrow) convf_handle();
-  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed");
+  const bool host_injected = injected_alloc_failure();
+  convf_handle* h = host_injected ? nullptr : new (std::nothrow) convf_handle();
+  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed%s", host_injected ? " (injected)" : "");
   h->desc = *desc;
   h->out_bf16 = desc->out_dtype == CONVF_OUT_BF16;
   h->has_res = desc->residual != 0;
@@ -1127,11 +1150,12 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
   }
   const size_t o_status = carve(sizeof(int));
   h->dev_bytes = off;
-  ce = cudaMalloc(&h->dev, h->dev_bytes);
+  const bool dev_injected = injected_alloc_failure();
+  ce = dev_injected ? cudaErrorMemoryAllocation : cudaMalloc(&h->dev, h->dev_bytes);
   if (ce != cudaSuccess) {
-    cudaGetLastError();
+    if (!dev_injected) cudaGetLastError();
     delete h;
-    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s", off, cudaGetErrorString(ce));
+    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s%s", off, cudaGetErrorString(ce), dev_injected ? " (injected)" : "");
   }
   char* base = static_cast<char*>(h->dev);
   h->status = reinterpret_cast<int*>(base + o_status);
@@ -1446,8 +1470,9 @@ convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint1
   if (d->Cout % 4) return fail(CONVF_ERR_UNSUPPORTED, "fused block: Cout %% 4 == 0 (16-byte output stores)");
   if ((long long)d->N * d->H * d->W * d->Cin > 0x7FFFFFFFLL || (long long)d->N * d->H * d->W * d->Cout > 0x7FFFFFFFLL)
     return fail(CONVF_ERR_UNSUPPORTED, "tensor sizes exceed the 2^31-element indexing limit");
-  convf_handle* h = new (std::nothrow) convf_handle();
-  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed");
+  const bool host_injected = injected_alloc_failure();
+  convf_handle* h = host_injected ? nullptr : new (std::nothrow) convf_handle();
+  if (!h) return fail(CONVF_ERR_OOM, "host allocation failed%s", host_injected ? " (injected)" : "");
   cudaError_t ce = cudaGetDevice(&h->device);
   if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (ce != cudaSuccess) {
@@ -1519,11 +1544,12 @@ convf_status conv_fused_create_mbv2_block(const convf_block_desc* d, const uint1
       delete h;
       return fail(CONVF_ERR_INVALID_ARG, "an expand or depthwise affine value is not finite");
     }
-  ce = cudaMalloc(&h->dev, h->dev_bytes);
+  const bool dev_injected = injected_alloc_failure();
+  ce = dev_injected ? cudaErrorMemoryAllocation : cudaMalloc(&h->dev, h->dev_bytes);
   if (ce != cudaSuccess) {
-    cudaGetLastError();
+    if (!dev_injected) cudaGetLastError();
     delete h;
-    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s", h->dev_bytes, cudaGetErrorString(ce));
+    return fail(CONVF_ERR_OOM, "cudaMalloc(%zu) failed: %s%s", h->dev_bytes, cudaGetErrorString(ce), dev_injected ? " (injected)" : "");
   }
   ce = cudaMemcpy(h->dev, st.data(), h->dev_bytes, cudaMemcpyHostToDevice);
   char* base = static_cast<char*>(h->dev);
@@ -1884,6 +1910,14 @@ void conv_fused_destroy(convf_handle* h) {
   cudaFree(h->dev);
   delete h;
 }
+
+convf_status conv_fused_debug_fail_alloc(int n) {
+  if (n < 0) return fail(CONVF_ERR_INVALID_ARG, "n=%d is negative", n);
+  g_fail_countdown.store(n);
+  return ok();
+}
+
+int conv_fused_debug_live_handles(void) { return g_live_handles.load(); }
 
 int conv_fused_variant(const convf_handle* h) {
   convf_status st = check_handle(h);

@@ -320,6 +320,20 @@ const char* conv_fused_last_error(void);
 convf_status conv_fused_watchdog_selftest(int32_t* status_dev, long long budget_cycles,
                                           void* stream);
 
+/* Test hook for the allocation-failure path of the create calls (conv_fused_create,
+ * _create_qlinear, _create_preact, _create_mbv2_block).  After conv_fused_debug_fail_alloc(n)
+ * with n >= 1, the n-th allocation that create calls make from then on fails as if memory had
+ * run out; host allocations (the handle) and device allocations (its one cudaMalloc) count
+ * alike, in the order a call makes them: the handle first, before any CUDA call, then the
+ * device block.  The failing call frees what it already holds and returns CONVF_ERR_OOM; its
+ * conv_fused_last_error message ends in "(injected)".  The hook then disarms itself; n = 0
+ * disarms it at once; a negative n is CONVF_ERR_INVALID_ARG.  Process-wide, for tests: calls
+ * on other threads in the meantime draw on the same count.
+ * conv_fused_debug_live_handles returns how many handles exist (created and not yet
+ * destroyed), so a test can check that a failed create left nothing behind. */
+convf_status conv_fused_debug_fail_alloc(int n);
+int conv_fused_debug_live_handles(void);
+
 /* Measurement helper (the int8 path's roofline denominator): times back-to-back
  * mma.sync.m16n8k32 int8 MMAs on register operands over every SM of the current device and
  * returns the rate in TOP/s (2 ops per multiply-add).  Synchronises `stream`. */

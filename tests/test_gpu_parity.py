@@ -8,6 +8,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 import convolution_onnx_conv_gb300 as cf
 from convolution_onnx_conv_gb300 import synthetic, workloads
 from convolution_onnx_conv_gb300.workloads import ConvSpec, ACT_NONE, ACT_RELU, ACT_RELU6, ACT_CLIP
@@ -495,6 +497,39 @@ def test_back_to_back_runs_reuse_buffers():
 def test_int8_mma_rate_measurement():
     tops = cf.conv_fused_measure_int8_mma_rate()
     assert 1.0 < tops < 20000.0
+
+
+def test_injected_device_allocation_failure_leaves_the_library_usable():
+    """The allocation-failure hook on the device allocation (a create call's second allocation):
+    create returns CONVF_ERR_OOM, frees its handle and takes no device memory; the next creates
+    and runs are unaffected and still match the oracle."""
+    spec = S("oom_then_ok", 2, 64, 15, 15, 64, 3, 3, pads=(1, 1, 1, 1))
+    inp = inputs_for(spec, 4242)
+    live = cf.conv_fused_debug_live_handles()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    cf.conv_fused_debug_fail_alloc(2)
+    with pytest.raises(cf.ConvFusedError) as e:
+        make_conv(spec, inp)
+    assert e.value.status == cf.CONVF_ERR_OOM and "cudaMalloc" in str(e.value) and "(injected)" in str(e.value)
+    assert cf.conv_fused_debug_live_handles() == live
+    assert torch.cuda.mem_get_info()[0] >= free0 - (2 << 20)
+    # a countdown of 3: the first create (handle, device block) succeeds, the second fails at
+    # its handle allocation; the first handle is unaffected
+    cf.conv_fused_debug_fail_alloc(3)
+    conv = make_conv(spec, inp)
+    with pytest.raises(cf.ConvFusedError) as e:
+        make_conv(spec, inp)
+    assert e.value.status == cf.CONVF_ERR_OOM and "host allocation failed (injected)" in str(e.value)
+    assert cf.conv_fused_debug_live_handles() == live + 1
+    y = conv(to_device_nhwc(inp["x"]))
+    torch.cuda.synchronize()
+    assert conv.status() == cf.CONVF_OK
+    conv.close()
+    assert cf.conv_fused_debug_live_handles() == live
+    ok, worst, idx = oracle.tolerance_ok(y.cpu().contiguous().numpy(), oracle_full(spec, inp))
+    assert ok, (worst, idx)
+    _assert(check_full(spec, 4243), spec)
 
 
 def test_watchdog_gives_up_and_reports():

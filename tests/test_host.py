@@ -437,3 +437,43 @@ def test_grouped_selection(C, K, group, R, variant, tile, ktot):
         Kg, Cg = K // group, C // group
         assert bn % Kg == 0 or Kg % bn == 0
         assert all(((j * bn) // Kg) * Cg % 8 == 0 for j in range(-(-K // bn)))
+
+
+def test_injected_host_allocation_failure_cleans_up_before_any_cuda_call():
+    """The allocation-failure hook: the handle allocation is a create call's first allocation and
+    comes before any CUDA call, so its failure is testable without a GPU.  The call returns
+    CONVF_ERR_OOM, says the failure was injected, leaves no handle behind, and the hook disarms."""
+    live = cf.conv_fused_debug_live_handles()
+    w = np.zeros((32, 16, 3, 3), np.uint16)
+    cf.conv_fused_debug_fail_alloc(1)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create(desc(), w)
+    assert e.value.status == cf.CONVF_ERR_OOM and str(e.value).endswith("(injected)")
+    assert cf.conv_fused_debug_live_handles() == live
+    # the same for the other create calls: pre-activation and the fused block
+    cf.conv_fused_debug_fail_alloc(1)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create_preact(desc(), w, pre_scale=np.ones(16, np.float32), pre_shift=np.zeros(16, np.float32))
+    assert e.value.status == cf.CONVF_ERR_OOM and "(injected)" in str(e.value)
+    bd = cf.BlockDesc()
+    bd.N, bd.H, bd.W, bd.Cin, bd.Ch, bd.Cout, bd.stride, bd.expand, bd.residual = 1, 8, 8, 16, 96, 16, 1, 1, 1
+    ones = np.ones(96, np.float32)
+    cf.conv_fused_debug_fail_alloc(1)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_create_mbv2_block(bd, np.zeros((96, 16), np.uint16), ones, ones, np.zeros((96, 9), np.uint16),
+                                        ones, ones, np.zeros((16, 96), np.uint16), ones[:16], ones[:16])
+    assert e.value.status == cf.CONVF_ERR_OOM and "(injected)" in str(e.value)
+    assert cf.conv_fused_debug_live_handles() == live
+    # disarmed: the next failure (if any: no GPU here) is not an injected one
+    try:
+        h = cf.conv_fused_create(desc(), w)
+    except cf.ConvFusedError as err:
+        assert "(injected)" not in str(err)
+    else:
+        cf.conv_fused_destroy(h)
+    # a countdown past the first allocation does not fire on it; 0 disarms; negatives are refused
+    cf.conv_fused_debug_fail_alloc(5)
+    cf.conv_fused_debug_fail_alloc(0)
+    with pytest.raises(cf.ConvFusedError) as e:
+        cf.conv_fused_debug_fail_alloc(-1)
+    assert e.value.status == cf.CONVF_ERR_INVALID_ARG
