@@ -1,13 +1,16 @@
 // Depthwise convolution (group == C == K) on CUDA cores: memory-bound (about 2-3 flop per
 // byte), so no tensor cores.  NHWC bf16 in, fp32 taps with the BN scale folded in, fp32 out.
 //
-// 3x3, dilation 1, strides {1, 2}: a persistent kernel over tiles of 7 output rows x 16 output
-// columns x 32 channels.  One thread per CTA streams each tile's input window (with its halo)
-// into a ring of shared-memory stages with a single 4-D TMA load, so the loads of the next
+// 3x3, dilation 1, strides {1, 2}: persistent kernels over tiles of 7 output rows x 16 or 32
+// output columns x 32 channels.  One thread per CTA streams each tile's input window (with its
+// halo) into a ring of shared-memory stages with a single 4-D TMA load, so the loads of the next
 // tiles are in flight while the current one is computed and no register holds a byte in flight;
-// padding is the TMA's zero fill.  Each thread owns 4 channels of one output column and walks
-// the window's input rows once, scattering every converted row into the (up to three) output
-// rows it feeds, then stores each output row as one 16-byte vector as soon as it is complete.
+// padding is the TMA's zero fill.  Each thread owns 4 channels of one output column (stride 2,
+// and stride-1 images 16k but not 32k columns wide) or of two neighbouring output columns
+// (stride 1 otherwise), walks the window's input rows once, scattering every converted row into
+// the (up to three) output rows it feeds, then stores each output row as one 16-byte vector per
+// column as soon as it is complete.  The taps of a CTA's first channel slab load before the wait
+// for the previous kernel.
 #include <cuda_bf16.h>
 
 #include "convf_internal.h"
@@ -50,9 +53,73 @@ __device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c) {
 // a 32-bit word holding two bf16 values (channel e in the low half) -> fp32 pair (e, e+1)
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack_f32x2(w << 16, w & 0xFFFF0000u); }
 
-// Column lanes per image in a tile: 16, or 8 when the output is at most 8 columns wide, in
-// which case one tile holds two images (the 16 lanes stay busy on 7-wide layers).
+// Column lanes per image in a stride-2 tile: 16, or 8 when the output is at most 8 columns
+// wide, in which case one tile holds two images (the 16 lanes stay busy on 7-wide layers).
 __host__ __device__ __forceinline__ int dw_tile_cols(int Wo) { return Wo <= 8 ? 8 : 16; }
+// Stride-1 tiles of the two-column kernel have 32 column lanes: 32 columns of one image, or 16
+// of two, or 8 of four.
+__host__ __device__ __forceinline__ int dw_pair_cols(int Wo) { return Wo <= 8 ? 8 : Wo <= 16 ? 16 : 32; }
+// Stride 1 runs on the two-column kernel unless its 32-column blocks leave more columns idle than
+// the one-column kernel's 16-column blocks (e.g. 112 = 7 x 16 columns: measured 7 us faster per
+// MobileNetV2 layer on 16-column tiles; 56-wide layers are faster on 32-column pairs).
+__host__ __device__ __forceinline__ bool dw_use_pair(int Wo) {
+  return Wo <= 16 || (Wo + 31) / 32 * 32 <= (Wo + 15) / 16 * 16;
+}
+
+// The nine taps and the bias of channels c..c+3 as fp32 pairs (zero past the last channel).
+__device__ __forceinline__ void dw_load_taps(const DwParams& p, int c, f32x2 (&tap)[9][2], f32x2 (&bias)[2]) {
+  const bool ok = c < p.C;
+#pragma unroll
+  for (int j = 0; j < 9; ++j) {
+    const float4 v = ok ? __ldg(reinterpret_cast<const float4*>(p.taps + j * p.C + c)) : make_float4(0, 0, 0, 0);
+    tap[j][0] = pack_f32x2(v.x, v.y);
+    tap[j][1] = pack_f32x2(v.z, v.w);
+  }
+  const float4 b = ok ? __ldg(reinterpret_cast<const float4*>(p.bias + c)) : make_float4(0, 0, 0, 0);
+  bias[0] = pack_f32x2(b.x, b.y);
+  bias[1] = pack_f32x2(b.z, b.w);
+}
+
+// Epilogue of four channels of one output pixel at element offset e of y: clamp and a streaming
+// 16-byte fp32 store, or (EXT) the residual added first and fp32 or bf16 (nearest even) stores.
+template <bool EXT>
+__device__ __forceinline__ void dw_store4(const DwParams& p, size_t e, f32x2 a0, f32x2 a1) {
+  float v0, v1, v2, v3;
+  unpack_f32x2(a0, v0, v1);
+  unpack_f32x2(a1, v2, v3);
+  if (!EXT) {
+    // streaming store: the output is not re-read here, keep L2 for the input windows
+    __stcs(reinterpret_cast<float4*>(p.y + e), make_float4(clampf(v0, p.lo, p.hi), clampf(v1, p.lo, p.hi),
+                                                           clampf(v2, p.lo, p.hi), clampf(v3, p.lo, p.hi)));
+    return;
+  }
+  if (p.res != nullptr) {
+    if (p.out_bf16) {
+      const uint2 r = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
+      v0 += __uint_as_float(r.x << 16);
+      v1 += __uint_as_float(r.x & 0xFFFF0000u);
+      v2 += __uint_as_float(r.y << 16);
+      v3 += __uint_as_float(r.y & 0xFFFF0000u);
+    } else {
+      const float4 r = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
+      v0 += r.x;
+      v1 += r.y;
+      v2 += r.z;
+      v3 += r.w;
+    }
+  }
+  v0 = clampf(v0, p.lo, p.hi);
+  v1 = clampf(v1, p.lo, p.hi);
+  v2 = clampf(v2, p.lo, p.hi);
+  v3 = clampf(v3, p.lo, p.hi);
+  if (p.out_bf16) {
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(v0, v1), b1 = __floats2bfloat162_rn(v2, v3);
+    __stcs(reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.y) + e),
+           make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1)));
+  } else {
+    __stcs(reinterpret_cast<float4*>(p.y + e), make_float4(v0, v1, v2, v3));
+  }
+}
 
 template <int SW>
 struct DwTile {
@@ -104,6 +171,11 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
   }
   __syncthreads();
   pdl_launch_dependents();
+  // the taps and bias of this CTA's first channel slab (the slab index varies fastest in the
+  // tile order) are constants of the handle, so they load before the wait for the previous kernel
+  f32x2 tap[9][2], bias[2];    // channel pairs (c, c+1), (c+2, c+3)
+  int cur_slab = static_cast<int>(blockIdx.x - fast_div(blockIdx.x, p.f_slabs) * p.f_slabs.d);
+  dw_load_taps(p, cur_slab * T::kCS + cq * 4, tap, bias);
   pdl_wait_prior();
 
   const int slabs = p.f_slabs.d;
@@ -140,8 +212,6 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
       if (static_cast<int>(blockIdx.x) + j * G < units) issue(j, blockIdx.x + j * G);
   }
 
-  f32x2 tap[9][2], bias[2];    // channel pairs (c, c+1), (c+2, c+3)
-  int cur_slab = -1;
   int k = 0;
   for (int u = blockIdx.x; u < units; u += G, ++k) {
     if (*abort_v) break;
@@ -156,15 +226,7 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
     const bool c_ok = c < p.C;
     if (slab != cur_slab) {
       cur_slab = slab;
-#pragma unroll
-      for (int j = 0; j < 9; ++j) {
-        const float4 v = c_ok ? __ldg(reinterpret_cast<const float4*>(p.taps + j * p.C + c)) : make_float4(0, 0, 0, 0);
-        tap[j][0] = pack_f32x2(v.x, v.y);
-        tap[j][1] = pack_f32x2(v.z, v.w);
-      }
-      const float4 b = c_ok ? __ldg(reinterpret_cast<const float4*>(p.bias + c)) : make_float4(0, 0, 0, 0);
-      bias[0] = pack_f32x2(b.x, b.y);
-      bias[1] = pack_f32x2(b.z, b.w);
+      dw_load_taps(p, c, tap, bias);
     }
     const int ow = owb * tcols + col;
     const bool col_ok = c_ok && ow < p.Wo && n < p.N;
@@ -207,48 +269,170 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
       if (i >= 2 && (i - 2) % SW == 0) {
         const int o = (i - 2) / SW;
         f32x2 (&a)[2] = acc[o % T::kSlots];
-        if (col_ok && oh0 + o < p.Ho) {
-          float v0, v1, v2, v3;
-          unpack_f32x2(a[0], v0, v1);
-          unpack_f32x2(a[1], v2, v3);
-          if (!EXT) {
-            // streaming store: the output is not re-read here, keep L2 for the input windows
-            __stcs(reinterpret_cast<float4*>(ybase + o * yrow),
-                   make_float4(clampf(v0, p.lo, p.hi), clampf(v1, p.lo, p.hi), clampf(v2, p.lo, p.hi),
-                               clampf(v3, p.lo, p.hi)));
-          } else {
-            // the element offset of this thread's 4 channels in y (and in the residual)
-            const size_t e = static_cast<size_t>(ybase - p.y) + static_cast<size_t>(o) * yrow;
-            if (p.res != nullptr) {
-              if (p.out_bf16) {
-                const uint2 r = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
-                v0 += __uint_as_float(r.x << 16);
-                v1 += __uint_as_float(r.x & 0xFFFF0000u);
-                v2 += __uint_as_float(r.y << 16);
-                v3 += __uint_as_float(r.y & 0xFFFF0000u);
-              } else {
-                const float4 r = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.res) + e));
-                v0 += r.x;
-                v1 += r.y;
-                v2 += r.z;
-                v3 += r.w;
-              }
-            }
-            v0 = clampf(v0, p.lo, p.hi);
-            v1 = clampf(v1, p.lo, p.hi);
-            v2 = clampf(v2, p.lo, p.hi);
-            v3 = clampf(v3, p.lo, p.hi);
-            if (p.out_bf16) {
-              const __nv_bfloat162 b0 = __floats2bfloat162_rn(v0, v1), b1 = __floats2bfloat162_rn(v2, v3);
-              __stcs(reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.y) + e),
-                     make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1)));
-            } else {
-              __stcs(reinterpret_cast<float4*>(p.y + e), make_float4(v0, v1, v2, v3));
-            }
-          }
-        }
+        if (col_ok && oh0 + o < p.Ho)
+          dw_store4<EXT>(p, static_cast<size_t>(ybase - p.y) + static_cast<size_t>(o) * yrow, a[0], a[1]);
         a[0] = bias[0];
         a[1] = bias[1];
+      }
+    }
+    // this warp is done with the stage
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(&empty[stage]);
+  }
+  // on a timeout, let the loads still in flight land (bounded) before the CTA's smem goes away
+  if (tid == 0 && *abort_v) {
+    for (int j = waited; j < issued; ++j) {
+      int quiet = 0;
+      mbar_wait(&full[j % T::kStages], (j / T::kStages) & 1, &quiet, nullptr, 20000000LL);
+    }
+  }
+}
+
+// Stride 1: tiles of 7 output rows x 32 output columns (one image, or 16 columns of two, or 8
+// of four) x 32 channels, 128 threads; each thread owns two neighbouring output columns x 4
+// channels, so one input row's four pixels (loaded and converted once) feed both columns' three
+// taps: a third fewer shared-memory loads and conversions per output than one column per thread.
+template <int TCOLS>
+struct DwPairTile {
+  static constexpr int kTH = 7;
+  static constexpr int kLanes = 32;
+  static constexpr int kCS = 32;
+  static constexpr int kThreads = kLanes / 2 * kCS / 4;   // 128
+  static constexpr int kInH = kTH + 2;
+  static constexpr int kNb = kLanes / TCOLS;             // images per tile
+  static constexpr int kInW = TCOLS + 2;
+  static constexpr int kBytes = kNb * kInH * kInW * kCS * 2;
+  static constexpr int kStageBytes = (kBytes + 127) / 128 * 128;
+  static constexpr int kStages = 2;
+  static constexpr int kSlots = 3;
+  static constexpr int kSmem = kStages * kStageBytes + 128 + 2 * 8 * kStages;
+};
+
+template <int TCOLS, bool EXT>
+__global__ void __launch_bounds__(128) dw3x3_pair_kernel(const __grid_constant__ CUtensorMap tmX, const DwParams p) {
+  using T = DwPairTile<TCOLS>;
+  extern __shared__ uint8_t dw_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dw_smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kStages * T::kStageBytes);
+  uint64_t* empty = full + T::kStages;
+  __shared__ int abort_flag;
+  volatile int* abort_v = &abort_flag;
+
+  const int tid = threadIdx.x;
+  const int cq = tid & 7;                  // 4-channel group within the tile's 32 channels
+  const int lane = (tid >> 3) * 2;         // first of the thread's two column lanes
+  const int img = lane / TCOLS;            // its image within the tile
+  const int col = lane - img * TCOLS;      // and its first output column within the column block
+  if (tid == 0) {
+#pragma unroll
+    for (int st = 0; st < T::kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], T::kThreads / 32);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    abort_flag = 0;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  f32x2 tap[9][2], bias[2];
+  int cur_slab = static_cast<int>(blockIdx.x - fast_div(blockIdx.x, p.f_slabs) * p.f_slabs.d);
+  dw_load_taps(p, cur_slab * T::kCS + cq * 4, tap, bias);
+  pdl_wait_prior();
+
+  const int units = (p.N + T::kNb - 1) / T::kNb * p.f_ohbs.d * p.f_owbs.d * p.f_slabs.d;
+  const int G = gridDim.x;
+  int issued = 0, waited = 0;
+  auto decode = [&](uint32_t u, int& slab, int& owb, int& ohb, int& ng) {
+    const uint32_t t = fast_div(u, p.f_slabs);
+    slab = static_cast<int>(u - t * p.f_slabs.d);
+    const uint32_t t2 = fast_div(t, p.f_owbs);
+    owb = static_cast<int>(t - t2 * p.f_owbs.d);
+    ng = static_cast<int>(fast_div(t2, p.f_ohbs));
+    ohb = static_cast<int>(t2 - ng * p.f_ohbs.d);
+  };
+  auto issue = [&](int j, int u) {
+    const int stage = j % T::kStages;
+    if (j >= T::kStages && !mbar_wait(&empty[stage], ((j / T::kStages) - 1) & 1, abort_v, p.status)) return;
+    int slab, owb, ohb, ng;
+    decode(u, slab, owb, ohb, ng);
+    mbar_arrive_expect_tx(&full[stage], T::kBytes);
+    tma_load_4d(smem + stage * T::kStageBytes, &tmX, &full[stage], slab * T::kCS, owb * TCOLS - p.pl,
+                ohb * T::kTH - p.pt, ng * T::kNb);
+    ++issued;
+  };
+  if (tid == 0 && static_cast<int>(blockIdx.x) < units) issue(0, blockIdx.x);
+
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += G, ++k) {
+    if (*abort_v) break;
+    const int stage = k % T::kStages;
+    if (tid == 0 && u + G < units) issue(k + 1, u + G);
+    if (!mbar_wait(&full[stage], (k / T::kStages) & 1, abort_v, p.status)) break;
+    waited = k + 1;
+    int slab, owb, ohb, n;
+    decode(u, slab, owb, ohb, n);
+    n = n * T::kNb + img;
+    const int c = slab * T::kCS + cq * 4;
+    if (slab != cur_slab) {
+      cur_slab = slab;
+      dw_load_taps(p, c, tap, bias);
+    }
+    const int ow = owb * TCOLS + col;
+    const bool ok0 = c < p.C && n < p.N && ow < p.Wo;
+    const bool ok1 = ok0 && ow + 1 < p.Wo;
+    const int oh0 = ohb * T::kTH;
+    const size_t ebase = ((static_cast<size_t>(n) * p.Ho + oh0) * p.Wo + ow) * p.C + c;
+    const size_t yrow = static_cast<size_t>(p.Wo) * p.C;
+    // this thread's 4 channels of window column col of its image, as 8-byte words; the window
+    // is [image][row][column][32 channels], one pixel = 8 words
+    const uint2* win = reinterpret_cast<const uint2*>(smem + stage * T::kStageBytes) +
+                       (img * T::kInH * T::kInW + col) * 8 + cq;
+
+    f32x2 acc[T::kSlots][2][2];   // [output row slot][column][channel pair]
+#pragma unroll
+    for (int q = 0; q < T::kSlots; ++q)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[q][j][0] = bias[0];
+        acc[q][j][1] = bias[1];
+      }
+#pragma unroll
+    for (int i = 0; i < T::kInH; ++i) {
+      f32x2 xv[4][2];
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) {
+        const uint2 v = win[(i * T::kInW + s2) * 8];
+        xv[s2][0] = bf16x2_to_f32x2(v.x);
+        xv[s2][1] = bf16x2_to_f32x2(v.y);
+      }
+      // input row i feeds output row o = i - r through filter row r
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int o = i - r;
+        if (o < 0 || o >= T::kTH) continue;
+#pragma unroll
+        for (int s2 = 0; s2 < 3; ++s2)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            acc[o % T::kSlots][0][e] = fma_f32x2(xv[s2][e], tap[r * 3 + s2][e], acc[o % T::kSlots][0][e]);
+            acc[o % T::kSlots][1][e] = fma_f32x2(xv[s2 + 1][e], tap[r * 3 + s2][e], acc[o % T::kSlots][1][e]);
+          }
+      }
+      // output row o = i - 2 is complete
+      if (i >= 2) {
+        const int o = i - 2;
+        f32x2 (&a)[2][2] = acc[o % T::kSlots];
+        if (oh0 + o < p.Ho) {
+          const size_t e0 = ebase + static_cast<size_t>(o) * yrow;
+          if (ok0) dw_store4<EXT>(p, e0, a[0][0], a[0][1]);
+          if (ok1) dw_store4<EXT>(p, e0 + p.C, a[1][0], a[1][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          a[j][0] = bias[0];
+          a[j][1] = bias[1];
+        }
       }
     }
     // this warp is done with the stage
@@ -385,10 +569,17 @@ bool dw_uses_tma(const DwParams& p) {
 }
 
 void dw_tile_box(int stride, int Wo, int* box_w, int* box_h, int* box_n) {
+  if (stride == 1 && dw_use_pair(Wo)) {
+    const int cols = dw_pair_cols(Wo);
+    *box_w = cols + 2;
+    *box_h = DwPairTile<32>::kInH;
+    *box_n = DwPairTile<32>::kLanes / cols;
+    return;
+  }
   const int cols = dw_tile_cols(Wo);
   *box_w = stride == 1 ? DwTile<1>::in_w(cols) : DwTile<2>::in_w(cols);
   *box_h = stride == 1 ? DwTile<1>::kInH : DwTile<2>::kInH;
-  *box_n = DwTile<1>::kLanes / cols;
+  *box_n = DwTile<2>::kLanes / cols;
 }
 
 namespace {
@@ -423,6 +614,34 @@ cudaError_t launch_dw_tma(const DwParams& p, const CUtensorMap* tmX, int num_sms
   return launch_pdl(dw3x3_tma_kernel<SW, TCOLS, EXT>, dim3(static_cast<unsigned>(grid)), dim3(T::kThreads), T::kSmem, stream, 1,
                     *tmX, q);
 }
+
+template <int TCOLS, bool EXT>
+cudaError_t launch_dw_pair(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream) {
+  using T = DwPairTile<TCOLS>;
+  static std::once_flag once;
+  static cudaError_t set_err = cudaSuccess;
+  static int occ = 0;
+  std::call_once(once, [] {
+    set_err = cudaFuncSetAttribute(dw3x3_pair_kernel<TCOLS, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
+    if (set_err == cudaSuccess)
+      set_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dw3x3_pair_kernel<TCOLS, EXT>, T::kThreads, T::kSmem);
+    if (set_err == cudaSuccess && occ < 1) set_err = cudaErrorInvalidConfiguration;
+  });
+  if (set_err != cudaSuccess) return set_err;
+  const long long slabs = (p.C + T::kCS - 1) / T::kCS;
+  const long long units = static_cast<long long>((p.N + T::kNb - 1) / T::kNb) * ((p.Ho + T::kTH - 1) / T::kTH) *
+                          ((p.Wo + TCOLS - 1) / TCOLS) * slabs;
+  if (units >= (1LL << 31)) return cudaErrorInvalidValue;
+  DwParams q = p;
+  q.f_slabs = make_fastdiv(static_cast<uint32_t>(slabs));
+  q.f_owbs = make_fastdiv(static_cast<uint32_t>((p.Wo + TCOLS - 1) / TCOLS));
+  q.f_ohbs = make_fastdiv(static_cast<uint32_t>((p.Ho + T::kTH - 1) / T::kTH));
+  long long grid = std::min<long long>(units, static_cast<long long>(num_sms) * occ);
+  // a multiple of the channel-slab count keeps every CTA on one slab (taps loaded once)
+  if (grid < units && grid >= slabs) grid -= grid % slabs;
+  return launch_pdl(dw3x3_pair_kernel<TCOLS, EXT>, dim3(static_cast<unsigned>(grid)), dim3(T::kThreads), T::kSmem,
+                    stream, 1, *tmX, q);
+}
 }  // namespace
 
 cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_sms, cudaStream_t stream) {
@@ -430,17 +649,26 @@ cudaError_t launch_depthwise(const DwParams& p, const CUtensorMap* tmX, int num_
   if (static_cast<long long>(p.N) * p.Ho * p.Wo * C8 == 0) return cudaSuccess;
   if (dw_uses_tma(p)) {
     if (!tmX) return cudaErrorInvalidValue;
+    const bool ext = p.out_bf16 || p.res != nullptr;
+    if (p.sh == 1 && dw_use_pair(p.Wo)) {
+      const int cols = dw_pair_cols(p.Wo);
+      if (ext)
+        return cols == 8 ? launch_dw_pair<8, true>(p, tmX, num_sms, stream)
+               : cols == 16 ? launch_dw_pair<16, true>(p, tmX, num_sms, stream)
+                            : launch_dw_pair<32, true>(p, tmX, num_sms, stream);
+      return cols == 8 ? launch_dw_pair<8, false>(p, tmX, num_sms, stream)
+             : cols == 16 ? launch_dw_pair<16, false>(p, tmX, num_sms, stream)
+                          : launch_dw_pair<32, false>(p, tmX, num_sms, stream);
+    }
     const bool narrow = dw_tile_cols(p.Wo) == 8;
-    if (p.out_bf16 || p.res != nullptr) {
-      if (p.sh == 1)
-        return narrow ? launch_dw_tma<1, 8, true>(p, tmX, num_sms, stream)
-                      : launch_dw_tma<1, 16, true>(p, tmX, num_sms, stream);
+    if (p.sh == 1) {
+      // wide images whose width is a multiple of 16 but not of 32: 16-column tiles
+      if (ext) return launch_dw_tma<1, 16, true>(p, tmX, num_sms, stream);
+      return launch_dw_tma<1, 16, false>(p, tmX, num_sms, stream);
+    }
+    if (ext)
       return narrow ? launch_dw_tma<2, 8, true>(p, tmX, num_sms, stream)
                     : launch_dw_tma<2, 16, true>(p, tmX, num_sms, stream);
-    }
-    if (p.sh == 1)
-      return narrow ? launch_dw_tma<1, 8, false>(p, tmX, num_sms, stream)
-                    : launch_dw_tma<1, 16, false>(p, tmX, num_sms, stream);
     return narrow ? launch_dw_tma<2, 8, false>(p, tmX, num_sms, stream)
                   : launch_dw_tma<2, 16, false>(p, tmX, num_sms, stream);
   }

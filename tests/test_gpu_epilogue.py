@@ -161,7 +161,7 @@ def E(name, N, C, H, W, K, R, S_, stride=(1, 1), pads=(0, 0, 0, 0), dil=(1, 1), 
 
 EXT_KERNELS = [
     # (spec, forced variant): the halo tiles (stride-1 3x3: the 56x56 ResNet layers), the TMA
-    # depthwise (3x3, strides 1 and 2, two images per tile) and the direct depthwise (5x5 dilated)
+    # depthwise (3x3, strides 1 and 2, several images per tile) and the direct depthwise (5x5 dilated)
     (E("halo_w56", 2, 64, 8, 56, 64, 3, 3, pads=(1, 1, 1, 1)), V.CONVF_VARIANT_IMPLICIT_GEMM_HALO),
     (E("halo_c128_k200", 2, 128, 14, 14, 200, 3, 3, pads=(1, 1, 1, 1), bias=True), V.CONVF_VARIANT_IMPLICIT_GEMM_HALO),
     (E("dw_s1_c96", 2, 96, 15, 17, 96, 3, 3, pads=(1, 1, 1, 1), group=96, act=ACT_RELU6),
@@ -169,6 +169,10 @@ EXT_KERNELS = [
     (E("dw_s2_c64", 2, 64, 17, 16, 64, 3, 3, (2, 2), (1, 1, 1, 1), group=64, act=ACT_RELU6),
      V.CONVF_VARIANT_DEPTHWISE),
     (E("dw_narrow_c96", 5, 96, 7, 7, 96, 3, 3, pads=(1, 1, 1, 1), group=96), V.CONVF_VARIANT_DEPTHWISE),
+    # stride 1 on 16-column tiles (a 48-wide image) and on 32-column pairs with an odd width
+    (E("dw_s1_w48_c64", 2, 64, 9, 48, 64, 3, 3, pads=(1, 1, 1, 1), group=64, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (E("dw_s1_w27_c40", 2, 40, 11, 27, 40, 3, 3, pads=(1, 1, 1, 1), group=40), V.CONVF_VARIANT_DEPTHWISE),
     (E("dw_5x5_dil2_c32", 2, 32, 13, 13, 32, 5, 5, (1, 1), (4, 4, 4, 4), (2, 2), group=32, act=ACT_NONE),
      V.CONVF_VARIANT_DEPTHWISE),
 ]

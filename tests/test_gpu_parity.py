@@ -94,6 +94,14 @@ SMALL = [
     # outputs at most 8 columns wide: two images per tile, the last image group half past N
     (S("dw_s1_narrow_odd_n", 5, 96, 7, 7, 96, 3, 3, pads=(1, 1, 1, 1), group=96, act=ACT_RELU6),
      V.CONVF_VARIANT_DEPTHWISE),
+    # stride-1 tiles of 32 column lanes: two 16-column images with an odd image count, an odd
+    # width (the second column of the last pair falls outside), two column blocks with a
+    # one-column tail and a ragged channel slab, tall images with a ragged last row block
+    (S("dw_s1_w16_three_images", 3, 48, 16, 16, 48, 3, 3, pads=(1, 1, 1, 1), group=48, act=ACT_RELU6),
+     V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s1_w9_odd", 2, 32, 9, 9, 32, 3, 3, pads=(1, 1, 1, 1), group=32, bias=True), V.CONVF_VARIANT_DEPTHWISE),
+    (S("dw_s1_w61_c40", 1, 40, 30, 61, 40, 3, 3, pads=(1, 1, 1, 1), group=40, act=ACT_NONE),
+     V.CONVF_VARIANT_DEPTHWISE),
     (S("dw_s2_narrow_odd_n", 3, 64, 13, 15, 64, 3, 3, (2, 2), (1, 1, 1, 1), group=64, bias=True),
      V.CONVF_VARIANT_DEPTHWISE),
 ]
