@@ -184,7 +184,10 @@ def build_layers(specs, seed_base, torch, cf, synthetic, s8=False):
 def build_ext_layers(specs, layers, torch, cf):
     """The ResNet-50 step with bf16 outputs (a bf16 network's activations) and the bottleneck
     shortcut added in each block's last 1x1 conv (a bf16 residual of y's shape): the extended
-    epilogue.  A layer it cannot serve (the 3-channel stem) keeps its fp32 handle."""
+    epilogue.  The residual is the block's shortcut tensor, as in the network's dataflow: the
+    block input (the input buffer of the block's first 1x1 conv), or in a stage's first block the
+    projection conv's output.  A layer the extended epilogue cannot serve (the 3-channel stem)
+    keeps its fp32 handle."""
     out = []
     for i, (spec, L) in enumerate(zip(specs, layers)):
         inp = L["inp"]
@@ -198,13 +201,21 @@ def build_ext_layers(specs, layers, torch, cf):
         except cf.ConvFusedError:
             out.append(L)
             continue
-        y = conv.new_output()
-        r = None
-        if res:
-            g = torch.Generator().manual_seed(9000 + i)
-            r = torch.randn(tuple(y.shape), generator=g).to(torch.bfloat16).contiguous(
+        out.append({"spec": spec, "conv": conv, "x": L["x"], "y": conv.new_output(), "r": None})
+    by_name = {E["spec"].name.split("_", 2)[2].split("@")[0]: E for E in out}   # "s0b0_1x1a" -> layer
+    for E in out:
+        name = E["spec"].name.split("_", 2)[2].split("@")[0]
+        if not name.endswith("1x1b"):
+            continue
+        block = name[: -len("_1x1b")]
+        src = by_name[block + "_proj"]["y"] if block + "_proj" in by_name else \
+            by_name[block + "_1x1a"]["x"] if block + "_1x1a" in by_name else None
+        if src is None:   # a subset of the layers without the block's first conv: a seeded tensor
+            g = torch.Generator().manual_seed(9000 + out.index(E))
+            src = torch.randn(tuple(E["y"].shape), generator=g).to(torch.bfloat16).contiguous(
                 memory_format=torch.channels_last).cuda()
-        out.append({"spec": spec, "conv": conv, "x": L["x"], "y": y, "r": r})
+        assert tuple(src.shape) == tuple(E["y"].shape) and src.dtype == E["y"].dtype, (name, src.shape)
+        E["r"] = src
     return out
 
 
@@ -752,7 +763,8 @@ def main():
                      "mma_sync_s8_rate_tops": s8_peak,
                      "vs_mma_sync_rate": s8_tops / s8_peak},
             "bf16_out_residual": {"workload": "the same 53 layers with bf16 outputs (fp32 stem) and a bf16 "
-                                              "residual added in each bottleneck's last 1x1 conv",
+                                              "residual added in each bottleneck's last 1x1 conv: the block's "
+                                              "shortcut tensor (its input, or the projection's output)",
                                   "ms_per_step": ext_ms, "tflops": flops_step / (ext_ms * 1e-3) / 1e12,
                                   "bf16_layers": ext_bf16, "residual_layers": ext_res},
             **extra,

@@ -21,13 +21,17 @@
 
 namespace convf {
 // defined once per tile width in tc_conv_inst.cu
-cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
+cudaError_t launch_tc_conv_bn32(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap*, int,
+                                bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
+cudaError_t launch_tc_conv_bn64(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap*, int,
+                                bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
+cudaError_t launch_tc_conv_bn128(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap*, int,
+                                bool, bool,
                                cudaStream_t);
-cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, int, bool, bool,
+cudaError_t launch_tc_conv_bn256(const TcConvParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap*, int,
+                                bool, bool,
                                cudaStream_t);
 }  // namespace convf
 
@@ -657,6 +661,9 @@ struct convf_handle {
   CUtensorMap tmB;
   CUtensorMap tmA;
   const void* map_x;
+  bool rsm;         // the bf16 residual is staged in shared memory by TMA (its map: tmR)
+  CUtensorMap tmR;
+  const void* map_r;
 };
 
 namespace {
@@ -1115,8 +1122,9 @@ convf_status create_impl(const convf_desc* desc, const void* W, const void* bias
       h->pair = h->sk = false;
     }
     h->kpb = 1;
+    h->rsm = !gather && tc_conv_rsm(h->bn, h->pair, h->sk, h->has_res, h->out_bf16, s.K);
     if (!gather) {
-      const int st = tc_conv_stages(h->bn, false, h->pair);
+      const int st = tc_conv_stages(h->bn, false, h->pair, h->rsm);
       const int nkb = h->ktot / 64;
       if (desc->kblocks_per_step) {
         if (st % desc->kblocks_per_step || nkb % desc->kblocks_per_step) {
@@ -1660,6 +1668,23 @@ convf_status encode_a_map(convf_handle* h, const void* x) {
 }  // namespace
 
 namespace {
+// staged residual (bf16 [M][K], K % 8 == 0): 2-D map {K, M}, 64 x 128 boxes of 128-byte rows in
+// the 128-byte swizzle; out-of-range rows and channels read as zero
+convf_status encode_r_map(convf_handle* h, const void* r) {
+  const Shape& s = h->s;
+  if (!load_encoders()) return fail(CONVF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)s.K, (cuuint64_t)s.M};
+  const cuuint64_t strides[1] = {(cuuint64_t)s.K * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult rc = g_encode_tiled(&h->tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(r), dims, strides, box,
+                               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (rc != CUDA_SUCCESS) return fail(CONVF_ERR_CUDA, "residual tensor map encoding failed (CUresult %d)", (int)rc);
+  h->map_r = r;
+  return CONVF_OK;
+}
+
 // depthwise 3x3: 4-D tiled map over x {C, W, H, N}, box = one tile's input window x 32 channels
 convf_status encode_dw_map(convf_handle* h, const void* x) {
   const Shape& s = h->s;
@@ -1813,9 +1838,9 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.q_bias = h->q_bias; p.q_mult = h->q_mult; p.q_shift = h->q_shift; p.q_scale = h->q_scale;
       p.q_zp = h->zp; p.q_lo = h->q_lo; p.q_hi = h->q_hi; p.y8 = static_cast<uint8_t*>(y);
       if (h->bn == 64)
-        ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, false, false, strm);
+        ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, nullptr, h->grid, false, false, strm);
       else
-        ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, false, false, strm);
+        ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, nullptr, h->grid, false, false, strm);
       break;
     }
     case CONVF_VARIANT_INT8: {
@@ -1859,11 +1884,15 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       // layers: 5 tiles per CTA gain, 10 and 20 lose)
       p.split_epi = h->num_tiles <= 8LL * h->grid ? 1 : 0;
       const bool gather = h->a_mode == kAGather;
+      if (h->rsm && res != h->map_r) {
+        if ((st = encode_r_map(h, res)) != CONVF_OK) return st;
+      }
+      const CUtensorMap* tmR = h->rsm ? &h->tmR : nullptr;
       switch (h->bn) {
-        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
-        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, h->grid, gather, h->pair, strm); break;
+        case 32: ce = launch_tc_conv_bn32(p, h->tmA, h->tmB, tmR, h->grid, gather, h->pair, strm); break;
+        case 64: ce = launch_tc_conv_bn64(p, h->tmA, h->tmB, tmR, h->grid, gather, h->pair, strm); break;
+        case 128: ce = launch_tc_conv_bn128(p, h->tmA, h->tmB, tmR, h->grid, gather, h->pair, strm); break;
+        default: ce = launch_tc_conv_bn256(p, h->tmA, h->tmB, tmR, h->grid, gather, h->pair, strm); break;
       }
     }
   }
@@ -1968,14 +1997,14 @@ convf_status conv_fused_describe(const convf_handle* h, char* buf, size_t len) {
   else
     snprintf(buf, len,
              "variant=%s M=%lld K=%d C=%d RxS=%dx%d stride=%d,%d group=%d preact=%d tile=%dx%d cta_pair=%d stream_k=%d kblocks=%d "
-             "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d out=%s residual=%d "
+             "kblocks_per_step=%d act_box_per_step=%d split_epilogue=%d out=%s residual=%d residual_staged=%d "
              "tiles=%d grid=%d patch_rows=%d tap_channels=%d weight_bytes=%zu",
              names[h->variant], s.M, s.K, s.C, s.R, s.S, s.sh, s.sw, h->desc.group, h->preact ? 1 : 0,
              h->pair ? 256 : 128, h->bn,
              h->pair ? 1 : 0,
              h->sk ? 1 : 0, h->num_kb, h->kpb, h->a3d ? 1 : 0,
              (h->bn >= 64 && !h->sk && h->a_mode != kAGather && h->num_tiles <= 8LL * h->grid) ? 1 : 0,
-             h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->num_tiles,
+             h->out_bf16 ? "bf16" : "f32", h->has_res ? 1 : 0, h->rsm ? 1 : 0, h->num_tiles,
              h->grid, h->patch_rows, h->cpt, h->dev_bytes);
   return ok();
 }
@@ -2134,9 +2163,9 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   p.scale = sc; p.bias = bi; p.x = xpad; p.lo = lo; p.hi = hi; p.status = status; p.y = static_cast<float*>(y);
   p.patch_rows = patch_rows_for(s, cpt); p.row_bytes = s.W * cpt * 2; p.cpt = cpt;
   switch (bn) {
-    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, grid, true, false, strm); break;
-    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, grid, true, false, strm); break;
-    default: ce = launch_tc_conv_bn128(p, tmA, tmB, grid, true, false, strm); break;
+    case 32: ce = launch_tc_conv_bn32(p, tmA, tmB, nullptr, grid, true, false, strm); break;
+    case 64: ce = launch_tc_conv_bn64(p, tmA, tmB, nullptr, grid, true, false, strm); break;
+    default: ce = launch_tc_conv_bn128(p, tmA, tmB, nullptr, grid, true, false, strm); break;
   }
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();

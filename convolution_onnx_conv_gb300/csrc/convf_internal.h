@@ -107,10 +107,17 @@ struct TcConvParams {
 };
 
 // Pipeline stages (64-wide k-blocks held in shared memory) of the TMA implicit-GEMM kernel per
-// tile width: operand ingest per SM does not grow with depth, so stages give way to the epilogue.
-constexpr int tc_conv_stages(int bn, bool gather, bool pair) {
+// tile width: operand ingest per SM does not grow with depth, so stages give way to the epilogue
+// (and, with rsm, to the two bf16 residual tiles staged in shared memory: 32 or 64 KB).
+constexpr int tc_conv_stages(int bn, bool gather, bool pair, bool rsm = false) {
   return gather ? (bn <= 64 ? 4 : 3)
+         : rsm  ? (bn == 128 ? 4 : 6)
                 : (pair ? (bn == 256 ? 6 : (bn == 128 ? 6 : 8)) : (bn == 256 ? 4 : (bn == 128 ? 6 : 8)));
+}
+// The bf16 residual is staged in shared memory by TMA (the tcgen05 kernel's EXTM 4) for single-CTA
+// whole tiles of 64 or 128 columns with bf16 outputs of K % 8 == 0 channels.
+constexpr bool tc_conv_rsm(int bn, bool pair, bool sk, bool res, bool out_bf16, int K) {
+  return res && out_bf16 && (K % 8) == 0 && !pair && !sk && (bn == 64 || bn == 128);
 }
 
 

@@ -32,9 +32,10 @@ constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kEpiCols = 32;
 constexpr int kEpiWarpBytes = 32 * kEpiCols * 4;   // one epilogue warp's 32 x 32 fp32 transpose
 constexpr int kPatchBufBytes = 32768;
+constexpr int kResAhead = 3;   // staged residual: tiles of L2 prefetch ahead of the smem load
 constexpr int kGatherThreads = 256;
 
-template <int BN, bool GATHER, bool PAIR>
+template <int BN, bool GATHER, bool PAIR, bool RSM = false>
 struct TcCfg {
   // with a CTA pair each CTA holds half of the weight tile (BN/2 rows)
   static constexpr int kBTileBytes = (PAIR ? BN / 2 : BN) * kBK * 2;
@@ -44,13 +45,16 @@ struct TcCfg {
   // tiles of 64+ columns: both groups can drain every tile, one column half each
   static constexpr bool kSplitEpiOk = kEpiGroups == 2 && BN >= 64;
   static constexpr int kThreads = 96 + 128 * kEpiGroups + (GATHER ? kGatherThreads : 0);
-  static constexpr int kStages = tc_conv_stages(BN, GATHER, PAIR);
+  static constexpr int kStages = tc_conv_stages(BN, GATHER, PAIR, RSM);
+  // RSM: two bf16 residual tiles (one per accumulator buffer), 128 rows of BN columns each, as
+  // 64-column boxes of 128-byte rows in the 128-byte swizzle
+  static constexpr int kResTileBytes = RSM ? kBM * BN * 2 : 0;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
   // gather mode: two buffers for the input rows one tile needs (TcConvParams::patch_rows)
   static constexpr int kPatchBytes = GATHER ? 2 * kPatchBufBytes : 0;
   static constexpr int kSmem = 1024 + kStages * (kATileBytes + kBTileBytes) + 4 * kEpiGroups * kEpiWarpBytes +
-                               kPatchBytes + kBarBytes;
+                               2 * kResTileBytes + kPatchBytes + kBarBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
 };
@@ -95,7 +99,10 @@ struct SegSched {
 
 // EXTM: 0 the plain fp32 epilogue; 1 a residual (fp32 or bf16 y); 2 bf16 y without a residual;
 // 3 a residual with bf16 y and K % 8 == 0 (the 16-byte mapping known at compile time, four
-// prefetched residual vectors instead of eight).
+// prefetched residual vectors instead of eight); 4 the same with the residual tile loaded by TMA
+// into shared memory while the tile's MMAs run (the activation producer issues it after the
+// tile's operands; the epilogue reads it from shared memory instead of waiting on global loads,
+// whose latency bounded the HBM-heavy residual layers).
 // Each its own instantiation: a shared epilogue cost the fp32 one 1.3% of the ResNet-50 step, and
 // the residual's prefetched rows (32 registers) made the bf16-only epilogue spill.
 // IQ: integer-exact mode for 8-bit convolutions (TcConvParams::iq_*): the accumulator restarts
@@ -105,15 +112,17 @@ struct SegSched {
 template <int BN, bool GATHER, bool PAIR, bool SK, int EXTM, bool IQ = false>
 __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
     tc_conv_kernel(const TcConvParams p, const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB) {
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmR) {
   static_assert(!(GATHER && PAIR), "the gathered-row mode runs on single CTAs");
   static_assert(!(SK && (GATHER || PAIR)), "stream-K runs on single CTAs with TMA activation loads");
   constexpr bool EXT = EXTM != 0;   // residual and/or bf16 output
-  constexpr bool RES = EXTM == 1 || EXTM == 3;   // a residual may be added
+  constexpr bool RES = EXTM == 1 || EXTM == 3 || EXTM == 4;   // a residual may be added
+  constexpr bool RSM = EXTM == 4;   // the bf16 residual tile staged in shared memory by TMA
+  static_assert(!RSM || (!PAIR && !SK && !GATHER && (BN == 64 || BN == 128)), "staged residual: single CTAs, whole tiles");
   static_assert(!(EXT && GATHER), "residual and bf16 output are served with TMA activation loads only");
   static_assert(!(IQ && (GATHER || PAIR || SK || EXT)), "the integer-exact mode runs whole tiles on single CTAs");
   static_assert(!IQ || BN == 64 || BN == 128, "the integer-exact epilogue holds 32 or 64 int32 sums per thread");
-  using Cfg = TcCfg<BN, GATHER, PAIR>;
+  using Cfg = TcCfg<BN, GATHER, PAIR, RSM>;
   // TcConvParams::split_epi on whole tiles of 64+ columns: both epilogue groups drain every
   // tile, one column half each (a tile's epilogue takes half as long, which shortens the last
   // tile of every CTA); otherwise (many tiles per CTA, stream-K segments, 32-column tiles,
@@ -135,7 +144,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATileBytes;
   uint8_t* sEpi = sB + kStages * Cfg::kBTileBytes;
-  uint8_t* sPatch = sEpi + 4 * Cfg::kEpiGroups * kEpiWarpBytes;
+  uint8_t* sRes = sEpi + 4 * Cfg::kEpiGroups * kEpiWarpBytes;   // RSM: [2][BN/64][128 rows][128 B]
+  uint8_t* sPatch = sRes + 2 * Cfg::kResTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sPatch + Cfg::kPatchBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -143,7 +153,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint64_t* pfull = bars + 2 * kStages + 4;    // input-row patch landed (gather mode)
   uint64_t* pempty = bars + 2 * kStages + 6;   // input-row patch consumed (gather mode)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 8);
+  uint64_t* rfull = bars + 2 * kStages + 8;    // RSM: residual tile landed (per buffer)
+  uint64_t* rempty = bars + 2 * kStages + 10;  // RSM: residual tile read (per buffer)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // gather mode: go/abort decisions broadcast by a leader thread through a named barrier; two
   // slots used alternately so the leader never overwrites a flag another thread has yet to read
@@ -164,12 +176,15 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       mbar_init(&tempty[b], (PAIR ? 2 : 1) * 4 * (split_epi ? 2 : 1));
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 1);
+      mbar_init(&rfull[b], 1);
+      mbar_init(&rempty[b], 4 * (split_epi ? 2 : 1));
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     if (!GATHER) tma_prefetch_desc(&tmA);
+    if (RSM) tma_prefetch_desc(&tmR);
   }
   if (warp == 2 && lane == 0) tma_prefetch_desc(&tmB);
   // the integer-exact mode keeps its running int32 sums in a third BN-column region
@@ -210,6 +225,16 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         else
           tma_load_3d(sB + stage * Cfg::kBTileBytes, &tmB, &full[stage], 0, n0, kb);
       }
+    }
+  }
+  // RSM: the residual boxes of this CTA's first tiles start towards L2 now (a prefetch reads no
+  // stale data: whatever the previous kernel still writes lands in L2, which serves every read
+  // after the wait)
+  if (RSM && warp == 0 && lane == 0) {
+    for (int j = 0; j < kResAhead; ++j) {
+      const int ft = tstart + j * tstep;
+      if (ft >= p.num_tiles) break;
+      for (int h = 0; h < BN / 64; ++h) tma_prefetch_l2_2d(&tmR, (ft % p.n_blocks) * BN + h * 64, (ft / p.n_blocks) * kTileM);
     }
   }
   pdl_wait_prior();
@@ -341,6 +366,23 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           if (stage == kStages) {
             stage = 0;
             phase ^= 1;
+          }
+        }
+        if (RSM) {
+          // the tile's residual, behind its operands: into buffer it & 1 once the epilogue has
+          // read that buffer's previous tile (rows past M and channels past K are zero fill)
+          const int rb = it & 1;
+          if (!mbar_wait(&rempty[rb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) goto teardown;
+          const int n0 = (tile % p.n_blocks) * BN;
+          mbar_arrive_expect_tx(&rfull[rb], static_cast<uint32_t>(Cfg::kResTileBytes));
+          for (int h = 0; h < BN / 64; ++h)
+            tma_load_2d(sRes + rb * Cfg::kResTileBytes + h * (kBM * 128), &tmR, &rfull[rb], n0 + h * 64, m0);
+          // and the residual of this CTA's tile kResAhead tiles on into L2, so that the shared-
+          // memory load above finds it there (two buffers alone leave too few bytes in flight)
+          const int ft = tile + kResAhead * tstep;
+          if (ft < p.num_tiles) {
+            const int fn0 = (ft % p.n_blocks) * BN, fm0 = (ft / p.n_blocks) * kTileM;
+            for (int h = 0; h < BN / 64; ++h) tma_prefetch_l2_2d(&tmR, fn0 + h * 64, fm0);
           }
         }
       }
@@ -664,6 +706,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
         else
           mbar_arrive(&tempty[acc]);
       }
+      // RSM: this tile's residual (buffer acc) in shared memory
+      if (RSM && !mbar_wait(&rfull[acc], acc_phase, abort_flag, p.status)) break;
+      const uint8_t* sResT = sRes + acc * Cfg::kResTileBytes;
       for (int ch = cbeg; ch < cend; ch += kRead) {
         const bool two = kRead == 2 && ch + 1 < cend;
         uint32_t v[kRead][32];
@@ -691,15 +736,37 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           // this thread's 4 channels (loaded before the transpose so their latency overlaps it)
           const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + nc + 4 * c4));
           const float4 bi = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + nc + 4 * c4));
+          // the 16-byte bf16 mapping (EXTM >= 3 at compile time): its 8 channels' scale and bias,
+          // likewise in flight before the transpose
+          float4 w16s0, w16s1, w16b0, w16b1;
+          if constexpr (EXTM >= 3) {
+            const int wcol = n0 + nc + 8 * (lane & 3);
+            w16s0 = __ldg(reinterpret_cast<const float4*>(p.scale + wcol));
+            w16s1 = __ldg(reinterpret_cast<const float4*>(p.scale + wcol + 4));
+            w16b0 = __ldg(reinterpret_cast<const float4*>(p.bias + wcol));
+            w16b1 = __ldg(reinterpret_cast<const float4*>(p.bias + wcol + 4));
+          }
           // EXT: the residual of this thread's eight (row, 4 channels), all eight loads in flight
           // before the transpose (one memory latency per chunk, not one per row).  bf16 output with
           // K % 8 == 0 (w16) maps threads to (row, 8 channels) instead, so that every load and
           // store moves 16 bytes; its residual bits sit in rv[0..3].
-          const bool w16 = EXTM == 3 || (EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0);
+          const bool w16 = EXTM >= 3 || (EXT && !SK && p.out_bf16 && (p.Kout & 7) == 0);
           const int sub8 = lane >> 2;   // w16: row within each group of eight
           const int c8 = lane & 3;      // w16: 8-channel column group
-          float4 rv[EXTM == 3 ? 4 : (RES ? 8 : 1)];
-          if (RES && w16) {
+          float4 rv[EXTM >= 3 ? 4 : (RES ? 8 : 1)];
+          if (RSM) {
+            // from the staged tile: row R's 16-byte chunk j sits at chunk j ^ (R & 7) of its
+            // 128-byte row (the 128-byte swizzle), one 64-column box after another
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = q * 32 + 8 * i + sub8;
+              const int col = nc + 8 * c8;
+              const uint4 w = *reinterpret_cast<const uint4*>(sResT + (col >> 6) * (kBM * 128) + rr * 128 +
+                                                              ((((col & 63) >> 3) ^ (rr & 7)) << 4));
+              rv[i] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                  __uint_as_float(w.w));
+            }
+          } else if (RES && w16) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -716,9 +783,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), 0.f, 0.f);
               }
             }
-          } else if (RES && EXTM != 3) {
+          } else if (RES && EXTM < 3) {
 #pragma unroll
-            for (int i = 0; i < (EXTM == 3 ? 0 : 8); ++i) {
+            for (int i = 0; i < (EXTM >= 3 ? 0 : 8); ++i) {
               rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
               const int r = 4 * i + sub;
               if (p.res == nullptr || (SK && mode == 2) || !col_ok || mt + r >= p.M) continue;
@@ -743,10 +810,18 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             // bf16 output, thread = (row 8i + sub8, channels 8*c8 .. +7): two 16-byte smem reads,
             // one 16-byte residual load (prefetched) and one 16-byte store per row
             const int col = nc + 8 * c8;
-            const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col));
-            const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col + 4));
-            const float4 b0 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col));
-            const float4 b1 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col + 4));
+            float4 s0, s1, b0, b1;
+            if constexpr (EXTM >= 3) {
+              s0 = w16s0;
+              s1 = w16s1;
+              b0 = w16b0;
+              b1 = w16b1;
+            } else {
+              s0 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col));
+              s1 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + col + 4));
+              b0 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col));
+              b1 = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + col + 4));
+            }
             float4 x0[4], x1[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -831,7 +906,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;   // element index
               float4 v = make_float4(fmaf(a[i].x, sc.x, bi.x), fmaf(a[i].y, sc.y, bi.y), fmaf(a[i].z, sc.z, bi.z),
                                      fmaf(a[i].w, sc.w, bi.w));
-              if (RES && EXTM != 3) {   // zero where there is no residual
+              if (RES && EXTM < 3) {   // zero where there is no residual
                 v.x += rv[EXTM == 1 ? i : 0].x;
                 v.y += rv[EXTM == 1 ? i : 0].y;
                 v.z += rv[EXTM == 1 ? i : 0].z;
@@ -872,6 +947,11 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           }
           __syncwarp();
         }
+      }
+      if (RSM) {
+        // this warp has read its rows of the staged residual: the producer may refill the buffer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[acc]);
       }
       if (SK && mode == 2) {
         // partial published: every thread's stores are visible before the flag
@@ -1037,14 +1117,15 @@ teardown:
   }
 }
 
+// tmR: the residual's tensor map (EXTM 4 only; any map otherwise, unused)
 template <int BN, bool GATHER, bool PAIR, bool SK = false, int EXTM = 0, bool IQ = false>
 cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             int grid, cudaStream_t stream) {
+                             const CUtensorMap& tmR, int grid, cudaStream_t stream) {
+  using Cfg = TcCfg<BN, GATHER, PAIR, EXTM == 4>;
   static bool configured = false;
   auto* k = tc_conv_kernel<BN, GATHER, PAIR, SK, EXTM, IQ>;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<BN, GATHER, PAIR>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     if (PAIR) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -1052,8 +1133,7 @@ cudaError_t launch_tc_conv_t(const TcConvParams& p, const CUtensorMap& tmA, cons
     }
     configured = true;
   }
-  return launch_pdl(k, dim3(grid), dim3(TcCfg<BN, GATHER, PAIR>::kThreads), TcCfg<BN, GATHER, PAIR>::kSmem, stream,
-                    PAIR ? 2 : 1, p, tmA, tmB);
+  return launch_pdl(k, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, stream, PAIR ? 2 : 1, p, tmA, tmB, tmR);
 }
 
 }  // namespace convf

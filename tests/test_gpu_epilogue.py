@@ -90,7 +90,14 @@ CASES = [
     (S("res_f32_stream_k", 2, 256, 14, 14, 256, 3, 3, pads=(1, 1, 1, 1)), False, True, {"stream_k": 2}),
     (S("res_bf16_cta_pair", 2, 128, 12, 12, 128, 3, 3, pads=(1, 1, 1, 1)), True, True, {"cta_pair": 2}),
     (S("bf16out_tile128_k256", 2, 128, 12, 12, 256, 3, 3, pads=(1, 1, 1, 1)), True, False, {"tile_n": 128}),
+    # the residual staged in shared memory by TMA: 128-wide tiles, ragged M, two tiles on some
+    # CTAs (both residual buffers), K a multiple of 8 but not of 64 (zero-filled box columns)
+    (S("res_bf16_staged_tile128", 4, 64, 56, 57, 264, 1, 1), True, True, {"tile_n": 128}),
+    (S("res_bf16_staged_3x3_k72", 3, 64, 17, 19, 72, 3, 3, pads=(1, 1, 1, 1)), True, True, {"tile_n": 64}),
 ]
+
+# handles whose bf16 residual is staged in shared memory (single CTAs, whole 64/128-wide tiles)
+STAGED = {"res_bf16_1x1_many_tiles", "res_bf16_staged_tile128", "res_bf16_staged_3x3_k72"}
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
@@ -101,6 +108,7 @@ def test_epilogue_options_every_output(case):
     conv = build(spec, inp, out_bf16, residual, **kw)
     d = conv.describe()
     assert f"out={'bf16' if out_bf16 else 'f32'} residual={int(residual)}" in d, d
+    assert f"residual_staged={int(spec.name in STAGED)}" in d, d
     r = residual_for(conv, seed + 1, out_bf16) if residual else None
     ref = oracle_ref(spec, inp, r)
     x = to_device_nhwc(inp["x"])
