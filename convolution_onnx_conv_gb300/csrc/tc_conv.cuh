@@ -33,6 +33,7 @@ constexpr int kEpiCols = 32;
 constexpr int kEpiWarpBytes = 32 * kEpiCols * 4;   // one epilogue warp's 32 x 32 fp32 transpose
 constexpr int kPatchBufBytes = 32768;
 constexpr int kResAhead = 3;   // staged residual: tiles of L2 prefetch ahead of the smem load
+constexpr int kActAhead = 4;   // tiles whose input rows are prefetched into L2 before the wait
 constexpr int kGatherThreads = 256;
 
 template <int BN, bool GATHER, bool PAIR, bool RSM = false>
@@ -227,9 +228,32 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
       }
     }
   }
-  // RSM: the residual boxes of this CTA's first tiles start towards L2 now (a prefetch reads no
-  // stale data: whatever the previous kernel still writes lands in L2, which serves every read
-  // after the wait)
+  // The input rows of this CTA's first kActAhead tiles start towards L2 now, behind the previous
+  // kernel's tail (a prefetch reads no stale data: whatever the previous kernel still writes
+  // lands in L2, which serves every read after the wait).  Whole NHWC rows of one image: the
+  // tile's pixels (1x1) or the input rows its output rows read (im2col).
+  if (!GATHER && warp == 0 && lane == 0) {
+    SegSched<SK> sched(p, tstart, tstep);
+    int tile, ka, kend;
+    for (int j = 0; j < kActAhead && sched.next(tile, ka, kend); ++j) {
+      const int m0 = (tile / p.n_blocks) * kTileM + mrow_off;
+      if (m0 >= p.M) break;
+      const int m1 = min(m0 + kBM, p.M) - 1;
+      if (p.a_mode == kA2D) {
+        bulk_prefetch_l2(p.x + static_cast<size_t>(m0) * p.C, static_cast<uint32_t>(m1 - m0 + 1) * p.C * 2);
+      } else {
+        const int hw = p.Ho * p.Wo;
+        const int img = m0 / hw;
+        const int last = min(m1 - img * hw, hw - 1);   // within the tile's first image
+        const int ih0 = max(0, ((m0 - img * hw) / p.Wo) * p.sh - p.pt);
+        const int ih1 = min(p.H - 1, (last / p.Wo) * p.sh - p.pt + (p.R - 1) * p.dh);
+        if (ih0 <= ih1)
+          bulk_prefetch_l2(p.x + (static_cast<size_t>(img) * p.H + ih0) * p.W * p.C,
+                           static_cast<uint32_t>(ih1 - ih0 + 1) * p.W * p.C * 2);
+      }
+    }
+  }
+  // RSM: the residual boxes of this CTA's first tiles start towards L2 now (as above)
   if (RSM && warp == 0 && lane == 0) {
     for (int j = 0; j < kResAhead; ++j) {
       const int ft = tstart + j * tstep;

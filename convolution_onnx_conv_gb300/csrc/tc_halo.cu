@@ -114,6 +114,17 @@ __global__ void __launch_bounds__(kHThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_launch_dependents();
+  // the input rows of this CTA's first two tiles start towards L2 behind the previous kernel's
+  // tail (a prefetch reads no stale data: what that kernel still writes lands in L2); the boxes
+  // start at column 0 and row max(0, .): the padding columns and rows hold no data
+  if (warp == 0 && lane == 0) {
+    for (int tile = blockIdx.x, j = 0; j < 2 && tile < p.num_tiles; tile += gridDim.x, ++j) {
+      const int rt = tile / p.n_blocks;
+      const int img = rt / p.tiles_per_img;
+      const int oh0 = (rt - img * p.tiles_per_img) * p.TR;
+      for (int cb = 0; cb < p.cblocks; ++cb) tma_prefetch_l2_4d(&tmA, cb * kHBK, 0, max(0, oh0 - p.pt), img);
+    }
+  }
   pdl_wait_prior();
 
   const int taps = p.R * p.S;
