@@ -13,7 +13,7 @@ from . import _build
 
 # --- enums (mirror include/conv_fused.h)
 CONVF_OK, CONVF_ERR_INVALID_ARG, CONVF_ERR_UNSUPPORTED, CONVF_ERR_OOM, CONVF_ERR_CUDA, \
-    CONVF_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+    CONVF_ERR_TIMEOUT, CONVF_ERR_BOUNDS = 0, -1, -2, -3, -4, -5, -6
 CONVF_BF16, CONVF_S8, CONVF_Q8 = 0, 1, 2
 CONVF_OUT_F32, CONVF_OUT_BF16 = 0, 1
 CONVF_NCHW, CONVF_NHWC = 0, 1
@@ -99,8 +99,14 @@ class ConvFusedError(RuntimeError):
 _LIB = None
 
 
+def _bounds_build() -> bool:
+    return os.environ.get("CONVF_DEBUG_BOUNDS", "") not in ("", "0")
+
+
 def library_path() -> str:
-    return _build.LIB
+    """The library this process loads: libconvfused.so, or the bounds-checking build when the
+    environment sets CONVF_DEBUG_BOUNDS=1."""
+    return _build.LIB_BOUNDS if _bounds_build() else _build.LIB
 
 
 def load_library(build_if_missing: bool = False):
@@ -108,11 +114,12 @@ def load_library(build_if_missing: bool = False):
     global _LIB
     if _LIB is not None:
         return _LIB
+    path = library_path()
     if build_if_missing:
-        _build.build()
-    if not os.path.exists(_build.LIB):
-        raise ImportError(f"libconvfused.so is not built ({_build.LIB}); run __graft_entry__.build()")
-    lib = ctypes.CDLL(_build.LIB)
+        _build.build(debug_bounds=_bounds_build())
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
     P = ctypes.POINTER
     dptr = P(ConvDesc)
     vp = ctypes.c_void_p

@@ -1850,6 +1850,7 @@ convf_status run_impl(convf_handle* h, const void* x, const void* res, void* y, 
       p.num_kb = s.R * s.S * s.C / 64;
       p.x = static_cast<const int8_t*>(x); p.w = h->w_s8; p.bias = h->qbias; p.mult = h->qmult;
       p.shift = h->qshift; p.y = static_cast<int8_t*>(y); p.zp = h->zp; p.relu = h->desc.act == CONVF_ACT_RELU;
+      p.status = h->status;
       ce = launch_s8_conv(p, strm);
       break;
     }
@@ -1922,6 +1923,8 @@ convf_status conv_fused_status(convf_handle* h) {
   cudaError_t ce = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost);
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "status read failed: %s", cudaGetErrorString(ce));
   if (v & kStatusTimeout) return fail(CONVF_ERR_TIMEOUT, "a bounded device wait ran out in an earlier run");
+  if (v & kStatusBounds)
+    return fail(CONVF_ERR_BOUNDS, "a kernel computed an index outside its tensor (bounds-checking build)");
   return ok();
 }
 

@@ -9,6 +9,25 @@ namespace convf {
 
 // Bit set in a handle's device status word when a bounded device wait ran out.
 constexpr int kStatusTimeout = 1;
+// Bit set by a build with CONVF_DEBUG_BOUNDS when a kernel computed a global index outside the
+// tensor its parameters describe; the access is skipped instead of made.
+constexpr int kStatusBounds = 2;
+
+// CONVF_IN_BOUNDS(ok, status): true when the checked condition holds.  Ordinary builds compile
+// it to `true` (the kernels' own masks already keep every access inside its tensor); the
+// CONVF_DEBUG_BOUNDS build evaluates the condition, and on failure sets kStatusBounds in the
+// status word and returns false so that the caller skips the access.
+#if defined(__CUDACC__)
+__device__ __forceinline__ bool convf_bounds_ok(bool ok, int* status) {
+  if (!ok && status) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#endif
+#ifdef CONVF_DEBUG_BOUNDS
+#define CONVF_IN_BOUNDS(ok, status) (::convf::convf_bounds_ok((ok), (status)))
+#else
+#define CONVF_IN_BOUNDS(ok, status) (true)
+#endif
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream finishes; every kernel here waits (griddepcontrol.wait) before its
@@ -303,6 +322,7 @@ struct S8Params {
   const int32_t* shift;  // [K]
   int8_t* y;              // NHWC int8
   int zp, relu;
+  int* status;            // device status word (bounds-checking build)
 };
 cudaError_t launch_s8_conv(const S8Params& p, cudaStream_t stream);
 cudaError_t measure_s8_mma_rate(int num_sms, cudaStream_t stream, double* tops);

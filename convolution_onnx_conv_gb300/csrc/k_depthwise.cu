@@ -84,6 +84,7 @@ __device__ __forceinline__ void dw_load_taps(const DwParams& p, int c, f32x2 (&t
 // 16-byte fp32 store, or (EXT) the residual added first and fp32 or bf16 (nearest even) stores.
 template <bool EXT>
 __device__ __forceinline__ void dw_store4(const DwParams& p, size_t e, f32x2 a0, f32x2 a1) {
+  if (!CONVF_IN_BOUNDS(e + 4 <= static_cast<size_t>(p.N) * p.Ho * p.Wo * p.C, p.status)) return;
   float v0, v1, v2, v3;
   unpack_f32x2(a0, v0, v1);
   unpack_f32x2(a1, v2, v3);
@@ -482,6 +483,7 @@ __global__ void __launch_bounds__(256) dw_generic_kernel(const DwParams p) {
       }
     }
     const size_t e = ((static_cast<size_t>(n) * p.Ho + oh) * p.Wo + ow) * p.C + c0;
+    if (!CONVF_IN_BOUNDS(e + 8 <= static_cast<size_t>(p.N) * p.Ho * p.Wo * p.C, p.status)) continue;
     if (p.res != nullptr) {
       if (p.out_bf16) {
         const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.res) + e));

@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(256, 1) s8_conv_kernel(const S8Params p) {
   for (int idx = tid; idx < kS8BM * (kS8BN / 16); idx += 256) {
     const int row = idx >> 3, ch = idx & 7;
     const int mm = m0 + row, nn = n0 + ch * 16;
-    if (mm < p.M && nn < p.Kout)
+    if (mm < p.M && nn < p.Kout &&
+        CONVF_IN_BOUNDS(static_cast<size_t>(mm) * p.Kout + nn + 16 <= static_cast<size_t>(p.M) * p.Kout, p.status))
       *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(mm) * p.Kout + nn) =
           *reinterpret_cast<const uint4*>(sOut + row * kS8BN + ch * 16);
   }

@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kMbThreads, 1)
             const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.bp + k));
             float4 o = make_float4(fmaf(__uint_as_float(v[e]), s4.x, b4.x), fmaf(__uint_as_float(v[e + 1]), s4.y, b4.y),
                                    fmaf(__uint_as_float(v[e + 2]), s4.z, b4.z), fmaf(__uint_as_float(v[e + 3]), s4.w, b4.w));
-            if (p.residual) {
+            if (p.residual && CONVF_IN_BOUNDS(hp < p.P && k < p.cin_kb * 64, p.status)) {
               const uint8_t* xr = sX + (ti % p.nxb) * p.x_buf_bytes + (k >> 6) * p.x_kb_bytes + (hp >> 3) * 1024 +
                                   (hp & 7) * 128;
               const uint2 w = *reinterpret_cast<const uint2*>(xr + (((((k & 63) >> 3) ^ (hp & 7))) << 4) + (k & 4) * 2);
@@ -421,7 +421,10 @@ __global__ void __launch_bounds__(kMbThreads, 1)
               o.z += __uint_as_float(w.y << 16);
               o.w += __uint_as_float(w.y & 0xffff0000u);
             }
-            *reinterpret_cast<float4*>(yrow + k) = o;
+            if (CONVF_IN_BOUNDS(((static_cast<size_t>(n) * p.Ho + oy0 + oy) * p.Wo + ox0 + ox) * p.Cout + k + 4 <=
+                                    static_cast<size_t>(p.N) * p.Ho * p.Wo * p.Cout,
+                                p.status))
+              *reinterpret_cast<float4*>(yrow + k) = o;
           }
         }
       }

@@ -662,7 +662,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             packed[h] = (static_cast<uint32_t>(qv[0]) & 0xffu) | ((static_cast<uint32_t>(qv[1]) & 0xffu) << 8) |
                         ((static_cast<uint32_t>(qv[2]) & 0xffu) << 16) | ((static_cast<uint32_t>(qv[3]) & 0xffu) << 24);
           }
-          *reinterpret_cast<uint4*>(yrow + col) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          if (CONVF_IN_BOUNDS(static_cast<size_t>(row) * p.Kout + col + 16 <= static_cast<size_t>(p.M) * p.Kout, p.status))
+            *reinterpret_cast<uint4*>(yrow + col) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
       }
       goto teardown;
@@ -798,6 +799,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const int col = nc + 8 * c8;
               if (p.res == nullptr || col >= left || mt + r >= p.M) continue;
               const uint16_t* rp = static_cast<const uint16_t*>(p.res) + static_cast<size_t>(mt + r) * p.Kout + n0 + col;
+              if (!CONVF_IN_BOUNDS(static_cast<size_t>(mt + r) * p.Kout + n0 + col + (col + 8 <= left ? 8 : 4) <=
+                                       static_cast<size_t>(p.M) * p.Kout, p.status))
+                continue;
               if (col + 8 <= left) {
                 const uint4 q = __ldg(reinterpret_cast<const uint4*>(rp));
                 rv[i] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
@@ -814,6 +818,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               const int r = 4 * i + sub;
               if (p.res == nullptr || (SK && mode == 2) || !col_ok || mt + r >= p.M) continue;
               const size_t e = static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4;
+              if (!CONVF_IN_BOUNDS(e + 4 <= static_cast<size_t>(p.M) * p.Kout, p.status)) continue;
               if (p.out_bf16) {
                 const uint2 rb = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.res) + e));
                 rv[i] = make_float4(__uint_as_float(rb.x << 16), __uint_as_float(rb.x & 0xffff0000u),
@@ -876,6 +881,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
                 pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
               }
               uint16_t* yp = reinterpret_cast<uint16_t*>(p.y) + static_cast<size_t>(mt + r) * p.Kout + n0 + col;
+              if (!CONVF_IN_BOUNDS(static_cast<size_t>(mt + r) * p.Kout + n0 + col + (col + 8 <= left ? 8 : 4) <=
+                                       static_cast<size_t>(p.M) * p.Kout, p.status))
+                continue;
               if (col + 8 <= left)
                 *reinterpret_cast<uint4*>(yp) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               else
@@ -938,6 +946,7 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               }
               v = make_float4(fminf(fmaxf(v.x, p.lo), p.hi), fminf(fmaxf(v.y, p.lo), p.hi),
                               fminf(fmaxf(v.z, p.lo), p.hi), fminf(fmaxf(v.w, p.lo), p.hi));
+              if (!CONVF_IN_BOUNDS(e + 4 <= static_cast<size_t>(p.M) * p.Kout, p.status)) continue;
               if (p.out_bf16) {
                 const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x, v.y);
                 const __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z, v.w);
@@ -954,7 +963,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
             if (!col_ok || mt + r >= p.M) continue;
             if (SK) {
               if (mode == 2) {
-                __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a[i]);
+                if (CONVF_IN_BOUNDS(static_cast<size_t>(q * 32 + r) * BN + nc + 4 * c4 + 4 <= static_cast<size_t>(kBM) * BN,
+                                    p.status))
+                  __stcg(reinterpret_cast<float4*>(wsw + static_cast<size_t>(r) * BN + nc + 4 * c4), a[i]);
                 continue;
               }
               a[i].x += part[i].x;
@@ -962,6 +973,9 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               a[i].z += part[i].z;
               a[i].w += part[i].w;
             }
+            if (!CONVF_IN_BOUNDS(static_cast<size_t>(mt + r) * p.Kout + n0 + nc + 4 * c4 + 4 <=
+                                     static_cast<size_t>(p.M) * p.Kout, p.status))
+              continue;
             *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
                 make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
                             fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),
@@ -1044,7 +1058,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           for (int i = 0; i < 8; ++i) {
             v[i] = make_uint2(0, 0);
             const int ih = ih0 + r * p.dh, iw = iw0 + s * p.dw;
-            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W &&
+                CONVF_IN_BOUNDS(!use_patch || (ih >= ih_first && ih - ih_first < p.patch_rows), p.status))
               v[i] = *reinterpret_cast<const uint2*>(src + ((ih - ih_first) * p.W + iw) * 4);
             if (++s == p.S) {
               s = 0;
@@ -1064,7 +1079,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
           for (int i = 0; i < 4; ++i) {
             v[i] = make_uint4(0, 0, 0, 0);
             const int ih = ih0 + r * p.dh, iw = iw0 + s * p.dw;
-            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+            if (row_ok && r < p.R && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W &&
+                CONVF_IN_BOUNDS(!use_patch || (ih >= ih_first && ih - ih_first < p.patch_rows), p.status))
               v[i] = *reinterpret_cast<const uint4*>(src + ((ih - ih_first) * p.W + iw) * 8);
             if (++s == p.S) {
               s = 0;
@@ -1089,7 +1105,8 @@ __global__ void __launch_bounds__(TcCfg<BN, GATHER, PAIR>::kThreads, 1)
               if (row_ok && r < p.R) {
                 const int ih = ih0 + r * p.dh;
                 const int iw = iw0 + s * p.dw;
-                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+                if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W &&
+                    CONVF_IN_BOUNDS(!use_patch || (ih >= ih_first && ih - ih_first < p.patch_rows), p.status))
                   val = use_patch ? src[((ih - ih_first) * p.W + iw) * p.C + c]
                                   : __ldg(src + (static_cast<size_t>(ih) * p.W + iw) * p.C + c);
               }

@@ -257,6 +257,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
       const int left = p.Kout - n0;
       const int nchunks = left >= BN ? BN / kHEpiCols : (left + kHEpiCols - 1) / kHEpiCols;
       float* ybase = p.y + (static_cast<size_t>(img) * p.Ho + oh0) * p.Wo * p.Kout + n0;
+      // elements of y (bounds-checking build): images x Ho x Wo x Kout
+      const size_t ytotal = static_cast<size_t>(p.num_tiles / p.n_blocks / p.tiles_per_img) * p.Ho * p.Wo * p.Kout;
+      (void)ytotal;
       for (int ch = 0; ch < nchunks; ch += 2) {
         const bool two = ch + 1 < nchunks;
         uint32_t v[2][32];
@@ -296,6 +299,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
             const int tr = q * 32 + 4 * i + sub;
             const int off = rm_off[tr];
             if (!col_ok || off < 0 || oh0 + rm_dr[tr] >= p.Ho) continue;
+            if (!CONVF_IN_BOUNDS(static_cast<size_t>(ybase - p.y) + static_cast<size_t>(off) * p.Kout + nc + 4 * c4 + 4 <=
+                                     ytotal, p.status))
+              continue;
             if (!EXT) {
               *reinterpret_cast<float4*>(ybase + static_cast<size_t>(off) * p.Kout + nc + 4 * c4) =
                   make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),

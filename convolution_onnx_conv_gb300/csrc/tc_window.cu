@@ -244,7 +244,10 @@ __global__ void __launch_bounds__(kWinThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = 4 * (i0 + i) + sub;
-              if (col_ok && ow0 + r < p.Wo)
+              if (col_ok && ow0 + r < p.Wo &&
+                  CONVF_IN_BOUNDS((static_cast<size_t>(orow) * p.Wo + ow0 + r) * p.Kout + nc + 4 * c4 + 4 <=
+                                      static_cast<size_t>(p.num_tiles / p.ow_blocks) * p.Wo * p.Kout,
+                                  p.status))
                 *reinterpret_cast<float4*>(yw + static_cast<size_t>(r) * p.Kout + nc + 4 * c4) =
                     make_float4(fminf(fmaxf(fmaf(a[i].x, sc.x, bi.x), p.lo), p.hi),
                                 fminf(fmaxf(fmaf(a[i].y, sc.y, bi.y), p.lo), p.hi),

@@ -60,7 +60,10 @@ typedef enum {
   CONVF_ERR_UNSUPPORTED = -2,  /* well-formed but not served by any kernel: refused, no fallback */
   CONVF_ERR_OOM = -3,          /* device allocation failed at create */
   CONVF_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
-  CONVF_ERR_TIMEOUT = -5       /* a bounded device wait ran out during a run */
+  CONVF_ERR_TIMEOUT = -5,      /* a bounded device wait ran out during a run */
+  CONVF_ERR_BOUNDS = -6        /* only in a library built with CONVF_DEBUG_BOUNDS: a kernel computed
+                                  a global index outside the tensor its parameters describe and
+                                  skipped that access (a library defect, never the caller's) */
 } convf_status;
 
 /* CONVF_Q8: ONNX QLinearConv -- 8-bit x, W and y with scales and zero points
@@ -290,13 +293,14 @@ convf_status conv_fused_run(convf_handle* h, const void* x, void* y, void* strea
 
 /* conv_fused_run for a handle created with residual = 1: y = act(scale * conv(x) + bias' + r).
  * r (device, NHWC, the element type of y, y's shape) must be 16-byte aligned; it may be y itself
- * (each element is read before it is written, by the same thread) but must not overlap y
+ * (each element of the residual is read before the same element of y is written) but must not overlap y
  * otherwise, nor x.  conv_fused_run refuses residual handles and this call refuses the others
  * (CONVF_ERR_INVALID_ARG). */
 convf_status conv_fused_run_residual(convf_handle* h, const void* x, const void* r, void* y, void* stream);
 
 /* Device status of the handle's previous runs, read after the caller synchronised the
- * stream: CONVF_OK, or CONVF_ERR_TIMEOUT if a bounded wait ran out (the status is sticky
+ * stream: CONVF_OK, or CONVF_ERR_TIMEOUT if a bounded wait ran out, or (bounds-checking build
+ * only) CONVF_ERR_BOUNDS (the status is sticky
  * until conv_fused_clear_status). */
 convf_status conv_fused_status(convf_handle* h);
 convf_status conv_fused_clear_status(convf_handle* h);
