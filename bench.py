@@ -497,6 +497,12 @@ def profile_layers(which):
                                   y_zero_point=inp["y_zp"], relu=True, stride=spec.stride, pads=spec.pads)
             x = inp["x"].contiguous(memory_format=torch.channels_last).cuda()
             layers.append({"spec": spec, "conv": conv, "x": x, "y": conv.new_output()})
+    elif kind == "ext":
+        # ResNet-50 b32 layers with bf16 output (and, on a bottleneck's last 1x1 conv, a bf16
+        # residual: the staged-residual epilogue)
+        specs = workloads.resnet50_layers(32)
+        sel = [specs[i] for i in idx]
+        layers = build_ext_layers(sel, build_layers(sel, 3, torch, cf, synthetic), torch, cf)
     else:
         table = {"r50": (workloads.resnet50_layers(32), 3, False), "dw": (workloads.depthwise_layers(64), 4, False),
                  "s8": (workloads.int8_layers(64), 5, True)}
@@ -504,10 +510,10 @@ def profile_layers(which):
         layers = build_layers([specs[i] for i in idx], base, torch, cf, synthetic, s8=s8)
     for _ in range(2):
         for L in layers:
-            L["conv"](L["x"], L["y"])
+            L["conv"](L["x"], L["y"], r=L.get("r"))
     torch.cuda.synchronize()
     for L in layers:
-        L["conv"](L["x"], L["y"])
+        L["conv"](L["x"], L["y"], r=L.get("r"))
         torch.cuda.synchronize()
         print(L["spec"].name, L["conv"].describe())
 
@@ -523,9 +529,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile", default=None,
-                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I', 's8:I', 'q8:I' (QLinearConv) "
-                         "or 'mb:I' (fused MobileNetV2 block) runs those layers twice (warm-up) and then once "
-                         "more each, printing their kernel descriptions")
+                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I', 's8:I', 'q8:I' (QLinearConv), "
+                         "'ext:I' (ResNet-50 layer with bf16 output and, on a block's last 1x1 conv, a bf16 "
+                         "residual) or 'mb:I' (fused MobileNetV2 block) runs those layers twice (warm-up) and "
+                         "then once more each, printing their kernel descriptions")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
