@@ -9,8 +9,8 @@
 // and stride-1 images 16k but not 32k columns wide) or of two neighbouring output columns
 // (stride 1 otherwise), walks the window's input rows once, scattering every converted row into
 // the (up to three) output rows it feeds, then stores each output row as one 16-byte vector per
-// column as soon as it is complete.  The taps of a CTA's first channel slab load before the wait
-// for the previous kernel.
+// column as soon as it is complete.  The taps of a CTA's first channel slab load, and its first
+// tile's input window is prefetched into L2, before the wait for the previous kernel.
 #include <cuda_bf16.h>
 
 #include "convf_internal.h"
@@ -78,6 +78,23 @@ __device__ __forceinline__ void dw_load_taps(const DwParams& p, int c, f32x2 (&t
   const float4 b = ok ? __ldg(reinterpret_cast<const float4*>(p.bias + c)) : make_float4(0, 0, 0, 0);
   bias[0] = pack_f32x2(b.x, b.y);
   bias[1] = pack_f32x2(b.z, b.w);
+}
+
+// The input window of this CTA's first tile (tile index blockIdx.x: channel slab fastest, then
+// column block, row block, image group) towards L2 before the wait for the previous kernel (a
+// prefetch reads no stale data: what that kernel still writes lands in L2, which serves every
+// read after the wait).  The box starts at column and row max(0, .): the padding holds no data.
+__device__ __forceinline__ void dw_prefetch_first_window(const DwParams& p, const CUtensorMap* tm, int col_step,
+                                                         int row_step, int nb, int cs) {
+  const uint32_t u = blockIdx.x;
+  const uint32_t t = fast_div(u, p.f_slabs);
+  const int slab = static_cast<int>(u - t * p.f_slabs.d);
+  const uint32_t t2 = fast_div(t, p.f_owbs);
+  const int owb = static_cast<int>(t - t2 * p.f_owbs.d);
+  const int ng = static_cast<int>(fast_div(t2, p.f_ohbs));
+  const int ohb = static_cast<int>(t2 - ng * p.f_ohbs.d);
+  if (ng * nb >= p.N) return;
+  tma_prefetch_l2_4d(tm, slab * cs, max(0, owb * col_step - p.pl), max(0, ohb * row_step - p.pt), ng * nb);
 }
 
 // Epilogue of four channels of one output pixel at element offset e of y: clamp and a streaming
@@ -177,6 +194,7 @@ __global__ void __launch_bounds__(DwTile<SW>::kThreads) dw3x3_tma_kernel(const _
   f32x2 tap[9][2], bias[2];    // channel pairs (c, c+1), (c+2, c+3)
   int cur_slab = static_cast<int>(blockIdx.x - fast_div(blockIdx.x, p.f_slabs) * p.f_slabs.d);
   dw_load_taps(p, cur_slab * T::kCS + cq * 4, tap, bias);
+  if (tid == 0) dw_prefetch_first_window(p, &tmX, tcols * SW, T::kTH * SW, nb, T::kCS);
   pdl_wait_prior();
 
   const int slabs = p.f_slabs.d;
@@ -339,6 +357,7 @@ __global__ void __launch_bounds__(128) dw3x3_pair_kernel(const __grid_constant__
   f32x2 tap[9][2], bias[2];
   int cur_slab = static_cast<int>(blockIdx.x - fast_div(blockIdx.x, p.f_slabs) * p.f_slabs.d);
   dw_load_taps(p, cur_slab * T::kCS + cq * 4, tap, bias);
+  if (tid == 0) dw_prefetch_first_window(p, &tmX, TCOLS, T::kTH, T::kNb, T::kCS);
   pdl_wait_prior();
 
   const int units = (p.N + T::kNb - 1) / T::kNb * p.f_ohbs.d * p.f_owbs.d * p.f_slabs.d;
