@@ -6,5 +6,5 @@ seeded synthetic inputs of the workloads.  Importing it does not load the librar
 call does, and fails loudly if the library is not built.
 """
 from ._binding import *  # noqa: F401,F403
-from ._binding import (ConvDesc, ConvFusedError, FusedConv, load_library, make_desc,  # noqa: F401
+from ._binding import (ConvDesc, ConvFusedError, FusedConv, ConvChain, load_library, make_desc,  # noqa: F401
                        library_path, EXPORTED, VARIANT_NAMES)

@@ -35,7 +35,9 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_variant", "conv_fused_describe", "conv_fused_last_error",
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
             "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact",
-            "conv_fused_create_mbv2_block", "conv_fused_debug_fail_alloc", "conv_fused_debug_live_handles"]
+            "conv_fused_create_mbv2_block", "conv_fused_debug_fail_alloc", "conv_fused_debug_live_handles",
+            "conv_fused_chain_create", "conv_fused_chain_run", "conv_fused_chain_status",
+            "conv_fused_chain_clear_status", "conv_fused_chain_describe", "conv_fused_chain_destroy"]
 
 
 class ConvDesc(ctypes.Structure):
@@ -55,6 +57,11 @@ class BlockDesc(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int), ("Cin", ctypes.c_int),
                 ("Ch", ctypes.c_int), ("Cout", ctypes.c_int), ("stride", ctypes.c_int), ("expand", ctypes.c_int),
                 ("residual", ctypes.c_int)]
+
+
+class ChainStep(ctypes.Structure):
+    """convf_chain_step: one conv run of a chain (handle, x, residual or NULL, y)."""
+    _fields_ = [("conv", ctypes.c_void_p), ("x", ctypes.c_void_p), ("r", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 class QParams(ctypes.Structure):
@@ -149,8 +156,15 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_measure_int8_mma_rate.argtypes = [vp, P(ctypes.c_double)]
     lib.conv_fused_debug_fail_alloc.argtypes = [ctypes.c_int]
     lib.conv_fused_debug_live_handles.argtypes = []
+    lib.conv_fused_chain_create.argtypes = [P(ChainStep), ctypes.c_int, P(vp)]
+    lib.conv_fused_chain_run.argtypes = [vp, vp]
+    lib.conv_fused_chain_status.argtypes = [vp]
+    lib.conv_fused_chain_clear_status.argtypes = [vp]
+    lib.conv_fused_chain_describe.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.conv_fused_chain_destroy.argtypes = [vp]
+    lib.conv_fused_chain_destroy.restype = None
     for name in EXPORTED:
-        if name not in ("conv_fused_destroy", "conv_fused_last_error"):
+        if name not in ("conv_fused_destroy", "conv_fused_last_error", "conv_fused_chain_destroy"):
             getattr(lib, name).restype = ctypes.c_int
     _LIB = lib
     return lib
@@ -327,6 +341,41 @@ def conv_fused_run_noalloc(desc: ConvDesc, x, w_packed, scale, bias, y, status=N
                                                  _addr(bias), _addr(y), _addr(status), s))
 
 
+def conv_fused_chain_create(steps) -> int:
+    """steps: sequence of (handle, x, r or None, y) with device pointers (ints) or CUDA tensors."""
+    arr = (ChainStep * len(steps))()
+    for i, (h, x, r, y) in enumerate(steps):
+        arr[i] = ChainStep(h, _addr(x), _addr(r), _addr(y))
+    c = ctypes.c_void_p()
+    _check(load_library().conv_fused_chain_create(arr, len(steps), ctypes.byref(c)))
+    return c.value
+
+
+def conv_fused_chain_run(chain: int, stream=None):
+    s = stream
+    if s is not None and hasattr(s, "cuda_stream"):
+        s = s.cuda_stream
+    _check(load_library().conv_fused_chain_run(chain, s))
+
+
+def conv_fused_chain_status(chain: int) -> int:
+    return load_library().conv_fused_chain_status(chain)
+
+
+def conv_fused_chain_clear_status(chain: int):
+    _check(load_library().conv_fused_chain_clear_status(chain))
+
+
+def conv_fused_chain_describe(chain: int) -> str:
+    buf = ctypes.create_string_buffer(65536)
+    _check(load_library().conv_fused_chain_describe(chain, buf, 65536))
+    return buf.value.decode()
+
+
+def conv_fused_chain_destroy(chain: int):
+    load_library().conv_fused_chain_destroy(chain)
+
+
 # --------------------------------------------------------------------------- torch convenience
 
 class FusedConv:
@@ -494,3 +543,47 @@ class InvertedResidualBlock(FusedConv):
         self.s8 = False
         self.out_bf16 = False
         self.residual = False
+
+
+class ConvChain:
+    """A sequence of FusedConv runs as one persistent launch (conv_fused_chain_*).
+
+    ``steps`` is a sequence of ``(conv, x, y)`` or ``(conv, x, y, r)`` with ``conv`` a FusedConv
+    (1x1-GEMM or im2col implicit-GEMM variant) and ``x``, ``y``, ``r`` CUDA tensors in
+    channels-last storage.  A step whose ``x`` (or ``r``) is an earlier step's ``y`` reads that
+    output.  The tensors and the convs must outlive the chain; calling it runs every step on the
+    current torch stream."""
+
+    def __init__(self, steps):
+        self._keep = [tuple(st) for st in steps]
+        items = []
+        for st in self._keep:
+            conv, x, y = st[0], st[1], st[2]
+            r = st[3] if len(st) > 3 else None
+            items.append((conv.handle, x.data_ptr(), None if r is None else r.data_ptr(), y.data_ptr()))
+        self.handle = conv_fused_chain_create(items)
+
+    def describe(self) -> str:
+        return conv_fused_chain_describe(self.handle)
+
+    def __call__(self, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+        conv_fused_chain_run(self.handle, s)
+
+    def status(self) -> int:
+        return conv_fused_chain_status(self.handle)
+
+    def clear_status(self):
+        conv_fused_chain_clear_status(self.handle)
+
+    def close(self):
+        if self.handle:
+            conv_fused_chain_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -28,7 +28,8 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxe
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
 UNITS = [("api.cu", []), ("k_depthwise.cu", []), ("k_int8.cu", []), ("k_watchdog.cu", []), ("k_pad.cu", []),
-         ("tc_window.cu", []), ("tc_halo.cu", []), ("k_mbblock.cu", [])] + [
+         ("tc_window.cu", []), ("tc_halo.cu", []), ("k_mbblock.cu", []), ("chain.cu", []),
+         ("tc_chain.cu", [])] + [
     ("tc_conv_inst.cu", [f"-DCONVF_BN={bn}"]) for bn in (32, 64, 128, 256)]
 
 

@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "../../include/conv_fused.h"
+#include "api_internal.h"
 #include "convf_internal.h"
 
 namespace convf {
@@ -579,13 +580,6 @@ int gather_cpt(const Shape& s) {
 }
 
 // ------------------------------------------------------------------ driver entry points
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode_tiled = nullptr;
 EncodeIm2colFn g_encode_im2col = nullptr;
 std::once_flag g_encode_once;
@@ -2173,3 +2167,57 @@ extern "C" convf_status conv_fused_run_noalloc(const convf_desc* desc, const voi
   if (ce != cudaSuccess) return fail(CONVF_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return ok();
 }
+
+// ====================================================================== services for chain.cu
+namespace convf {
+
+convf_status record_error(convf_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+convf_status record_ok() { return ok(); }
+bool take_injected_alloc_failure() { return injected_alloc_failure(); }
+
+bool tensor_map_encoders(EncodeTiledFn* tiled, EncodeIm2colFn* im2col) {
+  if (!load_encoders()) return false;
+  *tiled = g_encode_tiled;
+  *im2col = g_encode_im2col;
+  return true;
+}
+
+convf_status chain_conv_info(const convf_handle* h, ChainConvInfo* o) {
+  convf_status st = check_handle(h);
+  if (st != CONVF_OK) return st;
+  if (h->variant != CONVF_VARIANT_GEMM_1X1 && h->variant != CONVF_VARIANT_IMPLICIT_GEMM)
+    return fail(CONVF_ERR_UNSUPPORTED, "variant %d is not a tcgen05 1x1-GEMM or im2col implicit-GEMM conv",
+                h->variant);
+  if (h->desc.dtype != CONVF_BF16) return fail(CONVF_ERR_UNSUPPORTED, "only bf16 convs can be chain steps");
+  if (h->desc.group != 1) return fail(CONVF_ERR_UNSUPPORTED, "grouped convs (group %d) cannot be chain steps", h->desc.group);
+  if (h->preact) return fail(CONVF_ERR_UNSUPPORTED, "convs with a pre-activation prologue cannot be chain steps");
+  const Shape& s = h->s;
+  o->variant = h->variant;
+  o->a_mode = h->a_mode;
+  o->cblocks = h->cblocks;
+  o->ktot = h->ktot;
+  o->num_kb = h->ktot / 64;
+  o->N = s.N; o->C = s.C; o->H = s.H; o->W = s.W; o->K = s.K; o->R = s.R; o->S = s.S;
+  o->sh = s.sh; o->sw = s.sw; o->dh = s.dh; o->dw = s.dw;
+  o->pt = s.pt; o->pl = s.pl; o->pb = s.pb; o->pr = s.pr;
+  o->Ho = s.Ho; o->Wo = s.Wo; o->M = s.M;
+  o->w = h->w_bf16;
+  o->scale = h->scale;
+  o->bias = h->bias;
+  o->lo = h->lo;
+  o->hi = h->hi;
+  o->out_bf16 = h->out_bf16;
+  o->has_res = h->has_res;
+  o->device = h->device;
+  return CONVF_OK;
+}
+
+}  // namespace convf

@@ -330,4 +330,46 @@ cudaError_t measure_s8_mma_rate(int num_sms, cudaStream_t stream, double* tops);
 // ---------------------------------------------------------------- watchdog self-test
 cudaError_t launch_watchdog_selftest(int32_t* status, long long budget, cudaStream_t stream);
 
+// ---------------------------------------------------------------- conv chain (tc_chain.cu)
+// A sequence of tcgen05 convs (1x1-GEMM or im2col implicit-GEMM steps) run by one persistent
+// launch.  Output tiles of 128 rows x bn channels are numbered step after step (row blocks
+// major within a step); CTA b takes tiles b, b + grid, b + 2*grid, ...  A tile whose input (or
+// residual) is an earlier step's output first waits until the 128-row blocks of that output it
+// reads are complete: every 128-row block of every step has a counter, raised by one when one of
+// the block's tiles has been stored and made visible (kChainArrivals per tile).  In launch e
+// (0, 1, ...) a block is complete when its counter reaches (e + 1) * kChainArrivals * n_blocks
+// of its step: the counters only grow, so no launch has to clear them.
+constexpr int kChainArrivals = 1;
+struct ChainStep {   // (aligned as its tensor maps)
+  CUtensorMap tmA;           // activations: 2-D {C, M} box {64, 128}; 3-D {64, M, C/64} box
+                             // {64, 128, 2} (a3d); or im2col {C, W, H, N}, 128 pixels x 64 channels
+  CUtensorMap tmB;           // weights: 3-D {64, K, num_kb} box {64, bn, 2} over [K][num_kb * 64]
+  int a_mode, a3d;           // AMode (kA2D or kAIm2col); a3d: one box per two k-blocks (2-D mode)
+  int M, Kout, C, H, W, Ho, Wo, R, S, sh, sw, pt, pl, dh, dw;
+  int cblocks, num_kb, bn, n_blocks, mtiles;
+  int tile0, tile_end;       // this step's tiles [tile0, tile_end) in the launch-wide numbering
+  uint32_t idesc;            // tcgen05 instruction descriptor: 128 x bn, bf16 inputs, fp32 sums
+  float lo, hi;              // activation clamp
+  const float* scale;        // [>= n_blocks * bn] epilogue scale (folded BN)
+  const float* bias;         // [>= n_blocks * bn] epilogue bias
+  const void* x;             // NHWC bf16 input [N][H][W][C] (the activation map's tensor)
+  void* y;                   // NHWC [M][Kout], fp32 or bf16 bits (the chain's output type)
+  const void* res;           // residual of y's type and shape added before the clamp, or null
+  int src;                   // step whose y is this step's x, or -1 (x is written by no step)
+  int rsrc;                  // step whose y is this step's residual, or -1
+  uint32_t* done;            // [mtiles] arrival counters of this step's 128-row blocks
+};
+struct ChainParams {
+  const ChainStep* steps;    // device array [nsteps]
+  int nsteps, total_tiles;
+  uint32_t* counters;        // every step's done[] array, total_mtiles words in all
+  int total_mtiles;
+  uint32_t* state;           // [0] launches completed so far (the epoch), [1] CTAs done this launch
+  int* status;               // device status word (timeout / bounds bits), sticky
+};
+// out_bf16: y and the residuals hold bf16 (else fp32).  grid <= co-resident CTAs (one per SM).
+cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, int grid, cudaStream_t stream);
+// CTAs of the chain kernel that fit one SM at a time (1 on sm_103a; 0 if it cannot run)
+int tc_chain_blocks_per_sm(bool out_bf16);
+
 }  // namespace convf

@@ -1,0 +1,602 @@
+// Conv chain: a sequence of tcgen05 convolutions (1x1 GEMM or im2col implicit GEMM) in one
+// persistent launch.
+//
+// Each step is the same fused operation as one run of the tcgen05 kernel (implicit GEMM with
+// the folded BN + bias + clamp epilogue, "tensorforge", section "ResNet fusion"; an optional
+// residual added before the clamp, "Kyanite" README, section "Cuda Executor"), but the steps
+// share one launch: the per-launch costs of a short layer (CTA start, TMEM allocation, the
+// first operands' latency, the last tiles' epilogue while other SMs idle) are paid once for
+// the whole sequence, and a step's first tiles start while the previous step's last tiles are
+// still in flight.  A step that reads an earlier step's output waits only for the 128-row
+// blocks it reads (ChainStep::done), so a network's layers pipeline through the GPU.
+//
+// Warp roles (one CTA per SM, tiles b, b + grid, ... of the launch-wide numbering):
+//   warp 0      activation producer: the dependency wait of each tile, then TMA activation
+//               loads (even k-blocks of a step; both, as one box, in the 3-D 1x1 mode)
+//   warp 1      TMEM allocation + single-thread tcgen05.mma issue into two 128-column fp32
+//               accumulators
+//   warp 2      weight producer: one TMA box per pipeline step (two k-blocks) plus the odd
+//               k-block's activation load (its own dependency wait first)
+//   warps 3-10  epilogue, two warpgroups on the two column halves of every tile:
+//               tcgen05.ld -> smem transpose -> clamp(scale*acc + bias (+ r)) -> 16-byte stores
+//   warp 11     publisher: per stored tile, a gpu-scope fence and the increment of the tile's
+//               row-block counter (off the epilogue warps' path)
+// Pipeline: 3 steps of two 64-wide k-blocks each in shared memory (a step's odd k-block is
+// zero fill past a step's last block).
+#include <cuda_bf16.h>
+
+#include "convf_internal.h"
+#include "ptx.cuh"
+
+namespace convf {
+namespace {
+
+constexpr int kQM = 128;                    // tile rows
+constexpr int kQK = 64;                     // reduction block
+constexpr int kQBNMax = 128;                // widest tile (TMEM buffer stride)
+constexpr int kQSlots = 6;                  // k-block slots
+constexpr int kQSteps = kQSlots / 2;        // pipeline steps of two k-blocks
+constexpr int kQATile = kQM * kQK * 2;      // 16 KB
+constexpr int kQBTile = kQBNMax * kQK * 2;  // 16 KB
+constexpr int kQEpiWarpBytes = 32 * 32 * 4;
+constexpr int kQThreads = 96 + 256 + 32;     // producer, MMA, weight producer, 8 epilogue warps, publisher
+constexpr int kQPub = 4;                    // tiles a CTA may have stored but not yet published
+constexpr int kQSmem = 1024 + kQSlots * (kQATile + kQBTile) + 8 * kQEpiWarpBytes + 256;
+static_assert(kQSmem <= 232448, "shared memory budget");
+static_assert(kChainArrivals == 1, "one arrival per tile (the publisher's)");
+
+// Wait until the counter reaches `target` (wrap-safe).  Gives up, raising the CTA's abort flag,
+// when another role of this CTA aborted, when any CTA flagged an error in the status word, or
+// after the watchdog budget (then the timeout bit is set).
+__device__ bool chain_wait(const uint32_t* ctr, uint32_t target, int* status, volatile int* abort_flag) {
+  if (static_cast<int>(ld_acquire_gpu_u32(ctr) - target) >= 0) return true;
+  const long long t0 = clock64();
+  uint32_t ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+    if (static_cast<int>(ld_acquire_gpu_u32(ctr) - target) >= 0) return true;
+    if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+      *abort_flag = 1;
+      return false;
+    }
+    if (clock64() - t0 > kWatchdogCycles) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Input pixels (flat NHWC row indices of the step's x, which are the producing step's output
+// rows) that the tile of output rows [m0, m0 + 128) reads: whole input rows, conservatively.
+__device__ __forceinline__ void chain_input_rows(const ChainStep& s, int m0, int& lo, int& hi) {
+  const int m1 = min(m0 + kQM, s.M) - 1;
+  if (s.a_mode == kA2D) {
+    lo = m0;
+    hi = m1;
+    return;
+  }
+  const int hw = s.Ho * s.Wo;
+  const int i0 = m0 / hw, i1 = m1 / hw;
+  const int oh0 = (m0 - i0 * hw) / s.Wo, oh1 = (m1 - i1 * hw) / s.Wo;
+  const int h0 = min(max(0, oh0 * s.sh - s.pt), s.H - 1);
+  const int h1 = max(min(s.H - 1, oh1 * s.sh - s.pt + (s.R - 1) * s.dh), 0);
+  lo = (i0 * s.H + h0) * s.W;
+  hi = (i1 * s.H + h1) * s.W + s.W - 1;
+}
+
+// Walks the launch-wide tile numbering in increasing order, keeping the step that holds it.
+struct ChainCursor {
+  const ChainStep* steps;
+  int L, end;
+  __device__ explicit ChainCursor(const ChainStep* s) : steps(s), L(0), end(s[0].tile_end) {}
+  __device__ int at(int t) {
+    while (t >= end) end = steps[++L].tile_end;
+    return L;
+  }
+};
+
+// filter tap (r, s) and channel block of a k-block (im2col mode), stepped one block at a time
+struct ChainKPos {
+  int r, s, cb;
+  __device__ void next(int cblocks, int S) {
+    if (++cb == cblocks) {
+      cb = 0;
+      if (++s == S) {
+        s = 0;
+        ++r;
+      }
+    }
+  }
+};
+
+// Producer roles.  ROLE 0 (warp 0): activation loads of the even k-blocks (both k-blocks as one
+// box in the 3-D mode).  ROLE 2 (warp 2): the weight box of each step and the odd k-block's
+// activation load.  Each waits for the tile's input rows before its first activation load.
+template <int ROLE>
+__device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
+                               uint32_t epoch1, volatile int* abort_flag) {
+  const ChainStep* steps = p.steps;
+  ChainCursor cur(steps);
+  int stage = 0;
+  uint32_t phase = 0;
+  int dep_step = -1, dep_done = -1;   // row blocks of the source verified for step dep_step
+  int last = -1;
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    const int L = cur.at(t);
+    const ChainStep& s = steps[L];
+    if (L != last) {
+      last = L;
+      if (ROLE == 0 || !s.a3d) tma_prefetch_desc(&s.tmA);
+      if (ROLE == 2) tma_prefetch_desc(&s.tmB);
+    }
+    const int local = t - s.tile0;
+    const int mt = local / s.n_blocks;
+    const int n0 = (local - mt * s.n_blocks) * s.bn;
+    const int m0 = mt * kQM;
+    const bool loads_a = ROLE == 0 || !s.a3d;
+    if (loads_a && s.src >= 0) {
+      int lo, hi;
+      chain_input_rows(s, m0, lo, hi);
+      const ChainStep& ps = steps[s.src];
+      const uint32_t target = epoch1 * static_cast<uint32_t>(kChainArrivals * ps.n_blocks);
+      if (L != dep_step) {
+        dep_step = L;
+        dep_done = -1;
+      }
+      // this CTA's tiles of one step visit increasing rows, so the blocks below dep_done that
+      // the range still covers were verified for an earlier tile
+      for (int b = max(lo / kQM, dep_done + 1); b <= hi / kQM; ++b)
+        if (!chain_wait(ps.done + b, target, p.status, abort_flag)) return;
+      dep_done = max(dep_done, hi / kQM);
+      fence_proxy_async_global();   // the source's generic stores before this thread's TMA reads
+    }
+    int img = 0, hb = 0, wb = 0;
+    if (s.a_mode == kAIm2col) {
+      const int hw = s.Ho * s.Wo;
+      img = m0 / hw;
+      const int rem = m0 - img * hw;
+      const int oh = rem / s.Wo;
+      hb = oh * s.sh - s.pt;
+      wb = (rem - oh * s.Wo) * s.sw - s.pl;
+    }
+    // the step's fields the loop needs, in registers (the issuing thread's scalar work delays
+    // its next copy)
+    const int num_kb = s.num_kb, cbl = s.cblocks, Sl = s.S, dwl = s.dw, dhl = s.dh;
+    const bool a3d = s.a3d != 0, a2d = s.a_mode == kA2D;
+    const CUtensorMap* tmA = &s.tmA;
+    const CUtensorMap* tmB = &s.tmB;
+    // the weight box holds two k-blocks (zero fill past the last), one if the step has one
+    const uint32_t b_bytes = static_cast<uint32_t>((num_kb > 1 ? 2 : 1) * s.bn * kQK * 2);
+    ChainKPos q{0, 0, 0};
+    for (int kb = 0; kb < num_kb; kb += 2) {
+      const bool two = kb + 1 < num_kb;
+      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) return;
+      uint8_t* a0 = sA + stage * 2 * kQATile;
+      ChainKPos q1 = q;   // k-block kb + 1
+      q1.next(cbl, Sl);
+      if (ROLE == 0) {
+        if (a3d) {
+          mbar_arrive_expect_tx(&full[stage], 2 * kQATile);
+          tma_load_3d(a0, tmA, &full[stage], 0, m0, kb);
+        } else {
+          mbar_arrive_expect_tx(&full[stage], kQATile);
+          if (a2d)
+            tma_load_2d(a0, tmA, &full[stage], kb * kQK, m0);
+          else
+            tma_load_im2col_4d(a0, tmA, &full[stage], q.cb * kQK, wb, hb, img, static_cast<uint16_t>(q.s * dwl),
+                               static_cast<uint16_t>(q.r * dhl));
+        }
+      } else {
+        const bool odd_a = !a3d && two;
+        mbar_arrive_expect_tx(&full[stage], b_bytes + (odd_a ? kQATile : 0u));
+        tma_load_3d(sB + stage * 2 * kQBTile, tmB, &full[stage], 0, n0, kb);
+        if (odd_a) {
+          if (a2d)
+            tma_load_2d(a0 + kQATile, tmA, &full[stage], (kb + 1) * kQK, m0);
+          else
+            tma_load_im2col_4d(a0 + kQATile, tmA, &full[stage], q1.cb * kQK, wb, hb, img,
+                               static_cast<uint16_t>(q1.s * dwl), static_cast<uint16_t>(q1.r * dhl));
+        }
+      }
+      q = q1;
+      q.next(cbl, Sl);
+      if (++stage == kQSteps) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  }
+}
+
+// MMA issuer (one thread): per tile, one 128 x bn accumulator buffer (alternating), four
+// K = 16 MMAs per k-block.
+__device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
+                          uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
+  const ChainStep* steps = p.steps;
+  ChainCursor cur(steps);
+  const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(sA));
+  const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(sB));
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    const ChainStep& s = steps[cur.at(t)];
+    const uint32_t idesc = s.idesc;
+    const int num_kb = s.num_kb;
+    const uint32_t bblock = static_cast<uint32_t>(s.bn * kQK * 2);   // bytes of one k-block's weights
+    if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) return;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kQBNMax);
+    for (int kb = 0; kb < num_kb; kb += 2) {
+      if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) return;
+      tc_fence_after();
+      const int nk = kb + 1 < num_kb ? 2 : 1;
+      for (int j = 0; j < nk; ++j) {
+        const uint64_t adesc = adesc0 + (static_cast<uint32_t>((stage * 2 + j) * kQATile) >> 4);
+        const uint64_t bdesc = bdesc0 + ((static_cast<uint32_t>(stage * 2 * kQBTile) + j * bblock) >> 4);
+#pragma unroll
+        for (int k = 0; k < kQK / 16; ++k)
+          tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j > 0 || k > 0) ? 1u : 0u);
+      }
+      tc_commit(&empty[stage]);
+      if (++stage == kQSteps) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    tc_commit(&tfull[acc]);
+    if (++acc == 2) {
+      acc = 0;
+      acc_phase ^= 1;
+    }
+  }
+}
+
+// Epilogue warp (two warpgroups; group eg drains columns [eg*bn/2, (eg+1)*bn/2) of every tile,
+// the warp its TMEM lane quadrant q = rows 32q..32q+31).  Per 32-column chunk: tcgen05.ld ->
+// this warp's 4 KB of smem (thread = row) -> read back as thread = (row, 4 or 8 channels) ->
+// clamp(scale*acc + bias (+ r)) -> 16-byte stores.  After a tile's stores the warp arrives on the
+// tile's publication barrier (stored[j % kQPub] for the CTA's j-th tile) and moves on: the
+// publisher warp makes the stores visible at gpu scope and raises the row-block counter, so no
+// epilogue warp waits for its stores to reach L2.
+template <bool OUT_BF16>
+__device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tfull, uint64_t* tempty,
+                               uint64_t* stored, uint64_t* pubfree, uint32_t tmem_base, uint32_t epoch1,
+                               volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int eg = (warp - 3) >> 2;
+  const int q = warp & 3;   // TMEM lane quadrant this warp may access
+  float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kQEpiWarpBytes);
+  const ChainStep* steps = p.steps;
+  ChainCursor cur(steps);
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  int j = 0;   // tiles of this CTA so far
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
+    const ChainStep& s = steps[cur.at(t)];
+    const int local = t - s.tile0;
+    const int mt = local / s.n_blocks;
+    const int n0 = (local - mt * s.n_blocks) * s.bn;
+    const int row0 = mt * kQM + q * 32;
+    const int M = s.M, Kout = s.Kout;
+    const float lo = s.lo, hi = s.hi;
+    const float* scale = s.scale;
+    const float* bias = s.bias;
+    const int half = s.bn >> 1;
+    const int nch = half >> 5;
+    const void* res = s.res;
+    const int rsrc = s.rsrc;
+    [[maybe_unused]] const size_t total = static_cast<size_t>(M) * Kout;   // (bounds-checking build)
+    if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) return;
+    tc_fence_after();
+    if (res != nullptr && rsrc >= 0) {
+      // the residual rows of this tile are the producing step's row block mt (same shape)
+      int ok = 1;
+      if (lane == 0) {
+        const ChainStep& rs = steps[rsrc];
+        ok = chain_wait(rs.done + mt, epoch1 * static_cast<uint32_t>(kChainArrivals * rs.n_blocks), p.status,
+                        abort_flag);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+    for (int c = 0; c < nch; ++c) {
+      const int tcol = eg * half + c * 32;   // tile column of this chunk
+      const int col0 = n0 + tcol;
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kQBNMax + tcol), v);
+      if constexpr (OUT_BF16) {
+        // thread = (rows 8i + sub8, channels col .. col + 7): 16-byte residual loads and stores;
+        // the epilogue vectors and the residual are in flight while the accumulator is read
+        const int sub8 = lane >> 2, c8 = lane & 3;
+        const int col = col0 + 8 * c8;
+        const bool col_ok = col < Kout;   // Kout % 8 == 0: whole 8-channel groups
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, b0 = s0, b1 = s0;
+        if (col_ok) {
+          s0 = __ldg(reinterpret_cast<const float4*>(scale + col));
+          s1 = __ldg(reinterpret_cast<const float4*>(scale + col + 4));
+          b0 = __ldg(reinterpret_cast<const float4*>(bias + col));
+          b1 = __ldg(reinterpret_cast<const float4*>(bias + col + 4));
+        }
+        uint4 rv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          rv[i] = make_uint4(0u, 0u, 0u, 0u);
+          const int r = row0 + 8 * i + sub8;
+          const size_t e = static_cast<size_t>(r) * Kout + col;
+          // written by an earlier step of this launch: read through L2 (not the read-only path)
+          if (res != nullptr && col_ok && r < M && CONVF_IN_BOUNDS(e + 8 <= total, p.status))
+            rv[i] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(res) + e));
+        }
+        tmem_ld_wait();
+        if (c == nch - 1) {
+          // the warp's last TMEM read of the tile: release the buffer to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<float4*>(wst + lane * 32 + ((cc ^ (lane & 7)) << 2)) =
+              make_float4(__uint_as_float(v[4 * cc]), __uint_as_float(v[4 * cc + 1]), __uint_as_float(v[4 * cc + 2]),
+                          __uint_as_float(v[4 * cc + 3]));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 8 * i + sub8;
+          const int r = row0 + rr;
+          const float4 x0 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8) ^ (rr & 7)) << 2));
+          const float4 x1 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8 + 1) ^ (rr & 7)) << 2));
+          if (!col_ok || r >= M) continue;
+          const float o[8] = {fmaf(x0.x, s0.x, b0.x), fmaf(x0.y, s0.y, b0.y), fmaf(x0.z, s0.z, b0.z),
+                              fmaf(x0.w, s0.w, b0.w), fmaf(x1.x, s1.x, b1.x), fmaf(x1.y, s1.y, b1.y),
+                              fmaf(x1.z, s1.z, b1.z), fmaf(x1.w, s1.w, b1.w)};
+          const uint32_t rw[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // residual (zero bits when there is none) before the clamp, then RNE to bf16
+            const float a0 = fminf(fmaxf(o[2 * j] + __uint_as_float(rw[j] << 16), lo), hi);
+            const float a1 = fminf(fmaxf(o[2 * j + 1] + __uint_as_float(rw[j] & 0xffff0000u), lo), hi);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+            pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          const size_t e = static_cast<size_t>(r) * Kout + col;
+          if (CONVF_IN_BOUNDS(e + 8 <= total, p.status))
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.y) + e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      } else {
+        // thread = (rows 4i + sub, channels col .. col + 3)
+        const int sub = lane >> 3, c4 = lane & 7;
+        const int col = col0 + 4 * c4;
+        const bool col_ok = col < Kout;   // Kout % 4 == 0
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bi = sc;
+        if (col_ok) {
+          sc = __ldg(reinterpret_cast<const float4*>(scale + col));
+          bi = __ldg(reinterpret_cast<const float4*>(bias + col));
+        }
+        tmem_ld_wait();
+        if (c == nch - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<float4*>(wst + lane * 32 + ((cc ^ (lane & 7)) << 2)) =
+              make_float4(__uint_as_float(v[4 * cc]), __uint_as_float(v[4 * cc + 1]), __uint_as_float(v[4 * cc + 2]),
+                          __uint_as_float(v[4 * cc + 3]));
+        __syncwarp();
+        float4 rv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int r = row0 + 4 * i + sub;
+          const size_t e = static_cast<size_t>(r) * Kout + col;
+          if (res != nullptr && col_ok && r < M && CONVF_IN_BOUNDS(e + 4 <= total, p.status))
+            rv[i] = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(res) + e));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + sub;
+          const int r = row0 + rr;
+          const float4 a = *reinterpret_cast<const float4*>(wst + rr * 32 + ((c4 ^ (rr & 7)) << 2));
+          if (!col_ok || r >= M) continue;
+          const float4 o = make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x) + rv[i].x, lo), hi),
+                                       fminf(fmaxf(fmaf(a.y, sc.y, bi.y) + rv[i].y, lo), hi),
+                                       fminf(fmaxf(fmaf(a.z, sc.z, bi.z) + rv[i].z, lo), hi),
+                                       fminf(fmaxf(fmaf(a.w, sc.w, bi.w) + rv[i].w, lo), hi));
+          const size_t e = static_cast<size_t>(r) * Kout + col;
+          if (CONVF_IN_BOUNDS(e + 4 <= total, p.status)) *reinterpret_cast<float4*>(static_cast<float*>(s.y) + e) = o;
+        }
+      }
+      __syncwarp();   // the chunk's smem reads are done before the next chunk is written
+    }
+    // the tile is stored: hand it to the publisher (once it has taken the slot's previous tile)
+    __syncwarp();
+    if (lane == 0) {
+      const int slot = j % kQPub;
+      bool ok = j < kQPub || mbar_wait(&pubfree[slot], static_cast<uint32_t>((j / kQPub - 1) & 1), abort_flag, p.status);
+      if (ok) mbar_arrive(&stored[slot]);
+    }
+    if (++acc == 2) {
+      acc = 0;
+      acc_phase ^= 1;
+    }
+  }
+}
+
+// Publisher (one thread): for each of the CTA's tiles in order, once all eight epilogue warps
+// have arrived (their stores ordered before their arrivals), a gpu-scope fence makes those
+// stores visible -- the fence is cumulative over what the barrier let this thread observe -- and
+// the tile's row-block counter is raised by one.
+__device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t* pubfree, volatile int* abort_flag) {
+  const ChainStep* steps = p.steps;
+  ChainCursor cur(steps);
+  int j = 0;
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
+    const ChainStep& s = steps[cur.at(t)];
+    const int mt = (t - s.tile0) / s.n_blocks;
+    const int slot = j % kQPub;
+    if (!mbar_wait(&stored[slot], static_cast<uint32_t>((j / kQPub) & 1), abort_flag, p.status)) return;
+    fence_acq_rel_gpu();
+    fence_proxy_async_global();   // ... and ordered before later async-proxy (TMA) reads of them
+    red_relaxed_gpu_add(s.done + mt, 1u);
+    mbar_arrive(&pubfree[slot]);
+  }
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kQSlots * kQATile;
+  uint8_t* sEpi = sB + kQSlots * kQBTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 8 * kQEpiWarpBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kQSteps;
+  uint64_t* tfull = bars + 2 * kQSteps;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* stored = tempty + 2;       // [kQPub] a tile's stores are done (eight epilogue warps)
+  uint64_t* pubfree = stored + kQPub;  // [kQPub] the publisher has taken the slot's tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pubfree + kQPub);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* epoch_slot = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQSteps; ++s) {
+      mbar_init(&full[s], 2);    // activation producer + weight producer
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);  // every epilogue warp
+    }
+    for (int b = 0; b < kQPub; ++b) {
+      mbar_init(&stored[b], 8);  // every epilogue warp
+      mbar_init(&pubfree[b], 1); // the publisher
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * kQBNMax);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // the next kernel may launch once every CTA of this grid has started (so none of this
+  // grid's CTAs can be kept from an SM by it: the CTAs wait for one another's tiles)
+  pdl_launch_dependents();
+  // The first tile's operands start towards L2 behind the previous kernel's tail: its weight
+  // boxes, and its input rows when no step of this chain writes them (a prefetch reads no stale
+  // data: whatever the previous kernel still writes lands in L2, which serves every read after
+  // the wait).
+  if (lane == 0 && (warp == 0 || warp == 2)) {
+    const int t = blockIdx.x;
+    int L = 0;
+    while (t >= p.steps[L].tile_end) ++L;
+    const ChainStep& s = p.steps[L];
+    const int local = t - s.tile0;
+    const int mt = local / s.n_blocks;
+    if (warp == 2) {
+      tma_prefetch_desc(&s.tmB);
+      for (int kb = 0; kb < min(s.num_kb, 4); kb += 2) tma_prefetch_l2_3d(&s.tmB, 0, (local - mt * s.n_blocks) * s.bn, kb);
+    } else if (s.src < 0) {
+      tma_prefetch_desc(&s.tmA);
+      int lo, hi;
+      chain_input_rows(s, mt * kQM, lo, hi);
+      bulk_prefetch_l2(static_cast<const uint16_t*>(s.x) + static_cast<size_t>(lo) * s.C,
+                       static_cast<uint32_t>(hi - lo + 1) * s.C * 2);
+    }
+  }
+  pdl_wait_prior();
+  if (threadIdx.x == 0) *epoch_slot = *reinterpret_cast<volatile uint32_t*>(p.state);
+  __syncthreads();
+  const uint32_t epoch1 = *epoch_slot + 1u;
+
+  if (warp == 0) {
+    if (lane == 0) chain_producer<0>(p, sA, sB, full, empty, epoch1, abort_flag);
+  } else if (warp == 2) {
+    if (lane == 0) chain_producer<2>(p, sA, sB, full, empty, epoch1, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) chain_mma(p, sA, sB, full, empty, tfull, tempty, tmem_base, abort_flag);
+  } else if (warp == 11) {
+    if (lane == 0) chain_publisher(p, stored, pubfree, abort_flag);
+  } else {
+    chain_epilogue<OUT_BF16>(p, sEpi, tfull, tempty, stored, pubfree, tmem_base, epoch1, abort_flag);
+  }
+
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // a wait ran out: give copies and MMAs already in flight time to land before TMEM is freed
+    for (int i = 0; i < 2000; ++i) __nanosleep(100000);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * kQBNMax);
+  }
+  if (threadIdx.x == 0) {
+    // the last CTA out advances the epoch (or, after an error, restarts the counters at zero)
+    __threadfence();
+    const uint32_t prev = atomicAdd(p.state + 1, 1u);
+    if (prev == gridDim.x - 1) {
+      __threadfence();
+      if (*reinterpret_cast<volatile int*>(p.status) != 0) {
+        for (int i = 0; i < p.total_mtiles; ++i) p.counters[i] = 0u;
+        p.state[0] = 0u;
+      } else {
+        p.state[0] = epoch1;
+      }
+      p.state[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+template <bool OUT_BF16>
+cudaError_t chain_configure() {
+  static cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel<OUT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              kQSmem);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, int grid, cudaStream_t stream) {
+  if (out_bf16) {
+    cudaError_t e = chain_configure<true>();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc_chain_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, stream, 1, p);
+  }
+  cudaError_t e = chain_configure<false>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tc_chain_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, stream, 1, p);
+}
+
+int tc_chain_blocks_per_sm(bool out_bf16) {
+  int n = 0;
+  cudaError_t e;
+  if (out_bf16) {
+    e = chain_configure<true>();
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_chain_kernel<true>, kQThreads, kQSmem);
+  } else {
+    e = chain_configure<false>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_chain_kernel<false>, kQThreads, kQSmem);
+  }
+  return e == cudaSuccess ? n : 0;
+}
+
+}  // namespace convf

@@ -372,6 +372,64 @@ convf_status conv_fused_run_noalloc(const convf_desc* desc, const void* x, const
                                     const float* scale, const float* bias, void* y,
                                     int32_t* status_dev, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Conv chain: a sequence of conv runs executed by ONE persistent kernel launch.
+ *
+ * The steps compute exactly what conv_fused_run / conv_fused_run_residual would compute if they
+ * were called one after another on one stream, with the same per-element arithmetic (fp32
+ * accumulation of bf16 products, y = clamp(scale*acc + bias' (+ r), lo, hi), fp32 output or
+ * bf16 rounded to nearest even).  A network's layers are short: a launch per layer pays the
+ * kernel's start-up, its first operands' latency and its last tiles' epilogue (while other SMs
+ * idle) every time.  A chain pays them once and lets a step's first tiles start while the
+ * previous step's last ones are still running.
+ *
+ * Dependencies are taken from buffer identity: when a step's x (or residual) is exactly an
+ * earlier step's y (same device pointer, same size and shape), the step reads that output, and
+ * each of its 128-row output tiles waits (inside the kernel, bounded) only until the rows it
+ * reads have been stored.  Every other x or residual is an input of the chain that no step
+ * writes.  Refused (CONVF_ERR_UNSUPPORTED, named) at create: a step's x or residual partially
+ * overlapping an output; a step reading an output that the same or a later step writes; two
+ * steps writing overlapping outputs; an fp32 output read as a bf16 input.
+ *
+ * Steps: handles of CONVF_VARIANT_GEMM_1X1 or CONVF_VARIANT_IMPLICIT_GEMM (force the variant in
+ * the desc if the selector would pick another), bf16, group 1, no pre-activation; C and K
+ * multiples of 8; every step's output type the same (all fp32 or all bf16).  The chain chooses
+ * its own tile width per step (128 x 64 for K <= 64, else 128 x 128) and ignores the handles'
+ * performance knobs.  The handles must outlive the chain (it reads their prepacked weights);
+ * the buffers are fixed at create (the tensor maps are encoded for them).
+ *
+ * The chain's CTAs wait for one another's tiles, so they must all be resident at once: the
+ * launch uses at most one CTA per SM.  A wait that runs out (or any error bit in the chain's
+ * status word) makes every CTA give up; conv_fused_chain_status then reports it, and runs
+ * after that give up at once until conv_fused_chain_clear_status.
+ */
+typedef struct convf_chain convf_chain;
+typedef struct {
+  convf_handle* conv;   /* the step's conv (see above)                                            */
+  const void* x;        /* device NHWC bf16 input, 16-byte aligned                                */
+  const void* r;        /* device residual of y's type and shape (handle created with residual =
+                           1), else NULL                                                         */
+  void* y;              /* device NHWC output, 16-byte aligned                                    */
+} convf_chain_step;
+
+/* Validates the n steps (host array, copied), finds their dependencies, encodes their tensor
+ * maps and uploads the step table (one device allocation; synchronises the device once). */
+convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf_chain** out);
+/* One launch of the whole sequence on `stream` (a cudaStream_t, NULL = legacy default stream).
+ * Asynchronous; allocates nothing; may be captured in a CUDA graph.  Runs of one chain must not
+ * overlap in time (use one stream). */
+convf_status conv_fused_chain_run(convf_chain* c, void* stream);
+/* Device status of earlier runs (read after the caller synchronised): CONVF_OK, CONVF_ERR_TIMEOUT
+ * or (bounds-checking build) CONVF_ERR_BOUNDS; sticky until conv_fused_chain_clear_status. */
+convf_status conv_fused_chain_status(convf_chain* c);
+convf_status conv_fused_chain_clear_status(convf_chain* c);
+/* One line: step count, tiles, grid, and per step its filter, rows, channels, tile width,
+ * reduction blocks and the steps it reads (src = x's producer, res = the residual's; -1 = an
+ * input of the chain). */
+convf_status conv_fused_chain_describe(const convf_chain* c, char* buf, size_t len);
+/* Frees the chain's device memory (the caller must have synchronised); NULL is ignored. */
+void conv_fused_chain_destroy(convf_chain* c);
+
 #ifdef __cplusplus
 }
 #endif
