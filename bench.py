@@ -3,10 +3,13 @@
 A step is one pass of the ResNet-50 (v2) conv stack at batch 32: all 53 conv layers (7x7/2
 stem, 1x1 and 3x3 bottleneck convs, strided projections) with folded BN + ReLU, bf16 inputs,
 fp32 accumulation and output, each layer on its own resident input/output buffers (about
-2.2 GB per step, far larger than L2, so every layer reads its input from HBM).  `value` is
-the whole-job TFLOP/s (2*N*K*Ho*Wo*C*R*S per layer, padded taps included).  The same run
-also times the MobileNetV2 depthwise layers at batch 64 (GB/s against HBM) and the static
-int8 ResNet 3x3 layers at batch 64 (TOP/s), and reports them beside the headline.
+2.2 GB per step, far larger than L2, so every layer reads its input from HBM).  The step runs
+as two launches: the stem (window-mode tcgen05 kernel, with its channel-padding pre-pass) and
+one conv-chain launch holding the 52 other layers (conv_fused_chain_*).  `value` is the
+whole-job TFLOP/s (2*N*K*Ho*Wo*C*R*S per layer, padded taps included).  The same run reports
+the step as 53 per-layer launches, ResNet-50's own dataflow as one dependent chain (bf16
+activations and residuals), the MobileNetV2 depthwise layers at batch 64 (GB/s against HBM),
+the static int8 ResNet 3x3 layers at batch 64 (TOP/s) and the other configurations.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--layers-out F]
 
@@ -34,26 +37,25 @@ WORKLOAD = ("ResNet-50 v2 conv stack, 53 layers (7x7/2 stem, 1x1 and 3x3 bottlen
             "folded BN + ReLU epilogue, channels-last")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of tc_conv_kernel per launch (mean over the 49 tc_conv launches of one ResNet-50
-# pass): dram__bytes_read.sum plus the bytes the SMs wrote into L2 (lts__t_sectors_srcunit_tex_op_write
-# x 32: every one of them reaches DRAM, but ncu flushes the caches around each kernel and
-# dram__bytes_write.sum counts only what was evicted while the kernel ran, 3.12 MB), captured with
-#   python bench.py --profile r50:0,1,...,52
+# DRAM traffic of one tc_chain_kernel launch (the 52-step chain of the step), captured with
+#   python bench.py --profile chain:0
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,lts__t_sectors_srcunit_tex_op_write.sum,
-#       gpu__time_duration.sum --clock-control none -k regex:tc_conv -s 98 -c 49 --csv
-#       python bench.py --profile r50:0,1,...,52
-# It describes the kernel sources it was taken on (SHA-256 prefix of their code with comments
-# and blank space removed) and is reported as null for any other sources.
-TC_TRAFFIC = {"bytes_per_launch": 38.75e6, "read_per_launch": 13.38e6, "write_per_launch": 25.36e6,
-              "dram_write_during_launch": 3.12e6, "sources_sha256_16": "0ebe5ec29b370072"}
-TC_SOURCES = ("tc_conv.cuh", "tc_conv_inst.cu", "ptx.cuh", "convf_internal.h", "api.cu")
+#       gpu__time_duration.sum --clock-control none -k regex:tc_chain -s 2 -c 1 --csv
+#       python bench.py --profile chain:0
+# traffic = dram__bytes_read.sum plus the bytes the SMs wrote into L2 (lts__t_sectors_srcunit_tex_op_write
+# x 32: every one of them reaches DRAM, but ncu flushes the caches around each kernel and
+# dram__bytes_write.sum counts only what was evicted while the kernel ran).  It describes the
+# kernel sources it was taken on (SHA-256 prefix of their code with comments and blank space
+# removed) and is reported as null for any other sources.
+CHAIN_TRAFFIC = None
+CHAIN_SOURCES = ("tc_chain.cu", "chain.cu", "ptx.cuh", "convf_internal.h", "api_internal.h")
 
 
 def sources_digest():
-    """SHA-256 prefix of the conv kernel's sources, comments and blank space removed."""
+    """SHA-256 prefix of the chain kernel's sources, comments and blank space removed."""
     import re
     h = hashlib.sha256()
-    for f in TC_SOURCES:
+    for f in CHAIN_SOURCES:
         with open(os.path.join(ROOT, "convolution_onnx_conv_gb300", "csrc", f)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -62,8 +64,10 @@ def sources_digest():
     return h.hexdigest()[:16]
 
 
-def tc_traffic():
-    return TC_TRAFFIC["bytes_per_launch"] if sources_digest() == TC_TRAFFIC["sources_sha256_16"] else None
+def chain_traffic():
+    if CHAIN_TRAFFIC is None or sources_digest() != CHAIN_TRAFFIC["sources_sha256_16"]:
+        return None
+    return CHAIN_TRAFFIC["bytes_per_launch"]
 
 
 def max_over_ranks(x, world, device):
@@ -219,6 +223,58 @@ def build_ext_layers(specs, layers, torch, cf):
     return out
 
 
+def chain_conv(spec, inp, cf, out_bf16=False, residual=False):
+    """A handle of a kind the conv chain runs: the 1x1-GEMM variant for plain 1x1 convs, the
+    im2col implicit GEMM for every other shape."""
+    scale, shift = cf.conv_bn_scale_shift(*[t.numpy() for t in inp["bn"]], 1e-5) \
+        if inp["bn"] is not None else (None, None)
+    plain = spec.R == 1 and spec.S == 1 and tuple(spec.stride) == (1, 1) and tuple(spec.pads) == (0, 0, 0, 0)
+    return cf.FusedConv(spec.N, spec.C, spec.H, spec.W, spec.K, spec.R, spec.S, inp["w"], inp["bias"], scale, shift,
+                        stride=spec.stride, pads=spec.pads, group=spec.group, act=spec.act,
+                        variant=cf.CONVF_VARIANT_GEMM_1X1 if plain else cf.CONVF_VARIANT_IMPLICIT_GEMM,
+                        out_bf16=out_bf16, residual=residual)
+
+
+def build_chain(layers, cf, convs=None, xs=None, ys=None):
+    """The layers as one chain of independent steps (each on its own input and output buffers:
+    no step reads another's output), with the layers' own buffers unless others are given."""
+    convs = convs or [chain_conv(L["spec"], L["inp"], cf) for L in layers]
+    xs = xs or [L["x"] for L in layers]
+    ys = ys or [L["y"] for L in layers]
+    return cf.ConvChain(list(zip(convs, xs, ys))), convs
+
+
+def build_network_chain(specs, layers, torch, cf, workloads, synthetic):
+    """ResNet-50's own dataflow as one chain: the 52 bottleneck layers in workloads.resnet50_dataflow
+    order, bf16 outputs, each layer reading the output of the layer before it and each block's
+    last 1x1 conv adding the block's shortcut; the input is a seeded N(0,1) bf16 tensor of the
+    stem's pooled output shape (32 x 64 x 56 x 56).  Weights and BN are the step's, with each
+    block's last BN damped (synthetic.residual_branch_inputs)."""
+    g = torch.Generator().manual_seed(7001)
+    x0 = torch.randn((specs[1].N, 64, 56, 56), generator=g).to(torch.bfloat16).contiguous(
+        memory_format=torch.channels_last).cuda()
+    ys, steps, convs = [], [], []
+    for li, src, rsrc in workloads.resnet50_dataflow():
+        # a block's last conv with the damped residual-branch BN (synthetic.residual_branch_inputs)
+        inp = synthetic.residual_branch_inputs(specs[li], synthetic.seed_for(3, li)) if rsrc is not None \
+            else layers[li]["inp"]
+        c = chain_conv(specs[li], inp, cf, out_bf16=True, residual=rsrc is not None)
+        y = c.new_output()
+        x = x0 if src < 0 else ys[src]
+        steps.append((c, x, y) if rsrc is None else (c, x, y, x0 if rsrc < 0 else ys[rsrc]))
+        ys.append(y)
+        convs.append(c)
+    return cf.ConvChain(steps), convs
+
+
+def capture_fn(fn, torch):
+    """One CUDA graph of whatever `fn` launches on the current stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 def capture_graph(layers, torch, reps=1):
     """One CUDA graph that launches every layer of the sequence `reps` times, in order."""
     g = torch.cuda.CUDAGraph()
@@ -307,8 +363,18 @@ def other_configs(args, torch, cf, synthetic, workloads, peaks):
     mv = workloads.mobilenetv2_layers(64)
     ms, Ls = timed(mv, 4)
     pw = [s for s in mv if s.R == 1]
-    ms_pw, _ = timed(pw, 6)
+    ms_pw, Lpw = timed(pw, 6)
     pw_bytes = sum(s.algorithmic_bytes for s in pw)
+    # the same 1x1 layers as one conv-chain launch (independent steps)
+    ch_pw, _ = build_chain(Lpw, cf)
+    ch_pw()
+    g_pw = capture_fn(lambda: ch_pw(), torch)
+    for _ in range(args.warmup):
+        g_pw.replay()
+    torch.cuda.synchronize()
+    ms_pwc = time_graph(g_pw, steps, torch) / steps
+    if ch_pw.status() != 0:
+        raise SystemExit("device status error in the MobileNetV2 1x1 chain")
     out["mobilenetv2_b64"] = {
         "workload": "MobileNetV2 conv stack (17 blocks: 1x1 expand + ReLU6, depthwise 3x3 + ReLU6, 1x1 "
                     "project) at batch 64, bf16 in, fp32 out",
@@ -316,7 +382,12 @@ def other_configs(args, torch, cf, synthetic, workloads, peaks):
         "gb_s": sum(s.algorithmic_bytes for s in mv) / (ms * 1e-3) / 1e9,
         "expand_project_1x1": {"layers": len(pw), "ms": ms_pw, "gb_s": pw_bytes / (ms_pw * 1e-3) / 1e9,
                                "pct_hbm": pw_bytes / (ms_pw * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                               "tflops": sum(s.flops for s in pw) / (ms_pw * 1e-3) / 1e12}}
+                               "tflops": sum(s.flops for s in pw) / (ms_pw * 1e-3) / 1e12,
+                               "execution": "one launch per layer",
+                               "chain": {"ms": ms_pwc, "gb_s": pw_bytes / (ms_pwc * 1e-3) / 1e9,
+                                         "pct_hbm": pw_bytes / (ms_pwc * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                         "tflops": sum(s.flops for s in pw) / (ms_pwc * 1e-3) / 1e12,
+                                         "execution": "the same layers as one conv-chain launch"}}}
     # the same stack as 17 fused inverted-residual blocks (one kernel per block: the expanded
     # tensor never goes to HBM); GB/s against each block's own algorithmic bytes (input, output,
     # weights)
@@ -472,6 +543,24 @@ def profile_layers(which):
     cf.load_library(build_if_missing=True)
     kind, idx = which.split(":")
     idx = [int(i) for i in idx.split(",")]
+    if kind in ("chain", "chainrep"):
+        # chain:0 the step's 52-layer chain, chain:1 ResNet-50's dataflow as one dependent chain,
+        # chainrep:I six independent copies of ResNet-50 layer I (the kernel's steady state on one
+        # shape): three launches, the third the profiled one
+        specs = workloads.resnet50_layers(32)
+        if kind == "chainrep":
+            layers = build_layers([specs[idx[0]]], 3, torch, cf, synthetic)
+            conv = chain_conv(layers[0]["spec"], layers[0]["inp"], cf)
+            ch = cf.ConvChain([(conv, layers[0]["x"], conv.new_output()) for _ in range(6)])
+        else:
+            layers = build_layers(specs, 3, torch, cf, synthetic)
+            ch = build_chain(layers[1:], cf)[0] if idx[0] == 0 else \
+                build_network_chain(specs, layers, torch, cf, workloads, synthetic)[0]
+        for _ in range(3):
+            ch()
+        torch.cuda.synchronize()
+        print(ch.describe().split(" |")[0], "status", ch.status())
+        return
     if kind == "mb":
         # fused MobileNetV2 blocks at batch 64
         blocks = workloads.mobilenetv2_blocks(64)
@@ -529,7 +618,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile", default=None,
-                    help="profiling target instead of the benchmark: 'r50:I,J', 'dw:I', 's8:I', 'q8:I' (QLinearConv), "
+                    help="profiling target instead of the benchmark: 'chain:0' (the step's 52-layer chain), "
+                         "'chain:1' (ResNet-50's dataflow as one chain), 'chainrep:I' (six copies of layer I as one "
+                         "chain), 'r50:I,J', 'dw:I', 's8:I', 'q8:I' (QLinearConv), "
                          "'ext:I' (ResNet-50 layer with bf16 output and, on a block's last 1x1 conv, a bf16 "
                          "residual) or 'mb:I' (fused MobileNetV2 block) runs those layers twice (warm-up) and "
                          "then once more each, printing their kernel descriptions")
@@ -560,32 +651,30 @@ def main():
     peaks, peak_src = load_peaks()
     specs = workloads.resnet50_layers(32)
     layers = build_layers(specs, 3, torch, cf, synthetic)
+    stem = layers[0]
+    chain, chain_convs = build_chain(layers[1:], cf)
     dw_specs = workloads.depthwise_layers(64)
     dw_layers = build_layers(dw_specs, 4, torch, cf, synthetic)
     s8_specs = workloads.int8_layers(64)
     s8_layers = build_layers(s8_specs, 5, torch, cf, synthetic, s8=True)
 
+    def step():
+        stem["conv"](stem["x"], stem["y"])
+        chain()
+
     for _ in range(args.warmup):
+        step()
         for L in layers + dw_layers + s8_layers:
             L["conv"](L["x"], L["y"])
     torch.cuda.synchronize()
-    g_r50 = capture_graph(layers, torch)
+    g_step = capture_fn(step, torch)            # the step: stem + the 52-layer chain
+    g_r50 = capture_graph(layers, torch)        # the same 53 layers as per-layer launches
+    g_chain = capture_fn(lambda: chain(), torch)  # the dominant kernel alone
     g_dw = capture_graph(dw_layers, torch)
     g_s8 = capture_graph(s8_layers, torch)
-    for g in (g_r50, g_dw, g_s8):
+    for g in (g_step, g_r50, g_chain, g_dw, g_s8):
         for _ in range(args.warmup):
             g.replay()
-    torch.cuda.synchronize()
-
-    # dominant kernel: the tcgen05 implicit-GEMM conv (every 1x1 and every strided 3x3 layer; the
-    # halo and window kernels take the other four).  Its time per step is a graph replay of only
-    # its own layers, in step order, on their own resident buffers: a subset of the step, so it
-    # cannot exceed the step's time.
-    tc_idx = [i for i, L in enumerate(layers)
-              if L["conv"].describe().split()[0] in ("variant=gemm_1x1", "variant=implicit_gemm_im2col")]
-    g_tc = capture_graph([layers[i] for i in tc_idx], torch)
-    for _ in range(args.warmup):
-        g_tc.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -593,11 +682,12 @@ def main():
     time.sleep(0.1)
     barrier()
     torch.cuda.synchronize()
-    total_ms = time_graph(g_r50, args.steps, torch)            # the timed region: K steps
+    total_ms = time_graph(g_step, args.steps, torch)           # the timed region: K steps
     torch.cuda.synchronize()
     barrier()
-    tc_steps = max(3, args.steps // 2)
-    tc_ms = time_graph(g_tc, tc_steps, torch) / tc_steps
+    sub_steps = max(3, args.steps // 2)
+    chain_ms = time_graph(g_chain, sub_steps, torch) / sub_steps
+    r50_ms = time_graph(g_r50, sub_steps, torch) / sub_steps
     lsteps = max(3, args.steps // 5)
     per_layer = time_launches(layers, lsteps, torch)
     dw_steps = max(3, args.steps // 2)
@@ -608,7 +698,7 @@ def main():
     s8_per = time_launches(s8_layers, lsteps, torch)
     clocks = sampler.stop()
 
-    statuses = [L["conv"].status() for L in layers + dw_layers + s8_layers]
+    statuses = [L["conv"].status() for L in layers + dw_layers + s8_layers] + [chain.status()]
     if any(s != 0 for s in statuses):
         raise SystemExit(f"device status error: {statuses}")
 
@@ -617,34 +707,51 @@ def main():
     value = whole_job_tflops(world, flops_step, args.steps, total_ms)
     ms_per_step = total_ms / args.steps
 
-    # per-layer times: event pairs around each launch (serialised, no dependent-launch overlap)
-    # rescaled so that they add up to the graph-timed step
-    per_layer = scale_to(per_layer, lsteps, ms_per_step)
+    # per-layer times of the per-layer launch path: event pairs around each launch (serialised,
+    # no dependent-launch overlap) rescaled so that they add up to its graph-timed pass
+    per_layer = scale_to(per_layer, lsteps, r50_ms)
     dw_per = scale_to(dw_per, lsteps, dw_total / dw_steps)
     s8_per = scale_to(s8_per, lsteps, s8_total / s8_steps)
 
-    tc_flops = sum(specs[i].flops for i in tc_idx)
-    achieved = tc_flops / (tc_ms * 1e-3) / 1e12
-    # attainable time of each layer: its FLOPs at the tensor peak or its algorithmic bytes at the
+    chain_specs = specs[1:]
+    chain_flops = sum(s.flops for s in chain_specs)
+    achieved = chain_flops / (chain_ms * 1e-3) / 1e12
+    # attainable time of each step: its FLOPs at the tensor peak or its algorithmic bytes at the
     # HBM bandwidth, whichever is longer (the bound of that layer)
-    att_ms = [attainable_ms(specs[i], peaks) for i in tc_idx]
-    n_tensor = sum(1 for i in tc_idx if layer_bound(specs[i], peaks) == "tensor")
+    att_ms = [attainable_ms(s, peaks) for s in chain_specs]
+    n_tensor = sum(1 for s in chain_specs if layer_bound(s, peaks) == "tensor")
+    cd = chain.describe()
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops"], "traffic": tc_traffic(),
-            "traffic_note": "per launch: DRAM reads + bytes written into L2 (all of which reach DRAM), ncu, mean "
-                            "of the 49 launches; against per_launch_algorithmic_bytes",
-            "kernel": f"tc_conv_kernel (tcgen05 implicit GEMM, all tile widths; {len(tc_idx)} layers per step)",
-            "peak_source": f"{peak_src} bf16 dense, burst (the kernel's layers timed alone as one graph replay)",
-            "kernel_ms_per_step": tc_ms, "launches_per_step": len(tc_idx),
-            "per_launch_flops": tc_flops / len(tc_idx), "launch_ms": tc_ms / len(tc_idx),
-            "per_launch_algorithmic_bytes": sum(specs[i].algorithmic_bytes for i in tc_idx) / len(tc_idx),
-            "layer_bounds": {"tensor": n_tensor, "hbm": len(tc_idx) - n_tensor},
-            "attainable_frac": sum(att_ms) / tc_ms,
-            "attainable_note": "sum over the kernel's layers of max(FLOPs / bf16 burst peak, algorithmic "
-                               "bytes / HBM peak), divided by the measured time of the same layers"}
-    idx17 = [i for i, s in enumerate(specs) if s.R > 1]
-    f17 = sum(specs[i].flops for i in idx17)
-    t17 = sum(per_layer[i] for i in idx17)
+            "frac": achieved / peaks["bf16_tflops"], "traffic": chain_traffic(),
+            "traffic_note": "per launch: DRAM reads + bytes written into L2 (all of which reach DRAM), ncu; "
+                            "against per_launch_algorithmic_bytes",
+            "kernel": "tc_chain_kernel (tcgen05 implicit GEMM, the 52 non-stem layers as one persistent launch: "
+                      + cd.split(" |")[0] + ")",
+            "peak_source": f"{peak_src} bf16 dense, burst (the kernel timed alone as one graph replay)",
+            "kernel_ms_per_step": chain_ms, "launches_per_step": 1,
+            "per_launch_flops": chain_flops, "launch_ms": chain_ms,
+            "per_launch_algorithmic_bytes": sum(s.algorithmic_bytes for s in chain_specs),
+            "layer_bounds": {"tensor": n_tensor, "hbm": len(chain_specs) - n_tensor},
+            "attainable_frac": sum(att_ms) / chain_ms,
+            "attainable_note": "sum over the chain's layers of max(FLOPs / bf16 burst peak, algorithmic "
+                               "bytes / HBM peak), divided by the measured time of the launch"}
+
+    # the 17 implicit-GEMM layers (stem + 16 3x3): the stem launch and a chain of the 16 3x3
+    # layers (independent steps), one graph replay
+    idx3 = [i for i, sp in enumerate(specs) if sp.R > 1 and i > 0]
+    chain3, _ = build_chain([layers[i] for i in idx3], cf, convs=[chain_convs[i - 1] for i in idx3])
+
+    def step17():
+        stem["conv"](stem["x"], stem["y"])
+        chain3()
+
+    step17()
+    g17 = capture_fn(step17, torch)
+    for _ in range(args.warmup):
+        g17.replay()
+    torch.cuda.synchronize()
+    t17 = time_graph(g17, sub_steps, torch) / sub_steps
+    f17 = specs[0].flops + sum(specs[i].flops for i in idx3)
     tf17 = f17 / (t17 * 1e-3) / 1e12
     dw_bytes = sum(s.algorithmic_bytes for s in dw_specs)
     dw_ms = dw_total / dw_steps
@@ -657,7 +764,8 @@ def main():
     extra = other_configs(args, torch, cf, synthetic, workloads, peaks)
     extra["qlinear"] = qlinear_config(args, torch, cf, synthetic, workloads, peaks)
 
-    # the same step with bf16 outputs and the bottleneck shortcuts (extended epilogue)
+    # the same step with bf16 outputs and the bottleneck shortcuts (extended epilogue), per-layer
+    # launches
     ext_layers = build_ext_layers(specs, layers, torch, cf)
     for _ in range(args.warmup):
         for L in ext_layers:
@@ -666,56 +774,87 @@ def main():
     for _ in range(args.warmup):
         g_ext.replay()
     torch.cuda.synchronize()
-    ext_steps = max(3, args.steps // 2)
-    ext_ms = time_graph(g_ext, ext_steps, torch) / ext_steps
+    ext_ms = time_graph(g_ext, sub_steps, torch) / sub_steps
     ext_bf16 = sum(1 for L in ext_layers if getattr(L["conv"], "out_bf16", False))
     ext_res = sum(1 for L in ext_layers if L.get("r") is not None)
     if any(L["conv"].status() != 0 for L in ext_layers):
         raise SystemExit("device status error in the bf16-output / residual step")
 
-    # end to end through the public API with host buffers (pinned), copies inside the timing: each
-    # layer's input goes up on a copy stream, the conv runs on the compute stream once its input
-    # has landed, and its output comes back on a second copy stream, so copies of one layer
-    # overlap the kernels and copies of the others
-    e2e_steps = max(2, min(5, args.steps))
+    # ResNet-50's dataflow as one dependent chain (bf16 activations, residuals), with the stem
+    net, _ = build_network_chain(specs, layers, torch, cf, workloads, synthetic)
+
+    def net_step():
+        stem["conv"](stem["x"], stem["y"])
+        net()
+
+    net_step()
+    g_net = capture_fn(net_step, torch)
+    for _ in range(args.warmup):
+        g_net.replay()
+    torch.cuda.synchronize()
+    net_ms = time_graph(g_net, sub_steps, torch) / sub_steps
+    if net.status() != 0 or chain3.status() != 0:
+        raise SystemExit("device status error in a chain")
+
+    # end to end through the public API with host buffers (pinned), copies inside the timing.
+    # Two device buffer sets alternate between steps: while the chain of step i runs on one set,
+    # step i+1's inputs go up into the other on a copy stream and step i-1's outputs come back
+    # on a second one.
+    e2e_steps = max(3, min(6, args.steps))
     for L in layers:
         L["x_pin"] = L["x_host"].pin_memory()
         L["y_pin"] = torch.empty_strided(L["y"].shape, L["y"].stride(), dtype=L["y"].dtype, pin_memory=True)
     h2d = sum(L["x"].numel() * L["x"].element_size() for L in layers)
     d2h = sum(L["y"].numel() * L["y"].element_size() for L in layers)
+    xs2 = [torch.empty_like(L["x"]) for L in layers]
+    ys2 = [torch.empty_like(L["y"]) for L in layers]
+    chain2, _ = build_chain(layers[1:], cf, convs=chain_convs, xs=xs2[1:], ys=ys2[1:])
+    sets = [{"x": [L["x"] for L in layers], "y": [L["y"] for L in layers], "chain": chain},
+            {"x": xs2, "y": ys2, "chain": chain2}]
     s_comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    for S in sets:
+        for k in ("ev_comp", "ev_out"):
+            S[k] = torch.cuda.Event()
+            S[k].record(s_comp)
 
-    def e2e_step():
-        start = torch.cuda.Event()
-        start.record(s_comp)
-        s_in.wait_event(start)
-        s_out.wait_event(start)
-        for L in layers:
-            with torch.cuda.stream(s_in):
-                L["x"].copy_(L["x_pin"], non_blocking=True)
-                L["ev_in"] = torch.cuda.Event()
-                L["ev_in"].record(s_in)
-            s_comp.wait_event(L["ev_in"])
-            L["conv"](L["x"], L["y"])
-            ev_run = torch.cuda.Event()
-            ev_run.record(s_comp)
-            s_out.wait_event(ev_run)
-            with torch.cuda.stream(s_out):
-                L["y_pin"].copy_(L["y"], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(s_out)
-        s_comp.wait_event(done)
+    def e2e_step(i):
+        S = sets[i % 2]
+        s_in.wait_event(S["ev_comp"])        # the set's previous chain has read its inputs
+        with torch.cuda.stream(s_in):
+            for L, x in zip(layers, S["x"]):
+                x.copy_(L["x_pin"], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        s_comp.wait_event(ev_in)
+        s_comp.wait_event(S["ev_out"])       # the set's previous outputs have been read back
+        stem["conv"](S["x"][0], S["y"][0])
+        S["chain"]()
+        S["ev_comp"] = torch.cuda.Event()
+        S["ev_comp"].record(s_comp)
+        s_out.wait_event(S["ev_comp"])
+        with torch.cuda.stream(s_out):
+            for L, y in zip(layers, S["y"]):
+                L["y_pin"].copy_(y, non_blocking=True)
+            S["ev_out"] = torch.cuda.Event()
+            S["ev_out"].record(s_out)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record()
+    e0.record(s_comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    for S in sets:
+        s_comp.wait_event(S["ev_out"])
+    e1.record(s_comp)
     torch.cuda.synchronize()
+    if chain2.status() != 0:
+        raise SystemExit("device status error in the end-to-end chain")
     e2e_val = whole_job_tflops(world, flops_step, e2e_steps, max_over_ranks(e0.elapsed_time(e1), world, "cuda"))
 
     cpu = None
@@ -733,9 +872,9 @@ def main():
                 # attainable: the tensor peak or the HBM bandwidth times the layer's intensity
                 att = min(peaks["bf16_tflops"], ai * peaks["hbm_gbs"] / 1e3)
                 tf = s.flops / (ms * 1e-3) / 1e12
-                f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "tflops": tf,
-                                    "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9, "ai": ai,
-                                    "attainable_tflops": att, "pct_attainable": tf / att}) + "\n")
+                f.write(json.dumps({"layer": s.name, "path": "per-layer launch", "kernel": L["conv"].describe(),
+                                    "ms": ms, "tflops": tf, "gbs": s.algorithmic_bytes / (ms * 1e-3) / 1e9,
+                                    "ai": ai, "attainable_tflops": att, "pct_attainable": tf / att}) + "\n")
             for s, L, ms in zip(dw_specs, dw_layers, dw_per):
                 gbs = s.algorithmic_bytes / (ms * 1e-3) / 1e9
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms, "gbs": gbs,
@@ -744,21 +883,37 @@ def main():
                 f.write(json.dumps({"layer": s.name, "kernel": L["conv"].describe(), "ms": ms,
                                     "tops": s.flops / (ms * 1e-3) / 1e12}) + "\n")
 
-    # one kernel per conv, plus the channel-padding pre-pass of gathered-row convs with few
-    # channels and the channel/column pre-pass of the window variant
-    launches_per_step = sum(1 + (("tap_channels=0" not in L["conv"].describe() and
-                                  "implicit_gemm_gather" in L["conv"].describe()) or
-                                 "implicit_gemm_window" in L["conv"].describe()) for L in layers)
+    # the stem (its channel/column pre-pass and the window kernel) and the chain
+    stem_launches = 1 + ("implicit_gemm_window" in stem["conv"].describe() or
+                         ("tap_channels=0" not in stem["conv"].describe() and
+                          "implicit_gemm_gather" in stem["conv"].describe()))
+    launches_per_step = stem_launches + 1
+    per_layer_launches = sum(1 + (("tap_channels=0" not in L["conv"].describe() and
+                                   "implicit_gemm_gather" in L["conv"].describe()) or
+                                  "implicit_gemm_window" in L["conv"].describe()) for L in layers)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": 32 * world, "parallelism": f"replicas{world}",
+                       "execution": "stem launch + one conv-chain launch of the 52 other layers (independent "
+                                    "steps, each on its own input)",
                        "l2": "inputs larger than L2: 53 distinct resident input/output buffer pairs, "
                              f"{(h2d + d2h) / 1e9:.2f} GB per step"},
             "pct_bf16_peak": value / peaks["bf16_tflops"],
-            "implicit_gemm_3x3_7x7": {"layers": len(idx17), "tflops": tf17, "pct_bf16_peak": tf17 / peaks["bf16_tflops"]},
+            "implicit_gemm_3x3_7x7": {"layers": 1 + len(idx3), "tflops": tf17, "pct_bf16_peak": tf17 / peaks["bf16_tflops"],
+                                      "ms": t17, "execution": "stem launch + one chain launch of the 16 3x3 layers"},
+            "per_layer_launches": {"workload": "the same 53 layers, one launch each (the shape-keyed selector's "
+                                               "kernels), one CUDA-graph replay",
+                                   "ms_per_step": r50_ms, "tflops": flops_step / (r50_ms * 1e-3) / 1e12,
+                                   "launches": per_layer_launches},
+            "network_chain": {"workload": "ResNet-50's own dataflow: the 52 bottleneck layers as one dependent "
+                                          "chain (each layer reads the previous one's bf16 output, each block's "
+                                          "last 1x1 conv adds the block's shortcut), plus the stem launch; bf16 "
+                                          "activations, fp32 accumulation",
+                              "ms_per_step": net_ms, "tflops": flops_step / (net_ms * 1e-3) / 1e12,
+                              "pct_bf16_peak": flops_step / (net_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
             "depthwise": {"workload": "MobileNetV2 depthwise 3x3 layers (17) at batch 64, bf16 in, fp32 out",
                           "gb_s": dw_gbs, "pct_hbm": dw_gbs / peaks["hbm_gbs"], "ms": dw_ms},
             "int8": {"workload": "ResNet-50 3x3 shapes (7) at batch 64, int8 in/out, exact int32 sums, "
@@ -771,7 +926,8 @@ def main():
                      "vs_mma_sync_rate": s8_tops / s8_peak},
             "bf16_out_residual": {"workload": "the same 53 layers with bf16 outputs (fp32 stem) and a bf16 "
                                               "residual added in each bottleneck's last 1x1 conv: the block's "
-                                              "shortcut tensor (its input, or the projection's output)",
+                                              "shortcut tensor (its input, or the projection's output); "
+                                              "per-layer launches",
                                   "ms_per_step": ext_ms, "tflops": flops_step / (ext_ms * 1e-3) / 1e12,
                                   "bf16_layers": ext_bf16, "residual_layers": ext_res},
             **extra,
@@ -779,12 +935,14 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "copies": "pinned host buffers; H2D and D2H on two copy streams "
-                                                   "overlapping the kernels on the compute stream"},
+                    "steps": e2e_steps, "copies": "pinned host buffers; per step the stem + chain launches on "
+                                                   "the compute stream, H2D of the inputs and D2H of the outputs "
+                                                   "on two copy streams, two device buffer sets alternating so "
+                                                   "that copies of neighbouring steps overlap the kernels"},
             "gpu_launches": launches_per_step * args.steps,
-            "timing": "step = one CUDA-graph replay of the 53 conv launches; the dominant kernel = one graph "
-                      "replay of its own layers; per-layer times (layer log) from event pairs around each "
-                      "launch, rescaled to add up to the step",
+            "timing": "step = one CUDA-graph replay of the stem launch and the chain launch; the dominant kernel "
+                      "= one graph replay of the chain launch alone; per-layer times (layer log) belong to the "
+                      "per-layer launch path (event pairs around each launch, rescaled to its graph-timed pass)",
             "clocks": clocks,
         }
         print(json.dumps(line))

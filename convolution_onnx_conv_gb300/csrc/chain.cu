@@ -171,38 +171,44 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
       if (rsrc >= 0 && (info[rsrc].M != f.M || info[rsrc].K != f.K))
         return record_error(CONVF_ERR_INVALID_ARG, "step %d's residual is not shaped like step %d's output", j, rsrc);
     }
-    c.a_mode = f.a_mode;
-    c.M = static_cast<int>(f.M);
-    c.Kout = f.K;
-    c.C = f.C; c.H = f.H; c.W = f.W; c.Ho = f.Ho; c.Wo = f.Wo; c.R = f.R; c.S = f.S;
-    c.sh = f.sh; c.sw = f.sw; c.pt = f.pt; c.pl = f.pl; c.dh = f.dh; c.dw = f.dw;
-    c.cblocks = f.cblocks;
-    c.num_kb = f.num_kb;
-    c.bn = f.K <= 64 ? 64 : 128;
-    c.n_blocks = (f.K + c.bn - 1) / c.bn;
-    c.mtiles = static_cast<int>((f.M + 127) / 128);
-    c.tile0 = static_cast<int>(tiles);
-    tiles += static_cast<long long>(c.mtiles) * c.n_blocks;
+    ChainGeom& g = c.g;
+    g.a_mode = f.a_mode;
+    g.M = static_cast<int>(f.M);
+    g.Kout = f.K;
+    g.C = f.C; g.H = f.H; g.W = f.W; g.Ho = f.Ho; g.Wo = f.Wo; g.R = f.R; g.S = f.S;
+    g.sh = f.sh; g.sw = f.sw; g.pt = f.pt; g.pl = f.pl; g.dh = f.dh; g.dw = f.dw;
+    g.cblocks = f.cblocks;
+    g.num_kb = f.num_kb;
+    g.mtiles = static_cast<int>((f.M + 127) / 128);
+    // 128 x 128 tiles (128 x 64 for K <= 64): narrower tiles for steps with fewer tiles than
+    // SMs measured slower, in a chain of independent steps and in a dependent one alike (an
+    // im2col tile's activation loads per FLOP double)
+    g.bn = f.K <= 64 ? 64 : 128;
+    g.n_blocks = (f.K + g.bn - 1) / g.bn;
+    g.tile0 = static_cast<int>(tiles);
+    tiles += static_cast<long long>(g.mtiles) * g.n_blocks;
     if (tiles > (1LL << 30)) return record_error(CONVF_ERR_UNSUPPORTED, "more than 2^30 tiles in one chain");
-    c.tile_end = static_cast<int>(tiles);
-    c.idesc = idesc_bf16_f32(128, c.bn);
-    c.lo = f.lo;
-    c.hi = f.hi;
-    c.scale = f.scale;
-    c.bias = f.bias;
-    c.x = st.x;
-    c.y = st.y;
-    c.res = st.r;
-    c.src = src;
-    c.rsrc = rsrc;
-    c.done = reinterpret_cast<uint32_t*>(static_cast<uintptr_t>(mtiles_total));   // offset until uploaded
-    mtiles_total += c.mtiles;
+    g.tile_end = static_cast<int>(tiles);
+    g.idesc = idesc_bf16_f32(128, g.bn);
+    g.lo = f.lo;
+    g.hi = f.hi;
+    g.scale = f.scale;
+    g.bias = f.bias;
+    g.x = st.x;
+    g.y = st.y;
+    g.res = st.r;
+    g.src = src;
+    g.rsrc = rsrc;
+    g.src_nb = src >= 0 ? cs[src].g.n_blocks : 0;
+    g.rsrc_nb = rsrc >= 0 ? cs[rsrc].g.n_blocks : 0;
+    g.done = reinterpret_cast<uint32_t*>(static_cast<uintptr_t>(mtiles_total));   // offsets until uploaded
+    mtiles_total += g.mtiles;
     filter[j] = f.R * 100 + f.S;
 
     CUresult r;
     if (f.a_mode == kA2D) {
-      c.a3d = f.C % 64 == 0 && f.num_kb % 2 == 0;
-      if (c.a3d) {
+      g.a3d = f.C % 64 == 0 && f.num_kb % 2 == 0;
+      if (g.a3d) {
         // {64 channels of a k-block, pixel, k-block}: one box = the two k-blocks of a step
         const cuuint64_t dims[3] = {64, (cuuint64_t)f.M, (cuuint64_t)(f.C / 64)};
         const cuuint64_t strides[2] = {(cuuint64_t)f.C * 2, 128};
@@ -237,7 +243,7 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
       // (one when the reduction is a single block)
       const cuuint64_t dims[3] = {64, (cuuint64_t)f.K, (cuuint64_t)f.num_kb};
       const cuuint64_t strides[2] = {(cuuint64_t)f.ktot * 2, 128};
-      const cuuint32_t box[3] = {64, (cuuint32_t)c.bn, (cuuint32_t)std::min(2, f.num_kb)};
+      const cuuint32_t box[3] = {64, (cuuint32_t)g.bn, (cuuint32_t)std::min(2, f.num_kb)};
       const cuuint32_t es[3] = {1, 1, 1};
       r = enc_tiled(&c.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(f.w), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -279,7 +285,11 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
   c->d_counters = reinterpret_cast<uint32_t*>(base + steps_bytes);
   c->d_state = reinterpret_cast<uint32_t*>(base + steps_bytes + ctr_bytes);
   c->d_status = reinterpret_cast<int*>(base + steps_bytes + ctr_bytes + 16);
-  for (ChainStep& s : cs) s.done = c->d_counters + reinterpret_cast<uintptr_t>(s.done);
+  for (ChainStep& s : cs) s.g.done = c->d_counters + reinterpret_cast<uintptr_t>(s.g.done);
+  for (ChainStep& s : cs) {
+    s.g.src_done = s.g.src >= 0 ? cs[s.g.src].g.done : nullptr;
+    s.g.rsrc_done = s.g.rsrc >= 0 ? cs[s.g.rsrc].g.done : nullptr;
+  }
   cudaError_t e = cudaMemcpy(c->d_steps, cs.data(), sizeof(ChainStep) * n, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(base + steps_bytes, 0, ctr_bytes + 256);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -344,7 +354,7 @@ convf_status conv_fused_chain_describe(const convf_chain* c, char* buf, size_t l
            c->out_bf16 ? "bf16" : "f32");
   s += line;
   for (int j = 0; j < c->nsteps; ++j) {
-    const ChainStep& q = c->steps[j];
+    const ChainGeom& q = c->steps[j].g;
     char rs[16];
     if (!q.res)
       snprintf(rs, sizeof rs, "none");

@@ -340,10 +340,9 @@ cudaError_t launch_watchdog_selftest(int32_t* status, long long budget, cudaStre
 // (0, 1, ...) a block is complete when its counter reaches (e + 1) * kChainArrivals * n_blocks
 // of its step: the counters only grow, so no launch has to clear them.
 constexpr int kChainArrivals = 1;
-struct ChainStep {   // (aligned as its tensor maps)
-  CUtensorMap tmA;           // activations: 2-D {C, M} box {64, 128}; 3-D {64, M, C/64} box
-                             // {64, 128, 2} (a3d); or im2col {C, W, H, N}, 128 pixels x 64 channels
-  CUtensorMap tmB;           // weights: 3-D {64, K, num_kb} box {64, bn, 2} over [K][num_kb * 64]
+// The scalar description of one chain step (kept apart from its tensor maps so that a kernel
+// role can hold the fields it uses in registers while it works on the step's tiles).
+struct ChainGeom {
   int a_mode, a3d;           // AMode (kA2D or kAIm2col); a3d: one box per two k-blocks (2-D mode)
   int M, Kout, C, H, W, Ho, Wo, R, S, sh, sw, pt, pl, dh, dw;
   int cblocks, num_kb, bn, n_blocks, mtiles;
@@ -357,7 +356,16 @@ struct ChainStep {   // (aligned as its tensor maps)
   const void* res;           // residual of y's type and shape added before the clamp, or null
   int src;                   // step whose y is this step's x, or -1 (x is written by no step)
   int rsrc;                  // step whose y is this step's residual, or -1
+  int src_nb, rsrc_nb;       // n_blocks of those steps (their row blocks' tile counts)
   uint32_t* done;            // [mtiles] arrival counters of this step's 128-row blocks
+  const uint32_t* src_done;  // the source step's counters, or null
+  const uint32_t* rsrc_done; // the residual's source step's counters, or null
+};
+struct ChainStep {
+  CUtensorMap tmA;           // activations: 2-D {C, M} box {64, 128}; 3-D {64, M, C/64} box
+                             // {64, 128, 2} (a3d); or im2col {C, W, H, N}, 128 pixels x 64 channels
+  CUtensorMap tmB;           // weights: 3-D {64, K, num_kb} box {64, bn, 2} over [K][num_kb * 64]
+  ChainGeom g;
 };
 struct ChainParams {
   const ChainStep* steps;    // device array [nsteps]

@@ -12,11 +12,10 @@
 //
 // Warp roles (one CTA per SM, tiles b, b + grid, ... of the launch-wide numbering):
 //   warp 0      activation producer: the dependency wait of each tile, then TMA activation
-//               loads (even k-blocks of a step; both, as one box, in the 3-D 1x1 mode)
+//               loads (one box per k-block, or one per pipeline step in the 3-D 1x1 mode)
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue into two 128-column fp32
 //               accumulators
-//   warp 2      weight producer: one TMA box per pipeline step (two k-blocks) plus the odd
-//               k-block's activation load (its own dependency wait first)
+//   warp 2      weight producer: one TMA box per pipeline step (two k-blocks)
 //   warps 3-10  epilogue, two warpgroups on the two column halves of every tile:
 //               tcgen05.ld -> smem transpose -> clamp(scale*acc + bias (+ r)) -> 16-byte stores
 //   warp 11     publisher: per stored tile, a gpu-scope fence and the increment of the tile's
@@ -70,29 +69,29 @@ __device__ bool chain_wait(const uint32_t* ctr, uint32_t target, int* status, vo
 
 // Input pixels (flat NHWC row indices of the step's x, which are the producing step's output
 // rows) that the tile of output rows [m0, m0 + 128) reads: whole input rows, conservatively.
-__device__ __forceinline__ void chain_input_rows(const ChainStep& s, int m0, int& lo, int& hi) {
-  const int m1 = min(m0 + kQM, s.M) - 1;
-  if (s.a_mode == kA2D) {
+__device__ __forceinline__ void chain_input_rows(const ChainGeom& g, int m0, int& lo, int& hi) {
+  const int m1 = min(m0 + kQM, g.M) - 1;
+  if (g.a_mode == kA2D) {
     lo = m0;
     hi = m1;
     return;
   }
-  const int hw = s.Ho * s.Wo;
+  const int hw = g.Ho * g.Wo;
   const int i0 = m0 / hw, i1 = m1 / hw;
-  const int oh0 = (m0 - i0 * hw) / s.Wo, oh1 = (m1 - i1 * hw) / s.Wo;
-  const int h0 = min(max(0, oh0 * s.sh - s.pt), s.H - 1);
-  const int h1 = max(min(s.H - 1, oh1 * s.sh - s.pt + (s.R - 1) * s.dh), 0);
-  lo = (i0 * s.H + h0) * s.W;
-  hi = (i1 * s.H + h1) * s.W + s.W - 1;
+  const int oh0 = (m0 - i0 * hw) / g.Wo, oh1 = (m1 - i1 * hw) / g.Wo;
+  const int h0 = min(max(0, oh0 * g.sh - g.pt), g.H - 1);
+  const int h1 = max(min(g.H - 1, oh1 * g.sh - g.pt + (g.R - 1) * g.dh), 0);
+  lo = (i0 * g.H + h0) * g.W;
+  hi = (i1 * g.H + h1) * g.W + g.W - 1;
 }
 
 // Walks the launch-wide tile numbering in increasing order, keeping the step that holds it.
 struct ChainCursor {
   const ChainStep* steps;
   int L, end;
-  __device__ explicit ChainCursor(const ChainStep* s) : steps(s), L(0), end(s[0].tile_end) {}
+  __device__ explicit ChainCursor(const ChainStep* s) : steps(s), L(0), end(s[0].g.tile_end) {}
   __device__ int at(int t) {
-    while (t >= end) end = steps[++L].tile_end;
+    while (t >= end) end = steps[++L].g.tile_end;
     return L;
   }
 };
@@ -111,9 +110,12 @@ struct ChainKPos {
   }
 };
 
-// Producer roles.  ROLE 0 (warp 0): activation loads of the even k-blocks (both k-blocks as one
-// box in the 3-D mode).  ROLE 2 (warp 2): the weight box of each step and the odd k-block's
-// activation load.  Each waits for the tile's input rows before its first activation load.
+// Producer roles.  ROLE 0 (warp 0): the dependency wait of each tile, then the activation loads
+// of both k-blocks of every pipeline step (one box in the 3-D mode, else one per k-block).
+// ROLE 2 (warp 2): the weight box of each step.  (Moving the odd k-block's activation load from
+// the weight producer to the activation producer measured 2-5% faster on every layer shape.)
+// Every role keeps the current step's fields in registers (ChainGeom, reloaded when the step
+// changes): the issuing thread's scalar work delays its next copy.
 template <int ROLE>
 __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
                                uint32_t epoch1, volatile int* abort_flag) {
@@ -121,87 +123,81 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
   ChainCursor cur(steps);
   int stage = 0;
   uint32_t phase = 0;
-  int dep_step = -1, dep_done = -1;   // row blocks of the source verified for step dep_step
+  int dep_done = -1;   // row blocks of the source verified for the current step
   int last = -1;
+  ChainGeom g;
+  const CUtensorMap* tmA = nullptr;
+  const CUtensorMap* tmB = nullptr;
+  uint32_t b_bytes = 0, target = 0;
   for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
     const int L = cur.at(t);
-    const ChainStep& s = steps[L];
     if (L != last) {
       last = L;
-      if (ROLE == 0 || !s.a3d) tma_prefetch_desc(&s.tmA);
-      if (ROLE == 2) tma_prefetch_desc(&s.tmB);
+      g = steps[L].g;
+      tmA = &steps[L].tmA;
+      tmB = &steps[L].tmB;
+      tma_prefetch_desc(ROLE == 0 ? tmA : tmB);
+      dep_done = -1;
+      // the weight box holds two k-blocks (zero fill past the last), one if the step has one
+      b_bytes = static_cast<uint32_t>((g.num_kb > 1 ? 2 : 1) * g.bn * kQK * 2);
+      target = epoch1 * static_cast<uint32_t>(kChainArrivals * g.src_nb);
     }
-    const int local = t - s.tile0;
-    const int mt = local / s.n_blocks;
-    const int n0 = (local - mt * s.n_blocks) * s.bn;
+    const int local = t - g.tile0;
+    const int mt = local / g.n_blocks;
+    const int n0 = (local - mt * g.n_blocks) * g.bn;
     const int m0 = mt * kQM;
-    const bool loads_a = ROLE == 0 || !s.a3d;
-    if (loads_a && s.src >= 0) {
+    const bool a3d = g.a3d != 0, a2d = g.a_mode == kA2D;
+    if (ROLE == 0 && g.src >= 0) {
       int lo, hi;
-      chain_input_rows(s, m0, lo, hi);
-      const ChainStep& ps = steps[s.src];
-      const uint32_t target = epoch1 * static_cast<uint32_t>(kChainArrivals * ps.n_blocks);
-      if (L != dep_step) {
-        dep_step = L;
-        dep_done = -1;
-      }
+      chain_input_rows(g, m0, lo, hi);
       // this CTA's tiles of one step visit increasing rows, so the blocks below dep_done that
       // the range still covers were verified for an earlier tile
       for (int b = max(lo / kQM, dep_done + 1); b <= hi / kQM; ++b)
-        if (!chain_wait(ps.done + b, target, p.status, abort_flag)) return;
+        if (!chain_wait(g.src_done + b, target, p.status, abort_flag)) return;
       dep_done = max(dep_done, hi / kQM);
-      fence_proxy_async_global();   // the source's generic stores before this thread's TMA reads
+      fence_proxy_async_global();   // the source's stores before this thread's TMA reads
     }
     int img = 0, hb = 0, wb = 0;
-    if (s.a_mode == kAIm2col) {
-      const int hw = s.Ho * s.Wo;
+    if (ROLE == 0 && !a2d) {
+      const int hw = g.Ho * g.Wo;
       img = m0 / hw;
       const int rem = m0 - img * hw;
-      const int oh = rem / s.Wo;
-      hb = oh * s.sh - s.pt;
-      wb = (rem - oh * s.Wo) * s.sw - s.pl;
+      const int oh = rem / g.Wo;
+      hb = oh * g.sh - g.pt;
+      wb = (rem - oh * g.Wo) * g.sw - g.pl;
     }
-    // the step's fields the loop needs, in registers (the issuing thread's scalar work delays
-    // its next copy)
-    const int num_kb = s.num_kb, cbl = s.cblocks, Sl = s.S, dwl = s.dw, dhl = s.dh;
-    const bool a3d = s.a3d != 0, a2d = s.a_mode == kA2D;
-    const CUtensorMap* tmA = &s.tmA;
-    const CUtensorMap* tmB = &s.tmB;
-    // the weight box holds two k-blocks (zero fill past the last), one if the step has one
-    const uint32_t b_bytes = static_cast<uint32_t>((num_kb > 1 ? 2 : 1) * s.bn * kQK * 2);
     ChainKPos q{0, 0, 0};
-    for (int kb = 0; kb < num_kb; kb += 2) {
-      const bool two = kb + 1 < num_kb;
+    for (int kb = 0; kb < g.num_kb; kb += 2) {
+      const bool two = kb + 1 < g.num_kb;
       if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) return;
       uint8_t* a0 = sA + stage * 2 * kQATile;
-      ChainKPos q1 = q;   // k-block kb + 1
-      q1.next(cbl, Sl);
-      if (ROLE == 0) {
+      if constexpr (ROLE == 0) {
+        ChainKPos q1 = q;   // k-block kb + 1
+        q1.next(g.cblocks, g.S);
         if (a3d) {
           mbar_arrive_expect_tx(&full[stage], 2 * kQATile);
           tma_load_3d(a0, tmA, &full[stage], 0, m0, kb);
         } else {
-          mbar_arrive_expect_tx(&full[stage], kQATile);
+          mbar_arrive_expect_tx(&full[stage], kQATile * (two ? 2u : 1u));
           if (a2d)
             tma_load_2d(a0, tmA, &full[stage], kb * kQK, m0);
           else
-            tma_load_im2col_4d(a0, tmA, &full[stage], q.cb * kQK, wb, hb, img, static_cast<uint16_t>(q.s * dwl),
-                               static_cast<uint16_t>(q.r * dhl));
+            tma_load_im2col_4d(a0, tmA, &full[stage], q.cb * kQK, wb, hb, img, static_cast<uint16_t>(q.s * g.dw),
+                               static_cast<uint16_t>(q.r * g.dh));
+          if (two) {
+            if (a2d)
+              tma_load_2d(a0 + kQATile, tmA, &full[stage], (kb + 1) * kQK, m0);
+            else
+              tma_load_im2col_4d(a0 + kQATile, tmA, &full[stage], q1.cb * kQK, wb, hb, img,
+                                 static_cast<uint16_t>(q1.s * g.dw), static_cast<uint16_t>(q1.r * g.dh));
+          }
         }
+        q = q1;
+        q.next(g.cblocks, g.S);
       } else {
-        const bool odd_a = !a3d && two;
-        mbar_arrive_expect_tx(&full[stage], b_bytes + (odd_a ? kQATile : 0u));
+        mbar_arrive_expect_tx(&full[stage], b_bytes);
         tma_load_3d(sB + stage * 2 * kQBTile, tmB, &full[stage], 0, n0, kb);
-        if (odd_a) {
-          if (a2d)
-            tma_load_2d(a0 + kQATile, tmA, &full[stage], (kb + 1) * kQK, m0);
-          else
-            tma_load_im2col_4d(a0 + kQATile, tmA, &full[stage], q1.cb * kQK, wb, hb, img,
-                               static_cast<uint16_t>(q1.s * dwl), static_cast<uint16_t>(q1.r * dhl));
-        }
       }
-      q = q1;
-      q.next(cbl, Sl);
       if (++stage == kQSteps) {
         stage = 0;
         phase ^= 1;
@@ -222,11 +218,17 @@ __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
+  int last = -1;
+  uint32_t idesc = 0, bblock = 0;
+  int num_kb = 0;
   for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-    const ChainStep& s = steps[cur.at(t)];
-    const uint32_t idesc = s.idesc;
-    const int num_kb = s.num_kb;
-    const uint32_t bblock = static_cast<uint32_t>(s.bn * kQK * 2);   // bytes of one k-block's weights
+    const int L = cur.at(t);
+    if (L != last) {
+      last = L;
+      idesc = steps[L].g.idesc;
+      num_kb = steps[L].g.num_kb;
+      bblock = static_cast<uint32_t>(steps[L].g.bn * kQK * 2);   // bytes of one k-block's weights
+    }
     if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) return;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kQBNMax);
@@ -256,12 +258,127 @@ __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64
 }
 
 // Epilogue warp (two warpgroups; group eg drains columns [eg*bn/2, (eg+1)*bn/2) of every tile,
-// the warp its TMEM lane quadrant q = rows 32q..32q+31).  Per 32-column chunk: tcgen05.ld ->
-// this warp's 4 KB of smem (thread = row) -> read back as thread = (row, 4 or 8 channels) ->
-// clamp(scale*acc + bias (+ r)) -> 16-byte stores.  After a tile's stores the warp arrives on the
+// the warp its TMEM lane quadrant q = rows 32q..32q+31).  Both of a tile's 32-column chunks are
+// read from TMEM at once (the buffer goes back to the MMA issuer after one wait), then per
+// chunk: this warp's 4 KB of smem (thread = row) -> read back as thread = (row, 4 or 8 channels)
+// -> clamp(scale*acc + bias (+ r)) -> 16-byte stores; a chunk's epilogue vectors and residual
+// are loaded before its accumulator is needed.  After a tile's stores the warp arrives on the
 // tile's publication barrier (stored[j % kQPub] for the CTA's j-th tile) and moves on: the
 // publisher warp makes the stores visible at gpu scope and raises the row-block counter, so no
 // epilogue warp waits for its stores to reach L2.
+template <bool OUT_BF16>
+struct ChainEpiChunk;
+template <>
+struct ChainEpiChunk<true> {   // bf16 y: thread = (rows 8i + sub8, channels col .. col + 7)
+  float4 s0, s1, b0, b1;
+  uint4 rv[4];
+  int col;
+  bool col_ok;
+  __device__ void load(const ChainGeom& g, int col0, int row0, int lane, int* status) {
+    const int sub8 = lane >> 2, c8 = lane & 3;
+    col = col0 + 8 * c8;
+    col_ok = col < g.Kout;   // Kout % 8 == 0: whole 8-channel groups
+    s0 = s1 = b0 = b1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col_ok) {
+      s0 = __ldg(reinterpret_cast<const float4*>(g.scale + col));
+      s1 = __ldg(reinterpret_cast<const float4*>(g.scale + col + 4));
+      b0 = __ldg(reinterpret_cast<const float4*>(g.bias + col));
+      b1 = __ldg(reinterpret_cast<const float4*>(g.bias + col + 4));
+    }
+    [[maybe_unused]] const size_t total = static_cast<size_t>(g.M) * g.Kout;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      rv[i] = make_uint4(0u, 0u, 0u, 0u);
+      const int r = row0 + 8 * i + sub8;
+      const size_t e = static_cast<size_t>(r) * g.Kout + col;
+      // written by an earlier step of this launch: read through L2 (not the read-only path)
+      if (g.res != nullptr && col_ok && r < g.M && CONVF_IN_BOUNDS(e + 8 <= total, status))
+        rv[i] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(g.res) + e));
+    }
+  }
+  __device__ void store(const ChainGeom& g, const float* wst, int row0, int lane, int* status) const {
+    const int sub8 = lane >> 2, c8 = lane & 3;
+    [[maybe_unused]] const size_t total = static_cast<size_t>(g.M) * g.Kout;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rr = 8 * i + sub8;
+      const int r = row0 + rr;
+      const float4 x0 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8) ^ (rr & 7)) << 2));
+      const float4 x1 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8 + 1) ^ (rr & 7)) << 2));
+      if (!col_ok || r >= g.M) continue;
+      const float o[8] = {fmaf(x0.x, s0.x, b0.x), fmaf(x0.y, s0.y, b0.y), fmaf(x0.z, s0.z, b0.z),
+                          fmaf(x0.w, s0.w, b0.w), fmaf(x1.x, s1.x, b1.x), fmaf(x1.y, s1.y, b1.y),
+                          fmaf(x1.z, s1.z, b1.z), fmaf(x1.w, s1.w, b1.w)};
+      const uint32_t rw[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+      uint32_t pk[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        // residual (zero bits when there is none) before the clamp, then RNE to bf16
+        const float a0 = fminf(fmaxf(o[2 * j] + __uint_as_float(rw[j] << 16), g.lo), g.hi);
+        const float a1 = fminf(fmaxf(o[2 * j + 1] + __uint_as_float(rw[j] & 0xffff0000u), g.lo), g.hi);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+        pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      const size_t e = static_cast<size_t>(r) * g.Kout + col;
+      if (CONVF_IN_BOUNDS(e + 8 <= total, status))
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.y) + e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+};
+template <>
+struct ChainEpiChunk<false> {   // fp32 y: thread = (rows 4i + sub, channels col .. col + 3)
+  float4 sc, bi;
+  float4 rv[8];
+  int col;
+  bool col_ok;
+  __device__ void load(const ChainGeom& g, int col0, int row0, int lane, int* status) {
+    const int sub = lane >> 3, c4 = lane & 7;
+    col = col0 + 4 * c4;
+    col_ok = col < g.Kout;   // Kout % 4 == 0
+    sc = bi = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col_ok) {
+      sc = __ldg(reinterpret_cast<const float4*>(g.scale + col));
+      bi = __ldg(reinterpret_cast<const float4*>(g.bias + col));
+    }
+    [[maybe_unused]] const size_t total = static_cast<size_t>(g.M) * g.Kout;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int r = row0 + 4 * i + sub;
+      const size_t e = static_cast<size_t>(r) * g.Kout + col;
+      if (g.res != nullptr && col_ok && r < g.M && CONVF_IN_BOUNDS(e + 4 <= total, status))
+        rv[i] = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(g.res) + e));
+    }
+  }
+  __device__ void store(const ChainGeom& g, const float* wst, int row0, int lane, int* status) const {
+    const int sub = lane >> 3, c4 = lane & 7;
+    [[maybe_unused]] const size_t total = static_cast<size_t>(g.M) * g.Kout;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + sub;
+      const int r = row0 + rr;
+      const float4 a = *reinterpret_cast<const float4*>(wst + rr * 32 + ((c4 ^ (rr & 7)) << 2));
+      if (!col_ok || r >= g.M) continue;
+      const float4 o = make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x) + rv[i].x, g.lo), g.hi),
+                                   fminf(fmaxf(fmaf(a.y, sc.y, bi.y) + rv[i].y, g.lo), g.hi),
+                                   fminf(fmaxf(fmaf(a.z, sc.z, bi.z) + rv[i].z, g.lo), g.hi),
+                                   fminf(fmaxf(fmaf(a.w, sc.w, bi.w) + rv[i].w, g.lo), g.hi));
+      const size_t e = static_cast<size_t>(r) * g.Kout + col;
+      if (CONVF_IN_BOUNDS(e + 4 <= total, status)) *reinterpret_cast<float4*>(static_cast<float*>(g.y) + e) = o;
+    }
+  }
+};
+
+// one 32 x 32 fp32 chunk, row `lane` of the accumulator -> smem, 16-byte chunks XOR-swizzled by
+// row (both the write and the read-back are conflict-free)
+__device__ __forceinline__ void chain_stage_chunk(float* wst, const uint32_t (&v)[32], int lane) {
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc)
+    *reinterpret_cast<float4*>(wst + lane * 32 + ((cc ^ (lane & 7)) << 2)) =
+        make_float4(__uint_as_float(v[4 * cc]), __uint_as_float(v[4 * cc + 1]), __uint_as_float(v[4 * cc + 2]),
+                    __uint_as_float(v[4 * cc + 3]));
+}
+
 template <bool OUT_BF16>
 __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tfull, uint64_t* tempty,
                                uint64_t* stored, uint64_t* pubfree, uint32_t tmem_base, uint32_t epoch1,
@@ -275,151 +392,59 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
   ChainCursor cur(steps);
   int acc = 0;
   uint32_t acc_phase = 0;
+  int last = -1;
+  ChainGeom g;
+  uint32_t rtarget = 0;
   int j = 0;   // tiles of this CTA so far
   for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
-    const ChainStep& s = steps[cur.at(t)];
-    const int local = t - s.tile0;
-    const int mt = local / s.n_blocks;
-    const int n0 = (local - mt * s.n_blocks) * s.bn;
+    const int L = cur.at(t);
+    if (L != last) {
+      last = L;
+      g = steps[L].g;
+      rtarget = epoch1 * static_cast<uint32_t>(kChainArrivals * g.rsrc_nb);
+    }
+    const int local = t - g.tile0;
+    const int mt = local / g.n_blocks;
+    const int n0 = (local - mt * g.n_blocks) * g.bn;
     const int row0 = mt * kQM + q * 32;
-    const int M = s.M, Kout = s.Kout;
-    const float lo = s.lo, hi = s.hi;
-    const float* scale = s.scale;
-    const float* bias = s.bias;
-    const int half = s.bn >> 1;
-    const int nch = half >> 5;
-    const void* res = s.res;
-    const int rsrc = s.rsrc;
-    [[maybe_unused]] const size_t total = static_cast<size_t>(M) * Kout;   // (bounds-checking build)
+    const int half = g.bn >> 1;
+    const bool two = half > 32;   // two 32-column chunks (128-wide tiles) or one
+    const int col0 = n0 + eg * half;
     if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) return;
     tc_fence_after();
-    if (res != nullptr && rsrc >= 0) {
+    if (g.res != nullptr && g.rsrc >= 0) {
       // the residual rows of this tile are the producing step's row block mt (same shape)
       int ok = 1;
-      if (lane == 0) {
-        const ChainStep& rs = steps[rsrc];
-        ok = chain_wait(rs.done + mt, epoch1 * static_cast<uint32_t>(kChainArrivals * rs.n_blocks), p.status,
-                        abort_flag);
-      }
+      if (lane == 0) ok = chain_wait(g.rsrc_done + mt, rtarget, p.status, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     }
-    for (int c = 0; c < nch; ++c) {
-      const int tcol = eg * half + c * 32;   // tile column of this chunk
-      const int col0 = n0 + tcol;
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kQBNMax + tcol), v);
-      if constexpr (OUT_BF16) {
-        // thread = (rows 8i + sub8, channels col .. col + 7): 16-byte residual loads and stores;
-        // the epilogue vectors and the residual are in flight while the accumulator is read
-        const int sub8 = lane >> 2, c8 = lane & 3;
-        const int col = col0 + 8 * c8;
-        const bool col_ok = col < Kout;   // Kout % 8 == 0: whole 8-channel groups
-        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, b0 = s0, b1 = s0;
-        if (col_ok) {
-          s0 = __ldg(reinterpret_cast<const float4*>(scale + col));
-          s1 = __ldg(reinterpret_cast<const float4*>(scale + col + 4));
-          b0 = __ldg(reinterpret_cast<const float4*>(bias + col));
-          b1 = __ldg(reinterpret_cast<const float4*>(bias + col + 4));
-        }
-        uint4 rv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          rv[i] = make_uint4(0u, 0u, 0u, 0u);
-          const int r = row0 + 8 * i + sub8;
-          const size_t e = static_cast<size_t>(r) * Kout + col;
-          // written by an earlier step of this launch: read through L2 (not the read-only path)
-          if (res != nullptr && col_ok && r < M && CONVF_IN_BOUNDS(e + 8 <= total, p.status))
-            rv[i] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(res) + e));
-        }
-        tmem_ld_wait();
-        if (c == nch - 1) {
-          // the warp's last TMEM read of the tile: release the buffer to the MMA issuer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
-        }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<float4*>(wst + lane * 32 + ((cc ^ (lane & 7)) << 2)) =
-              make_float4(__uint_as_float(v[4 * cc]), __uint_as_float(v[4 * cc + 1]), __uint_as_float(v[4 * cc + 2]),
-                          __uint_as_float(v[4 * cc + 3]));
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = 8 * i + sub8;
-          const int r = row0 + rr;
-          const float4 x0 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8) ^ (rr & 7)) << 2));
-          const float4 x1 = *reinterpret_cast<const float4*>(wst + rr * 32 + (((2 * c8 + 1) ^ (rr & 7)) << 2));
-          if (!col_ok || r >= M) continue;
-          const float o[8] = {fmaf(x0.x, s0.x, b0.x), fmaf(x0.y, s0.y, b0.y), fmaf(x0.z, s0.z, b0.z),
-                              fmaf(x0.w, s0.w, b0.w), fmaf(x1.x, s1.x, b1.x), fmaf(x1.y, s1.y, b1.y),
-                              fmaf(x1.z, s1.z, b1.z), fmaf(x1.w, s1.w, b1.w)};
-          const uint32_t rw[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
-          uint32_t pk[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // residual (zero bits when there is none) before the clamp, then RNE to bf16
-            const float a0 = fminf(fmaxf(o[2 * j] + __uint_as_float(rw[j] << 16), lo), hi);
-            const float a1 = fminf(fmaxf(o[2 * j + 1] + __uint_as_float(rw[j] & 0xffff0000u), lo), hi);
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-            pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          const size_t e = static_cast<size_t>(r) * Kout + col;
-          if (CONVF_IN_BOUNDS(e + 8 <= total, p.status))
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(s.y) + e) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-      } else {
-        // thread = (rows 4i + sub, channels col .. col + 3)
-        const int sub = lane >> 3, c4 = lane & 7;
-        const int col = col0 + 4 * c4;
-        const bool col_ok = col < Kout;   // Kout % 4 == 0
-        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bi = sc;
-        if (col_ok) {
-          sc = __ldg(reinterpret_cast<const float4*>(scale + col));
-          bi = __ldg(reinterpret_cast<const float4*>(bias + col));
-        }
-        tmem_ld_wait();
-        if (c == nch - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
-        }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<float4*>(wst + lane * 32 + ((cc ^ (lane & 7)) << 2)) =
-              make_float4(__uint_as_float(v[4 * cc]), __uint_as_float(v[4 * cc + 1]), __uint_as_float(v[4 * cc + 2]),
-                          __uint_as_float(v[4 * cc + 3]));
-        __syncwarp();
-        float4 rv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          rv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          const int r = row0 + 4 * i + sub;
-          const size_t e = static_cast<size_t>(r) * Kout + col;
-          if (res != nullptr && col_ok && r < M && CONVF_IN_BOUNDS(e + 4 <= total, p.status))
-            rv[i] = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(res) + e));
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + sub;
-          const int r = row0 + rr;
-          const float4 a = *reinterpret_cast<const float4*>(wst + rr * 32 + ((c4 ^ (rr & 7)) << 2));
-          if (!col_ok || r >= M) continue;
-          const float4 o = make_float4(fminf(fmaxf(fmaf(a.x, sc.x, bi.x) + rv[i].x, lo), hi),
-                                       fminf(fmaxf(fmaf(a.y, sc.y, bi.y) + rv[i].y, lo), hi),
-                                       fminf(fmaxf(fmaf(a.z, sc.z, bi.z) + rv[i].z, lo), hi),
-                                       fminf(fmaxf(fmaf(a.w, sc.w, bi.w) + rv[i].w, lo), hi));
-          const size_t e = static_cast<size_t>(r) * Kout + col;
-          if (CONVF_IN_BOUNDS(e + 4 <= total, p.status)) *reinterpret_cast<float4*>(static_cast<float*>(s.y) + e) = o;
-        }
-      }
-      __syncwarp();   // the chunk's smem reads are done before the next chunk is written
+    uint32_t v0[32], v1[32];
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kQBNMax + eg * half);
+    tmem_ld_32x32b_x32(taddr, v0);
+    if (two) tmem_ld_32x32b_x32(taddr + 32, v1);
+    ChainEpiChunk<OUT_BF16> ch;
+    ch.load(g, col0, row0, lane, p.status);
+    tmem_ld_wait();
+    // the warp's TMEM reads of the tile are done: the buffer goes back to the MMA issuer
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[acc]);
+    chain_stage_chunk(wst, v0, lane);
+    __syncwarp();
+    ch.store(g, wst, row0, lane, p.status);
+    __syncwarp();   // the chunk's smem reads are done before the next chunk is written
+    if (two) {
+      ch.load(g, col0 + 32, row0, lane, p.status);
+      chain_stage_chunk(wst, v1, lane);
+      __syncwarp();
+      ch.store(g, wst, row0, lane, p.status);
+      __syncwarp();
     }
     // the tile is stored: hand it to the publisher (once it has taken the slot's previous tile)
-    __syncwarp();
     if (lane == 0) {
       const int slot = j % kQPub;
-      bool ok = j < kQPub || mbar_wait(&pubfree[slot], static_cast<uint32_t>((j / kQPub - 1) & 1), abort_flag, p.status);
+      const bool ok =
+          j < kQPub || mbar_wait(&pubfree[slot], static_cast<uint32_t>((j / kQPub - 1) & 1), abort_flag, p.status);
       if (ok) mbar_arrive(&stored[slot]);
     }
     if (++acc == 2) {
@@ -436,15 +461,23 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
 __device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t* pubfree, volatile int* abort_flag) {
   const ChainStep* steps = p.steps;
   ChainCursor cur(steps);
+  int last = -1, tile0 = 0, nb = 1;
+  uint32_t* done = nullptr;
   int j = 0;
   for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
-    const ChainStep& s = steps[cur.at(t)];
-    const int mt = (t - s.tile0) / s.n_blocks;
+    const int L = cur.at(t);
+    if (L != last) {
+      last = L;
+      tile0 = steps[L].g.tile0;
+      nb = steps[L].g.n_blocks;
+      done = steps[L].g.done;
+    }
+    const int mt = (t - tile0) / nb;
     const int slot = j % kQPub;
     if (!mbar_wait(&stored[slot], static_cast<uint32_t>((j / kQPub) & 1), abort_flag, p.status)) return;
     fence_acq_rel_gpu();
     fence_proxy_async_global();   // ... and ordered before later async-proxy (TMA) reads of them
-    red_relaxed_gpu_add(s.done + mt, 1u);
+    red_relaxed_gpu_add(done + mt, 1u);
     mbar_arrive(&pubfree[slot]);
   }
 }
@@ -504,19 +537,20 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
   if (lane == 0 && (warp == 0 || warp == 2)) {
     const int t = blockIdx.x;
     int L = 0;
-    while (t >= p.steps[L].tile_end) ++L;
-    const ChainStep& s = p.steps[L];
-    const int local = t - s.tile0;
-    const int mt = local / s.n_blocks;
+    while (t >= p.steps[L].g.tile_end) ++L;
+    const ChainGeom& g = p.steps[L].g;
+    const int local = t - g.tile0;
+    const int mt = local / g.n_blocks;
     if (warp == 2) {
-      tma_prefetch_desc(&s.tmB);
-      for (int kb = 0; kb < min(s.num_kb, 4); kb += 2) tma_prefetch_l2_3d(&s.tmB, 0, (local - mt * s.n_blocks) * s.bn, kb);
-    } else if (s.src < 0) {
-      tma_prefetch_desc(&s.tmA);
+      tma_prefetch_desc(&p.steps[L].tmB);
+      for (int kb = 0; kb < min(g.num_kb, 4); kb += 2)
+        tma_prefetch_l2_3d(&p.steps[L].tmB, 0, (local - mt * g.n_blocks) * g.bn, kb);
+    } else if (g.src < 0) {
+      tma_prefetch_desc(&p.steps[L].tmA);
       int lo, hi;
-      chain_input_rows(s, mt * kQM, lo, hi);
-      bulk_prefetch_l2(static_cast<const uint16_t*>(s.x) + static_cast<size_t>(lo) * s.C,
-                       static_cast<uint32_t>(hi - lo + 1) * s.C * 2);
+      chain_input_rows(g, mt * kQM, lo, hi);
+      bulk_prefetch_l2(static_cast<const uint16_t*>(g.x) + static_cast<size_t>(lo) * g.C,
+                       static_cast<uint32_t>(hi - lo + 1) * g.C * 2);
     }
   }
   pdl_wait_prior();

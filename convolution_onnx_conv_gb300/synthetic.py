@@ -8,7 +8,9 @@ shapes are used):
 * ``uniform``: x, W ~ U[-1, 1] rounded to bf16 (round-to-nearest-even),
   bias ~ U[-0.1, 0.1] fp32.
 * ``normal``: x ~ N(0, 1) -> bf16; W He-normal (sigma^2 = 2 / fan_in) -> bf16;
-  BN gamma ~ U[0.5, 1.5], beta ~ N(0, 0.1), mean ~ N(0, 0.1), var ~ U[0.5, 1.5].
+  BN gamma ~ U[0.5, 1.5], beta ~ N(0, 0.1), mean ~ N(0, 0.1), var ~ U[0.5, 1.5]; when the
+  ResNet-50 layers run as one network, each block's last BN has gamma scaled by
+  RESIDUAL_BRANCH_GAMMA (``residual_branch_inputs``).
 * ``int``: x ~ U{-128..127}, W ~ U{-127..127} (int8), bias ~ U{-2^16..2^16}
   (int32), per-channel requant multiplier M in [2^30, 2^31) and shift sh with
   M / 2^sh ~ 127 / (4 sigma_acc) * U[0.5, 1.5], sigma_acc = 73.9^2 sqrt(C R S),
@@ -63,6 +65,23 @@ def conv_inputs(spec: ConvSpec, seed: int) -> Dict[str, Optional[torch.Tensor]]:
         mean = torch.randn(spec.K, generator=g) * 0.1
         var = _uniform(g, (spec.K,), 0.5, 1.5)
         out["bn"] = (gamma, beta, mean, var)
+    return out
+
+
+# The BN scale (gamma) of each bottleneck's last conv, relative to conv_inputs', when the layers
+# run as one network: with every BN drawn as in conv_inputs the residual stream roughly doubles
+# in every block (each block adds a branch of its own size), reaching 10^4 by the last stage, where
+# a conv output is a near-cancelling sum of terms up to 10^5 that no fp32 accumulation resolves
+# to 1e-3 of its value.  A smaller gamma on the branch (the usual initialisation of a residual
+# network keeps it small, or zero) keeps the stream's scale steady.
+RESIDUAL_BRANCH_GAMMA = 0.25
+
+
+def residual_branch_inputs(spec: ConvSpec, seed: int) -> Dict[str, Optional[torch.Tensor]]:
+    """conv_inputs with the BN gamma scaled by RESIDUAL_BRANCH_GAMMA (a block's last conv)."""
+    out = conv_inputs(spec, seed)
+    gamma, beta, mean, var = out["bn"]
+    out["bn"] = (gamma * RESIDUAL_BRANCH_GAMMA, beta, mean, var)
     return out
 
 

@@ -109,6 +109,33 @@ def resnet50_layers(n: int = 32) -> List[ConvSpec]:
     return L
 
 
+def resnet50_dataflow() -> List[Tuple[int, int, Optional[int]]]:
+    """The bottleneck layers of ``resnet50_layers`` (all but the stem) in an order in which every
+    layer comes after the layers it reads, as ``(layer, src, rsrc)``: the index into
+    ``resnet50_layers`` and the positions in this list of the layers whose outputs are its input
+    (``src``) and the residual added in its epilogue (``rsrc``: each block's last 1x1 conv adds
+    the block's shortcut, the projection's output or the block input), -1 standing for the
+    stack's input (the stem's 56x56x64 output after max pooling) and ``rsrc`` None for no
+    residual.  Per block: the projection (first block of a stage), the 1x1 reduce, the 3x3, the
+    1x1 expand."""
+    names = [s.name.split("_", 2)[2].split("@")[0] for s in resnet50_layers(1)]
+    index = {n: i for i, n in enumerate(names)}
+    out: List[Tuple[int, int, Optional[int]]] = []
+    block_in = -1
+    for stage, (mid, blocks) in enumerate(((64, 3), (128, 4), (256, 6), (512, 3))):
+        for b in range(blocks):
+            pre = f"s{stage}b{b}"
+            shortcut = block_in
+            if pre + "_proj" in index:
+                out.append((index[pre + "_proj"], block_in, None))
+                shortcut = len(out) - 1
+            out.append((index[pre + "_1x1a"], block_in, None))
+            out.append((index[pre + "_3x3"], len(out) - 1, None))
+            out.append((index[pre + "_1x1b"], len(out) - 1, shortcut))
+            block_in = len(out) - 1
+    return out
+
+
 MOBILENETV2_BLOCKS = [  # (C_in, hidden, C_out, H_in, stride)
     (32, 32, 16, 112, 1),
     (16, 96, 24, 112, 2),

@@ -394,7 +394,7 @@ convf_status conv_fused_run_noalloc(const convf_desc* desc, const void* x, const
  * Steps: handles of CONVF_VARIANT_GEMM_1X1 or CONVF_VARIANT_IMPLICIT_GEMM (force the variant in
  * the desc if the selector would pick another), bf16, group 1, no pre-activation; C and K
  * multiples of 8; every step's output type the same (all fp32 or all bf16).  The chain chooses
- * its own tile width per step (128 x 64 for K <= 64, else 128 x 128) and ignores the handles'
+ * its own tile width per step (128 x 128; 128 x 64 for K <= 64) and ignores the handles'
  * performance knobs.  The handles must outlive the chain (it reads their prepacked weights);
  * the buffers are fixed at create (the tensor maps are encoded for them).
  *
