@@ -289,6 +289,8 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
   for (ChainStep& s : cs) {
     s.g.src_done = s.g.src >= 0 ? cs[s.g.src].g.done : nullptr;
     s.g.rsrc_done = s.g.rsrc >= 0 ? cs[s.g.rsrc].g.done : nullptr;
+    if (s.g.src >= 0) cs[s.g.src].g.consumed = 1;
+    if (s.g.rsrc >= 0) cs[s.g.rsrc].g.consumed = 1;
   }
   cudaError_t e = cudaMemcpy(c->d_steps, cs.data(), sizeof(ChainStep) * n, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(base + steps_bytes, 0, ctr_bytes + 256);

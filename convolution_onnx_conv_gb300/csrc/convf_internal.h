@@ -357,6 +357,7 @@ struct ChainGeom {
   int src;                   // step whose y is this step's x, or -1 (x is written by no step)
   int rsrc;                  // step whose y is this step's residual, or -1
   int src_nb, rsrc_nb;       // n_blocks of those steps (their row blocks' tile counts)
+  int consumed;              // a later step reads this step's output: its tiles are published
   uint32_t* done;            // [mtiles] arrival counters of this step's 128-row blocks
   const uint32_t* src_done;  // the source step's counters, or null
   const uint32_t* rsrc_done; // the residual's source step's counters, or null

@@ -18,8 +18,9 @@
 //   warp 2      weight producer: one TMA box per pipeline step (two k-blocks)
 //   warps 3-10  epilogue, two warpgroups on the two column halves of every tile:
 //               tcgen05.ld -> smem transpose -> clamp(scale*acc + bias (+ r)) -> 16-byte stores
-//   warp 11     publisher: per stored tile, a gpu-scope fence and the increment of the tile's
-//               row-block counter (off the epilogue warps' path)
+//   warp 11     publisher: per stored tile of a step whose output a later step reads, a
+//               gpu-scope fence and the increment of the tile's row-block counter (off the
+//               epilogue warps' path)
 // Pipeline: 3 steps of two 64-wide k-blocks each in shared memory (a step's odd k-block is
 // zero fill past a step's last block).
 #include <cuda_bf16.h>
@@ -395,8 +396,8 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
   int last = -1;
   ChainGeom g;
   uint32_t rtarget = 0;
-  int j = 0;   // tiles of this CTA so far
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
+  int j = 0;   // tiles of this CTA handed to the publisher so far
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
@@ -440,12 +441,16 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
       ch.store(g, wst, row0, lane, p.status);
       __syncwarp();
     }
-    // the tile is stored: hand it to the publisher (once it has taken the slot's previous tile)
-    if (lane == 0) {
-      const int slot = j % kQPub;
-      const bool ok =
-          j < kQPub || mbar_wait(&pubfree[slot], static_cast<uint32_t>((j / kQPub - 1) & 1), abort_flag, p.status);
-      if (ok) mbar_arrive(&stored[slot]);
+    // the tile is stored: hand it to the publisher (once it has taken the slot's previous tile),
+    // unless no later step reads this step's output
+    if (g.consumed) {
+      if (lane == 0) {
+        const int slot = j % kQPub;
+        const bool ok = j < kQPub ||
+                        mbar_wait(&pubfree[slot], static_cast<uint32_t>((j / kQPub - 1) & 1), abort_flag, p.status);
+        if (ok) mbar_arrive(&stored[slot]);
+      }
+      ++j;
     }
     if (++acc == 2) {
       acc = 0;
@@ -454,24 +459,29 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
   }
 }
 
-// Publisher (one thread): for each of the CTA's tiles in order, once all eight epilogue warps
-// have arrived (their stores ordered before their arrivals), a gpu-scope fence makes those
-// stores visible -- the fence is cumulative over what the barrier let this thread observe -- and
-// the tile's row-block counter is raised by one.
+// Publisher (one thread): for each of the CTA's tiles whose step's output a later step reads,
+// in order, once all eight epilogue warps have arrived (their stores ordered before their
+// arrivals), a gpu-scope fence makes those stores visible -- the fence is cumulative over what
+// the barrier let this thread observe -- and the tile's row-block counter is raised by one.
+// (Sharing one fence among tiles already stored when their turn comes saved nothing on the
+// independent steps and delayed the dependent ones' consumers: one fence per tile.)
 __device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t* pubfree, volatile int* abort_flag) {
   const ChainStep* steps = p.steps;
   ChainCursor cur(steps);
   int last = -1, tile0 = 0, nb = 1;
+  bool consumed = false;
   uint32_t* done = nullptr;
   int j = 0;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++j) {
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
       tile0 = steps[L].g.tile0;
       nb = steps[L].g.n_blocks;
       done = steps[L].g.done;
+      consumed = steps[L].g.consumed != 0;
     }
+    if (!consumed) continue;
     const int mt = (t - tile0) / nb;
     const int slot = j % kQPub;
     if (!mbar_wait(&stored[slot], static_cast<uint32_t>((j / kQPub) & 1), abort_flag, p.status)) return;
@@ -479,6 +489,7 @@ __device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t
     fence_proxy_async_global();   // ... and ordered before later async-proxy (TMA) reads of them
     red_relaxed_gpu_add(done + mt, 1u);
     mbar_arrive(&pubfree[slot]);
+    ++j;
   }
 }
 
