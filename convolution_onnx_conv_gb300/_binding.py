@@ -36,7 +36,7 @@ EXPORTED = ["conv_fused_output_shape", "conv_fused_resolve_pads", "conv_bn_scale
             "conv_fused_watchdog_selftest", "conv_fused_run_noalloc", "conv_fused_measure_int8_mma_rate",
             "conv_fused_run_residual", "conv_fused_create_qlinear", "conv_fused_create_preact",
             "conv_fused_create_mbv2_block", "conv_fused_debug_fail_alloc", "conv_fused_debug_live_handles",
-            "conv_fused_chain_create", "conv_fused_chain_run", "conv_fused_chain_status",
+            "conv_fused_chain_create", "conv_fused_chain_create_ex", "conv_fused_chain_run", "conv_fused_chain_status",
             "conv_fused_chain_clear_status", "conv_fused_chain_describe", "conv_fused_chain_destroy"]
 
 
@@ -157,6 +157,7 @@ def load_library(build_if_missing: bool = False):
     lib.conv_fused_debug_fail_alloc.argtypes = [ctypes.c_int]
     lib.conv_fused_debug_live_handles.argtypes = []
     lib.conv_fused_chain_create.argtypes = [P(ChainStep), ctypes.c_int, P(vp)]
+    lib.conv_fused_chain_create_ex.argtypes = [P(ChainStep), ctypes.c_int, ctypes.c_int, P(vp)]
     lib.conv_fused_chain_run.argtypes = [vp, vp]
     lib.conv_fused_chain_status.argtypes = [vp]
     lib.conv_fused_chain_clear_status.argtypes = [vp]
@@ -341,13 +342,14 @@ def conv_fused_run_noalloc(desc: ConvDesc, x, w_packed, scale, bias, y, status=N
                                                  _addr(bias), _addr(y), _addr(status), s))
 
 
-def conv_fused_chain_create(steps) -> int:
-    """steps: sequence of (handle, x, r or None, y) with device pointers (ints) or CUDA tensors."""
+def conv_fused_chain_create(steps, cta_pairs: int = 0) -> int:
+    """steps: sequence of (handle, x, r or None, y) with device pointers (ints) or CUDA tensors;
+    cta_pairs: 0 automatic, 1 single CTAs, 2 CTA pairs (conv_fused_chain_create_ex)."""
     arr = (ChainStep * len(steps))()
     for i, (h, x, r, y) in enumerate(steps):
         arr[i] = ChainStep(h, _addr(x), _addr(r), _addr(y))
     c = ctypes.c_void_p()
-    _check(load_library().conv_fused_chain_create(arr, len(steps), ctypes.byref(c)))
+    _check(load_library().conv_fused_chain_create_ex(arr, len(steps), cta_pairs, ctypes.byref(c)))
     return c.value
 
 
@@ -554,14 +556,14 @@ class ConvChain:
     output.  The tensors and the convs must outlive the chain; calling it runs every step on the
     current torch stream."""
 
-    def __init__(self, steps):
+    def __init__(self, steps, cta_pairs: int = 0):
         self._keep = [tuple(st) for st in steps]
         items = []
         for st in self._keep:
             conv, x, y = st[0], st[1], st[2]
             r = st[3] if len(st) > 3 else None
             items.append((conv.handle, x.data_ptr(), None if r is None else r.data_ptr(), y.data_ptr()))
-        self.handle = conv_fused_chain_create(items)
+        self.handle = conv_fused_chain_create(items, cta_pairs)
 
     def describe(self) -> str:
         return conv_fused_chain_describe(self.handle)

@@ -40,6 +40,7 @@ struct convf_chain {
   int device;
   int grid, nsteps, total_tiles, total_mtiles;
   bool out_bf16;
+  bool pair;             // CTA pairs (256-row tiles)
   void* dev;             // one device allocation: step table, counters, state, status
   ChainStep* d_steps;
   uint32_t* d_counters;
@@ -92,7 +93,14 @@ int find_source(const std::vector<Range>& outs, const convf_chain_step* steps, i
 extern "C" {
 
 convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf_chain** out) {
+  return conv_fused_chain_create_ex(steps, n, 0, out);
+}
+
+convf_status conv_fused_chain_create_ex(const convf_chain_step* steps, int n, int cta_pairs, convf_chain** out) {
   if (!out) return record_error(CONVF_ERR_INVALID_ARG, "out is NULL");
+  if (cta_pairs < 0 || cta_pairs > 2)
+    return record_error(CONVF_ERR_INVALID_ARG, "cta_pairs=%d must be 0 (auto), 1 (single CTAs) or 2 (CTA pairs)",
+                        cta_pairs);
   *out = nullptr;
   if (!steps) return record_error(CONVF_ERR_INVALID_ARG, "steps is NULL");
   if (n < 1 || n > kMaxChainSteps)
@@ -141,14 +149,11 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
       if (outs[i].overlaps(outs[j]))
         return record_error(CONVF_ERR_UNSUPPORTED, "steps %d and %d write overlapping outputs", i, j);
 
-  std::vector<ChainStep> cs(n);
-  std::vector<int> filter(n);
-  long long tiles = 0, mtiles_total = 0;
+  std::vector<int> srcs(n, -1), rsrcs(n, -1);
+  bool dependent = false;
   for (int j = 0; j < n; ++j) {
     const ChainConvInfo& f = info[j];
     const convf_chain_step& st = steps[j];
-    ChainStep& c = cs[j];
-    std::memset(&c, 0, sizeof c);
     const size_t esize = out_bf16 ? 2 : 4;
     const size_t xbytes = static_cast<size_t>(f.N) * f.H * f.W * f.C * 2;
     const Range xr = range_of(st.x, xbytes);
@@ -171,6 +176,30 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
       if (rsrc >= 0 && (info[rsrc].M != f.M || info[rsrc].K != f.K))
         return record_error(CONVF_ERR_INVALID_ARG, "step %d's residual is not shaped like step %d's output", j, rsrc);
     }
+    srcs[j] = src;
+    rsrcs[j] = rsrc;
+    dependent = dependent || src >= 0 || rsrc >= 0;
+  }
+  // CTA pairs: 256-row tiles of up to 256 columns, half the weight bytes per FLOP.  Per layer
+  // shape (ResNet-50, batch 32, steady state) they were 6-25% faster on the wide compute-bound
+  // steps (C and K >= 256 and at least ~150 FLOP per algorithmic byte) and up to 50% slower on
+  // the narrow or HBM-bound ones; they also halve every step's tiles, which leaves SMs idle where
+  // a step waits for a small predecessor.  The automatic choice takes them only for chains of
+  // independent steps that are all wide.
+  bool all_wide = true;
+  for (int j = 0; j < n; ++j) all_wide = all_wide && info[j].C >= 256 && info[j].K >= 256;
+  const bool pair = cta_pairs == 2 || (cta_pairs == 0 && !dependent && all_wide);
+  const int tile_m = pair ? 256 : 128;
+
+  std::vector<ChainStep> cs(n);
+  std::vector<int> filter(n);
+  long long tiles = 0, mtiles_total = 0;
+  for (int j = 0; j < n; ++j) {
+    const ChainConvInfo& f = info[j];
+    const convf_chain_step& st = steps[j];
+    const int src = srcs[j], rsrc = rsrcs[j];
+    ChainStep& c = cs[j];
+    std::memset(&c, 0, sizeof c);
     ChainGeom& g = c.g;
     g.a_mode = f.a_mode;
     g.M = static_cast<int>(f.M);
@@ -179,17 +208,18 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
     g.sh = f.sh; g.sw = f.sw; g.pt = f.pt; g.pl = f.pl; g.dh = f.dh; g.dw = f.dw;
     g.cblocks = f.cblocks;
     g.num_kb = f.num_kb;
-    g.mtiles = static_cast<int>((f.M + 127) / 128);
-    // 128 x 128 tiles (128 x 64 for K <= 64): narrower tiles for steps with fewer tiles than
-    // SMs measured slower, in a chain of independent steps and in a dependent one alike (an
-    // im2col tile's activation loads per FLOP double)
-    g.bn = f.K <= 64 ? 64 : 128;
+    g.mtiles = static_cast<int>((f.M + 127) / 128);   // 128-row blocks (the dependency counters)
+    // single CTAs: 128 x 128 tiles (128 x 64 for K <= 64; narrower tiles for steps with fewer
+    // tiles than SMs measured slower, in a chain of independent steps and in a dependent one
+    // alike: an im2col tile's activation loads per FLOP double); pairs: 256 x 256 (256 x 128 for
+    // K <= 128, 256 x 64 for K <= 64)
+    g.bn = f.K <= 64 ? 64 : (f.K <= 128 || !pair ? 128 : 256);
     g.n_blocks = (f.K + g.bn - 1) / g.bn;
     g.tile0 = static_cast<int>(tiles);
-    tiles += static_cast<long long>(g.mtiles) * g.n_blocks;
+    tiles += (f.M + tile_m - 1) / tile_m * g.n_blocks;
     if (tiles > (1LL << 30)) return record_error(CONVF_ERR_UNSUPPORTED, "more than 2^30 tiles in one chain");
     g.tile_end = static_cast<int>(tiles);
-    g.idesc = idesc_bf16_f32(128, g.bn);
+    g.idesc = idesc_bf16_f32(tile_m, g.bn);
     g.lo = f.lo;
     g.hi = f.hi;
     g.scale = f.scale;
@@ -243,7 +273,7 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
       // (one when the reduction is a single block)
       const cuuint64_t dims[3] = {64, (cuuint64_t)f.K, (cuuint64_t)f.num_kb};
       const cuuint64_t strides[2] = {(cuuint64_t)f.ktot * 2, 128};
-      const cuuint32_t box[3] = {64, (cuuint32_t)g.bn, (cuuint32_t)std::min(2, f.num_kb)};
+      const cuuint32_t box[3] = {64, (cuuint32_t)(pair ? g.bn / 2 : g.bn), (cuuint32_t)std::min(2, f.num_kb)};
       const cuuint32_t es[3] = {1, 1, 1};
       r = enc_tiled(&c.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(f.w), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -253,11 +283,11 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
     }
   }
 
-  const int bps = tc_chain_blocks_per_sm(out_bf16);
   int num_sms = 0;
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
     return record_error(CONVF_ERR_CUDA, "cannot query the SM count");
-  if (bps < 1) return record_error(CONVF_ERR_CUDA, "the chain kernel cannot be resident on this device");
+  const int max_ctas = tc_chain_max_ctas(out_bf16, pair, num_sms);
+  if (max_ctas < (pair ? 2 : 1)) return record_error(CONVF_ERR_CUDA, "the chain kernel cannot be resident on this device");
 
   const bool host_injected = take_injected_alloc_failure();
   convf_chain* c = host_injected ? nullptr : new (std::nothrow) convf_chain();
@@ -268,7 +298,10 @@ convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf
   c->total_tiles = static_cast<int>(tiles);
   c->total_mtiles = static_cast<int>(mtiles_total);
   c->out_bf16 = out_bf16;
-  c->grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(bps) * num_sms));
+  c->pair = pair;
+  // every CTA resident at once (they wait for one another's tiles); a pair takes a tile
+  c->grid = pair ? 2 * static_cast<int>(std::min<long long>(tiles, max_ctas / 2))
+                 : static_cast<int>(std::min<long long>(tiles, max_ctas));
   const size_t steps_bytes = (sizeof(ChainStep) * n + 255) / 256 * 256;
   const size_t ctr_bytes = (static_cast<size_t>(mtiles_total) * 4 + 255) / 256 * 256;
   const size_t bytes = steps_bytes + ctr_bytes + 256;
@@ -320,7 +353,7 @@ convf_status conv_fused_chain_run(convf_chain* c, void* stream) {
   p.total_mtiles = c->total_mtiles;
   p.state = c->d_state;
   p.status = c->d_status;
-  const cudaError_t e = launch_tc_chain(p, c->out_bf16, c->grid, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_tc_chain(p, c->out_bf16, c->pair, c->grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_error(CONVF_ERR_CUDA, "chain launch failed: %s", cudaGetErrorString(e));
   return record_ok();
 }
@@ -352,8 +385,8 @@ convf_status conv_fused_chain_describe(const convf_chain* c, char* buf, size_t l
   if (!buf || len == 0) return record_error(CONVF_ERR_INVALID_ARG, "buf is NULL or len is 0");
   std::string s;
   char line[160];
-  snprintf(line, sizeof line, "steps=%d tiles=%d grid=%d out=%s", c->nsteps, c->total_tiles, c->grid,
-           c->out_bf16 ? "bf16" : "f32");
+  snprintf(line, sizeof line, "steps=%d tiles=%d grid=%d cta_pairs=%d out=%s", c->nsteps, c->total_tiles, c->grid,
+           c->pair ? 1 : 0, c->out_bf16 ? "bf16" : "f32");
   s += line;
   for (int j = 0; j < c->nsteps; ++j) {
     const ChainGeom& q = c->steps[j].g;
@@ -362,8 +395,8 @@ convf_status conv_fused_chain_describe(const convf_chain* c, char* buf, size_t l
       snprintf(rs, sizeof rs, "none");
     else
       snprintf(rs, sizeof rs, "%d", q.rsrc);
-    snprintf(line, sizeof line, " | %d:%dx%d M=%d K=%d tile=128x%d kb=%d%s src=%d res=%s", j, c->filter[j] / 100,
-             c->filter[j] % 100, q.M, q.Kout, q.bn, q.num_kb, q.a3d ? " a3d" : "", q.src, rs);
+    snprintf(line, sizeof line, " | %d:%dx%d M=%d K=%d tile=%dx%d kb=%d%s src=%d res=%s", j, c->filter[j] / 100,
+             c->filter[j] % 100, q.M, q.Kout, c->pair ? 256 : 128, q.bn, q.num_kb, q.a3d ? " a3d" : "", q.src, rs);
     s += line;
   }
   snprintf(buf, len, "%s", s.c_str());

@@ -376,9 +376,11 @@ struct ChainParams {
   uint32_t* state;           // [0] launches completed so far (the epoch), [1] CTAs done this launch
   int* status;               // device status word (timeout / bounds bits), sticky
 };
-// out_bf16: y and the residuals hold bf16 (else fp32).  grid <= co-resident CTAs (one per SM).
-cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, int grid, cudaStream_t stream);
-// CTAs of the chain kernel that fit one SM at a time (1 on sm_103a; 0 if it cannot run)
-int tc_chain_blocks_per_sm(bool out_bf16);
+// out_bf16: y and the residuals hold bf16 (else fp32).  pair: CTA pairs (clusters of two, 256-row
+// tiles; the step table's tile numbering and weight maps must be made for them).  grid <= the
+// CTAs that can be resident at once (tc_chain_max_ctas), even for pairs.
+cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, bool pair, int grid, cudaStream_t stream);
+// CTAs of the chain kernel that can be resident at once on a GPU of num_sms SMs (0 if none)
+int tc_chain_max_ctas(bool out_bf16, bool pair, int num_sms);
 
 }  // namespace convf

@@ -33,17 +33,39 @@ namespace {
 
 constexpr int kQM = 128;                    // tile rows
 constexpr int kQK = 64;                     // reduction block
-constexpr int kQBNMax = 128;                // widest tile (TMEM buffer stride)
 constexpr int kQSlots = 6;                  // k-block slots
 constexpr int kQSteps = kQSlots / 2;        // pipeline steps of two k-blocks
 constexpr int kQATile = kQM * kQK * 2;      // 16 KB
-constexpr int kQBTile = kQBNMax * kQK * 2;  // 16 KB
+constexpr int kQBTile = 128 * kQK * 2;      // 16 KB: one k-block of up to 128 weight rows
 constexpr int kQEpiWarpBytes = 32 * 32 * 4;
 constexpr int kQThreads = 96 + 256 + 32;     // producer, MMA, weight producer, 8 epilogue warps, publisher
 constexpr int kQPub = 4;                    // tiles a CTA may have stored but not yet published
 constexpr int kQSmem = 1024 + kQSlots * (kQATile + kQBTile) + 8 * kQEpiWarpBytes + 256;
 static_assert(kQSmem <= 232448, "shared memory budget");
 static_assert(kChainArrivals == 1, "one arrival per tile (the publisher's)");
+
+// Single CTAs (128-row tiles, up to 128 columns) or CTA pairs (cta_group::2: 256-row tiles of up
+// to 256 columns, each CTA of the cluster holding its own 128 rows of activations and of the
+// accumulator and half of the weight rows).  A pair moves half the weight bytes per FLOP of a
+// single CTA's 128 x 128 tile and issues M = 256 MMAs.
+template <bool PAIR>
+struct ChainShape {
+  static constexpr int kTileM = PAIR ? 256 : 128;   // output rows per tile
+  static constexpr int kBNMax = PAIR ? 256 : 128;   // widest tile (TMEM buffer stride)
+};
+
+// The tiles of this CTA (or CTA pair) and this CTA's first row within a tile.
+template <bool PAIR>
+struct ChainSched {
+  int tstart, tstep, rowoff;
+  uint32_t crank;
+  __device__ ChainSched() {
+    crank = PAIR ? cluster_ctarank() : 0u;
+    tstart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    tstep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    rowoff = static_cast<int>(crank) * kQM;
+  }
+};
 
 // Wait until the counter reaches `target` (wrap-safe).  Gives up, raising the CTA's abort flag,
 // when another role of this CTA aborted, when any CTA flagged an error in the status word, or
@@ -116,11 +138,15 @@ struct ChainKPos {
 // ROLE 2 (warp 2): the weight box of each step.  (Moving the odd k-block's activation load from
 // the weight producer to the activation producer measured 2-5% faster on every layer shape.)
 // Every role keeps the current step's fields in registers (ChainGeom, reloaded when the step
-// changes): the issuing thread's scalar work delays its next copy.
-template <int ROLE>
+// changes): the issuing thread's scalar work delays its next copy.  In a CTA pair both CTAs load
+// their own operands; every load completes on the leader's full barrier, which the leader's
+// producers arm with both CTAs' bytes.
+template <int ROLE, bool PAIR>
 __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
                                uint32_t epoch1, volatile int* abort_flag) {
   const ChainStep* steps = p.steps;
+  const ChainSched<PAIR> sch;
+  const bool leader = sch.crank == 0;
   ChainCursor cur(steps);
   int stage = 0;
   uint32_t phase = 0;
@@ -130,7 +156,8 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
   const CUtensorMap* tmA = nullptr;
   const CUtensorMap* tmB = nullptr;
   uint32_t b_bytes = 0, target = 0;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  int bcol = 0;        // this CTA's first weight row within a tile (half of the tile in a pair)
+  for (int t = sch.tstart; t < p.total_tiles; t += sch.tstep) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
@@ -139,16 +166,19 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
       tmB = &steps[L].tmB;
       tma_prefetch_desc(ROLE == 0 ? tmA : tmB);
       dep_done = -1;
-      // the weight box holds two k-blocks (zero fill past the last), one if the step has one
-      b_bytes = static_cast<uint32_t>((g.num_kb > 1 ? 2 : 1) * g.bn * kQK * 2);
+      // this CTA's weight box: two k-blocks (zero fill past the last), one if the step has one,
+      // of bn rows (bn / 2 in a pair)
+      const int brows = PAIR ? g.bn / 2 : g.bn;
+      b_bytes = static_cast<uint32_t>((g.num_kb > 1 ? 2 : 1) * brows * kQK * 2);
+      bcol = static_cast<int>(sch.crank) * brows;
       target = epoch1 * static_cast<uint32_t>(kChainArrivals * g.src_nb);
     }
     const int local = t - g.tile0;
     const int mt = local / g.n_blocks;
     const int n0 = (local - mt * g.n_blocks) * g.bn;
-    const int m0 = mt * kQM;
+    const int m0 = mt * ChainShape<PAIR>::kTileM + sch.rowoff;   // this CTA's first output row
     const bool a3d = g.a3d != 0, a2d = g.a_mode == kA2D;
-    if (ROLE == 0 && g.src >= 0) {
+    if (ROLE == 0 && g.src >= 0 && m0 < g.M) {
       int lo, hi;
       chain_input_rows(g, m0, lo, hi);
       // this CTA's tiles of one step visit increasing rows, so the blocks below dep_done that
@@ -172,32 +202,44 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
       const bool two = kb + 1 < g.num_kb;
       if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) return;
       uint8_t* a0 = sA + stage * 2 * kQATile;
+      uint64_t* fb = &full[stage];
+      const uint32_t fbar = PAIR ? map_to_rank(smem_u32(fb), 0) : smem_u32(fb);   // the leader's
       if constexpr (ROLE == 0) {
         ChainKPos q1 = q;   // k-block kb + 1
         q1.next(g.cblocks, g.S);
+        const uint32_t a_bytes = a3d || two ? 2u * kQATile : static_cast<uint32_t>(kQATile);
+        if (leader) mbar_arrive_expect_tx(fb, PAIR ? 2 * a_bytes : a_bytes);
         if (a3d) {
-          mbar_arrive_expect_tx(&full[stage], 2 * kQATile);
-          tma_load_3d(a0, tmA, &full[stage], 0, m0, kb);
-        } else {
-          mbar_arrive_expect_tx(&full[stage], kQATile * (two ? 2u : 1u));
-          if (a2d)
-            tma_load_2d(a0, tmA, &full[stage], kb * kQK, m0);
+          if (PAIR)
+            tma_load_3d_pair(a0, tmA, fbar, 0, m0, kb);
           else
-            tma_load_im2col_4d(a0, tmA, &full[stage], q.cb * kQK, wb, hb, img, static_cast<uint16_t>(q.s * g.dw),
-                               static_cast<uint16_t>(q.r * g.dh));
-          if (two) {
-            if (a2d)
-              tma_load_2d(a0 + kQATile, tmA, &full[stage], (kb + 1) * kQK, m0);
-            else
-              tma_load_im2col_4d(a0 + kQATile, tmA, &full[stage], q1.cb * kQK, wb, hb, img,
-                                 static_cast<uint16_t>(q1.s * g.dw), static_cast<uint16_t>(q1.r * g.dh));
+            tma_load_3d(a0, tmA, fb, 0, m0, kb);
+        } else {
+          for (int jk = 0; jk < (two ? 2 : 1); ++jk) {
+            const ChainKPos& qq = jk == 0 ? q : q1;
+            uint8_t* dst = a0 + jk * kQATile;
+            if (a2d) {
+              if (PAIR)
+                tma_load_2d_pair(dst, tmA, fbar, (kb + jk) * kQK, m0);
+              else
+                tma_load_2d(dst, tmA, fb, (kb + jk) * kQK, m0);
+            } else {
+              const uint16_t ow = static_cast<uint16_t>(qq.s * g.dw), oh = static_cast<uint16_t>(qq.r * g.dh);
+              if (PAIR)
+                tma_load_im2col_4d_pair(dst, tmA, fbar, qq.cb * kQK, wb, hb, img, ow, oh);
+              else
+                tma_load_im2col_4d(dst, tmA, fb, qq.cb * kQK, wb, hb, img, ow, oh);
+            }
           }
         }
         q = q1;
         q.next(g.cblocks, g.S);
       } else {
-        mbar_arrive_expect_tx(&full[stage], b_bytes);
-        tma_load_3d(sB + stage * 2 * kQBTile, tmB, &full[stage], 0, n0, kb);
+        if (leader) mbar_arrive_expect_tx(fb, PAIR ? 2 * b_bytes : b_bytes);
+        if (PAIR)
+          tma_load_3d_pair(sB + stage * 2 * kQBTile, tmB, fbar, 0, n0 + bcol, kb);
+        else
+          tma_load_3d(sB + stage * 2 * kQBTile, tmB, fb, 0, n0, kb);
       }
       if (++stage == kQSteps) {
         stage = 0;
@@ -207,11 +249,14 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
   }
 }
 
-// MMA issuer (one thread): per tile, one 128 x bn accumulator buffer (alternating), four
-// K = 16 MMAs per k-block.
+// MMA issuer (one thread; the leader's in a CTA pair): per tile, one kTileM x bn accumulator
+// buffer (alternating), four K = 16 MMAs per k-block.  A pair's MMAs read both CTAs' operands and
+// write both CTAs' TMEM; their commits arrive on the barriers of both CTAs.
+template <bool PAIR>
 __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
                           uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
   const ChainStep* steps = p.steps;
+  const ChainSched<PAIR> sch;
   ChainCursor cur(steps);
   const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(sA));
   const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(sB));
@@ -222,17 +267,18 @@ __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64
   int last = -1;
   uint32_t idesc = 0, bblock = 0;
   int num_kb = 0;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  for (int t = sch.tstart; t < p.total_tiles; t += sch.tstep) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
       idesc = steps[L].g.idesc;
       num_kb = steps[L].g.num_kb;
-      bblock = static_cast<uint32_t>(steps[L].g.bn * kQK * 2);   // bytes of one k-block's weights
+      // bytes of one k-block's weights in this CTA's shared memory
+      bblock = static_cast<uint32_t>((PAIR ? steps[L].g.bn / 2 : steps[L].g.bn) * kQK * 2);
     }
     if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) return;
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kQBNMax);
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ChainShape<PAIR>::kBNMax);
     for (int kb = 0; kb < num_kb; kb += 2) {
       if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) return;
       tc_fence_after();
@@ -241,16 +287,27 @@ __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64
         const uint64_t adesc = adesc0 + (static_cast<uint32_t>((stage * 2 + j) * kQATile) >> 4);
         const uint64_t bdesc = bdesc0 + ((static_cast<uint32_t>(stage * 2 * kQBTile) + j * bblock) >> 4);
 #pragma unroll
-        for (int k = 0; k < kQK / 16; ++k)
-          tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kQK / 16; ++k) {
+          const uint32_t accum = (kb + j > 0 || k > 0) ? 1u : 0u;
+          if (PAIR)
+            tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, accum);
+          else
+            tc_mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, accum);
+        }
       }
-      tc_commit(&empty[stage]);
+      if (PAIR)
+        tc_commit_pair(&empty[stage], 3);
+      else
+        tc_commit(&empty[stage]);
       if (++stage == kQSteps) {
         stage = 0;
         phase ^= 1;
       }
     }
-    tc_commit(&tfull[acc]);
+    if (PAIR)
+      tc_commit_pair(&tfull[acc], 3);
+    else
+      tc_commit(&tfull[acc]);
     if (++acc == 2) {
       acc = 0;
       acc_phase ^= 1;
@@ -380,7 +437,7 @@ __device__ __forceinline__ void chain_stage_chunk(float* wst, const uint32_t (&v
                     __uint_as_float(v[4 * cc + 3]));
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool PAIR>
 __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tfull, uint64_t* tempty,
                                uint64_t* stored, uint64_t* pubfree, uint32_t tmem_base, uint32_t epoch1,
                                volatile int* abort_flag) {
@@ -390,6 +447,7 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
   const int q = warp & 3;   // TMEM lane quadrant this warp may access
   float* wst = reinterpret_cast<float*>(sEpi + (warp - 3) * kQEpiWarpBytes);
   const ChainStep* steps = p.steps;
+  const ChainSched<PAIR> sch;
   ChainCursor cur(steps);
   int acc = 0;
   uint32_t acc_phase = 0;
@@ -397,7 +455,7 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
   ChainGeom g;
   uint32_t rtarget = 0;
   int j = 0;   // tiles of this CTA handed to the publisher so far
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  for (int t = sch.tstart; t < p.total_tiles; t += sch.tstep) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
@@ -407,43 +465,83 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
     const int local = t - g.tile0;
     const int mt = local / g.n_blocks;
     const int n0 = (local - mt * g.n_blocks) * g.bn;
-    const int row0 = mt * kQM + q * 32;
-    const int half = g.bn >> 1;
-    const bool two = half > 32;   // two 32-column chunks (128-wide tiles) or one
+    const int m0 = mt * ChainShape<PAIR>::kTileM + sch.rowoff;   // this CTA's first row of the tile
+    const int rb = m0 / kQM;                                     // its 128-row block
+    const bool rows = m0 < g.M;                                  // a pair's second half may lie past M
+    const int row0 = m0 + q * 32;
+    const int half = g.bn >> 1;   // this group's columns: 32, 64 or 128
+    const int nch = half >> 5;
     const int col0 = n0 + eg * half;
     if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) return;
     tc_fence_after();
-    if (g.res != nullptr && g.rsrc >= 0) {
-      // the residual rows of this tile are the producing step's row block mt (same shape)
+    if (rows && g.res != nullptr && g.rsrc >= 0) {
+      // the residual rows of this tile are the producing step's row block rb (same shape)
       int ok = 1;
-      if (lane == 0) ok = chain_wait(g.rsrc_done + mt, rtarget, p.status, abort_flag);
+      if (lane == 0) ok = chain_wait(g.rsrc_done + rb, rtarget, p.status, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     }
-    uint32_t v0[32], v1[32];
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kQBNMax + eg * half);
-    tmem_ld_32x32b_x32(taddr, v0);
-    if (two) tmem_ld_32x32b_x32(taddr + 32, v1);
-    ChainEpiChunk<OUT_BF16> ch;
-    ch.load(g, col0, row0, lane, p.status);
-    tmem_ld_wait();
-    // the warp's TMEM reads of the tile are done: the buffer goes back to the MMA issuer
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&tempty[acc]);
-    chain_stage_chunk(wst, v0, lane);
-    __syncwarp();
-    ch.store(g, wst, row0, lane, p.status);
-    __syncwarp();   // the chunk's smem reads are done before the next chunk is written
-    if (two) {
-      ch.load(g, col0 + 32, row0, lane, p.status);
-      chain_stage_chunk(wst, v1, lane);
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(acc * ChainShape<PAIR>::kBNMax + eg * half);
+    // chunk pairs: both chunks of a pair read from TMEM at once; after the last pair's reads the
+    // buffer goes back to the MMA issuer (the leader's barrier in a CTA pair)
+    auto release_tmem = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && sch.crank != 0)
+          mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+        else
+          mbar_arrive(&tempty[acc]);
+      }
+    };
+    if constexpr (!PAIR) {
+      // at most one pair (128-column tiles): straight-line code, as few registers as possible
+      const bool two = nch > 1;
+      uint32_t v0[32], v1[32];
+      tmem_ld_32x32b_x32(taddr, v0);
+      if (two) tmem_ld_32x32b_x32(taddr + 32, v1);
+      ChainEpiChunk<OUT_BF16> ch;
+      ch.load(g, col0, row0, lane, p.status);
+      tmem_ld_wait();
+      release_tmem();
+      chain_stage_chunk(wst, v0, lane);
       __syncwarp();
       ch.store(g, wst, row0, lane, p.status);
-      __syncwarp();
+      __syncwarp();   // the chunk's smem reads are done before the next chunk is written
+      if (two) {
+        ch.load(g, col0 + 32, row0, lane, p.status);
+        chain_stage_chunk(wst, v1, lane);
+        __syncwarp();
+        ch.store(g, wst, row0, lane, p.status);
+        __syncwarp();
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < nch; c += 2) {
+        const bool two = c + 1 < nch;
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr + 32 * c, v0);
+        if (two) tmem_ld_32x32b_x32(taddr + 32 * c + 32, v1);
+        ChainEpiChunk<OUT_BF16> ch;
+        ch.load(g, col0 + 32 * c, row0, lane, p.status);
+        tmem_ld_wait();
+        if (c + 2 >= nch) release_tmem();
+        chain_stage_chunk(wst, v0, lane);
+        __syncwarp();
+        ch.store(g, wst, row0, lane, p.status);
+        __syncwarp();
+        if (two) {
+          ch.load(g, col0 + 32 * c + 32, row0, lane, p.status);
+          chain_stage_chunk(wst, v1, lane);
+          __syncwarp();
+          ch.store(g, wst, row0, lane, p.status);
+          __syncwarp();
+        }
+      }
     }
     // the tile is stored: hand it to the publisher (once it has taken the slot's previous tile),
     // unless no later step reads this step's output
-    if (g.consumed) {
+    if (g.consumed && rows) {
       if (lane == 0) {
         const int slot = j % kQPub;
         const bool ok = j < kQPub ||
@@ -462,39 +560,44 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
 // Publisher (one thread): for each of the CTA's tiles whose step's output a later step reads,
 // in order, once all eight epilogue warps have arrived (their stores ordered before their
 // arrivals), a gpu-scope fence makes those stores visible -- the fence is cumulative over what
-// the barrier let this thread observe -- and the tile's row-block counter is raised by one.
-// (Sharing one fence among tiles already stored when their turn comes saved nothing on the
-// independent steps and delayed the dependent ones' consumers: one fence per tile.)
+// the barrier let this thread observe -- and the counter of the CTA's 128-row block of the tile
+// is raised by one.  (Sharing one fence among tiles already stored when their turn comes saved
+// nothing on the independent steps and delayed the dependent ones' consumers: one fence per
+// tile.)
+template <bool PAIR>
 __device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t* pubfree, volatile int* abort_flag) {
   const ChainStep* steps = p.steps;
+  const ChainSched<PAIR> sch;
   ChainCursor cur(steps);
-  int last = -1, tile0 = 0, nb = 1;
+  int last = -1, tile0 = 0, nb = 1, M = 0;
   bool consumed = false;
   uint32_t* done = nullptr;
   int j = 0;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  for (int t = sch.tstart; t < p.total_tiles; t += sch.tstep) {
     const int L = cur.at(t);
     if (L != last) {
       last = L;
       tile0 = steps[L].g.tile0;
       nb = steps[L].g.n_blocks;
       done = steps[L].g.done;
+      M = steps[L].g.M;
       consumed = steps[L].g.consumed != 0;
     }
-    if (!consumed) continue;
-    const int mt = (t - tile0) / nb;
+    const int m0 = ((t - tile0) / nb) * ChainShape<PAIR>::kTileM + sch.rowoff;
+    if (!consumed || m0 >= M) continue;
     const int slot = j % kQPub;
     if (!mbar_wait(&stored[slot], static_cast<uint32_t>((j / kQPub) & 1), abort_flag, p.status)) return;
     fence_acq_rel_gpu();
     fence_proxy_async_global();   // ... and ordered before later async-proxy (TMA) reads of them
-    red_relaxed_gpu_add(done + mt, 1u);
+    red_relaxed_gpu_add(done + m0 / kQM, 1u);
     mbar_arrive(&pubfree[slot]);
     ++j;
   }
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool PAIR>
 __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParams p) {
+  constexpr uint32_t kTmemCols = 2 * ChainShape<PAIR>::kBNMax;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -516,12 +619,12 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQSteps; ++s) {
-      mbar_init(&full[s], 2);    // activation producer + weight producer
+      mbar_init(&full[s], 2);    // activation producer + weight producer (the leader's, in a pair)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // every epilogue warp
+      mbar_init(&tempty[b], PAIR ? 16 : 8);  // every epilogue warp (of both CTAs of a pair)
     }
     for (int b = 0; b < kQPub; ++b) {
       mbar_init(&stored[b], 8);  // every epilogue warp
@@ -531,11 +634,17 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * kQBNMax);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers and TMEM exist before any cross-CTA operation
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // the next kernel may launch once every CTA of this grid has started (so none of this
@@ -546,20 +655,24 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
   // data: whatever the previous kernel still writes lands in L2, which serves every read after
   // the wait).
   if (lane == 0 && (warp == 0 || warp == 2)) {
-    const int t = blockIdx.x;
+    const ChainSched<PAIR> sch;
+    const int t = sch.tstart;
     int L = 0;
     while (t >= p.steps[L].g.tile_end) ++L;
     const ChainGeom& g = p.steps[L].g;
     const int local = t - g.tile0;
     const int mt = local / g.n_blocks;
+    const int m0 = mt * ChainShape<PAIR>::kTileM + sch.rowoff;
     if (warp == 2) {
+      const int brows = PAIR ? g.bn / 2 : g.bn;
       tma_prefetch_desc(&p.steps[L].tmB);
       for (int kb = 0; kb < min(g.num_kb, 4); kb += 2)
-        tma_prefetch_l2_3d(&p.steps[L].tmB, 0, (local - mt * g.n_blocks) * g.bn, kb);
-    } else if (g.src < 0) {
+        tma_prefetch_l2_3d(&p.steps[L].tmB, 0, (local - mt * g.n_blocks) * g.bn + static_cast<int>(sch.crank) * brows,
+                           kb);
+    } else if (g.src < 0 && m0 < g.M) {
       tma_prefetch_desc(&p.steps[L].tmA);
       int lo, hi;
-      chain_input_rows(g, mt * kQM, lo, hi);
+      chain_input_rows(g, m0, lo, hi);
       bulk_prefetch_l2(static_cast<const uint16_t*>(g.x) + static_cast<size_t>(lo) * g.C,
                        static_cast<uint32_t>(hi - lo + 1) * g.C * 2);
     }
@@ -568,17 +681,18 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
   if (threadIdx.x == 0) *epoch_slot = *reinterpret_cast<volatile uint32_t*>(p.state);
   __syncthreads();
   const uint32_t epoch1 = *epoch_slot + 1u;
+  const bool leader = !PAIR || cluster_ctarank() == 0;
 
   if (warp == 0) {
-    if (lane == 0) chain_producer<0>(p, sA, sB, full, empty, epoch1, abort_flag);
+    if (lane == 0) chain_producer<0, PAIR>(p, sA, sB, full, empty, epoch1, abort_flag);
   } else if (warp == 2) {
-    if (lane == 0) chain_producer<2>(p, sA, sB, full, empty, epoch1, abort_flag);
+    if (lane == 0) chain_producer<2, PAIR>(p, sA, sB, full, empty, epoch1, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) chain_mma(p, sA, sB, full, empty, tfull, tempty, tmem_base, abort_flag);
+    if (lane == 0 && leader) chain_mma<PAIR>(p, sA, sB, full, empty, tfull, tempty, tmem_base, abort_flag);
   } else if (warp == 11) {
-    if (lane == 0) chain_publisher(p, stored, pubfree, abort_flag);
+    if (lane == 0) chain_publisher<PAIR>(p, stored, pubfree, abort_flag);
   } else {
-    chain_epilogue<OUT_BF16>(p, sEpi, tfull, tempty, stored, pubfree, tmem_base, epoch1, abort_flag);
+    chain_epilogue<OUT_BF16, PAIR>(p, sEpi, tfull, tempty, stored, pubfree, tmem_base, epoch1, abort_flag);
   }
 
   __syncthreads();
@@ -587,10 +701,14 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
     for (int i = 0; i < 2000; ++i) __nanosleep(100000);
   }
   __syncthreads();
+  if (PAIR) cluster_sync();   // no CTA of a pair leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * kQBNMax);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
   if (threadIdx.x == 0) {
     // the last CTA out advances the epoch (or, after an error, restarts the counters at zero)
@@ -610,38 +728,62 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
   }
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool PAIR>
 cudaError_t chain_configure() {
-  static cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel<OUT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              kQSmem);
+  static cudaError_t e = [] {
+    cudaError_t r = cudaFuncSetAttribute(tc_chain_kernel<OUT_BF16, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kQSmem);
+    if (r == cudaSuccess && PAIR)
+      r = cudaFuncSetAttribute(tc_chain_kernel<OUT_BF16, PAIR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    return r;
+  }();
   return e;
+}
+
+template <bool OUT_BF16, bool PAIR>
+cudaError_t chain_launch(const ChainParams& p, int grid, cudaStream_t stream) {
+  const cudaError_t e = chain_configure<OUT_BF16, PAIR>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tc_chain_kernel<OUT_BF16, PAIR>, dim3(grid), dim3(kQThreads), kQSmem, stream, PAIR ? 2 : 1, p);
+}
+
+// CTAs that can be resident at once: one per SM, or (pairs) two per co-resident cluster
+template <bool OUT_BF16, bool PAIR>
+int chain_max_ctas(int num_sms) {
+  if (chain_configure<OUT_BF16, PAIR>() != cudaSuccess) return 0;
+  if (!PAIR) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_chain_kernel<OUT_BF16, PAIR>, kQThreads, kQSmem) !=
+        cudaSuccess)
+      return 0;
+    return n * num_sms;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = kQSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, tc_chain_kernel<OUT_BF16, PAIR>, &cfg) != cudaSuccess) return 0;
+  return 2 * clusters;
 }
 
 }  // namespace
 
-cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, int grid, cudaStream_t stream) {
-  if (out_bf16) {
-    cudaError_t e = chain_configure<true>();
-    if (e != cudaSuccess) return e;
-    return launch_pdl(tc_chain_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, stream, 1, p);
-  }
-  cudaError_t e = chain_configure<false>();
-  if (e != cudaSuccess) return e;
-  return launch_pdl(tc_chain_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, stream, 1, p);
+cudaError_t launch_tc_chain(const ChainParams& p, bool out_bf16, bool pair, int grid, cudaStream_t stream) {
+  if (pair) return out_bf16 ? chain_launch<true, true>(p, grid, stream) : chain_launch<false, true>(p, grid, stream);
+  return out_bf16 ? chain_launch<true, false>(p, grid, stream) : chain_launch<false, false>(p, grid, stream);
 }
 
-int tc_chain_blocks_per_sm(bool out_bf16) {
-  int n = 0;
-  cudaError_t e;
-  if (out_bf16) {
-    e = chain_configure<true>();
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_chain_kernel<true>, kQThreads, kQSmem);
-  } else {
-    e = chain_configure<false>();
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_chain_kernel<false>, kQThreads, kQSmem);
-  }
-  return e == cudaSuccess ? n : 0;
+int tc_chain_max_ctas(bool out_bf16, bool pair, int num_sms) {
+  if (pair) return out_bf16 ? chain_max_ctas<true, true>(num_sms) : chain_max_ctas<false, true>(num_sms);
+  return out_bf16 ? chain_max_ctas<true, false>(num_sms) : chain_max_ctas<false, false>(num_sms);
 }
 
 }  // namespace convf

@@ -394,12 +394,12 @@ convf_status conv_fused_run_noalloc(const convf_desc* desc, const void* x, const
  * Steps: handles of CONVF_VARIANT_GEMM_1X1 or CONVF_VARIANT_IMPLICIT_GEMM (force the variant in
  * the desc if the selector would pick another), bf16, group 1, no pre-activation; C and K
  * multiples of 8; every step's output type the same (all fp32 or all bf16).  The chain chooses
- * its own tile width per step (128 x 128; 128 x 64 for K <= 64) and ignores the handles'
+ * its own tile shape per step (see conv_fused_chain_create_ex) and ignores the handles'
  * performance knobs.  The handles must outlive the chain (it reads their prepacked weights);
  * the buffers are fixed at create (the tensor maps are encoded for them).
  *
  * The chain's CTAs wait for one another's tiles, so they must all be resident at once: the
- * launch uses at most one CTA per SM.  A wait that runs out (or any error bit in the chain's
+ * launch uses at most one CTA per SM (and, with CTA pairs, at most the clusters that fit).  A wait that runs out (or any error bit in the chain's
  * status word) makes every CTA give up; conv_fused_chain_status then reports it, and runs
  * after that give up at once until conv_fused_chain_clear_status.
  */
@@ -413,8 +413,16 @@ typedef struct {
 } convf_chain_step;
 
 /* Validates the n steps (host array, copied), finds their dependencies, encodes their tensor
- * maps and uploads the step table (one device allocation; synchronises the device once). */
+ * maps and uploads the step table (one device allocation; synchronises the device once).
+ * Equivalent to conv_fused_chain_create_ex(steps, n, 0, out). */
 convf_status conv_fused_chain_create(const convf_chain_step* steps, int n, convf_chain** out);
+/* The same with a choice of tiles: cta_pairs = 1 runs single CTAs (128-row tiles of 64 or 128
+ * columns); 2 runs CTA pairs (clusters of two CTAs sharing tcgen05 MMAs of 256 rows: tiles of
+ * 256 rows and 64, 128 or 256 columns, each CTA loading half the weight rows, which halves the
+ * weight bytes per FLOP but also the number of tiles); 0 chooses pairs when no step reads another
+ * step's output and every step has C and K of at least 256, single CTAs otherwise.  Results are
+ * the same either way. */
+convf_status conv_fused_chain_create_ex(const convf_chain_step* steps, int n, int cta_pairs, convf_chain** out);
 /* One launch of the whole sequence on `stream` (a cudaStream_t, NULL = legacy default stream).
  * Asynchronous; allocates nothing; may be captured in a CUDA graph.  Runs of one chain must not
  * overlap in time (use one stream). */

@@ -99,7 +99,8 @@ INDEP = [
 ]
 
 
-def test_independent_steps_match_the_oracle_every_output():
+@pytest.mark.parametrize("pairs", [1, 2], ids=["single", "pairs"])
+def test_independent_steps_match_the_oracle_every_output(pairs):
     steps, refs, convs, ys, keep = [], [], [], [], []
     for i, spec in enumerate(INDEP):
         inp = inputs_for(spec, 9100 + i)
@@ -111,9 +112,9 @@ def test_independent_steps_match_the_oracle_every_output():
         ys.append(y)
         keep.append(x)
         refs.append(oracle_step(spec, inp["x"].double().numpy(), inp))
-    chain = cf.ConvChain(steps)
+    chain = cf.ConvChain(steps, cta_pairs=pairs)
     d = chain.describe()
-    assert f"steps={len(INDEP)}" in d and "out=f32" in d, d
+    assert f"steps={len(INDEP)}" in d and "out=f32" in d and f"cta_pairs={pairs - 1}" in d, d
     assert " a3d" in d and "src=-1" in d and "src=0" not in d, d
     first = None
     for run in range(3):
@@ -160,7 +161,7 @@ def bottleneck_chain(N, H, W, cin, mid, cout, stride, blocks, seed):
     return [(spec, inputs_for(spec, seed + i), src, rsrc) for i, (spec, src, rsrc) in enumerate(out)]
 
 
-def run_bf16_chain(N, H, W, cin, mid, cout, stride, blocks, seed, graph=False):
+def run_bf16_chain(N, H, W, cin, mid, cout, stride, blocks, seed, graph=False, pairs=0):
     plan = bottleneck_chain(N, H, W, cin, mid, cout, stride, blocks, seed)
     g = torch.Generator().manual_seed(seed - 1)
     x0 = torch.randn((N, cin, H, W), generator=g).to(torch.bfloat16)
@@ -176,7 +177,7 @@ def run_bf16_chain(N, H, W, cin, mid, cout, stride, blocks, seed, graph=False):
             steps.append((conv, x, y, x0d if rsrc < 0 else ys[rsrc]))
         convs.append(conv)
         ys.append(y)
-    chain = cf.ConvChain(steps)
+    chain = cf.ConvChain(steps, cta_pairs=pairs)
     # the oracle's chain: each output rounded like the kernel's (float32, then bf16)
     refs = []
     for spec, inp, src, rsrc in plan:
@@ -209,6 +210,7 @@ def run_bf16_chain(N, H, W, cin, mid, cout, stride, blocks, seed, graph=False):
     return plan, refs, results, d
 
 
+@pytest.mark.parametrize("pairs", [0, 2], ids=["auto", "pairs"])
 @pytest.mark.parametrize("shape", [
     # (N, H, W, cin, mid, cout, stride, blocks): few tiles per step (every step in flight at
     # once), and more tiles per step than there are SMs (row blocks completed wave by wave)
@@ -216,9 +218,10 @@ def run_bf16_chain(N, H, W, cin, mid, cout, stride, blocks, seed, graph=False):
     (8, 56, 56, 64, 64, 256, 1, 2),
     (4, 28, 28, 256, 128, 512, 2, 2),
 ], ids=["small", "56x56_b8", "28x28_s2_b4"])
-def test_bottleneck_chain_matches_the_oracle_chain(shape):
-    plan, refs, results, d = run_bf16_chain(*shape, seed=9300 + shape[1], graph=False)
+def test_bottleneck_chain_matches_the_oracle_chain(shape, pairs):
+    plan, refs, results, d = run_bf16_chain(*shape, seed=9300 + shape[1], graph=False, pairs=pairs)
     assert "out=bf16" in d and "src=1" in d and "res=0" in d, d
+    assert f"cta_pairs={1 if pairs == 2 else 0}" in d, d   # narrow or dependent steps: single CTAs unless asked
     for run, outs in enumerate(results):
         for (spec, _, src, rsrc), got, ref in zip(plan, outs, refs):
             assert np.all(np.isfinite(got)), (spec.name, run, "a tile read its input before it was stored")
@@ -309,7 +312,8 @@ def test_chain_allocation_failure_is_reported_and_leaves_nothing_behind():
 
 # ------------------------------------------------------------------ exact integer chain
 
-def test_integer_chain_is_bit_exact():
+@pytest.mark.parametrize("pairs", [1, 2], ids=["single", "pairs"])
+def test_integer_chain_is_bit_exact(pairs):
     """Three bottleneck blocks (projection, stride 2, identity shortcuts) on integers: the
     kernel's chain and the oracle's are the same numbers (module docstring)."""
     N, H, W, cin, mid, cout = 4, 30, 30, 64, 64, 128
@@ -332,7 +336,7 @@ def test_integer_chain_is_bit_exact():
         convs.append(conv)
         ys.append(y)
         ws.append(w)
-    chain = cf.ConvChain(steps)
+    chain = cf.ConvChain(steps, cta_pairs=pairs)
     refs = []
     for (spec, _, src, rsrc), w in zip(plan, ws):
         x = x0.double().numpy() if src < 0 else refs[src]
