@@ -766,19 +766,30 @@ def main():
     # attainable time of each step: its FLOPs at the tensor peak or its algorithmic bytes at the
     # HBM bandwidth, whichever is longer (the bound of that layer)
     att_ms = [attainable_ms(s, peaks) for s in chain_specs]
-    n_tensor = sum(1 for s in chain_specs if layer_bound(s, peaks) == "tensor")
+    tensor_layers = [s for s in chain_specs if layer_bound(s, peaks) == "tensor"]
+    att_tensor_ms = sum(attainable_ms(s, peaks) for s in tensor_layers)
+    chain_bytes = sum(s.algorithmic_bytes for s in chain_specs)
+    achieved_gbs = chain_bytes / (chain_ms * 1e-3) / 1e9
     cd = chain.describe()
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops"], "traffic": chain_traffic(),
+    # The launch's bound is the one that holds for most of its attainable time: with fp32 outputs
+    # 38 of the 52 layers are HBM-bound and make up ~84% of the attainable time, so the roofline
+    # is algorithmic bytes against the measured HBM bandwidth; the tensor view is kept beside it.
+    roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": chain_traffic(),
             "traffic_note": "per launch: DRAM reads + bytes written into L2 (all of which reach DRAM), ncu; "
                             "against per_launch_algorithmic_bytes",
             "kernel": "tc_chain_kernel (tcgen05 implicit GEMM, the 52 non-stem layers as one persistent launch: "
                       + cd.split(" |")[0] + ")",
-            "peak_source": f"{peak_src} bf16 dense, burst (the kernel timed alone as one graph replay)",
+            "peak_source": f"{peak_src} HBM copy bandwidth (the kernel timed alone as one graph replay)",
             "kernel_ms_per_step": chain_ms, "launches_per_step": 1,
             "per_launch_flops": chain_flops, "launch_ms": chain_ms,
-            "per_launch_algorithmic_bytes": sum(s.algorithmic_bytes for s in chain_specs),
-            "layer_bounds": {"tensor": n_tensor, "hbm": len(chain_specs) - n_tensor},
+            "per_launch_algorithmic_bytes": chain_bytes,
+            "tensor_view": {"achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": achieved / peaks["bf16_tflops"],
+                            "peak_source": f"{peak_src} bf16 dense, burst"},
+            "layer_bounds": {"tensor": len(tensor_layers), "hbm": len(chain_specs) - len(tensor_layers),
+                             "attainable_ms_tensor_bound": att_tensor_ms,
+                             "attainable_ms_hbm_bound": sum(att_ms) - att_tensor_ms},
             "attainable_frac": sum(att_ms) / chain_ms,
             "attainable_note": "sum over the chain's layers of max(FLOPs / bf16 burst peak, algorithmic "
                                "bytes / HBM peak), divided by the measured time of the launch"}
