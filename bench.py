@@ -47,8 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum counts only what was evicted while the kernel ran).  It describes the
 # kernel sources it was taken on (SHA-256 prefix of their code with comments and blank space
 # removed) and is reported as null for any other sources.
-CHAIN_TRAFFIC = {"bytes_per_launch": 1.9738e9, "read_per_launch": 654.0e6, "write_per_launch": 1319.8e6,
-                 "dram_write_during_launch": 1278.8e6, "sources_sha256_16": "8b306a5b5b4619f3"}
+CHAIN_TRAFFIC = {"bytes_per_launch": 1.9770e9, "read_per_launch": 657.1e6, "write_per_launch": 1319.8e6,
+                 "dram_write_during_launch": 1281.1e6, "sources_sha256_16": "12a87a18773bd2ab"}
 CHAIN_SOURCES = ("tc_chain.cu", "chain.cu", "ptx.cuh", "convf_internal.h", "api_internal.h")
 
 

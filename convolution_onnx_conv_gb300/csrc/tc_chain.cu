@@ -13,8 +13,8 @@
 // Warp roles (one CTA per SM, tiles b, b + grid, ... of the launch-wide numbering):
 //   warp 0      activation producer: the dependency wait of each tile, then TMA activation
 //               loads (one box per k-block, or one per pipeline step in the 3-D 1x1 mode)
-//   warp 1      TMEM allocation + single-thread tcgen05.mma issue into two 128-column fp32
-//               accumulators
+//   warp 1      TMEM allocation + single-thread tcgen05.mma issue into four 128-column fp32
+//               accumulators (two of 256 columns in a CTA pair)
 //   warp 2      weight producer: one TMA box per pipeline step (two k-blocks)
 //   warps 3-10  epilogue, two warpgroups on the two column halves of every tile:
 //               tcgen05.ld -> smem transpose -> clamp(scale*acc + bias (+ r)) -> 16-byte stores
@@ -42,6 +42,9 @@ constexpr int kQThreads = 96 + 256 + 32;     // producer, MMA, weight producer, 
 constexpr int kQPub = 4;                    // tiles a CTA may have stored but not yet published
 constexpr int kQSmem = 1024 + kQSlots * (kQATile + kQBTile) + 8 * kQEpiWarpBytes + 256;
 static_assert(kQSmem <= 232448, "shared memory budget");
+// the barrier block after the epilogue staging: full/empty per step, tfull/tempty per
+// accumulator (4), stored/pubfree per publication slot, then the TMEM slot, abort flag and epoch
+static_assert((2 * kQSteps + 2 * 4 + 2 * kQPub) * 8 + 3 * 4 <= 256, "barrier block");
 static_assert(kChainArrivals == 1, "one arrival per tile (the publisher's)");
 
 // Single CTAs (128-row tiles, up to 128 columns) or CTA pairs (cta_group::2: 256-row tiles of up
@@ -50,6 +53,10 @@ static_assert(kChainArrivals == 1, "one arrival per tile (the publisher's)");
 // single CTA's 128 x 128 tile and issues M = 256 MMAs.
 template <bool PAIR>
 struct ChainShape {
+  // TMEM accumulators, all 512 columns: the MMA issuer may run that many tiles minus one ahead of
+  // the epilogue (four on single CTAs measured 4% faster over ResNet-50's 52 layers than two,
+  // the MMA running ahead through compute-bound steps while the epilogue drains HBM-bound ones)
+  static constexpr int kAcc = PAIR ? 2 : 4;
   static constexpr int kTileM = PAIR ? 256 : 128;   // output rows per tile
   static constexpr int kBNMax = PAIR ? 256 : 128;   // widest tile (TMEM buffer stride)
 };
@@ -250,7 +257,7 @@ __device__ void chain_producer(const ChainParams& p, uint8_t* sA, uint8_t* sB, u
 }
 
 // MMA issuer (one thread; the leader's in a CTA pair): per tile, one kTileM x bn accumulator
-// buffer (alternating), four K = 16 MMAs per k-block.  A pair's MMAs read both CTAs' operands and
+// buffer (in turn), four K = 16 MMAs per k-block.  A pair's MMAs read both CTAs' operands and
 // write both CTAs' TMEM; their commits arrive on the barriers of both CTAs.
 template <bool PAIR>
 __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t* empty,
@@ -319,7 +326,7 @@ __device__ void chain_mma(const ChainParams& p, uint8_t* sA, uint8_t* sB, uint64
       tc_commit_pair(&tfull[acc], 3);
     else
       tc_commit(&tfull[acc]);
-    if (++acc == 2) {
+    if (++acc == ChainShape<PAIR>::kAcc) {
       acc = 0;
       acc_phase ^= 1;
     }
@@ -561,7 +568,7 @@ __device__ void chain_epilogue(const ChainParams& p, uint8_t* sEpi, uint64_t* tf
       }
       ++j;
     }
-    if (++acc == 2) {
+    if (++acc == ChainShape<PAIR>::kAcc) {
       acc = 0;
       acc_phase ^= 1;
     }
@@ -608,7 +615,7 @@ __device__ void chain_publisher(const ChainParams& p, uint64_t* stored, uint64_t
 
 template <bool OUT_BF16, bool PAIR>
 __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParams p) {
-  constexpr uint32_t kTmemCols = 2 * ChainShape<PAIR>::kBNMax;
+  constexpr uint32_t kTmemCols = ChainShape<PAIR>::kAcc * ChainShape<PAIR>::kBNMax;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -619,8 +626,8 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
   uint64_t* full = bars;
   uint64_t* empty = bars + kQSteps;
   uint64_t* tfull = bars + 2 * kQSteps;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* stored = tempty + 2;       // [kQPub] a tile's stores are done (eight epilogue warps)
+  uint64_t* tempty = tfull + 4;        // tfull, tempty: [kAcc <= 4] per accumulator
+  uint64_t* stored = tempty + 4;       // [kQPub] a tile's stores are done (eight epilogue warps)
   uint64_t* pubfree = stored + kQPub;  // [kQPub] the publisher has taken the slot's tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pubfree + kQPub);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kQThreads, 1) tc_chain_kernel(const ChainParam
       mbar_init(&full[s], 2);    // activation producer + weight producer (the leader's, in a pair)
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < ChainShape<PAIR>::kAcc; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], PAIR ? 16 : 8);  // every epilogue warp (of both CTAs of a pair)
     }
